@@ -1,0 +1,313 @@
+/*
+ * dfl.h -- C ABI of the block-diffusion draft-step library (libdfl.so), sm_103a.
+ *
+ * The library computes one single-pass block-diffusion draft step: per draft
+ * layer a softmax mix of target hidden states followed by RMSNorm, separate
+ * K/V projections for target-context and draft features with queries from the
+ * draft features only, block attention in which every block query sees every
+ * context key and attends bidirectionally inside the block, the shared LM head
+ * with argmax, greedy acceptance, and optional K-draft sampling with
+ * streak-score self-selection.
+ *
+ * Sources (page title, section):
+ *   DFlare post   "DFlare: Scaling Up Draft Capacity for Block Diffusion
+ *                 Speculative Decoding" (iplexlaw blog)
+ *   DFlash article "DFlash: Block Diffusion for Flash Speculative Decoding"
+ *                 (Qiita)
+ *   SpecDiff-2 notes "SpecDiff-2 -- Scaling Diffusion Drafter Alignment For
+ *                 Faster Speculative Decoding" (MLSys 2026 talk notes)
+ *
+ * Conventions for every entry point
+ *   Ownership  All tensor pointers are caller-owned DEVICE memory (for
+ *              example a torch tensor's data_ptr()).  The library never
+ *              allocates or frees device memory.  Scratch space comes from the
+ *              caller as (ws, ws_bytes); dfl_workspace_size() gives the size.
+ *              Host pointers appear only where stated (parameter structs).
+ *   Launch     Calls are asynchronous on the given stream (a cudaStream_t
+ *              passed as void*, NULL = legacy default stream).  They do not
+ *              synchronise and may be captured into a CUDA graph.
+ *   Layout     Row-major, contiguous.  Weights are [out][in] (in contiguous).
+ *              bf16 tensors hold raw bf16 bits (2 bytes per element).
+ *              The block residual stream Xb is always fp32.
+ *   Alignment  Every tensor pointer must be 16-byte aligned and d, hd,
+ *              Hq*hd a multiple of 8, else DFL_ERR_MISALIGNED.
+ *   Errors     Argument checks run on the host before any launch and return
+ *              a non-zero dfl_status with nothing launched.  A launch failure
+ *              returns DFL_ERR_CUDA.  Kernels never trap: a bounded wait that
+ *              runs out records DFL_ERR_TIMEOUT in a per-device error word,
+ *              read (and cleared) by dfl_get_device_error().
+ */
+#ifndef DFL_H
+#define DFL_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum dfl_status {
+    DFL_OK = 0,
+    DFL_ERR_INVALID_ARG = 1,       /* null pointer, non-positive size, bad enum */
+    DFL_ERR_UNSUPPORTED_SHAPE = 2, /* a shape this build has no kernel for */
+    DFL_ERR_MISALIGNED = 3,        /* pointer or size breaks the 16-byte rule */
+    DFL_ERR_WORKSPACE = 4,         /* ws_bytes smaller than dfl_workspace_size() */
+    DFL_ERR_CUDA = 5,              /* a CUDA runtime call or launch failed */
+    DFL_ERR_TIMEOUT = 6,           /* a device-side bounded wait ran out */
+    DFL_ERR_NO_DEVICE = 7          /* no sm_103a device is current */
+} dfl_status;
+
+typedef enum dfl_dtype { DFL_F32 = 0, DFL_BF16 = 1 } dfl_dtype;
+
+typedef void* dfl_stream;          /* a cudaStream_t */
+
+/* Host-side parameters of K-draft sampling. */
+typedef struct dfl_sample_params {
+    int32_t K;        /* drafts per sequence, 1..64 */
+    float T;          /* temperature, > 0 */
+    uint64_t seed;    /* Philox4x32-10 key (low word, high word) */
+} dfl_sample_params;
+
+/* Shape descriptor for dfl_workspace_size(). Unused fields may be 0. */
+typedef struct dfl_shape {
+    int32_t N, C, B, d, Hq, Hkv, hd, D, L, V, K, G, row0;
+    int32_t dtype;    /* a dfl_dtype */
+} dfl_shape;
+
+typedef enum dfl_op {
+    DFL_OP_DUAL_KV_PROJ = 1,
+    DFL_OP_BLOCK_ATTN = 2,
+    DFL_OP_LM_HEAD = 3,
+    DFL_OP_SELF_SELECT = 4,
+    DFL_OP_DRAFT_STEP = 5
+} dfl_op;
+
+/* Library version string (static storage). */
+const char* dfl_version(void);
+
+/* Message for a status code (static storage). */
+const char* dfl_status_string(dfl_status s);
+
+/* Bytes of scratch the operation needs for this shape; 0 if it needs none or
+ * the shape is invalid. */
+size_t dfl_workspace_size(dfl_op op, const dfl_shape* shape);
+
+/*
+ * dfl_rope_table -- rotary cos/sin table for positions 0..P-1.
+ *   Reading (the pages give no position scheme): without positions every
+ *   [MASK] row of the block is identical; rotary embedding (rotate-half pairs
+ *   i, i+hd/2, angle p * theta^(-2i/hd)) is used, context at 0..C-1 and the
+ *   block at C..C+B-1.
+ *   table  out, device fp32 [P][hd/2][2] = (cos, sin), computed in fp64 and
+ *          rounded to fp32.
+ *   Errors: INVALID_ARG if P <= 0, hd <= 0 or hd odd, theta <= 0.
+ */
+dfl_status dfl_rope_table(float* table, int32_t P, int32_t hd, double theta,
+                          dfl_stream stream);
+
+/*
+ * dfl_layer_mix_rmsnorm -- per-draft-layer mixture of target hidden states.
+ *   DFlare post, "Per-draft-layer mixing of different information": each
+ *   draft layer learns mixing ratios over L target hidden states, softmax-
+ *   normalised, and applies RMSNorm: Xc_l = RMSNorm(sum_i softmax(mix_l)_i H_i).
+ *   D draft layers are produced from ONE read of H.
+ *   H           in, dt [L] slabs of [rows][d]; slab i starts at element
+ *               i * layer_stride.
+ *   mix_logits  in, device fp32 [D][L].
+ *   gain        in, device fp32 [D][d] RMSNorm gains.
+ *   Xc          out, dt [D] slabs of [rows][d] at element l * xc_layer_stride.
+ *   Accumulation fp32; bf16 outputs rounded to nearest even.
+ *   Errors: INVALID_ARG (null, L/D outside 1..32, rows/d <= 0, strides too
+ *   small), MISALIGNED.
+ */
+dfl_status dfl_layer_mix_rmsnorm(const void* H, int64_t layer_stride, int32_t L,
+                                 int64_t rows, int32_t d, dfl_dtype dt, int32_t D,
+                                 const float* mix_logits, const float* gain, float eps,
+                                 void* Xc, int64_t xc_layer_stride, dfl_stream stream);
+
+/*
+ * dfl_dual_kv_proj -- dual-source projections of one draft layer.
+ *   DFlare post, "Separate KV projections by information source": target
+ *   context features and draft (anchor + [MASK]) features get separate
+ *   key/value projections; queries come from the draft features only.
+ *     Kc = Xc Wkc^T, Vc = Xc Wvc^T                    (context rows)
+ *     Xn = RMSNorm(Xb; blk_gain)  (reading: pre-norm block input)
+ *     Q = Xn Wq^T, Kb = Xn Wkb^T, Vb = Xn Wvb^T      (block rows)
+ *   then rotary embedding on Q, Kb (positions C..C+B-1) and Kc (0..C-1).
+ *   Xc   in, dt [N*C][d] (rows ordered sequence-major)
+ *   Xb   in, fp32 [N*B][d] block residual stream
+ *   Wq [Hq*hd][d], Wkc/Wvc/Wkb/Wvb [Hkv*hd][d]: in, dt
+ *   rope in, fp32 [C+B][hd/2][2] from dfl_rope_table, or NULL (no rotary)
+ *   Q out dt [N*B][Hq][hd]; Kc, Vc out dt [N*C][Hkv][hd]; Kb, Vb out dt [N*B][Hkv][hd]
+ *   ws   scratch of dfl_workspace_size(DFL_OP_DUAL_KV_PROJ) bytes
+ *   bf16: tcgen05 tensor-core GEMMs, fp32 accumulation.  fp32: CUDA-core GEMMs.
+ *   Errors: INVALID_ARG, UNSUPPORTED_SHAPE (bf16 needs hd in {64,128},
+ *   Hq % Hkv == 0, d % 8 == 0), MISALIGNED, WORKSPACE.
+ */
+dfl_status dfl_dual_kv_proj(const void* Xc, const float* Xb, int32_t N, int32_t C,
+                            int32_t B, int32_t d, dfl_dtype dt, const float* blk_gain,
+                            float eps, const void* Wq, const void* Wkc, const void* Wvc,
+                            const void* Wkb, const void* Wvb, int32_t Hq, int32_t Hkv,
+                            int32_t hd, const float* rope, void* Q, void* Kc, void* Vc,
+                            void* Kb, void* Vb, void* ws, size_t ws_bytes,
+                            dfl_stream stream);
+
+/*
+ * dfl_block_attn -- block attention, output projection and residual add.
+ *   DFlare post, "Generating candidates in parallel, the target decides
+ *   acceptance": one forward predicts all mask positions with bidirectional
+ *   attention inside the block; DFlash article, "Writing a whole block in one
+ *   forward pass": target features enter the K/V of every draft layer.
+ *     O = softmax(Q [Kc;Kb]^T / sqrt(hd)) [Vc;Vb]   (no mask; query head h
+ *         reads K/V head h / (Hq/Hkv))
+ *     Xb <- Xb + O Wo^T                              (reading: output
+ *         projection with residual, as in the drafter's transformer layers)
+ *   Q, Kc, Vc, Kb, Vb  in, dt, layouts as produced by dfl_dual_kv_proj
+ *   Wo   in, dt [d][Hq*hd]
+ *   Xb   in/out, fp32 [N*B][d]
+ *   ws   scratch of dfl_workspace_size(DFL_OP_BLOCK_ATTN) bytes (split-KV
+ *        partial results)
+ *   Errors: INVALID_ARG, UNSUPPORTED_SHAPE, MISALIGNED, WORKSPACE.
+ */
+dfl_status dfl_block_attn(const void* Q, const void* Kc, const void* Vc, const void* Kb,
+                          const void* Vb, int32_t N, int32_t C, int32_t B, int32_t Hq,
+                          int32_t Hkv, int32_t hd, dfl_dtype dt, const void* Wo, int32_t d,
+                          float* Xb, void* ws, size_t ws_bytes, dfl_stream stream);
+
+/*
+ * dfl_lm_head_argmax -- shared frozen LM head, argmax, optional K-draft sampling.
+ *   DFlare post, "Stabilise the front, weight the back": the embedding and LM
+ *   head are frozen and shared with the target.  Reading: a final RMSNorm
+ *   precedes the head.  For rows r = row0..B-1 of each sequence:
+ *     z = RMSNorm(Xb_r; final_gain) W_lm^T,  draft = argmax_v z_v
+ *   (lowest index on equal fp32 maxima).
+ *   SpecDiff-2 notes, "Parallel drafting with diffusion LMs" / "Self-Selection
+ *   Acceptance": with sp != NULL, K independent draws from softmax(z/T) per
+ *   row by inverting the CDF at u = ((x0 >> 8) + 1/2) 2^-24, x0 word 0 of
+ *   Philox4x32-10(counter (n, r-row0, k, 0), key (seed lo, seed hi)).
+ *   Xb          in, fp32 [N][B][d]
+ *   W_lm        in, dt [V][d]
+ *   argmax_out  out, int32 [N][B-row0]
+ *   logits_out  out (nullable), fp32 [N*(B-row0)][V]; required when sp != NULL
+ *   sp          in, HOST pointer (nullable)
+ *   samples_out out, int32 [N][K][B-row0] (required when sp != NULL)
+ *   Errors: INVALID_ARG (row0 outside 0..B-1, V <= 0, K outside 1..64,
+ *   T <= 0), UNSUPPORTED_SHAPE, MISALIGNED, WORKSPACE.
+ */
+dfl_status dfl_lm_head_argmax(const float* Xb, int32_t N, int32_t B, int32_t row0,
+                              int32_t d, dfl_dtype dt, const float* final_gain, float eps,
+                              const void* W_lm, int32_t V, int32_t* argmax_out,
+                              float* logits_out, const dfl_sample_params* sp,
+                              int32_t* samples_out, void* ws, size_t ws_bytes,
+                              dfl_stream stream);
+
+/*
+ * dfl_greedy_accept -- greedy acceptance of one block per sequence.
+ *   DFlare post, "Generating candidates in parallel, the target decides
+ *   acceptance": under greedy decoding the prefix up to the first mismatch is
+ *   accepted and the target supplies the next token.
+ *   draft   in, int32 [N][n]     window positions 1..n
+ *   target  in, int32 [N][n+1]   target argmax t_1..t_{n+1}
+ *   accept_len out, int32 [N]    a = number of leading j with draft_j == t_j
+ *   bonus      out, int32 [N]    t_{a+1}
+ *   Errors: INVALID_ARG (null, N <= 0, n < 0 or n > 1024).
+ */
+dfl_status dfl_greedy_accept(const int32_t* draft, const int32_t* target, int32_t N,
+                             int32_t n, int32_t* accept_len, int32_t* bonus,
+                             dfl_stream stream);
+
+/*
+ * dfl_self_select -- streak-score self-selection and greedy acceptance.
+ *   SpecDiff-2 notes, "Streak-Distillation" (streak equation) and
+ *   "Self-Selection Acceptance": each of K drafts is scored with
+ *     S_k = sum_{m=1}^{G} prod_{j<=m} p_j(x_j^k),
+ *     p_j(x) = softmax(vlog[n][k][j-1])_x,
+ *   the argmax draft k* (lowest k on ties) is selected and greedy acceptance
+ *   is applied to it against the argmax of its own verifier rows, reusing the
+ *   cached verifier logits (draft probabilities are not used).
+ *   vlog    in, dt [N][K][G+1][V]; row G serves the bonus token
+ *   drafts  in, int32 [N][K][G]
+ *   scores  out, fp32 [N][K]; selected, accept_len, bonus out, int32 [N]
+ *   ws      scratch of dfl_workspace_size(DFL_OP_SELF_SELECT) bytes
+ *   Errors: INVALID_ARG (K outside 1..64, G outside 1..1024), MISALIGNED,
+ *   WORKSPACE.
+ */
+dfl_status dfl_self_select(const void* vlog, dfl_dtype dt, const int32_t* drafts,
+                           int32_t N, int32_t K, int32_t G, int32_t V, float* scores,
+                           int32_t* selected, int32_t* accept_len, int32_t* bonus,
+                           void* ws, size_t ws_bytes, dfl_stream stream);
+
+/* One draft layer's weights (device pointers, dtype of the step). */
+typedef struct dfl_layer_weights {
+    const void* Wq;   /* [Hq*hd][d] */
+    const void* Wkc;  /* [Hkv*hd][d] */
+    const void* Wvc;  /* [Hkv*hd][d] */
+    const void* Wkb;  /* [Hkv*hd][d] */
+    const void* Wvb;  /* [Hkv*hd][d] */
+    const void* Wo;   /* [d][Hq*hd] */
+} dfl_layer_weights;
+
+/* Arguments of a whole draft step.  Host struct; tensors are device memory. */
+typedef struct dfl_step_args {
+    int32_t N, C, B, d, Hq, Hkv, hd, D, L, V;
+    int32_t dtype;                 /* a dfl_dtype */
+    float eps;
+    const void* H;                 /* in [L][N*C][d] */
+    int64_t h_layer_stride;        /* elements between target-layer slabs */
+    const float* mix_logits;       /* in [D][L] */
+    const float* mix_gain;         /* in [D][d] */
+    const float* blk_gain;         /* in [D][d] */
+    const float* final_gain;       /* in [d] */
+    const float* rope;             /* in [C+B][hd/2][2] or NULL */
+    const dfl_layer_weights* layers;  /* HOST array [D] */
+    const void* W_lm;              /* in [V][d]; NULL when V == 0 */
+    const float* Xb0;              /* in [N][B][d] anchor + [MASK] features */
+    float* Xb;                     /* out [N][B][d] residual stream after D layers */
+    int32_t* draft;                /* out [N][B-1] argmax drafts (V > 0) */
+    float* logits;                 /* out, nullable: [N*(B-1)][V] */
+    const int32_t* target;         /* in, nullable: [N][B] target argmax tokens */
+    int32_t* accept_len;           /* out [N] when target != NULL */
+    int32_t* bonus;                /* out [N] when target != NULL */
+    const dfl_sample_params* sample;  /* HOST, nullable: K-draft sampling */
+    int32_t* samples;              /* out [N][K][B-1] when sample != NULL */
+    const void* vlog;              /* in, nullable: [N][K][B][V] verifier logits */
+    float* scores;                 /* out [N][K] when vlog != NULL */
+    int32_t* selected;             /* out [N] when vlog != NULL */
+} dfl_step_args;
+
+/*
+ * dfl_draft_step -- the whole single-pass draft step on one stream.
+ *   DFlare post / DFlash article: one block forward through D draft layers
+ *   (dfl_layer_mix_rmsnorm once for all layers, then per layer
+ *   dfl_dual_kv_proj and dfl_block_attn), the LM head (dfl_lm_head_argmax on
+ *   the B-1 mask rows) and the acceptance epilogue: dfl_greedy_accept against
+ *   `target`, or, with `sample` and `vlog`, sampling plus dfl_self_select
+ *   (whose results replace accept_len/bonus).  V == 0 stops after the layers.
+ *   ws: dfl_workspace_size(DFL_OP_DRAFT_STEP) bytes holding the mixed context
+ *   features of all D layers and each layer's Q/K/V.
+ *   Errors: those of the calls it makes; nothing is launched on a host-side
+ *   argument error.
+ */
+dfl_status dfl_draft_step(const dfl_step_args* args, void* ws, size_t ws_bytes,
+                          dfl_stream stream);
+
+/* Synchronise `stream`, then read and clear this device's error word (DFL_OK
+ * if no kernel recorded an error). */
+dfl_status dfl_get_device_error(dfl_stream stream, int32_t* code);
+
+/* Upper bound, in nanoseconds, on any single device-side wait (mbarrier or
+ * flag) in subsequently launched kernels.  Default 2e9 (2 s). */
+dfl_status dfl_set_wait_limit_ns(uint64_t ns);
+
+/* Self-test of the bounded wait: launches one block that waits on an
+ * mbarrier no thread arrives at, for at most limit_ns; the kernel records
+ * DFL_ERR_TIMEOUT in *status_out (device int32) and returns.  Used by tests
+ * to show that a wait which runs out leaves the context usable. */
+dfl_status dfl_selftest_bounded_wait(uint64_t limit_ns, int32_t* status_out,
+                                     dfl_stream stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DFL_H */

@@ -1,0 +1,522 @@
+"""Pins of the fp64 oracle against what the pages and the mathematics fix.
+
+Each test checks the oracle against something other than itself: a
+hand-worked case, a closed form, an invariant, brute-force enumeration, or an
+independent scalar-loop restatement on tiny inputs.  CPU only.
+"""
+import itertools
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle as orc
+from dfl_synth import WORKLOADS, Workload, plant_targets
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ----------------------------------------------------------------- mixture --
+
+def test_mix_coefficient_counts_match_pages():
+    # DFlare post, "Per-draft-layer mixing": 7 draft layers x 9 target layers
+    # = 63 coefficients; the GPT-OSS drafter is 8 layers x 7 target layers.
+    assert WORKLOADS["qwen3_8b_drafter"].n_mix_coefficients == 63
+    assert WORKLOADS["gpt_oss_20b_drafter"].n_mix_coefficients == 56
+    a = orc.mix_weights(np.random.default_rng(0).normal(size=(7, 9)))
+    assert a.shape == (7, 9)
+
+
+@pytest.mark.parametrize("scale", [1.0, 30.0, 300.0])
+def test_mix_weights_sum_to_one(scale):
+    z = np.random.default_rng(1).normal(size=(7, 9)) * scale
+    a = orc.mix_weights(z)
+    assert np.all(a >= 0)
+    assert np.max(np.abs(a.sum(axis=-1) - 1.0)) < 1e-12
+
+
+def test_mix_worked_example():
+    # logits (0, ln 3) -> ratios (1/4, 3/4); H_0 = (4, 0), H_1 = (0, 4)
+    # -> x = (1, 3), mean(x^2) = 5 -> RMSNorm(x) = (1, 3)/sqrt(5)  (eps = 0).
+    H = np.array([[[4.0, 0.0]], [[0.0, 4.0]]])
+    out = orc.mix_rmsnorm(H, [0.0, math.log(3.0)], [1.0, 1.0], 0.0)
+    assert np.allclose(out, [[1 / math.sqrt(5), 3 / math.sqrt(5)]], rtol=0, atol=1e-15)
+    # gain multiplies after normalisation
+    out = orc.mix_rmsnorm(H, [0.0, math.log(3.0)], [2.0, -1.0], 0.0)
+    assert np.allclose(out, [[2 / math.sqrt(5), -3 / math.sqrt(5)]], atol=1e-15)
+
+
+def test_rmsnorm_worked_example_with_eps():
+    # x = (3, 4): mean(x^2) = 12.5; with eps = 0.5 the divisor is sqrt(13).
+    out = orc.rmsnorm([3.0, 4.0], [1.0, 1.0], 0.5)
+    assert np.allclose(out, [3 / math.sqrt(13), 4 / math.sqrt(13)], atol=1e-15)
+
+
+def test_mix_one_hot_limit_is_rmsnorm_of_that_layer():
+    rng = np.random.default_rng(2)
+    H = rng.normal(size=(5, 7, 32))
+    g = rng.uniform(0.5, 1.5, size=32)
+    for i in range(5):
+        z = np.zeros(5)
+        z[i] = 50.0
+        direct = H[i] / np.sqrt(np.mean(H[i] ** 2, axis=-1, keepdims=True) + 1e-6) * g
+        assert np.allclose(orc.mix_rmsnorm(H, z, g, 1e-6), direct, rtol=1e-12, atol=1e-12)
+
+
+def test_mix_of_equal_layers_ignores_logits():
+    rng = np.random.default_rng(3)
+    h = rng.normal(size=(4, 16))
+    H = np.stack([h] * 3)
+    ref = orc.rmsnorm(h, np.ones(16), 1e-6)
+    for z in ([0, 0, 0], [5, -3, 1], [-40, 2, 9]):
+        assert np.allclose(orc.mix_rmsnorm(H, z, np.ones(16), 1e-6), ref, atol=1e-12)
+
+
+def test_rmsnorm_scale_invariance():
+    rng = np.random.default_rng(4)
+    x = rng.normal(size=(3, 64))
+    a = orc.rmsnorm(x, np.ones(64), 1e-12)
+    b = orc.rmsnorm(1e3 * x, np.ones(64), 1e-12)
+    assert np.allclose(a, b, rtol=1e-12, atol=1e-12)
+    assert np.allclose(np.mean(a ** 2, axis=-1), 1.0, atol=1e-9)
+
+
+def test_mix_is_linear_combination_then_norm_not_norm_then_mix():
+    # Negative control for the order: normalising each layer first differs.
+    rng = np.random.default_rng(5)
+    H = rng.normal(size=(3, 2, 8)) * np.array([0.5, 1.0, 2.0])[:, None, None]
+    z = np.array([0.3, -0.2, 0.9])
+    a = orc.mix_weights(z)
+    other = sum(a[i] * orc.rmsnorm(H[i], np.ones(8), 1e-6) for i in range(3))
+    assert not np.allclose(orc.mix_rmsnorm(H, z, np.ones(8), 1e-6), other, atol=1e-3)
+
+
+# ------------------------------------------------------------------- RoPE --
+
+def test_rope_two_dim_closed_form():
+    # hd = 2: one pair rotated by angle = position * theta^0 = position.
+    cos, sin = orc.rope_cos_sin([0, 1, 2.5], 2, 1e6)
+    x = np.array([[[1.0, 2.0]]] * 3)
+    out = orc.apply_rope(x, cos, sin)
+    for p_i, p in enumerate([0, 1, 2.5]):
+        exp = [math.cos(p) - 2 * math.sin(p), 2 * math.cos(p) + math.sin(p)]
+        assert np.allclose(out[p_i, 0], exp, atol=1e-15)
+
+
+def test_rope_frequency_closed_form():
+    hd, theta = 8, 10000.0
+    cos, sin = orc.rope_cos_sin([3], hd, theta)
+    for i in range(hd // 2):
+        ang = 3 * theta ** (-2 * i / hd)
+        assert abs(cos[0, i] - math.cos(ang)) < 1e-15
+        assert abs(sin[0, i] - math.sin(ang)) < 1e-15
+
+
+def test_rope_preserves_norm_and_is_relative():
+    rng = np.random.default_rng(6)
+    hd = 16
+    q = rng.normal(size=(1, 1, hd))
+    k = rng.normal(size=(1, 1, hd))
+
+    def rot(x, p):
+        c, s = orc.rope_cos_sin([p], hd, 1e4)
+        return orc.apply_rope(x, c, s)[0, 0]
+
+    assert np.allclose(rot(q, 0), q[0, 0], atol=1e-15)
+    assert abs(np.linalg.norm(rot(q, 37)) - np.linalg.norm(q)) < 1e-12
+    d1 = rot(q, 10) @ rot(k, 4)
+    d2 = rot(q, 106) @ rot(k, 100)
+    assert abs(d1 - d2) < 1e-10
+
+
+# -------------------------------------------------------------- attention --
+
+def _attention_scalar_loops(Q, K, V, visible):
+    """Independent restatement: one query row and head at a time, scalars."""
+    Bq, Hq, hd = Q.shape
+    S, Hkv, _ = K.shape
+    group = Hq // Hkv
+    O = np.zeros_like(Q, dtype=float)
+    for b in range(Bq):
+        for h in range(Hq):
+            g = h // group
+            logits = []
+            for s in range(S):
+                if visible[b][s]:
+                    logits.append((s, sum(Q[b, h, e] * K[s, g, e] for e in range(hd)) / math.sqrt(hd)))
+            m = max(l for _, l in logits)
+            ws = [(s, math.exp(l - m)) for s, l in logits]
+            tot = sum(w for _, w in ws)
+            for e in range(hd):
+                O[b, h, e] = sum(w * V[s, g, e] for s, w in ws) / tot
+    return O
+
+
+@pytest.mark.parametrize("C,B,Hq,Hkv", [(3, 2, 2, 1), (0, 3, 4, 2), (5, 1, 2, 2)])
+def test_attention_matches_scalar_loops(C, B, Hq, Hkv):
+    rng = np.random.default_rng(7)
+    hd = 4
+    Q = rng.normal(size=(B, Hq, hd))
+    K = rng.normal(size=(C + B, Hkv, hd))
+    V = rng.normal(size=(C + B, Hkv, hd))
+    vis = orc.block_visibility(C, B)
+    assert vis.shape == (B, C + B) and vis.all()
+    assert np.allclose(orc.attention(Q, K, V, vis), _attention_scalar_loops(Q, K, V, vis), atol=1e-12)
+    causal = np.array([[s <= C + b for s in range(C + B)] for b in range(B)])
+    assert np.allclose(orc.attention(Q, K, V, causal), _attention_scalar_loops(Q, K, V, causal), atol=1e-12)
+
+
+def test_attention_single_key_returns_value():
+    rng = np.random.default_rng(8)
+    Q = rng.normal(size=(1, 2, 8))
+    K = rng.normal(size=(1, 1, 8))
+    V = rng.normal(size=(1, 1, 8))
+    O = orc.attention(Q, K, V, orc.block_visibility(0, 1))
+    assert np.allclose(O[0, 0], V[0, 0], atol=1e-15) and np.allclose(O[0, 1], V[0, 0], atol=1e-15)
+
+
+def test_attention_identical_keys_average_values():
+    rng = np.random.default_rng(9)
+    Q = rng.normal(size=(3, 2, 8))
+    K = np.repeat(rng.normal(size=(1, 1, 8)), 6, axis=0)
+    V = rng.normal(size=(6, 1, 8))
+    O = orc.attention(Q, K, V, orc.block_visibility(3, 3))
+    assert np.allclose(O, V[:, 0].mean(axis=0)[None, None, :], atol=1e-12)
+
+
+def test_attention_gqa_equals_repeated_kv_heads():
+    rng = np.random.default_rng(10)
+    Q = rng.normal(size=(4, 8, 16))
+    K = rng.normal(size=(9, 2, 16))
+    V = rng.normal(size=(9, 2, 16))
+    vis = orc.block_visibility(5, 4)
+    a = orc.attention(Q, K, V, vis)
+    b = orc.attention(Q, np.repeat(K, 4, axis=1), np.repeat(V, 4, axis=1), vis)
+    assert np.allclose(a, b, atol=1e-13)
+
+
+def test_block_attention_is_bidirectional_and_order_free():
+    # Every key is visible, so permuting keys with their values changes nothing,
+    # while a causal mask (negative control) changes the early block rows.
+    rng = np.random.default_rng(11)
+    C, B = 6, 4
+    Q = rng.normal(size=(B, 2, 8))
+    K = rng.normal(size=(C + B, 1, 8))
+    V = rng.normal(size=(C + B, 1, 8))
+    vis = orc.block_visibility(C, B)
+    perm = rng.permutation(C + B)
+    a = orc.attention(Q, K, V, vis)
+    assert np.allclose(a, orc.attention(Q, K[perm], V[perm], vis), atol=1e-13)
+    causal = np.array([[s <= C + b for s in range(C + B)] for b in range(B)])
+    c = orc.attention(Q, K, V, causal)
+    assert not np.allclose(a[0], c[0], atol=1e-6)
+    assert np.allclose(a[B - 1], c[B - 1], atol=1e-13)   # last row sees everything either way
+
+
+# ------------------------------------------------------------ draft layer --
+
+def _tiny_layer_inputs(seed=12, B=3, C=4, L=2, d=8, Hq=2, Hkv=1, hd=4):
+    rng = np.random.default_rng(seed)
+    W = {"Wq": rng.normal(size=(Hq * hd, d)), "Wkc": rng.normal(size=(Hkv * hd, d)),
+         "Wvc": rng.normal(size=(Hkv * hd, d)), "Wkb": rng.normal(size=(Hkv * hd, d)),
+         "Wvb": rng.normal(size=(Hkv * hd, d)), "Wo": rng.normal(size=(d, Hq * hd))}
+    return dict(Xb=rng.normal(size=(B, d)), Hn=rng.normal(size=(L, C, d)),
+                mix=rng.normal(size=L), g_mix=rng.uniform(0.5, 1.5, d),
+                g_blk=rng.uniform(0.5, 1.5, d), W=W,
+                shape={"Hq": Hq, "Hkv": Hkv, "hd": hd})
+
+
+def _layer_scalar_loops(Xb, Hn, mix, g_mix, g_blk, W, shape, eps, theta):
+    """Independent scalar restatement of one draft layer on tiny inputs."""
+    B, d = Xb.shape
+    L, C, _ = Hn.shape
+    Hq, Hkv, hd = shape["Hq"], shape["Hkv"], shape["hd"]
+    ez = [math.exp(z) for z in mix]
+    a = [e / sum(ez) for e in ez]
+
+    def norm(row, g):
+        r = math.sqrt(sum(v * v for v in row) / len(row) + eps)
+        return [row[i] / r * g[i] for i in range(len(row))]
+
+    Xc = [norm([sum(a[i] * Hn[i, c, e] for i in range(L)) for e in range(d)], g_mix) for c in range(C)]
+    Xn = [norm(list(Xb[b]), g_blk) for b in range(B)]
+
+    def proj(rows, Wm):
+        return [[sum(r[k] * Wm[o, k] for k in range(d)) for o in range(Wm.shape[0])] for r in rows]
+
+    def rope(rows, heads, pos0):
+        out = []
+        for p, r in enumerate(rows):
+            pos = pos0 + p
+            nr = list(r)
+            for h in range(heads):
+                for i in range(hd // 2):
+                    ang = pos * theta ** (-2.0 * i / hd)
+                    x1, x2 = r[h * hd + i], r[h * hd + i + hd // 2]
+                    nr[h * hd + i] = x1 * math.cos(ang) - x2 * math.sin(ang)
+                    nr[h * hd + i + hd // 2] = x2 * math.cos(ang) + x1 * math.sin(ang)
+            out.append(nr)
+        return out
+
+    Q = rope(proj(Xn, W["Wq"]), Hq, C)
+    Kb = rope(proj(Xn, W["Wkb"]), Hkv, C)
+    Kc = rope(proj(Xc, W["Wkc"]), Hkv, 0)
+    Vb, Vc = proj(Xn, W["Wvb"]), proj(Xc, W["Wvc"])
+    keys, vals = Kc + Kb, Vc + Vb
+    O = [[0.0] * (Hq * hd) for _ in range(B)]
+    for b in range(B):
+        for h in range(Hq):
+            g = h // (Hq // Hkv)
+            s = [sum(Q[b][h * hd + e] * k[g * hd + e] for e in range(hd)) / math.sqrt(hd) for k in keys]
+            m = max(s)
+            w = [math.exp(x - m) for x in s]
+            for e in range(hd):
+                O[b][h * hd + e] = sum(w[j] * vals[j][g * hd + e] for j in range(len(keys))) / sum(w)
+    out = [[Xb[b, o] + sum(O[b][k] * W["Wo"][o, k] for k in range(Hq * hd)) for o in range(d)]
+           for b in range(B)]
+    return np.array(Xc), np.array(Q), np.array(out)
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(2, 1), (2, 2)])
+def test_draft_layer_matches_scalar_restatement(Hq, Hkv):
+    t = _tiny_layer_inputs(Hq=Hq, Hkv=Hkv)
+    got = orc.draft_layer(t["Xb"], t["Hn"], t["mix"], t["g_mix"], t["g_blk"], t["W"], t["shape"], 1e-6, 100.0)
+    Xc, Q, Xb = _layer_scalar_loops(t["Xb"], t["Hn"], t["mix"], t["g_mix"], t["g_blk"], t["W"], t["shape"], 1e-6, 100.0)
+    assert np.allclose(got["Xc"], Xc, atol=1e-12)
+    assert np.allclose(got["Q"].reshape(Q.shape), Q, atol=1e-12)
+    assert np.allclose(got["Xb"], Xb, atol=1e-12)
+
+
+def test_queries_come_from_draft_features_only():
+    # DFlare post, "Separate KV projections by information source": queries
+    # are built from the draft features, so the target hidden states reach Q
+    # never and reach the output only through the context K/V.
+    t = _tiny_layer_inputs()
+    a = orc.draft_layer(t["Xb"], t["Hn"], t["mix"], t["g_mix"], t["g_blk"], t["W"], t["shape"], 1e-6, 100.0)
+    b = orc.draft_layer(t["Xb"], 3.0 * t["Hn"][::-1], t["mix"], t["g_mix"], t["g_blk"], t["W"], t["shape"], 1e-6, 100.0)
+    for k in ("Q", "Kb", "Vb"):
+        assert np.allclose(a[k], b[k], atol=1e-14)
+    assert not np.allclose(a["Kc"], b["Kc"]) and not np.allclose(a["Xb"], b["Xb"])
+
+
+def test_context_and_block_kv_weights_are_separate():
+    t = _tiny_layer_inputs()
+    a = orc.draft_layer(t["Xb"], t["Hn"], t["mix"], t["g_mix"], t["g_blk"], t["W"], t["shape"], 1e-6, 100.0)
+    W2 = dict(t["W"])
+    W2["Wkc"], W2["Wkb"] = t["W"]["Wkb"], t["W"]["Wkc"]
+    b = orc.draft_layer(t["Xb"], t["Hn"], t["mix"], t["g_mix"], t["g_blk"], W2, t["shape"], 1e-6, 100.0)
+    assert not np.allclose(a["Xb"], b["Xb"], atol=1e-6)
+
+
+def test_draft_forward_chains_layers():
+    t = _tiny_layer_inputs()
+    layers = [t["W"], {k: 0.5 * v for k, v in t["W"].items()}]
+    mix = np.stack([t["mix"], -t["mix"]])
+    g2 = np.stack([t["g_mix"]] * 2)
+    gb = np.stack([t["g_blk"]] * 2)
+    out = orc.draft_forward(t["Xb"], t["Hn"], mix, g2, gb, layers, t["shape"], 1e-6, 100.0)
+    x1 = orc.draft_layer(t["Xb"], t["Hn"], mix[0], g2[0], gb[0], layers[0], t["shape"], 1e-6, 100.0)["Xb"]
+    x2 = orc.draft_layer(x1, t["Hn"], mix[1], g2[1], gb[1], layers[1], t["shape"], 1e-6, 100.0)["Xb"]
+    assert np.allclose(out["Xb"], x2, atol=1e-13)
+
+
+# ---------------------------------------------------------------- LM head --
+
+def test_lm_head_logits_scalar_and_chunking():
+    rng = np.random.default_rng(13)
+    X = rng.normal(size=(3, 6))
+    W = rng.normal(size=(11, 6))
+    g = rng.uniform(0.5, 1.5, 6)
+    z = orc.lm_head_logits(X, g, 1e-6, W, chunk=4)
+    for r in range(3):
+        rms = math.sqrt(sum(v * v for v in X[r]) / 6 + 1e-6)
+        for v in range(11):
+            exp = sum(X[r, k] / rms * g[k] * W[v, k] for k in range(6))
+            assert abs(z[r, v] - exp) < 1e-12
+    assert np.array_equal(z, orc.lm_head_logits(X, g, 1e-6, W, chunk=1000))
+
+
+def test_argmax_ties_take_lowest_index():
+    z = np.array([[1.0, 3.0, 3.0, 2.0], [5.0, 5.0, 5.0, 5.0], [-1.0, -2.0, -1.0, -3.0]])
+    assert orc.argmax_lowest(z).tolist() == [1, 0, 0]
+
+
+# ----------------------------------------------------------------- greedy --
+
+def _golden_greedy():
+    rows = []
+    with open(os.path.join(GOLDEN, "greedy_cases.txt")) as f:
+        for line in f:
+            if line.strip() and not line.startswith("#"):
+                d, t, a, b = [p.split() for p in line.split("|")]
+                rows.append(([int(x) for x in d], [int(x) for x in t], int(a[0]), int(b[0])))
+    return rows
+
+
+@pytest.mark.parametrize("case", _golden_greedy())
+def test_greedy_accept_golden(case):
+    d, t, a, b = case
+    assert orc.greedy_accept(d, t) == (a, b)
+
+
+def test_greedy_planted_prefix_closed_form():
+    # Targets planted to agree for exactly G_n leading positions give
+    # accepted = G_n and bonus = t_{G_n+1}; the mean of G_n approaches
+    # sum_{k=1}^{B-1} (1-p)^k (Geometric failures before the first success,
+    # truncated at B-1).
+    w = Workload("plant", N=20000, d=1, Hq=1, Hkv=1, hd=2, D=1, L=1, B=16,
+                 C=1, V=1000, dtype="f32", seed=77, geom_p=0.15)
+    rng = np.random.default_rng(14)
+    drafts = rng.integers(0, w.V, size=(w.N, w.B - 1))
+    t = plant_targets(w, drafts)
+    from dfl_synth import geometric_prefix
+    G = geometric_prefix(w)
+    acc = [orc.greedy_accept(drafts[n], t[n]) for n in range(w.N)]
+    assert all(a == G[n] and bonus == t[n, a] for n, (a, bonus) in enumerate(acc))
+    expected = sum((1 - w.geom_p) ** k for k in range(1, w.B))
+    assert abs(np.mean(G) - expected) < 0.08   # ~5 sigma at N = 20000
+    assert abs(expected - 5.17) < 0.01          # B = 16, p = 0.15
+
+
+# ----------------------------------------------------------------- Philox --
+
+def _golden_philox():
+    rows = []
+    with open(os.path.join(GOLDEN, "philox_kat.txt")) as f:
+        for line in f:
+            if line.strip() and not line.startswith("#"):
+                c, k, x = [[int(v, 16) for v in p.split()] for p in line.split("|")]
+                rows.append((c, k, x))
+    return rows
+
+
+@pytest.mark.parametrize("case", _golden_philox())
+def test_philox_known_answers(case):
+    c, k, x = case
+    assert list(orc.philox4x32_10(c, k)) == x
+
+
+def test_philox_uniform_statistics():
+    u = np.array([orc.draw_uniform(0x5EEDD1F5, n, j, k) for n in range(8) for j in range(64) for k in range(8)])
+    assert np.all((u > 0) & (u < 1))
+    counts, _ = np.histogram(u, bins=16, range=(0, 1))
+    chi2 = np.sum((counts - len(u) / 16) ** 2 / (len(u) / 16))
+    assert chi2 < 45.0   # 15 dof; p ~ 1e-4
+
+
+def test_philox_avalanche():
+    base = orc.philox4x32_10((1, 2, 3, 4), (5, 6))
+    flips = []
+    for bit in range(32):
+        x = orc.philox4x32_10((1 ^ (1 << bit), 2, 3, 4), (5, 6))
+        flips.append(sum(bin(a ^ b).count("1") for a, b in zip(base, x)))
+    assert 48 < np.mean(flips) < 80   # ~64 of 128 output bits flip
+
+
+# --------------------------------------------------------------- sampling --
+
+def test_sampling_one_hot_is_deterministic():
+    z = np.zeros(50)
+    z[17] = 200.0
+    for u in (1e-7, 0.3, 0.999999):
+        assert orc.sample_inverse_cdf(z, 1.5, u)[0] == 17
+
+
+def test_sampling_uniform_grid_reproduces_marginal():
+    # Inversion of the CDF on the grid u_i = (i + 1/2)/M gives every token a
+    # count within 1 of M * q_v, q = softmax(z / T).
+    rng = np.random.default_rng(15)
+    z, T, M = rng.normal(size=8) * 2, 1.5, 4000
+    q = np.exp(z / T) / np.exp(z / T).sum()
+    counts = np.zeros(8)
+    for i in range(M):
+        counts[orc.sample_inverse_cdf(z, T, (i + 0.5) / M)[0]] += 1
+    assert np.all(np.abs(counts - M * q) <= 1.0 + 1e-9)
+
+
+def test_sampling_low_temperature_is_argmax_and_margin():
+    rng = np.random.default_rng(16)
+    z = rng.normal(size=100)
+    assert orc.sample_inverse_cdf(z, 1e-4, 0.5)[0] == int(np.argmax(z))
+    v, margin = orc.sample_inverse_cdf(np.zeros(4), 1.0, 0.5)   # boundary exactly at 0.5
+    assert margin == 0.0 and v == 2
+
+
+# ------------------------------------------------------------ streak / TV --
+
+def test_streak_worked_example():
+    assert orc.streak_score([0.5, 0.5]) == 0.75
+    assert orc.streak_score([1.0, 1.0, 1.0]) == 3.0
+    assert orc.streak_score([0.0, 1.0]) == 0.0
+
+
+@pytest.mark.parametrize("V,G", [(2, 1), (3, 3), (4, 4), (2, 4)])
+def test_streak_equation_by_enumeration(V, G):
+    # SpecDiff-2 notes, "Streak-Distillation": Tokens/Draft = E[sum_m prod_{j<=m} alpha_j].
+    # Enumerate every verifier outcome y in V^G, y_j ~ P_j independently; a
+    # draft token is accepted while y_j equals it; the expected number accepted
+    # must equal the streak score of p_j = P_j(x_j).
+    rng = np.random.default_rng(V * 10 + G)
+    P = rng.dirichlet(np.ones(V), size=G)
+    x = rng.integers(0, V, size=G)
+    expect = 0.0
+    for y in itertools.product(range(V), repeat=G):
+        prob = np.prod([P[j, y[j]] for j in range(G)])
+        acc = 0
+        while acc < G and y[acc] == x[acc]:
+            acc += 1
+        expect += prob * acc
+    assert abs(orc.streak_score([P[j, x[j]] for j in range(G)]) - expect) < 1e-12
+
+
+def test_tv_acceptance_closed_form_and_theorem():
+    rng = np.random.default_rng(17)
+    for _ in range(20):
+        P, Q = rng.dirichlet(np.ones(6)), rng.dirichlet(np.ones(6))
+        a = orc.tv_acceptance(P, Q)
+        assert abs(a - np.minimum(P, Q).sum()) < 1e-12      # 1 - TV = sum min
+        assert a >= np.sum(P * Q) - 1e-15                    # alpha_SD >= alpha_greedy
+    P = rng.dirichlet(np.ones(5))
+    assert abs(orc.tv_acceptance(P, P) - 1.0) < 1e-15
+
+
+def test_tv_acceptance_monte_carlo():
+    # Speculative sampling accepts x ~ Q with probability min(1, P(x)/Q(x));
+    # its acceptance rate is the TV proxy.
+    rng = np.random.default_rng(18)
+    P, Q = rng.dirichlet(np.ones(4)), rng.dirichlet(np.ones(4))
+    n = 200000
+    x = rng.choice(4, size=n, p=Q)
+    acc = rng.random(n) < np.minimum(1.0, P[x] / Q[x])
+    assert abs(acc.mean() - orc.tv_acceptance(P, Q)) < 5 * math.sqrt(0.25 / n)
+
+
+# ---------------------------------------------------------- self-selection --
+
+def test_self_select_scores_by_enumeration_and_greedy():
+    rng = np.random.default_rng(19)
+    K, G, V = 3, 3, 3
+    vlog = rng.normal(size=(K, G + 1, V)) * 2
+    drafts = rng.integers(0, V, size=(K, G))
+    scores, ks, a, bonus = orc.self_select(vlog, drafts)
+    for k in range(K):
+        P = np.exp(vlog[k]) / np.exp(vlog[k]).sum(axis=-1, keepdims=True)
+        expect = 0.0
+        for y in itertools.product(range(V), repeat=G):
+            prob = np.prod([P[j, y[j]] for j in range(G)])
+            acc = 0
+            while acc < G and y[acc] == drafts[k, acc]:
+                acc += 1
+            expect += prob * acc
+        assert abs(scores[k] - expect) < 1e-12
+    assert ks == int(np.argmax(scores))
+    t = [int(np.argmax(vlog[ks, j])) for j in range(G + 1)]
+    assert (a, bonus) == orc.greedy_accept(drafts[ks], t)
+
+
+def test_self_select_ties_take_lowest_draft():
+    vlog = np.zeros((3, 3, 4))
+    drafts = np.array([[1, 2], [1, 2], [0, 0]])
+    scores, ks, _, _ = orc.self_select(vlog, drafts)
+    assert scores[0] == scores[1] == scores[2] and ks == 0
