@@ -1,0 +1,16 @@
+"""Block-diffusion speculative drafting on GB300 (sm_103a).
+
+The compute path is libdfl.so (hand-written CUDA kernels behind a C ABI,
+declared in include/dfl.h); this package only builds it, binds it with
+ctypes and manages device buffers with torch.
+"""
+from ._build import build, LIB
+from ._lib import (DflError, load, version, status_string, workspace_size, ptr, EXPORTED,
+                   DFL_F32, DFL_BF16, DFL_OP_DUAL_KV_PROJ, DFL_OP_BLOCK_ATTN, DFL_OP_LM_HEAD,
+                   DFL_OP_SELF_SELECT, DFL_OP_DRAFT_STEP,
+                   dfl_rope_table, dfl_layer_mix_rmsnorm, dfl_dual_kv_proj, dfl_block_attn,
+                   dfl_lm_head_argmax, dfl_greedy_accept, dfl_self_select, dfl_draft_step,
+                   dfl_get_device_error, dfl_set_wait_limit_ns, dfl_selftest_bounded_wait)
+from .step import DraftShape, DraftModel
+
+__all__ = [n for n in dir() if not n.startswith("_")]

@@ -1,0 +1,455 @@
+// C-ABI entry points of libdfl: argument checks, workspace layout and the
+// order of kernel launches for each operation of the draft step.
+#include <atomic>
+#include <mutex>
+
+#include "internal.h"
+#include "small_kernels.h"
+
+// Per-device error word: the first kernel that records an error wins.
+__device__ int g_dfl_error_word;
+
+namespace dfl {
+
+namespace {
+std::atomic<uint64_t> g_wait_ns{2000000000ull};
+constexpr int kMaxDevices = 64;
+DeviceCtx g_ctx[kMaxDevices];
+std::atomic<bool> g_ready[kMaxDevices];
+std::mutex g_mu;
+
+inline size_t al256(size_t b) { return (b + 255) & ~size_t(255); }
+inline size_t esz(int dt) { return dt == DFL_BF16 ? 2 : 4; }
+inline uint8_t* carve(uint8_t*& p, size_t bytes) {
+    uint8_t* r = p;
+    p += al256(bytes);
+    return r;
+}
+}  // namespace
+
+DeviceCtx* current_ctx() {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    if (g_ready[dev].load(std::memory_order_acquire)) return &g_ctx[dev];
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_ready[dev].load(std::memory_order_relaxed)) return &g_ctx[dev];
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return nullptr;
+    if (major != 10 || minor != 3) return nullptr;   // kernels are built for sm_103a only
+    DeviceCtx& c = g_ctx[dev];
+    if (cudaGetSymbolAddress(reinterpret_cast<void**>(&c.err_word), g_dfl_error_word) != cudaSuccess)
+        return nullptr;
+    c.device = dev;
+    c.sm_count = sms;
+    g_ready[dev].store(true, std::memory_order_release);
+    return &c;
+}
+
+DevErr dev_err(DeviceCtx* ctx) { return DevErr{ctx->err_word, g_wait_ns.load()}; }
+uint64_t wait_limit_ns() { return g_wait_ns.load(); }
+
+// ------------------------------------------------------------ workspaces
+
+size_t ws_dual_kv_proj(int N, int B, int d, int dt) { return al256((size_t)N * B * d * esz(dt)); }
+
+size_t ws_block_attn(int N, int C, int B, int Hq, int Hkv, int hd, int dt) {
+    size_t b = al256((size_t)N * B * Hq * hd * esz(dt));
+    if (dt == DFL_BF16) b += al256(attn_ws_bytes(N, C, B, Hq, Hkv, hd));
+    return b;
+}
+
+size_t ws_lm_head(int N, int B, int row0, int d, int V, int dt, bool logits_missing) {
+    const size_t M = (size_t)N * (B - row0);
+    const size_t tiles = (size_t)(V + 255) / 256;
+    size_t b = al256(M * d * esz(dt)) + al256(M * tiles * 4) * 2 + al256(M * tiles * 8);
+    if (logits_missing) b += al256(M * (size_t)V * 4);
+    return b;
+}
+
+}  // namespace dfl
+
+using namespace dfl;
+
+// ------------------------------------------------------------------ misc
+
+extern "C" const char* dfl_version(void) { return "dfl 0.1.0 (sm_103a)"; }
+
+extern "C" const char* dfl_status_string(dfl_status s) {
+    switch (s) {
+        case DFL_OK: return "ok";
+        case DFL_ERR_INVALID_ARG: return "invalid argument";
+        case DFL_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+        case DFL_ERR_MISALIGNED: return "pointer or size not 16-byte aligned";
+        case DFL_ERR_WORKSPACE: return "workspace too small";
+        case DFL_ERR_CUDA: return "CUDA call or launch failed";
+        case DFL_ERR_TIMEOUT: return "device-side wait timed out";
+        case DFL_ERR_NO_DEVICE: return "no sm_103a device is current";
+    }
+    return "unknown status";
+}
+
+extern "C" size_t dfl_workspace_size(dfl_op op, const dfl_shape* s) {
+    if (!s) return 0;
+    switch (op) {
+        case DFL_OP_DUAL_KV_PROJ: return ws_dual_kv_proj(s->N, s->B, s->d, s->dtype);
+        case DFL_OP_BLOCK_ATTN: return ws_block_attn(s->N, s->C, s->B, s->Hq, s->Hkv, s->hd, s->dtype);
+        case DFL_OP_LM_HEAD:
+            if (s->row0 < 0 || s->row0 >= s->B || s->V <= 0) return 0;
+            return ws_lm_head(s->N, s->B, s->row0, s->d, s->V, s->dtype, s->dtype == DFL_F32);
+        case DFL_OP_SELF_SELECT: return al256(select_ws_bytes(s->N, s->K, s->G));
+        case DFL_OP_DRAFT_STEP: {
+            const size_t e = esz(s->dtype);
+            size_t b = al256((size_t)s->D * s->N * s->C * s->d * e);                 // Xc, all layers
+            b += al256((size_t)s->N * s->B * s->Hq * s->hd * e);                     // Q
+            b += 2 * al256((size_t)s->N * s->C * s->Hkv * s->hd * e);                // Kc, Vc
+            b += 2 * al256((size_t)s->N * s->B * s->Hkv * s->hd * e);                // Kb, Vb
+            size_t sub = ws_dual_kv_proj(s->N, s->B, s->d, s->dtype);
+            const size_t at = ws_block_attn(s->N, s->C, s->B, s->Hq, s->Hkv, s->hd, s->dtype);
+            if (at > sub) sub = at;
+            if (s->V > 0) {
+                const size_t lm = ws_lm_head(s->N, s->B, 1, s->d, s->V, s->dtype, true);
+                if (lm > sub) sub = lm;
+                if (s->K > 0) {
+                    const size_t se = al256(select_ws_bytes(s->N, s->K, s->B - 1));
+                    if (se > sub) sub = se;
+                    b += al256((size_t)s->N * s->K * (s->B - 1) * 4);               // samples
+                }
+                b += al256((size_t)s->N * (s->B - 1) * 4);                          // drafts
+            }
+            return b + sub;
+        }
+    }
+    return 0;
+}
+
+extern "C" dfl_status dfl_get_device_error(dfl_stream stream, int32_t* code) {
+    if (!code) return DFL_ERR_INVALID_ARG;
+    DeviceCtx* ctx = current_ctx();
+    if (!ctx) return DFL_ERR_NO_DEVICE;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return DFL_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_dfl_error_word, sizeof(int)) != cudaSuccess) return DFL_ERR_CUDA;
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_dfl_error_word, &zero, sizeof(int)) != cudaSuccess) return DFL_ERR_CUDA;
+    *code = v;
+    return DFL_OK;
+}
+
+extern "C" dfl_status dfl_set_wait_limit_ns(uint64_t ns) {
+    if (ns == 0) return DFL_ERR_INVALID_ARG;
+    g_wait_ns.store(ns);
+    return DFL_OK;
+}
+
+extern "C" dfl_status dfl_selftest_bounded_wait(uint64_t limit_ns, int32_t* status_out, dfl_stream stream) {
+    if (!status_out || limit_ns == 0 || limit_ns > 10000000000ull) return DFL_ERR_INVALID_ARG;
+    if (!current_ctx()) return DFL_ERR_NO_DEVICE;
+    return selftest_wait(status_out, limit_ns, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" dfl_status dfl_rope_table(float* table, int32_t P, int32_t hd, double theta, dfl_stream stream) {
+    if (!table || P <= 0 || hd <= 0 || (hd & 1) || !(theta > 0.0)) return DFL_ERR_INVALID_ARG;
+    if (!current_ctx()) return DFL_ERR_NO_DEVICE;
+    return rope_table(table, P, hd, theta, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" dfl_status dfl_greedy_accept(const int32_t* draft, const int32_t* target, int32_t N, int32_t n,
+                                        int32_t* accept_len, int32_t* bonus, dfl_stream stream) {
+    if (!target || !accept_len || !bonus || N <= 0 || n < 0 || n > 1024 || (n > 0 && !draft))
+        return DFL_ERR_INVALID_ARG;
+    if (!current_ctx()) return DFL_ERR_NO_DEVICE;
+    return greedy_accept(draft, target, N, n, accept_len, bonus, static_cast<cudaStream_t>(stream));
+}
+
+// ------------------------------------------------------- dual projection
+
+extern "C" dfl_status dfl_dual_kv_proj(const void* Xc, const float* Xb, int32_t N, int32_t C, int32_t B, int32_t d,
+                                       dfl_dtype dt, const float* blk_gain, float eps, const void* Wq,
+                                       const void* Wkc, const void* Wvc, const void* Wkb, const void* Wvb,
+                                       int32_t Hq, int32_t Hkv, int32_t hd, const float* rope, void* Q, void* Kc,
+                                       void* Vc, void* Kb, void* Vb, void* ws, size_t ws_bytes,
+                                       dfl_stream stream) {
+    if (N <= 0 || C < 0 || B <= 0 || d <= 0 || Hq <= 0 || Hkv <= 0 || hd <= 0 || Hq % Hkv != 0)
+        return DFL_ERR_INVALID_ARG;
+    if (dt != DFL_F32 && dt != DFL_BF16) return DFL_ERR_INVALID_ARG;
+    if (!Xb || !blk_gain || !Wq || !Wkb || !Wvb || !Q || !Kb || !Vb || !ws) return DFL_ERR_INVALID_ARG;
+    if (C > 0 && (!Xc || !Wkc || !Wvc || !Kc || !Vc)) return DFL_ERR_INVALID_ARG;
+    if (rope && (hd & 1)) return DFL_ERR_INVALID_ARG;
+    const void* ptrs[] = {Xb, blk_gain, Wq, Wkb, Wvb, Q, Kb, Vb, ws, rope ? rope : Xb};
+    for (const void* p : ptrs) if (!aligned16(p)) return DFL_ERR_MISALIGNED;
+    if (C > 0) {
+        const void* cp[] = {Xc, Wkc, Wvc, Kc, Vc};
+        for (const void* p : cp) if (!aligned16(p)) return DFL_ERR_MISALIGNED;
+    }
+    if (d % 8 != 0 || hd % 8 != 0) return DFL_ERR_MISALIGNED;
+    if (ws_bytes < ws_dual_kv_proj(N, B, d, dt)) return DFL_ERR_WORKSPACE;
+    DeviceCtx* ctx = current_ctx();
+    if (!ctx) return DFL_ERR_NO_DEVICE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int kv = Hkv * hd, qd = Hq * hd;
+    dfl_status rc;
+
+    if (dt == DFL_F32) {
+        float* Xn = static_cast<float*>(ws);
+        if ((rc = rmsnorm_rows(Xb, d, (int64_t)N * B, 1, 1, 0, blk_gain, eps, Xn, false, st)) != DFL_OK) return rc;
+        const float* w[3] = {static_cast<const float*>(Wq), static_cast<const float*>(Wkb),
+                             static_cast<const float*>(Wvb)};
+        float* o[3] = {static_cast<float*>(Q), static_cast<float*>(Kb), static_cast<float*>(Vb)};
+        const int nout[3] = {qd, kv, kv};
+        for (int j = 0; j < 3; ++j)
+            if ((rc = gemm_f32(Xn, w[j], o[j], N * B, nout[j], d, nout[j], 0, st)) != DFL_OK) return rc;
+        if (C > 0) {
+            const float* xc = static_cast<const float*>(Xc);
+            if ((rc = gemm_f32(xc, static_cast<const float*>(Wkc), static_cast<float*>(Kc), N * C, kv, d, kv, 0,
+                               st)) != DFL_OK)
+                return rc;
+            if ((rc = gemm_f32(xc, static_cast<const float*>(Wvc), static_cast<float*>(Vc), N * C, kv, d, kv, 0,
+                               st)) != DFL_OK)
+                return rc;
+        }
+        if (rope) {
+            if ((rc = rope_inplace_f32(static_cast<float*>(Q), (int64_t)N * B, Hq, hd, B, C, rope, st)) != DFL_OK)
+                return rc;
+            if ((rc = rope_inplace_f32(static_cast<float*>(Kb), (int64_t)N * B, Hkv, hd, B, C, rope, st)) != DFL_OK)
+                return rc;
+            if (C > 0 &&
+                (rc = rope_inplace_f32(static_cast<float*>(Kc), (int64_t)N * C, Hkv, hd, C, 0, rope, st)) != DFL_OK)
+                return rc;
+        }
+        return DFL_OK;
+    }
+
+    // bf16: tensor-core GEMMs with the rotary embedding in the epilogue
+    if (hd != 64 && hd != 128) return DFL_ERR_UNSUPPORTED_SHAPE;
+    if (kv % 128 != 0 || qd % 128 != 0) return DFL_ERR_UNSUPPORTED_SHAPE;
+    void* Xn = ws;
+    if ((rc = rmsnorm_rows(Xb, d, (int64_t)N * B, 1, 1, 0, blk_gain, eps, Xn, true, st)) != DFL_OK) return rc;
+
+    if (C > 0) {   // context rows: [Kc | Vc] = Xc [Wkc ; Wvc]^T
+        GemmArgs g{};
+        g.A = Xc; g.M = N * C; g.K = d;
+        g.B[0] = Wkc; g.B[1] = Wvc; g.b_rows[0] = kv; g.b_rows[1] = kv;
+        g.b_begin[0] = 0; g.b_begin[1] = kv; g.nb = 2; g.N = 2 * kv;
+        g.bn = (kv % 256 == 0) ? 256 : 128;
+        g.m_inner = 0;
+        g.epi = EPI_STORE;
+        g.ep.seg[0] = GemmSeg{Kc, 0, kv, rope != nullptr};
+        g.ep.seg[1] = GemmSeg{Vc, kv, kv, 0};
+        g.ep.nseg = 2;
+        g.ep.rope = rope; g.ep.hd = hd; g.ep.rows_per_seq = C; g.ep.pos_off = 0;
+        if ((rc = gemm_tc(ctx, g, st)) != DFL_OK) return rc;
+    }
+    {   // block rows: [Q | Kb | Vb] = Xn [Wq ; Wkb ; Wvb]^T
+        GemmArgs g{};
+        g.A = Xn; g.M = N * B; g.K = d;
+        g.B[0] = Wq; g.B[1] = Wkb; g.B[2] = Wvb;
+        g.b_rows[0] = qd; g.b_rows[1] = kv; g.b_rows[2] = kv;
+        g.b_begin[0] = 0; g.b_begin[1] = qd; g.b_begin[2] = qd + kv; g.nb = 3; g.N = qd + 2 * kv;
+        g.bn = 128;
+        g.m_inner = 1;
+        g.epi = EPI_STORE;
+        g.ep.seg[0] = GemmSeg{Q, 0, qd, rope != nullptr};
+        g.ep.seg[1] = GemmSeg{Kb, qd, kv, rope != nullptr};
+        g.ep.seg[2] = GemmSeg{Vb, qd + kv, kv, 0};
+        g.ep.nseg = 3;
+        g.ep.rope = rope; g.ep.hd = hd; g.ep.rows_per_seq = B; g.ep.pos_off = C;
+        if ((rc = gemm_tc(ctx, g, st)) != DFL_OK) return rc;
+    }
+    return DFL_OK;
+}
+
+// -------------------------------------------------------- block attention
+
+extern "C" dfl_status dfl_block_attn(const void* Q, const void* Kc, const void* Vc, const void* Kb, const void* Vb,
+                                     int32_t N, int32_t C, int32_t B, int32_t Hq, int32_t Hkv, int32_t hd,
+                                     dfl_dtype dt, const void* Wo, int32_t d, float* Xb, void* ws, size_t ws_bytes,
+                                     dfl_stream stream) {
+    if (N <= 0 || C < 0 || B <= 0 || d <= 0 || Hq <= 0 || Hkv <= 0 || hd <= 0 || Hq % Hkv != 0)
+        return DFL_ERR_INVALID_ARG;
+    if (dt != DFL_F32 && dt != DFL_BF16) return DFL_ERR_INVALID_ARG;
+    if (!Q || !Kb || !Vb || !Wo || !Xb || !ws || (C > 0 && (!Kc || !Vc))) return DFL_ERR_INVALID_ARG;
+    const void* ptrs[] = {Q, Kb, Vb, Wo, Xb, ws, C > 0 ? Kc : Q, C > 0 ? Vc : Q};
+    for (const void* p : ptrs) if (!aligned16(p)) return DFL_ERR_MISALIGNED;
+    if (d % 8 != 0 || hd % 8 != 0) return DFL_ERR_MISALIGNED;
+    if (ws_bytes < ws_block_attn(N, C, B, Hq, Hkv, hd, dt)) return DFL_ERR_WORKSPACE;
+    DeviceCtx* ctx = current_ctx();
+    if (!ctx) return DFL_ERR_NO_DEVICE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int qd = Hq * hd;
+    dfl_status rc;
+    uint8_t* p = static_cast<uint8_t*>(ws);
+    void* O = carve(p, (size_t)N * B * qd * esz(dt));
+    if (dt == DFL_F32) {
+        if (hd > 128) return DFL_ERR_UNSUPPORTED_SHAPE;
+        if ((rc = attn_f32(static_cast<const float*>(Q), static_cast<const float*>(Kc), static_cast<const float*>(Vc),
+                           static_cast<const float*>(Kb), static_cast<const float*>(Vb), N, C, B, Hq, Hkv, hd,
+                           static_cast<float*>(O), st)) != DFL_OK)
+            return rc;
+        return gemm_f32(static_cast<const float*>(O), static_cast<const float*>(Wo), Xb, N * B, d, qd, d, 1, st);
+    }
+    if (hd != 64 && hd != 128) return DFL_ERR_UNSUPPORTED_SHAPE;
+    if (d % 32 != 0) return DFL_ERR_UNSUPPORTED_SHAPE;
+    if ((rc = attn_bf16(Q, Kc, Vc, Kb, Vb, N, C, B, Hq, Hkv, hd, O, p, st)) != DFL_OK) return rc;
+    GemmArgs g{};   // Xb += O Wo^T
+    g.A = O; g.M = N * B; g.K = qd;
+    g.B[0] = Wo; g.b_rows[0] = d; g.b_begin[0] = 0; g.nb = 1; g.N = d;
+    g.bn = 128;
+    g.m_inner = 1;
+    g.epi = EPI_RESID;
+    g.ep.resid = Xb; g.ep.ld_resid = d;
+    return gemm_tc(ctx, g, st);
+}
+
+// ---------------------------------------------------------------- LM head
+
+extern "C" dfl_status dfl_lm_head_argmax(const float* Xb, int32_t N, int32_t B, int32_t row0, int32_t d,
+                                         dfl_dtype dt, const float* final_gain, float eps, const void* W_lm,
+                                         int32_t V, int32_t* argmax_out, float* logits_out,
+                                         const dfl_sample_params* sp, int32_t* samples_out, void* ws,
+                                         size_t ws_bytes, dfl_stream stream) {
+    if (N <= 0 || B <= 0 || row0 < 0 || row0 >= B || d <= 0 || V <= 0) return DFL_ERR_INVALID_ARG;
+    if (dt != DFL_F32 && dt != DFL_BF16) return DFL_ERR_INVALID_ARG;
+    if (!Xb || !final_gain || !W_lm || !argmax_out || !ws) return DFL_ERR_INVALID_ARG;
+    if (sp && (sp->K < 1 || sp->K > 64 || !(sp->T > 0.f) || !samples_out)) return DFL_ERR_INVALID_ARG;
+    if (sp && dt == DFL_BF16 && !logits_out) return DFL_ERR_INVALID_ARG;
+    const void* ptrs[] = {Xb, final_gain, W_lm, ws, logits_out ? logits_out : Xb};
+    for (const void* p : ptrs) if (!aligned16(p)) return DFL_ERR_MISALIGNED;
+    if (d % 8 != 0) return DFL_ERR_MISALIGNED;
+    const bool logits_missing = (dt == DFL_F32) && !logits_out;
+    if (ws_bytes < ws_lm_head(N, B, row0, d, V, dt, logits_missing)) return DFL_ERR_WORKSPACE;
+    DeviceCtx* ctx = current_ctx();
+    if (!ctx) return DFL_ERR_NO_DEVICE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int nr = B - row0;
+    const int64_t M = (int64_t)N * nr;
+    const int tiles = (V + 255) / 256;
+    uint8_t* p = static_cast<uint8_t*>(ws);
+    void* Xn = carve(p, (size_t)M * d * esz(dt));
+    float* pmax = reinterpret_cast<float*>(carve(p, (size_t)M * tiles * 4));
+    int* pidx = reinterpret_cast<int*>(carve(p, (size_t)M * tiles * 4));
+    double* psum = reinterpret_cast<double*>(carve(p, (size_t)M * tiles * 8));
+    const float inv_T = sp ? 1.0f / sp->T : 1.0f;
+    dfl_status rc;
+    if ((rc = rmsnorm_rows(Xb, d, M, nr, B, row0, final_gain, eps, Xn, dt == DFL_BF16, st)) != DFL_OK) return rc;
+    if (dt == DFL_F32) {
+        float* lg = logits_out ? logits_out : reinterpret_cast<float*>(carve(p, (size_t)M * V * 4));
+        if ((rc = gemm_f32(static_cast<const float*>(Xn), static_cast<const float*>(W_lm), lg, (int)M, V, d, V, 0,
+                           st)) != DFL_OK)
+            return rc;
+        if ((rc = tile_partials(lg, V, M, V, 256, tiles, inv_T, pmax, pidx, sp ? psum : nullptr, st)) != DFL_OK)
+            return rc;
+        if ((rc = argmax_combine(pmax, pidx, M, tiles, argmax_out, st)) != DFL_OK) return rc;
+        if (sp) return sample_rows(lg, V, pmax, psum, M, nr, tiles, 256, V, sp->K, sp->T, sp->seed, samples_out, st);
+        return DFL_OK;
+    }
+    GemmArgs g{};
+    g.A = Xn; g.M = (int)M; g.K = d;
+    g.B[0] = W_lm; g.b_rows[0] = V; g.b_begin[0] = 0; g.nb = 1; g.N = V;
+    g.bn = 256;
+    g.m_inner = 1;
+    g.epi = EPI_ARGMAX;
+    g.ep.part_max = pmax; g.ep.part_idx = pidx; g.ep.part_sum = sp ? psum : nullptr;
+    g.ep.inv_T = inv_T;
+    g.ep.logits = logits_out; g.ep.ld_logits = V;
+    if ((rc = gemm_tc(ctx, g, st)) != DFL_OK) return rc;
+    if ((rc = argmax_combine(pmax, pidx, M, tiles, argmax_out, st)) != DFL_OK) return rc;
+    if (sp) return sample_rows(logits_out, V, pmax, psum, M, nr, tiles, 256, V, sp->K, sp->T, sp->seed, samples_out, st);
+    return DFL_OK;
+}
+
+// --------------------------------------------------------- self-selection
+
+extern "C" dfl_status dfl_self_select(const void* vlog, dfl_dtype dt, const int32_t* drafts, int32_t N, int32_t K,
+                                      int32_t G, int32_t V, float* scores, int32_t* selected, int32_t* accept_len,
+                                      int32_t* bonus, void* ws, size_t ws_bytes, dfl_stream stream) {
+    if (N <= 0 || K < 1 || K > 64 || G < 1 || G > 1024 || V <= 0) return DFL_ERR_INVALID_ARG;
+    if (dt != DFL_F32 && dt != DFL_BF16) return DFL_ERR_INVALID_ARG;
+    if (!vlog || !drafts || !scores || !selected || !accept_len || !bonus || !ws) return DFL_ERR_INVALID_ARG;
+    if (!aligned16(vlog) || !aligned16(ws)) return DFL_ERR_MISALIGNED;
+    if (ws_bytes < al256(select_ws_bytes(N, K, G))) return DFL_ERR_WORKSPACE;
+    if (!current_ctx()) return DFL_ERR_NO_DEVICE;
+    return self_select_run(vlog, dt == DFL_BF16, drafts, N, K, G, V, scores, selected, accept_len, bonus, ws,
+                           static_cast<cudaStream_t>(stream));
+}
+
+// ---------------------------------------------------------- whole step
+
+extern "C" dfl_status dfl_draft_step(const dfl_step_args* a, void* ws, size_t ws_bytes, dfl_stream stream) {
+    if (!a || !ws) return DFL_ERR_INVALID_ARG;
+    const int dt = a->dtype;
+    if (dt != DFL_F32 && dt != DFL_BF16) return DFL_ERR_INVALID_ARG;
+    if (a->N <= 0 || a->C <= 0 || a->B < 2 || a->d <= 0 || a->D < 1 || a->D > 8 || a->L < 1 || a->V < 0)
+        return DFL_ERR_INVALID_ARG;
+    if (!a->H || !a->mix_logits || !a->mix_gain || !a->blk_gain || !a->layers || !a->Xb0 || !a->Xb)
+        return DFL_ERR_INVALID_ARG;
+    if (a->V > 0 && (!a->W_lm || !a->final_gain || !a->draft)) return DFL_ERR_INVALID_ARG;
+    if (a->target && (!a->accept_len || !a->bonus)) return DFL_ERR_INVALID_ARG;
+    if (a->sample && (!a->samples || a->V == 0)) return DFL_ERR_INVALID_ARG;
+    if (a->vlog && (!a->sample || !a->scores || !a->selected || !a->accept_len || !a->bonus))
+        return DFL_ERR_INVALID_ARG;
+    for (int l = 0; l < a->D; ++l) {
+        const dfl_layer_weights& w = a->layers[l];
+        if (!w.Wq || !w.Wkc || !w.Wvc || !w.Wkb || !w.Wvb || !w.Wo) return DFL_ERR_INVALID_ARG;
+    }
+    dfl_shape s{};
+    s.N = a->N; s.C = a->C; s.B = a->B; s.d = a->d; s.Hq = a->Hq; s.Hkv = a->Hkv; s.hd = a->hd; s.D = a->D;
+    s.L = a->L; s.V = a->V; s.K = a->sample ? a->sample->K : 0; s.G = a->B - 1; s.row0 = 1; s.dtype = dt;
+    if (ws_bytes < dfl_workspace_size(DFL_OP_DRAFT_STEP, &s)) return DFL_ERR_WORKSPACE;
+    if (!aligned16(ws)) return DFL_ERR_MISALIGNED;
+    if (!current_ctx()) return DFL_ERR_NO_DEVICE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const dfl_dtype ddt = static_cast<dfl_dtype>(dt);
+    const size_t e = esz(dt);
+    const int N = a->N, C = a->C, B = a->B, d = a->d;
+    const int64_t ctx_rows = (int64_t)N * C;
+    uint8_t* p = static_cast<uint8_t*>(ws);
+    uint8_t* Xc = carve(p, (size_t)a->D * ctx_rows * d * e);
+    void* Q = carve(p, (size_t)N * B * a->Hq * a->hd * e);
+    void* Kc = carve(p, (size_t)ctx_rows * a->Hkv * a->hd * e);
+    void* Vc = carve(p, (size_t)ctx_rows * a->Hkv * a->hd * e);
+    void* Kb = carve(p, (size_t)N * B * a->Hkv * a->hd * e);
+    void* Vb = carve(p, (size_t)N * B * a->Hkv * a->hd * e);
+    int32_t* samples = a->samples;
+    if (a->V > 0 && s.K > 0) {
+        int32_t* own = reinterpret_cast<int32_t*>(carve(p, (size_t)N * s.K * (B - 1) * 4));
+        if (!samples) samples = own;
+    }
+    if (a->V > 0) carve(p, (size_t)N * (B - 1) * 4);
+    uint8_t* sub = p;
+    const size_t sub_bytes = ws_bytes - (size_t)(sub - static_cast<uint8_t*>(ws));
+    dfl_status rc;
+
+    if (cudaMemcpyAsync(a->Xb, a->Xb0, (size_t)N * B * d * sizeof(float), cudaMemcpyDeviceToDevice, st) !=
+        cudaSuccess)
+        return DFL_ERR_CUDA;
+    if ((rc = dfl_layer_mix_rmsnorm(a->H, a->h_layer_stride, a->L, ctx_rows, d, ddt, a->D, a->mix_logits,
+                                    a->mix_gain, a->eps, Xc, ctx_rows * d, stream)) != DFL_OK)
+        return rc;
+    for (int l = 0; l < a->D; ++l) {
+        const dfl_layer_weights& w = a->layers[l];
+        if ((rc = dfl_dual_kv_proj(Xc + (size_t)l * ctx_rows * d * e, a->Xb, N, C, B, d, ddt,
+                                   a->blk_gain + (size_t)l * d, a->eps, w.Wq, w.Wkc, w.Wvc, w.Wkb, w.Wvb, a->Hq,
+                                   a->Hkv, a->hd, a->rope, Q, Kc, Vc, Kb, Vb, sub, sub_bytes, stream)) != DFL_OK)
+            return rc;
+        if ((rc = dfl_block_attn(Q, Kc, Vc, Kb, Vb, N, C, B, a->Hq, a->Hkv, a->hd, ddt, w.Wo, d, a->Xb, sub,
+                                 sub_bytes, stream)) != DFL_OK)
+            return rc;
+    }
+    if (a->V == 0) return DFL_OK;
+    float* logits = a->logits;
+    if (!logits && a->sample) {   // sampling walks the logits; borrow the Xc area (no longer needed)
+        if ((size_t)N * (B - 1) * a->V * 4 > (size_t)a->D * ctx_rows * d * e) return DFL_ERR_WORKSPACE;
+        logits = reinterpret_cast<float*>(Xc);
+    }
+    if ((rc = dfl_lm_head_argmax(a->Xb, N, B, 1, d, ddt, a->final_gain, a->eps, a->W_lm, a->V, a->draft, logits,
+                                 a->sample, samples, sub, sub_bytes, stream)) != DFL_OK)
+        return rc;
+    if (a->vlog)
+        return dfl_self_select(a->vlog, ddt, samples, N, a->sample->K, B - 1, a->V, a->scores, a->selected,
+                               a->accept_len, a->bonus, sub, sub_bytes, stream);
+    if (a->target) return dfl_greedy_accept(a->draft, a->target, N, B - 1, a->accept_len, a->bonus, stream);
+    return DFL_OK;
+}

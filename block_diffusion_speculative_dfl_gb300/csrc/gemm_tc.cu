@@ -1,0 +1,92 @@
+// Host launcher of the tcgen05 GEMM: TMA descriptors, tile grid, launch.
+#include <mutex>
+
+#include "gemm_tc.cuh"
+#include "internal.h"
+
+namespace dfl {
+
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// bf16 [rows][K] row-major, box = box_rows x 64 elements, 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, int rows, int K, int box_rows) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+    cuuint32_t box[2] = {(cuuint32_t)GEMM_BK, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int BN, int EPI>
+dfl_status launch(DeviceCtx* ctx, const GemmArgs& g, const GemmShape& sh, const CUtensorMap (&mb)[3],
+                  const CUtensorMap& ma, cudaStream_t st, int slot) {
+    auto kern = gemm_tc_kernel<BN, EPI>;
+    if (!ctx->gemm_attr_set[slot]) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, GemmCfg<BN>::SMEM) !=
+            cudaSuccess)
+            return DFL_ERR_CUDA;
+        ctx->gemm_attr_set[slot] = true;
+    }
+    const int tiles = sh.tiles_m * sh.tiles_n;
+    const int grid = tiles < ctx->sm_count ? tiles : ctx->sm_count;
+    kern<<<grid, GEMM_THREADS, GemmCfg<BN>::SMEM, st>>>(ma, mb[0], mb[1], mb[2], sh, g.ep, dev_err(ctx));
+    return last_launch();
+}
+
+}  // namespace
+
+dfl_status gemm_tc(DeviceCtx* ctx, const GemmArgs& g, cudaStream_t st) {
+    if (g.M <= 0 || g.N <= 0 || g.K <= 0) return DFL_ERR_INVALID_ARG;
+    if (g.K % 8 != 0 || !aligned16(g.A)) return DFL_ERR_MISALIGNED;
+    if (g.bn != 128 && g.bn != 256) return DFL_ERR_UNSUPPORTED_SHAPE;
+    if (g.nb < 1 || g.nb > 3) return DFL_ERR_INVALID_ARG;
+    GemmShape sh{};
+    sh.M = g.M; sh.N = g.N; sh.K = g.K;
+    sh.tiles_m = (g.M + GEMM_BM - 1) / GEMM_BM;
+    sh.tiles_n = (g.N + g.bn - 1) / g.bn;
+    sh.num_kb = (g.K + GEMM_BK - 1) / GEMM_BK;
+    sh.m_inner = g.m_inner;
+    sh.nb = g.nb;
+    CUtensorMap ma, mb[3];
+    if (!make_map(&ma, g.A, g.M, g.K, GEMM_BM)) return DFL_ERR_CUDA;
+    for (int j = 0; j < 3; ++j) {
+        const int jj = j < g.nb ? j : 0;
+        if (!aligned16(g.B[jj])) return DFL_ERR_MISALIGNED;
+        // every tile of BN columns must come from one B map
+        if (j < g.nb && (g.b_begin[j] % g.bn != 0)) return DFL_ERR_UNSUPPORTED_SHAPE;
+        if (!make_map(&mb[j], g.B[jj], g.b_rows[jj], g.K, g.bn)) return DFL_ERR_CUDA;
+        sh.b_begin[j] = g.b_begin[jj];
+    }
+    const int slot = (g.bn == 256 ? 0 : 3) + g.epi;
+    if (g.bn == 256) {
+        if (g.epi == EPI_STORE) return launch<256, EPI_STORE>(ctx, g, sh, mb, ma, st, slot);
+        if (g.epi == EPI_RESID) return launch<256, EPI_RESID>(ctx, g, sh, mb, ma, st, slot);
+        return launch<256, EPI_ARGMAX>(ctx, g, sh, mb, ma, st, slot);
+    }
+    if (g.epi == EPI_STORE) return launch<128, EPI_STORE>(ctx, g, sh, mb, ma, st, slot);
+    if (g.epi == EPI_RESID) return launch<128, EPI_RESID>(ctx, g, sh, mb, ma, st, slot);
+    return launch<128, EPI_ARGMAX>(ctx, g, sh, mb, ma, st, slot);
+}
+
+}  // namespace dfl

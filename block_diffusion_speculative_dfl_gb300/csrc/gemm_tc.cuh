@@ -1,0 +1,354 @@
+// tcgen05 tensor-core GEMM for sm_103a: C[M][N] = A[M][K] * B[N][K]^T.
+//
+// A and B are bf16, K-major (row-major with K contiguous), loaded by TMA with
+// 128-byte swizzling into a shared-memory ring; one elected thread issues
+// tcgen05.mma (128 x BN x 16) into a double-buffered TMEM accumulator; four
+// epilogue warps read TMEM with tcgen05.ld and apply one of three epilogues:
+//   EPI_STORE  bf16 store into up to three column segments, rotary embedding
+//              on segments that ask for it;
+//   EPI_RESID  fp32 residual accumulate (out += C);
+//   EPI_ARGMAX per-row max / argmax over the tile's columns (lowest column on
+//              ties), optional fp32 logits store and optional per-tile
+//              sum of exp((z - tile max) / T) in fp64 for sampling.
+// The grid is persistent (one CTA per SM); tiles are walked in an order that
+// keeps the shared operand of consecutive tiles in L2.
+#pragma once
+
+#include "common.cuh"
+
+namespace dfl {
+
+enum EpiKind { EPI_STORE = 0, EPI_RESID = 1, EPI_ARGMAX = 2 };
+
+struct GemmSeg {
+    void* out;        // bf16 [M][ld] (EPI_STORE)
+    int n_begin;      // first global column of the segment
+    int ld;           // row stride, elements
+    int rope;         // apply rotate-half rotary embedding
+};
+
+struct GemmEpi {
+    GemmSeg seg[3];
+    int nseg;
+    // rotary: row r sits at position pos_off + (r % rows_per_seq)
+    const float* rope;   // [P][hd/2][2] (cos, sin)
+    int hd;
+    int rows_per_seq;
+    int pos_off;
+    // residual
+    float* resid;        // fp32 [M][ld_resid]
+    int ld_resid;
+    // argmax / sampling partials, [M][tiles_n]
+    float* part_max;
+    int* part_idx;
+    double* part_sum;    // nullable: sum exp((z - tile max) * inv_T)
+    float inv_T;
+    float* logits;       // nullable fp32 [M][ld_logits]
+    int64_t ld_logits;
+};
+
+struct GemmShape {
+    int M, N, K;
+    int tiles_m, tiles_n, num_kb;
+    int m_inner;         // 1: consecutive tiles walk M (share B); 0: walk N (share A)
+    int b_begin[3];      // first column served by B tensor map 1, 2, 3
+    int nb;              // number of B tensor maps
+};
+
+constexpr int GEMM_BM = 128;
+constexpr int GEMM_BK = 64;
+constexpr int GEMM_THREADS = 192;
+
+template <int BN>
+struct GemmCfg {
+    static constexpr int STAGES = (BN == 256) ? 4 : 6;
+    static constexpr int A_BYTES = GEMM_BM * GEMM_BK * 2;
+    static constexpr int B_BYTES = BN * GEMM_BK * 2;
+    static constexpr int TMEM_COLS = 2 * BN;
+    static constexpr int BAR_BYTES = 256;
+    static constexpr int SMEM = 1024 + STAGES * (A_BYTES + B_BYTES) + BAR_BYTES;
+};
+
+__device__ __forceinline__ void tile_coords(const GemmShape& sh, int t, int& tm, int& tn) {
+    if (sh.m_inner) { tm = t % sh.tiles_m; tn = t / sh.tiles_m; }
+    else            { tn = t % sh.tiles_n; tm = t / sh.tiles_n; }
+}
+
+__device__ __forceinline__ void store_bf16x32(void* dst, const float (&v)[32]) {
+    uint4* p = reinterpret_cast<uint4*>(dst);
+    #pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        uint4 u;
+        u.x = pack_bf16(v[8 * q + 0], v[8 * q + 1]);
+        u.y = pack_bf16(v[8 * q + 2], v[8 * q + 3]);
+        u.z = pack_bf16(v[8 * q + 4], v[8 * q + 5]);
+        u.w = pack_bf16(v[8 * q + 6], v[8 * q + 7]);
+        p[q] = u;
+    }
+}
+
+// ---------------------------------------------------------------- epilogues
+
+template <int BN>
+__device__ __forceinline__ void epi_store(const GemmShape& sh, const GemmEpi& ep, uint32_t tbase,
+                                          int row, int n0) {
+    int s = 0;
+    #pragma unroll
+    for (int j = 1; j < 3; ++j)
+        if (j < ep.nseg && n0 >= ep.seg[j].n_begin) s = j;
+    const GemmSeg sg = ep.seg[s];
+    const bool ok = row < sh.M;
+    __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(sg.out) + (int64_t)(ok ? row : 0) * sg.ld +
+                         (n0 - sg.n_begin);
+    if (!sg.rope) {
+        #pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+            float v[32];
+            tmem_ld32(tbase + c * 32, v);
+            if (ok) store_bf16x32(out + c * 32, v);
+        }
+        return;
+    }
+    const int hd = ep.hd;
+    const int half = hd >> 1;
+    const int pos = ep.pos_off + (ok ? row : 0) % ep.rows_per_seq;
+    const float2* cs = reinterpret_cast<const float2*>(ep.rope) + (int64_t)pos * half;
+    #pragma unroll 1
+    for (int h0 = 0; h0 < BN; h0 += hd) {
+        #pragma unroll 1
+        for (int c = 0; c < half; c += 32) {
+            float x[32], y[32];
+            tmem_ld32(tbase + h0 + c, x);
+            tmem_ld32(tbase + h0 + c + half, y);
+            if (ok) {
+                #pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const float2 t = __ldg(cs + c + j);
+                    const float a = x[j], b = y[j];
+                    x[j] = a * t.x - b * t.y;
+                    y[j] = b * t.x + a * t.y;
+                }
+                store_bf16x32(out + h0 + c, x);
+                store_bf16x32(out + h0 + c + half, y);
+            }
+        }
+    }
+}
+
+template <int BN>
+__device__ __forceinline__ void epi_resid(const GemmShape& sh, const GemmEpi& ep, uint32_t tbase,
+                                          int row, int n0) {
+    const bool ok = row < sh.M;
+    float* out = ep.resid + (int64_t)(ok ? row : 0) * ep.ld_resid + n0;
+    #pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+        float v[32];
+        tmem_ld32(tbase + c * 32, v);
+        if (ok && n0 + c * 32 < sh.N) {
+            float4* p = reinterpret_cast<float4*>(out + c * 32);
+            #pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                float4 o = p[q];
+                o.x += v[4 * q + 0]; o.y += v[4 * q + 1]; o.z += v[4 * q + 2]; o.w += v[4 * q + 3];
+                p[q] = o;
+            }
+        }
+    }
+}
+
+template <int BN>
+__device__ __forceinline__ void epi_argmax(const GemmShape& sh, const GemmEpi& ep, uint32_t tbase,
+                                           int row, int n0, int tn) {
+    const bool ok = row < sh.M;
+    float best = -INFINITY;
+    int bidx = n0;
+    float* lg = ep.logits ? ep.logits + (int64_t)(ok ? row : 0) * ep.ld_logits : nullptr;
+    #pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+        float v[32];
+        tmem_ld32(tbase + c * 32, v);
+        const int cb = n0 + c * 32;
+        #pragma unroll
+        for (int j = 0; j < 32; ++j)
+            if (cb + j < sh.N && v[j] > best) { best = v[j]; bidx = cb + j; }
+        if (ok && lg) {
+            if (cb + 32 <= sh.N && (ep.ld_logits & 3) == 0) {
+                float4* p = reinterpret_cast<float4*>(lg + cb);
+                #pragma unroll
+                for (int q = 0; q < 8; ++q) p[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+            } else {
+                #pragma unroll
+                for (int j = 0; j < 32; ++j) if (cb + j < sh.N) lg[cb + j] = v[j];
+            }
+        }
+    }
+    double s = 0.0;
+    if (ep.part_sum) {
+        #pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+            float v[32];
+            tmem_ld32(tbase + c * 32, v);
+            const int cb = n0 + c * 32;
+            #pragma unroll
+            for (int j = 0; j < 32; ++j)
+                if (cb + j < sh.N) s += (double)expf((v[j] - best) * ep.inv_T);
+        }
+    }
+    if (ok) {
+        const int64_t o = (int64_t)row * sh.tiles_n + tn;
+        ep.part_max[o] = best;
+        ep.part_idx[o] = bidx;
+        if (ep.part_sum) ep.part_sum[o] = s;
+    }
+}
+
+// ------------------------------------------------------------------- kernel
+
+template <int BN, int EPI>
+__global__ void __launch_bounds__(GEMM_THREADS, 1)
+gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
+               const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmB2,
+               const GemmShape sh, const GemmEpi ep, const DevErr err) {
+    using Cfg = GemmCfg<BN>;
+    constexpr int STAGES = Cfg::STAGES;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sA = smem;
+    uint8_t* sB = smem + STAGES * Cfg::A_BYTES;
+    uint64_t* full = reinterpret_cast<uint64_t*>(sB + STAGES * Cfg::B_BYTES);
+    uint64_t* empty = full + STAGES;
+    uint64_t* tfull = empty + STAGES;
+    uint64_t* tempty = tfull + 2;
+    uint64_t* drain = tempty + 2;
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
+        for (int a = 0; a < 2; ++a) { mbar_init(&tfull[a], 1); mbar_init(&tempty[a], 128); }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tensormap(&tmA);
+        prefetch_tensormap(&tmB0);
+        if (sh.nb > 1) prefetch_tensormap(&tmB1);
+        if (sh.nb > 2) prefetch_tensormap(&tmB2);
+    }
+    if (warp == 1) { tmem_alloc(tmem_holder, Cfg::TMEM_COLS); tmem_relinquish(); }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+    const int total = sh.tiles_m * sh.tiles_n;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------- TMA producer
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t fills = 0;   // bit s: stage s has been filled at least once
+            bool aborted = false;
+            for (int t = blockIdx.x; t < total && !aborted; t += gridDim.x) {
+                int tm, tn;
+                tile_coords(sh, t, tm, tn);
+                const int m0 = tm * GEMM_BM, n0 = tn * BN;
+                const CUtensorMap* mb = &tmB0;
+                int nb0 = n0;
+                if (sh.nb > 2 && n0 >= sh.b_begin[2]) { mb = &tmB2; nb0 = n0 - sh.b_begin[2]; }
+                else if (sh.nb > 1 && n0 >= sh.b_begin[1]) { mb = &tmB1; nb0 = n0 - sh.b_begin[1]; }
+                for (int kb = 0; kb < sh.num_kb; ++kb) {
+                    if (*abort_flag || !mbar_wait(&empty[stage], phase ^ 1, err)) { aborted = true; break; }
+                    mbar_arrive_expect_tx(&full[stage], Cfg::A_BYTES + Cfg::B_BYTES);
+                    tma_load_2d(sA + stage * Cfg::A_BYTES, &tmA, kb * GEMM_BK, m0, &full[stage]);
+                    tma_load_2d(sB + stage * Cfg::B_BYTES, mb, kb * GEMM_BK, nb0, &full[stage]);
+                    fills |= 1u << stage;
+                    if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                }
+            }
+            if (aborted) {
+                *abort_flag = 1;
+                // Let every copy already issued land before the CTA exits.  The
+                // latest fill of stage s has parity phase(s) computed from the
+                // position of the ring at exit.
+                for (int s = 0; s < STAGES; ++s) {
+                    if (!(fills & (1u << s))) continue;
+                    const uint32_t par = (s < stage) ? phase : (phase ^ 1);
+                    mbar_wait(&full[s], par, err);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---------------- MMA issuer
+            constexpr uint32_t idesc = idesc_bf16(GEMM_BM, BN);
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            bool aborted = false;
+            bool issued = false;
+            for (int t = blockIdx.x; t < total && !aborted; t += gridDim.x) {
+                if (*abort_flag || !mbar_wait(&tempty[acc], acc_phase ^ 1, err)) { aborted = true; break; }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + acc * BN;
+                for (int kb = 0; kb < sh.num_kb; ++kb) {
+                    if (*abort_flag || !mbar_wait(&full[stage], phase, err)) { aborted = true; break; }
+                    tc_fence_after();
+                    const uint64_t ad = sw128_desc(smem_u32(sA + stage * Cfg::A_BYTES));
+                    const uint64_t bd = sw128_desc(smem_u32(sB + stage * Cfg::B_BYTES));
+                    #pragma unroll
+                    for (int k = 0; k < GEMM_BK / 16; ++k)
+                        mma_bf16(d_tmem, ad + 2 * k, bd + 2 * k, idesc, (kb | k) != 0);
+                    issued = true;
+                    mma_commit(&empty[stage]);
+                    if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                }
+                if (aborted) break;
+                mma_commit(&tfull[acc]);
+                acc ^= 1;
+                if (acc == 0) acc_phase ^= 1;
+            }
+            if (aborted) {
+                *abort_flag = 1;
+                if (issued) {   // let issued MMAs finish before TMEM is released
+                    mma_commit(drain);
+                    mbar_wait(drain, 0, err);
+                }
+            }
+        }
+    } else {
+        // ---------------- epilogue warps 2..5: TMEM lane quadrant = warp % 4
+        const int q = warp & 3;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int t = blockIdx.x; t < total; t += gridDim.x) {
+            if (__any_sync(0xFFFFFFFFu, *abort_flag != 0)) break;
+            const bool ready = mbar_wait(&tfull[acc], acc_phase, err);
+            if (!__all_sync(0xFFFFFFFFu, ready)) { *abort_flag = 1; break; }
+            tc_fence_after();
+            int tm, tn;
+            tile_coords(sh, t, tm, tn);
+            const int row = tm * GEMM_BM + q * 32 + lane;
+            const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
+            if (EPI == EPI_STORE) epi_store<BN>(sh, ep, tbase, row, tn * BN);
+            else if (EPI == EPI_RESID) epi_resid<BN>(sh, ep, tbase, row, tn * BN);
+            else epi_argmax<BN>(sh, ep, tbase, row, tn * BN, tn);
+            tc_fence_before();
+            mbar_arrive(&tempty[acc]);
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1;
+        }
+    }
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+    }
+}
+
+}  // namespace dfl

@@ -1,0 +1,54 @@
+// Host-side internals shared by the library's translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/dfl.h"
+#include "gemm_tc.cuh"
+
+namespace dfl {
+
+// Per-device context: error-word address, SM count, cached attributes.
+struct DeviceCtx {
+    int device = -1;
+    int sm_count = 0;
+    int* err_word = nullptr;       // device address of this device's error word
+    bool gemm_attr_set[8] = {};    // max-dynamic-smem set for gemm instantiations
+    bool mix_attr_set = false;
+};
+
+// Context of the current device (initialised on first use); nullptr if no
+// usable device.
+DeviceCtx* current_ctx();
+DevErr dev_err(DeviceCtx* ctx);
+uint64_t wait_limit_ns();
+
+inline dfl_status cuda_status(cudaError_t e) { return e == cudaSuccess ? DFL_OK : DFL_ERR_CUDA; }
+inline dfl_status last_launch() { return cuda_status(cudaGetLastError()); }
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ---------------------------------------------------------------- GEMM --
+
+struct GemmArgs {
+    const void* A;          // bf16 [M][K]
+    int M, K;
+    const void* B[3];       // bf16 [n_b][K] each; B[j] serves columns from b_begin[j]
+    int b_rows[3];
+    int b_begin[3];
+    int nb;
+    int N;                  // total columns
+    int m_inner;
+    int bn;                 // 128 or 256
+    int epi;                // EpiKind
+    GemmEpi ep;
+};
+
+dfl_status gemm_tc(DeviceCtx* ctx, const GemmArgs& g, cudaStream_t st);
+
+// fp32 CUDA-core GEMM: C = A[M][K] * B[N][K]^T; mode 0 store (ldc), 1 accumulate.
+dfl_status gemm_f32(const float* A, const float* B, float* C, int M, int N, int K, int ldc, int accumulate,
+                    cudaStream_t st);
+
+}  // namespace dfl

@@ -1,0 +1,199 @@
+// Streak-score self-selection of K drafts and greedy acceptance.
+//
+// SpecDiff-2 notes, "Streak-Distillation": expected accepted tokens per draft
+// = sum_{m=1}^{gamma} prod_{j<=m} alpha_j.  "Self-Selection Acceptance": K
+// drafts sampled from one denoising step are scored with the verifier's
+// per-token posteriors, the best draft is kept, and greedy acceptance runs
+// on it reusing the cached verifier probabilities (draft probabilities are
+// not used).
+//
+// Pass 1 (HBM-bound, one read of the verifier logits): per verifier row its
+// log-sum-exp, argmax (lowest index on ties) and the logit at the draft
+// token.  Pass 2 (one warp per sequence): log p_j = z[x_j] - LSE_j,
+// S_k = sum_m exp(sum_{j<=m} log p_j) in fp64, k* = argmax_k S_k (lowest k on
+// ties), then the prefix of x^{k*} matching the argmax of its verifier rows
+// and the bonus token.
+#include "internal.h"
+#include "small_kernels.h"
+
+namespace dfl {
+
+namespace {
+
+constexpr int RS_THREADS = 256;
+
+struct RowStat {
+    float m;    // running max
+    float s;    // sum exp(x - m)
+    int idx;    // lowest index of the max
+};
+
+__device__ __forceinline__ RowStat rs_combine(RowStat a, RowStat b) {
+    RowStat r;
+    r.m = fmaxf(a.m, b.m);
+    r.idx = (b.m > a.m || (b.m == a.m && b.idx < a.idx)) ? b.idx : a.idx;
+    const float sa = a.m == -INFINITY ? 0.f : a.s * expf(a.m - r.m);
+    const float sb = b.m == -INFINITY ? 0.f : b.s * expf(b.m - r.m);
+    r.s = sa + sb;
+    return r;
+}
+
+__device__ __forceinline__ void rs_push8(RowStat& st, const float (&x)[8], int base) {
+    float vm = x[0];
+    #pragma unroll
+    for (int j = 1; j < 8; ++j) vm = fmaxf(vm, x[j]);
+    if (vm > st.m) {
+        st.s = st.m == -INFINITY ? 0.f : st.s * expf(st.m - vm);
+        st.m = vm;
+        int f = 7;
+        #pragma unroll
+        for (int j = 7; j >= 0; --j) if (x[j] == vm) f = j;
+        st.idx = base + f;
+    }
+    float acc = 0.f;
+    #pragma unroll
+    for (int j = 0; j < 8; ++j) acc += expf(x[j] - st.m);
+    st.s += acc;
+}
+
+template <bool BF16>
+__device__ __forceinline__ float load1(const void* row, int64_t i) {
+    if constexpr (BF16) {
+        const uint16_t u = static_cast<const uint16_t*>(row)[i];
+        return __uint_as_float((uint32_t)u << 16);
+    } else {
+        return static_cast<const float*>(row)[i];
+    }
+}
+
+template <bool BF16>
+__global__ void __launch_bounds__(RS_THREADS) verifier_row_stats_kernel(const void* vlog, int K, int G, int V,
+                                                                        const int32_t* drafts, float* lse, int* amax,
+                                                                        float* zx) {
+    const int64_t rr = blockIdx.x;
+    const int G1 = G + 1;
+    const size_t esz = BF16 ? 2 : 4;
+    const uint8_t* row = static_cast<const uint8_t*>(vlog) + rr * (int64_t)V * esz;
+    RowStat st{-INFINITY, 0.f, 0x7FFFFFFF};
+    const bool vec = (V % 8) == 0;
+    if (vec) {
+        const int chunks = V / 8;
+        for (int c = threadIdx.x; c < chunks; c += RS_THREADS) {
+            float x[8];
+            if constexpr (BF16) {
+                const uint4 u = reinterpret_cast<const uint4*>(row)[c];
+                x[0] = bf16lo(u.x); x[1] = bf16hi(u.x); x[2] = bf16lo(u.y); x[3] = bf16hi(u.y);
+                x[4] = bf16lo(u.z); x[5] = bf16hi(u.z); x[6] = bf16lo(u.w); x[7] = bf16hi(u.w);
+            } else {
+                const float4 u0 = reinterpret_cast<const float4*>(row)[2 * c];
+                const float4 u1 = reinterpret_cast<const float4*>(row)[2 * c + 1];
+                x[0] = u0.x; x[1] = u0.y; x[2] = u0.z; x[3] = u0.w;
+                x[4] = u1.x; x[5] = u1.y; x[6] = u1.z; x[7] = u1.w;
+            }
+            rs_push8(st, x, c * 8);
+        }
+    } else {
+        for (int i = threadIdx.x; i < V; i += RS_THREADS) {
+            const float x = load1<BF16>(row, i);
+            if (x > st.m) {
+                st.s = st.m == -INFINITY ? 0.f : st.s * expf(st.m - x);
+                st.m = x;
+                st.idx = i;
+            }
+            st.s += expf(x - st.m);
+        }
+    }
+    #pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        RowStat b;
+        b.m = __shfl_xor_sync(0xFFFFFFFFu, st.m, o);
+        b.s = __shfl_xor_sync(0xFFFFFFFFu, st.s, o);
+        b.idx = __shfl_xor_sync(0xFFFFFFFFu, st.idx, o);
+        st = rs_combine(st, b);
+    }
+    __shared__ RowStat red[RS_THREADS / 32];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) red[warp] = st;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        RowStat t = red[0];
+        for (int w = 1; w < RS_THREADS / 32; ++w) t = rs_combine(t, red[w]);
+        lse[rr] = t.m + logf(t.s);
+        amax[rr] = t.idx;
+        const int j = (int)(rr % G1);
+        if (j < G) {
+            const int64_t nk = rr / G1;   // n * K + k
+            const int32_t x = drafts[nk * G + j];
+            zx[rr] = (x >= 0 && x < V) ? load1<BF16>(row, x) : -INFINITY;
+        }
+    }
+}
+
+__global__ void streak_select_kernel(const int32_t* drafts, int N, int K, int G, const float* lse, const int* amax,
+                                     const float* zx, float* scores, int32_t* selected, int32_t* accept_len,
+                                     int32_t* bonus) {
+    const int n = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (n >= N) return;
+    const int G1 = G + 1;
+    double best = -1.0;
+    int bk = 0x7FFFFFFF;
+    for (int k = lane; k < K; k += 32) {
+        const int64_t r0 = ((int64_t)n * K + k) * G1;
+        double c = 0.0, S = 0.0;
+        for (int j = 0; j < G; ++j) {
+            c += (double)zx[r0 + j] - (double)lse[r0 + j];
+            S += exp(c);
+        }
+        scores[(int64_t)n * K + k] = (float)S;
+        if (S > best) { best = S; bk = k; }
+    }
+    #pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const double v = __shfl_xor_sync(0xFFFFFFFFu, best, o);
+        const int i = __shfl_xor_sync(0xFFFFFFFFu, bk, o);
+        if (v > best || (v == best && i < bk)) { best = v; bk = i; }
+    }
+    const int64_t r0 = ((int64_t)n * K + bk) * G1;
+    const int32_t* x = drafts + ((int64_t)n * K + bk) * G;
+    int a = G;
+    for (int j0 = 0; j0 < G; j0 += 32) {
+        const int j = j0 + lane;
+        const unsigned mism = __ballot_sync(0xFFFFFFFFu, j < G && x[j] != amax[r0 + j]);
+        if (mism) { a = j0 + __ffs(mism) - 1; break; }
+    }
+    if (lane == 0) {
+        selected[n] = bk;
+        accept_len[n] = a;
+        bonus[n] = amax[r0 + a];
+    }
+}
+
+}  // namespace
+
+size_t select_ws_bytes(int N, int K, int G) {
+    const size_t rows = (size_t)N * K * (G + 1);
+    return 3 * ((rows * 4 + 255) & ~size_t(255));
+}
+
+dfl_status self_select_run(const void* vlog, bool bf16, const int32_t* drafts, int N, int K, int G, int V,
+                           float* scores, int32_t* selected, int32_t* accept_len, int32_t* bonus, void* ws,
+                           cudaStream_t st) {
+    const size_t rows = (size_t)N * K * (G + 1);
+    const size_t slot = (rows * 4 + 255) & ~size_t(255);
+    float* lse = static_cast<float*>(ws);
+    int* amax = reinterpret_cast<int*>(static_cast<uint8_t*>(ws) + slot);
+    float* zx = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + 2 * slot);
+    if (bf16)
+        verifier_row_stats_kernel<true><<<(unsigned)rows, RS_THREADS, 0, st>>>(vlog, K, G, V, drafts, lse, amax, zx);
+    else
+        verifier_row_stats_kernel<false><<<(unsigned)rows, RS_THREADS, 0, st>>>(vlog, K, G, V, drafts, lse, amax,
+                                                                                 zx);
+    dfl_status rc = last_launch();
+    if (rc != DFL_OK) return rc;
+    streak_select_kernel<<<(N + 3) / 4, 128, 0, st>>>(drafts, N, K, G, lse, amax, zx, scores, selected, accept_len,
+                                                        bonus);
+    return last_launch();
+}
+
+}  // namespace dfl

@@ -1,0 +1,42 @@
+// Host launchers of the draft step's smaller kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/dfl.h"
+
+namespace dfl {
+
+dfl_status rope_table(float* table, int P, int hd, double theta, cudaStream_t st);
+// out[m] = RMSNorm(in[(m / per) * stride + off + m % per]) * gain; bf16 or fp32 out.
+dfl_status rmsnorm_rows(const float* in, int d, int64_t M, int per, int stride, int off, const float* gain,
+                        float eps, void* out, bool bf16, cudaStream_t st);
+dfl_status greedy_accept(const int32_t* draft, const int32_t* target, int N, int n, int32_t* accept_len,
+                         int32_t* bonus, cudaStream_t st);
+dfl_status argmax_combine(const float* pmax, const int* pidx, int64_t M, int tiles, int32_t* out,
+                          cudaStream_t st);
+dfl_status sample_rows(const float* logits, int64_t ld, const float* pmax, const double* psum, int64_t M, int per,
+                       int tiles, int bn, int V, int K, float T, uint64_t seed, int32_t* samples, cudaStream_t st);
+dfl_status tile_partials(const float* logits, int64_t ld, int64_t M, int V, int bn, int tiles, float inv_T,
+                         float* pmax, int* pidx, double* psum, cudaStream_t st);
+dfl_status rope_inplace_f32(float* x, int64_t rows, int heads, int hd, int per, int pos_off, const float* rope,
+                            cudaStream_t st);
+dfl_status attn_f32(const float* Q, const float* Kc, const float* Vc, const float* Kb, const float* Vb, int N, int C,
+                    int B, int Hq, int Hkv, int hd, float* O, cudaStream_t st);
+dfl_status selftest_wait(int* status, uint64_t limit_ns, cudaStream_t st);
+
+// bf16 block attention (tensor cores); writes O bf16 [N*B][Hq*hd].  ws holds
+// split-KV partials when more than one split is used.
+int attn_splits(int N, int C, int B, int Hkv);
+size_t attn_ws_bytes(int N, int C, int B, int Hq, int Hkv, int hd);
+dfl_status attn_bf16(const void* Q, const void* Kc, const void* Vc, const void* Kb, const void* Vb, int N, int C,
+                     int B, int Hq, int Hkv, int hd, void* O, void* ws, cudaStream_t st);
+
+// self-selection
+size_t select_ws_bytes(int N, int K, int G);
+dfl_status self_select_run(const void* vlog, bool bf16, const int32_t* drafts, int N, int K, int G, int V,
+                           float* scores, int32_t* selected, int32_t* accept_len, int32_t* bonus, void* ws,
+                           cudaStream_t st);
+
+}  // namespace dfl

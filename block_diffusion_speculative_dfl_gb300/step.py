@@ -1,0 +1,144 @@
+"""Device-resident drafter and one-call draft step over the C ABI.
+
+``DraftModel`` owns the drafter's parameters on the GPU (torch tensors used as
+device memory only), the rotary table, the workspace and the output buffers
+for a fixed shape; ``step()`` runs the whole single-pass draft step through
+``dfl_draft_step`` on the current stream.  All pointers stay fixed between
+calls, so a step can be captured into a CUDA graph.  ``step_from_host()``
+is the end-to-end form: pinned host inputs are copied in and the per-sequence
+results copied back on the same stream.
+"""
+from __future__ import annotations
+
+import ctypes as C
+from dataclasses import dataclass
+
+import torch
+
+from . import _lib
+from ._lib import DFL_BF16, DFL_F32, LayerWeights, SampleParams, StepArgs
+
+
+@dataclass(frozen=True)
+class DraftShape:
+    N: int
+    d: int
+    Hq: int
+    Hkv: int
+    hd: int
+    D: int
+    L: int
+    B: int
+    C: int
+    V: int
+    dtype: str = "bf16"
+    K: int = 0
+    T: float = 1.0
+    seed: int = 0
+    eps: float = 1e-6
+    rope_theta: float = 1e6
+
+    @property
+    def torch_dtype(self):
+        return torch.bfloat16 if self.dtype == "bf16" else torch.float32
+
+    @property
+    def dt(self) -> int:
+        return DFL_BF16 if self.dtype == "bf16" else DFL_F32
+
+
+class DraftModel:
+    """Drafter parameters, workspace and outputs for one shape on one device."""
+
+    def __init__(self, shape: DraftShape, mix_logits, mix_gain, blk_gain, final_gain, layers, W_lm=None,
+                 device="cuda"):
+        s = self.shape = shape
+        dev = torch.device(device)
+        wd = shape.torch_dtype
+
+        def dev_t(x, dtype):
+            return torch.as_tensor(x).to(device=dev, dtype=dtype).contiguous()
+
+        self.mix_logits = dev_t(mix_logits, torch.float32)
+        self.mix_gain = dev_t(mix_gain, torch.float32)
+        self.blk_gain = dev_t(blk_gain, torch.float32)
+        self.final_gain = dev_t(final_gain, torch.float32)
+        self.layers = [{k: dev_t(v, wd) for k, v in w.items()} for w in layers]
+        self.W_lm = dev_t(W_lm, wd) if (W_lm is not None and s.V > 0) else None
+        self.rope = torch.empty((s.C + s.B, s.hd // 2, 2), dtype=torch.float32, device=dev)
+        _lib.dfl_rope_table(self.rope, s.C + s.B, s.hd, s.rope_theta)
+        self._lw = (LayerWeights * s.D)(*[LayerWeights(*[_lib.ptr(w[k]) for k in
+                                                          ("Wq", "Wkc", "Wvc", "Wkb", "Wvb", "Wo")])
+                                          for w in self.layers])
+        self._sp = SampleParams(s.K, s.T, s.seed) if s.K > 0 else None
+        self.ws_bytes = _lib.workspace_size(_lib.DFL_OP_DRAFT_STEP, N=s.N, C=s.C, B=s.B, d=s.d, Hq=s.Hq, Hkv=s.Hkv,
+                                            hd=s.hd, D=s.D, L=s.L, V=s.V, K=s.K, G=s.B - 1, row0=1, dtype=s.dt)
+        self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
+        self.Xb = torch.empty((s.N, s.B, s.d), dtype=torch.float32, device=dev)
+        n = s.B - 1
+        self.draft = torch.empty((s.N, n), dtype=torch.int32, device=dev) if s.V > 0 else None
+        self.accept_len = torch.empty((s.N,), dtype=torch.int32, device=dev)
+        self.bonus = torch.empty((s.N,), dtype=torch.int32, device=dev)
+        self.samples = torch.empty((s.N, s.K, n), dtype=torch.int32, device=dev) if s.K > 0 else None
+        self.scores = torch.empty((s.N, s.K), dtype=torch.float32, device=dev) if s.K > 0 else None
+        self.selected = torch.empty((s.N,), dtype=torch.int32, device=dev) if s.K > 0 else None
+        self.logits = None
+
+    def want_logits(self, on: bool = True):
+        """Keep the fp32 logits [N*(B-1)][V] of each step (needed to check argmax bit-exactly)."""
+        s = self.shape
+        self.logits = (torch.empty((s.N * (s.B - 1), s.V), dtype=torch.float32, device=self.Xb.device)
+                       if on and s.V > 0 else None)
+
+    def _args(self, H, Xb0, target, vlog) -> StepArgs:
+        s = self.shape
+        a = StepArgs()
+        a.N, a.C, a.B, a.d, a.Hq, a.Hkv, a.hd, a.D, a.L, a.V = s.N, s.C, s.B, s.d, s.Hq, s.Hkv, s.hd, s.D, s.L, s.V
+        a.dtype, a.eps = s.dt, s.eps
+        a.H, a.h_layer_stride = _lib.ptr(H), s.N * s.C * s.d
+        a.mix_logits, a.mix_gain, a.blk_gain = _lib.ptr(self.mix_logits), _lib.ptr(self.mix_gain), _lib.ptr(self.blk_gain)
+        a.final_gain, a.rope = _lib.ptr(self.final_gain), _lib.ptr(self.rope)
+        a.layers = C.cast(self._lw, C.POINTER(LayerWeights))
+        a.W_lm, a.Xb0, a.Xb = _lib.ptr(self.W_lm), _lib.ptr(Xb0), _lib.ptr(self.Xb)
+        a.draft, a.logits = _lib.ptr(self.draft), _lib.ptr(self.logits)
+        a.target = _lib.ptr(target)
+        a.accept_len, a.bonus = _lib.ptr(self.accept_len), _lib.ptr(self.bonus)
+        if self._sp is not None:
+            a.sample = C.pointer(self._sp)
+            a.samples = _lib.ptr(self.samples)
+            if vlog is not None:
+                a.vlog, a.scores, a.selected = _lib.ptr(vlog), _lib.ptr(self.scores), _lib.ptr(self.selected)
+        return a
+
+    def step(self, H, Xb0, target=None, vlog=None, stream=None):
+        """One draft step on device-resident inputs (H [L][N*C][d], Xb0 [N][B][d] fp32)."""
+        self._last_args = self._args(H, Xb0, target, vlog)
+        _lib.dfl_draft_step(self._last_args, self.ws, self.ws_bytes, stream)
+
+    def step_from_host(self, H_host, Xb0_host, target_host=None, vlog_host=None, dev_in=None, stream=None):
+        """End-to-end step: copy pinned host inputs in, run, copy results out.
+
+        ``dev_in`` is a dict of preallocated device buffers with the inputs'
+        shapes (allocated on first use).  Returns host tensors of the
+        per-sequence results.
+        """
+        st = stream or torch.cuda.current_stream()
+        if dev_in is None:
+            dev_in = {}
+        ins = {"H": H_host, "Xb0": Xb0_host, "target": target_host, "vlog": vlog_host}
+        with torch.cuda.stream(st):
+            for k, h in ins.items():
+                if h is None:
+                    continue
+                if k not in dev_in:
+                    dev_in[k] = torch.empty(h.shape, dtype=h.dtype, device=self.Xb.device)
+                dev_in[k].copy_(h, non_blocking=True)
+            self.step(dev_in["H"], dev_in["Xb0"], dev_in.get("target"), dev_in.get("vlog"), stream=st)
+            out = {"accept_len": self.accept_len.to("cpu", non_blocking=True),
+                   "bonus": self.bonus.to("cpu", non_blocking=True)}
+            if self.draft is not None:
+                out["draft"] = self.draft.to("cpu", non_blocking=True)
+            if self.selected is not None and vlog_host is not None:
+                out["selected"] = self.selected.to("cpu", non_blocking=True)
+        st.synchronize()
+        return out, dev_in

@@ -1,0 +1,49 @@
+"""Helpers shared by the GPU parity tests (tolerances, transfers)."""
+import numpy as np
+import torch
+
+# Parity bars: fp32 max-abs 1e-4; bf16 max|gpu - oracle| / rms(oracle) 3e-2.
+F32_MAX_ABS = 1e-4
+BF16_REL_RMS = 3e-2
+# A tighter check on the typical element for bf16 (mean error / rms), which a
+# wrong weight or index shows long before the max-error bar does.
+BF16_MEAN_REL = 4e-3
+
+
+def rel_rms_err(gpu, ref):
+    gpu = np.asarray(gpu, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    rms = np.sqrt(np.mean(ref * ref))
+    return float(np.max(np.abs(gpu - ref)) / rms), float(np.mean(np.abs(gpu - ref)) / rms)
+
+
+def assert_bf16_close(gpu, ref, name="", mean_bar=BF16_MEAN_REL):
+    mx, mean = rel_rms_err(gpu, ref)
+    assert mx <= BF16_REL_RMS, f"{name}: max err / rms = {mx:.3e}"
+    assert mean <= mean_bar, f"{name}: mean err / rms = {mean:.3e}"
+
+
+def assert_f32_close(gpu, ref, name=""):
+    err = float(np.max(np.abs(np.asarray(gpu, np.float64) - np.asarray(ref, np.float64))))
+    assert err <= F32_MAX_ABS, f"{name}: max-abs error {err:.3e}"
+
+
+def dev(x, dtype=None):
+    """numpy -> cuda tensor (bf16 when dtype == 'bf16'; values already bf16-exact)."""
+    t = torch.from_numpy(np.ascontiguousarray(x))
+    if dtype == "bf16":
+        return t.to(torch.float32).cuda().to(torch.bfloat16)
+    return t.cuda()
+
+
+def host(t):
+    return t.detach().float().cpu().numpy() if t.dtype in (torch.bfloat16, torch.float16) else t.detach().cpu().numpy()
+
+
+def bf16_round(x):
+    from dfl_synth import round_bf16
+    return round_bf16(np.asarray(x, dtype=np.float32))
+
+
+def rng_bf16(rng, shape, scale=1.0):
+    return bf16_round(rng.standard_normal(shape).astype(np.float32) * np.float32(scale))

@@ -1,0 +1,69 @@
+"""The C-ABI library builds, loads and exports every function include/dfl.h declares.
+
+No compute call is made here: these run without a GPU.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import block_diffusion_speculative_dfl_gb300 as dfl
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "dfl.h")
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(dfl_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_six_path_calls():
+    names = _declared()
+    for n in ("dfl_layer_mix_rmsnorm", "dfl_dual_kv_proj", "dfl_block_attn", "dfl_lm_head_argmax",
+              "dfl_greedy_accept", "dfl_self_select"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol():
+    dfl.build()
+    lib = ctypes.CDLL(dfl.LIB)
+    names = _declared()
+    assert names, "no declarations parsed"
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, missing
+    assert sorted(dfl.EXPORTED) == names
+
+
+def test_host_only_calls_work_without_a_gpu():
+    lib = dfl.load()
+    assert dfl.version().startswith("dfl")
+    assert dfl.status_string(0) == "ok"
+    assert "workspace" in dfl.status_string(4)
+    # workspace sizes are pure host arithmetic
+    ws = dfl.workspace_size(dfl.DFL_OP_LM_HEAD, N=2, B=16, row0=1, d=256, V=1000, dtype=dfl.DFL_BF16)
+    assert ws >= 2 * 15 * 256 * 2
+    assert dfl.workspace_size(dfl.DFL_OP_LM_HEAD, N=2, B=16, row0=16, d=256, V=1000, dtype=1) == 0
+    assert lib.dfl_set_wait_limit_ns(0) == 1   # invalid argument, checked on the host
+
+
+def test_invalid_arguments_rejected_before_any_launch():
+    # Host-side checks return a status without touching a device.
+    lib = dfl.load()
+    assert lib.dfl_greedy_accept(None, None, 1, 4, None, None, None) == 1
+    assert lib.dfl_layer_mix_rmsnorm(None, 0, 9, 16, 64, 1, 7, None, None, 1e-6, None, 0, None) == 1
+    sp = dfl._lib.SampleParams(0, 1.5, 1)
+    assert lib.dfl_lm_head_argmax(16, 1, 16, 1, 64, 1, 16, 1e-6, 16, 100, 16, 16, ctypes.byref(sp), 16, 16,
+                                  1 << 20, None) == 1   # K = 0 is invalid
+    # misaligned pointer (not a multiple of 16) is refused on the host
+    assert lib.dfl_self_select(8, 1, 16, 1, 2, 3, 100, 16, 16, 16, 16, 16, 1 << 20, None) == 3
+
+
+@pytest.mark.parametrize("dt", [0, 1])
+def test_step_workspace_grows_with_layers(dt):
+    a = dfl.workspace_size(dfl.DFL_OP_DRAFT_STEP, N=1, C=64, B=16, d=256, Hq=4, Hkv=4, hd=64, D=1, L=3, V=1000,
+                           K=0, G=15, row0=1, dtype=dt)
+    b = dfl.workspace_size(dfl.DFL_OP_DRAFT_STEP, N=1, C=64, B=16, d=256, Hq=4, Hkv=4, hd=64, D=2, L=3, V=1000,
+                           K=0, G=15, row0=1, dtype=dt)
+    assert b - a >= 64 * 256 * (2 if dt else 4)

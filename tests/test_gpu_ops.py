@@ -1,0 +1,355 @@
+"""Per-operation parity of the CUDA path against the fp64 oracle (GPU).
+
+Sizes span several tiles with ragged tails; every call goes through the C ABI.
+"""
+import numpy as np
+import pytest
+import torch
+
+import block_diffusion_speculative_dfl_gb300 as dfl
+import oracle as orc
+from gpu_util import assert_bf16_close, assert_f32_close, dev, host, rng_bf16
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    dfl.build()
+    dfl.load()
+    torch.cuda.set_device(0)
+    yield
+    assert dfl.dfl_get_device_error() == 0
+
+
+def _ws(nbytes):
+    return torch.empty(max(nbytes, 256), dtype=torch.uint8, device="cuda")
+
+
+# ------------------------------------------------------------------- mix --
+
+@pytest.mark.parametrize("rows,d,L,D", [(300, 512, 9, 7), (200, 2880, 7, 8), (5, 4096, 9, 1), (149, 256, 3, 2)])
+def test_mix_rmsnorm_bf16(rows, d, L, D):
+    rng = np.random.default_rng(rows + d)
+    H = rng_bf16(rng, (L, rows, d)) * rng.uniform(0.5, 2, (L, 1, 1)).astype(np.float32)
+    from dfl_synth import round_bf16
+    H = round_bf16(H)
+    mix = rng.standard_normal((D, L)).astype(np.float32)
+    gain = rng.uniform(0.5, 1.5, (D, d)).astype(np.float32)
+    Xc = torch.empty((D, rows, d), dtype=torch.bfloat16, device="cuda")
+    dfl.dfl_layer_mix_rmsnorm(dev(H, "bf16"), rows * d, L, rows, d, dfl.DFL_BF16, D, dev(mix), dev(gain), 1e-6,
+                              Xc, rows * d)
+    got = host(Xc)
+    for l in range(D):
+        ref = orc.mix_rmsnorm(H, mix[l], gain[l], 1e-6)
+        assert_bf16_close(got[l], ref, f"Xc[{l}]")
+
+
+def test_mix_rmsnorm_f32():
+    rng = np.random.default_rng(3)
+    rows, d, L, D = 37, 256, 3, 2
+    H = rng.standard_normal((L, rows, d)).astype(np.float32)
+    mix = rng.standard_normal((D, L)).astype(np.float32)
+    gain = rng.uniform(0.5, 1.5, (D, d)).astype(np.float32)
+    Xc = torch.empty((D, rows, d), dtype=torch.float32, device="cuda")
+    dfl.dfl_layer_mix_rmsnorm(dev(H), rows * d, L, rows, d, dfl.DFL_F32, D, dev(mix), dev(gain), 1e-6, Xc,
+                              rows * d)
+    got = host(Xc)
+    for l in range(D):
+        assert_f32_close(got[l], orc.mix_rmsnorm(H, mix[l], gain[l], 1e-6), f"Xc[{l}]")
+
+
+# --------------------------------------------------------- dual projection --
+
+def _proj_case(N, C, B, d, Hq, Hkv, hd, dtype, seed):
+    rng = np.random.default_rng(seed)
+    mk = (lambda s, sc=1.0: rng_bf16(rng, s, sc)) if dtype == "bf16" else \
+        (lambda s, sc=1.0: (rng.standard_normal(s) * sc).astype(np.float32))
+    W = {"Wq": mk((Hq * hd, d), d ** -0.5), "Wkc": mk((Hkv * hd, d), d ** -0.5), "Wvc": mk((Hkv * hd, d), d ** -0.5),
+         "Wkb": mk((Hkv * hd, d), d ** -0.5), "Wvb": mk((Hkv * hd, d), d ** -0.5)}
+    return dict(Xc=mk((N * C, d)), Xb=rng.standard_normal((N * B, d)).astype(np.float32),
+                g=rng.uniform(0.5, 1.5, d).astype(np.float32), W=W)
+
+
+def _proj_ref(c, N, C, B, Hq, Hkv, hd, rope, theta=1e6):
+    d = c["Xb"].shape[1]
+    Xn = orc.rmsnorm(c["Xb"], c["g"], 1e-6)
+    W = {k: v.astype(np.float64) for k, v in c["W"].items()}
+    Q = (Xn @ W["Wq"].T).reshape(N, B, Hq, hd)
+    Kb = (Xn @ W["Wkb"].T).reshape(N, B, Hkv, hd)
+    Vb = (Xn @ W["Wvb"].T).reshape(N, B, Hkv, hd)
+    Xc = c["Xc"].astype(np.float64)
+    Kc = (Xc @ W["Wkc"].T).reshape(N, C, Hkv, hd)
+    Vc = (Xc @ W["Wvc"].T).reshape(N, C, Hkv, hd)
+    if rope:
+        cos, sin = orc.rope_cos_sin(np.arange(C + B), hd, theta)
+        for n in range(N):
+            Q[n] = orc.apply_rope(Q[n], cos[C:], sin[C:])
+            Kb[n] = orc.apply_rope(Kb[n], cos[C:], sin[C:])
+            Kc[n] = orc.apply_rope(Kc[n], cos[:C], sin[:C])
+    return {"Q": Q, "Kb": Kb, "Vb": Vb, "Kc": Kc, "Vc": Vc}
+
+
+@pytest.mark.parametrize("N,C,B,d,Hq,Hkv,hd,rope", [
+    (2, 200, 16, 512, 8, 2, 128, True),    # ctx BN=256, ragged M (400 rows)
+    (2, 200, 16, 520, 8, 2, 128, False),   # K tail (520 = 8 * 65), no rotary
+    (3, 150, 8, 256, 16, 2, 64, True),     # hd 64: ctx BN=128, GQA group 8
+    (1, 64, 33, 256, 4, 2, 128, True),     # 33-row block (anchor + 32 masks)
+])
+def test_dual_kv_proj_bf16(N, C, B, d, Hq, Hkv, hd, rope):
+    c = _proj_case(N, C, B, d, Hq, Hkv, hd, "bf16", seed=N * 1000 + C + d)
+    kv, qd = Hkv * hd, Hq * hd
+    out = {k: torch.empty(s, dtype=torch.bfloat16, device="cuda") for k, s in
+           {"Q": (N * B, qd), "Kc": (N * C, kv), "Vc": (N * C, kv), "Kb": (N * B, kv), "Vb": (N * B, kv)}.items()}
+    table = None
+    if rope:
+        table = torch.empty((C + B, hd // 2, 2), dtype=torch.float32, device="cuda")
+        dfl.dfl_rope_table(table, C + B, hd, 1e6)
+    wsb = dfl.workspace_size(dfl.DFL_OP_DUAL_KV_PROJ, N=N, B=B, d=d, dtype=dfl.DFL_BF16)
+    ws = _ws(wsb)
+    Wd = {k: dev(v, "bf16") for k, v in c["W"].items()}
+    dfl.dfl_dual_kv_proj(dev(c["Xc"], "bf16"), dev(c["Xb"]), N, C, B, d, dfl.DFL_BF16, dev(c["g"]), 1e-6,
+                         Wd["Wq"], Wd["Wkc"], Wd["Wvc"], Wd["Wkb"], Wd["Wvb"], Hq, Hkv, hd, table,
+                         out["Q"], out["Kc"], out["Vc"], out["Kb"], out["Vb"], ws, wsb)
+    ref = _proj_ref(c, N, C, B, Hq, Hkv, hd, rope)
+    for k in ("Q", "Kb", "Vb", "Kc", "Vc"):
+        assert_bf16_close(host(out[k]).reshape(ref[k].shape), ref[k], k)
+
+
+def test_dual_kv_proj_f32():
+    N, C, B, d, Hq, Hkv, hd = 1, 64, 16, 256, 4, 4, 64
+    c = _proj_case(N, C, B, d, Hq, Hkv, hd, "f32", seed=5)
+    kv, qd = Hkv * hd, Hq * hd
+    out = {k: torch.empty(s, dtype=torch.float32, device="cuda") for k, s in
+           {"Q": (N * B, qd), "Kc": (N * C, kv), "Vc": (N * C, kv), "Kb": (N * B, kv), "Vb": (N * B, kv)}.items()}
+    table = torch.empty((C + B, hd // 2, 2), dtype=torch.float32, device="cuda")
+    dfl.dfl_rope_table(table, C + B, hd, 1e6)
+    wsb = dfl.workspace_size(dfl.DFL_OP_DUAL_KV_PROJ, N=N, B=B, d=d, dtype=dfl.DFL_F32)
+    ws = _ws(wsb)
+    Wd = {k: dev(v) for k, v in c["W"].items()}
+    dfl.dfl_dual_kv_proj(dev(c["Xc"]), dev(c["Xb"]), N, C, B, d, dfl.DFL_F32, dev(c["g"]), 1e-6, Wd["Wq"],
+                         Wd["Wkc"], Wd["Wvc"], Wd["Wkb"], Wd["Wvb"], Hq, Hkv, hd, table, out["Q"], out["Kc"],
+                         out["Vc"], out["Kb"], out["Vb"], ws, wsb)
+    ref = _proj_ref(c, N, C, B, Hq, Hkv, hd, True)
+    for k in ("Q", "Kb", "Vb", "Kc", "Vc"):
+        assert_f32_close(host(out[k]).reshape(ref[k].shape), ref[k], k)
+
+
+def test_rope_table_matches_oracle():
+    P, hd = 300, 128
+    t = torch.empty((P, hd // 2, 2), dtype=torch.float32, device="cuda")
+    dfl.dfl_rope_table(t, P, hd, 1e6)
+    cos, sin = orc.rope_cos_sin(np.arange(P), hd, 1e6)
+    g = host(t)
+    assert np.max(np.abs(g[..., 0] - cos)) < 1e-7 and np.max(np.abs(g[..., 1] - sin)) < 1e-7
+
+
+# ------------------------------------------------------------- attention --
+
+@pytest.mark.parametrize("N,C,B,Hq,Hkv,hd,d", [
+    (2, 200, 16, 8, 2, 128, 512),     # 4 units -> several key splits, ragged last tile
+    (40, 48, 16, 16, 8, 128, 256),    # 320 units -> one split, keys < one tile + block
+    (2, 130, 8, 16, 2, 64, 320),      # hd 64, GQA group 8
+    (1, 100, 33, 16, 4, 128, 256),    # 132 query rows per unit (9 warps)
+    (1, 70, 64, 32, 2, 64, 256),      # 1024 query rows per unit -> rows split over CTAs
+])
+def test_block_attn_bf16(N, C, B, Hq, Hkv, hd, d):
+    rng = np.random.default_rng(N * 7 + C)
+    Q = rng_bf16(rng, (N * B, Hq, hd))
+    Kc, Vc = rng_bf16(rng, (N * C, Hkv, hd)), rng_bf16(rng, (N * C, Hkv, hd))
+    Kb, Vb = rng_bf16(rng, (N * B, Hkv, hd)), rng_bf16(rng, (N * B, Hkv, hd))
+    Wo = rng_bf16(rng, (d, Hq * hd), (Hq * hd) ** -0.5)
+    Xb = rng.standard_normal((N * B, d)).astype(np.float32)
+    Xb_d = dev(Xb)
+    wsb = dfl.workspace_size(dfl.DFL_OP_BLOCK_ATTN, N=N, C=C, B=B, Hq=Hq, Hkv=Hkv, hd=hd, dtype=dfl.DFL_BF16)
+    ws = _ws(wsb)
+    dfl.dfl_block_attn(dev(Q, "bf16"), dev(Kc, "bf16"), dev(Vc, "bf16"), dev(Kb, "bf16"), dev(Vb, "bf16"), N, C, B,
+                       Hq, Hkv, hd, dfl.DFL_BF16, dev(Wo, "bf16"), d, Xb_d, ws, wsb)
+    ref = np.empty((N * B, d))
+    for n in range(N):
+        K = np.concatenate([Kc[n * C:(n + 1) * C], Kb[n * B:(n + 1) * B]])
+        V = np.concatenate([Vc[n * C:(n + 1) * C], Vb[n * B:(n + 1) * B]])
+        O = orc.attention(Q[n * B:(n + 1) * B], K, V, orc.block_visibility(C, B))
+        ref[n * B:(n + 1) * B] = Xb[n * B:(n + 1) * B] + O.reshape(B, Hq * hd) @ Wo.astype(np.float64).T
+    got = host(Xb_d)
+    assert_bf16_close(got - Xb, ref - Xb, "O Wo^T")
+
+
+def test_block_attn_f32():
+    N, C, B, Hq, Hkv, hd, d = 1, 64, 16, 4, 4, 64, 256
+    rng = np.random.default_rng(11)
+    f = lambda s, sc=1.0: (rng.standard_normal(s) * sc).astype(np.float32)
+    Q, Kc, Vc, Kb, Vb = f((B, Hq, hd)), f((C, Hkv, hd)), f((C, Hkv, hd)), f((B, Hkv, hd)), f((B, Hkv, hd))
+    Wo, Xb = f((d, Hq * hd), (Hq * hd) ** -0.5), f((B, d))
+    Xb_d = dev(Xb)
+    wsb = dfl.workspace_size(dfl.DFL_OP_BLOCK_ATTN, N=N, C=C, B=B, Hq=Hq, Hkv=Hkv, hd=hd, dtype=dfl.DFL_F32)
+    ws = _ws(wsb)
+    dfl.dfl_block_attn(dev(Q), dev(Kc), dev(Vc), dev(Kb), dev(Vb), N, C, B, Hq, Hkv, hd, dfl.DFL_F32, dev(Wo), d,
+                       Xb_d, ws, wsb)
+    O = orc.attention(Q, np.concatenate([Kc, Kb]), np.concatenate([Vc, Vb]), orc.block_visibility(C, B))
+    assert_f32_close(host(Xb_d), Xb + O.reshape(B, -1) @ Wo.astype(np.float64).T, "Xb")
+
+
+# --------------------------------------------------------------- LM head --
+
+def _lm_case(N, B, d, V, seed, dtype="bf16"):
+    rng = np.random.default_rng(seed)
+    X = rng.standard_normal((N, B, d)).astype(np.float32)
+    g = rng.uniform(0.5, 1.5, d).astype(np.float32)
+    W = rng_bf16(rng, (V, d), d ** -0.5) if dtype == "bf16" else \
+        (rng.standard_normal((V, d)) * d ** -0.5).astype(np.float32)
+    return X, g, W
+
+
+@pytest.mark.parametrize("N,B,row0,d,V", [(3, 16, 1, 512, 1000), (2, 9, 1, 256, 5003), (1, 16, 0, 256, 256)])
+def test_lm_head_argmax_bf16(N, B, row0, d, V):
+    X, g, W = _lm_case(N, B, d, V, seed=V)
+    nr = B - row0
+    am = torch.empty((N, nr), dtype=torch.int32, device="cuda")
+    lg = torch.empty((N * nr, V), dtype=torch.float32, device="cuda")
+    wsb = dfl.workspace_size(dfl.DFL_OP_LM_HEAD, N=N, B=B, row0=row0, d=d, V=V, dtype=dfl.DFL_BF16)
+    ws = _ws(wsb)
+    dfl.dfl_lm_head_argmax(dev(X), N, B, row0, d, dfl.DFL_BF16, dev(g), 1e-6, dev(W, "bf16"), V, am, lg, None, None,
+                           ws, wsb)
+    z = host(lg)
+    ref = orc.lm_head_logits(X[:, row0:].reshape(-1, d), g, 1e-6, W)
+    assert_bf16_close(z, ref, "logits")
+    # argmax is bit-exact against the oracle's argmax of the same fp32 buffer
+    assert np.array_equal(host(am).reshape(-1), orc.argmax_lowest(z))
+
+
+def test_lm_head_argmax_ties_take_lowest_index():
+    N, B, d, V = 1, 4, 256, 1000
+    rng = np.random.default_rng(21)
+    x = rng.standard_normal(d).astype(np.float32)
+    X = np.broadcast_to(x, (N, B, d)).copy()
+    g = np.ones(d, np.float32)
+    W = rng_bf16(rng, (V, d), 1e-3)
+    from dfl_synth import round_bf16
+    u = round_bf16(x / np.linalg.norm(x) * 4)
+    for v in (300, 301, 900):         # tie inside a 256-column tile and across tiles
+        W[v] = u
+    am = torch.empty((N, B), dtype=torch.int32, device="cuda")
+    lg = torch.empty((N * B, V), dtype=torch.float32, device="cuda")
+    wsb = dfl.workspace_size(dfl.DFL_OP_LM_HEAD, N=N, B=B, row0=0, d=d, V=V, dtype=dfl.DFL_BF16)
+    ws = _ws(wsb)
+    dfl.dfl_lm_head_argmax(dev(X), N, B, 0, d, dfl.DFL_BF16, dev(g), 1e-6, dev(W, "bf16"), V, am, lg, None, None,
+                           ws, wsb)
+    z = host(lg)
+    assert np.all(z[:, 300] == z[:, 900]) and np.all(z[:, 300] == z[:, 301])
+    assert np.all(host(am) == 300)
+    # all-zero head: every logit ties at 0 -> index 0
+    dfl.dfl_lm_head_argmax(dev(X), N, B, 0, d, dfl.DFL_BF16, dev(g), 1e-6, dev(np.zeros((V, d), np.float32), "bf16"),
+                           V, am, None, None, None, ws, wsb)
+    assert np.all(host(am) == 0)
+
+
+def _check_samples(samples, z, seed, K, T, per):
+    """Samples equal the oracle's inverse-CDF draws on the same logits, except
+    within 1e-6 of a CDF boundary, where the neighbour is also correct."""
+    M, V = z.shape
+    near = 0
+    for m in range(M):
+        n, j = divmod(m, per)
+        for k in range(K):
+            u = orc.draw_uniform(seed, n, j, k)
+            v, margin = orc.sample_inverse_cdf(z[m], T, u)
+            s = int(samples[n, k, j])
+            if margin >= 1e-6:
+                assert s == v, (m, k, s, v, margin)
+            else:
+                near += 1
+                assert abs(s - v) <= 1, (m, k, s, v, margin)
+    return near
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_lm_head_sampling(dtype):
+    N, B, d, V, K, T, seed = 2, 9, 256, 1000, 8, 1.5, 0x5EEDD1F5
+    X, g, W = _lm_case(N, B, d, V, seed=77, dtype=dtype)
+    dt = dfl.DFL_BF16 if dtype == "bf16" else dfl.DFL_F32
+    nr = B - 1
+    am = torch.empty((N, nr), dtype=torch.int32, device="cuda")
+    lg = torch.empty((N * nr, V), dtype=torch.float32, device="cuda")
+    sm = torch.empty((N, K, nr), dtype=torch.int32, device="cuda")
+    wsb = dfl.workspace_size(dfl.DFL_OP_LM_HEAD, N=N, B=B, row0=1, d=d, V=V, dtype=dt)
+    ws = _ws(wsb)
+    dfl.dfl_lm_head_argmax(dev(X), N, B, 1, d, dt, dev(g), 1e-6, dev(W, dtype if dtype == "bf16" else None), V, am,
+                           lg, (K, T, seed), sm, ws, wsb)
+    z = host(lg)
+    near = _check_samples(host(sm), z, seed, K, T, nr)
+    assert near <= 3
+    assert np.array_equal(host(am).reshape(-1), orc.argmax_lowest(z))
+
+
+# ------------------------------------------------------------- acceptance --
+
+def _golden_greedy():
+    import os
+    rows = []
+    with open(os.path.join(os.path.dirname(__file__), "golden", "greedy_cases.txt")) as f:
+        for line in f:
+            if line.strip() and not line.startswith("#"):
+                d_, t_, a_, b_ = [p.split() for p in line.split("|")]
+                rows.append(([int(x) for x in d_], [int(x) for x in t_], int(a_[0]), int(b_[0])))
+    return rows
+
+
+def test_greedy_accept_golden_and_planted():
+    for d_, t_, a_, b_ in _golden_greedy():
+        n = len(d_)
+        al = torch.empty(1, dtype=torch.int32, device="cuda")
+        bo = torch.empty(1, dtype=torch.int32, device="cuda")
+        dfl.dfl_greedy_accept(dev(np.array([d_], np.int32)), dev(np.array([t_], np.int32)), 1, n, al, bo)
+        assert (int(al.item()), int(bo.item())) == (a_, b_)
+    from dfl_synth import Workload, geometric_prefix, plant_targets
+    w = Workload("p", N=500, d=1, Hq=1, Hkv=1, hd=2, D=1, L=1, B=40, C=1, V=50, dtype="f32", seed=9, geom_p=0.1)
+    rng = np.random.default_rng(2)
+    drafts = rng.integers(0, w.V, (w.N, w.B - 1)).astype(np.int32)
+    t = plant_targets(w, drafts)
+    al = torch.empty(w.N, dtype=torch.int32, device="cuda")
+    bo = torch.empty(w.N, dtype=torch.int32, device="cuda")
+    dfl.dfl_greedy_accept(dev(drafts), dev(t), w.N, w.B - 1, al, bo)
+    G = geometric_prefix(w)
+    assert np.array_equal(host(al), G)
+    assert np.array_equal(host(bo), t[np.arange(w.N), G])
+
+
+@pytest.mark.parametrize("N,K,G,V", [(3, 4, 5, 1000), (2, 8, 32, 2048), (1, 64, 1, 96), (2, 3, 40, 1001)])
+def test_self_select(N, K, G, V):
+    rng = np.random.default_rng(N * K + G)
+    vlog = rng_bf16(rng, (N, K, G + 1, V), 4.0)
+    drafts = rng.integers(0, V, (N, K, G)).astype(np.int32)
+    # make some drafts follow the verifier's argmax for a while, so acceptance is non-trivial
+    for n in range(N):
+        for k in range(K):
+            p = rng.integers(0, G + 1)
+            drafts[n, k, :p] = np.argmax(vlog[n, k, :p], axis=-1)
+    sc = torch.empty((N, K), dtype=torch.float32, device="cuda")
+    se, al, bo = (torch.empty(N, dtype=torch.int32, device="cuda") for _ in range(3))
+    wsb = dfl.workspace_size(dfl.DFL_OP_SELF_SELECT, N=N, K=K, G=G)
+    ws = _ws(wsb)
+    dfl.dfl_self_select(dev(vlog, "bf16"), dfl.DFL_BF16, dev(drafts), N, K, G, V, sc, se, al, bo, ws, wsb)
+    for n in range(N):
+        scores, ks, a, b = orc.self_select(vlog[n], drafts[n])
+        g_sc = host(sc)[n]
+        assert np.allclose(g_sc, scores, rtol=1e-4, atol=0), (g_sc, scores)
+        top = np.sort(scores)[::-1]
+        k_gpu = int(host(se)[n])
+        if K > 1 and (top[0] - top[1]) <= 1e-5 * top[0]:
+            assert scores[k_gpu] >= top[1]      # near-tie: either top draft is correct
+        else:
+            assert k_gpu == ks
+        t = [int(np.argmax(vlog[n, k_gpu, j])) for j in range(G + 1)]
+        assert (int(host(al)[n]), int(host(bo)[n])) == orc.greedy_accept(drafts[n, k_gpu], t)
+
+
+def test_bounded_wait_times_out_and_context_survives():
+    st = torch.empty(1, dtype=torch.int32, device="cuda")
+    dfl.dfl_selftest_bounded_wait(20_000_000, st)   # 20 ms on a barrier nothing arrives at
+    torch.cuda.synchronize()
+    assert int(st.item()) == 6                       # DFL_ERR_TIMEOUT
+    al = torch.empty(1, dtype=torch.int32, device="cuda")
+    bo = torch.empty(1, dtype=torch.int32, device="cuda")
+    dfl.dfl_greedy_accept(dev(np.array([[1, 2]], np.int32)), dev(np.array([[1, 5, 7]], np.int32)), 1, 2, al, bo)
+    assert (int(al.item()), int(bo.item())) == (1, 5)
