@@ -1,0 +1,420 @@
+#!/usr/bin/env python
+"""Throughput of the block-diffusion draft step on GB300, one JSON line.
+
+A step is one pass of the whole hot path over one batch of synthetic input:
+the L-way mix + RMSNorm of every draft layer, D draft layers (dual-source
+projections, block attention, output projection), the LM head with argmax
+and the acceptance epilogue (greedy, or K-draft sampling + streak-score
+self-selection).  value = drafted block-tokens (N * B per step, all ranks)
+per second of device time.
+
+  python bench.py [--workload qwen3_8b_drafter] [--steps K] [--warmup W]
+  python bench.py --impl reference      # the fp64 CPU oracle on the same workload
+  torchrun --nproc-per-node N bench.py --gpus N   # one replica per GPU (weak scaling)
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "drafted block-tokens/sec on 1 GB300 (+accept epilogue); % of HBM/tensor roofline"
+UNIT = "block-tokens/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 256 << 20
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default="qwen3_8b_drafter")
+    p.add_argument("--e2e-steps", type=int, default=3)
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args(argv)
+
+
+# ------------------------------------------------------------------ ranks --
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def dist_init(world, backend):
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def reduce_scalar(x: float, world: int, op: str, device=None) -> float:
+    """MAX or SUM of a host scalar over ranks (identity on one rank)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX if op == "max" else dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def aggregate(units_per_rank: float, seconds_max: float, world: int) -> float:
+    """Whole-job throughput: units all ranks processed / slowest rank's time."""
+    return units_per_rank * world / seconds_max
+
+
+# ---------------------------------------------------------------- helpers --
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_hash(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "block_diffusion_speculative_dfl_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+# kernel trace name -> source files its code lives in (for the traffic record)
+KERNEL_SOURCES = {
+    "gemm_ctx_kv": ["gemm_tc.cuh", "gemm_tc.cu"], "gemm_block_qkv": ["gemm_tc.cuh", "gemm_tc.cu"],
+    "gemm_o_proj": ["gemm_tc.cuh", "gemm_tc.cu"], "gemm_lm_head": ["gemm_tc.cuh", "gemm_tc.cu"],
+    "mix_rmsnorm_bf16": ["mix_rmsnorm.cu"], "attn_bf16": ["block_attn.cu"],
+    "verifier_row_stats": ["self_select.cu"],
+}
+
+
+def ncu_traffic(kernel, workload):
+    """DRAM bytes per launch from profiles/ncu_traffic.txt, if taken on the current source."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+    if not os.path.exists(path) or kernel not in KERNEL_SOURCES:
+        return None
+    cur = source_hash(KERNEL_SOURCES[kernel])
+    with open(path) as f:
+        for line in f:
+            parts = line.split()
+            if len(parts) >= 4 and not line.startswith("#") and parts[0] == kernel and parts[1] == workload:
+                return float(parts[2]) if parts[3] == cur else None
+    return None
+
+
+def kernel_work(w):
+    """Algorithmic work per launch: {kernel: (flops, bytes)} (bf16 operands, 2 B)."""
+    N, C, B, d, Hq, Hkv, hd, D, L, V = w.N, w.C, w.B, w.d, w.Hq, w.Hkv, w.hd, w.D, w.L, w.V
+    kv, qd = Hkv * hd, Hq * hd
+    rows_c, rows_b = N * C, N * B
+    work = {
+        "mix_rmsnorm_bf16": (2.0 * D * L * rows_c * d, 2.0 * (L + D) * rows_c * d),
+        "gemm_ctx_kv": (2.0 * rows_c * 2 * kv * d, 2.0 * (rows_c * d + 2 * kv * d + rows_c * 2 * kv)),
+        "gemm_block_qkv": (2.0 * rows_b * (qd + 2 * kv) * d,
+                           2.0 * (rows_b * d + (qd + 2 * kv) * d + rows_b * (qd + 2 * kv))),
+        "attn_bf16": (4.0 * rows_b * Hq * (C + B) * hd,
+                      2.0 * (2 * N * (C + B) * kv + 2 * rows_b * qd)),
+        "gemm_o_proj": (2.0 * rows_b * d * qd, 2.0 * (rows_b * qd + d * qd) + 8.0 * rows_b * d),
+    }
+    if V > 0:
+        M = N * (B - 1)
+        work["gemm_lm_head"] = (2.0 * M * V * d, 2.0 * (M * d + V * d) + (4.0 * M * V if w.K > 0 else 0.0))
+    if w.K > 0:
+        work["verifier_row_stats"] = (0.0, 2.0 * N * w.K * B * V)
+    return work
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 200 ms."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200",
+                 "-i", str(gpu_index)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower() in ("active", "1"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# -------------------------------------------------------------- workloads --
+
+def workload(name, rank=0):
+    import dataclasses
+    from dfl_synth import WORKLOADS
+    w = WORKLOADS[name]
+    if rank:   # every rank drafts its own batch of sequences (weak scaling)
+        w = dataclasses.replace(w, seed=w.seed + 1000 * rank)
+    return w
+
+
+def host_params(w):
+    from dfl_synth import gen_gains, gen_layer_weights, gen_lm_head, gen_mix_logits
+    g_mix, g_blk, g_fin = gen_gains(w)
+    return {"mix": gen_mix_logits(w), "g_mix": g_mix, "g_blk": g_blk, "g_fin": g_fin,
+            "layers": [gen_layer_weights(w, l) for l in range(w.D)],
+            "W_lm_bits": gen_lm_head(w, as_bits=True) if w.V > 0 else None}
+
+
+def oracle_step(w, p, n, W_lm_f32, vlog_n=None):
+    """The fp64 oracle's draft step for sequence n (test infrastructure, CPU)."""
+    import oracle as orc
+    from dfl_synth import gen_block_init, gen_hidden, plant_targets  # noqa: F401
+    Hn = gen_hidden(w, seqs=[n])
+    Xb0 = gen_block_init(w)[n]
+    t0 = time.perf_counter()
+    out = orc.draft_forward(Xb0, Hn, p["mix"], p["g_mix"], p["g_blk"], p["layers"],
+                            {"Hq": w.Hq, "Hkv": w.Hkv, "hd": w.hd}, w.eps, w.rope_theta)
+    if w.V > 0:
+        z = orc.lm_head_logits(out["Xb"][1:], p["g_fin"], w.eps, W_lm_f32)
+        drafts = orc.argmax_lowest(z)
+        if w.K > 0:
+            samples = np.array([[orc.sample_inverse_cdf(z[j], w.T, orc.draw_uniform(w.philox_seed, n, j, k))[0]
+                                 for j in range(w.gamma)] for k in range(w.K)])
+            orc.self_select(vlog_n, samples)
+        else:
+            orc.greedy_accept(drafts, np.concatenate([drafts, [0]]))
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(w, p, seqs):
+    from dfl_synth import bits_to_f32, gen_verifier_logits
+    W_lm = bits_to_f32(p["W_lm_bits"]) if w.V > 0 else None
+    total = 0.0
+    for n in seqs:
+        vl = gen_verifier_logits(w, seqs=[n])[0] if w.K > 0 else None
+        total += oracle_step(w, p, n, W_lm, vl)
+    return total
+
+
+def describe_sample(w, seqs):
+    parts = "all D draft layers, LM head and " + ("K-draft sampling + self-selection" if w.K > 0 else
+                                                  "greedy acceptance" if w.V > 0 else "no head")
+    return f"{len(seqs)} of {w.N} sequences of {w.name} ({parts}), fp64 NumPy"
+
+
+# -------------------------------------------------------------- our arm --
+
+def run_ours(args, rank, world, local):
+    import torch
+
+    import block_diffusion_speculative_dfl_gb300 as dfl
+    from dfl_synth import gen_block_init, gen_hidden, gen_verifier_logits, plant_targets
+
+    torch.cuda.set_device(local)
+    dist_init(world, "nccl")
+    dfl.build()
+    dfl.load()
+    w = workload(args.workload, rank)
+    p = host_params(w)
+    shape = dfl.DraftShape(N=w.N, d=w.d, Hq=w.Hq, Hkv=w.Hkv, hd=w.hd, D=w.D, L=w.L, B=w.B, C=w.C, V=w.V,
+                           dtype=w.dtype, K=w.K, T=w.T, seed=w.philox_seed, eps=w.eps, rope_theta=w.rope_theta)
+    W_lm = (torch.from_numpy(p["W_lm_bits"].view(np.int16)).view(torch.bfloat16) if w.V > 0 else None)
+    model = dfl.DraftModel(shape, p["mix"], p["g_mix"], p["g_blk"], p["g_fin"], p["layers"], W_lm)
+    H_host = torch.from_numpy(gen_hidden(w, as_bits=True).view(np.int16)).view(torch.bfloat16)
+    X_host = torch.from_numpy(gen_block_init(w))
+    H, X0 = H_host.cuda(), X_host.cuda()
+    vlog_host = vlog = None
+    if w.K > 0:
+        vlog_host = torch.from_numpy(gen_verifier_logits(w, as_bits=True).view(np.int16)).view(torch.bfloat16)
+        vlog = vlog_host.cuda()
+    target_host = target = None
+    if w.V > 0 and w.K == 0:   # plant the target's argmax against this step's drafts
+        model.step(H, X0)
+        torch.cuda.synchronize()
+        target_host = torch.from_numpy(plant_targets(w, model.draft.cpu().numpy()))
+        target = target_host.cuda()
+
+    def step():
+        model.step(H, X0, target=target, vlog=vlog)
+
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    for _ in range(max(args.warmup, 0)):
+        step()
+        flush.zero_()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    clocks = ClockSampler(torch.cuda.current_device())
+    time.sleep(0.3)
+    dfl.dfl_profile_enable(True)
+    barrier(world)
+    torch.cuda.synchronize()
+    for a, b in evs:
+        a.record()
+        step()
+        b.record()
+        flush.zero_()
+    torch.cuda.synchronize()
+    barrier(world)
+    dfl.dfl_profile_enable(False)
+    clk = clocks.stop()
+    prof, launches = dfl.dfl_profile_report()
+    err = dfl.dfl_get_device_error()
+    if err:
+        raise RuntimeError(f"device error {err} during the timed steps")
+    ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    ms_max = reduce_scalar(ms, world, "max", device="cuda")
+    units = w.N * w.B
+    value = aggregate(units, ms_max / 1e3, world)
+
+    # roofline of the dominant kernel (largest share of traced time)
+    peaks, peak_src = load_peaks()
+    work = kernel_work(w)
+    traced = sum(t for _, t in prof.values())
+    kernels = {}
+    for name, (n_l, tot) in sorted(prof.items(), key=lambda kv: -kv[1][1]):
+        per = tot / n_l
+        ent = {"launches": n_l, "ms_per_launch": round(per, 5), "share": round(tot / traced, 4)}
+        if name in work:
+            fl, by = work[name]
+            tensor = fl / (peaks["bf16_tflops_sustained"] * 1e12) >= by / (peaks["hbm_gbs"] * 1e9)
+            ent["bound"] = "tensor" if tensor else "hbm"
+            ent["achieved"] = round(fl / (per / 1e3) / 1e12, 2) if tensor else round(by / (per / 1e3) / 1e9, 1)
+            ent["frac"] = round(ent["achieved"] / (peaks["bf16_tflops_sustained"] if tensor else peaks["hbm_gbs"]),
+                                4)
+        kernels[name] = ent
+    dom = next(k for k in kernels if k in work)
+    de = kernels[dom]
+    roofline = {"kernel": dom, "bound": de["bound"], "achieved": de["achieved"],
+                "peak": peaks["bf16_tflops_sustained"] if de["bound"] == "tensor" else peaks["hbm_gbs"],
+                "unit": "TFLOP/s" if de["bound"] == "tensor" else "GB/s", "frac": de["frac"],
+                "traffic": ncu_traffic(dom, w.name),
+                "peak_source": f"{peak_src} ({'bf16 dense sustained' if de['bound'] == 'tensor' else 'HBM copy'})",
+                "algorithmic_per_launch": work[dom][0] if de["bound"] == "tensor" else work[dom][1]}
+
+    # end to end through the public API: pinned host inputs in, results out
+    e2e = None
+    if not args.no_e2e and args.e2e_steps > 0:
+        H_pin, X_pin = H_host.pin_memory(), X_host.pin_memory()
+        t_pin = target_host.pin_memory() if target_host is not None else None
+        v_pin = vlog_host.pin_memory() if vlog_host is not None else None
+        dev_in = {}
+        out, dev_in = model.step_from_host(H_pin, X_pin, t_pin, v_pin, dev_in)   # allocate device buffers
+        times = []
+        for _ in range(args.e2e_steps):
+            t0 = time.perf_counter()
+            out, dev_in = model.step_from_host(H_pin, X_pin, t_pin, v_pin, dev_in)
+            times.append(time.perf_counter() - t0)
+        e2e_s = reduce_scalar(statistics.mean(times), world, "max", device="cuda")
+        h2d = sum(t.numel() * t.element_size() for t in (H_pin, X_pin, t_pin, v_pin) if t is not None)
+        d2h = sum(t.numel() * t.element_size() for t in out.values())
+        e2e = {"value": round(aggregate(units, e2e_s, world), 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_s * 1e3, 3)}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        seqs = [0] if w.N > 1 else [0]
+        t_cpu = cpu_baseline(w, p, seqs)
+        cpu = {"value": round(len(seqs) * w.B / t_cpu, 3), "unit": UNIT, "cores": len(os.sched_getaffinity(0)),
+               "kind": "oracle", "sample": describe_sample(w, seqs), "seconds": round(t_cpu, 2)}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": round(ms_max, 4), "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32",
+                "data": "synthetic (seeded NumPy PCG64; shapes and distributions of the workload)",
+                "config": {"workload": w.name, "N_per_gpu": w.N, "d": w.d, "Hq": w.Hq, "Hkv": w.Hkv, "hd": w.hd,
+                           "draft_layers": w.D, "target_layers": w.L, "block": w.B, "context": w.C, "vocab": w.V,
+                           "K": w.K, "T": w.T, "parallelism": f"replicas x{world}",
+                           "l2": "inputs larger than L2 and a 256 MB L2 flush between timed steps"},
+                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
+                "clocks": clk, "kernels": kernels}
+        print(json.dumps(line), flush=True)
+    barrier(world)
+
+
+# -------------------------------------------------------- reference arm --
+
+def run_reference(args, rank, world):
+    """The fp64 CPU oracle on the same workload, one sequence per step."""
+    if rank != 0:
+        return
+    from dfl_synth import bits_to_f32, gen_verifier_logits
+    w = workload(args.workload)
+    p = host_params(w)
+    W_lm = bits_to_f32(p["W_lm_bits"]) if w.V > 0 else None
+    times = []
+    for i in range(args.warmup + args.steps):
+        n = i % w.N
+        vl = gen_verifier_logits(w, seqs=[n])[0] if w.K > 0 else None
+        t = oracle_step(w, p, n, W_lm, vl)
+        if i >= args.warmup:
+            times.append(t)
+    total = sum(times)
+    value = w.B * len(times) / total
+    cores = len(os.sched_getaffinity(0))
+    sample = f"one sequence of {w.name} per step (" + describe_sample(w, [0]).split("(", 1)[1]
+    line = {"metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(1e3 * total / len(times), 2), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "impl": "reference",
+            "data": "synthetic (seeded NumPy PCG64; shapes and distributions of the workload)",
+            "config": {"workload": w.name, "N": w.N, "B": w.B, "context": w.C, "draft_layers": w.D},
+            "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    run_ours(args, rank, world, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

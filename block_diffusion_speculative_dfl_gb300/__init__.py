@@ -10,7 +10,8 @@ from ._lib import (DflError, load, version, status_string, workspace_size, ptr, 
                    DFL_OP_SELF_SELECT, DFL_OP_DRAFT_STEP,
                    dfl_rope_table, dfl_layer_mix_rmsnorm, dfl_dual_kv_proj, dfl_block_attn,
                    dfl_lm_head_argmax, dfl_greedy_accept, dfl_self_select, dfl_draft_step,
-                   dfl_get_device_error, dfl_set_wait_limit_ns, dfl_selftest_bounded_wait)
+                   dfl_get_device_error, dfl_set_wait_limit_ns, dfl_selftest_bounded_wait,
+                   dfl_profile_enable, dfl_profile_report)
 from .step import DraftShape, DraftModel
 
 __all__ = [n for n in dir() if not n.startswith("_")]

@@ -20,7 +20,7 @@ DFL_OP_DUAL_KV_PROJ, DFL_OP_BLOCK_ATTN, DFL_OP_LM_HEAD, DFL_OP_SELF_SELECT, DFL_
 EXPORTED = ("dfl_version", "dfl_status_string", "dfl_workspace_size", "dfl_rope_table",
             "dfl_layer_mix_rmsnorm", "dfl_dual_kv_proj", "dfl_block_attn", "dfl_lm_head_argmax",
             "dfl_greedy_accept", "dfl_self_select", "dfl_draft_step", "dfl_get_device_error",
-            "dfl_set_wait_limit_ns", "dfl_selftest_bounded_wait")
+            "dfl_set_wait_limit_ns", "dfl_selftest_bounded_wait", "dfl_profile_enable", "dfl_profile_report")
 
 
 class DflError(RuntimeError):
@@ -72,6 +72,8 @@ _SIGS = {
     "dfl_get_device_error": ([_P, C.POINTER(_I32)], _I32),
     "dfl_set_wait_limit_ns": ([C.c_uint64], _I32),
     "dfl_selftest_bounded_wait": ([C.c_uint64, _P, _P], _I32),
+    "dfl_profile_enable": ([_I32], _I32),
+    "dfl_profile_report": ([C.c_char_p, _SZ, C.POINTER(_I32)], _I32),
 }
 
 _lib = None
@@ -194,3 +196,16 @@ def dfl_set_wait_limit_ns(ns: int):
 def dfl_selftest_bounded_wait(limit_ns, status_out, stream=None):
     _check("dfl_selftest_bounded_wait",
            load().dfl_selftest_bounded_wait(limit_ns, ptr(status_out), _stream(stream)))
+
+
+def dfl_profile_enable(on: bool = True):
+    _check("dfl_profile_enable", load().dfl_profile_enable(1 if on else 0))
+
+
+def dfl_profile_report() -> tuple[dict, int]:
+    """Per-kernel {name: (launches, total_ms)} since tracing was enabled, and the launch count."""
+    import json
+    buf = C.create_string_buffer(1 << 16)
+    n = _I32(0)
+    _check("dfl_profile_report", load().dfl_profile_report(buf, len(buf), C.byref(n)))
+    return {k: (int(v[0]), float(v[1])) for k, v in json.loads(buf.value.decode()).items()}, int(n.value)

@@ -1,7 +1,11 @@
 // C-ABI entry points of libdfl: argument checks, workspace layout and the
 // order of kernel launches for each operation of the draft step.
 #include <atomic>
+#include <cstdio>
+#include <cstring>
 #include <mutex>
+#include <string>
+#include <vector>
 
 #include "internal.h"
 #include "small_kernels.h"
@@ -240,6 +244,7 @@ extern "C" dfl_status dfl_dual_kv_proj(const void* Xc, const float* Xb, int32_t 
         g.ep.seg[1] = GemmSeg{Vc, kv, kv, 0};
         g.ep.nseg = 2;
         g.ep.rope = rope; g.ep.hd = hd; g.ep.rows_per_seq = C; g.ep.pos_off = 0;
+        g.tag = "gemm_ctx_kv";
         if ((rc = gemm_tc(ctx, g, st)) != DFL_OK) return rc;
     }
     {   // block rows: [Q | Kb | Vb] = Xn [Wq ; Wkb ; Wvb]^T
@@ -256,6 +261,7 @@ extern "C" dfl_status dfl_dual_kv_proj(const void* Xc, const float* Xb, int32_t 
         g.ep.seg[2] = GemmSeg{Vb, qd + kv, kv, 0};
         g.ep.nseg = 3;
         g.ep.rope = rope; g.ep.hd = hd; g.ep.rows_per_seq = B; g.ep.pos_off = C;
+        g.tag = "gemm_block_qkv";
         if ((rc = gemm_tc(ctx, g, st)) != DFL_OK) return rc;
     }
     return DFL_OK;
@@ -300,6 +306,7 @@ extern "C" dfl_status dfl_block_attn(const void* Q, const void* Kc, const void* 
     g.m_inner = 1;
     g.epi = EPI_RESID;
     g.ep.resid = Xb; g.ep.ld_resid = d;
+    g.tag = "gemm_o_proj";
     return gemm_tc(ctx, g, st);
 }
 
@@ -354,6 +361,7 @@ extern "C" dfl_status dfl_lm_head_argmax(const float* Xb, int32_t N, int32_t B, 
     g.ep.part_max = pmax; g.ep.part_idx = pidx; g.ep.part_sum = sp ? psum : nullptr;
     g.ep.inv_T = inv_T;
     g.ep.logits = logits_out; g.ep.ld_logits = V;
+    g.tag = "gemm_lm_head";
     if ((rc = gemm_tc(ctx, g, st)) != DFL_OK) return rc;
     if ((rc = argmax_combine(pmax, pidx, M, tiles, argmax_out, st)) != DFL_OK) return rc;
     if (sp) return sample_rows(logits_out, V, pmax, psum, M, nr, tiles, 256, V, sp->K, sp->T, sp->seed, samples_out, st);
@@ -422,9 +430,12 @@ extern "C" dfl_status dfl_draft_step(const dfl_step_args* a, void* ws, size_t ws
     const size_t sub_bytes = ws_bytes - (size_t)(sub - static_cast<uint8_t*>(ws));
     dfl_status rc;
 
+    {
+    ProfScope ps("copy_block_init", st);
     if (cudaMemcpyAsync(a->Xb, a->Xb0, (size_t)N * B * d * sizeof(float), cudaMemcpyDeviceToDevice, st) !=
         cudaSuccess)
         return DFL_ERR_CUDA;
+    }
     if ((rc = dfl_layer_mix_rmsnorm(a->H, a->h_layer_stride, a->L, ctx_rows, d, ddt, a->D, a->mix_logits,
                                     a->mix_gain, a->eps, Xc, ctx_rows * d, stream)) != DFL_OK)
         return rc;
@@ -451,5 +462,86 @@ extern "C" dfl_status dfl_draft_step(const dfl_step_args* a, void* ws, size_t ws
         return dfl_self_select(a->vlog, ddt, samples, N, a->sample->K, B - 1, a->V, a->scores, a->selected,
                                a->accept_len, a->bonus, sub, sub_bytes, stream);
     if (a->target) return dfl_greedy_accept(a->draft, a->target, N, B - 1, a->accept_len, a->bonus, stream);
+    return DFL_OK;
+}
+
+// ---------------------------------------------------------------- tracing
+
+namespace dfl {
+namespace {
+struct ProfRec {
+    const char* name;
+    cudaEvent_t beg, end;
+};
+std::mutex g_prof_mu;
+std::atomic<bool> g_prof_on{false};
+std::vector<ProfRec> g_prof_recs;     // recorded pairs (events owned by the pool)
+std::vector<std::pair<cudaEvent_t, cudaEvent_t>> g_prof_pool;
+size_t g_prof_used = 0;
+}  // namespace
+
+ProfScope::ProfScope(const char* name, cudaStream_t st) : st_(st) {
+    if (!g_prof_on.load(std::memory_order_relaxed)) return;
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    if (g_prof_used == g_prof_pool.size()) {
+        cudaEvent_t a, b;
+        if (cudaEventCreate(&a) != cudaSuccess) return;
+        if (cudaEventCreate(&b) != cudaSuccess) { cudaEventDestroy(a); return; }
+        g_prof_pool.emplace_back(a, b);
+    }
+    const auto& ev = g_prof_pool[g_prof_used];
+    if (cudaEventRecord(ev.first, st) != cudaSuccess) return;
+    slot_ = (int)g_prof_recs.size();
+    g_prof_recs.push_back(ProfRec{name, ev.first, ev.second});
+    ++g_prof_used;
+}
+
+ProfScope::~ProfScope() {
+    if (slot_ < 0) return;
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    cudaEventRecord(g_prof_recs[slot_].end, st_);
+}
+
+}  // namespace dfl
+
+extern "C" dfl_status dfl_profile_enable(int32_t on) {
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    if (on) {
+        g_prof_recs.clear();
+        g_prof_used = 0;
+    }
+    g_prof_on.store(on != 0);
+    return DFL_OK;
+}
+
+extern "C" dfl_status dfl_profile_report(char* buf, size_t buf_len, int32_t* launches) {
+    if (!buf || buf_len == 0) return DFL_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    std::vector<std::string> names;
+    std::vector<std::pair<int, double>> agg;
+    for (const ProfRec& r : g_prof_recs) {
+        if (cudaEventSynchronize(r.end) != cudaSuccess) return DFL_ERR_CUDA;
+        float ms = 0.f;
+        if (cudaEventElapsedTime(&ms, r.beg, r.end) != cudaSuccess) return DFL_ERR_CUDA;
+        size_t i = 0;
+        while (i < names.size() && names[i] != r.name) ++i;
+        if (i == names.size()) { names.emplace_back(r.name); agg.emplace_back(0, 0.0); }
+        agg[i].first += 1;
+        agg[i].second += ms;
+    }
+    std::string out = "{";
+    for (size_t i = 0; i < names.size(); ++i) {
+        char tmp[256];
+        snprintf(tmp, sizeof(tmp), "%s\"%s\": [%d, %.6f]", i ? ", " : "", names[i].c_str(), agg[i].first,
+                 agg[i].second);
+        out += tmp;
+    }
+    out += "}";
+    const size_t n = out.size() < buf_len - 1 ? out.size() : buf_len - 1;
+    memcpy(buf, out.data(), n);
+    buf[n] = '\0';
+    if (launches) *launches = (int32_t)g_prof_recs.size();
+    g_prof_recs.clear();
+    g_prof_used = 0;
     return DFL_OK;
 }

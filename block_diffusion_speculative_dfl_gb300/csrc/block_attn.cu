@@ -284,6 +284,9 @@ dfl_status attn_bf16(const void* Q, const void* Kc, const void* Vc, const void* 
     NW = (NW + zblocks - 1) / zblocks;
     const int smem = attn_smem(NW, hd);
     dim3 grid(N * Hkv, a.S, zblocks);
+    dfl_status rc;
+    {
+    ProfScope ps("attn_bf16", st);
     if (hd == 128) {
         if (cudaFuncSetAttribute(attn_bf16_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
             cudaSuccess)
@@ -297,8 +300,10 @@ dfl_status attn_bf16(const void* Q, const void* Kc, const void* Vc, const void* 
     } else {
         return DFL_ERR_UNSUPPORTED_SHAPE;
     }
-    dfl_status rc = last_launch();
+    rc = last_launch();
+    }
     if (rc != DFL_OK || a.S == 1) return rc;
+    ProfScope ps("attn_combine", st);
     attn_combine_kernel<<<(unsigned)NQ, hd, 0, st>>>(a.Opart, a.lse, a.S, (int64_t)NQ, hd, a.O);
     return last_launch();
 }

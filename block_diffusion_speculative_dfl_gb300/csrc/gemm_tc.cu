@@ -50,6 +50,7 @@ dfl_status launch(DeviceCtx* ctx, const GemmArgs& g, const GemmShape& sh, const 
     }
     const int tiles = sh.tiles_m * sh.tiles_n;
     const int grid = tiles < ctx->sm_count ? tiles : ctx->sm_count;
+    ProfScope ps(g.tag ? g.tag : "gemm_tc", st);
     kern<<<grid, GEMM_THREADS, GemmCfg<BN>::SMEM, st>>>(ma, mb[0], mb[1], mb[2], sh, g.ep, dev_err(ctx));
     return last_launch();
 }

@@ -29,6 +29,21 @@ inline dfl_status cuda_status(cudaError_t e) { return e == cudaSuccess ? DFL_OK 
 inline dfl_status last_launch() { return cuda_status(cudaGetLastError()); }
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// --------------------------------------------------------------- tracing --
+
+// Records a CUDA event pair around the launches in its scope when tracing is
+// on (dfl_profile_enable); a no-op otherwise.
+class ProfScope {
+public:
+    ProfScope(const char* name, cudaStream_t st);
+    ~ProfScope();
+    ProfScope(const ProfScope&) = delete;
+    ProfScope& operator=(const ProfScope&) = delete;
+private:
+    int slot_ = -1;
+    cudaStream_t st_;
+};
+
 // ---------------------------------------------------------------- GEMM --
 
 struct GemmArgs {
@@ -43,6 +58,7 @@ struct GemmArgs {
     int bn;                 // 128 or 256
     int epi;                // EpiKind
     GemmEpi ep;
+    const char* tag;        // name in kernel traces
 };
 
 dfl_status gemm_tc(DeviceCtx* ctx, const GemmArgs& g, cudaStream_t st);

@@ -271,6 +271,7 @@ extern "C" dfl_status dfl_layer_mix_rmsnorm(const void* H, int64_t layer_stride,
         MixArgs a{static_cast<const __nv_bfloat16*>(H), layer_stride, L, rows, d, D, mix_logits, gain, eps,
                   static_cast<__nv_bfloat16*>(Xc), xc_layer_stride};
         const int64_t grid = rows < ctx->sm_count ? rows : ctx->sm_count;
+        ProfScope ps("mix_rmsnorm_bf16", st);
         mix_rmsnorm_bf16_kernel<<<(unsigned)grid, MIX_THREADS, smem, st>>>(a, dev_err(ctx));
         return last_launch();
     }
@@ -281,6 +282,7 @@ extern "C" dfl_status dfl_layer_mix_rmsnorm(const void* H, int64_t layer_stride,
             cudaSuccess)
         return DFL_ERR_CUDA;
     if (rows > 0x7FFFFFFF) return DFL_ERR_UNSUPPORTED_SHAPE;
+    ProfScope ps("mix_rmsnorm_f32", st);
     mix_rmsnorm_f32_kernel<<<(unsigned)rows, 256, smem, st>>>(static_cast<const float*>(H), layer_stride, L, rows,
                                                              d, D, mix_logits, gain, eps, static_cast<float*>(Xc),
                                                              xc_layer_stride);

@@ -184,13 +184,18 @@ dfl_status self_select_run(const void* vlog, bool bf16, const int32_t* drafts, i
     float* lse = static_cast<float*>(ws);
     int* amax = reinterpret_cast<int*>(static_cast<uint8_t*>(ws) + slot);
     float* zx = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + 2 * slot);
+    dfl_status rc;
+    {
+    ProfScope ps("verifier_row_stats", st);
     if (bf16)
         verifier_row_stats_kernel<true><<<(unsigned)rows, RS_THREADS, 0, st>>>(vlog, K, G, V, drafts, lse, amax, zx);
     else
         verifier_row_stats_kernel<false><<<(unsigned)rows, RS_THREADS, 0, st>>>(vlog, K, G, V, drafts, lse, amax,
                                                                                  zx);
-    dfl_status rc = last_launch();
+    rc = last_launch();
+    }
     if (rc != DFL_OK) return rc;
+    ProfScope ps("streak_select", st);
     streak_select_kernel<<<(N + 3) / 4, 128, 0, st>>>(drafts, N, K, G, lse, amax, zx, scores, selected, accept_len,
                                                         bonus);
     return last_launch();

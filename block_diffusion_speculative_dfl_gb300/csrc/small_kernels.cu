@@ -23,6 +23,7 @@ __global__ void rope_table_kernel(float* table, int P, int hd, double theta) {
 dfl_status rope_table(float* table, int P, int hd, double theta, cudaStream_t st) {
     const int64_t n = (int64_t)P * (hd / 2);
     const int grid = (int)((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096);
+    ProfScope ps("rope_table", st);
     rope_table_kernel<<<grid, 256, 0, st>>>(table, P, hd, theta);
     return last_launch();
 }
@@ -65,6 +66,7 @@ __global__ void rmsnorm_rows_kernel(const float* in, int d, int64_t M, int per, 
 dfl_status rmsnorm_rows(const float* in, int d, int64_t M, int per, int stride, int off, const float* gain,
                         float eps, void* out, bool bf16, cudaStream_t st) {
     const unsigned grid = (unsigned)((M + 7) / 8);
+    ProfScope ps("rmsnorm_rows", st);
     if (bf16)
         rmsnorm_rows_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(in, d, M, per, stride, off, gain, eps,
                                                                  static_cast<__nv_bfloat16*>(out));
@@ -100,6 +102,7 @@ __global__ void greedy_accept_kernel(const int32_t* draft, const int32_t* target
 
 dfl_status greedy_accept(const int32_t* draft, const int32_t* target, int N, int n, int32_t* accept_len,
                          int32_t* bonus, cudaStream_t st) {
+    ProfScope ps("greedy_accept", st);
     greedy_accept_kernel<<<(N + 7) / 8, 256, 0, st>>>(draft, target, N, n, accept_len, bonus);
     return last_launch();
 }
@@ -131,6 +134,7 @@ __global__ void argmax_combine_kernel(const float* pmax, const int* pidx, int64_
 
 dfl_status argmax_combine(const float* pmax, const int* pidx, int64_t M, int tiles, int32_t* out,
                           cudaStream_t st) {
+    ProfScope ps("argmax_combine", st);
     argmax_combine_kernel<<<(unsigned)((M + 7) / 8), 256, 0, st>>>(pmax, pidx, M, tiles, out);
     return last_launch();
 }
@@ -231,6 +235,7 @@ dfl_status sample_rows(const float* logits, int64_t ld, const float* pmax, const
     if (smem > 48 * 1024 &&
         cudaFuncSetAttribute(sample_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return DFL_ERR_CUDA;
+    ProfScope ps("sample_inverse_cdf", st);
     sample_kernel<<<(unsigned)((M + warps - 1) / warps), warps * 32, smem, st>>>(
         logits, ld, pmax, psum, M, per, tiles, bn, V, K, 1.0f / T, (uint32_t)(seed & 0xFFFFFFFFu),
         (uint32_t)(seed >> 32), samples);
@@ -262,6 +267,7 @@ __global__ void tile_partials_kernel(const float* logits, int64_t ld, int64_t M,
 dfl_status tile_partials(const float* logits, int64_t ld, int64_t M, int V, int bn, int tiles, float inv_T,
                          float* pmax, int* pidx, double* psum, cudaStream_t st) {
     const int64_t n = M * tiles;
+    ProfScope ps("tile_partials", st);
     tile_partials_kernel<<<(unsigned)((n + 127) / 128), 128, 0, st>>>(logits, ld, M, V, bn, tiles, inv_T, pmax,
                                                                        pidx, psum);
     return last_launch();
@@ -312,6 +318,7 @@ __global__ void gemm_f32_kernel(const float* A, const float* B, float* C, int M,
 dfl_status gemm_f32(const float* A, const float* B, float* C, int M, int N, int K, int ldc, int accumulate,
                     cudaStream_t st) {
     dim3 grid((N + 63) / 64, (M + 63) / 64);
+    ProfScope ps("gemm_f32", st);
     gemm_f32_kernel<<<grid, 256, 0, st>>>(A, B, C, M, N, K, ldc, accumulate);
     return last_launch();
 }
@@ -339,6 +346,7 @@ dfl_status rope_inplace_f32(float* x, int64_t rows, int heads, int hd, int per, 
                             cudaStream_t st) {
     const int64_t n = rows * heads * (hd / 2);
     const int grid = (int)((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096);
+    ProfScope ps("rope_f32", st);
     rope_inplace_f32_kernel<<<grid, 256, 0, st>>>(x, rows, heads, hd, per, pos_off, rope);
     return last_launch();
 }
@@ -377,6 +385,7 @@ __global__ void attn_f32_kernel(const float* Q, const float* Kc, const float* Vc
 
 dfl_status attn_f32(const float* Q, const float* Kc, const float* Vc, const float* Kb, const float* Vb, int N, int C,
                     int B, int Hq, int Hkv, int hd, float* O, cudaStream_t st) {
+    ProfScope ps("attn_f32", st);
     attn_f32_kernel<<<N * Hq, 128, 0, st>>>(Q, Kc, Vc, Kb, Vb, N, C, B, Hq, Hkv, hd, O);
     return last_launch();
 }
@@ -395,6 +404,7 @@ __global__ void selftest_wait_kernel(int* status, uint64_t limit_ns) {
 }
 
 dfl_status selftest_wait(int* status, uint64_t limit_ns, cudaStream_t st) {
+    ProfScope ps("selftest_wait", st);
     selftest_wait_kernel<<<1, 32, 0, st>>>(status, limit_ns);
     return last_launch();
 }

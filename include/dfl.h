@@ -307,6 +307,20 @@ dfl_status dfl_set_wait_limit_ns(uint64_t ns);
 dfl_status dfl_selftest_bounded_wait(uint64_t limit_ns, int32_t* status_out,
                                      dfl_stream stream);
 
+/*
+ * Kernel tracing.  While enabled, every kernel the library launches is
+ * bracketed by a pair of CUDA events recorded on its stream (events come from
+ * a pool the library owns; no device memory is allocated).
+ * dfl_profile_enable(1) clears earlier records; dfl_profile_enable(0) stops
+ * recording.  dfl_profile_report() waits for the recorded events, writes
+ * {"kernel": [launches, total_ms], ...} as JSON into buf (truncated to
+ * buf_len, NUL-terminated), stores the number of launches in *launches
+ * (nullable) and clears the records.
+ * Errors: INVALID_ARG (buf NULL or buf_len 0), CUDA.
+ */
+dfl_status dfl_profile_enable(int32_t on);
+dfl_status dfl_profile_report(char* buf, size_t buf_len, int32_t* launches);
+
 #ifdef __cplusplus
 }
 #endif

@@ -1,0 +1,205 @@
+"""Whole draft steps through dfl_draft_step against the fp64 oracle (GPU).
+
+Small shapes are checked completely; the full-size workloads run in the same
+launch configuration the benchmark times and are checked on sampled
+sequences (the oracle recomputes those one by one) plus bit-exact epilogue
+checks on every sequence from the GPU's own logits / verifier buffers.
+"""
+import numpy as np
+import pytest
+import torch
+
+import block_diffusion_speculative_dfl_gb300 as dfl
+import oracle as orc
+from dfl_synth import (WORKLOADS, Workload, gen_block_init, gen_gains, gen_hidden, gen_layer_weights, gen_lm_head,
+                       gen_mix_logits, gen_verifier_logits, geometric_prefix, plant_targets)
+from gpu_util import assert_bf16_close, assert_f32_close, check_samples, host
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    dfl.build()
+    dfl.load()
+    torch.cuda.set_device(0)
+    yield
+    assert dfl.dfl_get_device_error() == 0
+
+
+def _shape(w):
+    return {"Hq": w.Hq, "Hkv": w.Hkv, "hd": w.hd}
+
+
+def _model(w, random_gains=False):
+    mix = gen_mix_logits(w)
+    g_mix, g_blk, g_fin = gen_gains(w, random=random_gains)
+    layers = [gen_layer_weights(w, l) for l in range(w.D)]
+    W_lm = gen_lm_head(w, as_bits=(w.dtype == "bf16")) if w.V > 0 else None
+    shape = dfl.DraftShape(N=w.N, d=w.d, Hq=w.Hq, Hkv=w.Hkv, hd=w.hd, D=w.D, L=w.L, B=w.B, C=w.C, V=w.V,
+                           dtype=w.dtype, K=w.K, T=w.T, seed=w.philox_seed, eps=w.eps, rope_theta=w.rope_theta)
+    W_lm_t = None
+    if W_lm is not None:
+        W_lm_t = torch.from_numpy(W_lm.view(np.int16)).view(torch.bfloat16) if w.dtype == "bf16" else \
+            torch.from_numpy(W_lm)
+    model = dfl.DraftModel(shape, mix, g_mix, g_blk, g_fin, layers, W_lm_t)
+    return model, dict(mix=mix, g_mix=g_mix, g_blk=g_blk, g_fin=g_fin, layers=layers, W_lm=W_lm)
+
+
+def _hidden_dev(w):
+    if w.dtype == "bf16":
+        return torch.from_numpy(gen_hidden(w, as_bits=True).view(np.int16)).cuda().view(torch.bfloat16)
+    return torch.from_numpy(gen_hidden(w)).cuda()
+
+
+def _oracle_seq(w, p, n):
+    """fp64 oracle draft forward + logits for sequence n."""
+    Hn = gen_hidden(w, seqs=[n])
+    Xb0 = gen_block_init(w)[n]
+    out = orc.draft_forward(Xb0, Hn, p["mix"], p["g_mix"], p["g_blk"], p["layers"], _shape(w), w.eps, w.rope_theta)
+    z = None
+    if w.V > 0:
+        from dfl_synth import bits_to_f32
+        W_lm = bits_to_f32(p["W_lm"]) if w.dtype == "bf16" else p["W_lm"]
+        z = orc.lm_head_logits(out["Xb"][1:], p["g_fin"], w.eps, W_lm)
+    return out["Xb"], z
+
+
+def _run_greedy_workload(w, seqs, random_gains=False):
+    model, p = _model(w, random_gains)
+    model.want_logits()
+    H = _hidden_dev(w)
+    X0 = torch.from_numpy(gen_block_init(w)).cuda()
+    model.step(H, X0)
+    torch.cuda.synchronize()
+    drafts = host(model.draft)
+    target = torch.from_numpy(plant_targets(w, drafts)).cuda()
+    model.step(H, X0, target=target)
+    torch.cuda.synchronize()
+    # the step is deterministic: the second pass drafts the same tokens
+    assert np.array_equal(host(model.draft), drafts)
+    z = host(model.logits).reshape(w.N, w.B - 1, w.V)
+    # argmax bit-exact on the GPU's own logits, every sequence
+    assert np.array_equal(orc.argmax_lowest(z), drafts)
+    # greedy acceptance bit-exact, every sequence; equals the planted prefix
+    t = host(target)
+    G = geometric_prefix(w)
+    for n in range(w.N):
+        a, b = orc.greedy_accept(drafts[n], t[n])
+        assert (a, b) == (int(host(model.accept_len)[n]), int(host(model.bonus)[n]))
+        assert a == G[n]
+    Xb = host(model.Xb)
+    for n in seqs:
+        ref_xb, ref_z = _oracle_seq(w, p, n)
+        if w.dtype == "f32":
+            assert_f32_close(Xb[n], ref_xb, f"Xb[{n}]")
+            assert_f32_close(z[n], ref_z, f"logits[{n}]")
+        else:
+            assert_bf16_close(Xb[n] - gen_block_init(w)[n], ref_xb - gen_block_init(w)[n], f"dXb[{n}]",
+                              mean_bar=8e-3)
+            assert_bf16_close(z[n], ref_z, f"logits[{n}]", mean_bar=8e-3)
+
+
+def test_tiny_f32_workload_end_to_end():
+    _run_greedy_workload(WORKLOADS["tiny_f32"], seqs=[0])
+
+
+def test_tiny_f32_random_gains():
+    _run_greedy_workload(WORKLOADS["tiny_f32"], seqs=[0], random_gains=True)
+
+
+def test_small_bf16_drafter():
+    w = Workload("small", N=3, d=512, Hq=8, Hkv=2, hd=128, D=3, L=5, B=16, C=200, V=3000, dtype="bf16", seed=41,
+                 geom_p=0.3)
+    _run_greedy_workload(w, seqs=[0, 2], random_gains=True)
+
+
+def test_small_bf16_drafter_hd64():
+    w = Workload("small64", N=2, d=320, Hq=8, Hkv=2, hd=64, D=2, L=7, B=8, C=130, V=1001, dtype="bf16", seed=43,
+                 geom_p=0.2)
+    _run_greedy_workload(w, seqs=[1])
+
+
+def _run_select_workload(w, seqs, rows_checked):
+    model, p = _model(w)
+    model.want_logits()
+    H = _hidden_dev(w)
+    X0 = torch.from_numpy(gen_block_init(w)).cuda()
+    vlog_bits = gen_verifier_logits(w, as_bits=True)
+    vlog = torch.from_numpy(vlog_bits.view(np.int16)).cuda().view(torch.bfloat16)
+    model.step(H, X0, vlog=vlog)
+    torch.cuda.synchronize()
+    G = w.gamma
+    z = host(model.logits).reshape(w.N, G, w.V)
+    samples = host(model.samples)
+    assert np.array_equal(orc.argmax_lowest(z), host(model.draft))
+    # samples: the oracle's inverse-CDF draw on the same logits
+    check_samples(samples, lambda n, j: z[n, j], w.philox_seed, w.K, w.T, [(n, j) for n in seqs for j in rows_checked])
+    # selection and acceptance from the GPU's samples and the verifier buffer
+    from dfl_synth import bits_to_f32
+    sel, al, bo, sc = host(model.selected), host(model.accept_len), host(model.bonus), host(model.scores)
+    for n in seqs:
+        vl = bits_to_f32(vlog_bits[n])
+        scores, ks, a, b = orc.self_select(vl, samples[n])
+        assert np.allclose(sc[n], scores, rtol=1e-4, atol=0)
+        top = np.sort(scores)[::-1]
+        if w.K > 1 and top[0] - top[1] <= 1e-5 * top[0]:
+            assert scores[sel[n]] >= top[1]
+        else:
+            assert sel[n] == ks
+        t = [int(np.argmax(vl[sel[n], j])) for j in range(G + 1)]
+        assert (int(al[n]), int(bo[n])) == orc.greedy_accept(samples[n, sel[n]], t)
+    Xb = host(model.Xb)
+    for n in seqs[:1]:
+        ref_xb, ref_z = _oracle_seq(w, p, n)
+        X0n = gen_block_init(w)[n]
+        assert_bf16_close(Xb[n] - X0n, ref_xb - X0n, f"dXb[{n}]", mean_bar=8e-3)
+        assert_bf16_close(z[n], ref_z, f"logits[{n}]", mean_bar=8e-3)
+
+
+def test_small_self_selection_step():
+    w = Workload("smallsel", N=3, d=512, Hq=8, Hkv=2, hd=128, D=2, L=4, B=9, C=100, V=2000, dtype="bf16", seed=47,
+                 K=8, T=1.5, philox_seed=0x5EEDD1F5)
+    _run_select_workload(w, seqs=[0, 1, 2], rows_checked=range(w.gamma))
+
+
+def test_step_from_host_matches_device_step():
+    w = Workload("e2e", N=2, d=256, Hq=4, Hkv=2, hd=64, D=2, L=3, B=16, C=64, V=1000, dtype="bf16", seed=53,
+                 geom_p=0.3)
+    model, _ = _model(w)
+    H_host = torch.from_numpy(gen_hidden(w, as_bits=True).view(np.int16)).view(torch.bfloat16).pin_memory()
+    X_host = torch.from_numpy(gen_block_init(w)).pin_memory()
+    model.step(H_host.cuda(), X_host.cuda())
+    torch.cuda.synchronize()
+    drafts = host(model.draft)
+    t_host = torch.from_numpy(plant_targets(w, drafts)).pin_memory()
+    out, _ = model.step_from_host(H_host, X_host, t_host)
+    assert np.array_equal(out["draft"].numpy(), drafts)
+    assert np.array_equal(out["accept_len"].numpy(), geometric_prefix(w))
+
+
+# ---------------------------------------------------------- full sizes --
+
+def test_qwen3_8b_single_layer_full_size():
+    w = WORKLOADS["qwen3_8b_layer"]
+    model, p = _model(w)
+    H = _hidden_dev(w)
+    X0 = torch.from_numpy(gen_block_init(w)).cuda()
+    model.step(H, X0)
+    torch.cuda.synchronize()
+    ref_xb, _ = _oracle_seq(w, p, 0)
+    X0n = gen_block_init(w)[0]
+    assert_bf16_close(host(model.Xb)[0] - X0n, ref_xb - X0n, "dXb", mean_bar=8e-3)
+
+
+def test_qwen3_8b_drafter_full_size():
+    _run_greedy_workload(WORKLOADS["qwen3_8b_drafter"], seqs=[0, 31])
+
+
+def test_gpt_oss_20b_drafter_full_size():
+    _run_greedy_workload(WORKLOADS["gpt_oss_20b_drafter"], seqs=[5])
+
+
+def test_specdiff2_selection_full_size():
+    w = WORKLOADS["specdiff2_select"]
+    _run_select_workload(w, seqs=[0, 15], rows_checked=[0, 1, 17, 31])
