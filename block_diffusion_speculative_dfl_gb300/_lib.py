@@ -20,7 +20,8 @@ DFL_OP_DUAL_KV_PROJ, DFL_OP_BLOCK_ATTN, DFL_OP_LM_HEAD, DFL_OP_SELF_SELECT, DFL_
 EXPORTED = ("dfl_version", "dfl_status_string", "dfl_workspace_size", "dfl_rope_table",
             "dfl_layer_mix_rmsnorm", "dfl_dual_kv_proj", "dfl_block_attn", "dfl_lm_head_argmax",
             "dfl_greedy_accept", "dfl_self_select", "dfl_draft_step", "dfl_get_device_error",
-            "dfl_set_wait_limit_ns", "dfl_selftest_bounded_wait", "dfl_profile_enable", "dfl_profile_report")
+            "dfl_set_wait_limit_ns", "dfl_selftest_bounded_wait", "dfl_profile_enable", "dfl_profile_report",
+            "dfl_self_select_noalloc")
 
 
 class DflError(RuntimeError):
@@ -74,6 +75,7 @@ _SIGS = {
     "dfl_selftest_bounded_wait": ([C.c_uint64, _P, _P], _I32),
     "dfl_profile_enable": ([_I32], _I32),
     "dfl_profile_report": ([C.c_char_p, _SZ, C.POINTER(_I32)], _I32),
+    "dfl_self_select_noalloc": ([_P, _I32, _P, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _P], _I32),
 }
 
 _lib = None
@@ -209,3 +211,10 @@ def dfl_profile_report() -> tuple[dict, int]:
     n = _I32(0)
     _check("dfl_profile_report", load().dfl_profile_report(buf, len(buf), C.byref(n)))
     return {k: (int(v[0]), float(v[1])) for k, v in json.loads(buf.value.decode()).items()}, int(n.value)
+
+
+def dfl_self_select_noalloc(vlog, dt, drafts, N, K, G, V, scores, selected, accept_len, bonus, stream=None):
+    """dfl_self_select with the scratch in the library's fixed device array (no workspace argument)."""
+    _check("dfl_self_select_noalloc",
+           load().dfl_self_select_noalloc(ptr(vlog), dt, ptr(drafts), N, K, G, V, ptr(scores), ptr(selected),
+                                          ptr(accept_len), ptr(bonus), _stream(stream)))

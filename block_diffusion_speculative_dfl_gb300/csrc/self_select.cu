@@ -13,6 +13,8 @@
 // S_k = sum_m exp(sum_{j<=m} log p_j) in fp64, k* = argmax_k S_k (lowest k on
 // ties), then the prefix of x^{k*} matching the argmax of its verifier rows
 // and the bonus token.
+#include <mutex>
+
 #include "internal.h"
 #include "small_kernels.h"
 
@@ -202,3 +204,71 @@ dfl_status self_select_run(const void* vlog, bool bf16, const int32_t* drafts, i
 }
 
 }  // namespace dfl
+
+// --------------------------------------------------- no-allocation variant
+//
+// Some callers cannot hand the library a workspace: a plugin inside a serving
+// engine that owns all device memory through its own pool and gives plugins
+// no way to borrow from it, or a latency-critical host loop that must never
+// call cudaMalloc (which can synchronise the device or fail under memory
+// pressure in the middle of serving).  For them, dfl_self_select_noalloc runs
+// the same two kernels as dfl_self_select with their scratch in a fixed array
+// that lives in the library's own device image.
+//
+// Limits and sharing: the array is 768 KiB, enough for N*K*(G+1) <= 65536
+// verifier rows; every GPU that loads the library holds it until the process
+// exits.  All calls on a device share it and it keeps the previous call's
+// contents; nothing needs clearing because each call writes every entry it
+// later reads.  Calls whose kernels overlap on the GPU (different streams, or
+// several host threads) race on the array and must be serialised by the
+// caller.
+
+namespace dfl {
+namespace {
+
+constexpr size_t kNoAllocRows = 65536;
+constexpr size_t kNoAllocSlot = kNoAllocRows * 4;   // one fp32/int32 per row, per array
+
+static __device__ __align__(256) uint8_t g_select_scratch[3 * kNoAllocSlot];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[64] = {};
+
+// Device address of the array on the current device.  Host code cannot use
+// the symbol itself (it names a host-side stand-in), so the address is looked
+// up once per device with that device current, then cached.
+dfl_status noalloc_scratch(void** out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return DFL_ERR_CUDA;
+    if (dev < 0 || dev >= 64) return DFL_ERR_NO_DEVICE;
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_select_scratch) != cudaSuccess || !p) return DFL_ERR_CUDA;
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return DFL_OK;
+}
+
+}  // namespace
+
+}  // namespace dfl
+
+extern "C" dfl_status dfl_self_select_noalloc(const void* vlog, dfl_dtype dt, const int32_t* drafts, int32_t N,
+                                              int32_t K, int32_t G, int32_t V, float* scores, int32_t* selected,
+                                              int32_t* accept_len, int32_t* bonus, dfl_stream stream) {
+    using namespace dfl;
+    if (N <= 0 || K < 1 || K > 64 || G < 1 || G > 1024 || V <= 0) return DFL_ERR_INVALID_ARG;
+    if (dt != DFL_F32 && dt != DFL_BF16) return DFL_ERR_INVALID_ARG;
+    if (!vlog || !drafts || !scores || !selected || !accept_len || !bonus) return DFL_ERR_INVALID_ARG;
+    if (!aligned16(vlog)) return DFL_ERR_MISALIGNED;
+    if ((size_t)N * K * (G + 1) > kNoAllocRows) return DFL_ERR_WORKSPACE;   // beyond the fixed array
+    if (!current_ctx()) return DFL_ERR_NO_DEVICE;
+    void* scratch = nullptr;
+    const dfl_status rc = noalloc_scratch(&scratch);
+    if (rc != DFL_OK) return rc;
+    return self_select_run(vlog, dt == DFL_BF16, drafts, N, K, G, V, scores, selected, accept_len, bonus, scratch,
+                           static_cast<cudaStream_t>(stream));
+}
+

@@ -238,6 +238,29 @@ dfl_status dfl_self_select(const void* vlog, dfl_dtype dt, const int32_t* drafts
                            int32_t* selected, int32_t* accept_len, int32_t* bonus,
                            void* ws, size_t ws_bytes, dfl_stream stream);
 
+/*
+ * dfl_self_select_noalloc -- dfl_self_select without a caller workspace.
+ *   The pages have no counterpart to this call; it exists for callers that
+ *   cannot provide device scratch memory, such as a plugin inside a serving
+ *   engine that owns all device memory through its own pool, or a host loop
+ *   that must not call cudaMalloc while serving.  It computes exactly what
+ *   dfl_self_select computes, with the same arguments minus (ws, ws_bytes).
+ *   Scratch: a fixed 768 KiB array inside the library's device image, held
+ *   on every GPU that loads the library until the process exits; it fits
+ *   N*K*(G+1) <= 65536 verifier rows, larger calls return DFL_ERR_WORKSPACE
+ *   with nothing launched.  The library allocates nothing for this call.
+ *   The first call on each device looks up the array's device address
+ *   (cudaGetSymbolAddress) and caches it; make that first call before any
+ *   stream capture on that device.  All calls on a device share the array
+ *   and it keeps the last call's contents (no call relies on them); calls
+ *   whose kernels overlap on the GPU race on it and must be serialised.
+ *   Errors: as dfl_self_select, plus DFL_ERR_WORKSPACE for the size limit.
+ */
+dfl_status dfl_self_select_noalloc(const void* vlog, dfl_dtype dt, const int32_t* drafts,
+                                   int32_t N, int32_t K, int32_t G, int32_t V, float* scores,
+                                   int32_t* selected, int32_t* accept_len, int32_t* bonus,
+                                   dfl_stream stream);
+
 /* One draft layer's weights (device pointers, dtype of the step). */
 typedef struct dfl_layer_weights {
     const void* Wq;   /* [Hq*hd][d] */
