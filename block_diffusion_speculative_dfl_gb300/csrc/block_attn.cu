@@ -221,18 +221,43 @@ __global__ void __launch_bounds__(ATT_MAX_WARPS * 32) attn_bf16_kernel(const Att
     }
 }
 
-// O[q] = sum_s 2^(lse_s - max) O_s / sum_s 2^(lse_s - max); one CTA per query row.
-__global__ void attn_combine_kernel(const float* Opart, const float* lse, int S, int64_t NQ, int hd,
-                                    __nv_bfloat16* O) {
-    const int64_t q = blockIdx.x;
-    float mx = -INFINITY;
-    for (int s = 0; s < S; ++s) mx = fmaxf(mx, lse[s * NQ + q]);
-    float den = 0.f;
-    for (int s = 0; s < S; ++s) den += exp2f(lse[s * NQ + q] - mx);
-    for (int e = threadIdx.x; e < hd; e += blockDim.x) {
-        float num = 0.f;
-        for (int s = 0; s < S; ++s) num += exp2f(lse[s * NQ + q] - mx) * Opart[(s * NQ + q) * hd + e];
-        O[q * hd + e] = __float2bfloat16_rn(num / den);
+// O[q] = sum_s 2^(lse_s - max) O_s / sum_s 2^(lse_s - max).  One warp per
+// query row; lane i owns HD/32 consecutive elements; split weights are formed
+// once per row (S <= 64).
+template <int HD>
+__global__ void attn_combine_kernel(const float* Opart, const float* lse, int S, int64_t NQ, __nv_bfloat16* O) {
+    constexpr int PER = HD / 32;
+    const int64_t q = blockIdx.x * (int64_t)(blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (q >= NQ) return;
+    float l0 = lane < S ? lse[lane * NQ + q] : -INFINITY;
+    float l1 = lane + 32 < S ? lse[(lane + 32) * NQ + q] : -INFINITY;
+    const float mx = warp_max(fmaxf(l0, l1));
+    const float w0 = lane < S ? exp2f(l0 - mx) : 0.f;
+    const float w1 = lane + 32 < S ? exp2f(l1 - mx) : 0.f;
+    const float inv = 1.f / warp_sum(w0 + w1);
+    float acc[PER];
+    #pragma unroll
+    for (int e = 0; e < PER; ++e) acc[e] = 0.f;
+    for (int sp = 0; sp < S; ++sp) {
+        const float wgt = __shfl_sync(0xFFFFFFFFu, sp < 32 ? w0 : w1, sp & 31);
+        const float* src = Opart + (sp * NQ + q) * HD + lane * PER;
+        if constexpr (PER == 4) {
+            const float4 t = *reinterpret_cast<const float4*>(src);
+            acc[0] += wgt * t.x; acc[1] += wgt * t.y; acc[2] += wgt * t.z; acc[3] += wgt * t.w;
+        } else {
+            const float2 t = *reinterpret_cast<const float2*>(src);
+            acc[0] += wgt * t.x; acc[1] += wgt * t.y;
+        }
+    }
+    __nv_bfloat16* dst = O + q * HD + lane * PER;
+    if constexpr (PER == 4) {
+        uint2 u;
+        u.x = pack_bf16(acc[0] * inv, acc[1] * inv);
+        u.y = pack_bf16(acc[2] * inv, acc[3] * inv);
+        *reinterpret_cast<uint2*>(dst) = u;
+    } else {
+        *reinterpret_cast<uint32_t*>(dst) = pack_bf16(acc[0] * inv, acc[1] * inv);
     }
 }
 
@@ -240,14 +265,17 @@ int attn_smem(int NW, int hd) { return 128 + NW * 16 * hd * 2 + 2 * 2 * KT * hd 
 
 }  // namespace
 
-// Splits of the key range: enough CTAs for ~2 per SM of a 148-SM part, each
-// split at least one 64-key tile.  Depends on the shape only.
+// Splits of the key range: enough CTAs for ~2 per SM of a 152-SM GB300, each
+// split at least one 64-key tile, at most 64 splits (the combine keeps two
+// split weights per lane).  Depends on the shape only, so workspace sizes do
+// not depend on the device.
 int attn_splits(int N, int C, int B, int Hkv) {
     const int units = N * Hkv;
     const int tiles = (C + B + KT - 1) / KT;
-    int S = (296 + units - 1) / units;
+    int S = (304 + units - 1) / units;
     if (S < 1) S = 1;
     if (S > tiles) S = tiles;
+    if (S > 64) S = 64;
     const int per = (tiles + S - 1) / S;
     return (tiles + per - 1) / per;
 }
@@ -304,7 +332,11 @@ dfl_status attn_bf16(const void* Q, const void* Kc, const void* Vc, const void* 
     }
     if (rc != DFL_OK || a.S == 1) return rc;
     ProfScope ps("attn_combine", st);
-    attn_combine_kernel<<<(unsigned)NQ, hd, 0, st>>>(a.Opart, a.lse, a.S, (int64_t)NQ, hd, a.O);
+    const unsigned cgrid = (unsigned)((NQ + 7) / 8);
+    if (hd == 128)
+        attn_combine_kernel<128><<<cgrid, 256, 0, st>>>(a.Opart, a.lse, a.S, (int64_t)NQ, a.O);
+    else
+        attn_combine_kernel<64><<<cgrid, 256, 0, st>>>(a.Opart, a.lse, a.S, (int64_t)NQ, a.O);
     return last_launch();
 }
 

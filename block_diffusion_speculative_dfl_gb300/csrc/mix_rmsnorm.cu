@@ -7,7 +7,8 @@
 // H, so the stack is streamed from HBM once per draft step.
 //
 // bf16 kernel: per row, TMA bulk copies stage the L slices H_i[r] in shared
-// memory (two rows in flight).  The L -> D mixing is a tiny matrix product per
+// memory (two rows in flight when they fit), and the D normalised rows are
+// staged in shared memory and written back with one bulk copy each.  The L -> D mixing is a tiny matrix product per
 // group of positions, run on the tensor cores with mma.sync m16n8k16: A holds
 // the mixing weights (rows 0..7 the bf16-rounded weight of draft layer
 // 0..7, rows 8..15 the bf16 remainder, so hi + lo carries the fp32 weight
@@ -25,6 +26,8 @@ namespace {
 constexpr int MIX_WARPS = 16;
 constexpr int MIX_THREADS = MIX_WARPS * 32;
 constexpr int MIX_MAXG = 20;            // 16-position groups per warp -> d <= 5120
+constexpr int MIX_GCOLS = 4 * MIX_MAXG;  // TMEM columns of gains per thread
+constexpr int MIX_TMEM_COLS = 512;       // 4 column blocks of MIX_GCOLS, rounded to a power of two
 
 __device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
                                               uint32_t& r3) {
@@ -71,38 +74,75 @@ struct MixArgs {
     int64_t xc_stride;
 };
 
-__global__ void __launch_bounds__(MIX_THREADS, 1) mix_rmsnorm_bf16_kernel(const MixArgs a, const DevErr err) {
+// Shared-memory plan of the bf16 kernel: `nstage` input stages of L padded
+// slabs, one output stage of D padded slabs, the zero row, the reduction
+// array and the barriers.  Slabs are padded by 16 bytes so that the rows of
+// one ldmatrix (8 layers) and the bf16x2 writes of one warp (8 draft layers)
+// fall on distinct banks.
+struct MixSmem {
+    int slab, stage_bytes, out_bytes, nstage, total;
+};
+
+__host__ __device__ inline MixSmem mix_smem_plan(int L, int D, int d, int nstage) {
+    MixSmem m;
+    m.slab = d * 2 + 16;
+    m.stage_bytes = ((L * m.slab + 127) / 128) * 128;
+    m.out_bytes = ((D * m.slab + 127) / 128) * 128;
+    m.nstage = nstage;
+    m.total = 128 + nstage * m.stage_bytes + m.out_bytes + 128 + MIX_WARPS * 8 * 4 + 2 * 8 + 16;
+    return m;
+}
+
+__device__ __forceinline__ void bulk_s2g(void* dst, const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
+                 :: "l"(dst), "r"(smem_u32(src)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+__global__ void __launch_bounds__(MIX_THREADS, 1) mix_rmsnorm_bf16_kernel(const MixArgs a, const int nstage,
+                                                                         const DevErr err) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
-    const int slab = a.d * 2 + 16;                       // padded: rows of 8 layers hit distinct banks
-    const int stage_bytes = ((a.L * slab + 127) / 128) * 128;
-    uint8_t* stage[2] = {smem, smem + stage_bytes};
-    uint8_t* zero_row = smem + 2 * stage_bytes;          // 16 zero bytes
-    float* red = reinterpret_cast<float*>(zero_row + 128);   // [MIX_WARPS][8]
+    const MixSmem P = mix_smem_plan(a.L, a.D, a.d, nstage);
+    uint8_t* in0 = smem;                                   // stage s at in0 + s * stage_bytes
+    uint8_t* out = smem + nstage * P.stage_bytes;          // D padded output slabs
+    uint8_t* zero_row = out + P.out_bytes;                 // 16 zero bytes
+    float* red = reinterpret_cast<float*>(zero_row + 128); // [MIX_WARPS][8]
     uint64_t* full = reinterpret_cast<uint64_t*>(red + MIX_WARPS * 8);
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(full + 2);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t tx_bytes = (uint32_t)a.L * (uint32_t)a.d * 2u;
+    const uint32_t row_bytes = (uint32_t)a.d * 2u;
 
     if (tid == 0) {
-        mbar_init(&full[0], 1);
-        mbar_init(&full[1], 1);
+        for (int q = 0; q < nstage; ++q) mbar_init(&full[q], 1);
         fence_barrier_init();
     }
     if (tid < 4) reinterpret_cast<uint32_t*>(zero_row)[tid] = 0u;
+    // The RMSNorm gains do not change from row to row: each thread keeps the
+    // 4 * MIX_MAXG gains of the positions it writes in its own TMEM lane
+    // (quadrant warp % 4, column block warp / 4) instead of re-reading them
+    // from L2 for every row.
+    if (warp == 0) { tmem_alloc(tmem_holder, MIX_TMEM_COLS); tmem_relinquish(); }
+    tc_fence_before();
     __syncthreads();
+    tc_fence_after();
+    const uint32_t tgain = *tmem_holder + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)((warp >> 2) * MIX_GCOLS);
 
-    uint32_t fills[2] = {0u, 0u};   // copies issued per stage (thread 0 only)
+    uint32_t fills0 = 0u, fills1 = 0u;   // copies issued per stage (thread 0 only)
     auto issue = [&](int64_t row, int s) {
-        ++fills[s];
+        if (s) ++fills1; else ++fills0;
+        uint8_t* dst = in0 + s * P.stage_bytes;
         mbar_arrive_expect_tx(&full[s], tx_bytes);
         for (int i = 0; i < a.L; ++i)
-            bulk_g2s(stage[s] + i * slab, a.H + i * a.layer_stride + row * a.d, (uint32_t)a.d * 2u, &full[s]);
+            bulk_g2s(dst + i * P.slab, a.H + i * a.layer_stride + row * a.d, row_bytes, &full[s]);
     };
-    if (tid == 0) {
-        if (blockIdx.x < a.rows) issue(blockIdx.x, 0);
-        if (blockIdx.x + gridDim.x < a.rows) issue(blockIdx.x + gridDim.x, 1);
-    }
+    if (tid == 0)
+        for (int q = 0; q < nstage; ++q)
+            if (blockIdx.x + (int64_t)q * gridDim.x < a.rows) issue(blockIdx.x + (int64_t)q * gridDim.x, q);
 
     // A fragments: mixing weights of draft layer l = lane/4 (hi rows 0..7, lo rows 8..15).
     uint32_t afrag[4];
@@ -127,22 +167,48 @@ __global__ void __launch_bounds__(MIX_THREADS, 1) mix_rmsnorm_bf16_kernel(const 
     const int my_off = (lane >> 4) * 8;
     const int groups = a.d / 16;
     const int l_out = lane >> 2;
-    const float* gain_l = a.gain + (int64_t)(l_out < a.D ? l_out : 0) * a.d;
+    const bool writes = l_out < a.D;
+    const float* gain_l = a.gain + (int64_t)(writes ? l_out : 0) * a.d;
+    uint8_t* out_l = out + l_out * P.slab;
+    const uint32_t zero_addr = smem_u32(zero_row);
+    {
+        const int n = 2 * (lane & 3);
+        #pragma unroll
+        for (int c = 0; c < MIX_MAXG / 4; ++c) {
+            uint32_t gv[16];
+            #pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int g = warp + (4 * c + q) * MIX_WARPS;
+                float2 g0 = make_float2(0.f, 0.f), g1 = make_float2(0.f, 0.f);
+                if (writes && g < groups) {
+                    g0 = __ldg(reinterpret_cast<const float2*>(gain_l + g * 16 + n));
+                    g1 = __ldg(reinterpret_cast<const float2*>(gain_l + g * 16 + n + 8));
+                }
+                gv[4 * q + 0] = __float_as_uint(g0.x);
+                gv[4 * q + 1] = __float_as_uint(g0.y);
+                gv[4 * q + 2] = __float_as_uint(g1.x);
+                gv[4 * q + 3] = __float_as_uint(g1.y);
+            }
+            tmem_st16(tgain + 16 * c, gv);
+        }
+        tmem_st_wait();
+    }
 
     int it = 0;
     for (int64_t row = blockIdx.x; row < a.rows; row += gridDim.x, ++it) {
-        const int s = it & 1;
-        const uint32_t par = (it >> 1) & 1;
+        const int s = (nstage == 2) ? (it & 1) : 0;
+        const uint32_t par = (nstage == 2) ? ((it >> 1) & 1) : (it & 1);
         const bool ok = mbar_wait(&full[s], par, err);
         if (!__syncthreads_and(ok)) {
             // A bounded wait ran out (error recorded): let issued copies land, then leave.
-            if (tid == 0)
-                for (int q = 0; q < 2; ++q)
-                    if (fills[q]) mbar_wait(&full[q], (fills[q] - 1) & 1, err);
-            return;
+            if (tid == 0) {
+                if (fills0) mbar_wait(&full[0], (fills0 - 1) & 1, err);
+                if (fills1) mbar_wait(&full[1], (fills1 - 1) & 1, err);
+            }
+            break;
         }
-
-        const uint32_t base = smem_u32(my_k < a.L ? stage[s] + my_k * slab : zero_row);
+        const uint32_t stage_addr = smem_u32(in0) + (uint32_t)(s * P.stage_bytes);
+        const uint32_t base = my_k < a.L ? stage_addr + (uint32_t)(my_k * P.slab) : zero_addr;
         const uint32_t step = my_k < a.L ? 2u : 0u;
         float v[MIX_MAXG][4];
         float ss = 0.f;
@@ -166,28 +232,50 @@ __global__ void __launch_bounds__(MIX_THREADS, 1) mix_rmsnorm_bf16_kernel(const 
         ss += __shfl_xor_sync(0xFFFFFFFFu, ss, 1);
         ss += __shfl_xor_sync(0xFFFFFFFFu, ss, 2);
         if ((lane & 3) == 0) red[warp * 8 + l_out] = ss;
-        __syncthreads();   // stage s fully read; partial sums visible
-        if (tid == 0 && row + 2 * (int64_t)gridDim.x < a.rows) issue(row + 2 * (int64_t)gridDim.x, s);
+        if (tid == 0) bulk_wait_read0();   // previous row's output stage has been read out
+        __syncthreads();                    // stage s consumed; partial sums visible; output stage free
+        if (tid == 0 && row + (int64_t)nstage * gridDim.x < a.rows) issue(row + (int64_t)nstage * gridDim.x, s);
         float tot = 0.f;
         #pragma unroll
         for (int w = 0; w < MIX_WARPS; ++w) tot += red[w * 8 + l_out];
         const float rs = rsqrtf(tot / (float)a.d + a.eps);
-        if (l_out < a.D) {
-            __nv_bfloat16* out = a.Xc + l_out * a.xc_stride + row * a.d;
+        {
             const int n = 2 * (lane & 3);
             #pragma unroll
-            for (int j = 0; j < MIX_MAXG; ++j) {
-                const int g = warp + j * MIX_WARPS;
-                if (g < groups) {
-                    const int p = g * 16 + n;
-                    const float2 g0 = *reinterpret_cast<const float2*>(gain_l + p);
-                    const float2 g1 = *reinterpret_cast<const float2*>(gain_l + p + 8);
-                    *reinterpret_cast<uint32_t*>(out + p) = pack_bf16(v[j][0] * rs * g0.x, v[j][1] * rs * g0.y);
-                    *reinterpret_cast<uint32_t*>(out + p + 8) = pack_bf16(v[j][2] * rs * g1.x, v[j][3] * rs * g1.y);
+            for (int c = 0; c < MIX_MAXG / 4; ++c) {
+                if (warp + 4 * c * MIX_WARPS >= groups) break;   // warp-uniform
+                float gv[16];
+                tmem_ld16(tgain + 16 * c, gv);
+                if (writes) {
+                    #pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int j = 4 * c + q;
+                        const int g = warp + j * MIX_WARPS;
+                        if (g < groups) {
+                            const int p = g * 16 + n;
+                            *reinterpret_cast<uint32_t*>(out_l + p * 2) =
+                                pack_bf16(v[j][0] * rs * gv[4 * q], v[j][1] * rs * gv[4 * q + 1]);
+                            *reinterpret_cast<uint32_t*>(out_l + (p + 8) * 2) =
+                                pack_bf16(v[j][2] * rs * gv[4 * q + 2], v[j][3] * rs * gv[4 * q + 3]);
+                        }
+                    }
                 }
             }
         }
-        __syncthreads();   // red[] reads done before the next row writes it
+        fence_proxy_async_smem();   // make the output stage visible to the bulk copies
+        __syncthreads();
+        if (tid == 0) {
+            for (int l = 0; l < a.D; ++l)
+                bulk_s2g(a.Xc + l * a.xc_stride + row * a.d, out + l * P.slab, row_bytes);
+            bulk_commit();
+        }
+    }
+    if (tid == 0) bulk_wait0();
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(*tmem_holder, MIX_TMEM_COLS);
     }
 }
 
@@ -233,12 +321,6 @@ __global__ void mix_rmsnorm_f32_kernel(const float* H, int64_t layer_stride, int
 
 }  // namespace
 
-int mix_bf16_smem_bytes(int L, int d) {
-    const int slab = d * 2 + 16;
-    const int stage_bytes = ((L * slab + 127) / 128) * 128;
-    return 128 + 2 * stage_bytes + 128 + MIX_WARPS * 8 * 4 + 16 + 64;
-}
-
 }  // namespace dfl
 
 using namespace dfl;
@@ -260,7 +342,9 @@ extern "C" dfl_status dfl_layer_mix_rmsnorm(const void* H, int64_t layer_stride,
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (dt == DFL_BF16) {
         if (d % 16 != 0 || d > 16 * MIX_WARPS * MIX_MAXG) return DFL_ERR_UNSUPPORTED_SHAPE;
-        const int smem = mix_bf16_smem_bytes(L, d);
+        int nstage = 2;
+        if (mix_smem_plan(L, D, d, 2).total > 227 * 1024) nstage = 1;
+        const int smem = mix_smem_plan(L, D, d, nstage).total;
         if (smem > 227 * 1024) return DFL_ERR_UNSUPPORTED_SHAPE;
         if (!ctx->mix_attr_set) {
             if (cudaFuncSetAttribute(mix_rmsnorm_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -272,7 +356,7 @@ extern "C" dfl_status dfl_layer_mix_rmsnorm(const void* H, int64_t layer_stride,
                   static_cast<__nv_bfloat16*>(Xc), xc_layer_stride};
         const int64_t grid = rows < ctx->sm_count ? rows : ctx->sm_count;
         ProfScope ps("mix_rmsnorm_bf16", st);
-        mix_rmsnorm_bf16_kernel<<<(unsigned)grid, MIX_THREADS, smem, st>>>(a, dev_err(ctx));
+        mix_rmsnorm_bf16_kernel<<<(unsigned)grid, MIX_THREADS, smem, st>>>(a, nstage, dev_err(ctx));
         return last_launch();
     }
     const size_t smem = (size_t)(D * L + D * 32 + (size_t)D * d) * sizeof(float);

@@ -31,48 +31,68 @@ dfl_status rope_table(float* table, int P, int hd, double theta, cudaStream_t st
 // ------------------------------------------------------------ row RMSNorm
 
 // out[m] = RMSNorm(in[src_row(m)]) * gain, src_row(m) = (m / per) * stride + off + m % per.
-// One warp per row.  OutT = __nv_bfloat16 or float.
+// One 128-thread CTA per row; the row stays in registers between the sum of
+// squares and the scaled store (d <= 128 * 4 * RN_MAXV).  OutT = bf16 or float.
+constexpr int RN_THREADS = 128;
+constexpr int RN_MAXV = 12;   // float4 per thread -> d <= 6144
+
 template <typename OutT>
-__global__ void rmsnorm_rows_kernel(const float* in, int d, int64_t M, int per, int stride, int off,
-                                    const float* gain, float eps, OutT* out) {
-    const int64_t m = blockIdx.x * (int64_t)(blockDim.x >> 5) + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    if (m >= M) return;
+__global__ void __launch_bounds__(RN_THREADS) rmsnorm_rows_kernel(const float* in, int d, int64_t M, int per,
+                                                                  int stride, int off, const float* gain, float eps,
+                                                                  OutT* out) {
+    const int64_t m = blockIdx.x;
+    const int tid = threadIdx.x;
     const int64_t src = (m / per) * stride + off + m % per;
-    const float* x = in + src * d;
+    const float4* x = reinterpret_cast<const float4*>(in + src * d);
+    const int nv = d / 4;
+    float4 v[RN_MAXV];
     float ss = 0.f;
-    for (int e = lane * 4; e < d; e += 128) {
-        const float4 v = *reinterpret_cast<const float4*>(x + e);
-        ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+    #pragma unroll
+    for (int j = 0; j < RN_MAXV; ++j) {
+        const int e = tid + j * RN_THREADS;
+        v[j] = e < nv ? x[e] : make_float4(0.f, 0.f, 0.f, 0.f);
+        ss += v[j].x * v[j].x + v[j].y * v[j].y + v[j].z * v[j].z + v[j].w * v[j].w;
     }
+    __shared__ float red[RN_THREADS / 32];
     ss = warp_sum(ss);
-    const float rs = rsqrtf(ss / (float)d + eps);
+    if ((tid & 31) == 0) red[tid >> 5] = ss;
+    __syncthreads();
+    float tot = 0.f;
+    #pragma unroll
+    for (int w = 0; w < RN_THREADS / 32; ++w) tot += red[w];
+    const float rs = rsqrtf(tot / (float)d + eps);
     OutT* o = out + m * d;
-    for (int e = lane * 4; e < d; e += 128) {
-        const float4 v = *reinterpret_cast<const float4*>(x + e);
-        const float4 g = *reinterpret_cast<const float4*>(gain + e);
-        const float y0 = v.x * rs * g.x, y1 = v.y * rs * g.y, y2 = v.z * rs * g.z, y3 = v.w * rs * g.w;
-        if constexpr (sizeof(OutT) == 2) {
-            uint2 u;
-            u.x = pack_bf16(y0, y1);
-            u.y = pack_bf16(y2, y3);
-            *reinterpret_cast<uint2*>(o + e) = u;
-        } else {
-            *reinterpret_cast<float4*>(o + e) = make_float4(y0, y1, y2, y3);
+    const float4* g4 = reinterpret_cast<const float4*>(gain);
+    #pragma unroll
+    for (int j = 0; j < RN_MAXV; ++j) {
+        const int e = tid + j * RN_THREADS;
+        if (e < nv) {
+            const float4 g = __ldg(g4 + e);
+            const float y0 = v[j].x * rs * g.x, y1 = v[j].y * rs * g.y, y2 = v[j].z * rs * g.z,
+                        y3 = v[j].w * rs * g.w;
+            if constexpr (sizeof(OutT) == 2) {
+                uint2 u;
+                u.x = pack_bf16(y0, y1);
+                u.y = pack_bf16(y2, y3);
+                *reinterpret_cast<uint2*>(o + 4 * e) = u;
+            } else {
+                *reinterpret_cast<float4*>(o + 4 * e) = make_float4(y0, y1, y2, y3);
+            }
         }
     }
 }
 
 dfl_status rmsnorm_rows(const float* in, int d, int64_t M, int per, int stride, int off, const float* gain,
                         float eps, void* out, bool bf16, cudaStream_t st) {
-    const unsigned grid = (unsigned)((M + 7) / 8);
+    if (d > RN_THREADS * 4 * RN_MAXV || d % 4 != 0) return DFL_ERR_UNSUPPORTED_SHAPE;
+    if (M > 0x7FFFFFFF) return DFL_ERR_UNSUPPORTED_SHAPE;
     ProfScope ps("rmsnorm_rows", st);
     if (bf16)
-        rmsnorm_rows_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(in, d, M, per, stride, off, gain, eps,
-                                                                 static_cast<__nv_bfloat16*>(out));
+        rmsnorm_rows_kernel<__nv_bfloat16><<<(unsigned)M, RN_THREADS, 0, st>>>(in, d, M, per, stride, off, gain, eps,
+                                                                               static_cast<__nv_bfloat16*>(out));
     else
-        rmsnorm_rows_kernel<float><<<grid, 256, 0, st>>>(in, d, M, per, stride, off, gain, eps,
-                                                         static_cast<float*>(out));
+        rmsnorm_rows_kernel<float><<<(unsigned)M, RN_THREADS, 0, st>>>(in, d, M, per, stride, off, gain, eps,
+                                                                       static_cast<float*>(out));
     return last_launch();
 }
 
