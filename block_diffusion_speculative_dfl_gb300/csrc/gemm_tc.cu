@@ -38,21 +38,44 @@ bool make_map(CUtensorMap* m, const void* base, int rows, int K, int box_rows) {
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BN, int EPI>
+template <int BN, int EPI, int CM>
 dfl_status launch(DeviceCtx* ctx, const GemmArgs& g, const GemmShape& sh, const CUtensorMap (&mb)[3],
                   const CUtensorMap& ma, cudaStream_t st, int slot) {
-    auto kern = gemm_tc_kernel<BN, EPI>;
+    auto kern = gemm_tc_kernel<BN, EPI, CM>;
     if (!ctx->gemm_attr_set[slot]) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, GemmCfg<BN>::SMEM) !=
             cudaSuccess)
             return DFL_ERR_CUDA;
+        if (CM > 1 && cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 0) != cudaSuccess)
+            return DFL_ERR_CUDA;
         ctx->gemm_attr_set[slot] = true;
     }
-    const int tiles = sh.tiles_m * sh.tiles_n;
-    const int grid = tiles < ctx->sm_count ? tiles : ctx->sm_count;
+    const int tiles = ((sh.tiles_m + CM - 1) / CM) * sh.tiles_n;
+    const int max_clusters = ctx->sm_count / CM;
+    const int grid = (tiles < max_clusters ? tiles : max_clusters) * CM;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(GEMM_THREADS);
+    cfg.dynamicSmemBytes = GemmCfg<BN>::SMEM;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CM;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const DevErr err = dev_err(ctx);
     ProfScope ps(g.tag ? g.tag : "gemm_tc", st);
-    kern<<<grid, GEMM_THREADS, GemmCfg<BN>::SMEM, st>>>(ma, mb[0], mb[1], mb[2], sh, g.ep, dev_err(ctx));
+    if (cudaLaunchKernelEx(&cfg, kern, ma, mb[0], mb[1], mb[2], sh, g.ep, err) != cudaSuccess) return DFL_ERR_CUDA;
     return last_launch();
+}
+
+template <int BN, int EPI>
+dfl_status launch_cm(DeviceCtx* ctx, const GemmArgs& g, const GemmShape& sh, const CUtensorMap (&mb)[3],
+                     const CUtensorMap& ma, cudaStream_t st, int slot, int cm) {
+    if (cm == 2) return launch<BN, EPI, 2>(ctx, g, sh, mb, ma, st, slot + 6);
+    return launch<BN, EPI, 1>(ctx, g, sh, mb, ma, st, slot);
 }
 
 }  // namespace
@@ -69,6 +92,9 @@ dfl_status gemm_tc(DeviceCtx* ctx, const GemmArgs& g, cudaStream_t st) {
     sh.num_kb = (g.K + GEMM_BK - 1) / GEMM_BK;
     sh.m_inner = g.m_inner;
     sh.nb = g.nb;
+    // Pair the M-tiles of each N-tile in 2-CTA clusters (B tile multicast) when
+    // there is more than one M-tile.
+    const int cm = sh.tiles_m >= 2 ? 2 : 1;
     CUtensorMap ma, mb[3];
     if (!make_map(&ma, g.A, g.M, g.K, GEMM_BM)) return DFL_ERR_CUDA;
     for (int j = 0; j < 3; ++j) {
@@ -76,18 +102,18 @@ dfl_status gemm_tc(DeviceCtx* ctx, const GemmArgs& g, cudaStream_t st) {
         if (!aligned16(g.B[jj])) return DFL_ERR_MISALIGNED;
         // every tile of BN columns must come from one B map
         if (j < g.nb && (g.b_begin[j] % g.bn != 0)) return DFL_ERR_UNSUPPORTED_SHAPE;
-        if (!make_map(&mb[j], g.B[jj], g.b_rows[jj], g.K, g.bn)) return DFL_ERR_CUDA;
+        if (!make_map(&mb[j], g.B[jj], g.b_rows[jj], g.K, g.bn / cm)) return DFL_ERR_CUDA;
         sh.b_begin[j] = g.b_begin[jj];
     }
     const int slot = (g.bn == 256 ? 0 : 3) + g.epi;
     if (g.bn == 256) {
-        if (g.epi == EPI_STORE) return launch<256, EPI_STORE>(ctx, g, sh, mb, ma, st, slot);
-        if (g.epi == EPI_RESID) return launch<256, EPI_RESID>(ctx, g, sh, mb, ma, st, slot);
-        return launch<256, EPI_ARGMAX>(ctx, g, sh, mb, ma, st, slot);
+        if (g.epi == EPI_STORE) return launch_cm<256, EPI_STORE>(ctx, g, sh, mb, ma, st, slot, cm);
+        if (g.epi == EPI_RESID) return launch_cm<256, EPI_RESID>(ctx, g, sh, mb, ma, st, slot, cm);
+        return launch_cm<256, EPI_ARGMAX>(ctx, g, sh, mb, ma, st, slot, cm);
     }
-    if (g.epi == EPI_STORE) return launch<128, EPI_STORE>(ctx, g, sh, mb, ma, st, slot);
-    if (g.epi == EPI_RESID) return launch<128, EPI_RESID>(ctx, g, sh, mb, ma, st, slot);
-    return launch<128, EPI_ARGMAX>(ctx, g, sh, mb, ma, st, slot);
+    if (g.epi == EPI_STORE) return launch_cm<128, EPI_STORE>(ctx, g, sh, mb, ma, st, slot, cm);
+    if (g.epi == EPI_RESID) return launch_cm<128, EPI_RESID>(ctx, g, sh, mb, ma, st, slot, cm);
+    return launch_cm<128, EPI_ARGMAX>(ctx, g, sh, mb, ma, st, slot, cm);
 }
 
 }  // namespace dfl

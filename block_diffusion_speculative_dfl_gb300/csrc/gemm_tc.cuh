@@ -69,9 +69,10 @@ struct GemmCfg {
     static constexpr int SMEM = 1024 + STAGES * (A_BYTES + B_BYTES) + BAR_BYTES;
 };
 
-__device__ __forceinline__ void tile_coords(const GemmShape& sh, int t, int& tm, int& tn) {
-    if (sh.m_inner) { tm = t % sh.tiles_m; tn = t / sh.tiles_m; }
-    else            { tn = t % sh.tiles_n; tm = t / sh.tiles_n; }
+// Tile t of a (tiles_mc x tiles_n) grid of cluster tiles, in walking order.
+__device__ __forceinline__ void tile_coords(const GemmShape& sh, int tiles_mc, int t, int& tmc, int& tn) {
+    if (sh.m_inner) { tmc = t % tiles_mc; tn = t / tiles_mc; }
+    else            { tn = t % sh.tiles_n; tmc = t / sh.tiles_n; }
 }
 
 __device__ __forceinline__ void store_bf16x32(void* dst, const float (&v)[32]) {
@@ -203,8 +204,16 @@ __device__ __forceinline__ void epi_argmax(const GemmShape& sh, const GemmEpi& e
 }
 
 // ------------------------------------------------------------------- kernel
+//
+// CM = 1: one CTA per output tile.  CM = 2: clusters of two CTAs own the two
+// M-tiles (2*tmc, 2*tmc + 1) of the same N-tile; the B tile they share is
+// loaded once, each CTA fetching half of it with TMA multicast into both
+// CTAs' shared memory, which halves each SM's B traffic from L2.  Every CTA
+// still issues its own cta_group::1 MMAs; a stage is refilled only after the
+// MMAs of both CTAs have released it (each CTA's commit arrives on both
+// CTAs' `empty` barrier).
 
-template <int BN, int EPI>
+template <int BN, int EPI, int CM>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmB2,
@@ -226,8 +235,13 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
+    const uint32_t crank = (CM > 1) ? cluster_ctarank() : 0u;
+    const int cid = blockIdx.x / CM, nclusters = gridDim.x / CM;
+    const int tiles_mc = (sh.tiles_m + CM - 1) / CM;
+    constexpr uint16_t kPair = (1u << CM) - 1u;
+
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
+        for (int s = 0; s < STAGES; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], CM); }
         for (int a = 0; a < 2; ++a) { mbar_init(&tfull[a], 1); mbar_init(&tempty[a], 128); }
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -241,10 +255,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     }
     if (warp == 1) { tmem_alloc(tmem_holder, Cfg::TMEM_COLS); tmem_relinquish(); }
     tc_fence_before();
-    __syncthreads();
+    if (CM > 1) cluster_sync(); else __syncthreads();   // peers' barriers are initialised before any multicast
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
-    const int total = sh.tiles_m * sh.tiles_n;
+    const int total = tiles_mc * sh.tiles_n;
 
     if (warp == 0) {
         if (lane == 0) {
@@ -253,10 +267,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             uint32_t phase = 0;
             uint32_t fills = 0;   // bit s: stage s has been filled at least once
             bool aborted = false;
-            for (int t = blockIdx.x; t < total && !aborted; t += gridDim.x) {
-                int tm, tn;
-                tile_coords(sh, t, tm, tn);
-                const int m0 = tm * GEMM_BM, n0 = tn * BN;
+            for (int t = cid; t < total && !aborted; t += nclusters) {
+                int tmc, tn;
+                tile_coords(sh, tiles_mc, t, tmc, tn);
+                const int m0 = (tmc * CM + (int)crank) * GEMM_BM, n0 = tn * BN;
                 const CUtensorMap* mb = &tmB0;
                 int nb0 = n0;
                 if (sh.nb > 2 && n0 >= sh.b_begin[2]) { mb = &tmB2; nb0 = n0 - sh.b_begin[2]; }
@@ -265,7 +279,12 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     if (*abort_flag || !mbar_wait(&empty[stage], phase ^ 1, err)) { aborted = true; break; }
                     mbar_arrive_expect_tx(&full[stage], Cfg::A_BYTES + Cfg::B_BYTES);
                     tma_load_2d(sA + stage * Cfg::A_BYTES, &tmA, kb * GEMM_BK, m0, &full[stage]);
-                    tma_load_2d(sB + stage * Cfg::B_BYTES, mb, kb * GEMM_BK, nb0, &full[stage]);
+                    if (CM == 1) {
+                        tma_load_2d(sB + stage * Cfg::B_BYTES, mb, kb * GEMM_BK, nb0, &full[stage]);
+                    } else {   // this CTA's share of the B tile, to every CTA of the cluster
+                        tma_load_2d_mc(sB + stage * Cfg::B_BYTES + crank * (Cfg::B_BYTES / CM), mb, kb * GEMM_BK,
+                                       nb0 + (int)crank * (BN / CM), &full[stage], kPair);
+                    }
                     fills |= 1u << stage;
                     if (++stage == STAGES) { stage = 0; phase ^= 1; }
                 }
@@ -292,7 +311,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             uint32_t acc_phase = 0;
             bool aborted = false;
             bool issued = false;
-            for (int t = blockIdx.x; t < total && !aborted; t += gridDim.x) {
+            for (int t = cid; t < total && !aborted; t += nclusters) {
                 if (*abort_flag || !mbar_wait(&tempty[acc], acc_phase ^ 1, err)) { aborted = true; break; }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
@@ -305,7 +324,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     for (int k = 0; k < GEMM_BK / 16; ++k)
                         mma_bf16(d_tmem, ad + 2 * k, bd + 2 * k, idesc, (kb | k) != 0);
                     issued = true;
-                    mma_commit(&empty[stage]);
+                    if (CM == 1) mma_commit(&empty[stage]);
+                    else mma_commit_mc(&empty[stage], kPair);
                     if (++stage == STAGES) { stage = 0; phase ^= 1; }
                 }
                 if (aborted) break;
@@ -326,14 +346,14 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         const int q = warp & 3;
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (int t = blockIdx.x; t < total; t += gridDim.x) {
+        for (int t = cid; t < total; t += nclusters) {
             if (__any_sync(0xFFFFFFFFu, *abort_flag != 0)) break;
             const bool ready = mbar_wait(&tfull[acc], acc_phase, err);
             if (!__all_sync(0xFFFFFFFFu, ready)) { *abort_flag = 1; break; }
             tc_fence_after();
-            int tm, tn;
-            tile_coords(sh, t, tm, tn);
-            const int row = tm * GEMM_BM + q * 32 + lane;
+            int tmc, tn;
+            tile_coords(sh, tiles_mc, t, tmc, tn);
+            const int row = (tmc * CM + (int)crank) * GEMM_BM + q * 32 + lane;
             const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
             if (EPI == EPI_STORE) epi_store<BN>(sh, ep, tbase, row, tn * BN);
             else if (EPI == EPI_RESID) epi_resid<BN>(sh, ep, tbase, row, tn * BN);
@@ -349,6 +369,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         tc_fence_after();
         tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
     }
+    if (CM > 1) cluster_sync();   // no CTA leaves while a peer may still arrive on its barriers
 }
 
 }  // namespace dfl

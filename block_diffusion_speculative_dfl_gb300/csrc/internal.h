@@ -15,7 +15,7 @@ struct DeviceCtx {
     int device = -1;
     int sm_count = 0;
     int* err_word = nullptr;       // device address of this device's error word
-    bool gemm_attr_set[8] = {};    // max-dynamic-smem set for gemm instantiations
+    bool gemm_attr_set[12] = {};   // max-dynamic-smem set for gemm instantiations
     bool mix_attr_set = false;
 };
 

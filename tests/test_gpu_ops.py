@@ -201,7 +201,8 @@ def _lm_case(N, B, d, V, seed, dtype="bf16"):
     return X, g, W
 
 
-@pytest.mark.parametrize("N,B,row0,d,V", [(3, 16, 1, 512, 1000), (2, 9, 1, 256, 5003), (1, 16, 0, 256, 256)])
+@pytest.mark.parametrize("N,B,row0,d,V", [(3, 16, 1, 512, 1000), (2, 9, 1, 256, 5003), (1, 16, 0, 256, 256),
+                                            (10, 16, 1, 256, 3000), (20, 16, 1, 256, 1000)])
 def test_lm_head_argmax_bf16(N, B, row0, d, V):
     X, g, W = _lm_case(N, B, d, V, seed=V)
     nr = B - row0
