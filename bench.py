@@ -43,6 +43,7 @@ def parse_args(argv=None):
     p.add_argument("--workload", default="qwen3_8b_drafter")
     p.add_argument("--batch", type=int, default=0,
                    help="override sequences per GPU (a smaller case of the same kernels, e.g. for ncu)")
+    p.add_argument("--context", type=int, default=0, help="override the context length (smaller case, e.g. for ncu)")
     p.add_argument("--e2e-steps", type=int, default=3)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -190,12 +191,14 @@ class ClockSampler:
 
 # -------------------------------------------------------------- workloads --
 
-def workload(name, rank=0, batch=0):
+def workload(name, rank=0, batch=0, context=0):
     import dataclasses
     from dfl_synth import WORKLOADS
     w = WORKLOADS[name]
     if batch:
         w = dataclasses.replace(w, N=batch)
+    if context:
+        w = dataclasses.replace(w, C=context)
     if rank:   # every rank drafts its own batch of sequences (weak scaling)
         w = dataclasses.replace(w, seed=w.seed + 1000 * rank)
     return w
@@ -258,7 +261,7 @@ def run_ours(args, rank, world, local):
     dist_init(world, "nccl")
     dfl.build()
     dfl.load()
-    w = workload(args.workload, rank, args.batch)
+    w = workload(args.workload, rank, args.batch, args.context)
     p = host_params(w)
     shape = dfl.DraftShape(N=w.N, d=w.d, Hq=w.Hq, Hkv=w.Hkv, hd=w.hd, D=w.D, L=w.L, B=w.B, C=w.C, V=w.V,
                            dtype=w.dtype, K=w.K, T=w.T, seed=w.philox_seed, eps=w.eps, rope_theta=w.rope_theta)
@@ -383,7 +386,7 @@ def run_reference(args, rank, world):
     if rank != 0:
         return
     from dfl_synth import bits_to_f32, gen_verifier_logits
-    w = workload(args.workload, 0, args.batch)
+    w = workload(args.workload, 0, args.batch, args.context)
     p = host_params(w)
     W_lm = bits_to_f32(p["W_lm_bits"]) if w.V > 0 else None
     times = []

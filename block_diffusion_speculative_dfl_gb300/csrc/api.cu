@@ -253,7 +253,7 @@ extern "C" dfl_status dfl_dual_kv_proj(const void* Xc, const float* Xb, int32_t 
         g.B[0] = Wq; g.B[1] = Wkb; g.B[2] = Wvb;
         g.b_rows[0] = qd; g.b_rows[1] = kv; g.b_rows[2] = kv;
         g.b_begin[0] = 0; g.b_begin[1] = qd; g.b_begin[2] = qd + kv; g.nb = 3; g.N = qd + 2 * kv;
-        g.bn = 128;
+        g.bn = 0;   // chosen per shape
         g.m_inner = 1;
         g.epi = EPI_STORE;
         g.ep.seg[0] = GemmSeg{Q, 0, qd, rope != nullptr};
@@ -302,7 +302,7 @@ extern "C" dfl_status dfl_block_attn(const void* Q, const void* Kc, const void* 
     GemmArgs g{};   // Xb += O Wo^T
     g.A = O; g.M = N * B; g.K = qd;
     g.B[0] = Wo; g.b_rows[0] = d; g.b_begin[0] = 0; g.nb = 1; g.N = d;
-    g.bn = 128;
+    g.bn = 0;   // chosen per shape
     g.m_inner = 1;
     g.epi = EPI_RESID;
     g.ep.resid = Xb; g.ep.ld_resid = d;

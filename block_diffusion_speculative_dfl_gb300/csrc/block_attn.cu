@@ -39,7 +39,8 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, int sr
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" :: "r"(dst), "l"(src), "r"(src_bytes) : "memory");
 }
 __device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory"); }
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
@@ -57,7 +58,8 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], 
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-template <int HD>
+// ST: K/V stages in the ring (ST - 1 tiles in flight while one is used).
+template <int HD, int ST>
 __global__ void __launch_bounds__(ATT_MAX_WARPS * 32) attn_bf16_kernel(const AttnArgs a) {
     constexpr int CH = HD / 8;        // 16-byte chunks per row
     constexpr int ROWB = HD * 2;
@@ -113,6 +115,10 @@ __global__ void __launch_bounds__(ATT_MAX_WARPS * 32) attn_bf16_kernel(const Att
     };
     load_tile(0, 0);
     cp_commit();
+    if (ST == 3) {
+        if (ntiles > 1) load_tile(1, 1);
+        cp_commit();
+    }
 
     uint32_t qf[HD / 16][4];
     float o[HD / 8][4];
@@ -121,10 +127,10 @@ __global__ void __launch_bounds__(ATT_MAX_WARPS * 32) attn_bf16_kernel(const Att
     float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};
 
     for (int t = 0; t < ntiles; ++t) {
-        const int s = t & 1;
-        if (t + 1 < ntiles) load_tile(t + 1, s ^ 1);
+        const int s = t % ST;
+        if (t + ST - 1 < ntiles) load_tile(t + ST - 1, (t + ST - 1) % ST);
         cp_commit();
-        cp_wait1();
+        cp_wait<ST - 1>();
         __syncthreads();
         if (t == 0) {
             #pragma unroll
@@ -261,23 +267,31 @@ __global__ void attn_combine_kernel(const float* Opart, const float* lse, int S,
     }
 }
 
-int attn_smem(int NW, int hd) { return 128 + NW * 16 * hd * 2 + 2 * 2 * KT * hd * 2; }
+int attn_smem(int NW, int hd, int st) { return 128 + NW * 16 * hd * 2 + st * 2 * KT * hd * 2; }
 
 }  // namespace
 
-// Splits of the key range: enough CTAs for ~2 per SM of a 152-SM GB300, each
-// split at least one 64-key tile, at most 64 splits (the combine keeps two
-// split weights per lane).  Depends on the shape only, so workspace sizes do
-// not depend on the device.
+// Splits of the key range.  Model of the makespan on a 152-SM GB300 with two
+// CTAs per SM: (rounds of CTAs over the 304 slots) x (64-key tiles per split
+// + ~1.5 tiles of fixed per-CTA cost: Q load, pipeline fill, partial
+// write-out, combine); the smallest S at the minimum wins.  At most 64 splits
+// (the combine keeps two split weights per lane).  Depends on the shape only,
+// so workspace sizes do not depend on the device.
 int attn_splits(int N, int C, int B, int Hkv) {
     const int units = N * Hkv;
     const int tiles = (C + B + KT - 1) / KT;
-    int S = (304 + units - 1) / units;
-    if (S < 1) S = 1;
-    if (S > tiles) S = tiles;
-    if (S > 64) S = 64;
-    const int per = (tiles + S - 1) / S;
-    return (tiles + per - 1) / per;
+    const int slots = 304;
+    int best_s = 1;
+    double best = 1e30;
+    for (int S = 1; S <= 64 && S <= tiles; ++S) {
+        const int per = (tiles + S - 1) / S;
+        const int s_eff = (tiles + per - 1) / per;
+        if (s_eff != S) continue;
+        const double rounds = (double)((units * S + slots - 1) / slots);
+        const double cost = rounds * (per + 1.5);
+        if (cost < best - 1e-9) { best = cost; best_s = S; }
+    }
+    return best_s;
 }
 
 size_t attn_ws_bytes(int N, int C, int B, int Hq, int Hkv, int hd) {
@@ -310,24 +324,23 @@ dfl_status attn_bf16(const void* Q, const void* Kc, const void* Vc, const void* 
     int NW = (a.R + 15) / 16;
     const int zblocks = (NW + ATT_MAX_WARPS - 1) / ATT_MAX_WARPS;
     NW = (NW + zblocks - 1) / zblocks;
-    const int smem = attn_smem(NW, hd);
+    // three stages if two CTAs still fit on an SM, else two
+    const int stages = 2 * (attn_smem(NW, hd, 3) + 1024) <= 228 * 1024 ? 3 : 2;
+    const int smem = attn_smem(NW, hd, stages);
     dim3 grid(N * Hkv, a.S, zblocks);
     dfl_status rc;
     {
     ProfScope ps("attn_bf16", st);
-    if (hd == 128) {
-        if (cudaFuncSetAttribute(attn_bf16_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
-            cudaSuccess)
-            return DFL_ERR_CUDA;
-        attn_bf16_kernel<128><<<grid, NW * 32, smem, st>>>(a);
-    } else if (hd == 64) {
-        if (cudaFuncSetAttribute(attn_bf16_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
-            cudaSuccess)
-            return DFL_ERR_CUDA;
-        attn_bf16_kernel<64><<<grid, NW * 32, smem, st>>>(a);
-    } else {
-        return DFL_ERR_UNSUPPORTED_SHAPE;
-    }
+    auto run = [&](auto kern) -> bool {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return false;
+        kern<<<grid, NW * 32, smem, st>>>(a);
+        return true;
+    };
+    bool ok;
+    if (hd == 128) ok = stages == 3 ? run(attn_bf16_kernel<128, 3>) : run(attn_bf16_kernel<128, 2>);
+    else if (hd == 64) ok = stages == 3 ? run(attn_bf16_kernel<64, 3>) : run(attn_bf16_kernel<64, 2>);
+    else return DFL_ERR_UNSUPPORTED_SHAPE;
+    if (!ok) return DFL_ERR_CUDA;
     rc = last_launch();
     }
     if (rc != DFL_OK || a.S == 1) return rc;

@@ -80,7 +80,28 @@ dfl_status launch_cm(DeviceCtx* ctx, const GemmArgs& g, const GemmShape& sh, con
 
 }  // namespace
 
-dfl_status gemm_tc(DeviceCtx* ctx, const GemmArgs& g, cudaStream_t st) {
+// Tile width for bn == 0: the one that minimises (rounds of cluster tiles
+// over the persistent grid) x (tile width) -- i.e. the time of the busiest
+// SM when every tile costs ~its width -- preferring 256 on ties; 256 needs
+// every B segment to start on a 256-column boundary.
+static int pick_bn(const GemmArgs& g, int sm_count) {
+    bool ok256 = true;
+    for (int j = 0; j < g.nb; ++j) ok256 = ok256 && (g.b_begin[j] % 256 == 0);
+    if (!ok256) return 128;
+    const int tiles_m = (g.M + GEMM_BM - 1) / GEMM_BM;
+    const int cm = tiles_m >= 2 ? 2 : 1;
+    const int tiles_mc = (tiles_m + cm - 1) / cm;
+    const int clusters = sm_count / cm;
+    auto cost = [&](int bn) {
+        const int tiles = tiles_mc * ((g.N + bn - 1) / bn);
+        return (long)((tiles + clusters - 1) / clusters) * bn;
+    };
+    return cost(256) <= cost(128) ? 256 : 128;
+}
+
+dfl_status gemm_tc(DeviceCtx* ctx, const GemmArgs& g_in, cudaStream_t st) {
+    GemmArgs g = g_in;
+    if (g.bn == 0) g.bn = pick_bn(g, ctx->sm_count);
     if (g.M <= 0 || g.N <= 0 || g.K <= 0) return DFL_ERR_INVALID_ARG;
     if (g.K % 8 != 0 || !aligned16(g.A)) return DFL_ERR_MISALIGNED;
     if (g.bn != 128 && g.bn != 256) return DFL_ERR_UNSUPPORTED_SHAPE;
