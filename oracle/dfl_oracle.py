@@ -384,3 +384,75 @@ def tv_acceptance(P, Q) -> float:
     P = np.asarray(P, dtype=F64)
     Q = np.asarray(Q, dtype=F64)
     return 1.0 - 0.5 * np.sum(np.abs(P - Q))
+
+
+# ---------------------------------------------------------------------------
+# TV acceptance diagnostic and lossless stochastic acceptance (SpecDiff-2
+# notes, "Streak-Distillation"; DFlare post, "Generating candidates in
+# parallel, the target decides acceptance")
+# ---------------------------------------------------------------------------
+
+def softmax_t(z, T: float = 1.0) -> np.ndarray:
+    """softmax(z / T) in fp64."""
+    z = np.asarray(z, dtype=F64) / T
+    e = np.exp(z - z.max())
+    return e / e.sum()
+
+
+def tv_alpha(z_row, T: float, v_row) -> float:
+    """Per-position acceptance proxy alpha = 1 - TV(P, Q).
+
+    Q = softmax(z / T) is the drafter's marginal at the position (the
+    distribution the draft token is drawn from), P = softmax(v) the
+    verifier's distribution there; alpha = 1 - 1/2 sum_x |P(x) - Q(x)|
+    (SpecDiff-2 notes, "Streak-Distillation": the acceptance proxy).
+    """
+    return tv_acceptance(softmax_t(v_row), softmax_t(z_row, T))
+
+
+def draw_uniform_stream(seed: int, n: int, j: int, k: int, stream: int) -> float:
+    """u from Philox counter (n, j, k, stream): stream 0 draws the drafts,
+    1 the acceptance tests, 2 the residual / bonus samples."""
+    x0 = philox4x32_10((n, j, k, stream), (seed & _MASK32, (seed >> 32) & _MASK32))[0]
+    return ((x0 >> 8) + 0.5) * 2.0 ** -24
+
+
+def inverse_cdf(w, u: float):
+    """Smallest index whose cumulative weight exceeds u * total (weights >= 0),
+    and the distance of u * total to the nearest boundary / total."""
+    w = np.asarray(w, dtype=F64)
+    cdf = np.cumsum(w)
+    total = cdf[-1]
+    t = u * total
+    v = min(int(np.searchsorted(cdf, t, side="right")), len(w) - 1)
+    lo = cdf[v - 1] if v > 0 else 0.0
+    return v, min(abs(t - lo), abs(cdf[v] - t)) / total
+
+
+def speculative_accept(z_rows, T: float, v_rows, x, u_acc, u_res):
+    """Lossless stochastic acceptance of one draft x_1..x_G.
+
+    Position j (1-based) is accepted with probability min(1, P_j(x_j) /
+    Q_j(x_j)), i.e. when u_acc[j] * Q_j(x_j) < P_j(x_j), with Q_j =
+    softmax(z_j / T) the drafter's marginal and P_j = softmax(v_j) the
+    verifier's.  At the first rejection the next token is drawn from the
+    residual max(0, P_j - Q_j) (normalised) with u_res[j]; if all G are
+    accepted the bonus token is drawn from P_{G+1} with u_res[G].  This keeps
+    the verifier's distribution (the DFlare post's "proper acceptance
+    procedure" for stochastic decoding).  Returns (accepted, token, margin):
+    margin is the relative distance of the deciding test or draw to its
+    boundary (how close floating point came to changing the result).
+    """
+    G = len(x)
+    for j in range(G):
+        Q = softmax_t(z_rows[j], T)
+        P = softmax_t(v_rows[j])
+        q, p = Q[x[j]], P[x[j]]
+        if u_acc[j] * q < p:
+            continue
+        acc_margin = abs(u_acc[j] * q - p) / max(p, 1e-300)
+        r = np.maximum(P - Q, 0.0)
+        y, m = inverse_cdf(r, u_res[j])
+        return j, y, min(acc_margin, m)
+    y, m = inverse_cdf(softmax_t(v_rows[G]), u_res[G])
+    return G, y, m

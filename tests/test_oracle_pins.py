@@ -520,3 +520,83 @@ def test_self_select_ties_take_lowest_draft():
     drafts = np.array([[1, 2], [1, 2], [0, 0]])
     scores, ks, _, _ = orc.self_select(vlog, drafts)
     assert scores[0] == scores[1] == scores[2] and ks == 0
+
+
+# ------------------------------------------------ stochastic acceptance --
+
+def test_tv_alpha_matches_closed_form_and_limits():
+    rng = np.random.default_rng(30)
+    z, v = rng.normal(size=12), rng.normal(size=12) * 2
+    P = np.exp(v) / np.exp(v).sum()
+    Q = np.exp(z / 1.5) / np.exp(z / 1.5).sum()
+    assert abs(orc.tv_alpha(z, 1.5, v) - np.minimum(P, Q).sum()) < 1e-14
+    assert abs(orc.tv_alpha(v, 1.0, v) - 1.0) < 1e-14          # identical distributions
+    zz = np.full(4, -1e3); zz[0] = 1e3
+    vv = np.full(4, -1e3); vv[1] = 1e3
+    assert abs(orc.tv_alpha(zz, 1.0, vv)) < 1e-12                # disjoint supports
+
+
+def test_inverse_cdf_grid_and_margin():
+    w = np.array([1.0, 0.0, 3.0])
+    assert orc.inverse_cdf(w, 0.1)[0] == 0 and orc.inverse_cdf(w, 0.3)[0] == 2
+    assert orc.inverse_cdf(w, 0.25)[1] == 0.0                    # exactly on a boundary
+
+
+def _spec_output_distribution(z, T, v, n_grid=400):
+    """Distribution of the first committed token, by exact enumeration over the
+    draft token and midpoint grids of both uniforms (G = 1)."""
+    V = len(z)
+    Q = orc.softmax_t(z, T)
+    out = np.zeros(V)
+    grid = (np.arange(n_grid) + 0.5) / n_grid
+    for x in range(V):
+        for ua in grid:
+            # token committed at position 1: x if accepted, else the residual draw
+            acc, y, _ = orc.speculative_accept([z], T, [v, v], [x], [ua], [0.0, 0.0])
+            if acc == 1:
+                out[x] += Q[x] / n_grid
+            else:
+                for ur in grid:
+                    _, y, _ = orc.speculative_accept([z], T, [v, v], [x], [ua], [ur, 0.0])
+                    out[y] += Q[x] / n_grid / n_grid
+    return out
+
+
+def test_speculative_accept_keeps_the_verifier_distribution():
+    # Lossless property: the first committed token is distributed as P_1,
+    # whatever the drafter's Q (up to the discretisation of the uniforms).
+    rng = np.random.default_rng(31)
+    z, v = rng.normal(size=4) * 1.5, rng.normal(size=4)
+    out = _spec_output_distribution(z, 1.3, v)
+    assert np.allclose(out, orc.softmax_t(v), atol=6e-3)
+
+
+def test_speculative_accept_rate_is_the_tv_proxy():
+    # P(accept position 1) = sum_x Q(x) min(1, P(x)/Q(x)) = sum_x min(P, Q) = alpha.
+    rng = np.random.default_rng(32)
+    z, v = rng.normal(size=5), rng.normal(size=5)
+    Q = orc.softmax_t(z, 1.0)
+    grid = (np.arange(2000) + 0.5) / 2000
+    rate = sum(Q[x] * np.mean([orc.speculative_accept([z], 1.0, [v, v], [x], [u], [0.5, 0.5])[0] == 1
+                               for u in grid]) for x in range(5))
+    assert abs(rate - orc.tv_alpha(z, 1.0, v)) < 2e-3
+
+
+def test_speculative_accept_prefix_and_bonus():
+    # Draft that the verifier is certain of: every position accepted, bonus
+    # drawn from the last row; a draft the verifier gives no mass: rejected at 1
+    # and the residual draw lands on the verifier's token.
+    V = 6
+    z = np.zeros(V)
+    v_sure = np.full(V, -1e4); v_sure[2] = 0.0
+    v_last = np.full(V, -1e4); v_last[5] = 0.0
+    acc, y, _ = orc.speculative_accept([z, z], 1.0, [v_sure, v_sure, v_last], [2, 2], [0.99, 0.99], [0.3, 0.3, 0.3])
+    assert (acc, y) == (2, 5)
+    acc, y, _ = orc.speculative_accept([z, z], 1.0, [v_sure, v_sure, v_last], [4, 2], [0.01, 0.5], [0.7, 0.3, 0.3])
+    assert (acc, y) == (0, 2)
+
+
+def test_uniform_streams_are_distinct():
+    a = orc.draw_uniform_stream(7, 1, 2, 0, 0)
+    assert a == orc.draw_uniform(7, 1, 2, 0)
+    assert len({orc.draw_uniform_stream(7, 1, 2, 0, s) for s in range(3)}) == 3
