@@ -15,13 +15,14 @@ DFL_OK, DFL_ERR_INVALID_ARG, DFL_ERR_UNSUPPORTED_SHAPE, DFL_ERR_MISALIGNED = 0, 
 DFL_ERR_WORKSPACE, DFL_ERR_CUDA, DFL_ERR_TIMEOUT, DFL_ERR_NO_DEVICE = 4, 5, 6, 7
 DFL_F32, DFL_BF16 = 0, 1
 DFL_OP_DUAL_KV_PROJ, DFL_OP_BLOCK_ATTN, DFL_OP_LM_HEAD, DFL_OP_SELF_SELECT, DFL_OP_DRAFT_STEP = 1, 2, 3, 4, 5
+DFL_OP_TV_ACCEPTANCE, DFL_OP_SPEC_ACCEPT = 6, 7
 
 # Every function the header declares; tests check each is exported.
 EXPORTED = ("dfl_version", "dfl_status_string", "dfl_workspace_size", "dfl_rope_table",
             "dfl_layer_mix_rmsnorm", "dfl_dual_kv_proj", "dfl_block_attn", "dfl_lm_head_argmax",
             "dfl_greedy_accept", "dfl_self_select", "dfl_draft_step", "dfl_get_device_error",
             "dfl_set_wait_limit_ns", "dfl_selftest_bounded_wait", "dfl_profile_enable", "dfl_profile_report",
-            "dfl_self_select_noalloc")
+            "dfl_self_select_noalloc", "dfl_tv_acceptance", "dfl_spec_accept")
 
 
 class DflError(RuntimeError):
@@ -76,6 +77,8 @@ _SIGS = {
     "dfl_profile_enable": ([_I32], _I32),
     "dfl_profile_report": ([C.c_char_p, _SZ, C.POINTER(_I32)], _I32),
     "dfl_self_select_noalloc": ([_P, _I32, _P, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _P], _I32),
+    "dfl_tv_acceptance": ([_P, _F, _P, _I32, _I32, _I32, _I32, _I32, _P, _P, _P, _SZ, _P], _I32),
+    "dfl_spec_accept": ([_P, _F, _P, _I32, _P, _P, _I32, _I32, _I32, _I32, C.c_uint64, _P, _P, _P, _SZ, _P], _I32),
 }
 
 _lib = None
@@ -218,3 +221,16 @@ def dfl_self_select_noalloc(vlog, dt, drafts, N, K, G, V, scores, selected, acce
     _check("dfl_self_select_noalloc",
            load().dfl_self_select_noalloc(ptr(vlog), dt, ptr(drafts), N, K, G, V, ptr(scores), ptr(selected),
                                           ptr(accept_len), ptr(bonus), _stream(stream)))
+
+
+def dfl_tv_acceptance(logits, T, vlog, dt, N, K, G, V, alpha, tokens_per_draft, ws, ws_bytes, stream=None):
+    _check("dfl_tv_acceptance",
+           load().dfl_tv_acceptance(ptr(logits), T, ptr(vlog), dt, N, K, G, V, ptr(alpha), ptr(tokens_per_draft),
+                                    ptr(ws), ws_bytes, _stream(stream)))
+
+
+def dfl_spec_accept(logits, T, vlog, dt, drafts, sel, N, K, G, V, seed, accept_len, next_token, ws, ws_bytes,
+                    stream=None):
+    _check("dfl_spec_accept",
+           load().dfl_spec_accept(ptr(logits), T, ptr(vlog), dt, ptr(drafts), ptr(sel), N, K, G, V, seed,
+                                  ptr(accept_len), ptr(next_token), ptr(ws), ws_bytes, _stream(stream)))

@@ -104,6 +104,8 @@ extern "C" size_t dfl_workspace_size(dfl_op op, const dfl_shape* s) {
             if (s->row0 < 0 || s->row0 >= s->B || s->V <= 0) return 0;
             return ws_lm_head(s->N, s->B, s->row0, s->d, s->V, s->dtype, s->dtype == DFL_F32);
         case DFL_OP_SELF_SELECT: return al256(select_ws_bytes(s->N, s->K, s->G));
+        case DFL_OP_TV_ACCEPTANCE: return tv_ws_bytes(s->N, s->K, s->G);
+        case DFL_OP_SPEC_ACCEPT: return spec_ws_bytes(s->N, s->G);
         case DFL_OP_DRAFT_STEP: {
             const size_t e = esz(s->dtype);
             size_t b = al256((size_t)s->D * s->N * s->C * s->d * e);                 // Xc, all layers

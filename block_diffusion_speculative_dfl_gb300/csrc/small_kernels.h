@@ -33,6 +33,10 @@ size_t attn_ws_bytes(int N, int C, int B, int Hq, int Hkv, int hd);
 dfl_status attn_bf16(const void* Q, const void* Kc, const void* Vc, const void* Kb, const void* Vb, int N, int C,
                      int B, int Hq, int Hkv, int hd, void* O, void* ws, cudaStream_t st);
 
+// TV acceptance diagnostic and stochastic acceptance (workspace bytes)
+size_t tv_ws_bytes(int N, int K, int G);
+size_t spec_ws_bytes(int N, int G);
+
 // self-selection
 size_t select_ws_bytes(int N, int K, int G);
 dfl_status self_select_run(const void* vlog, bool bf16, const int32_t* drafts, int N, int K, int G, int V,

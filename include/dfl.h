@@ -80,7 +80,9 @@ typedef enum dfl_op {
     DFL_OP_BLOCK_ATTN = 2,
     DFL_OP_LM_HEAD = 3,
     DFL_OP_SELF_SELECT = 4,
-    DFL_OP_DRAFT_STEP = 5
+    DFL_OP_DRAFT_STEP = 5,
+    DFL_OP_TV_ACCEPTANCE = 6,
+    DFL_OP_SPEC_ACCEPT = 7
 } dfl_op;
 
 /* Library version string (static storage). */
@@ -260,6 +262,48 @@ dfl_status dfl_self_select_noalloc(const void* vlog, dfl_dtype dt, const int32_t
                                    int32_t N, int32_t K, int32_t G, int32_t V, float* scores,
                                    int32_t* selected, int32_t* accept_len, int32_t* bonus,
                                    dfl_stream stream);
+
+/*
+ * dfl_tv_acceptance -- per-position acceptance proxy of K drafts.
+ *   SpecDiff-2 notes, "Streak-Distillation": alpha = 1 - 1/2 sum_x |P(x) -
+ *   Q(x)| with Q = softmax(z_j / T) the drafter's marginal at window position
+ *   j and P = softmax(vlog[n][k][j]) the verifier's distribution there given
+ *   draft k's prefix; the expected accepted length of draft k under the
+ *   streak equation is sum_m prod_{j<=m} alpha_j.
+ *   logits  in, fp32 [N*G][V] (the drafter's rows, as from dfl_lm_head_argmax)
+ *   vlog    in, dt [N][K][G+1][V]
+ *   alpha   out, fp32 [N][K][G]; tokens_per_draft out (nullable) fp32 [N][K]
+ *   ws      dfl_workspace_size(DFL_OP_TV_ACCEPTANCE) bytes (row log-sum-exps)
+ *   Errors: INVALID_ARG (K outside 1..64, G outside 1..1024, T <= 0),
+ *   WORKSPACE.
+ */
+dfl_status dfl_tv_acceptance(const float* logits, float T, const void* vlog, dfl_dtype dt,
+                             int32_t N, int32_t K, int32_t G, int32_t V, float* alpha,
+                             float* tokens_per_draft, void* ws, size_t ws_bytes,
+                             dfl_stream stream);
+
+/*
+ * dfl_spec_accept -- lossless stochastic acceptance of one draft per sequence.
+ *   DFlare post, "Generating candidates in parallel, the target decides
+ *   acceptance": stochastic decoding needs an acceptance rule that keeps the
+ *   target's distribution.  For j = 1..G: accept x_j when u_j Q(x_j) <
+ *   P(x_j) (probability min(1, P/Q)), Q = softmax(z_j / T), P =
+ *   softmax(v_j); at the first rejection the next token is drawn from the
+ *   normalised residual max(0, P - Q); after G acceptances the bonus token is
+ *   drawn from P_{G+1}.  Uniforms: u = ((x0 >> 8) + 1/2) 2^-24 from
+ *   Philox4x32-10 at counter (n, j, 0, 1) for the tests and (n, j, 0, 2) for
+ *   the draw, key (seed lo, seed hi).
+ *   logits  in, fp32 [N*G][V]; vlog in, dt [N][K][G+1][V]
+ *   drafts  in, int32 [N][K][G]; sel in, int32 [N] draft to verify (nullable:
+ *           draft 0); a token outside [0, V) is rejected
+ *   accept_len out, int32 [N] (accepted drafts, 0..G); next_token out, int32 [N]
+ *   ws      dfl_workspace_size(DFL_OP_SPEC_ACCEPT) bytes
+ *   Errors: INVALID_ARG, WORKSPACE.
+ */
+dfl_status dfl_spec_accept(const float* logits, float T, const void* vlog, dfl_dtype dt,
+                           const int32_t* drafts, const int32_t* sel, int32_t N, int32_t K,
+                           int32_t G, int32_t V, uint64_t seed, int32_t* accept_len,
+                           int32_t* next_token, void* ws, size_t ws_bytes, dfl_stream stream);
 
 /* One draft layer's weights (device pointers, dtype of the step). */
 typedef struct dfl_layer_weights {
