@@ -44,6 +44,9 @@ def parse_args(argv=None):
     p.add_argument("--batch", type=int, default=0,
                    help="override sequences per GPU (a smaller case of the same kernels, e.g. for ncu)")
     p.add_argument("--context", type=int, default=0, help="override the context length (smaller case, e.g. for ncu)")
+    p.add_argument("--tv", action="store_true", help="self-selection workloads: add the TV acceptance proxy")
+    p.add_argument("--accept-rule", choices=["greedy", "stochastic"], default="greedy",
+                   help="self-selection workloads: acceptance of the selected draft")
     p.add_argument("--e2e-steps", type=int, default=3)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -147,7 +150,9 @@ def kernel_work(w):
         M = N * (B - 1)
         work["gemm_lm_head"] = (2.0 * M * V * d, 2.0 * (M * d + V * d) + (4.0 * M * V if w.K > 0 else 0.0))
     if w.K > 0:
+        G = B - 1
         work["verifier_row_stats"] = (0.0, 2.0 * N * w.K * B * V)
+        work["tv_alpha"] = (0.0, 4.0 * N * G * V + 2.0 * N * w.K * G * V)
     return work
 
 
@@ -266,7 +271,9 @@ def run_ours(args, rank, world, local):
     shape = dfl.DraftShape(N=w.N, d=w.d, Hq=w.Hq, Hkv=w.Hkv, hd=w.hd, D=w.D, L=w.L, B=w.B, C=w.C, V=w.V,
                            dtype=w.dtype, K=w.K, T=w.T, seed=w.philox_seed, eps=w.eps, rope_theta=w.rope_theta)
     W_lm = (torch.from_numpy(p["W_lm_bits"].view(np.int16)).view(torch.bfloat16) if w.V > 0 else None)
-    model = dfl.DraftModel(shape, p["mix"], p["g_mix"], p["g_blk"], p["g_fin"], p["layers"], W_lm)
+    model = dfl.DraftModel(shape, p["mix"], p["g_mix"], p["g_blk"], p["g_fin"], p["layers"], W_lm,
+                           tv=args.tv and w.K > 0, accept_rule=1 if (args.accept_rule == "stochastic" and w.K > 0) else 0,
+                           accept_seed=w.philox_seed ^ 0xACCE97)
     H_host = torch.from_numpy(gen_hidden(w, as_bits=True).view(np.int16)).view(torch.bfloat16)
     X_host = torch.from_numpy(gen_block_init(w))
     H, X0 = H_host.cuda(), X_host.cuda()
@@ -372,6 +379,9 @@ def run_ours(args, rank, world, local):
                 "config": {"workload": w.name, "N_per_gpu": w.N, "d": w.d, "Hq": w.Hq, "Hkv": w.Hkv, "hd": w.hd,
                            "draft_layers": w.D, "target_layers": w.L, "block": w.B, "context": w.C, "vocab": w.V,
                            "K": w.K, "T": w.T, "parallelism": f"replicas x{world}",
+                           "epilogue": ("self-selection" + (" + TV proxy" if args.tv else "") +
+                                        (" + stochastic acceptance" if args.accept_rule == "stochastic" else
+                                         " + greedy acceptance")) if w.K > 0 else "greedy acceptance",
                            "l2": "inputs larger than L2 and a 256 MB L2 flush between timed steps"},
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
                 "clocks": clk, "kernels": kernels}

@@ -52,7 +52,8 @@ class StepArgs(C.Structure):
                 [(n, C.c_void_p) for n in ("W_lm", "Xb0", "Xb", "draft", "logits", "target", "accept_len",
                                            "bonus")] +
                 [("sample", C.POINTER(SampleParams))] +
-                [(n, C.c_void_p) for n in ("samples", "vlog", "scores", "selected")])
+                [(n, C.c_void_p) for n in ("samples", "vlog", "scores", "selected", "tv_alpha", "tv_tokens")] +
+                [("accept_rule", C.c_int32), ("accept_seed", C.c_uint64)])
 
 
 _P, _I32, _I64, _F, _D, _SZ = C.c_void_p, C.c_int32, C.c_int64, C.c_float, C.c_double, C.c_size_t

@@ -64,35 +64,62 @@ __device__ __forceinline__ const void* row_ptr(const RowMap& m, int64_t r, int V
     return static_cast<const uint8_t*>(m.base) + off * (BF16 ? 2 : 4);
 }
 
-// lse[r] = log sum_x exp(scale * row[x]); one CTA per row, online rescaling.
+// 8 consecutive elements of a row (16-byte loads; row 16-byte aligned).
+template <bool BF16>
+__device__ __forceinline__ void load8(const void* row, int c, float (&x)[8]) {
+    if constexpr (BF16) {
+        const uint4 u = reinterpret_cast<const uint4*>(row)[c];
+        x[0] = bf16lo(u.x); x[1] = bf16hi(u.x); x[2] = bf16lo(u.y); x[3] = bf16hi(u.y);
+        x[4] = bf16lo(u.z); x[5] = bf16hi(u.z); x[6] = bf16lo(u.w); x[7] = bf16hi(u.w);
+    } else {
+        const float4 a = reinterpret_cast<const float4*>(row)[2 * c], b = reinterpret_cast<const float4*>(row)[2 * c + 1];
+        x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+    }
+}
+
+__device__ __forceinline__ void lse_merge(float& m, float& s, float m2, float s2) {
+    const float M = fmaxf(m, m2);
+    s = (m == -INFINITY ? 0.f : s * expf(m - M)) + (m2 == -INFINITY ? 0.f : s2 * expf(m2 - M));
+    m = M;
+}
+
+// lse[r] = log sum_x exp(scale * row[x]); one CTA per row, online rescaling,
+// 16-byte loads when V is a multiple of 8.
 template <bool BF16>
 __global__ void __launch_bounds__(XT) row_lse_kernel(RowMap m, int V, float scale, float* lse) {
     const int64_t r = blockIdx.x;
     const void* row = row_ptr<BF16>(m, r, V);
     float mx = -INFINITY, s = 0.f;
-    for (int i = threadIdx.x; i < V; i += XT) {
-        const float x = elem<BF16>(row, i) * scale;
-        if (x > mx) { s = (mx == -INFINITY ? 0.f : s * expf(mx - x)); mx = x; }
-        s += expf(x - mx);
+    if ((V & 7) == 0) {
+        for (int c = threadIdx.x; c < V / 8; c += XT) {
+            float x[8];
+            load8<BF16>(row, c, x);
+            float cm = x[0] * scale;
+            #pragma unroll
+            for (int q = 1; q < 8; ++q) cm = fmaxf(cm, x[q] * scale);
+            if (cm > mx) { s = (mx == -INFINITY ? 0.f : s * expf(mx - cm)); mx = cm; }
+            float a = 0.f;
+            #pragma unroll
+            for (int q = 0; q < 8; ++q) a += expf(x[q] * scale - mx);
+            s += a;
+        }
+    } else {
+        for (int i = threadIdx.x; i < V; i += XT) {
+            const float x = elem<BF16>(row, i) * scale;
+            if (x > mx) { s = (mx == -INFINITY ? 0.f : s * expf(mx - x)); mx = x; }
+            s += expf(x - mx);
+        }
     }
     #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const float m2 = __shfl_xor_sync(0xFFFFFFFFu, mx, o), s2 = __shfl_xor_sync(0xFFFFFFFFu, s, o);
-        const float M = fmaxf(mx, m2);
-        s = (mx == -INFINITY ? 0.f : s * expf(mx - M)) + (m2 == -INFINITY ? 0.f : s2 * expf(m2 - M));
-        mx = M;
-    }
+    for (int o = 16; o > 0; o >>= 1)
+        lse_merge(mx, s, __shfl_xor_sync(0xFFFFFFFFu, mx, o), __shfl_xor_sync(0xFFFFFFFFu, s, o));
     __shared__ float sm[XT / 32], ss[XT / 32];
     const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
     if (l == 0) { sm[w] = mx; ss[w] = s; }
     __syncthreads();
     if (threadIdx.x == 0) {
         float M = sm[0], S = ss[0];
-        for (int i = 1; i < XT / 32; ++i) {
-            const float M2 = fmaxf(M, sm[i]);
-            S = (M == -INFINITY ? 0.f : S * expf(M - M2)) + (sm[i] == -INFINITY ? 0.f : ss[i] * expf(sm[i] - M2));
-            M = M2;
-        }
+        for (int i = 1; i < XT / 32; ++i) lse_merge(M, S, sm[i], ss[i]);
         lse[r] = M + logf(S);
     }
 }
@@ -120,10 +147,26 @@ __global__ void __launch_bounds__(XT) tv_alpha_kernel(const float* logits, const
             vr[q] = static_cast<const uint8_t*>(vlog) + row * (int64_t)V * (BF16 ? 2 : 4);
             lv[q] = lse_v[row];
         }
-        for (int i = threadIdx.x; i < V; i += XT) {
-            const float qx = expf(z[i] * inv_T - lz);
-            #pragma unroll
-            for (int q = 0; q < 8; ++q) acc[q] += fabsf(expf(elem<BF16>(vr[q], i) - lv[q]) - qx);
+        if ((V & 7) == 0) {
+            for (int c = threadIdx.x; c < V / 8; c += XT) {
+                float zz[8], qx[8];
+                load8<false>(z, c, zz);
+                #pragma unroll
+                for (int e = 0; e < 8; ++e) qx[e] = expf(zz[e] * inv_T - lz);
+                #pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    float vv[8];
+                    load8<BF16>(vr[q], c, vv);
+                    #pragma unroll
+                    for (int e = 0; e < 8; ++e) acc[q] += fabsf(expf(vv[e] - lv[q]) - qx[e]);
+                }
+            }
+        } else {
+            for (int i = threadIdx.x; i < V; i += XT) {
+                const float qx = expf(z[i] * inv_T - lz);
+                #pragma unroll
+                for (int q = 0; q < 8; ++q) acc[q] += fabsf(expf(elem<BF16>(vr[q], i) - lv[q]) - qx);
+            }
         }
         const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
         #pragma unroll
@@ -153,79 +196,128 @@ __global__ void tv_streak_kernel(const float* alpha, int64_t NK, int G, float* t
     tpd[i] = (float)tot;
 }
 
-// Lossless stochastic acceptance of one draft per sequence; one CTA per
-// sequence.  Thread 0 runs the acceptance tests; all threads then draw the
-// correction (or bonus) token by inverting the CDF of the residual, each
-// thread owning a contiguous chunk of the vocabulary: chunk sums in fp64, an
-// exclusive scan, and a sequential re-walk of the chunk that holds the target
-// with the same arithmetic.
+// Lossless stochastic acceptance, in three kernels so that the
+// vocabulary-wide work of the correction draw spreads over the whole GPU.
+//  1. spec_test_kernel: per sequence, the acceptance tests u Q(x_j) < P(x_j)
+//     in order; stop[n] = first rejected position (G if none).
+//  2. residual_group_kernel: for every (sequence, group of RG consecutive
+//     tokens) the sum of the draw's weights -- max(0, P - Q) of the rejected
+//     position, or P of the bonus row -- lanes adding strided elements
+//     (coalesced) in fp32, the group total in fp64.
+//  3. residual_pick_kernel: per sequence, an exclusive scan of the group
+//     sums, the group holding u * total, and an index-ordered fp64 walk of that
+//     group; a target that the walk does not reach (rounding at the group's
+//     end) takes the group's last token.
+constexpr int RG = 1024;
+
+struct SpecArgs {
+    const float* logits;
+    const float* lse_z;
+    float inv_T;
+    RowMap vm;
+    const float* lse_v;   // [N][G+1] rows of the verified draft, or [N][K][G+1] when lse_all
+    int lse_all;
+    const int32_t* drafts;
+    int G, V;
+    uint32_t key0, key1;
+    int* stop;        // [N]
+    double* gsum;     // [N][ngroups]
+    int ngroups;
+};
+
+__device__ __forceinline__ float lse_row(const SpecArgs& a, int64_t n, int j) {
+    if (!a.lse_all) return a.lse_v[n * (a.G + 1) + j];
+    const int64_t k = a.vm.sel ? a.vm.sel[n] : 0;
+    return a.lse_v[(n * a.vm.K + k) * (a.G + 1) + j];
+}
+
 template <bool BF16>
-__global__ void __launch_bounds__(XT) spec_accept_kernel(const float* logits, const float* lse_z, float inv_T,
-                                                         RowMap vm, const float* lse_v, const int32_t* drafts,
-                                                         int G, int V, uint32_t key0, uint32_t key1,
-                                                         int32_t* accept_len, int32_t* next_token) {
+__device__ __forceinline__ float draw_weight(const SpecArgs& a, int64_t n, int j, int i) {
+    const bool bonus = (j == a.G);
+    const void* vr = row_ptr<BF16>(a.vm, n * (a.G + 1) + j, a.V);
+    const float p = expf(elem<BF16>(vr, i) - lse_row(a, n, j));
+    if (bonus) return p;
+    const float q = expf(a.logits[(n * a.G + j) * (int64_t)a.V + i] * a.inv_T - a.lse_z[n * a.G + j]);
+    return p > q ? p - q : 0.f;
+}
+
+template <bool BF16>
+__global__ void spec_test_kernel(const SpecArgs a, int N) {
+    const int64_t n = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+    if (n >= N) return;
+    const int64_t kd = a.vm.sel ? a.vm.sel[n] : 0;
+    const int32_t* x = a.drafts + (n * a.vm.K + kd) * a.G;
+    int j = 0;
+    for (; j < a.G; ++j) {
+        const int32_t xj = x[j];
+        if (xj < 0 || xj >= a.V) break;   // not a token: rejected
+        const float* z = a.logits + (n * a.G + j) * (int64_t)a.V;
+        const void* vr = row_ptr<BF16>(a.vm, n * (a.G + 1) + j, a.V);
+        const double q = exp((double)(z[xj] * a.inv_T - a.lse_z[n * a.G + j]));
+        const double p = exp((double)(elem<BF16>(vr, xj) - lse_row(a, n, j)));
+        const double u = uniform24(philox0((uint32_t)n, (uint32_t)j, 0u, 1u, a.key0, a.key1));
+        if (!(u * q < p)) break;
+    }
+    a.stop[n] = j;
+}
+
+template <bool BF16>
+__global__ void residual_group_kernel(const SpecArgs a) {
+    const int64_t n = blockIdx.y;
+    const int g = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (g >= a.ngroups) return;
+    const int j = a.stop[n];
+    const int b = g * RG;
+    float acc = 0.f;
+    for (int i = b + lane; i < b + RG && i < a.V; i += 32) acc += draw_weight<BF16>(a, n, j, i);
+    double t = (double)acc;
+    #pragma unroll
+    for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xFFFFFFFFu, t, o);
+    if (lane == 0) a.gsum[n * a.ngroups + g] = t;
+}
+
+template <bool BF16>
+__global__ void residual_pick_kernel(const SpecArgs a, int32_t* accept_len, int32_t* next_token) {
     const int64_t n = blockIdx.x;
-    const int64_t kd = vm.sel ? vm.sel[n] : 0;
-    const int32_t* x = drafts + (n * vm.K + kd) * G;
-    __shared__ int stop;
-    __shared__ double chunk[XT];
-    __shared__ double total_s;
-    if (threadIdx.x == 0) {
-        int j = 0;
-        for (; j < G; ++j) {
-            const int32_t xj = x[j];
-            if (xj < 0 || xj >= V) break;   // not a token: rejected
-            const float* z = logits + (n * G + j) * (int64_t)V;
-            const void* vr = row_ptr<BF16>(vm, n * (G + 1) + j, V);
-            const double q = exp((double)(z[xj] * inv_T - lse_z[n * G + j]));
-            const double p = exp((double)(elem<BF16>(vr, xj) - lse_v[n * (G + 1) + j]));
-            const double u = uniform24(philox0((uint32_t)n, (uint32_t)j, 0u, 1u, key0, key1));
-            if (!(u * q < p)) break;
-        }
-        stop = j;
-    }
-    __syncthreads();
-    const int j = stop;
-    const bool bonus = (j == G);
-    const float* z = logits + (n * G + (bonus ? 0 : j)) * (int64_t)V;
-    const float lz = bonus ? 0.f : lse_z[n * G + j];
-    const void* vr = row_ptr<BF16>(vm, n * (G + 1) + j, V);
-    const float lv = lse_v[n * (G + 1) + j];
-    const int per = (V + XT - 1) / XT;
-    const int c0 = threadIdx.x * per, c1 = min(V, c0 + per);
-    auto weight = [&](int i) -> double {
-        const float p = expf(elem<BF16>(vr, i) - lv);
-        if (bonus) return (double)p;
-        const float q = expf(z[i] * inv_T - lz);
-        return p > q ? (double)p - (double)q : 0.0;
-    };
-    double s = 0.0;
-    for (int i = c0; i < c1; ++i) s += weight(i);
-    chunk[threadIdx.x] = s;
-    __syncthreads();
-    if (threadIdx.x == 0) {   // exclusive scan of the chunk sums (256 entries)
+    const int lane = threadIdx.x;
+    const int j = a.stop[n];
+    const double* gs = a.gsum + n * a.ngroups;
+    // total and the group holding the target (lane 0, in group order)
+    __shared__ int gsel;
+    __shared__ double excl_s;
+    if (lane == 0) {
+        double total = 0.0;
+        for (int g = 0; g < a.ngroups; ++g) total += gs[g];
+        const double u = uniform24(philox0((uint32_t)n, (uint32_t)j, 0u, 2u, a.key0, a.key1));
+        const double target = u * total;
         double run = 0.0;
-        for (int t = 0; t < XT; ++t) { const double c = chunk[t]; chunk[t] = run; run += c; }
-        total_s = run;
-    }
-    __syncthreads();
-    const double total = total_s;
-    const double u = uniform24(philox0((uint32_t)n, (uint32_t)j, 0u, 2u, key0, key1));
-    const double target = u * total;
-    const double excl = chunk[threadIdx.x];
-    const double next = threadIdx.x + 1 < XT ? chunk[threadIdx.x + 1] : total;
-    // The chunk whose [excl, next) holds the target walks itself again, adding
-    // from zero in the same order as its chunk sum; the last non-empty chunk
-    // also takes a target at or beyond the total (rounding).
-    const bool last = c1 == V;
-    if (c0 < c1 && target >= excl && (target < next || last)) {
-        const double rel = target - excl;
-        double run = 0.0;
-        int pick = c1 - 1;
-        for (int i = c0; i < c1; ++i) {
-            run += weight(i);
-            if (run > rel) { pick = i; break; }
+        int g = 0;
+        for (; g < a.ngroups - 1; ++g) {
+            if (run + gs[g] > target) break;
+            run += gs[g];
         }
+        gsel = g;
+        excl_s = target - run;   // target relative to the group's start
+    }
+    __syncwarp();
+    const int g = gsel;
+    const double rel = excl_s;
+    const int b0 = g * RG, b1 = min(a.V, b0 + RG);
+    double run = 0.0;
+    int pick = b1 - 1;
+    for (int b = b0; b < b1; b += 32) {
+        double x = (b + lane < b1) ? (double)draw_weight<BF16>(a, n, j, b + lane) : 0.0;
+        #pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const double y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+            if (lane >= o) x += y;
+        }
+        const unsigned hit = __ballot_sync(0xFFFFFFFFu, b + lane < b1 && run + x > rel);
+        if (hit) { pick = b + __ffs(hit) - 1; break; }
+        run += __shfl_sync(0xFFFFFFFFu, x, 31);
+    }
+    if (lane == 0) {
         accept_len[n] = j;
         next_token[n] = pick;
     }
@@ -236,7 +328,59 @@ inline size_t al256(size_t b) { return (b + 255) & ~size_t(255); }
 }  // namespace
 
 size_t tv_ws_bytes(int N, int K, int G) { return al256((size_t)N * G * 4) + al256((size_t)N * K * (G + 1) * 4); }
-size_t spec_ws_bytes(int N, int G) { return al256((size_t)N * G * 4) + al256((size_t)N * (G + 1) * 4); }
+size_t spec_ws_bytes(int N, int G, int V) {
+    const size_t ng = (size_t)(V + RG - 1) / RG;
+    return al256((size_t)N * G * 4) + al256((size_t)N * (G + 1) * 4) + al256((size_t)N * 4) + al256((size_t)N * ng * 8);
+}
+
+// Internal runners with precomputed log-sum-exps (used by the draft step,
+// which already has the verifier rows' LSEs from self-selection).
+dfl_status lse_rows_f32(const float* logits, int rows, int V, float inv_T, float* lse, cudaStream_t st) {
+    ProfScope ps("row_lse", st);
+    row_lse_kernel<false><<<(unsigned)rows, XT, 0, st>>>(RowMap{logits, 1, 1, nullptr}, V, inv_T, lse);
+    return last_launch();
+}
+
+dfl_status tv_run(const float* logits, float inv_T, const void* vlog, bool bf, int N, int K, int G, int V,
+                  float* alpha, float* tpd, const float* lse_z, const float* lse_v_all, cudaStream_t st) {
+    {
+        ProfScope ps("tv_alpha", st);
+        if (bf) tv_alpha_kernel<true><<<(unsigned)(N * G), XT, 0, st>>>(logits, lse_z, inv_T, vlog, lse_v_all, K, G, V, alpha);
+        else tv_alpha_kernel<false><<<(unsigned)(N * G), XT, 0, st>>>(logits, lse_z, inv_T, vlog, lse_v_all, K, G, V, alpha);
+    }
+    dfl_status rc = last_launch();
+    if (rc != DFL_OK || !tpd) return rc;
+    ProfScope ps("tv_streak", st);
+    tv_streak_kernel<<<(unsigned)((N * K + 127) / 128), 128, 0, st>>>(alpha, (int64_t)N * K, G, tpd);
+    return last_launch();
+}
+
+size_t spec_scratch_bytes(int N, int V) {
+    return al256((size_t)N * 4) + al256((size_t)N * ((V + RG - 1) / RG) * 8);
+}
+
+dfl_status spec_run(const float* logits, float inv_T, const void* vlog, bool bf, const int32_t* drafts,
+                    const int32_t* sel, int N, int K, int G, int V, uint64_t seed, int32_t* accept_len,
+                    int32_t* next_token, const float* lse_z, const float* lse_v, bool lse_all, void* scratch,
+                    cudaStream_t st) {
+    ProfScope ps("spec_accept", st);
+    SpecArgs sa{logits, lse_z, inv_T, RowMap{vlog, K, G + 1, sel}, lse_v, lse_all ? 1 : 0, drafts, G, V,
+                (uint32_t)(seed & 0xFFFFFFFFu), (uint32_t)(seed >> 32), nullptr, nullptr, (V + RG - 1) / RG};
+    uint8_t* p = static_cast<uint8_t*>(scratch);
+    sa.stop = reinterpret_cast<int*>(p);
+    sa.gsum = reinterpret_cast<double*>(p + al256((size_t)N * 4));
+    const dim3 ggrid((sa.ngroups + 7) / 8, N);
+    if (bf) {
+        spec_test_kernel<true><<<(N + 127) / 128, 128, 0, st>>>(sa, N);
+        residual_group_kernel<true><<<ggrid, 256, 0, st>>>(sa);
+        residual_pick_kernel<true><<<N, 32, 0, st>>>(sa, accept_len, next_token);
+    } else {
+        spec_test_kernel<false><<<(N + 127) / 128, 128, 0, st>>>(sa, N);
+        residual_group_kernel<false><<<ggrid, 256, 0, st>>>(sa);
+        residual_pick_kernel<false><<<N, 32, 0, st>>>(sa, accept_len, next_token);
+    }
+    return last_launch();
+}
 
 }  // namespace dfl
 
@@ -266,15 +410,7 @@ extern "C" dfl_status dfl_tv_acceptance(const float* logits, float T, const void
     }
     dfl_status rc = last_launch();
     if (rc != DFL_OK) return rc;
-    {
-        ProfScope ps("tv_alpha", st);
-        if (bf) tv_alpha_kernel<true><<<(unsigned)(N * G), XT, 0, st>>>(logits, lse_z, inv_T, vlog, lse_v, K, G, V, alpha);
-        else tv_alpha_kernel<false><<<(unsigned)(N * G), XT, 0, st>>>(logits, lse_z, inv_T, vlog, lse_v, K, G, V, alpha);
-    }
-    if ((rc = last_launch()) != DFL_OK || !tokens_per_draft) return rc;
-    ProfScope ps("tv_streak", st);
-    tv_streak_kernel<<<(unsigned)((N * K + 127) / 128), 128, 0, st>>>(alpha, (int64_t)N * K, G, tokens_per_draft);
-    return last_launch();
+    return tv_run(logits, inv_T, vlog, bf, N, K, G, V, alpha, tokens_per_draft, lse_z, lse_v, st);
 }
 
 extern "C" dfl_status dfl_spec_accept(const float* logits, float T, const void* vlog, dfl_dtype dt,
@@ -285,7 +421,7 @@ extern "C" dfl_status dfl_spec_accept(const float* logits, float T, const void* 
         G > 1024 || V <= 0 || !(T > 0.f))
         return DFL_ERR_INVALID_ARG;
     if (dt != DFL_F32 && dt != DFL_BF16) return DFL_ERR_INVALID_ARG;
-    if (ws_bytes < spec_ws_bytes(N, G)) return DFL_ERR_WORKSPACE;
+    if (ws_bytes < spec_ws_bytes(N, G, V)) return DFL_ERR_WORKSPACE;
     if (!current_ctx()) return DFL_ERR_NO_DEVICE;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     float* lse_z = static_cast<float*>(ws);
@@ -301,13 +437,6 @@ extern "C" dfl_status dfl_spec_accept(const float* logits, float T, const void* 
     }
     dfl_status rc = last_launch();
     if (rc != DFL_OK) return rc;
-    ProfScope ps("spec_accept", st);
-    const uint32_t k0 = (uint32_t)(seed & 0xFFFFFFFFu), k1 = (uint32_t)(seed >> 32);
-    if (bf)
-        spec_accept_kernel<true><<<(unsigned)N, XT, 0, st>>>(logits, lse_z, inv_T, vm, lse_v, drafts, G, V, k0, k1,
-                                                             accept_len, next_token);
-    else
-        spec_accept_kernel<false><<<(unsigned)N, XT, 0, st>>>(logits, lse_z, inv_T, vm, lse_v, drafts, G, V, k0, k1,
-                                                              accept_len, next_token);
-    return last_launch();
+    return spec_run(logits, inv_T, vlog, bf, drafts, sel, N, K, G, V, seed, accept_len, next_token, lse_z, lse_v,
+                    false, static_cast<uint8_t*>(ws) + al256((size_t)N * G * 4) + al256((size_t)N * (G + 1) * 4), st);
 }

@@ -105,7 +105,7 @@ extern "C" size_t dfl_workspace_size(dfl_op op, const dfl_shape* s) {
             return ws_lm_head(s->N, s->B, s->row0, s->d, s->V, s->dtype, s->dtype == DFL_F32);
         case DFL_OP_SELF_SELECT: return al256(select_ws_bytes(s->N, s->K, s->G));
         case DFL_OP_TV_ACCEPTANCE: return tv_ws_bytes(s->N, s->K, s->G);
-        case DFL_OP_SPEC_ACCEPT: return spec_ws_bytes(s->N, s->G);
+        case DFL_OP_SPEC_ACCEPT: return spec_ws_bytes(s->N, s->G, s->V);
         case DFL_OP_DRAFT_STEP: {
             const size_t e = esz(s->dtype);
             size_t b = al256((size_t)s->D * s->N * s->C * s->d * e);                 // Xc, all layers
@@ -119,7 +119,10 @@ extern "C" size_t dfl_workspace_size(dfl_op op, const dfl_shape* s) {
                 const size_t lm = ws_lm_head(s->N, s->B, 1, s->d, s->V, s->dtype, true);
                 if (lm > sub) sub = lm;
                 if (s->K > 0) {
-                    const size_t se = al256(select_ws_bytes(s->N, s->K, s->B - 1));
+                    // self-selection scratch (its verifier-row LSEs are reused), drafter-row LSEs,
+                    // stochastic-acceptance scratch
+                    const size_t se = al256(select_ws_bytes(s->N, s->K, s->B - 1)) +
+                                      al256((size_t)s->N * (s->B - 1) * 4) + spec_scratch_bytes(s->N, s->V);
                     if (se > sub) sub = se;
                     b += al256((size_t)s->N * s->K * (s->B - 1) * 4);               // samples
                 }
@@ -400,6 +403,9 @@ extern "C" dfl_status dfl_draft_step(const dfl_step_args* a, void* ws, size_t ws
     if (a->sample && (!a->samples || a->V == 0)) return DFL_ERR_INVALID_ARG;
     if (a->vlog && (!a->sample || !a->scores || !a->selected || !a->accept_len || !a->bonus))
         return DFL_ERR_INVALID_ARG;
+    if ((a->tv_alpha || a->tv_tokens || a->accept_rule != 0) && !a->vlog) return DFL_ERR_INVALID_ARG;
+    if (a->tv_tokens && !a->tv_alpha) return DFL_ERR_INVALID_ARG;
+    if (a->accept_rule != 0 && a->accept_rule != 1) return DFL_ERR_INVALID_ARG;
     for (int l = 0; l < a->D; ++l) {
         const dfl_layer_weights& w = a->layers[l];
         if (!w.Wq || !w.Wkc || !w.Wvc || !w.Wkb || !w.Wvb || !w.Wo) return DFL_ERR_INVALID_ARG;
@@ -460,9 +466,28 @@ extern "C" dfl_status dfl_draft_step(const dfl_step_args* a, void* ws, size_t ws
     if ((rc = dfl_lm_head_argmax(a->Xb, N, B, 1, d, ddt, a->final_gain, a->eps, a->W_lm, a->V, a->draft, logits,
                                  a->sample, samples, sub, sub_bytes, stream)) != DFL_OK)
         return rc;
-    if (a->vlog)
-        return dfl_self_select(a->vlog, ddt, samples, N, a->sample->K, B - 1, a->V, a->scores, a->selected,
-                               a->accept_len, a->bonus, sub, sub_bytes, stream);
+    if (a->vlog) {
+        const int K = a->sample->K, G = B - 1;
+        if ((rc = dfl_self_select(a->vlog, ddt, samples, N, K, G, a->V, a->scores, a->selected, a->accept_len,
+                                  a->bonus, sub, sub_bytes, stream)) != DFL_OK)
+            return rc;
+        if (!a->tv_alpha && a->accept_rule == 0) return DFL_OK;
+        // Reuse self-selection's LSEs of every verifier row (at the start of its
+        // scratch); the drafter rows' LSEs are formed once for both epilogues.
+        const float* lse_v = reinterpret_cast<const float*>(sub);
+        uint8_t* q = sub + al256(select_ws_bytes(N, K, G));
+        float* lse_z = reinterpret_cast<float*>(q);
+        q += al256((size_t)N * G * 4);
+        const float inv_T = 1.0f / a->sample->T;
+        if ((rc = lse_rows_f32(logits, N * G, a->V, inv_T, lse_z, st)) != DFL_OK) return rc;
+        if (a->tv_alpha && (rc = tv_run(logits, inv_T, a->vlog, dt == DFL_BF16, N, K, G, a->V, a->tv_alpha,
+                                        a->tv_tokens, lse_z, lse_v, st)) != DFL_OK)
+            return rc;
+        if (a->accept_rule == 1)
+            return spec_run(logits, inv_T, a->vlog, dt == DFL_BF16, samples, a->selected, N, K, G, a->V,
+                            a->accept_seed, a->accept_len, a->bonus, lse_z, lse_v, true, q, st);
+        return DFL_OK;
+    }
     if (a->target) return dfl_greedy_accept(a->draft, a->target, N, B - 1, a->accept_len, a->bonus, stream);
     return DFL_OK;
 }

@@ -35,7 +35,15 @@ dfl_status attn_bf16(const void* Q, const void* Kc, const void* Vc, const void* 
 
 // TV acceptance diagnostic and stochastic acceptance (workspace bytes)
 size_t tv_ws_bytes(int N, int K, int G);
-size_t spec_ws_bytes(int N, int G);
+size_t spec_ws_bytes(int N, int G, int V);
+size_t spec_scratch_bytes(int N, int V);
+dfl_status lse_rows_f32(const float* logits, int rows, int V, float inv_T, float* lse, cudaStream_t st);
+dfl_status tv_run(const float* logits, float inv_T, const void* vlog, bool bf, int N, int K, int G, int V,
+                  float* alpha, float* tpd, const float* lse_z, const float* lse_v_all, cudaStream_t st);
+dfl_status spec_run(const float* logits, float inv_T, const void* vlog, bool bf, const int32_t* drafts,
+                    const int32_t* sel, int N, int K, int G, int V, uint64_t seed, int32_t* accept_len,
+                    int32_t* next_token, const float* lse_z, const float* lse_v, bool lse_all, void* scratch,
+                    cudaStream_t st);
 
 // self-selection
 size_t select_ws_bytes(int N, int K, int G);

@@ -51,7 +51,7 @@ class DraftModel:
     """Drafter parameters, workspace and outputs for one shape on one device."""
 
     def __init__(self, shape: DraftShape, mix_logits, mix_gain, blk_gain, final_gain, layers, W_lm=None,
-                 device="cuda"):
+                 device="cuda", tv=False, accept_rule=0, accept_seed=0):
         s = self.shape = shape
         dev = torch.device(device)
         wd = shape.torch_dtype
@@ -83,6 +83,10 @@ class DraftModel:
         self.scores = torch.empty((s.N, s.K), dtype=torch.float32, device=dev) if s.K > 0 else None
         self.selected = torch.empty((s.N,), dtype=torch.int32, device=dev) if s.K > 0 else None
         self.logits = None
+        # optional epilogues after self-selection: TV acceptance proxy, stochastic acceptance rule
+        self.tv_alpha = torch.empty((s.N, s.K, n), dtype=torch.float32, device=dev) if (tv and s.K > 0) else None
+        self.tv_tokens = torch.empty((s.N, s.K), dtype=torch.float32, device=dev) if (tv and s.K > 0) else None
+        self.accept_rule, self.accept_seed = int(accept_rule), int(accept_seed)
 
     def want_logits(self, on: bool = True):
         """Keep the fp32 logits [N*(B-1)][V] of each step (needed to check argmax bit-exactly)."""
@@ -108,6 +112,8 @@ class DraftModel:
             a.samples = _lib.ptr(self.samples)
             if vlog is not None:
                 a.vlog, a.scores, a.selected = _lib.ptr(vlog), _lib.ptr(self.scores), _lib.ptr(self.selected)
+                a.tv_alpha, a.tv_tokens = _lib.ptr(self.tv_alpha), _lib.ptr(self.tv_tokens)
+                a.accept_rule, a.accept_seed = self.accept_rule, self.accept_seed
         return a
 
     def step(self, H, Xb0, target=None, vlog=None, stream=None):

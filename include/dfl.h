@@ -297,7 +297,7 @@ dfl_status dfl_tv_acceptance(const float* logits, float T, const void* vlog, dfl
  *   drafts  in, int32 [N][K][G]; sel in, int32 [N] draft to verify (nullable:
  *           draft 0); a token outside [0, V) is rejected
  *   accept_len out, int32 [N] (accepted drafts, 0..G); next_token out, int32 [N]
- *   ws      dfl_workspace_size(DFL_OP_SPEC_ACCEPT) bytes
+ *   ws      dfl_workspace_size(DFL_OP_SPEC_ACCEPT) bytes (N, G and V of the shape)
  *   Errors: INVALID_ARG, WORKSPACE.
  */
 dfl_status dfl_spec_accept(const float* logits, float T, const void* vlog, dfl_dtype dt,
@@ -341,6 +341,14 @@ typedef struct dfl_step_args {
     const void* vlog;              /* in, nullable: [N][K][B][V] verifier logits */
     float* scores;                 /* out [N][K] when vlog != NULL */
     int32_t* selected;             /* out [N] when vlog != NULL */
+    /* Optional epilogues after self-selection (vlog != NULL): */
+    float* tv_alpha;               /* out, nullable: [N][K][B-1] TV acceptance proxy */
+    float* tv_tokens;              /* out, nullable: [N][K] streak sum of tv_alpha */
+    int32_t accept_rule;           /* 0: greedy on the selected draft; 1: lossless
+                                      stochastic acceptance (dfl_spec_accept), whose
+                                      accepted length and next token replace
+                                      accept_len / bonus */
+    uint64_t accept_seed;          /* Philox key of the stochastic rule */
 } dfl_step_args;
 
 /*

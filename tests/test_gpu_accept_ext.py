@@ -69,7 +69,7 @@ def test_spec_accept_matches_oracle(closeness):
     sel = rng.integers(0, K, N).astype(np.int32)
     al = torch.empty(N, dtype=torch.int32, device="cuda")
     nt = torch.empty(N, dtype=torch.int32, device="cuda")
-    wsb = dfl.workspace_size(dfl.DFL_OP_SPEC_ACCEPT, N=N, G=G)
+    wsb = dfl.workspace_size(dfl.DFL_OP_SPEC_ACCEPT, N=N, G=G, V=V)
     ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
     dfl.dfl_spec_accept(torch.from_numpy(z).cuda(), T, torch.from_numpy(v).cuda().to(torch.bfloat16), dfl.DFL_BF16,
                         torch.from_numpy(drafts).cuda(), torch.from_numpy(sel).cuda(), N, K, G, V, seed, al, nt, ws,

@@ -203,3 +203,38 @@ def test_gpt_oss_20b_drafter_full_size():
 def test_specdiff2_selection_full_size():
     w = WORKLOADS["specdiff2_select"]
     _run_select_workload(w, seqs=[0, 15], rows_checked=[0, 1, 17, 31])
+
+
+def test_self_selection_step_with_tv_and_stochastic_acceptance():
+    w = Workload("selext", N=3, d=256, Hq=4, Hkv=2, hd=64, D=2, L=3, B=9, C=80, V=1500, dtype="bf16", seed=61,
+                 K=4, T=1.5, philox_seed=0x5EEDD1F5)
+    mix = gen_mix_logits(w)
+    g_mix, g_blk, g_fin = gen_gains(w)
+    layers = [gen_layer_weights(w, l) for l in range(w.D)]
+    W_lm = gen_lm_head(w, as_bits=True)
+    shape = dfl.DraftShape(N=w.N, d=w.d, Hq=w.Hq, Hkv=w.Hkv, hd=w.hd, D=w.D, L=w.L, B=w.B, C=w.C, V=w.V,
+                           dtype=w.dtype, K=w.K, T=w.T, seed=w.philox_seed, eps=w.eps, rope_theta=w.rope_theta)
+    seed = 0xABCDEF12345
+    model = dfl.DraftModel(shape, mix, g_mix, g_blk, g_fin, layers,
+                           torch.from_numpy(W_lm.view(np.int16)).view(torch.bfloat16), tv=True, accept_rule=1,
+                           accept_seed=seed)
+    model.want_logits()
+    from dfl_synth import bits_to_f32
+    vbits = gen_verifier_logits(w, as_bits=True)
+    vlog = torch.from_numpy(vbits.view(np.int16)).cuda().view(torch.bfloat16)
+    model.step(_hidden_dev(w), torch.from_numpy(gen_block_init(w)).cuda(), vlog=vlog)
+    torch.cuda.synchronize()
+    G = w.gamma
+    z = host(model.logits).reshape(w.N, G, w.V)
+    samples, sel = host(model.samples), host(model.selected)
+    alpha = host(model.tv_alpha)
+    for n in range(w.N):
+        vl = bits_to_f32(vbits[n])
+        ref = np.array([[orc.tv_alpha(z[n, j], w.T, vl[k, j]) for j in range(G)] for k in range(w.K)])
+        assert np.max(np.abs(alpha[n] - ref)) <= 2e-5
+        assert np.allclose(host(model.tv_tokens)[n], [orc.streak_score(r) for r in ref], rtol=1e-4, atol=1e-6)
+        u_acc = [orc.draw_uniform_stream(seed, n, j, 0, 1) for j in range(G)]
+        u_res = [orc.draw_uniform_stream(seed, n, j, 0, 2) for j in range(G + 1)]
+        a, y, margin = orc.speculative_accept(z[n], w.T, vl[sel[n]], samples[n, sel[n]], u_acc, u_res)
+        if margin >= 1e-5:
+            assert (int(host(model.accept_len)[n]), int(host(model.bonus)[n])) == (a, y)
