@@ -200,8 +200,30 @@ def draft_layer(Xb, Hn, mix_logits, g_mix, g_blk, W: dict, shape: dict,
     O = attention(Q, np.concatenate([Kc, Kb]), np.concatenate([Vc, Vb]),
                   block_visibility(C, B))
     Xb_out = Xb + O.reshape(B, Hq * hd) @ f["Wo"].T
-    return {"Xc": Xc, "Xn": Xn, "Q": Q, "Kc": Kc, "Vc": Vc, "Kb": Kb,
-            "Vb": Vb, "O": O, "Xb": Xb_out}
+    out = {"Xc": Xc, "Xn": Xn, "Q": Q, "Kc": Kc, "Vc": Vc, "Kb": Kb,
+           "Vb": Vb, "O": O, "Xb_attn": Xb_out, "Xb": Xb_out}
+    if "W1" in f:
+        out["Xb"] = swiglu_ffn(Xb_out, W["g_ffn"], f["W1"], f["W3"], f["W2"], eps)
+    return out
+
+
+def silu(x) -> np.ndarray:
+    """x * sigmoid(x)."""
+    x = np.asarray(x, dtype=F64)
+    return x / (1.0 + np.exp(-x))
+
+
+def swiglu_ffn(Xb, g_ffn, W1, W3, W2, eps: float) -> np.ndarray:
+    """Residual SwiGLU feed-forward block of a Qwen-style decoder layer.
+
+    Reading (the pages give no width or form; the DFlash article's drafter
+    layers are the target family's decoder layers): Xn = RMSNorm(Xb; g_ffn),
+    Xb + (silu(Xn W1^T) * (Xn W3^T)) W2^T with W1, W3 [F][d] and W2 [d][F].
+    """
+    Xn = rmsnorm(Xb, g_ffn, eps)
+    gate = Xn @ np.asarray(W1, dtype=F64).T
+    up = Xn @ np.asarray(W3, dtype=F64).T
+    return np.asarray(Xb, dtype=F64) + (silu(gate) * up) @ np.asarray(W2, dtype=F64).T
 
 
 def lm_head_logits(X_rows, g_final, eps: float, W_lm, chunk: int = 8192) -> np.ndarray:

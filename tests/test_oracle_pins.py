@@ -600,3 +600,43 @@ def test_uniform_streams_are_distinct():
     a = orc.draw_uniform_stream(7, 1, 2, 0, 0)
     assert a == orc.draw_uniform(7, 1, 2, 0)
     assert len({orc.draw_uniform_stream(7, 1, 2, 0, s) for s in range(3)}) == 3
+
+
+
+# ----------------------------------------------------------- SwiGLU FFN --
+
+def test_silu_closed_form():
+    for x in (-3.0, -0.5, 0.0, 0.7, 4.0):
+        assert abs(orc.silu(x) - x / (1 + math.exp(-x))) < 1e-15
+    assert orc.silu(0.0) == 0.0
+
+
+def test_swiglu_ffn_scalar_restatement_and_identity():
+    rng = np.random.default_rng(40)
+    B, d, F = 3, 6, 5
+    Xb, g = rng.normal(size=(B, d)), rng.uniform(0.5, 1.5, d)
+    W1, W3, W2 = rng.normal(size=(F, d)), rng.normal(size=(F, d)), rng.normal(size=(d, F))
+    got = orc.swiglu_ffn(Xb, g, W1, W3, W2, 1e-6)
+    for b in range(B):
+        r = math.sqrt(sum(v * v for v in Xb[b]) / d + 1e-6)
+        xn = [Xb[b, k] / r * g[k] for k in range(d)]
+        h = []
+        for f in range(F):
+            a = sum(xn[k] * W1[f, k] for k in range(d))
+            u = sum(xn[k] * W3[f, k] for k in range(d))
+            h.append(a / (1 + math.exp(-a)) * u)
+        for o in range(d):
+            assert abs(got[b, o] - (Xb[b, o] + sum(h[f] * W2[o, f] for f in range(F)))) < 1e-12
+    assert np.allclose(orc.swiglu_ffn(Xb, g, W1, W3, np.zeros((d, F)), 1e-6), Xb, atol=0)
+
+
+def test_draft_layer_with_ffn_adds_the_ffn_after_attention():
+    t = _tiny_layer_inputs()
+    rng = np.random.default_rng(41)
+    d, F = t["Xb"].shape[1], 7
+    W = dict(t["W"], W1=rng.normal(size=(F, d)), W3=rng.normal(size=(F, d)), W2=rng.normal(size=(d, F)),
+             g_ffn=rng.uniform(0.5, 1.5, d))
+    a = orc.draft_layer(t["Xb"], t["Hn"], t["mix"], t["g_mix"], t["g_blk"], W, t["shape"], 1e-6, 100.0)
+    b = orc.draft_layer(t["Xb"], t["Hn"], t["mix"], t["g_mix"], t["g_blk"], t["W"], t["shape"], 1e-6, 100.0)
+    assert np.allclose(a["Xb_attn"], b["Xb"], atol=1e-13)
+    assert np.allclose(a["Xb"], orc.swiglu_ffn(b["Xb"], W["g_ffn"], W["W1"], W["W3"], W["W2"], 1e-6), atol=1e-12)
