@@ -146,6 +146,10 @@ def kernel_work(w):
                       2.0 * (2 * N * (C + B) * kv + 2 * rows_b * qd)),
         "gemm_o_proj": (2.0 * rows_b * d * qd, 2.0 * (rows_b * qd + d * qd) + 8.0 * rows_b * d),
     }
+    if w.F > 0:
+        M = rows_b
+        work["gemm_ffn_gate_up"] = (2.0 * M * 2 * w.F * d, 2.0 * (M * d + 2 * w.F * d + M * w.F))
+        work["gemm_ffn_down"] = (2.0 * M * d * w.F, 2.0 * (M * w.F + d * w.F) + 8.0 * M * d)
     if V > 0:
         M = N * (B - 1)
         work["gemm_lm_head"] = (2.0 * M * V * d, 2.0 * (M * d + V * d) + (4.0 * M * V if w.K > 0 else 0.0))
@@ -210,9 +214,9 @@ def workload(name, rank=0, batch=0, context=0):
 
 
 def host_params(w):
-    from dfl_synth import gen_gains, gen_layer_weights, gen_lm_head, gen_mix_logits
+    from dfl_synth import gen_ffn_gains, gen_gains, gen_layer_weights, gen_lm_head, gen_mix_logits
     g_mix, g_blk, g_fin = gen_gains(w)
-    return {"mix": gen_mix_logits(w), "g_mix": g_mix, "g_blk": g_blk, "g_fin": g_fin,
+    return {"mix": gen_mix_logits(w), "g_mix": g_mix, "g_blk": g_blk, "g_fin": g_fin, "g_ffn": gen_ffn_gains(w),
             "layers": [gen_layer_weights(w, l) for l in range(w.D)],
             "W_lm_bits": gen_lm_head(w, as_bits=True) if w.V > 0 else None}
 
@@ -224,7 +228,8 @@ def oracle_step(w, p, n, W_lm_f32, vlog_n=None):
     Hn = gen_hidden(w, seqs=[n])
     Xb0 = gen_block_init(w)[n]
     t0 = time.perf_counter()
-    out = orc.draft_forward(Xb0, Hn, p["mix"], p["g_mix"], p["g_blk"], p["layers"],
+    layers = [dict(W, g_ffn=p["g_ffn"][l]) if w.F > 0 else W for l, W in enumerate(p["layers"])]
+    out = orc.draft_forward(Xb0, Hn, p["mix"], p["g_mix"], p["g_blk"], layers,
                             {"Hq": w.Hq, "Hkv": w.Hkv, "hd": w.hd}, w.eps, w.rope_theta)
     if w.V > 0:
         z = orc.lm_head_logits(out["Xb"][1:], p["g_fin"], w.eps, W_lm_f32)
@@ -269,11 +274,12 @@ def run_ours(args, rank, world, local):
     w = workload(args.workload, rank, args.batch, args.context)
     p = host_params(w)
     shape = dfl.DraftShape(N=w.N, d=w.d, Hq=w.Hq, Hkv=w.Hkv, hd=w.hd, D=w.D, L=w.L, B=w.B, C=w.C, V=w.V,
-                           dtype=w.dtype, K=w.K, T=w.T, seed=w.philox_seed, eps=w.eps, rope_theta=w.rope_theta)
+                           dtype=w.dtype, K=w.K, T=w.T, seed=w.philox_seed, eps=w.eps, rope_theta=w.rope_theta,
+                           F=w.F)
     W_lm = (torch.from_numpy(p["W_lm_bits"].view(np.int16)).view(torch.bfloat16) if w.V > 0 else None)
     model = dfl.DraftModel(shape, p["mix"], p["g_mix"], p["g_blk"], p["g_fin"], p["layers"], W_lm,
                            tv=args.tv and w.K > 0, accept_rule=1 if (args.accept_rule == "stochastic" and w.K > 0) else 0,
-                           accept_seed=w.philox_seed ^ 0xACCE97)
+                           accept_seed=w.philox_seed ^ 0xACCE97, ffn_gain=p["g_ffn"])
     H_host = torch.from_numpy(gen_hidden(w, as_bits=True).view(np.int16)).view(torch.bfloat16)
     X_host = torch.from_numpy(gen_block_init(w))
     H, X0 = H_host.cuda(), X_host.cuda()
@@ -378,6 +384,7 @@ def run_ours(args, rank, world, local):
                 "data": "synthetic (seeded NumPy PCG64; shapes and distributions of the workload)",
                 "config": {"workload": w.name, "N_per_gpu": w.N, "d": w.d, "Hq": w.Hq, "Hkv": w.Hkv, "hd": w.hd,
                            "draft_layers": w.D, "target_layers": w.L, "block": w.B, "context": w.C, "vocab": w.V,
+                           "ffn": w.F,
                            "K": w.K, "T": w.T, "parallelism": f"replicas x{world}",
                            "epilogue": ("self-selection" + (" + TV proxy" if args.tv else "") +
                                         (" + stochastic acceptance" if args.accept_rule == "stochastic" else

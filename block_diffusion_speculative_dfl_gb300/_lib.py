@@ -15,14 +15,14 @@ DFL_OK, DFL_ERR_INVALID_ARG, DFL_ERR_UNSUPPORTED_SHAPE, DFL_ERR_MISALIGNED = 0, 
 DFL_ERR_WORKSPACE, DFL_ERR_CUDA, DFL_ERR_TIMEOUT, DFL_ERR_NO_DEVICE = 4, 5, 6, 7
 DFL_F32, DFL_BF16 = 0, 1
 DFL_OP_DUAL_KV_PROJ, DFL_OP_BLOCK_ATTN, DFL_OP_LM_HEAD, DFL_OP_SELF_SELECT, DFL_OP_DRAFT_STEP = 1, 2, 3, 4, 5
-DFL_OP_TV_ACCEPTANCE, DFL_OP_SPEC_ACCEPT = 6, 7
+DFL_OP_TV_ACCEPTANCE, DFL_OP_SPEC_ACCEPT, DFL_OP_BLOCK_FFN = 6, 7, 8
 
 # Every function the header declares; tests check each is exported.
 EXPORTED = ("dfl_version", "dfl_status_string", "dfl_workspace_size", "dfl_rope_table",
             "dfl_layer_mix_rmsnorm", "dfl_dual_kv_proj", "dfl_block_attn", "dfl_lm_head_argmax",
             "dfl_greedy_accept", "dfl_self_select", "dfl_draft_step", "dfl_get_device_error",
             "dfl_set_wait_limit_ns", "dfl_selftest_bounded_wait", "dfl_profile_enable", "dfl_profile_report",
-            "dfl_self_select_noalloc", "dfl_tv_acceptance", "dfl_spec_accept")
+            "dfl_self_select_noalloc", "dfl_tv_acceptance", "dfl_spec_accept", "dfl_block_ffn")
 
 
 class DflError(RuntimeError):
@@ -37,11 +37,11 @@ class SampleParams(C.Structure):
 
 class Shape(C.Structure):
     _fields_ = [(n, C.c_int32) for n in ("N", "C", "B", "d", "Hq", "Hkv", "hd", "D", "L", "V", "K", "G", "row0",
-                                         "dtype")]
+                                         "dtype", "F")]
 
 
 class LayerWeights(C.Structure):
-    _fields_ = [(n, C.c_void_p) for n in ("Wq", "Wkc", "Wvc", "Wkb", "Wvb", "Wo")]
+    _fields_ = [(n, C.c_void_p) for n in ("Wq", "Wkc", "Wvc", "Wkb", "Wvb", "Wo", "W1", "W3", "W2")]
 
 
 class StepArgs(C.Structure):
@@ -53,7 +53,7 @@ class StepArgs(C.Structure):
                                            "bonus")] +
                 [("sample", C.POINTER(SampleParams))] +
                 [(n, C.c_void_p) for n in ("samples", "vlog", "scores", "selected", "tv_alpha", "tv_tokens")] +
-                [("accept_rule", C.c_int32), ("accept_seed", C.c_uint64)])
+                [("accept_rule", C.c_int32), ("accept_seed", C.c_uint64), ("F", C.c_int32), ("ffn_gain", C.c_void_p)])
 
 
 _P, _I32, _I64, _F, _D, _SZ = C.c_void_p, C.c_int32, C.c_int64, C.c_float, C.c_double, C.c_size_t
@@ -80,6 +80,7 @@ _SIGS = {
     "dfl_self_select_noalloc": ([_P, _I32, _P, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _P], _I32),
     "dfl_tv_acceptance": ([_P, _F, _P, _I32, _I32, _I32, _I32, _I32, _P, _P, _P, _SZ, _P], _I32),
     "dfl_spec_accept": ([_P, _F, _P, _I32, _P, _P, _I32, _I32, _I32, _I32, C.c_uint64, _P, _P, _P, _SZ, _P], _I32),
+    "dfl_block_ffn": ([_P, _I32, _I32, _I32, _I32, _P, _F, _P, _P, _P, _I32, _P, _SZ, _P], _I32),
 }
 
 _lib = None
@@ -235,3 +236,9 @@ def dfl_spec_accept(logits, T, vlog, dt, drafts, sel, N, K, G, V, seed, accept_l
     _check("dfl_spec_accept",
            load().dfl_spec_accept(ptr(logits), T, ptr(vlog), dt, ptr(drafts), ptr(sel), N, K, G, V, seed,
                                   ptr(accept_len), ptr(next_token), ptr(ws), ws_bytes, _stream(stream)))
+
+
+def dfl_block_ffn(Xb, N, B, d, dt, ffn_gain, eps, W1, W3, W2, F, ws, ws_bytes, stream=None):
+    _check("dfl_block_ffn",
+           load().dfl_block_ffn(ptr(Xb), N, B, d, dt, ptr(ffn_gain), eps, ptr(W1), ptr(W3), ptr(W2), F, ptr(ws),
+                                ws_bytes, _stream(stream)))

@@ -65,6 +65,12 @@ size_t ws_block_attn(int N, int C, int B, int Hq, int Hkv, int hd, int dt) {
     return b;
 }
 
+size_t ws_block_ffn(int N, int B, int d, int F, int dt) {
+    const size_t M = (size_t)N * B;
+    if (dt == DFL_BF16) return al256(M * d * 2) + al256(M * F * 2);
+    return al256(M * d * 4) + 3 * al256(M * F * 4);
+}
+
 size_t ws_lm_head(int N, int B, int row0, int d, int V, int dt, bool logits_missing) {
     const size_t M = (size_t)N * (B - row0);
     const size_t tiles = (size_t)(V + 255) / 256;
@@ -106,6 +112,7 @@ extern "C" size_t dfl_workspace_size(dfl_op op, const dfl_shape* s) {
         case DFL_OP_SELF_SELECT: return al256(select_ws_bytes(s->N, s->K, s->G));
         case DFL_OP_TV_ACCEPTANCE: return tv_ws_bytes(s->N, s->K, s->G);
         case DFL_OP_SPEC_ACCEPT: return spec_ws_bytes(s->N, s->G, s->V);
+        case DFL_OP_BLOCK_FFN: return s->F > 0 ? ws_block_ffn(s->N, s->B, s->d, s->F, s->dtype) : 0;
         case DFL_OP_DRAFT_STEP: {
             const size_t e = esz(s->dtype);
             size_t b = al256((size_t)s->D * s->N * s->C * s->d * e);                 // Xc, all layers
@@ -115,6 +122,8 @@ extern "C" size_t dfl_workspace_size(dfl_op op, const dfl_shape* s) {
             size_t sub = ws_dual_kv_proj(s->N, s->B, s->d, s->dtype);
             const size_t at = ws_block_attn(s->N, s->C, s->B, s->Hq, s->Hkv, s->hd, s->dtype);
             if (at > sub) sub = at;
+            if (s->F > 0 && ws_block_ffn(s->N, s->B, s->d, s->F, s->dtype) > sub)
+                sub = ws_block_ffn(s->N, s->B, s->d, s->F, s->dtype);
             if (s->V > 0) {
                 const size_t lm = ws_lm_head(s->N, s->B, 1, s->d, s->V, s->dtype, true);
                 if (lm > sub) sub = lm;
@@ -315,6 +324,63 @@ extern "C" dfl_status dfl_block_attn(const void* Q, const void* Kc, const void* 
     return gemm_tc(ctx, g, st);
 }
 
+// ------------------------------------------------------- feed-forward
+
+extern "C" dfl_status dfl_block_ffn(float* Xb, int32_t N, int32_t B, int32_t d, dfl_dtype dt, const float* ffn_gain,
+                                    float eps, const void* W1, const void* W3, const void* W2, int32_t F, void* ws,
+                                    size_t ws_bytes, dfl_stream stream) {
+    if (!Xb || !ffn_gain || !W1 || !W3 || !W2 || !ws || N <= 0 || B <= 0 || d <= 0 || F <= 0)
+        return DFL_ERR_INVALID_ARG;
+    if (dt != DFL_F32 && dt != DFL_BF16) return DFL_ERR_INVALID_ARG;
+    const void* ptrs[] = {Xb, ffn_gain, W1, W3, W2, ws};
+    for (const void* p : ptrs) if (!aligned16(p)) return DFL_ERR_MISALIGNED;
+    if (d % 8 != 0 || F % 8 != 0) return DFL_ERR_MISALIGNED;
+    if (ws_bytes < ws_block_ffn(N, B, d, F, dt)) return DFL_ERR_WORKSPACE;
+    DeviceCtx* ctx = current_ctx();
+    if (!ctx) return DFL_ERR_NO_DEVICE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int64_t M = (int64_t)N * B;
+    uint8_t* p = static_cast<uint8_t*>(ws);
+    dfl_status rc;
+    if (dt == DFL_F32) {
+        float* Xn = reinterpret_cast<float*>(carve(p, (size_t)M * d * 4));
+        float* gate = reinterpret_cast<float*>(carve(p, (size_t)M * F * 4));
+        float* up = reinterpret_cast<float*>(carve(p, (size_t)M * F * 4));
+        float* h = reinterpret_cast<float*>(carve(p, (size_t)M * F * 4));
+        if ((rc = rmsnorm_rows(Xb, d, M, 1, 1, 0, ffn_gain, eps, Xn, false, st)) != DFL_OK) return rc;
+        if ((rc = gemm_f32(Xn, static_cast<const float*>(W1), gate, (int)M, F, d, F, 0, st)) != DFL_OK) return rc;
+        if ((rc = gemm_f32(Xn, static_cast<const float*>(W3), up, (int)M, F, d, F, 0, st)) != DFL_OK) return rc;
+        if ((rc = swiglu_f32(gate, up, h, M * F, st)) != DFL_OK) return rc;
+        return gemm_f32(h, static_cast<const float*>(W2), Xb, (int)M, d, F, d, 1, st);
+    }
+    if (F % 64 != 0 || d % 32 != 0) return DFL_ERR_UNSUPPORTED_SHAPE;
+    void* Xn = carve(p, (size_t)M * d * 2);
+    void* h = carve(p, (size_t)M * F * 2);
+    if ((rc = rmsnorm_rows(Xb, d, M, 1, 1, 0, ffn_gain, eps, Xn, true, st)) != DFL_OK) return rc;
+    {   // h = silu(Xn W1^T) * (Xn W3^T): tiles hold gate and up of the same features
+        GemmArgs g{};
+        g.A = Xn; g.M = (int)M; g.K = d;
+        g.B[0] = W1; g.B[1] = W3; g.b_rows[0] = F; g.b_rows[1] = F; g.nb = 2; g.N = 2 * F;
+        g.split_b = 1;
+        g.bn = 0;
+        g.m_inner = 1;
+        g.epi = EPI_SWIGLU;
+        g.ep.seg[0] = GemmSeg{h, 0, F, 0};
+        g.ep.nseg = 1;
+        g.tag = "gemm_ffn_gate_up";
+        if ((rc = gemm_tc(ctx, g, st)) != DFL_OK) return rc;
+    }
+    GemmArgs g{};   // Xb += h W2^T
+    g.A = h; g.M = (int)M; g.K = F;
+    g.B[0] = W2; g.b_rows[0] = d; g.b_begin[0] = 0; g.nb = 1; g.N = d;
+    g.bn = 0;
+    g.m_inner = 1;
+    g.epi = EPI_RESID;
+    g.ep.resid = Xb; g.ep.ld_resid = d;
+    g.tag = "gemm_ffn_down";
+    return gemm_tc(ctx, g, st);
+}
+
 // ---------------------------------------------------------------- LM head
 
 extern "C" dfl_status dfl_lm_head_argmax(const float* Xb, int32_t N, int32_t B, int32_t row0, int32_t d,
@@ -406,13 +472,16 @@ extern "C" dfl_status dfl_draft_step(const dfl_step_args* a, void* ws, size_t ws
     if ((a->tv_alpha || a->tv_tokens || a->accept_rule != 0) && !a->vlog) return DFL_ERR_INVALID_ARG;
     if (a->tv_tokens && !a->tv_alpha) return DFL_ERR_INVALID_ARG;
     if (a->accept_rule != 0 && a->accept_rule != 1) return DFL_ERR_INVALID_ARG;
+    if (a->F < 0 || (a->F > 0 && !a->ffn_gain)) return DFL_ERR_INVALID_ARG;
     for (int l = 0; l < a->D; ++l) {
         const dfl_layer_weights& w = a->layers[l];
         if (!w.Wq || !w.Wkc || !w.Wvc || !w.Wkb || !w.Wvb || !w.Wo) return DFL_ERR_INVALID_ARG;
+        if (a->F > 0 && (!w.W1 || !w.W3 || !w.W2)) return DFL_ERR_INVALID_ARG;
     }
     dfl_shape s{};
     s.N = a->N; s.C = a->C; s.B = a->B; s.d = a->d; s.Hq = a->Hq; s.Hkv = a->Hkv; s.hd = a->hd; s.D = a->D;
     s.L = a->L; s.V = a->V; s.K = a->sample ? a->sample->K : 0; s.G = a->B - 1; s.row0 = 1; s.dtype = dt;
+    s.F = a->F;
     if (ws_bytes < dfl_workspace_size(DFL_OP_DRAFT_STEP, &s)) return DFL_ERR_WORKSPACE;
     if (!aligned16(ws)) return DFL_ERR_MISALIGNED;
     if (!current_ctx()) return DFL_ERR_NO_DEVICE;
@@ -455,6 +524,9 @@ extern "C" dfl_status dfl_draft_step(const dfl_step_args* a, void* ws, size_t ws
             return rc;
         if ((rc = dfl_block_attn(Q, Kc, Vc, Kb, Vb, N, C, B, a->Hq, a->Hkv, a->hd, ddt, w.Wo, d, a->Xb, sub,
                                  sub_bytes, stream)) != DFL_OK)
+            return rc;
+        if (a->F > 0 && (rc = dfl_block_ffn(a->Xb, N, B, d, ddt, a->ffn_gain + (size_t)l * d, a->eps, w.W1, w.W3,
+                                            w.W2, a->F, sub, sub_bytes, stream)) != DFL_OK)
             return rc;
     }
     if (a->V == 0) return DFL_OK;

@@ -74,7 +74,7 @@ dfl_status launch(DeviceCtx* ctx, const GemmArgs& g, const GemmShape& sh, const 
 template <int BN, int EPI>
 dfl_status launch_cm(DeviceCtx* ctx, const GemmArgs& g, const GemmShape& sh, const CUtensorMap (&mb)[3],
                      const CUtensorMap& ma, cudaStream_t st, int slot, int cm) {
-    if (cm == 2) return launch<BN, EPI, 2>(ctx, g, sh, mb, ma, st, slot + 6);
+    if (cm == 2) return launch<BN, EPI, 2>(ctx, g, sh, mb, ma, st, slot + 8);
     return launch<BN, EPI, 1>(ctx, g, sh, mb, ma, st, slot);
 }
 
@@ -85,6 +85,7 @@ dfl_status launch_cm(DeviceCtx* ctx, const GemmArgs& g, const GemmShape& sh, con
 // SM when every tile costs ~its width -- preferring 256 on ties; 256 needs
 // every B segment to start on a 256-column boundary.
 static int pick_bn(const GemmArgs& g, int sm_count) {
+    if (g.split_b) return (g.N / 2) % 128 == 0 ? 256 : 128;
     bool ok256 = true;
     for (int j = 0; j < g.nb; ++j) ok256 = ok256 && (g.b_begin[j] % 256 == 0);
     if (!ok256) return 128;
@@ -113,6 +114,8 @@ dfl_status gemm_tc(DeviceCtx* ctx, const GemmArgs& g_in, cudaStream_t st) {
     sh.num_kb = (g.K + GEMM_BK - 1) / GEMM_BK;
     sh.m_inner = g.m_inner;
     sh.nb = g.nb;
+    sh.split_b = g.split_b;
+    if (g.split_b && (g.nb != 2 || (g.N / 2) % (g.bn / 2) != 0)) return DFL_ERR_UNSUPPORTED_SHAPE;
     // Pair the M-tiles of each N-tile in 2-CTA clusters (B tile multicast) when
     // there is more than one M-tile.
     const int cm = sh.tiles_m >= 2 ? 2 : 1;
@@ -122,18 +125,20 @@ dfl_status gemm_tc(DeviceCtx* ctx, const GemmArgs& g_in, cudaStream_t st) {
         const int jj = j < g.nb ? j : 0;
         if (!aligned16(g.B[jj])) return DFL_ERR_MISALIGNED;
         // every tile of BN columns must come from one B map
-        if (j < g.nb && (g.b_begin[j] % g.bn != 0)) return DFL_ERR_UNSUPPORTED_SHAPE;
-        if (!make_map(&mb[j], g.B[jj], g.b_rows[jj], g.K, g.bn / cm)) return DFL_ERR_CUDA;
+        if (j < g.nb && !g.split_b && (g.b_begin[j] % g.bn != 0)) return DFL_ERR_UNSUPPORTED_SHAPE;
+        if (!make_map(&mb[j], g.B[jj], g.b_rows[jj], g.K, g.split_b ? g.bn / 2 : g.bn / cm)) return DFL_ERR_CUDA;
         sh.b_begin[j] = g.b_begin[jj];
     }
-    const int slot = (g.bn == 256 ? 0 : 3) + g.epi;
+    const int slot = (g.bn == 256 ? 0 : 4) + g.epi;
     if (g.bn == 256) {
         if (g.epi == EPI_STORE) return launch_cm<256, EPI_STORE>(ctx, g, sh, mb, ma, st, slot, cm);
         if (g.epi == EPI_RESID) return launch_cm<256, EPI_RESID>(ctx, g, sh, mb, ma, st, slot, cm);
+        if (g.epi == EPI_SWIGLU) return launch_cm<256, EPI_SWIGLU>(ctx, g, sh, mb, ma, st, slot, cm);
         return launch_cm<256, EPI_ARGMAX>(ctx, g, sh, mb, ma, st, slot, cm);
     }
     if (g.epi == EPI_STORE) return launch_cm<128, EPI_STORE>(ctx, g, sh, mb, ma, st, slot, cm);
     if (g.epi == EPI_RESID) return launch_cm<128, EPI_RESID>(ctx, g, sh, mb, ma, st, slot, cm);
+    if (g.epi == EPI_SWIGLU) return launch_cm<128, EPI_SWIGLU>(ctx, g, sh, mb, ma, st, slot, cm);
     return launch_cm<128, EPI_ARGMAX>(ctx, g, sh, mb, ma, st, slot, cm);
 }
 

@@ -9,7 +9,9 @@
 //   EPI_RESID  fp32 residual accumulate (out += C);
 //   EPI_ARGMAX per-row max / argmax over the tile's columns (lowest column on
 //              ties), optional fp32 logits store and optional per-tile
-//              sum of exp((z - tile max) / T) in fp64 for sampling.
+//              sum of exp((z - tile max) / T) in fp64 for sampling;
+//   EPI_SWIGLU the B tile is [gate rows of W1 ; up rows of W3] for the same
+//              BN/2 features; stores silu(gate) * up as bf16.
 // The grid is persistent (one CTA per SM); tiles are walked in an order that
 // keeps the shared operand of consecutive tiles in L2.
 #pragma once
@@ -18,7 +20,7 @@
 
 namespace dfl {
 
-enum EpiKind { EPI_STORE = 0, EPI_RESID = 1, EPI_ARGMAX = 2 };
+enum EpiKind { EPI_STORE = 0, EPI_RESID = 1, EPI_ARGMAX = 2, EPI_SWIGLU = 3 };
 
 struct GemmSeg {
     void* out;        // bf16 [M][ld] (EPI_STORE)
@@ -53,6 +55,7 @@ struct GemmShape {
     int m_inner;         // 1: consecutive tiles walk M (share B); 0: walk N (share A)
     int b_begin[3];      // first column served by B tensor map 1, 2, 3
     int nb;              // number of B tensor maps
+    int split_b;         // B tile = [BN/2 rows of map 0 ; BN/2 rows of map 1] at rows tn * BN/2
 };
 
 constexpr int GEMM_BM = 128;
@@ -203,6 +206,24 @@ __device__ __forceinline__ void epi_argmax(const GemmShape& sh, const GemmEpi& e
     }
 }
 
+template <int BN>
+__device__ __forceinline__ void epi_swiglu(const GemmShape& sh, const GemmEpi& ep, uint32_t tbase, int row, int tn) {
+    const bool ok = row < sh.M;
+    const GemmSeg sg = ep.seg[0];
+    __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(sg.out) + (int64_t)(ok ? row : 0) * sg.ld + tn * (BN / 2);
+    #pragma unroll 1
+    for (int c = 0; c < BN / 64; ++c) {
+        float g[32], u[32];
+        tmem_ld32(tbase + c * 32, g);
+        tmem_ld32(tbase + BN / 2 + c * 32, u);
+        if (ok) {
+            #pragma unroll
+            for (int j = 0; j < 32; ++j) g[j] = g[j] / (1.f + expf(-g[j])) * u[j];
+            store_bf16x32(out + c * 32, g);
+        }
+    }
+}
+
 // ------------------------------------------------------------------- kernel
 //
 // CM = 1: one CTA per output tile.  CM = 2: clusters of two CTAs own the two
@@ -279,7 +300,17 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     if (*abort_flag || !mbar_wait(&empty[stage], phase ^ 1, err)) { aborted = true; break; }
                     mbar_arrive_expect_tx(&full[stage], Cfg::A_BYTES + Cfg::B_BYTES);
                     tma_load_2d(sA + stage * Cfg::A_BYTES, &tmA, kb * GEMM_BK, m0, &full[stage]);
-                    if (CM == 1) {
+                    if (sh.split_b) {   // [gate half (map 0) ; up half (map 1)] of the same features
+                        const int fr = tn * (BN / 2);
+                        if (CM == 1) {
+                            tma_load_2d(sB + stage * Cfg::B_BYTES, &tmB0, kb * GEMM_BK, fr, &full[stage]);
+                            tma_load_2d(sB + stage * Cfg::B_BYTES + Cfg::B_BYTES / 2, &tmB1, kb * GEMM_BK, fr,
+                                        &full[stage]);
+                        } else {
+                            tma_load_2d_mc(sB + stage * Cfg::B_BYTES + crank * (Cfg::B_BYTES / 2),
+                                           crank ? &tmB1 : &tmB0, kb * GEMM_BK, fr, &full[stage], kPair);
+                        }
+                    } else if (CM == 1) {
                         tma_load_2d(sB + stage * Cfg::B_BYTES, mb, kb * GEMM_BK, nb0, &full[stage]);
                     } else {   // this CTA's share of the B tile, to every CTA of the cluster
                         tma_load_2d_mc(sB + stage * Cfg::B_BYTES + crank * (Cfg::B_BYTES / CM), mb, kb * GEMM_BK,
@@ -357,6 +388,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
             if (EPI == EPI_STORE) epi_store<BN>(sh, ep, tbase, row, tn * BN);
             else if (EPI == EPI_RESID) epi_resid<BN>(sh, ep, tbase, row, tn * BN);
+            else if (EPI == EPI_SWIGLU) epi_swiglu<BN>(sh, ep, tbase, row, tn);
             else epi_argmax<BN>(sh, ep, tbase, row, tn * BN, tn);
             tc_fence_before();
             mbar_arrive(&tempty[acc]);

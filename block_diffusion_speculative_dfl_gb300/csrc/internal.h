@@ -15,7 +15,7 @@ struct DeviceCtx {
     int device = -1;
     int sm_count = 0;
     int* err_word = nullptr;       // device address of this device's error word
-    bool gemm_attr_set[12] = {};   // max-dynamic-smem set for gemm instantiations
+    bool gemm_attr_set[16] = {};   // max-dynamic-smem set for gemm instantiations
     bool mix_attr_set = false;
 };
 
@@ -59,6 +59,7 @@ struct GemmArgs {
     int epi;                // EpiKind
     GemmEpi ep;
     const char* tag;        // name in kernel traces
+    int split_b;            // EPI_SWIGLU: B tile halves from maps 0 (gate) and 1 (up); N = 2F
 };
 
 dfl_status gemm_tc(DeviceCtx* ctx, const GemmArgs& g, cudaStream_t st);

@@ -371,6 +371,21 @@ dfl_status rope_inplace_f32(float* x, int64_t rows, int heads, int hd, int per, 
     return last_launch();
 }
 
+// h[i] = silu(gate[i]) * up[i] (fp32 path of the feed-forward block).
+__global__ void swiglu_f32_kernel(const float* gate, const float* up, float* h, int64_t n) {
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        const float g = gate[i];
+        h[i] = g / (1.f + expf(-g)) * up[i];
+    }
+}
+
+dfl_status swiglu_f32(const float* gate, const float* up, float* h, int64_t n, cudaStream_t st) {
+    ProfScope ps("swiglu_f32", st);
+    const int64_t blocks = (n + 255) / 256;
+    swiglu_f32_kernel<<<(unsigned)(blocks < 4096 ? blocks : 4096), 256, 0, st>>>(gate, up, h, n);
+    return last_launch();
+}
+
 // fp32 block attention: one CTA per (sequence, query head), one warp per
 // query row at a time, online softmax over [context ; block] keys, no mask.
 __global__ void attn_f32_kernel(const float* Q, const float* Kc, const float* Vc, const float* Kb, const float* Vb,

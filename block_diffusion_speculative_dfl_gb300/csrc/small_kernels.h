@@ -25,6 +25,7 @@ dfl_status rope_inplace_f32(float* x, int64_t rows, int heads, int hd, int per, 
 dfl_status attn_f32(const float* Q, const float* Kc, const float* Vc, const float* Kb, const float* Vb, int N, int C,
                     int B, int Hq, int Hkv, int hd, float* O, cudaStream_t st);
 dfl_status selftest_wait(int* status, uint64_t limit_ns, cudaStream_t st);
+dfl_status swiglu_f32(const float* gate, const float* up, float* h, int64_t n, cudaStream_t st);
 
 // bf16 block attention (tensor cores); writes O bf16 [N*B][Hq*hd].  ws holds
 // split-KV partials when more than one split is used.

@@ -37,6 +37,7 @@ class DraftShape:
     seed: int = 0
     eps: float = 1e-6
     rope_theta: float = 1e6
+    F: int = 0
 
     @property
     def torch_dtype(self):
@@ -51,7 +52,7 @@ class DraftModel:
     """Drafter parameters, workspace and outputs for one shape on one device."""
 
     def __init__(self, shape: DraftShape, mix_logits, mix_gain, blk_gain, final_gain, layers, W_lm=None,
-                 device="cuda", tv=False, accept_rule=0, accept_seed=0):
+                 device="cuda", tv=False, accept_rule=0, accept_seed=0, ffn_gain=None):
         s = self.shape = shape
         dev = torch.device(device)
         wd = shape.torch_dtype
@@ -67,12 +68,13 @@ class DraftModel:
         self.W_lm = dev_t(W_lm, wd) if (W_lm is not None and s.V > 0) else None
         self.rope = torch.empty((s.C + s.B, s.hd // 2, 2), dtype=torch.float32, device=dev)
         _lib.dfl_rope_table(self.rope, s.C + s.B, s.hd, s.rope_theta)
-        self._lw = (LayerWeights * s.D)(*[LayerWeights(*[_lib.ptr(w[k]) for k in
-                                                          ("Wq", "Wkc", "Wvc", "Wkb", "Wvb", "Wo")])
-                                          for w in self.layers])
+        names = ("Wq", "Wkc", "Wvc", "Wkb", "Wvb", "Wo") + (("W1", "W3", "W2") if s.F > 0 else ())
+        self._lw = (LayerWeights * s.D)(*[LayerWeights(*[_lib.ptr(w[k]) for k in names]) for w in self.layers])
+        self.ffn_gain = dev_t(ffn_gain, torch.float32) if s.F > 0 else None
         self._sp = SampleParams(s.K, s.T, s.seed) if s.K > 0 else None
         self.ws_bytes = _lib.workspace_size(_lib.DFL_OP_DRAFT_STEP, N=s.N, C=s.C, B=s.B, d=s.d, Hq=s.Hq, Hkv=s.Hkv,
-                                            hd=s.hd, D=s.D, L=s.L, V=s.V, K=s.K, G=s.B - 1, row0=1, dtype=s.dt)
+                                            hd=s.hd, D=s.D, L=s.L, V=s.V, K=s.K, G=s.B - 1, row0=1, dtype=s.dt,
+                                            F=s.F)
         self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
         self.Xb = torch.empty((s.N, s.B, s.d), dtype=torch.float32, device=dev)
         n = s.B - 1
@@ -107,6 +109,7 @@ class DraftModel:
         a.draft, a.logits = _lib.ptr(self.draft), _lib.ptr(self.logits)
         a.target = _lib.ptr(target)
         a.accept_len, a.bonus = _lib.ptr(self.accept_len), _lib.ptr(self.bonus)
+        a.F, a.ffn_gain = s.F, _lib.ptr(self.ffn_gain)
         if self._sp is not None:
             a.sample = C.pointer(self._sp)
             a.samples = _lib.ptr(self.samples)

@@ -28,7 +28,7 @@ __all__ = [
     "Workload", "WORKLOADS", "round_bf16", "bf16_bits", "bits_to_f32",
     "gen_hidden", "gen_hidden_scales", "gen_mix_logits", "gen_gains",
     "gen_layer_weights", "gen_lm_head", "gen_block_init", "gen_verifier_logits",
-    "plant_targets", "geometric_prefix", "WEIGHT_NAMES",
+    "plant_targets", "geometric_prefix", "WEIGHT_NAMES", "FFN_WEIGHT_NAMES", "gen_ffn_gains",
 ]
 
 
@@ -56,6 +56,7 @@ class Workload:
     verifier_scale: float = 4.0
     rope_theta: float = 1.0e6
     eps: float = 1.0e-6
+    F: int = 0                 # feed-forward width of full draft layers (0: no FFN)
 
     @property
     def gamma(self) -> int:
@@ -86,12 +87,20 @@ WORKLOADS = {
                                  Hkv=8, hd=128, D=7, L=9, B=33, C=1024,
                                  V=151936, dtype="bf16", seed=1005, K=8,
                                  T=1.5, philox_seed=0x5EEDD1F5),
+    # A next-row workload (not one of the five): the Qwen3-8B drafter with full
+    # decoder layers, i.e. a SwiGLU feed-forward block of Qwen3-8B's width.
+    "qwen3_8b_drafter_ffn": Workload("qwen3_8b_drafter_ffn", N=32, d=4096, Hq=32,
+                                     Hkv=8, hd=128, D=7, L=9, B=16, C=2048,
+                                     V=151936, dtype="bf16", seed=1006,
+                                     geom_p=0.15, F=12288),
 }
 
 # Tensor ids keying the PCG64 streams.
 _TID_H, _TID_HSCALE, _TID_MIX, _TID_W, _TID_LM = 1, 2, 3, 4, 5
 _TID_ANCHOR, _TID_MASK, _TID_VLOG, _TID_PLANT, _TID_GAIN = 6, 7, 8, 9, 10
+_TID_FFN_GAIN = 11
 WEIGHT_NAMES = ("Wq", "Wkc", "Wvc", "Wkb", "Wvb", "Wo")
+FFN_WEIGHT_NAMES = ("W1", "W3", "W2")
 
 _THREADS = max(1, min(16, len(os.sched_getaffinity(0))))
 
@@ -190,22 +199,33 @@ def gen_gains(w: Workload, random: bool = False):
 
 def weight_shapes(w: Workload) -> dict:
     """[out][in] shapes (nn.Linear layout) of one draft layer's weights."""
-    return {"Wq": (w.Hq * w.hd, w.d), "Wkc": (w.Hkv * w.hd, w.d),
-            "Wvc": (w.Hkv * w.hd, w.d), "Wkb": (w.Hkv * w.hd, w.d),
-            "Wvb": (w.Hkv * w.hd, w.d), "Wo": (w.d, w.Hq * w.hd)}
+    shapes = {"Wq": (w.Hq * w.hd, w.d), "Wkc": (w.Hkv * w.hd, w.d),
+              "Wvc": (w.Hkv * w.hd, w.d), "Wkb": (w.Hkv * w.hd, w.d),
+              "Wvb": (w.Hkv * w.hd, w.d), "Wo": (w.d, w.Hq * w.hd)}
+    if w.F > 0:
+        shapes.update({"W1": (w.F, w.d), "W3": (w.F, w.d), "W2": (w.d, w.F)})
+    return shapes
+
+
+def gen_ffn_gains(w: Workload, random: bool = False) -> np.ndarray:
+    """Feed-forward RMSNorm gains [D][d]: ones, or U(0.5, 1.5) for tests."""
+    if not random:
+        return np.ones((w.D, w.d), np.float32)
+    return _rng(w.seed, _TID_FFN_GAIN).uniform(0.5, 1.5, (w.D, w.d)).astype(np.float32)
 
 
 def gen_layer_weights(w: Workload, layer: int) -> dict:
     """One draft layer's weights, each N(0, std 1/sqrt(fan_in))."""
     shapes = weight_shapes(w)
+    names = WEIGHT_NAMES + (FFN_WEIGHT_NAMES if w.F > 0 else ())
 
     def one(k):
-        name = WEIGHT_NAMES[k]
+        name = names[k]
         out_f, in_f = shapes[name]
         return _finish(_normal((w.seed, _TID_W, layer, k), (out_f, in_f),
                                1.0 / np.sqrt(in_f)), w.dtype)
 
-    return dict(zip(WEIGHT_NAMES, _parallel(one, list(range(len(WEIGHT_NAMES))))))
+    return dict(zip(names, _parallel(one, list(range(len(names))))))
 
 
 def gen_lm_head(w: Workload, as_bits: bool = False) -> np.ndarray:

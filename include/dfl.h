@@ -73,6 +73,7 @@ typedef struct dfl_sample_params {
 typedef struct dfl_shape {
     int32_t N, C, B, d, Hq, Hkv, hd, D, L, V, K, G, row0;
     int32_t dtype;    /* a dfl_dtype */
+    int32_t F;        /* FFN width (DFL_OP_BLOCK_FFN, DFL_OP_DRAFT_STEP) */
 } dfl_shape;
 
 typedef enum dfl_op {
@@ -82,7 +83,8 @@ typedef enum dfl_op {
     DFL_OP_SELF_SELECT = 4,
     DFL_OP_DRAFT_STEP = 5,
     DFL_OP_TV_ACCEPTANCE = 6,
-    DFL_OP_SPEC_ACCEPT = 7
+    DFL_OP_SPEC_ACCEPT = 7,
+    DFL_OP_BLOCK_FFN = 8
 } dfl_op;
 
 /* Library version string (static storage). */
@@ -305,6 +307,24 @@ dfl_status dfl_spec_accept(const float* logits, float T, const void* vlog, dfl_d
                            int32_t G, int32_t V, uint64_t seed, int32_t* accept_len,
                            int32_t* next_token, void* ws, size_t ws_bytes, dfl_stream stream);
 
+/*
+ * dfl_block_ffn -- residual SwiGLU feed-forward block of a full draft layer.
+ *   Reading (the pages give no width or form; the DFlash article's drafter
+ *   layers are decoder layers of the target family): Qwen-style gate/up/down
+ *     Xn = RMSNorm(Xb; ffn_gain),  Xb <- Xb + (silu(Xn W1^T) * (Xn W3^T)) W2^T
+ *   Xb   in/out, fp32 [N*B][d]
+ *   W1, W3 in, dt [F][d]; W2 in, dt [d][F]; ffn_gain in, fp32 [d]
+ *   ws   dfl_workspace_size(DFL_OP_BLOCK_FFN) bytes (normalised rows and the
+ *        [N*B][F] hidden activations)
+ *   bf16: one tensor-core GEMM for gate and up with the SwiGLU in its
+ *   epilogue (needs F % 64 == 0), then the down projection with a residual
+ *   epilogue.  fp32: CUDA-core GEMMs.
+ *   Errors: INVALID_ARG, UNSUPPORTED_SHAPE, MISALIGNED, WORKSPACE.
+ */
+dfl_status dfl_block_ffn(float* Xb, int32_t N, int32_t B, int32_t d, dfl_dtype dt,
+                         const float* ffn_gain, float eps, const void* W1, const void* W3,
+                         const void* W2, int32_t F, void* ws, size_t ws_bytes, dfl_stream stream);
+
 /* One draft layer's weights (device pointers, dtype of the step). */
 typedef struct dfl_layer_weights {
     const void* Wq;   /* [Hq*hd][d] */
@@ -313,6 +333,9 @@ typedef struct dfl_layer_weights {
     const void* Wkb;  /* [Hkv*hd][d] */
     const void* Wvb;  /* [Hkv*hd][d] */
     const void* Wo;   /* [d][Hq*hd] */
+    const void* W1;   /* [F][d] FFN gate, or NULL when the step's F == 0 */
+    const void* W3;   /* [F][d] FFN up */
+    const void* W2;   /* [d][F] FFN down */
 } dfl_layer_weights;
 
 /* Arguments of a whole draft step.  Host struct; tensors are device memory. */
@@ -349,6 +372,8 @@ typedef struct dfl_step_args {
                                       accepted length and next token replace
                                       accept_len / bonus */
     uint64_t accept_seed;          /* Philox key of the stochastic rule */
+    int32_t F;                     /* FFN width; 0: layers without a feed-forward block */
+    const float* ffn_gain;         /* in [D][d] when F > 0 */
 } dfl_step_args;
 
 /*

@@ -334,3 +334,35 @@ def test_bounded_wait_times_out_and_context_survives():
     bo = torch.empty(1, dtype=torch.int32, device="cuda")
     dfl.dfl_greedy_accept(dev(np.array([[1, 2]], np.int32)), dev(np.array([[1, 5, 7]], np.int32)), 1, 2, al, bo)
     assert (int(al.item()), int(bo.item())) == (1, 5)
+
+
+
+# --------------------------------------------------------- feed-forward --
+
+@pytest.mark.parametrize("N,B,d,F", [(3, 16, 256, 384), (20, 16, 512, 1024), (2, 33, 256, 192)])
+def test_block_ffn_bf16(N, B, d, F):
+    rng = np.random.default_rng(N * F)
+    Xb = rng.standard_normal((N * B, d)).astype(np.float32)
+    g = rng.uniform(0.5, 1.5, d).astype(np.float32)
+    W1, W3 = rng_bf16(rng, (F, d), d ** -0.5), rng_bf16(rng, (F, d), d ** -0.5)
+    W2 = rng_bf16(rng, (d, F), F ** -0.5)
+    Xd = dev(Xb)
+    wsb = dfl.workspace_size(dfl.DFL_OP_BLOCK_FFN, N=N, B=B, d=d, F=F, dtype=dfl.DFL_BF16)
+    ws = _ws(wsb)
+    dfl.dfl_block_ffn(Xd, N, B, d, dfl.DFL_BF16, dev(g), 1e-6, dev(W1, "bf16"), dev(W3, "bf16"), dev(W2, "bf16"), F,
+                      ws, wsb)
+    ref = orc.swiglu_ffn(Xb, g, W1, W3, W2, 1e-6)
+    assert_bf16_close(host(Xd) - Xb, ref - Xb, "ffn")
+
+
+def test_block_ffn_f32():
+    rng = np.random.default_rng(3)
+    N, B, d, F = 1, 16, 128, 200
+    f = lambda s, sc=1.0: (rng.standard_normal(s) * sc).astype(np.float32)
+    Xb, g = f((N * B, d)), rng.uniform(0.5, 1.5, d).astype(np.float32)
+    W1, W3, W2 = f((F, d), d ** -0.5), f((F, d), d ** -0.5), f((d, F), F ** -0.5)
+    Xd = dev(Xb)
+    wsb = dfl.workspace_size(dfl.DFL_OP_BLOCK_FFN, N=N, B=B, d=d, F=F, dtype=dfl.DFL_F32)
+    ws = _ws(wsb)
+    dfl.dfl_block_ffn(Xd, N, B, d, dfl.DFL_F32, dev(g), 1e-6, dev(W1), dev(W3), dev(W2), F, ws, wsb)
+    assert_f32_close(host(Xd), orc.swiglu_ffn(Xb, g, W1, W3, W2, 1e-6), "Xb")

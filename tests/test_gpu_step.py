@@ -11,8 +11,8 @@ import torch
 
 import block_diffusion_speculative_dfl_gb300 as dfl
 import oracle as orc
-from dfl_synth import (WORKLOADS, Workload, gen_block_init, gen_gains, gen_hidden, gen_layer_weights, gen_lm_head,
-                       gen_mix_logits, gen_verifier_logits, geometric_prefix, plant_targets)
+from dfl_synth import (WORKLOADS, Workload, gen_block_init, gen_ffn_gains, gen_gains, gen_hidden, gen_layer_weights,
+                       gen_lm_head, gen_mix_logits, gen_verifier_logits, geometric_prefix, plant_targets)
 from gpu_util import assert_bf16_close, assert_f32_close, check_samples, host
 
 pytestmark = pytest.mark.gpu
@@ -37,13 +37,15 @@ def _model(w, random_gains=False):
     layers = [gen_layer_weights(w, l) for l in range(w.D)]
     W_lm = gen_lm_head(w, as_bits=(w.dtype == "bf16")) if w.V > 0 else None
     shape = dfl.DraftShape(N=w.N, d=w.d, Hq=w.Hq, Hkv=w.Hkv, hd=w.hd, D=w.D, L=w.L, B=w.B, C=w.C, V=w.V,
-                           dtype=w.dtype, K=w.K, T=w.T, seed=w.philox_seed, eps=w.eps, rope_theta=w.rope_theta)
+                           dtype=w.dtype, K=w.K, T=w.T, seed=w.philox_seed, eps=w.eps, rope_theta=w.rope_theta,
+                           F=w.F)
+    g_ffn = gen_ffn_gains(w, random=random_gains)
     W_lm_t = None
     if W_lm is not None:
         W_lm_t = torch.from_numpy(W_lm.view(np.int16)).view(torch.bfloat16) if w.dtype == "bf16" else \
             torch.from_numpy(W_lm)
-    model = dfl.DraftModel(shape, mix, g_mix, g_blk, g_fin, layers, W_lm_t)
-    return model, dict(mix=mix, g_mix=g_mix, g_blk=g_blk, g_fin=g_fin, layers=layers, W_lm=W_lm)
+    model = dfl.DraftModel(shape, mix, g_mix, g_blk, g_fin, layers, W_lm_t, ffn_gain=g_ffn)
+    return model, dict(mix=mix, g_mix=g_mix, g_blk=g_blk, g_fin=g_fin, layers=layers, W_lm=W_lm, g_ffn=g_ffn)
 
 
 def _hidden_dev(w):
@@ -56,7 +58,8 @@ def _oracle_seq(w, p, n):
     """fp64 oracle draft forward + logits for sequence n."""
     Hn = gen_hidden(w, seqs=[n])
     Xb0 = gen_block_init(w)[n]
-    out = orc.draft_forward(Xb0, Hn, p["mix"], p["g_mix"], p["g_blk"], p["layers"], _shape(w), w.eps, w.rope_theta)
+    layers = [dict(W, g_ffn=p["g_ffn"][l]) if w.F > 0 else W for l, W in enumerate(p["layers"])]
+    out = orc.draft_forward(Xb0, Hn, p["mix"], p["g_mix"], p["g_blk"], layers, _shape(w), w.eps, w.rope_theta)
     z = None
     if w.V > 0:
         from dfl_synth import bits_to_f32
@@ -238,3 +241,20 @@ def test_self_selection_step_with_tv_and_stochastic_acceptance():
         a, y, margin = orc.speculative_accept(z[n], w.T, vl[sel[n]], samples[n, sel[n]], u_acc, u_res)
         if margin >= 1e-5:
             assert (int(host(model.accept_len)[n]), int(host(model.bonus)[n])) == (a, y)
+
+
+
+def test_small_bf16_drafter_with_ffn_layers():
+    w = Workload("smallffn", N=3, d=256, Hq=4, Hkv=2, hd=64, D=2, L=3, B=16, C=90, V=1200, dtype="bf16", seed=67,
+                 geom_p=0.3, F=384)
+    _run_greedy_workload(w, seqs=[0, 2], random_gains=True)
+
+
+def test_small_f32_drafter_with_ffn_layers():
+    w = Workload("smallffn32", N=1, d=128, Hq=2, Hkv=2, hd=64, D=2, L=2, B=8, C=40, V=500, dtype="f32", seed=71,
+                 geom_p=0.3, F=200, hidden_scale=False)
+    _run_greedy_workload(w, seqs=[0], random_gains=True)
+
+
+def test_qwen3_8b_drafter_ffn_full_size():
+    _run_greedy_workload(WORKLOADS["qwen3_8b_drafter_ffn"], seqs=[7])
