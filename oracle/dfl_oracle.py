@@ -267,6 +267,79 @@ def draft_forward(Xb0, Hn, mix, g_mix, g_blk, layers, shape: dict,
 
 
 # ---------------------------------------------------------------------------
+# Incremental context K/V (SpecDiff-2 notes, "Future work and limitations",
+# hardware-optimisation item: KV-cache support for gamma-length drafts)
+# ---------------------------------------------------------------------------
+
+def context_kv_rows(H_rows, mix_logits, g_mix, Wkc, Wvc, positions, shape: dict,
+                    eps: float, theta: float):
+    """Context keys and values of some context positions of one draft layer.
+
+    H_rows [L][m][d] holds the target hidden states of m context positions,
+    ``positions`` [m] their absolute positions.  The context side of a draft
+    layer works row by row: position t's key and value depend on the mixed,
+    normalised hidden states of position t alone, and the key also on t
+    through the rotary embedding.  So K/V computed for a context in pieces
+    equal K/V computed for it at once, which is what lets a drafter keep them
+    from one draft step to the next.
+    """
+    Hkv, hd = shape["Hkv"], shape["hd"]
+    Xc = mix_rmsnorm(H_rows, mix_logits, g_mix, eps)
+    m = Xc.shape[0]
+    K = (Xc @ np.asarray(Wkc, dtype=F64).T).reshape(m, Hkv, hd)
+    V = (Xc @ np.asarray(Wvc, dtype=F64).T).reshape(m, Hkv, hd)
+    cos, sin = rope_cos_sin(np.asarray(positions), hd, theta)
+    return apply_rope(K, cos, sin), V
+
+
+def draft_step_cached(Xb0, H_new, cache, mix, g_mix, g_blk, layers, shape: dict,
+                      eps: float, theta: float):
+    """One draft step over cached context K/V, appending the new positions.
+
+    ``cache`` is a list of D pairs (K [c0][Hkv][hd], V [c0][Hkv][hd]): the
+    context keys/values of the c0 positions seen in earlier steps, one pair per
+    draft layer.  H_new [L][m][d] holds the target hidden states of the m
+    positions c0..c0+m-1 that arrive with this step (m = 0 allowed).  Each
+    layer appends their K/V to its cache, then runs the block part over the
+    C = c0 + m cached positions, with the block at positions C..C+B-1 (the
+    same positions the one-shot step gives a context of length C).  Returns
+    the block output and the extended caches.
+
+    Reading (the pages name the missing cache, not its design): cached rows
+    are never recomputed, so the result equals the one-shot step over the
+    concatenated context.
+    """
+    Xb = np.asarray(Xb0, dtype=F64)
+    B = Xb.shape[0]
+    Hq, Hkv, hd = shape["Hq"], shape["Hkv"], shape["hd"]
+    H_new = np.asarray(H_new, dtype=F64)
+    m = H_new.shape[1]
+    new_cache = []
+    for l, W in enumerate(layers):
+        Kold, Vold = cache[l]
+        c0 = Kold.shape[0]
+        if m > 0:
+            Kn, Vn = context_kv_rows(H_new, mix[l], g_mix[l], W["Wkc"], W["Wvc"], np.arange(c0, c0 + m),
+                                     shape, eps, theta)
+            Kc, Vc = np.concatenate([Kold, Kn]), np.concatenate([Vold, Vn])
+        else:
+            Kc, Vc = np.asarray(Kold, dtype=F64), np.asarray(Vold, dtype=F64)
+        new_cache.append((Kc, Vc))
+        C = Kc.shape[0]
+        f = {k: np.asarray(v, dtype=F64) for k, v in W.items()}
+        Xn = rmsnorm(Xb, g_blk[l], eps)
+        cos, sin = rope_cos_sin(np.arange(C, C + B), hd, theta)
+        Q = apply_rope((Xn @ f["Wq"].T).reshape(B, Hq, hd), cos, sin)
+        Kb = apply_rope((Xn @ f["Wkb"].T).reshape(B, Hkv, hd), cos, sin)
+        Vb = (Xn @ f["Wvb"].T).reshape(B, Hkv, hd)
+        O = attention(Q, np.concatenate([Kc, Kb]), np.concatenate([Vc, Vb]), block_visibility(C, B))
+        Xb = Xb + O.reshape(B, Hq * hd) @ f["Wo"].T
+        if "W1" in f:
+            Xb = swiglu_ffn(Xb, W["g_ffn"], f["W1"], f["W3"], f["W2"], eps)
+    return Xb, new_cache
+
+
+# ---------------------------------------------------------------------------
 # Greedy acceptance (DFlare post, "Generating candidates in parallel")
 # ---------------------------------------------------------------------------
 

@@ -640,3 +640,71 @@ def test_draft_layer_with_ffn_adds_the_ffn_after_attention():
     b = orc.draft_layer(t["Xb"], t["Hn"], t["mix"], t["g_mix"], t["g_blk"], t["W"], t["shape"], 1e-6, 100.0)
     assert np.allclose(a["Xb_attn"], b["Xb"], atol=1e-13)
     assert np.allclose(a["Xb"], orc.swiglu_ffn(b["Xb"], W["g_ffn"], W["W1"], W["W3"], W["W2"], 1e-6), atol=1e-12)
+
+
+# ------------------------------------------------ incremental context K/V --
+
+def _two_layer_drafter(seed=51, B=3, C=11, L=2, d=8, Hq=4, Hkv=2, hd=4, F=0):
+    rng = np.random.default_rng(seed)
+    layers = []
+    for _ in range(2):
+        W = {"Wq": rng.normal(size=(Hq * hd, d)), "Wkc": rng.normal(size=(Hkv * hd, d)),
+             "Wvc": rng.normal(size=(Hkv * hd, d)), "Wkb": rng.normal(size=(Hkv * hd, d)),
+             "Wvb": rng.normal(size=(Hkv * hd, d)), "Wo": 0.3 * rng.normal(size=(d, Hq * hd))}
+        if F:
+            W.update(W1=rng.normal(size=(F, d)), W3=rng.normal(size=(F, d)), W2=0.3 * rng.normal(size=(d, F)),
+                     g_ffn=rng.uniform(0.5, 1.5, d))
+        layers.append(W)
+    return dict(Xb=rng.normal(size=(B, d)), Hn=rng.normal(size=(L, C, d)), mix=rng.normal(size=(2, L)),
+                g_mix=rng.uniform(0.5, 1.5, (2, d)), g_blk=rng.uniform(0.5, 1.5, (2, d)), layers=layers,
+                shape={"Hq": Hq, "Hkv": Hkv, "hd": hd})
+
+
+@pytest.mark.parametrize("F,chunks", [(0, (4, 0, 5, 2)), (5, (11,)), (0, (1,) * 11)])
+def test_cached_steps_equal_the_one_shot_step(F, chunks):
+    # Context K/V are a row-wise function of (hidden states, position), so a
+    # context that arrives in pieces over several steps gives the caches and
+    # the block output of one step over the whole context.
+    t = _two_layer_drafter(F=F)
+    D = 2
+    Hkv, hd = t["shape"]["Hkv"], t["shape"]["hd"]
+    cache = [(np.zeros((0, Hkv, hd)), np.zeros((0, Hkv, hd))) for _ in range(D)]
+    c0 = 0
+    for m in chunks:
+        Xb, cache = orc.draft_step_cached(t["Xb"], t["Hn"][:, c0:c0 + m], cache, t["mix"], t["g_mix"], t["g_blk"],
+                                          t["layers"], t["shape"], 1e-6, 100.0)
+        c0 += m
+        assert all(k.shape[0] == c0 and v.shape[0] == c0 for k, v in cache)
+        # every intermediate step equals the one-shot step over the prefix seen so far
+        ref = orc.draft_forward(t["Xb"], t["Hn"][:, :c0], t["mix"], t["g_mix"], t["g_blk"], t["layers"],
+                                t["shape"], 1e-6, 100.0, keep_layers=True)
+        assert np.allclose(Xb, ref["Xb"], atol=1e-12, rtol=0)
+    for l in range(D):
+        full = orc.draft_layer(t["Xb"], t["Hn"], t["mix"][l], t["g_mix"][l], t["g_blk"][l], t["layers"][l],
+                               t["shape"], 1e-6, 100.0)
+        assert np.allclose(cache[l][0], full["Kc"], atol=1e-12) and np.allclose(cache[l][1], full["Vc"], atol=1e-12)
+
+
+def test_cached_step_block_positions_follow_the_context_length():
+    # A step that appends nothing reproduces the output from the caches
+    # alone, and a cached key carries the rotation of the position it was
+    # appended at.
+    t = _two_layer_drafter()
+    C = t["Hn"].shape[1]
+    empty = [(np.zeros((0, 2, 4)), np.zeros((0, 2, 4))) for _ in range(2)]
+    Xa, cache = orc.draft_step_cached(t["Xb"], t["Hn"], empty, t["mix"], t["g_mix"], t["g_blk"], t["layers"],
+                                      t["shape"], 1e-6, 100.0)
+    # a step that appends nothing reproduces the same output from the caches alone
+    Xb, cache2 = orc.draft_step_cached(t["Xb"], t["Hn"][:, :0], cache, t["mix"], t["g_mix"], t["g_blk"],
+                                       t["layers"], t["shape"], 1e-6, 100.0)
+    assert np.allclose(Xa, Xb, atol=1e-13)
+    assert all(np.array_equal(a[0], b[0]) for a, b in zip(cache, cache2))
+    # keys of one position, cached at another position, are a different rotation
+    k_at_0, _ = orc.context_kv_rows(t["Hn"][:, :1], t["mix"][0], t["g_mix"][0], t["layers"][0]["Wkc"],
+                                    t["layers"][0]["Wvc"], [0], t["shape"], 1e-6, 100.0)
+    k_at_5, _ = orc.context_kv_rows(t["Hn"][:, :1], t["mix"][0], t["g_mix"][0], t["layers"][0]["Wkc"],
+                                    t["layers"][0]["Wvc"], [5], t["shape"], 1e-6, 100.0)
+    assert np.allclose(k_at_0, cache[0][0][:1], atol=1e-13)
+    assert not np.allclose(k_at_0, k_at_5)
+    # rotation keeps each rotated pair's norm
+    assert np.allclose(np.linalg.norm(k_at_0), np.linalg.norm(k_at_5), atol=1e-12)
