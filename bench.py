@@ -32,6 +32,7 @@ METRIC = "drafted block-tokens/sec on 1 GB300 (+accept epilogue); % of HBM/tenso
 UNIT = "block-tokens/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 256 << 20
+PREFILL_ROWS = 512   # context rows per sequence and step while a cached workload's caches are filled
 
 
 def parse_args(argv=None):
@@ -132,18 +133,24 @@ def ncu_traffic(kernel, workload):
     return None
 
 
-def kernel_work(w):
-    """Algorithmic work per launch: {kernel: (flops, bytes)} (bf16 operands, 2 B)."""
+def kernel_work(w, ctx_lens=None):
+    """Algorithmic work per launch: {kernel: (flops, bytes)} (bf16 operands, 2 B).
+
+    For a cached-context workload (w.R > 0) ``ctx_lens`` holds each
+    sequence's attended context length; the mix and the context projection
+    then cover the N*R new-row slots of one step.
+    """
     N, C, B, d, Hq, Hkv, hd, D, L, V = w.N, w.C, w.B, w.d, w.Hq, w.Hkv, w.hd, w.D, w.L, w.V
     kv, qd = Hkv * hd, Hq * hd
-    rows_c, rows_b = N * C, N * B
+    rows_c, rows_b = N * (w.R if w.R > 0 else C), N * B
+    keys = float(np.sum(np.asarray(ctx_lens) + B)) if w.R > 0 else float(N * (C + B))   # keys over all sequences
+    ctx = "gemm_ctx_kv_append" if w.R > 0 else "gemm_ctx_kv"
     work = {
         "mix_rmsnorm_bf16": (2.0 * D * L * rows_c * d, 2.0 * (L + D) * rows_c * d),
-        "gemm_ctx_kv": (2.0 * rows_c * 2 * kv * d, 2.0 * (rows_c * d + 2 * kv * d + rows_c * 2 * kv)),
+        ctx: (2.0 * rows_c * 2 * kv * d, 2.0 * (rows_c * d + 2 * kv * d + rows_c * 2 * kv)),
         "gemm_block_qkv": (2.0 * rows_b * (qd + 2 * kv) * d,
                            2.0 * (rows_b * d + (qd + 2 * kv) * d + rows_b * (qd + 2 * kv))),
-        "attn_bf16": (4.0 * rows_b * Hq * (C + B) * hd,
-                      2.0 * (2 * N * (C + B) * kv + 2 * rows_b * qd)),
+        "attn_bf16": (4.0 * B * Hq * keys * hd, 2.0 * (2 * keys * kv + 2 * rows_b * qd)),
         "gemm_o_proj": (2.0 * rows_b * d * qd, 2.0 * (rows_b * qd + d * qd) + 8.0 * rows_b * d),
     }
     if w.F > 0:
@@ -243,19 +250,73 @@ def oracle_step(w, p, n, W_lm_f32, vlog_n=None):
     return time.perf_counter() - t0
 
 
+def oracle_step_cached(w, p, n, W_lm_f32, vlog_n=None):
+    """The fp64 oracle's cached draft step for sequence n (test infrastructure, CPU).
+
+    The caches of the sequence's c0 positions are built first (not timed);
+    the timed part appends its n_new rows, runs the block and the LM head and
+    takes the argmax and greedy acceptance.
+    """
+    import oracle as orc
+    from dfl_synth import gen_block_init, gen_cache_state, gen_hidden_rows
+    c0, m = (int(x[n]) for x in gen_cache_state(w))
+    shape = {"Hq": w.Hq, "Hkv": w.Hkv, "hd": w.hd}
+    layers = [dict(W, g_ffn=p["g_ffn"][l]) if w.F > 0 else W for l, W in enumerate(p["layers"])]
+    Hc = gen_hidden_rows(w, n, 0, c0)
+    cache = [orc.context_kv_rows(Hc, p["mix"][l], p["g_mix"][l], W["Wkc"], W["Wvc"], np.arange(c0), shape, w.eps,
+                                 w.rope_theta) for l, W in enumerate(layers)]
+    H_new = gen_hidden_rows(w, n, c0, c0 + m)
+    Xb0 = gen_block_init(w)[n]
+    t0 = time.perf_counter()
+    Xb, _ = orc.draft_step_cached(Xb0, H_new, cache, p["mix"], p["g_mix"], p["g_blk"], layers, shape, w.eps,
+                                  w.rope_theta)
+    z = orc.lm_head_logits(Xb[1:], p["g_fin"], w.eps, W_lm_f32)
+    drafts = orc.argmax_lowest(z)
+    orc.greedy_accept(drafts, np.concatenate([drafts, [0]]))
+    return time.perf_counter() - t0
+
+
 def cpu_baseline(w, p, seqs):
     from dfl_synth import bits_to_f32, gen_verifier_logits
     W_lm = bits_to_f32(p["W_lm_bits"]) if w.V > 0 else None
+    step = oracle_step_cached if w.R > 0 else oracle_step
     total = 0.0
     for n in seqs:
         vl = gen_verifier_logits(w, seqs=[n])[0] if w.K > 0 else None
-        total += oracle_step(w, p, n, W_lm, vl)
+        total += step(w, p, n, W_lm, vl)
     return total
+
+
+def cached_rows(w, starts, counts, R):
+    """bf16 bits [L][N*R][d]: positions starts[n] .. starts[n]+counts[n]-1 of each sequence, zero-padded."""
+    from dfl_synth import gen_hidden_rows
+    H = np.zeros((w.L, w.N * R, w.d), np.uint16)
+    for n in range(w.N):
+        if counts[n] > 0:
+            H[:, n * R:n * R + counts[n]] = gen_hidden_rows(w, n, int(starts[n]), int(starts[n] + counts[n]),
+                                                            as_bits=True)
+    return H
+
+
+def prefill_cache(model, w, lengths, X0, chunk):
+    """Fill every sequence's context caches to lengths[n] with cached steps of up to `chunk` rows."""
+    import torch
+    cur = np.zeros(w.N, np.int64)
+    while (cur < lengths).any():
+        m = np.minimum(lengths - cur, chunk)
+        H = torch.from_numpy(cached_rows(w, cur, m, chunk).view(np.int16)).view(torch.bfloat16).cuda()
+        model.step(H, X0, torch.from_numpy(m.astype(np.int32)).cuda(), R=chunk)
+        cur += m
+    torch.cuda.synchronize()
+    if not np.array_equal(model.ctx_len.cpu().numpy(), lengths):
+        raise RuntimeError("cache prefill did not reach the requested lengths")
 
 
 def describe_sample(w, seqs):
     parts = "all D draft layers, LM head and " + ("K-draft sampling + self-selection" if w.K > 0 else
                                                   "greedy acceptance" if w.V > 0 else "no head")
+    if w.R > 0:
+        parts = "cached step: append of the new rows, " + parts
     return f"{len(seqs)} of {w.N} sequences of {w.name} ({parts}), fp64 NumPy"
 
 
@@ -265,7 +326,7 @@ def run_ours(args, rank, world, local):
     import torch
 
     import block_diffusion_speculative_dfl_gb300 as dfl
-    from dfl_synth import gen_block_init, gen_hidden, gen_verifier_logits, plant_targets
+    from dfl_synth import gen_block_init, gen_cache_state, gen_hidden, gen_verifier_logits, plant_targets
 
     torch.cuda.set_device(local)
     dist_init(world, "nccl")
@@ -277,25 +338,48 @@ def run_ours(args, rank, world, local):
                            dtype=w.dtype, K=w.K, T=w.T, seed=w.philox_seed, eps=w.eps, rope_theta=w.rope_theta,
                            F=w.F)
     W_lm = (torch.from_numpy(p["W_lm_bits"].view(np.int16)).view(torch.bfloat16) if w.V > 0 else None)
-    model = dfl.DraftModel(shape, p["mix"], p["g_mix"], p["g_blk"], p["g_fin"], p["layers"], W_lm,
-                           tv=args.tv and w.K > 0, accept_rule=1 if (args.accept_rule == "stochastic" and w.K > 0) else 0,
-                           accept_seed=w.philox_seed ^ 0xACCE97, ffn_gain=p["g_ffn"])
-    H_host = torch.from_numpy(gen_hidden(w, as_bits=True).view(np.int16)).view(torch.bfloat16)
+    cached = w.R > 0
+    kw = dict(tv=args.tv and w.K > 0, accept_rule=1 if (args.accept_rule == "stochastic" and w.K > 0) else 0,
+              accept_seed=w.philox_seed ^ 0xACCE97, ffn_gain=p["g_ffn"])
     X_host = torch.from_numpy(gen_block_init(w))
-    H, X0 = H_host.cuda(), X_host.cuda()
+    X0 = X_host.cuda()
+    n_host = n_new = None
+    ctx_lens = None
+    if cached:
+        # steady-state decoding: caches prefilled to the ragged lengths c0, then
+        # each timed step appends n_new rows (lengths held, so every step is alike)
+        model = dfl.CachedDraftModel(shape, PREFILL_ROWS, p["mix"], p["g_mix"], p["g_blk"], p["g_fin"],
+                                     p["layers"], W_lm, **kw)
+        c0, m_new = gen_cache_state(w)
+        prefill_cache(model, w, c0.astype(np.int64), X0, PREFILL_ROWS)
+        ctx_lens = c0 + m_new
+        H_host = torch.from_numpy(cached_rows(w, c0, m_new, w.R).view(np.int16)).view(torch.bfloat16)
+        n_host = torch.from_numpy(m_new)
+        n_new = n_host.cuda()
+    else:
+        model = dfl.DraftModel(shape, p["mix"], p["g_mix"], p["g_blk"], p["g_fin"], p["layers"], W_lm, **kw)
+        H_host = torch.from_numpy(gen_hidden(w, as_bits=True).view(np.int16)).view(torch.bfloat16)
+    H = H_host.cuda()
     vlog_host = vlog = None
     if w.K > 0:
         vlog_host = torch.from_numpy(gen_verifier_logits(w, as_bits=True).view(np.int16)).view(torch.bfloat16)
         vlog = vlog_host.cuda()
+
+    def run_step(target=None):
+        if cached:
+            model.step(H, X0, n_new, target=target, vlog=vlog, R=w.R, advance=False)
+        else:
+            model.step(H, X0, target=target, vlog=vlog)
+
     target_host = target = None
     if w.V > 0 and w.K == 0:   # plant the target's argmax against this step's drafts
-        model.step(H, X0)
+        run_step()
         torch.cuda.synchronize()
         target_host = torch.from_numpy(plant_targets(w, model.draft.cpu().numpy()))
         target = target_host.cuda()
 
     def step():
-        model.step(H, X0, target=target, vlog=vlog)
+        run_step(target)
 
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
     for _ in range(max(args.warmup, 0)):
@@ -328,7 +412,7 @@ def run_ours(args, rank, world, local):
 
     # roofline of the dominant kernel (largest share of traced time)
     peaks, peak_src = load_peaks()
-    work = kernel_work(w)
+    work = kernel_work(w, ctx_lens)
     traced = sum(t for _, t in prof.values())
     kernels = {}
     for name, (n_l, tot) in sorted(prof.items(), key=lambda kv: -kv[1][1]):
@@ -357,15 +441,22 @@ def run_ours(args, rank, world, local):
         H_pin, X_pin = H_host.pin_memory(), X_host.pin_memory()
         t_pin = target_host.pin_memory() if target_host is not None else None
         v_pin = vlog_host.pin_memory() if vlog_host is not None else None
+        n_pin = n_host.pin_memory() if n_host is not None else None
         dev_in = {}
-        out, dev_in = model.step_from_host(H_pin, X_pin, t_pin, v_pin, dev_in)   # allocate device buffers
+
+        def e2e_step(dev_in):
+            if cached:
+                return model.step_from_host(H_pin, X_pin, n_pin, t_pin, v_pin, dev_in, R=w.R, advance=False)
+            return model.step_from_host(H_pin, X_pin, t_pin, v_pin, dev_in)
+
+        out, dev_in = e2e_step(dev_in)   # allocate device buffers
         times = []
         for _ in range(args.e2e_steps):
             t0 = time.perf_counter()
-            out, dev_in = model.step_from_host(H_pin, X_pin, t_pin, v_pin, dev_in)
+            out, dev_in = e2e_step(dev_in)
             times.append(time.perf_counter() - t0)
         e2e_s = reduce_scalar(statistics.mean(times), world, "max", device="cuda")
-        h2d = sum(t.numel() * t.element_size() for t in (H_pin, X_pin, t_pin, v_pin) if t is not None)
+        h2d = sum(t.numel() * t.element_size() for t in (H_pin, X_pin, n_pin, t_pin, v_pin) if t is not None)
         d2h = sum(t.numel() * t.element_size() for t in out.values())
         e2e = {"value": round(aggregate(units, e2e_s, world), 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_s * 1e3, 3)}
@@ -384,7 +475,7 @@ def run_ours(args, rank, world, local):
                 "data": "synthetic (seeded NumPy PCG64; shapes and distributions of the workload)",
                 "config": {"workload": w.name, "N_per_gpu": w.N, "d": w.d, "Hq": w.Hq, "Hkv": w.Hkv, "hd": w.hd,
                            "draft_layers": w.D, "target_layers": w.L, "block": w.B, "context": w.C, "vocab": w.V,
-                           "ffn": w.F,
+                           "ffn": w.F, "new_rows_per_step": w.R or None,
                            "K": w.K, "T": w.T, "parallelism": f"replicas x{world}",
                            "epilogue": ("self-selection" + (" + TV proxy" if args.tv else "") +
                                         (" + stochastic acceptance" if args.accept_rule == "stochastic" else
@@ -407,10 +498,11 @@ def run_reference(args, rank, world):
     p = host_params(w)
     W_lm = bits_to_f32(p["W_lm_bits"]) if w.V > 0 else None
     times = []
+    step = oracle_step_cached if w.R > 0 else oracle_step
     for i in range(args.warmup + args.steps):
         n = i % w.N
         vl = gen_verifier_logits(w, seqs=[n])[0] if w.K > 0 else None
-        t = oracle_step(w, p, n, W_lm, vl)
+        t = step(w, p, n, W_lm, vl)
         if i >= args.warmup:
             times.append(t)
     total = sum(times)

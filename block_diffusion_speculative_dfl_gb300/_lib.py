@@ -15,14 +15,15 @@ DFL_OK, DFL_ERR_INVALID_ARG, DFL_ERR_UNSUPPORTED_SHAPE, DFL_ERR_MISALIGNED = 0, 
 DFL_ERR_WORKSPACE, DFL_ERR_CUDA, DFL_ERR_TIMEOUT, DFL_ERR_NO_DEVICE = 4, 5, 6, 7
 DFL_F32, DFL_BF16 = 0, 1
 DFL_OP_DUAL_KV_PROJ, DFL_OP_BLOCK_ATTN, DFL_OP_LM_HEAD, DFL_OP_SELF_SELECT, DFL_OP_DRAFT_STEP = 1, 2, 3, 4, 5
-DFL_OP_TV_ACCEPTANCE, DFL_OP_SPEC_ACCEPT, DFL_OP_BLOCK_FFN = 6, 7, 8
+DFL_OP_TV_ACCEPTANCE, DFL_OP_SPEC_ACCEPT, DFL_OP_BLOCK_FFN, DFL_OP_DRAFT_STEP_CACHED = 6, 7, 8, 9
 
 # Every function the header declares; tests check each is exported.
 EXPORTED = ("dfl_version", "dfl_status_string", "dfl_workspace_size", "dfl_rope_table",
             "dfl_layer_mix_rmsnorm", "dfl_dual_kv_proj", "dfl_block_attn", "dfl_lm_head_argmax",
             "dfl_greedy_accept", "dfl_self_select", "dfl_draft_step", "dfl_get_device_error",
             "dfl_set_wait_limit_ns", "dfl_selftest_bounded_wait", "dfl_profile_enable", "dfl_profile_report",
-            "dfl_self_select_noalloc", "dfl_tv_acceptance", "dfl_spec_accept", "dfl_block_ffn")
+            "dfl_self_select_noalloc", "dfl_tv_acceptance", "dfl_spec_accept", "dfl_block_ffn",
+            "dfl_draft_step_cached")
 
 
 class DflError(RuntimeError):
@@ -37,7 +38,7 @@ class SampleParams(C.Structure):
 
 class Shape(C.Structure):
     _fields_ = [(n, C.c_int32) for n in ("N", "C", "B", "d", "Hq", "Hkv", "hd", "D", "L", "V", "K", "G", "row0",
-                                         "dtype", "F")]
+                                         "dtype", "F", "R")]
 
 
 class LayerWeights(C.Structure):
@@ -56,6 +57,11 @@ class StepArgs(C.Structure):
                 [("accept_rule", C.c_int32), ("accept_seed", C.c_uint64), ("F", C.c_int32), ("ffn_gain", C.c_void_p)])
 
 
+class CtxCache(C.Structure):
+    _fields_ = [("K", C.c_void_p), ("V", C.c_void_p), ("layer_stride", C.c_int64), ("R", C.c_int32),
+                ("ctx_len", C.c_void_p), ("n_new", C.c_void_p), ("advance", C.c_int32)]
+
+
 _P, _I32, _I64, _F, _D, _SZ = C.c_void_p, C.c_int32, C.c_int64, C.c_float, C.c_double, C.c_size_t
 _SIGS = {
     "dfl_version": ([], C.c_char_p),
@@ -72,6 +78,7 @@ _SIGS = {
     "dfl_greedy_accept": ([_P, _P, _I32, _I32, _P, _P, _P], _I32),
     "dfl_self_select": ([_P, _I32, _P, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _SZ, _P], _I32),
     "dfl_draft_step": ([C.POINTER(StepArgs), _P, _SZ, _P], _I32),
+    "dfl_draft_step_cached": ([C.POINTER(StepArgs), C.POINTER(CtxCache), _P, _SZ, _P], _I32),
     "dfl_get_device_error": ([_P, C.POINTER(_I32)], _I32),
     "dfl_set_wait_limit_ns": ([C.c_uint64], _I32),
     "dfl_selftest_bounded_wait": ([C.c_uint64, _P, _P], _I32),
@@ -188,6 +195,11 @@ def dfl_self_select(vlog, dt, drafts, N, K, G, V, scores, selected, accept_len, 
 
 def dfl_draft_step(args: StepArgs, ws, ws_bytes, stream=None):
     _check("dfl_draft_step", load().dfl_draft_step(C.byref(args), ptr(ws), ws_bytes, _stream(stream)))
+
+
+def dfl_draft_step_cached(args: StepArgs, cache: CtxCache, ws, ws_bytes, stream=None):
+    _check("dfl_draft_step_cached",
+           load().dfl_draft_step_cached(C.byref(args), C.byref(cache), ptr(ws), ws_bytes, _stream(stream)))
 
 
 def dfl_get_device_error(stream=None) -> int:

@@ -1,5 +1,6 @@
 // C-ABI entry points of libdfl: argument checks, workspace layout and the
 // order of kernel launches for each operation of the draft step.
+#include <algorithm>
 #include <atomic>
 #include <cstdio>
 #include <cstring>
@@ -79,6 +80,39 @@ size_t ws_lm_head(int N, int B, int row0, int d, int V, int dt, bool logits_miss
     return b;
 }
 
+// Workspace of a whole draft step: the mixed context features of all D
+// layers, Q / (Kc, Vc) / Kb / Vb, the cached step's row plan, samples and
+// drafts, then scratch shared by the calls in turn.  The cached step mixes
+// and projects R rows per sequence, keeps K/V in the caller's cache (C is its
+// capacity) and, when sampling, lends the feature area to the logits.
+size_t step_ws_bytes(const dfl_shape& s, bool cached) {
+    if (cached && (s.dtype != DFL_BF16 || s.R < 1)) return 0;
+    const size_t e = esz(s.dtype);
+    const int64_t rows = (int64_t)s.N * (cached ? s.R : s.C);   // context rows mixed this step
+    size_t xc = (size_t)s.D * rows * s.d * e;
+    if (cached && s.V > 0 && s.K > 0) xc = std::max(xc, (size_t)s.N * (s.B - 1) * s.V * 4);
+    size_t b = al256(xc);
+    b += al256((size_t)s.N * s.B * s.Hq * s.hd * e);                         // Q
+    if (!cached) b += 2 * al256((size_t)s.N * s.C * s.Hkv * s.hd * e);       // Kc, Vc
+    b += 2 * al256((size_t)s.N * s.B * s.Hkv * s.hd * e);                    // Kb, Vb
+    if (cached) b += 2 * al256((size_t)rows * 4) + al256((size_t)s.N * s.B * 4) + al256((size_t)s.N * 4);
+    size_t sub = ws_dual_kv_proj(s.N, s.B, s.d, s.dtype);
+    sub = std::max(sub, ws_block_attn(s.N, s.C, s.B, s.Hq, s.Hkv, s.hd, s.dtype));
+    if (s.F > 0) sub = std::max(sub, ws_block_ffn(s.N, s.B, s.d, s.F, s.dtype));
+    if (s.V > 0) {
+        sub = std::max(sub, ws_lm_head(s.N, s.B, 1, s.d, s.V, s.dtype, true));
+        if (s.K > 0) {
+            // self-selection scratch (its verifier-row LSEs are reused), drafter-row LSEs,
+            // stochastic-acceptance scratch
+            sub = std::max(sub, al256(select_ws_bytes(s.N, s.K, s.B - 1)) + al256((size_t)s.N * (s.B - 1) * 4) +
+                                    spec_scratch_bytes(s.N, s.V));
+            b += al256((size_t)s.N * s.K * (s.B - 1) * 4);                   // samples
+        }
+        b += al256((size_t)s.N * (s.B - 1) * 4);                             // drafts
+    }
+    return b + sub;
+}
+
 }  // namespace dfl
 
 using namespace dfl;
@@ -113,32 +147,8 @@ extern "C" size_t dfl_workspace_size(dfl_op op, const dfl_shape* s) {
         case DFL_OP_TV_ACCEPTANCE: return tv_ws_bytes(s->N, s->K, s->G);
         case DFL_OP_SPEC_ACCEPT: return spec_ws_bytes(s->N, s->G, s->V);
         case DFL_OP_BLOCK_FFN: return s->F > 0 ? ws_block_ffn(s->N, s->B, s->d, s->F, s->dtype) : 0;
-        case DFL_OP_DRAFT_STEP: {
-            const size_t e = esz(s->dtype);
-            size_t b = al256((size_t)s->D * s->N * s->C * s->d * e);                 // Xc, all layers
-            b += al256((size_t)s->N * s->B * s->Hq * s->hd * e);                     // Q
-            b += 2 * al256((size_t)s->N * s->C * s->Hkv * s->hd * e);                // Kc, Vc
-            b += 2 * al256((size_t)s->N * s->B * s->Hkv * s->hd * e);                // Kb, Vb
-            size_t sub = ws_dual_kv_proj(s->N, s->B, s->d, s->dtype);
-            const size_t at = ws_block_attn(s->N, s->C, s->B, s->Hq, s->Hkv, s->hd, s->dtype);
-            if (at > sub) sub = at;
-            if (s->F > 0 && ws_block_ffn(s->N, s->B, s->d, s->F, s->dtype) > sub)
-                sub = ws_block_ffn(s->N, s->B, s->d, s->F, s->dtype);
-            if (s->V > 0) {
-                const size_t lm = ws_lm_head(s->N, s->B, 1, s->d, s->V, s->dtype, true);
-                if (lm > sub) sub = lm;
-                if (s->K > 0) {
-                    // self-selection scratch (its verifier-row LSEs are reused), drafter-row LSEs,
-                    // stochastic-acceptance scratch
-                    const size_t se = al256(select_ws_bytes(s->N, s->K, s->B - 1)) +
-                                      al256((size_t)s->N * (s->B - 1) * 4) + spec_scratch_bytes(s->N, s->V);
-                    if (se > sub) sub = se;
-                    b += al256((size_t)s->N * s->K * (s->B - 1) * 4);               // samples
-                }
-                b += al256((size_t)s->N * (s->B - 1) * 4);                          // drafts
-            }
-            return b + sub;
-        }
+        case DFL_OP_DRAFT_STEP: return step_ws_bytes(*s, false);
+        case DFL_OP_DRAFT_STEP_CACHED: return step_ws_bytes(*s, true);
     }
     return 0;
 }
@@ -183,6 +193,95 @@ extern "C" dfl_status dfl_greedy_accept(const int32_t* draft, const int32_t* tar
 }
 
 // ------------------------------------------------------- dual projection
+
+namespace dfl {
+namespace {
+// Row plan of the cached step: positions and cache rows of the new context
+// rows, positions of the block rows (device arrays).
+struct KvRowPlan {
+    const int32_t* ctx_pos;
+    const int32_t* ctx_dst;
+    const int32_t* blk_pos;
+};
+
+// bf16 projections of one draft layer: context rows [Kc | Vc] = Xc [Wkc ; Wvc]^T
+// (ctx_M rows, ctx_per rows per sequence), block rows [Q | Kb | Vb] =
+// RMSNorm(Xb) [Wq ; Wkb ; Wvb]^T, rotary embedding in the GEMM epilogues.
+// Without a plan, context row r sits at position r % ctx_per and block row r
+// at ctx_per + r % B; with one, the plan gives positions and context rows go
+// to plan->ctx_dst (rows < 0 dropped).
+dfl_status dual_kv_proj_bf16(DeviceCtx* ctx, const void* Xc, int64_t ctx_M, int ctx_per, const float* Xb, int N,
+                             int B, int d, const float* blk_gain, float eps, const void* Wq, const void* Wkc,
+                             const void* Wvc, const void* Wkb, const void* Wvb, int Hq, int Hkv, int hd,
+                             const float* rope, void* Q, void* Kc, void* Vc, void* Kb, void* Vb, void* ws,
+                             const KvRowPlan* plan, cudaStream_t st) {
+    const int kv = Hkv * hd, qd = Hq * hd;
+    dfl_status rc;
+    void* Xn = ws;
+    if ((rc = rmsnorm_rows(Xb, d, (int64_t)N * B, 1, 1, 0, blk_gain, eps, Xn, true, st)) != DFL_OK) return rc;
+
+    if (ctx_M > 0) {   // context rows: [Kc | Vc] = Xc [Wkc ; Wvc]^T
+        GemmArgs g{};
+        g.A = Xc; g.M = ctx_M; g.K = d;
+        g.B[0] = Wkc; g.B[1] = Wvc; g.b_rows[0] = kv; g.b_rows[1] = kv;
+        g.b_begin[0] = 0; g.b_begin[1] = kv; g.nb = 2; g.N = 2 * kv;
+        g.bn = (kv % 256 == 0) ? 256 : 128;
+        g.m_inner = 0;
+        g.epi = EPI_STORE;
+        g.ep.seg[0] = GemmSeg{Kc, 0, kv, rope != nullptr};
+        g.ep.seg[1] = GemmSeg{Vc, kv, kv, 0};
+        g.ep.nseg = 2;
+        g.ep.rope = rope; g.ep.hd = hd; g.ep.rows_per_seq = ctx_per; g.ep.pos_off = 0;
+        if (plan) { g.ep.row_pos = plan->ctx_pos; g.ep.row_dst = plan->ctx_dst; }
+        g.tag = plan ? "gemm_ctx_kv_append" : "gemm_ctx_kv";
+        if ((rc = gemm_tc(ctx, g, st)) != DFL_OK) return rc;
+    }
+    {   // block rows: [Q | Kb | Vb] = Xn [Wq ; Wkb ; Wvb]^T
+        GemmArgs g{};
+        g.A = Xn; g.M = N * B; g.K = d;
+        g.B[0] = Wq; g.B[1] = Wkb; g.B[2] = Wvb;
+        g.b_rows[0] = qd; g.b_rows[1] = kv; g.b_rows[2] = kv;
+        g.b_begin[0] = 0; g.b_begin[1] = qd; g.b_begin[2] = qd + kv; g.nb = 3; g.N = qd + 2 * kv;
+        g.bn = 0;   // chosen per shape
+        g.m_inner = 1;
+        g.epi = EPI_STORE;
+        g.ep.seg[0] = GemmSeg{Q, 0, qd, rope != nullptr};
+        g.ep.seg[1] = GemmSeg{Kb, qd, kv, rope != nullptr};
+        g.ep.seg[2] = GemmSeg{Vb, qd + kv, kv, 0};
+        g.ep.nseg = 3;
+        g.ep.rope = rope; g.ep.hd = hd; g.ep.rows_per_seq = B; g.ep.pos_off = ctx_per;
+        if (plan) g.ep.row_pos = plan->blk_pos;
+        g.tag = "gemm_block_qkv";
+        if ((rc = gemm_tc(ctx, g, st)) != DFL_OK) return rc;
+    }
+    return DFL_OK;
+}
+
+// bf16 block attention and output projection, Xb += Attn(Q, [Kc;Kb], [Vc;Vb]) Wo^T.
+// ctx_len (nullable, device [N]): context keys of each sequence, C the maximum
+// and C_stride the context rows per sequence of Kc / Vc.
+dfl_status block_attn_bf16(DeviceCtx* ctx, const void* Q, const void* Kc, const void* Vc, const void* Kb,
+                           const void* Vb, int N, int C, int B, int Hq, int Hkv, int hd, const void* Wo, int d,
+                           float* Xb, void* ws, const int32_t* ctx_len, int C_stride, cudaStream_t st) {
+    const int qd = Hq * hd;
+    dfl_status rc;
+    uint8_t* p = static_cast<uint8_t*>(ws);
+    void* O = carve(p, (size_t)N * B * qd * 2);
+    if ((rc = attn_bf16(Q, Kc, Vc, Kb, Vb, N, C, B, Hq, Hkv, hd, O, p, st, ctx_len, C_stride)) != DFL_OK) return rc;
+    GemmArgs g{};   // Xb += O Wo^T
+    g.A = O; g.M = N * B; g.K = qd;
+    g.B[0] = Wo; g.b_rows[0] = d; g.b_begin[0] = 0; g.nb = 1; g.N = d;
+    g.bn = 0;   // chosen per shape
+    g.m_inner = 1;
+    g.epi = EPI_RESID;
+    g.ep.resid = Xb; g.ep.ld_resid = d;
+    g.tag = "gemm_o_proj";
+    return gemm_tc(ctx, g, st);
+}
+
+}  // namespace
+}  // namespace dfl
+
 
 extern "C" dfl_status dfl_dual_kv_proj(const void* Xc, const float* Xb, int32_t N, int32_t C, int32_t B, int32_t d,
                                        dfl_dtype dt, const float* blk_gain, float eps, const void* Wq,
@@ -243,42 +342,8 @@ extern "C" dfl_status dfl_dual_kv_proj(const void* Xc, const float* Xb, int32_t 
     // bf16: tensor-core GEMMs with the rotary embedding in the epilogue
     if (hd != 64 && hd != 128) return DFL_ERR_UNSUPPORTED_SHAPE;
     if (kv % 128 != 0 || qd % 128 != 0) return DFL_ERR_UNSUPPORTED_SHAPE;
-    void* Xn = ws;
-    if ((rc = rmsnorm_rows(Xb, d, (int64_t)N * B, 1, 1, 0, blk_gain, eps, Xn, true, st)) != DFL_OK) return rc;
-
-    if (C > 0) {   // context rows: [Kc | Vc] = Xc [Wkc ; Wvc]^T
-        GemmArgs g{};
-        g.A = Xc; g.M = N * C; g.K = d;
-        g.B[0] = Wkc; g.B[1] = Wvc; g.b_rows[0] = kv; g.b_rows[1] = kv;
-        g.b_begin[0] = 0; g.b_begin[1] = kv; g.nb = 2; g.N = 2 * kv;
-        g.bn = (kv % 256 == 0) ? 256 : 128;
-        g.m_inner = 0;
-        g.epi = EPI_STORE;
-        g.ep.seg[0] = GemmSeg{Kc, 0, kv, rope != nullptr};
-        g.ep.seg[1] = GemmSeg{Vc, kv, kv, 0};
-        g.ep.nseg = 2;
-        g.ep.rope = rope; g.ep.hd = hd; g.ep.rows_per_seq = C; g.ep.pos_off = 0;
-        g.tag = "gemm_ctx_kv";
-        if ((rc = gemm_tc(ctx, g, st)) != DFL_OK) return rc;
-    }
-    {   // block rows: [Q | Kb | Vb] = Xn [Wq ; Wkb ; Wvb]^T
-        GemmArgs g{};
-        g.A = Xn; g.M = N * B; g.K = d;
-        g.B[0] = Wq; g.B[1] = Wkb; g.B[2] = Wvb;
-        g.b_rows[0] = qd; g.b_rows[1] = kv; g.b_rows[2] = kv;
-        g.b_begin[0] = 0; g.b_begin[1] = qd; g.b_begin[2] = qd + kv; g.nb = 3; g.N = qd + 2 * kv;
-        g.bn = 0;   // chosen per shape
-        g.m_inner = 1;
-        g.epi = EPI_STORE;
-        g.ep.seg[0] = GemmSeg{Q, 0, qd, rope != nullptr};
-        g.ep.seg[1] = GemmSeg{Kb, qd, kv, rope != nullptr};
-        g.ep.seg[2] = GemmSeg{Vb, qd + kv, kv, 0};
-        g.ep.nseg = 3;
-        g.ep.rope = rope; g.ep.hd = hd; g.ep.rows_per_seq = B; g.ep.pos_off = C;
-        g.tag = "gemm_block_qkv";
-        if ((rc = gemm_tc(ctx, g, st)) != DFL_OK) return rc;
-    }
-    return DFL_OK;
+    return dual_kv_proj_bf16(ctx, Xc, (int64_t)N * C, C, Xb, N, B, d, blk_gain, eps, Wq, Wkc, Wvc, Wkb, Wvb, Hq, Hkv,
+                             hd, rope, Q, Kc, Vc, Kb, Vb, ws, nullptr, st);
 }
 
 // -------------------------------------------------------- block attention
@@ -312,16 +377,7 @@ extern "C" dfl_status dfl_block_attn(const void* Q, const void* Kc, const void* 
     }
     if (hd != 64 && hd != 128) return DFL_ERR_UNSUPPORTED_SHAPE;
     if (d % 32 != 0) return DFL_ERR_UNSUPPORTED_SHAPE;
-    if ((rc = attn_bf16(Q, Kc, Vc, Kb, Vb, N, C, B, Hq, Hkv, hd, O, p, st)) != DFL_OK) return rc;
-    GemmArgs g{};   // Xb += O Wo^T
-    g.A = O; g.M = N * B; g.K = qd;
-    g.B[0] = Wo; g.b_rows[0] = d; g.b_begin[0] = 0; g.nb = 1; g.N = d;
-    g.bn = 0;   // chosen per shape
-    g.m_inner = 1;
-    g.epi = EPI_RESID;
-    g.ep.resid = Xb; g.ep.ld_resid = d;
-    g.tag = "gemm_o_proj";
-    return gemm_tc(ctx, g, st);
+    return block_attn_bf16(ctx, Q, Kc, Vc, Kb, Vb, N, C, B, Hq, Hkv, hd, Wo, d, Xb, ws, nullptr, C, st);
 }
 
 // ------------------------------------------------------- feed-forward
@@ -456,7 +512,13 @@ extern "C" dfl_status dfl_self_select(const void* vlog, dfl_dtype dt, const int3
 
 // ---------------------------------------------------------- whole step
 
-extern "C" dfl_status dfl_draft_step(const dfl_step_args* a, void* ws, size_t ws_bytes, dfl_stream stream) {
+namespace dfl {
+namespace {
+
+// The whole draft step; with `cache`, the incremental form over the caller's
+// context K/V cache (args->C its capacity, args->H the R new rows per sequence).
+dfl_status draft_step_impl(const dfl_step_args* a, const dfl_ctx_cache* cache, void* ws, size_t ws_bytes,
+                           dfl_stream stream) {
     if (!a || !ws) return DFL_ERR_INVALID_ARG;
     const int dt = a->dtype;
     if (dt != DFL_F32 && dt != DFL_BF16) return DFL_ERR_INVALID_ARG;
@@ -478,25 +540,50 @@ extern "C" dfl_status dfl_draft_step(const dfl_step_args* a, void* ws, size_t ws
         if (!w.Wq || !w.Wkc || !w.Wvc || !w.Wkb || !w.Wvb || !w.Wo) return DFL_ERR_INVALID_ARG;
         if (a->F > 0 && (!w.W1 || !w.W3 || !w.W2)) return DFL_ERR_INVALID_ARG;
     }
+    if (cache) {
+        if (dt != DFL_BF16) return DFL_ERR_UNSUPPORTED_SHAPE;
+        if (!cache->K || !cache->V || !cache->ctx_len || !cache->n_new || cache->R < 1) return DFL_ERR_INVALID_ARG;
+        if (cache->layer_stride < (int64_t)a->N * a->C * a->Hkv * a->hd) return DFL_ERR_INVALID_ARG;
+        if ((int64_t)a->N * a->C >= (int64_t)1 << 31) return DFL_ERR_UNSUPPORTED_SHAPE;
+        if (!aligned16(cache->K) || !aligned16(cache->V) || (cache->layer_stride * 2) % 16 != 0)
+            return DFL_ERR_MISALIGNED;
+        if (a->Hq <= 0 || a->Hkv <= 0 || a->Hq % a->Hkv != 0 || (a->hd != 64 && a->hd != 128))
+            return DFL_ERR_UNSUPPORTED_SHAPE;
+        if ((a->Hkv * a->hd) % 128 != 0 || (a->Hq * a->hd) % 128 != 0 || a->d % 32 != 0)
+            return DFL_ERR_UNSUPPORTED_SHAPE;
+        if (a->rope && !aligned16(a->rope)) return DFL_ERR_MISALIGNED;
+    }
     dfl_shape s{};
     s.N = a->N; s.C = a->C; s.B = a->B; s.d = a->d; s.Hq = a->Hq; s.Hkv = a->Hkv; s.hd = a->hd; s.D = a->D;
     s.L = a->L; s.V = a->V; s.K = a->sample ? a->sample->K : 0; s.G = a->B - 1; s.row0 = 1; s.dtype = dt;
-    s.F = a->F;
-    if (ws_bytes < dfl_workspace_size(DFL_OP_DRAFT_STEP, &s)) return DFL_ERR_WORKSPACE;
+    s.F = a->F; s.R = cache ? cache->R : 0;
+    if (ws_bytes < step_ws_bytes(s, cache != nullptr)) return DFL_ERR_WORKSPACE;
     if (!aligned16(ws)) return DFL_ERR_MISALIGNED;
-    if (!current_ctx()) return DFL_ERR_NO_DEVICE;
+    DeviceCtx* dctx = current_ctx();
+    if (!dctx) return DFL_ERR_NO_DEVICE;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const dfl_dtype ddt = static_cast<dfl_dtype>(dt);
     const size_t e = esz(dt);
     const int N = a->N, C = a->C, B = a->B, d = a->d;
-    const int64_t ctx_rows = (int64_t)N * C;
+    const int R = cache ? cache->R : C;
+    const int64_t ctx_rows = (int64_t)N * R;   // context rows mixed and projected this step
     uint8_t* p = static_cast<uint8_t*>(ws);
-    uint8_t* Xc = carve(p, (size_t)a->D * ctx_rows * d * e);
+    size_t xc_bytes = (size_t)a->D * ctx_rows * d * e;
+    if (cache && a->V > 0 && s.K > 0) xc_bytes = std::max(xc_bytes, (size_t)N * (B - 1) * a->V * 4);
+    uint8_t* Xc = carve(p, xc_bytes);
     void* Q = carve(p, (size_t)N * B * a->Hq * a->hd * e);
-    void* Kc = carve(p, (size_t)ctx_rows * a->Hkv * a->hd * e);
-    void* Vc = carve(p, (size_t)ctx_rows * a->Hkv * a->hd * e);
+    void* Kc = cache ? nullptr : carve(p, (size_t)ctx_rows * a->Hkv * a->hd * e);
+    void* Vc = cache ? nullptr : carve(p, (size_t)ctx_rows * a->Hkv * a->hd * e);
     void* Kb = carve(p, (size_t)N * B * a->Hkv * a->hd * e);
     void* Vb = carve(p, (size_t)N * B * a->Hkv * a->hd * e);
+    KvRowPlan plan{};
+    int32_t* len_new = nullptr;
+    if (cache) {
+        plan.ctx_pos = reinterpret_cast<int32_t*>(carve(p, (size_t)ctx_rows * 4));
+        plan.ctx_dst = reinterpret_cast<int32_t*>(carve(p, (size_t)ctx_rows * 4));
+        plan.blk_pos = reinterpret_cast<int32_t*>(carve(p, (size_t)N * B * 4));
+        len_new = reinterpret_cast<int32_t*>(carve(p, (size_t)N * 4));
+    }
     int32_t* samples = a->samples;
     if (a->V > 0 && s.K > 0) {
         int32_t* own = reinterpret_cast<int32_t*>(carve(p, (size_t)N * s.K * (B - 1) * 4));
@@ -513,18 +600,36 @@ extern "C" dfl_status dfl_draft_step(const dfl_step_args* a, void* ws, size_t ws
         cudaSuccess)
         return DFL_ERR_CUDA;
     }
+    if (cache &&
+        (rc = cache_plan(N, R, B, C, cache->ctx_len, cache->n_new, cache->advance, const_cast<int32_t*>(plan.ctx_pos),
+                         const_cast<int32_t*>(plan.ctx_dst), const_cast<int32_t*>(plan.blk_pos), len_new,
+                         dev_err(dctx), st)) != DFL_OK)
+        return rc;
     if ((rc = dfl_layer_mix_rmsnorm(a->H, a->h_layer_stride, a->L, ctx_rows, d, ddt, a->D, a->mix_logits,
                                     a->mix_gain, a->eps, Xc, ctx_rows * d, stream)) != DFL_OK)
         return rc;
     for (int l = 0; l < a->D; ++l) {
         const dfl_layer_weights& w = a->layers[l];
-        if ((rc = dfl_dual_kv_proj(Xc + (size_t)l * ctx_rows * d * e, a->Xb, N, C, B, d, ddt,
-                                   a->blk_gain + (size_t)l * d, a->eps, w.Wq, w.Wkc, w.Wvc, w.Wkb, w.Wvb, a->Hq,
-                                   a->Hkv, a->hd, a->rope, Q, Kc, Vc, Kb, Vb, sub, sub_bytes, stream)) != DFL_OK)
-            return rc;
-        if ((rc = dfl_block_attn(Q, Kc, Vc, Kb, Vb, N, C, B, a->Hq, a->Hkv, a->hd, ddt, w.Wo, d, a->Xb, sub,
-                                 sub_bytes, stream)) != DFL_OK)
-            return rc;
+        const void* xc_l = Xc + (size_t)l * ctx_rows * d * e;
+        if (cache) {
+            void* Kl = static_cast<uint8_t*>(cache->K) + (size_t)l * cache->layer_stride * 2;
+            void* Vl = static_cast<uint8_t*>(cache->V) + (size_t)l * cache->layer_stride * 2;
+            if ((rc = dual_kv_proj_bf16(dctx, xc_l, ctx_rows, R, a->Xb, N, B, d, a->blk_gain + (size_t)l * d, a->eps,
+                                        w.Wq, w.Wkc, w.Wvc, w.Wkb, w.Wvb, a->Hq, a->Hkv, a->hd, a->rope, Q, Kl, Vl,
+                                        Kb, Vb, sub, &plan, st)) != DFL_OK)
+                return rc;
+            if ((rc = block_attn_bf16(dctx, Q, Kl, Vl, Kb, Vb, N, C, B, a->Hq, a->Hkv, a->hd, w.Wo, d, a->Xb, sub,
+                                      len_new, C, st)) != DFL_OK)
+                return rc;
+        } else {
+            if ((rc = dfl_dual_kv_proj(xc_l, a->Xb, N, C, B, d, ddt, a->blk_gain + (size_t)l * d, a->eps, w.Wq,
+                                       w.Wkc, w.Wvc, w.Wkb, w.Wvb, a->Hq, a->Hkv, a->hd, a->rope, Q, Kc, Vc, Kb, Vb,
+                                       sub, sub_bytes, stream)) != DFL_OK)
+                return rc;
+            if ((rc = dfl_block_attn(Q, Kc, Vc, Kb, Vb, N, C, B, a->Hq, a->Hkv, a->hd, ddt, w.Wo, d, a->Xb, sub,
+                                     sub_bytes, stream)) != DFL_OK)
+                return rc;
+        }
         if (a->F > 0 && (rc = dfl_block_ffn(a->Xb, N, B, d, ddt, a->ffn_gain + (size_t)l * d, a->eps, w.W1, w.W3,
                                             w.W2, a->F, sub, sub_bytes, stream)) != DFL_OK)
             return rc;
@@ -532,7 +637,7 @@ extern "C" dfl_status dfl_draft_step(const dfl_step_args* a, void* ws, size_t ws
     if (a->V == 0) return DFL_OK;
     float* logits = a->logits;
     if (!logits && a->sample) {   // sampling walks the logits; borrow the Xc area (no longer needed)
-        if ((size_t)N * (B - 1) * a->V * 4 > (size_t)a->D * ctx_rows * d * e) return DFL_ERR_WORKSPACE;
+        if ((size_t)N * (B - 1) * a->V * 4 > xc_bytes) return DFL_ERR_WORKSPACE;
         logits = reinterpret_cast<float*>(Xc);
     }
     if ((rc = dfl_lm_head_argmax(a->Xb, N, B, 1, d, ddt, a->final_gain, a->eps, a->W_lm, a->V, a->draft, logits,
@@ -562,6 +667,19 @@ extern "C" dfl_status dfl_draft_step(const dfl_step_args* a, void* ws, size_t ws
     }
     if (a->target) return dfl_greedy_accept(a->draft, a->target, N, B - 1, a->accept_len, a->bonus, stream);
     return DFL_OK;
+}
+
+}  // namespace
+}  // namespace dfl
+
+extern "C" dfl_status dfl_draft_step(const dfl_step_args* a, void* ws, size_t ws_bytes, dfl_stream stream) {
+    return draft_step_impl(a, nullptr, ws, ws_bytes, stream);
+}
+
+extern "C" dfl_status dfl_draft_step_cached(const dfl_step_args* a, const dfl_ctx_cache* cache, void* ws,
+                                            size_t ws_bytes, dfl_stream stream) {
+    if (!cache) return DFL_ERR_INVALID_ARG;
+    return draft_step_impl(a, cache, ws, ws_bytes, stream);
 }
 
 // ---------------------------------------------------------------- tracing

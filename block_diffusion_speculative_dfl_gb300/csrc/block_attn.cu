@@ -28,6 +28,8 @@ constexpr int ATT_MAX_WARPS = 12;  // 16 query rows per warp; more rows -> more 
 struct AttnArgs {
     const __nv_bfloat16 *Q, *Kc, *Vc, *Kb, *Vb;
     int N, C, B, Hq, Hkv, G, R;
+    const int32_t* ctx_len;   // nullable [N]: context keys of each sequence (else C)
+    int C_stride;             // context rows per sequence in Kc / Vc
     int S, keys_per_split;
     __nv_bfloat16* O;   // written directly when S == 1
     float* Opart;       // [S][N*B*Hq][HD]
@@ -79,9 +81,24 @@ __global__ void __launch_bounds__(ATT_MAX_WARPS * 32) attn_bf16_kernel(const Att
     const int n = blockIdx.x / a.Hkv, g = blockIdx.x % a.Hkv;
     const int split = blockIdx.y;
     const int r0 = blockIdx.z * NW * 16;   // first query row of this CTA
+    const int Cn = a.ctx_len ? a.ctx_len[n] : a.C;   // this sequence's context keys
     const int k_begin = split * a.keys_per_split;
-    const int k_end = min(a.C + a.B, k_begin + a.keys_per_split);
-    const int ntiles = (k_end - k_begin + KT - 1) / KT;
+    const int k_end = min(Cn + a.B, k_begin + a.keys_per_split);
+    const int ntiles = k_end > k_begin ? (k_end - k_begin + KT - 1) / KT : 0;
+    const int64_t NQ = (int64_t)a.N * a.B * a.Hq;
+    if (ntiles == 0) {   // split past this sequence's keys: an empty partial (weight 0 in the combine)
+        if (a.S > 1) {
+            for (int i = threadIdx.x; i < NW * 16; i += nthr) {
+                const int row = r0 + i;
+                if (row >= a.R) continue;
+                const int64_t qrow = (int64_t)(n * a.B + row / a.G) * a.Hq + g * a.G + row % a.G;
+                a.lse[(int64_t)split * NQ + qrow] = -INFINITY;
+                float* out = a.Opart + ((int64_t)split * NQ + qrow) * HD;
+                for (int e = 0; e < HD; ++e) out[e] = 0.f;
+            }
+        }
+        return;
+    }
 
     // Q rows of this CTA: r -> (block row b = r / G, head g*G + r % G)
     for (int i = tid; i < NW * 16 * CH; i += nthr) {
@@ -101,11 +118,11 @@ __global__ void __launch_bounds__(ATT_MAX_WARPS * 32) attn_bf16_kernel(const Att
             const bool ok = key < k_end;
             const __nv_bfloat16 *ks = a.Q, *vs = a.Q;
             if (ok) {
-                if (key < a.C) {
-                    const int64_t off = ((int64_t)(n * a.C + key) * a.Hkv + g) * HD + c * 8;
+                if (key < Cn) {
+                    const int64_t off = (((int64_t)n * a.C_stride + key) * a.Hkv + g) * HD + c * 8;
                     ks = a.Kc + off; vs = a.Vc + off;
                 } else {
-                    const int64_t off = ((int64_t)(n * a.B + key - a.C) * a.Hkv + g) * HD + c * 8;
+                    const int64_t off = ((int64_t)(n * a.B + key - Cn) * a.Hkv + g) * HD + c * 8;
                     ks = a.Kb + off; vs = a.Vb + off;
                 }
             }
@@ -205,7 +222,6 @@ __global__ void __launch_bounds__(ATT_MAX_WARPS * 32) attn_bf16_kernel(const Att
         __syncthreads();
     }
 
-    const int64_t NQ = (int64_t)a.N * a.B * a.Hq;
     #pragma unroll
     for (int r = 0; r < 2; ++r) {
         const int row = r0 + warp * 16 + (lane >> 2) + 8 * r;
@@ -302,8 +318,11 @@ size_t attn_ws_bytes(int N, int C, int B, int Hq, int Hkv, int hd) {
 }
 
 dfl_status attn_bf16(const void* Q, const void* Kc, const void* Vc, const void* Kb, const void* Vb, int N, int C,
-                     int B, int Hq, int Hkv, int hd, void* O, void* ws, cudaStream_t st) {
+                     int B, int Hq, int Hkv, int hd, void* O, void* ws, cudaStream_t st, const int32_t* ctx_len,
+                     int C_stride) {
     AttnArgs a{};
+    a.ctx_len = ctx_len;
+    a.C_stride = ctx_len ? C_stride : C;
     a.Q = static_cast<const __nv_bfloat16*>(Q);
     a.Kc = static_cast<const __nv_bfloat16*>(Kc);
     a.Vc = static_cast<const __nv_bfloat16*>(Vc);

@@ -32,11 +32,14 @@ struct GemmSeg {
 struct GemmEpi {
     GemmSeg seg[3];
     int nseg;
-    // rotary: row r sits at position pos_off + (r % rows_per_seq)
+    // rotary: row r sits at position pos_off + (r % rows_per_seq), or at
+    // row_pos[r] when row_pos is given (per-sequence context lengths)
     const float* rope;   // [P][hd/2][2] (cos, sin)
     int hd;
     int rows_per_seq;
     int pos_off;
+    const int32_t* row_pos;   // nullable [M]
+    const int32_t* row_dst;   // nullable [M]: output row of GEMM row r (scatter), < 0 skips the row
     // residual
     float* resid;        // fp32 [M][ld_resid]
     int ld_resid;
@@ -101,9 +104,9 @@ __device__ __forceinline__ void epi_store(const GemmShape& sh, const GemmEpi& ep
     for (int j = 1; j < 3; ++j)
         if (j < ep.nseg && n0 >= ep.seg[j].n_begin) s = j;
     const GemmSeg sg = ep.seg[s];
-    const bool ok = row < sh.M;
-    __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(sg.out) + (int64_t)(ok ? row : 0) * sg.ld +
-                         (n0 - sg.n_begin);
+    const int64_t orow = (row < sh.M) ? (ep.row_dst ? (int64_t)ep.row_dst[row] : (int64_t)row) : -1;
+    const bool ok = orow >= 0;
+    __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(sg.out) + (ok ? orow : 0) * sg.ld + (n0 - sg.n_begin);
     if (!sg.rope) {
         #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
@@ -115,7 +118,7 @@ __device__ __forceinline__ void epi_store(const GemmShape& sh, const GemmEpi& ep
     }
     const int hd = ep.hd;
     const int half = hd >> 1;
-    const int pos = ep.pos_off + (ok ? row : 0) % ep.rows_per_seq;
+    const int pos = !ok ? 0 : (ep.row_pos ? ep.row_pos[row] : ep.pos_off + row % ep.rows_per_seq);
     const float2* cs = reinterpret_cast<const float2*>(ep.rope) + (int64_t)pos * half;
     #pragma unroll 1
     for (int h0 = 0; h0 < BN; h0 += hd) {

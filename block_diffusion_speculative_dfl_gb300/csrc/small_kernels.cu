@@ -127,6 +127,51 @@ dfl_status greedy_accept(const int32_t* draft, const int32_t* target, int N, int
     return last_launch();
 }
 
+// ------------------------------------------------------ context-cache plan
+
+// Row plan of a cached draft step (SpecDiff-2 notes, "Future work and
+// limitations": KV-cache support for the drafter).  Sequence n with c0 cached
+// positions and m new rows: new row i < m sits at position c0 + i and goes to
+// cache row n*C + c0 + i; rows i >= m are dropped (-1); the block sits at
+// c0 + m .. c0 + m + B - 1 and attends to c0 + m cached positions.  Lengths
+// out of range record DFL_ERR_INVALID_ARG and append nothing.  One CTA per
+// sequence.
+__global__ void cache_plan_kernel(int N, int R, int B, int C, int32_t* ctx_len, const int32_t* n_new, int advance,
+                                  int32_t* pos_ctx, int32_t* dst_ctx, int32_t* pos_blk, int32_t* len_new,
+                                  DevErr err) {
+    const int n = blockIdx.x;
+    __shared__ int s_c0, s_m;
+    if (threadIdx.x == 0) {
+        int c0 = ctx_len[n], m = n_new[n];
+        const bool ok = c0 >= 0 && c0 <= C && m >= 0 && m <= R && m <= C - c0;
+        if (!ok) {
+            record_error(err, DFL_ERR_INVALID_ARG);
+            c0 = min(max(c0, 0), C);
+            m = 0;
+        }
+        s_c0 = c0;
+        s_m = m;
+        len_new[n] = c0 + m;
+        if (advance && ok) ctx_len[n] = c0 + m;
+    }
+    __syncthreads();
+    const int c0 = s_c0, m = s_m;
+    for (int i = threadIdx.x; i < R; i += blockDim.x) {
+        pos_ctx[(int64_t)n * R + i] = i < m ? c0 + i : 0;
+        dst_ctx[(int64_t)n * R + i] = i < m ? n * C + c0 + i : -1;
+    }
+    for (int b = threadIdx.x; b < B; b += blockDim.x) pos_blk[(int64_t)n * B + b] = c0 + m + b;
+}
+
+dfl_status cache_plan(int N, int R, int B, int C, int32_t* ctx_len, const int32_t* n_new, int advance,
+                      int32_t* pos_ctx, int32_t* dst_ctx, int32_t* pos_blk, int32_t* len_new, DevErr err,
+                      cudaStream_t st) {
+    ProfScope ps("cache_plan", st);
+    cache_plan_kernel<<<N, 128, 0, st>>>(N, R, B, C, ctx_len, n_new, advance, pos_ctx, dst_ctx, pos_blk, len_new,
+                                         err);
+    return last_launch();
+}
+
 // --------------------------------------------------------- argmax combine
 
 // argmax over per-tile partials; equal maxima resolve to the lower column

@@ -8,10 +8,17 @@
 
 namespace dfl {
 
+struct DevErr;
+
 dfl_status rope_table(float* table, int P, int hd, double theta, cudaStream_t st);
 // out[m] = RMSNorm(in[(m / per) * stride + off + m % per]) * gain; bf16 or fp32 out.
 dfl_status rmsnorm_rows(const float* in, int d, int64_t M, int per, int stride, int off, const float* gain,
                         float eps, void* out, bool bf16, cudaStream_t st);
+// Row plan of a cached draft step: per-row positions and cache rows of the
+// new context rows, block positions and the attended context lengths.
+dfl_status cache_plan(int N, int R, int B, int C, int32_t* ctx_len, const int32_t* n_new, int advance,
+                      int32_t* pos_ctx, int32_t* dst_ctx, int32_t* pos_blk, int32_t* len_new, DevErr err,
+                      cudaStream_t st);
 dfl_status greedy_accept(const int32_t* draft, const int32_t* target, int N, int n, int32_t* accept_len,
                          int32_t* bonus, cudaStream_t st);
 dfl_status argmax_combine(const float* pmax, const int* pidx, int64_t M, int tiles, int32_t* out,
@@ -31,8 +38,11 @@ dfl_status swiglu_f32(const float* gate, const float* up, float* h, int64_t n, c
 // split-KV partials when more than one split is used.
 int attn_splits(int N, int C, int B, int Hkv);
 size_t attn_ws_bytes(int N, int C, int B, int Hq, int Hkv, int hd);
+// ctx_len (nullable, device [N]): per-sequence context keys, with C the
+// maximum (C_stride context rows per sequence in Kc / Vc).
 dfl_status attn_bf16(const void* Q, const void* Kc, const void* Vc, const void* Kb, const void* Vb, int N, int C,
-                     int B, int Hq, int Hkv, int hd, void* O, void* ws, cudaStream_t st);
+                     int B, int Hq, int Hkv, int hd, void* O, void* ws, cudaStream_t st,
+                     const int32_t* ctx_len = nullptr, int C_stride = 0);
 
 // TV acceptance diagnostic and stochastic acceptance (workspace bytes)
 size_t tv_ws_bytes(int N, int K, int G);

@@ -72,9 +72,7 @@ class DraftModel:
         self._lw = (LayerWeights * s.D)(*[LayerWeights(*[_lib.ptr(w[k]) for k in names]) for w in self.layers])
         self.ffn_gain = dev_t(ffn_gain, torch.float32) if s.F > 0 else None
         self._sp = SampleParams(s.K, s.T, s.seed) if s.K > 0 else None
-        self.ws_bytes = _lib.workspace_size(_lib.DFL_OP_DRAFT_STEP, N=s.N, C=s.C, B=s.B, d=s.d, Hq=s.Hq, Hkv=s.Hkv,
-                                            hd=s.hd, D=s.D, L=s.L, V=s.V, K=s.K, G=s.B - 1, row0=1, dtype=s.dt,
-                                            F=s.F)
+        self.ws_bytes = self._workspace_bytes()
         self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
         self.Xb = torch.empty((s.N, s.B, s.d), dtype=torch.float32, device=dev)
         n = s.B - 1
@@ -90,18 +88,26 @@ class DraftModel:
         self.tv_tokens = torch.empty((s.N, s.K), dtype=torch.float32, device=dev) if (tv and s.K > 0) else None
         self.accept_rule, self.accept_seed = int(accept_rule), int(accept_seed)
 
+    def _workspace_bytes(self) -> int:
+        s = self.shape
+        return _lib.workspace_size(_lib.DFL_OP_DRAFT_STEP, N=s.N, C=s.C, B=s.B, d=s.d, Hq=s.Hq, Hkv=s.Hkv, hd=s.hd,
+                                   D=s.D, L=s.L, V=s.V, K=s.K, G=s.B - 1, row0=1, dtype=s.dt, F=s.F)
+
     def want_logits(self, on: bool = True):
         """Keep the fp32 logits [N*(B-1)][V] of each step (needed to check argmax bit-exactly)."""
         s = self.shape
         self.logits = (torch.empty((s.N * (s.B - 1), s.V), dtype=torch.float32, device=self.Xb.device)
                        if on and s.V > 0 else None)
 
+    def _h_rows(self) -> int:
+        return self.shape.C
+
     def _args(self, H, Xb0, target, vlog) -> StepArgs:
         s = self.shape
         a = StepArgs()
         a.N, a.C, a.B, a.d, a.Hq, a.Hkv, a.hd, a.D, a.L, a.V = s.N, s.C, s.B, s.d, s.Hq, s.Hkv, s.hd, s.D, s.L, s.V
         a.dtype, a.eps = s.dt, s.eps
-        a.H, a.h_layer_stride = _lib.ptr(H), s.N * s.C * s.d
+        a.H, a.h_layer_stride = _lib.ptr(H), s.N * self._h_rows() * s.d
         a.mix_logits, a.mix_gain, a.blk_gain = _lib.ptr(self.mix_logits), _lib.ptr(self.mix_gain), _lib.ptr(self.blk_gain)
         a.final_gain, a.rope = _lib.ptr(self.final_gain), _lib.ptr(self.rope)
         a.layers = C.cast(self._lw, C.POINTER(LayerWeights))
@@ -149,5 +155,89 @@ class DraftModel:
                 out["draft"] = self.draft.to("cpu", non_blocking=True)
             if self.selected is not None and vlog_host is not None:
                 out["selected"] = self.selected.to("cpu", non_blocking=True)
+        st.synchronize()
+        return out, dev_in
+
+
+class CachedDraftModel(DraftModel):
+    """Drafter with per-layer context K/V caches (``dfl_draft_step_cached``).
+
+    ``shape.C`` is the cache capacity per sequence; a step brings up to ``R``
+    (at most ``R_max``) new context rows per sequence in H [L][N*R][d], whose
+    keys/values are appended to the caches at positions ``ctx_len[n]..``; the
+    block attends to every cached position of its sequence.  ``ctx_len``
+    lives on the device and, with ``advance``, moves forward inside the step.
+    """
+
+    def __init__(self, shape: DraftShape, R_max: int, *args, **kw):
+        if shape.dtype != "bf16":
+            raise ValueError("the cached draft step runs in bf16")
+        self.R_max = self.R = int(R_max)
+        super().__init__(shape, *args, **kw)
+        s = self.shape
+        dev = self.Xb.device
+        self.K_cache = torch.zeros((s.D, s.N, s.C, s.Hkv, s.hd), dtype=torch.bfloat16, device=dev)
+        self.V_cache = torch.zeros_like(self.K_cache)
+        self.ctx_len = torch.zeros((s.N,), dtype=torch.int32, device=dev)
+
+    def _workspace_bytes(self) -> int:
+        s = self.shape
+        return _lib.workspace_size(_lib.DFL_OP_DRAFT_STEP_CACHED, N=s.N, C=s.C, B=s.B, d=s.d, Hq=s.Hq, Hkv=s.Hkv,
+                                   hd=s.hd, D=s.D, L=s.L, V=s.V, K=s.K, G=s.B - 1, row0=1, dtype=s.dt, F=s.F,
+                                   R=self.R_max)
+
+    def _h_rows(self) -> int:
+        return self.R
+
+    def reset(self, ctx_len=None):
+        """Set the cached lengths (default: empty caches)."""
+        if ctx_len is None:
+            self.ctx_len.zero_()
+        else:
+            self.ctx_len.copy_(torch.as_tensor(ctx_len, dtype=torch.int32))
+
+    def step(self, H_new, Xb0, n_new, target=None, vlog=None, R=None, advance=True, stream=None):
+        """One cached draft step.
+
+        H_new [L][N*R][d]: the new context rows of each sequence (rows past
+        n_new[n] are ignored); n_new [N] device int32.
+        """
+        s = self.shape
+        self.R = self.R_max if R is None else int(R)
+        if not 1 <= self.R <= self.R_max:
+            raise ValueError(f"R={self.R} outside 1..{self.R_max}")
+        cache = _lib.CtxCache()
+        cache.K, cache.V = _lib.ptr(self.K_cache), _lib.ptr(self.V_cache)
+        cache.layer_stride = s.N * s.C * s.Hkv * s.hd
+        cache.R = self.R
+        cache.ctx_len = _lib.ptr(self.ctx_len)
+        cache.n_new = _lib.ptr(n_new)
+        cache.advance = 1 if advance else 0
+        self._last_args, self._last_cache = self._args(H_new, Xb0, target, vlog), cache
+        _lib.dfl_draft_step_cached(self._last_args, cache, self.ws, self.ws_bytes, stream)
+
+    def step_from_host(self, H_host, Xb0_host, n_new_host, target_host=None, vlog_host=None, dev_in=None, R=None,
+                       advance=True, stream=None):
+        """End-to-end cached step: pinned host inputs (the new rows, block init, n_new) in, results out.
+
+        The caches and lengths stay on the device between calls.
+        """
+        st = stream or torch.cuda.current_stream()
+        if dev_in is None:
+            dev_in = {}
+        ins = {"H": H_host, "Xb0": Xb0_host, "n_new": n_new_host, "target": target_host, "vlog": vlog_host}
+        with torch.cuda.stream(st):
+            for k, h in ins.items():
+                if h is None:
+                    continue
+                if k not in dev_in:
+                    dev_in[k] = torch.empty(h.shape, dtype=h.dtype, device=self.Xb.device)
+                dev_in[k].copy_(h, non_blocking=True)
+            self.step(dev_in["H"], dev_in["Xb0"], dev_in["n_new"], dev_in.get("target"), dev_in.get("vlog"), R=R,
+                      advance=advance, stream=st)
+            out = {"accept_len": self.accept_len.to("cpu", non_blocking=True),
+                   "bonus": self.bonus.to("cpu", non_blocking=True)}
+            if self.draft is not None:
+                out["draft"] = self.draft.to("cpu", non_blocking=True)
         st.synchronize()
         return out, dev_in

@@ -29,6 +29,7 @@ __all__ = [
     "gen_hidden", "gen_hidden_scales", "gen_mix_logits", "gen_gains",
     "gen_layer_weights", "gen_lm_head", "gen_block_init", "gen_verifier_logits",
     "plant_targets", "geometric_prefix", "WEIGHT_NAMES", "FFN_WEIGHT_NAMES", "gen_ffn_gains",
+    "gen_hidden_rows", "gen_cache_state",
 ]
 
 
@@ -57,6 +58,8 @@ class Workload:
     rope_theta: float = 1.0e6
     eps: float = 1.0e-6
     F: int = 0                 # feed-forward width of full draft layers (0: no FFN)
+    R: int = 0                 # cached-context workloads: new context rows per step
+                               # (C is then the cache capacity per sequence)
 
     @property
     def gamma(self) -> int:
@@ -93,12 +96,20 @@ WORKLOADS = {
                                      Hkv=8, hd=128, D=7, L=9, B=16, C=2048,
                                      V=151936, dtype="bf16", seed=1006,
                                      geom_p=0.15, F=12288),
+    # A next-row workload: the Qwen3-8B drafter in steady-state decoding with
+    # a per-layer context K/V cache.  Capacity 4096 positions per sequence,
+    # cached lengths ragged around 2048, up to 16 new rows per step.
+    "qwen3_8b_drafter_cached": Workload("qwen3_8b_drafter_cached", N=32, d=4096, Hq=32, Hkv=8, hd=128, D=7,
+                                        L=9, B=16, C=4096, V=151936, dtype="bf16", seed=1007, geom_p=0.15,
+                                        R=16),
 }
 
 # Tensor ids keying the PCG64 streams.
 _TID_H, _TID_HSCALE, _TID_MIX, _TID_W, _TID_LM = 1, 2, 3, 4, 5
 _TID_ANCHOR, _TID_MASK, _TID_VLOG, _TID_PLANT, _TID_GAIN = 6, 7, 8, 9, 10
 _TID_FFN_GAIN = 11
+_TID_HROWS, _TID_CACHE = 12, 13
+_HCHUNK = 256   # positions per stream of gen_hidden_rows
 WEIGHT_NAMES = ("Wq", "Wkc", "Wvc", "Wkb", "Wvb", "Wo")
 FFN_WEIGHT_NAMES = ("W1", "W3", "W2")
 
@@ -176,6 +187,44 @@ def gen_hidden(w: Workload, seqs=None, as_bits: bool = False) -> np.ndarray:
 
     _parallel(one, [(i, j) for i in range(w.L) for j in range(len(seqs))])
     return out
+
+
+def gen_hidden_rows(w: Workload, n: int, r0: int, r1: int, as_bits: bool = False) -> np.ndarray:
+    """Target hidden states of positions r0..r1-1 of sequence n: [L][r1-r0][d].
+
+    The cached-context workloads' hidden states: drawn in 256-position
+    streams keyed (seed, tensor id, layer, sequence, chunk), so the rows that
+    arrive with one step are regenerated without the positions before them.
+    Same distribution as ``gen_hidden`` (per-(sequence, layer) scale times
+    N(0, 1), bf16-rounded for bf16 workloads).
+    """
+    if as_bits and w.dtype != "bf16":
+        raise ValueError("as_bits needs a bf16 workload")
+    scales = gen_hidden_scales(w)
+    out = np.empty((w.L, r1 - r0, w.d), np.uint16 if as_bits else np.float32)
+    chunks = list(range(r0 // _HCHUNK, (r1 + _HCHUNK - 1) // _HCHUNK)) if r1 > r0 else []
+
+    def one(job):
+        i, c = job
+        x = _normal((w.seed, _TID_HROWS, i, n, c), (_HCHUNK, w.d))
+        a, b = max(r0, c * _HCHUNK), min(r1, (c + 1) * _HCHUNK)
+        x = _finish(x[a - c * _HCHUNK:b - c * _HCHUNK] * scales[n, i], w.dtype)
+        out[i, a - r0:b - r0] = bf16_bits(x) if as_bits else x
+
+    _parallel(one, [(i, c) for i in range(w.L) for c in chunks])
+    return out
+
+
+def gen_cache_state(w: Workload):
+    """Cached lengths c0[N] ~ U{C/4 .. 3C/4} and new rows n_new[N] = min(Geometric(p), R).
+
+    n_new stands for the tokens a verifier accepted in the previous step plus
+    its bonus token (at least 1, at most the R rows a step brings).
+    """
+    r = _rng(w.seed, _TID_CACHE)
+    c0 = r.integers(w.C // 4, 3 * w.C // 4 + 1, size=w.N)
+    m = np.minimum(r.geometric(w.geom_p, size=w.N), w.R)
+    return c0.astype(np.int32), m.astype(np.int32)
 
 
 def gen_mix_logits(w: Workload) -> np.ndarray:

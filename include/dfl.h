@@ -74,6 +74,8 @@ typedef struct dfl_shape {
     int32_t N, C, B, d, Hq, Hkv, hd, D, L, V, K, G, row0;
     int32_t dtype;    /* a dfl_dtype */
     int32_t F;        /* FFN width (DFL_OP_BLOCK_FFN, DFL_OP_DRAFT_STEP) */
+    int32_t R;        /* new context rows per sequence (DFL_OP_DRAFT_STEP_CACHED,
+                         where C is the cache capacity) */
 } dfl_shape;
 
 typedef enum dfl_op {
@@ -84,7 +86,8 @@ typedef enum dfl_op {
     DFL_OP_DRAFT_STEP = 5,
     DFL_OP_TV_ACCEPTANCE = 6,
     DFL_OP_SPEC_ACCEPT = 7,
-    DFL_OP_BLOCK_FFN = 8
+    DFL_OP_BLOCK_FFN = 8,
+    DFL_OP_DRAFT_STEP_CACHED = 9
 } dfl_op;
 
 /* Library version string (static storage). */
@@ -391,6 +394,45 @@ typedef struct dfl_step_args {
  */
 dfl_status dfl_draft_step(const dfl_step_args* args, void* ws, size_t ws_bytes,
                           dfl_stream stream);
+
+/* Per-layer context K/V cache of a batch of sequences.  Host struct; the
+ * tensors are device memory owned by the caller. */
+typedef struct dfl_ctx_cache {
+    void* K;                 /* in/out [D][N][C][Hkv][hd] (C = args->C, the capacity) */
+    void* V;                 /* in/out, same layout as K */
+    int64_t layer_stride;    /* elements between the draft layers' slabs, >= N*C*Hkv*hd */
+    int32_t R;               /* rows per sequence of args->H this step, >= 1 */
+    int32_t* ctx_len;        /* in/out device [N]: positions already cached */
+    const int32_t* n_new;    /* in device [N]: valid new rows of each sequence, <= R */
+    int32_t advance;         /* nonzero: ctx_len[n] += n_new[n] during the step */
+} dfl_ctx_cache;
+
+/*
+ * dfl_draft_step_cached -- the draft step with an incremental context K/V
+ * cache.  SpecDiff-2 notes, "Future work and limitations" (hardware
+ * optimisation): the drafter lacks KV-cache support for its gamma-length
+ * drafts.  A context key/value is a row-wise function of that position's
+ * target hidden states and of its position, so the keys/values of positions
+ * seen in earlier steps are kept and only the positions that arrive with this
+ * step are mixed and projected.
+ *   For sequence n with c0 = ctx_len[n] and m = n_new[n], rows 0..m-1 of its
+ *   R-row slot of H (args->H is [L][N*R][d]; rows m..R-1 are ignored) are the
+ *   target hidden states of positions c0..c0+m-1.  Every draft layer
+ *   appends their rotated keys and their values at rows c0..c0+m-1 of its
+ *   cache, then runs the block over the c0+m cached positions with the
+ *   block at positions c0+m..c0+m+B-1; the rest is dfl_draft_step.
+ *   args: as dfl_draft_step, with C the cache capacity per sequence and
+ *   args->rope holding C+B positions.  bf16 only.
+ *   ws: dfl_workspace_size(DFL_OP_DRAFT_STEP_CACHED) bytes, the shape's C the
+ *   capacity and R the rows per sequence.
+ *   Errors: host-side as dfl_draft_step, UNSUPPORTED_SHAPE for fp32.  A
+ *   sequence whose lengths are out of range on the device (c0 < 0, m < 0,
+ *   m > R or c0 + m > C) records DFL_ERR_INVALID_ARG in the device error
+ *   word and appends nothing; its block runs over min(max(c0, 0), C) cached
+ *   positions.
+ */
+dfl_status dfl_draft_step_cached(const dfl_step_args* args, const dfl_ctx_cache* cache,
+                                 void* ws, size_t ws_bytes, dfl_stream stream);
 
 /* Synchronise `stream`, then read and clear this device's error word (DFL_OK
  * if no kernel recorded an error). */
