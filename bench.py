@@ -151,6 +151,7 @@ def kernel_work(w, ctx_lens=None):
         "gemm_block_qkv": (2.0 * rows_b * (qd + 2 * kv) * d,
                            2.0 * (rows_b * d + (qd + 2 * kv) * d + rows_b * (qd + 2 * kv))),
         "attn_bf16": (4.0 * B * Hq * keys * hd, 2.0 * (2 * keys * kv + 2 * rows_b * qd)),
+        "attn_tc": (4.0 * B * Hq * keys * hd, 2.0 * (2 * keys * kv + 2 * rows_b * qd)),
         "gemm_o_proj": (2.0 * rows_b * d * qd, 2.0 * (rows_b * qd + d * qd) + 8.0 * rows_b * d),
     }
     if w.F > 0:

@@ -11,7 +11,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(os.path.dirname(PKG), "include")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT_DIR, "libdfl.so")
-SOURCES = ["api.cu", "mix_rmsnorm.cu", "gemm_tc.cu", "block_attn.cu", "small_kernels.cu", "self_select.cu",
+SOURCES = ["api.cu", "mix_rmsnorm.cu", "gemm_tc.cu", "block_attn.cu", "block_attn_tc.cu", "small_kernels.cu", "self_select.cu",
            "accept_ext.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I" + INCLUDE]

@@ -60,9 +60,9 @@ uint64_t wait_limit_ns() { return g_wait_ns.load(); }
 
 size_t ws_dual_kv_proj(int N, int B, int d, int dt) { return al256((size_t)N * B * d * esz(dt)); }
 
-size_t ws_block_attn(int N, int C, int B, int Hq, int Hkv, int hd, int dt) {
+size_t ws_block_attn(int N, int C, int B, int Hq, int Hkv, int hd, int dt, bool ragged = false) {
     size_t b = al256((size_t)N * B * Hq * hd * esz(dt));
-    if (dt == DFL_BF16) b += al256(attn_ws_bytes(N, C, B, Hq, Hkv, hd));
+    if (dt == DFL_BF16) b += al256(attn_ws_bytes(N, C, B, Hq, Hkv, hd, ragged));
     return b;
 }
 
@@ -97,7 +97,7 @@ size_t step_ws_bytes(const dfl_shape& s, bool cached) {
     b += 2 * al256((size_t)s.N * s.B * s.Hkv * s.hd * e);                    // Kb, Vb
     if (cached) b += 2 * al256((size_t)rows * 4) + al256((size_t)s.N * s.B * 4) + al256((size_t)s.N * 4);
     size_t sub = ws_dual_kv_proj(s.N, s.B, s.d, s.dtype);
-    sub = std::max(sub, ws_block_attn(s.N, s.C, s.B, s.Hq, s.Hkv, s.hd, s.dtype));
+    sub = std::max(sub, ws_block_attn(s.N, s.C, s.B, s.Hq, s.Hkv, s.hd, s.dtype, cached));
     if (s.F > 0) sub = std::max(sub, ws_block_ffn(s.N, s.B, s.d, s.F, s.dtype));
     if (s.V > 0) {
         sub = std::max(sub, ws_lm_head(s.N, s.B, 1, s.d, s.V, s.dtype, true));

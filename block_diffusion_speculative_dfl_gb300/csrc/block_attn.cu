@@ -310,7 +310,8 @@ int attn_splits(int N, int C, int B, int Hkv) {
     return best_s;
 }
 
-size_t attn_ws_bytes(int N, int C, int B, int Hq, int Hkv, int hd) {
+size_t attn_ws_bytes(int N, int C, int B, int Hq, int Hkv, int hd, bool ragged) {
+    if (attn_tc_supported(B, Hq, Hkv, hd)) return attn_tc_ws_bytes(N, C, B, Hq, Hkv, hd, ragged);
     const int S = attn_splits(N, C, B, Hkv);
     if (S == 1) return 0;
     const size_t NQ = (size_t)N * B * Hq;
@@ -320,6 +321,8 @@ size_t attn_ws_bytes(int N, int C, int B, int Hq, int Hkv, int hd) {
 dfl_status attn_bf16(const void* Q, const void* Kc, const void* Vc, const void* Kb, const void* Vb, int N, int C,
                      int B, int Hq, int Hkv, int hd, void* O, void* ws, cudaStream_t st, const int32_t* ctx_len,
                      int C_stride) {
+    if (attn_tc_supported(B, Hq, Hkv, hd)) return attn_tc(Q, Kc, Vc, Kb, Vb, N, C, B, Hq, Hkv, hd, O, ws, st, ctx_len,
+                                                          C_stride);
     AttnArgs a{};
     a.ctx_len = ctx_len;
     a.C_stride = ctx_len ? C_stride : C;

@@ -1,0 +1,669 @@
+// Block attention of one draft layer on the 5th-generation tensor cores.
+//
+// DFlare post, "Generating candidates in parallel, the target decides
+// acceptance": the block is predicted in one forward with bidirectional
+// attention inside the block; DFlash article, "Writing a whole block in one
+// forward pass": target context features enter every draft layer's K/V.  So
+// the R = B * (Hq/Hkv) query rows that share K/V head g of sequence n attend
+// to all of that sequence's context keys and all B block keys, no mask:
+//   O = softmax(Q [Kc;Kb]^T / sqrt(hd)) [Vc;Vb].
+//
+// Work item = (split s, sequence n, K/V head g): one range of at most `kps`
+// keys of the sequence's Cn + B keys.  A persistent kernel (one CTA per SM)
+// takes items from a global counter; empty items (past a shorter sequence's
+// keys) are skipped by the scheduler.  Per CTA:
+//   warp 0  scheduler + TMA producer: the item's Q rows (3-D box: head dim x
+//           G heads x B block rows, zero rows up to 128) and 64-key K/V tiles
+//           of the context cache, then one tile of the block's own keys;
+//   warp 1  MMA issuer: S = Q K^T (M = 128 padded query rows, N = 64 keys,
+//           K = hd) into a double-buffered TMEM tile, then O += P V (K = 64
+//           keys, N = hd, V read MN-major straight from its TMA tile) into a
+//           double-buffered TMEM accumulator;
+//   warps 2-5  one query row per thread (TMEM lane): masked online softmax
+//           in base 2 with lazy rescaling (O is rescaled in TMEM only when a
+//           row maximum grows by more than 2^8), P written to shared memory
+//           as bf16 in the 128-byte-swizzled K-major layout the MMA reads,
+//           and the item's epilogue (bf16 output, or fp32 partial + log-sum-
+//           exp when the sequence's keys span several items).
+// A combine kernel merges the partials of multi-item sequences.
+#include "internal.h"
+#include "small_kernels.h"
+
+namespace dfl {
+
+namespace {
+
+constexpr int AT_KT = 64;           // keys per tile
+constexpr int AT_M = 128;           // MMA rows (query rows, zero-padded)
+constexpr int AT_THREADS = 192;     // 6 warps
+constexpr float AT_LAZY = 8.f;      // rescale O only when a row max grows by more than this (log2 units)
+constexpr int AT_IRING = 4;         // scheduled items in flight between the warps
+
+struct AtArgs {
+    int N, B, Hq, Hkv, G, R;
+    int rb;                   // first MMA row holding a query row (64 when R <= 64: the softmax rows
+                              // then sit in TMEM lane quadrants 2-3, away from the producer / MMA warps)
+    int C;                    // context keys per sequence (the maximum when ctx_len is given)
+    int C_stride;             // context rows per sequence in Kc / Vc
+    const int32_t* ctx_len;   // nullable [N]
+    int kps;                  // keys per item (multiple of 64)
+    int S;                    // items per (sequence, K/V head)
+    int items;                // S * N * Hkv
+    int* counter;             // zeroed before the launch
+    __nv_bfloat16* O;         // [N*B*Hq][hd]
+    float* Opart;             // [S][N*B*Hq][hd]
+    float* lse;               // [S][N*B*Hq], log2 units
+    float scale_log2;         // log2(e) / sqrt(hd)
+};
+
+template <int HD>
+struct AtCfg {
+    static constexpr int KB = HD / 64;                 // 64-element K-blocks of a head row
+    static constexpr int Q_BYTES = AT_M * HD * 2;      // one Q buffer
+    static constexpr int QKB_BYTES = AT_M * 128;       // one K-block of Q (128 rows x 128 B)
+    static constexpr int P_BYTES = AT_M * AT_KT * 2;   // one P buffer
+    static constexpr int T_BYTES = AT_KT * HD * 2;     // one K or V tile
+    static constexpr int TKB_BYTES = AT_KT * 128;      // one K-block of a K/V tile
+    static constexpr int STAGES = HD == 128 ? 4 : 8;
+    static constexpr int O_COL = 2 * AT_KT;            // TMEM: S buffers at 0 / 64, O buffers from 128
+    static constexpr int TMEM_COLS = HD == 128 ? 512 : 256;
+    static constexpr int SMEM = 1024 + 2 * Q_BYTES + 2 * P_BYTES + STAGES * 2 * T_BYTES + 512;
+};
+
+// One work item, decoded identically by every warp.
+struct AtItem {
+    int n, g, s;
+    int Cn;          // context keys of the sequence
+    int lo, hi;      // key range [lo, hi) of the Cn + B keys
+    int nctx;        // context tiles (64 keys from lo, valid below min(hi, Cn))
+    int blk;         // 1 if the range reaches into the block keys
+    int direct;      // the whole sequence fits one item: write O directly
+};
+
+__device__ __forceinline__ bool at_decode(const AtArgs& a, int it, AtItem& x) {
+    const int units = a.N * a.Hkv;
+    x.s = it / units;
+    const int u = it - x.s * units;
+    x.n = u / a.Hkv;
+    x.g = u - x.n * a.Hkv;
+    x.Cn = a.ctx_len ? a.ctx_len[x.n] : a.C;
+    const int kn = x.Cn + a.B;
+    x.lo = x.s * a.kps;
+    if (x.lo >= kn) return false;
+    x.hi = min(kn, x.lo + a.kps);
+    const int ce = min(x.hi, x.Cn);
+    x.nctx = ce > x.lo ? (ce - x.lo + AT_KT - 1) / AT_KT : 0;
+    x.blk = x.hi > x.Cn ? 1 : 0;
+    x.direct = kn <= a.kps ? 1 : 0;
+    return true;
+}
+
+// Tile t of an item: context tile (t < nctx) or the block tile; the valid
+// keys of its 64 rows are [v0, v1).
+__device__ __forceinline__ void at_tile_range(const AtItem& x, int t, int& v0, int& v1) {
+    if (t < x.nctx) {
+        const int k0 = x.lo + t * AT_KT;
+        v0 = 0;
+        v1 = min(AT_KT, min(x.hi, x.Cn) - k0);
+    } else {
+        v0 = max(x.lo, x.Cn) - x.Cn;
+        v1 = x.hi - x.Cn;
+    }
+}
+
+template <int HD>
+__global__ void __launch_bounds__(AT_THREADS, 1)
+attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmKc,
+               const __grid_constant__ CUtensorMap tmVc, const __grid_constant__ CUtensorMap tmKb,
+               const __grid_constant__ CUtensorMap tmVb, const AtArgs a, const DevErr err) {
+    using Cfg = AtCfg<HD>;
+    constexpr int ST = Cfg::STAGES;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sQ = sm;                                   // [2][Q_BYTES]
+    uint8_t* sP = sQ + 2 * Cfg::Q_BYTES;                // [2][P_BYTES]
+    uint8_t* sKV = sP + 2 * Cfg::P_BYTES;               // [ST][K tile, V tile]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sKV + ST * 2 * Cfg::T_BYTES);
+    uint64_t* kv_full = bars;                           // [ST]
+    uint64_t* kv_empty = kv_full + ST;                  // [ST]
+    uint64_t* q_full = kv_empty + ST;                   // [2]
+    uint64_t* q_empty = q_full + 2;                     // [2]
+    uint64_t* s_full = q_empty + 2;                     // [2]
+    uint64_t* s_empty = s_full + 2;                     // [2]
+    uint64_t* p_full = s_empty + 2;                     // [2]
+    uint64_t* p_empty = p_full + 2;                     // [2]
+    uint64_t* o_full = p_empty + 2;                     // [2]
+    uint64_t* o_empty = o_full + 2;                     // [2]
+    uint64_t* i_full = o_empty + 2;                     // [AT_IRING]
+    uint64_t* i_empty = i_full + AT_IRING;              // [AT_IRING]
+    uint64_t* drain = i_empty + AT_IRING;
+    int* i_ring = reinterpret_cast<int*>(drain + 1);    // [AT_IRING]
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(i_ring + AT_IRING);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < ST; ++s) { mbar_init(&kv_full[s], 1); mbar_init(&kv_empty[s], 1); }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&q_full[b], 1); mbar_init(&q_empty[b], 1);
+            mbar_init(&s_full[b], 1); mbar_init(&s_empty[b], 128);
+            mbar_init(&p_full[b], 128); mbar_init(&p_empty[b], 1);
+            mbar_init(&o_full[b], 1); mbar_init(&o_empty[b], 128);
+        }
+        for (int r = 0; r < AT_IRING; ++r) { mbar_init(&i_full[r], 1); mbar_init(&i_empty[r], 1 + 4); }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    // Zero both Q buffers: rows R..127 stay zero (TMA writes only the R real rows).
+    for (int i = threadIdx.x; i < 2 * Cfg::Q_BYTES / 16; i += AT_THREADS)
+        reinterpret_cast<uint4*>(sQ)[i] = make_uint4(0, 0, 0, 0);
+    fence_proxy_async_smem();
+    if (warp == 0 && lane == 0) {
+        prefetch_tensormap(&tmQ); prefetch_tensormap(&tmKc); prefetch_tensormap(&tmVc);
+        prefetch_tensormap(&tmKb); prefetch_tensormap(&tmVb);
+    }
+    if (warp == 1) { tmem_alloc(tmem_holder, Cfg::TMEM_COLS); tmem_relinquish(); }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ------------------------------------------ scheduler + TMA producer
+            int icount = 0, tcount = 0, q_loads = 0;
+            uint32_t kv_fills = 0;
+            bool aborted = false;
+            while (true) {
+                int it = -1;
+                AtItem x;
+                while (true) {   // next non-empty item
+                    const int c = atomicAdd(a.counter, 1);
+                    if (c >= a.items) break;
+                    if (at_decode(a, c, x)) { it = c; break; }
+                }
+                const int r = icount % AT_IRING;
+                if (*abort_flag || !mbar_wait(&i_empty[r], ((icount / AT_IRING) & 1) ^ 1, err)) { aborted = true; break; }
+                i_ring[r] = it;
+                mbar_arrive(&i_full[r]);
+                if (it < 0) break;
+                const int qb = icount & 1;
+                if (*abort_flag || !mbar_wait(&q_empty[qb], ((icount >> 1) & 1) ^ 1, err)) { aborted = true; break; }
+                mbar_arrive_expect_tx(&q_full[qb], a.R * HD * 2);
+                #pragma unroll
+                for (int kb = 0; kb < Cfg::KB; ++kb)
+                    tma_load_3d(sQ + qb * Cfg::Q_BYTES + kb * Cfg::QKB_BYTES + a.rb * 128, &tmQ, kb * 64, x.g * a.G,
+                                x.n * a.B, &q_full[qb]);
+                ++q_loads;
+                const int nt = x.nctx + x.blk;
+                for (int t = 0; t < nt && !aborted; ++t) {
+                    const int s = tcount % ST;
+                    if (*abort_flag || !mbar_wait(&kv_empty[s], ((tcount / ST) & 1) ^ 1, err)) { aborted = true; break; }
+                    mbar_arrive_expect_tx(&kv_full[s], 2 * Cfg::T_BYTES);
+                    uint8_t* dK = sKV + s * 2 * Cfg::T_BYTES;
+                    uint8_t* dV = dK + Cfg::T_BYTES;
+                    const bool ctx = t < x.nctx;
+                    const int row = ctx ? x.n * a.C_stride + x.lo + t * AT_KT : x.n * a.B;
+                    #pragma unroll
+                    for (int kb = 0; kb < Cfg::KB; ++kb) {
+                        const int col = x.g * HD + kb * 64;
+                        tma_load_2d(dK + kb * Cfg::TKB_BYTES, ctx ? &tmKc : &tmKb, col, row, &kv_full[s]);
+                        tma_load_2d(dV + kb * Cfg::TKB_BYTES, ctx ? &tmVc : &tmVb, col, row, &kv_full[s]);
+                    }
+                    kv_fills |= 1u << s;
+                    ++tcount;
+                }
+                if (aborted) break;
+                ++icount;
+            }
+            if (aborted) {
+                *abort_flag = 1;
+                // let issued copies land before the CTA exits: the latest fill of
+                // each buffer has the parity of its fill count
+                for (int s = 0; s < ST; ++s) {
+                    if (!(kv_fills & (1u << s))) continue;
+                    const int last = tcount - 1 - ((tcount - 1 - s) % ST + ST) % ST;   // latest tile using stage s
+                    mbar_wait(&kv_full[s], (last / ST) & 1, err);
+                }
+                for (int qb = 0; qb < 2 && qb < q_loads; ++qb) {
+                    const int last = q_loads - 1 - ((q_loads - 1 - qb) & 1);   // latest load into buffer qb
+                    mbar_wait(&q_full[qb], (last >> 1) & 1, err);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ------------------------------------------------------ MMA issuer
+            constexpr uint32_t idesc_s = idesc_bf16(AT_M, AT_KT);
+            constexpr uint32_t idesc_o = idesc_bf16_bmn(AT_M, HD);
+            int icount = 0, tcount = 0;
+            bool aborted = false, issued = false;
+            // the P V product of the previous tile waits until its P is ready
+            int pv_t = -1, pv_first = 0, pv_last = 0, pv_ob = 0, pv_oi = 0;
+            auto issue_pv = [&]() -> bool {
+                const int b = pv_t & 1;
+                if (*abort_flag || !mbar_wait(&p_full[b], (pv_t >> 1) & 1, err)) return false;
+                if (pv_first && !mbar_wait(&o_empty[pv_ob], ((pv_oi >> 1) & 1) ^ 1, err)) return false;
+                tc_fence_after();
+                const int s = pv_t % ST;
+                const uint32_t vaddr = smem_u32(sKV + s * 2 * Cfg::T_BYTES + Cfg::T_BYTES);
+                const uint64_t pd = sw128_desc(smem_u32(sP + b * Cfg::P_BYTES));
+                const uint32_t o_tmem = tmem_base + Cfg::O_COL + pv_ob * HD;
+                #pragma unroll
+                for (int j = 0; j < AT_KT / 16; ++j)
+                    mma_bf16(o_tmem, pd + 2 * j, sw128_desc_mn(vaddr + j * 16 * 128, Cfg::TKB_BYTES, 1024), idesc_o,
+                             (pv_first && j == 0) ? 0 : 1);
+                issued = true;
+                mma_commit(&kv_empty[s]);
+                mma_commit(&p_empty[b]);
+                if (pv_last) mma_commit(&o_full[pv_ob]);
+                pv_t = -1;
+                return true;
+            };
+            while (!aborted) {
+                const int r = icount % AT_IRING;
+                if (*abort_flag || !mbar_wait(&i_full[r], (icount / AT_IRING) & 1, err)) { aborted = true; break; }
+                const int it = i_ring[r];
+                mbar_arrive(&i_empty[r]);
+                if (it < 0) break;
+                AtItem x;
+                at_decode(a, it, x);
+                const int qb = icount & 1;
+                if (*abort_flag || !mbar_wait(&q_full[qb], (icount >> 1) & 1, err)) { aborted = true; break; }
+                const uint32_t qaddr = smem_u32(sQ + qb * Cfg::Q_BYTES);
+                const int nt = x.nctx + x.blk;
+                for (int t = 0; t < nt; ++t) {
+                    const int s = tcount % ST, b = tcount & 1;
+                    if (*abort_flag || !mbar_wait(&kv_full[s], (tcount / ST) & 1, err) ||
+                        !mbar_wait(&s_empty[b], ((tcount >> 1) & 1) ^ 1, err)) { aborted = true; break; }
+                    tc_fence_after();
+                    const uint32_t kaddr = smem_u32(sKV + s * 2 * Cfg::T_BYTES);
+                    const uint32_t s_tmem = tmem_base + b * AT_KT;
+                    #pragma unroll
+                    for (int j = 0; j < HD / 16; ++j)
+                        mma_bf16(s_tmem, sw128_desc(qaddr + (j >> 2) * Cfg::QKB_BYTES + (j & 3) * 32),
+                                 sw128_desc(kaddr + (j >> 2) * Cfg::TKB_BYTES + (j & 3) * 32), idesc_s, j > 0);
+                    issued = true;
+                    mma_commit(&s_full[b]);
+                    if (t == nt - 1) mma_commit(&q_empty[qb]);
+                    if (pv_t >= 0 && !issue_pv()) { aborted = true; break; }
+                    pv_t = tcount; pv_first = t == 0; pv_last = t == nt - 1; pv_ob = icount & 1; pv_oi = icount;
+                    ++tcount;
+                }
+                if (aborted) break;
+                ++icount;
+            }
+            if (!aborted && pv_t >= 0 && !issue_pv()) aborted = true;
+            if (aborted) {
+                *abort_flag = 1;
+                if (issued) {   // let issued MMAs finish before TMEM is released
+                    mma_commit(drain);
+                    mbar_wait(drain, 0, err);
+                }
+            }
+        }
+    } else {
+        // ------------------------------- softmax + epilogue: one row per thread
+        const int q4 = warp & 3;
+        const int lrow = q4 * 32 + lane;                     // TMEM lane = MMA row
+        const int row = lrow - a.rb;                         // query row of the item (R of them)
+        const bool pad = q4 * 32 + 32 <= a.rb || q4 * 32 >= a.rb + a.R;   // warp holds padding rows only
+        const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
+        int icount = 0, tcount = 0;
+        bool ok = true;
+        while (ok) {
+            const int r = icount % AT_IRING;
+            ok = mbar_wait(&i_full[r], (icount / AT_IRING) & 1, err);
+            if (!__all_sync(0xFFFFFFFFu, ok) || __any_sync(0xFFFFFFFFu, *abort_flag != 0)) { ok = false; break; }
+            const int it = i_ring[r];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&i_empty[r]);
+            if (it < 0) break;
+            AtItem x;
+            at_decode(a, it, x);
+            const int ob = icount & 1;
+            const int nt = x.nctx + x.blk;
+            float m_run = -INFINITY, l_run = 0.f;
+            for (int t = 0; t < nt; ++t) {
+                const int b = tcount & 1;
+                ok = mbar_wait(&s_full[b], (tcount >> 1) & 1, err);
+                if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }   // also reconverges the warp
+                tc_fence_after();
+                int v0, v1;
+                at_tile_range(x, t, v0, v1);
+                if (pad) {   // nothing to compute; the MMA's padding rows of P may hold anything
+                    mbar_arrive(&s_empty[b]);
+                    goto zero_v;
+                }
+                {
+                float s[AT_KT];
+                tmem_ld64(tmem_base + lane_off + b * AT_KT, s);
+                tc_fence_before();
+                mbar_arrive(&s_empty[b]);
+                if (v0 > 0 || v1 < AT_KT) {   // edge tile (warp-uniform): keys outside [v0, v1) do not exist
+                    #pragma unroll
+                    for (int j = 0; j < AT_KT; ++j)
+                        if (j < v0 || j >= v1) s[j] = -INFINITY;
+                }
+                // row maximum of the raw scores (scale > 0 commutes with max), four partial chains
+                float m4[4] = {s[0], s[1], s[2], s[3]};
+                #pragma unroll
+                for (int j = 4; j < AT_KT; j += 4) {
+                    m4[0] = fmaxf(m4[0], s[j]); m4[1] = fmaxf(m4[1], s[j + 1]);
+                    m4[2] = fmaxf(m4[2], s[j + 2]); m4[3] = fmaxf(m4[3], s[j + 3]);
+                }
+                const float mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * a.scale_log2;
+                if (t == 0) {
+                    m_run = mt;
+                } else {
+                    const bool need = mt > m_run + AT_LAZY;
+                    if (__any_sync(0xFFFFFFFFu, need)) {
+                        // O of this item holds the P V products up to the previous tile: wait for the last one
+                        const int tp = tcount - 1;
+                        ok = mbar_wait(&p_empty[tp & 1], (tp >> 1) & 1, err);
+                        if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
+                        tc_fence_after();
+                        const float m_new = need ? mt : m_run;
+                        const float alpha = exp2f(m_run - m_new);
+                        #pragma unroll 1
+                        for (int c = 0; c < HD; c += 32) {
+                            float o[32];
+                            tmem_ld32(tmem_base + lane_off + Cfg::O_COL + ob * HD + c, o);
+                            #pragma unroll
+                            for (int j = 0; j < 32; ++j) o[j] *= alpha;
+                            tmem_st32(tmem_base + lane_off + Cfg::O_COL + ob * HD + c, o);
+                        }
+                        tmem_st_wait();
+                        tc_fence_before();
+                        l_run *= alpha;
+                        m_run = m_new;
+                    }
+                }
+                // p = 2^(s * scale - m): one FMA and one SFU op per score; four partial sums
+                float l4[4] = {0.f, 0.f, 0.f, 0.f};
+                uint32_t pk[AT_KT / 2];
+                const float neg_m = -m_run;
+                #pragma unroll
+                for (int j = 0; j < AT_KT; j += 2) {
+                    const float p0 = ex2_ftz(fmaf(s[j], a.scale_log2, neg_m));
+                    const float p1 = ex2_ftz(fmaf(s[j + 1], a.scale_log2, neg_m));
+                    l4[(j >> 1) & 3] += p0 + p1;
+                    pk[j / 2] = pack_bf16(p0, p1);
+                }
+                l_run += (l4[0] + l4[1]) + (l4[2] + l4[3]);
+                // P buffer b is free once the P V product of tile tcount - 2 is done
+                if (tcount >= 2) {
+                    ok = mbar_wait(&p_empty[b], ((tcount >> 1) & 1) ^ 1, err);
+                    if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
+                }
+                uint8_t* prow = sP + b * Cfg::P_BYTES + lrow * 128;
+                #pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    *reinterpret_cast<uint4*>(prow + ((c ^ (lrow & 7)) << 4)) =
+                        make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+                }
+            zero_v:
+                // Rows of the V tile outside [v0, v1) may hold anything (cache rows past
+                // the sequence's length): zero them, so that 0 * V adds exactly nothing.
+                if (v0 > 0 || v1 < AT_KT) {
+                    // the tile's copies have landed (its MMA has read K); the stage is not
+                    // refilled before this tile's P V product, which waits for these writes
+                    ok = mbar_wait(&kv_full[tcount % ST], (tcount / ST) & 1, err);
+                    if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
+                    uint8_t* vt = sKV + (tcount % ST) * 2 * Cfg::T_BYTES + Cfg::T_BYTES;
+                    for (int i = threadIdx.x - 64; i < AT_KT * Cfg::KB * 8; i += 128) {
+                        const int kr = (i >> 3) % AT_KT;
+                        if (kr >= v0 && kr < v1) continue;
+                        *reinterpret_cast<uint4*>(vt + (i >> 3) / AT_KT * Cfg::TKB_BYTES + kr * 128 + (i & 7) * 16) =
+                            make_uint4(0, 0, 0, 0);
+                    }
+                }
+                fence_proxy_async_smem();
+                mbar_arrive(&p_full[b]);
+                ++tcount;
+            }
+            if (!ok) break;
+            // ---- epilogue of the item
+            ok = mbar_wait(&o_full[ob], (icount >> 1) & 1, err);
+            if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
+            tc_fence_after();
+            const bool real = row >= 0 && row < a.R;   // other MMA rows are zero padding
+            const int64_t NQ = (int64_t)a.N * a.B * a.Hq;
+            const int64_t qrow = real ? (int64_t)(x.n * a.B + row / a.G) * a.Hq + x.g * a.G + row % a.G : 0;
+            const float inv = 1.f / l_run;
+            #pragma unroll 1
+            for (int c = 0; c < HD && !pad; c += 32) {
+                float o[32];
+                __syncwarp();
+                tmem_ld32(tmem_base + lane_off + Cfg::O_COL + ob * HD + c, o);
+                if (!real) continue;
+                if (x.direct) {
+                    uint4* dst = reinterpret_cast<uint4*>(a.O + qrow * HD + c);
+                    #pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        dst[j] = make_uint4(pack_bf16(o[8 * j] * inv, o[8 * j + 1] * inv),
+                                            pack_bf16(o[8 * j + 2] * inv, o[8 * j + 3] * inv),
+                                            pack_bf16(o[8 * j + 4] * inv, o[8 * j + 5] * inv),
+                                            pack_bf16(o[8 * j + 6] * inv, o[8 * j + 7] * inv));
+                } else {
+                    float4* dst = reinterpret_cast<float4*>(a.Opart + ((int64_t)x.s * NQ + qrow) * HD + c);
+                    #pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        dst[j] = make_float4(o[4 * j] * inv, o[4 * j + 1] * inv, o[4 * j + 2] * inv,
+                                             o[4 * j + 3] * inv);
+                }
+            }
+            __syncwarp();
+            tc_fence_before();
+            mbar_arrive(&o_empty[ob]);
+            if (real && !x.direct) a.lse[(int64_t)x.s * NQ + qrow] = m_run + log2f(l_run);
+            ++icount;
+        }
+        if (!ok) *abort_flag = 1;
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+    }
+}
+
+// O[q] = sum_s 2^(lse_s - max) O_s / sum_s 2^(lse_s - max) over the items of
+// q's sequence, for sequences whose keys span more than one item.  One warp
+// per query row; lane i owns HD/32 consecutive elements.
+template <int HD>
+__global__ void attn_tc_combine_kernel(const float* Opart, const float* lse, int64_t NQ, int rows_per_seq, int B,
+                                       int C, const int32_t* ctx_len, int kps, __nv_bfloat16* O) {
+    constexpr int PER = HD / 32;
+    const int64_t q = blockIdx.x * (int64_t)(blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (q >= NQ) return;
+    const int n = (int)(q / rows_per_seq);
+    const int S = ((ctx_len ? ctx_len[n] : C) + B + kps - 1) / kps;
+    if (S <= 1) return;   // written by the attention kernel
+    const float l0 = lane < S ? lse[lane * NQ + q] : -INFINITY;
+    const float l1 = lane + 32 < S ? lse[(lane + 32) * NQ + q] : -INFINITY;
+    const float mx = warp_max(fmaxf(l0, l1));
+    const float w0 = lane < S ? exp2f(l0 - mx) : 0.f;
+    const float w1 = lane + 32 < S ? exp2f(l1 - mx) : 0.f;
+    const float inv = 1.f / warp_sum(w0 + w1);
+    float acc[PER];
+    #pragma unroll
+    for (int e = 0; e < PER; ++e) acc[e] = 0.f;
+    for (int sp = 0; sp < S; ++sp) {
+        const float wgt = __shfl_sync(0xFFFFFFFFu, sp < 32 ? w0 : w1, sp & 31);
+        const float* src = Opart + (sp * NQ + q) * HD + lane * PER;
+        if constexpr (PER == 4) {
+            const float4 t = *reinterpret_cast<const float4*>(src);
+            acc[0] += wgt * t.x; acc[1] += wgt * t.y; acc[2] += wgt * t.z; acc[3] += wgt * t.w;
+        } else {
+            const float2 t = *reinterpret_cast<const float2*>(src);
+            acc[0] += wgt * t.x; acc[1] += wgt * t.y;
+        }
+    }
+    __nv_bfloat16* dst = O + q * HD + lane * PER;
+    if constexpr (PER == 4) {
+        uint2 u;
+        u.x = pack_bf16(acc[0] * inv, acc[1] * inv);
+        u.y = pack_bf16(acc[2] * inv, acc[3] * inv);
+        *reinterpret_cast<uint2*>(dst) = u;
+    } else {
+        *reinterpret_cast<uint32_t*>(dst) = pack_bf16(acc[0] * inv, acc[1] * inv);
+    }
+}
+
+// bf16 [rows][cols] row-major, box = box_rows x 64 columns, 128-byte swizzle.
+bool at_map_2d(CUtensorMap* m, const void* base, int64_t rows, int cols, int box_rows) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Q [N*B][Hq][hd] as (hd, Hq, N*B); box = 64 x G heads x B block rows.
+bool at_map_q(CUtensorMap* m, const void* base, int NB, int Hq, int hd, int G, int B) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)hd, (cuuint64_t)Hq, (cuuint64_t)NB};
+    cuuint64_t strides[2] = {(cuuint64_t)hd * 2, (cuuint64_t)Hq * hd * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)G, (cuuint32_t)B};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+constexpr int AT_SLOTS = 152;   // one persistent CTA per SM of a GB300
+
+}  // namespace
+
+bool attn_tc_supported(int B, int Hq, int Hkv, int hd) {
+    if (hd != 64 && hd != 128) return false;
+    if (Hkv <= 0 || Hq % Hkv != 0) return false;
+    const int G = Hq / Hkv;
+    return B >= 1 && B <= AT_KT && G <= 256 && B * G <= AT_M;
+}
+
+// Keys per item.  Makespan model over 152 persistent CTAs, in units of one
+// 64-key tile: with fixed lengths, (rounds of items) x (tiles per item + the
+// item's fixed cost: Q load and pipeline turn-around, plus the partial
+// write-out and combine when a sequence spans several items); with per-
+// sequence lengths (`ragged`, C the capacity), lengths are taken spread evenly
+// over [0, C] and items are handed out dynamically: total work / 152 + half an
+// item.  Depends on the shape only, so workspace sizes do not depend on the
+// device.
+int attn_tc_kps(int N, int C, int B, int Hkv, bool ragged) {
+    const int units = N * Hkv;
+    const int ktiles = (C + B + AT_KT - 1) / AT_KT;
+    int best_kps = ktiles * AT_KT;
+    double best = 1e30;
+    for (int S = 1; S <= 64 && S <= ktiles; ++S) {
+        const int per = (ktiles + S - 1) / S;
+        const int kps = per * AT_KT;
+        const int s_eff = (C + B + kps - 1) / kps;
+        if (s_eff != S) continue;
+        const double ovh = 0.5 + (S > 1 ? 1.0 : 0.0);
+        double cost;
+        if (!ragged) {
+            cost = (double)((units * S + AT_SLOTS - 1) / AT_SLOTS) * (per + 1 + ovh);
+        } else {
+            double total = 0.0;
+            const int samples = 16;
+            for (int i = 0; i < samples; ++i) {
+                const int cn = (int)((double)C * (i + 0.5) / samples);
+                const int kn = cn + B;
+                for (int s = 0; s * kps < kn; ++s) {
+                    const int lo = s * kps, hi = std::min(kn, lo + kps), ce = std::min(hi, cn);
+                    const int t = (ce > lo ? (ce - lo + AT_KT - 1) / AT_KT : 0) + (hi > cn ? 1 : 0);
+                    total += t + ovh;
+                }
+            }
+            total *= (double)units / samples;
+            cost = std::max((double)per + 1 + ovh, total / AT_SLOTS + 0.5 * (per + 1 + ovh));
+        }
+        if (cost < best - 1e-9) { best = cost; best_kps = kps; }
+    }
+    return best_kps;
+}
+
+size_t attn_tc_ws_bytes(int N, int C, int B, int Hq, int Hkv, int hd, bool ragged) {
+    const int kps = attn_tc_kps(N, C, B, Hkv, ragged);
+    const int S = (C + B + kps - 1) / kps;
+    const size_t NQ = (size_t)N * B * Hq;
+    size_t b = 256;   // item counter
+    if (S > 1) b += ((S * NQ * hd * sizeof(float) + 255) & ~size_t(255)) + ((S * NQ * sizeof(float) + 255) & ~size_t(255));
+    return b;
+}
+
+dfl_status attn_tc(const void* Q, const void* Kc, const void* Vc, const void* Kb, const void* Vb, int N, int C,
+                   int B, int Hq, int Hkv, int hd, void* O, void* ws, cudaStream_t st, const int32_t* ctx_len,
+                   int C_stride) {
+    DeviceCtx* ctx = current_ctx();
+    if (!ctx) return DFL_ERR_NO_DEVICE;
+    const bool ragged = ctx_len != nullptr;
+    AtArgs a{};
+    a.N = N; a.B = B; a.Hq = Hq; a.Hkv = Hkv; a.G = Hq / Hkv; a.R = B * a.G;
+    a.rb = a.R <= 64 ? 64 : 0;
+    a.C = C; a.C_stride = ragged ? C_stride : C; a.ctx_len = ctx_len;
+    a.kps = attn_tc_kps(N, C, B, Hkv, ragged);
+    a.S = (C + B + a.kps - 1) / a.kps;
+    a.items = a.S * N * Hkv;
+    const size_t NQ = (size_t)N * B * Hq;
+    uint8_t* p = static_cast<uint8_t*>(ws);
+    a.counter = reinterpret_cast<int*>(p);
+    p += 256;
+    if (a.S > 1) {
+        a.Opart = reinterpret_cast<float*>(p);
+        p += (a.S * NQ * hd * sizeof(float) + 255) & ~size_t(255);
+        a.lse = reinterpret_cast<float*>(p);
+    }
+    a.O = static_cast<__nv_bfloat16*>(O);
+    a.scale_log2 = 1.4426950408889634f / sqrtf((float)hd);
+    CUtensorMap mq, mkc, mvc, mkb, mvb;
+    const int kv = Hkv * hd;
+    const int64_t ctx_rows = (int64_t)N * a.C_stride;
+    const void* kc = C > 0 ? Kc : Kb;   // an empty context is never read; any valid map serves
+    const void* vc = C > 0 ? Vc : Vb;
+    if (!at_map_q(&mq, Q, N * B, Hq, hd, a.G, B) ||
+        !at_map_2d(&mkc, kc, C > 0 ? ctx_rows : (int64_t)N * B, kv, AT_KT) ||
+        !at_map_2d(&mvc, vc, C > 0 ? ctx_rows : (int64_t)N * B, kv, AT_KT) ||
+        !at_map_2d(&mkb, Kb, (int64_t)N * B, kv, AT_KT) || !at_map_2d(&mvb, Vb, (int64_t)N * B, kv, AT_KT))
+        return DFL_ERR_CUDA;
+    dfl_status rc;
+    {
+        ProfScope ps("attn_tc", st);
+        if (cudaMemsetAsync(a.counter, 0, sizeof(int), st) != cudaSuccess) return DFL_ERR_CUDA;
+        const int grid = std::min(ctx->sm_count, a.items);
+        const DevErr err = dev_err(ctx);
+        auto run = [&](auto kern, int smem, int slot) -> dfl_status {
+            if (!ctx->attn_attr_set[slot]) {
+                if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+                    return DFL_ERR_CUDA;
+                ctx->attn_attr_set[slot] = true;
+            }
+            kern<<<grid, AT_THREADS, smem, st>>>(mq, mkc, mvc, mkb, mvb, a, err);
+            return last_launch();
+        };
+        rc = hd == 128 ? run(attn_tc_kernel<128>, AtCfg<128>::SMEM, 1) : run(attn_tc_kernel<64>, AtCfg<64>::SMEM, 0);
+    }
+    if (rc != DFL_OK || a.S == 1) return rc;
+    ProfScope ps("attn_combine", st);
+    const unsigned cgrid = (unsigned)((NQ + 7) / 8);
+    if (hd == 128)
+        attn_tc_combine_kernel<128><<<cgrid, 256, 0, st>>>(a.Opart, a.lse, (int64_t)NQ, B * Hq, B, C, ctx_len, a.kps,
+                                                           a.O);
+    else
+        attn_tc_combine_kernel<64><<<cgrid, 256, 0, st>>>(a.Opart, a.lse, (int64_t)NQ, B * Hq, B, C, ctx_len, a.kps,
+                                                          a.O);
+    return last_launch();
+}
+
+}  // namespace dfl

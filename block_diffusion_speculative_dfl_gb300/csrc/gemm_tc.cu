@@ -6,12 +6,6 @@
 
 namespace dfl {
 
-namespace {
-
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
 EncodeTiledFn encode_fn() {
     static EncodeTiledFn fn = nullptr;
     static std::once_flag once;
@@ -24,6 +18,8 @@ EncodeTiledFn encode_fn() {
     });
     return fn;
 }
+
+namespace {
 
 // bf16 [rows][K] row-major, box = box_rows x 64 elements, 128-byte swizzle.
 bool make_map(CUtensorMap* m, const void* base, int rows, int K, int box_rows) {

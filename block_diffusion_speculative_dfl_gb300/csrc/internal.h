@@ -17,6 +17,7 @@ struct DeviceCtx {
     int* err_word = nullptr;       // device address of this device's error word
     bool gemm_attr_set[16] = {};   // max-dynamic-smem set for gemm instantiations
     bool mix_attr_set = false;
+    bool attn_attr_set[2] = {};    // tcgen05 attention, head dim 64 / 128
 };
 
 // Context of the current device (initialised on first use); nullptr if no
@@ -63,6 +64,12 @@ struct GemmArgs {
 };
 
 dfl_status gemm_tc(DeviceCtx* ctx, const GemmArgs& g, cudaStream_t st);
+
+// The driver's cuTensorMapEncodeTiled (resolved once; nullptr if unavailable).
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_fn();
 
 // fp32 CUDA-core GEMM: C = A[M][K] * B[N][K]^T; mode 0 store (ldc), 1 accumulate.
 dfl_status gemm_f32(const float* A, const float* B, float* C, int M, int N, int K, int ldc, int accumulate,

@@ -37,7 +37,15 @@ dfl_status swiglu_f32(const float* gate, const float* up, float* h, int64_t n, c
 // bf16 block attention (tensor cores); writes O bf16 [N*B][Hq*hd].  ws holds
 // split-KV partials when more than one split is used.
 int attn_splits(int N, int C, int B, int Hkv);
-size_t attn_ws_bytes(int N, int C, int B, int Hq, int Hkv, int hd);
+// Scratch of attn_bf16; `ragged`: per-sequence context lengths (C the capacity).
+size_t attn_ws_bytes(int N, int C, int B, int Hq, int Hkv, int hd, bool ragged = false);
+// tcgen05 attention (block_attn_tc.cu): shapes it serves, its scratch, launch.
+bool attn_tc_supported(int B, int Hq, int Hkv, int hd);
+int attn_tc_kps(int N, int C, int B, int Hkv, bool ragged);
+size_t attn_tc_ws_bytes(int N, int C, int B, int Hq, int Hkv, int hd, bool ragged);
+dfl_status attn_tc(const void* Q, const void* Kc, const void* Vc, const void* Kb, const void* Vb, int N, int C,
+                   int B, int Hq, int Hkv, int hd, void* O, void* ws, cudaStream_t st, const int32_t* ctx_len,
+                   int C_stride);
 // ctx_len (nullable, device [N]): per-sequence context keys, with C the
 // maximum (C_stride context rows per sequence in Kc / Vc).
 dfl_status attn_bf16(const void* Q, const void* Kc, const void* Vc, const void* Kb, const void* Vb, int N, int C,

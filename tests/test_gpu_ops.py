@@ -152,6 +152,10 @@ def test_rope_table_matches_oracle():
     (2, 130, 8, 16, 2, 64, 320),      # hd 64, GQA group 8
     (1, 100, 33, 16, 4, 128, 256),    # 132 query rows per unit (9 warps)
     (1, 70, 64, 32, 2, 64, 256),      # 1024 query rows per unit -> rows split over CTAs
+    (3, 0, 16, 8, 2, 128, 256),       # no context: the block's own keys only
+    (1, 300, 64, 4, 2, 128, 256),     # 128 query rows per unit (the padded MMA tile full)
+    (2, 1000, 8, 8, 4, 64, 256),      # hd 64, several items per sequence
+    (32, 2048, 16, 32, 8, 128, 512),  # the Qwen3-8B drafter's attention shape
 ])
 def test_block_attn_bf16(N, C, B, Hq, Hkv, hd, d):
     rng = np.random.default_rng(N * 7 + C)
