@@ -35,14 +35,11 @@ namespace {
 
 constexpr int AT_KT = 64;           // keys per tile
 constexpr int AT_M = 128;           // MMA rows (query rows, zero-padded)
-constexpr int AT_THREADS = 192;     // 6 warps
 constexpr float AT_LAZY = 8.f;      // rescale O only when a row max grows by more than this (log2 units)
 constexpr int AT_IRING = 4;         // scheduled items in flight between the warps
 
 struct AtArgs {
     int N, B, Hq, Hkv, G, R;
-    int rb;                   // first MMA row holding a query row (64 when R <= 64: the softmax rows
-                              // then sit in TMEM lane quadrants 2-3, away from the producer / MMA warps)
     int C;                    // context keys per sequence (the maximum when ctx_len is given)
     int C_stride;             // context rows per sequence in Kc / Vc
     const int32_t* ctx_len;   // nullable [N]
@@ -58,16 +55,24 @@ struct AtArgs {
 
 template <int HD>
 struct AtCfg {
+    static constexpr int NP = 2;                       // independent pipelines per CTA (two items in flight)
     static constexpr int KB = HD / 64;                 // 64-element K-blocks of a head row
     static constexpr int Q_BYTES = AT_M * HD * 2;      // one Q buffer
     static constexpr int QKB_BYTES = AT_M * 128;       // one K-block of Q (128 rows x 128 B)
     static constexpr int P_BYTES = AT_M * AT_KT * 2;   // one P buffer
     static constexpr int T_BYTES = AT_KT * HD * 2;     // one K or V tile
     static constexpr int TKB_BYTES = AT_KT * 128;      // one K-block of a K/V tile
-    static constexpr int STAGES = HD == 128 ? 4 : 8;
-    static constexpr int O_COL = 2 * AT_KT;            // TMEM: S buffers at 0 / 64, O buffers from 128
-    static constexpr int TMEM_COLS = HD == 128 ? 512 : 256;
-    static constexpr int SMEM = 1024 + 2 * Q_BYTES + 2 * P_BYTES + STAGES * 2 * T_BYTES + 512;
+    static constexpr int NQB = 1;                      // Q buffers per pipeline
+    static constexpr int NPB = HD == 128 ? 1 : 2;      // P buffers per pipeline
+    static constexpr int NSB = 2;                      // S buffers (TMEM) per pipeline
+    static constexpr int STAGES = HD == 128 ? 2 : 4;   // K/V stages per pipeline
+    static constexpr int PIPE_BYTES = NQB * Q_BYTES + NPB * P_BYTES + STAGES * 2 * T_BYTES;
+    static constexpr int O_COL = NSB * AT_KT;          // per pipeline: S buffers from column 0, O after them
+    static constexpr int PIPE_COLS = 256;              // TMEM columns per pipeline
+    static constexpr int TMEM_COLS = NP * PIPE_COLS;
+    static constexpr int THREADS = NP * 192;
+    static constexpr int BAR_BYTES = 512;              // barriers and scheduler slots per pipeline
+    static constexpr int SMEM = 1024 + NP * (PIPE_BYTES + BAR_BYTES);
 };
 
 // One work item, decoded identically by every warp.
@@ -111,54 +116,63 @@ __device__ __forceinline__ void at_tile_range(const AtItem& x, int t, int& v0, i
     }
 }
 
+// Barriers and scheduler slots of one pipeline.
+template <int ST, int NQB, int NPB, int NSB>
+struct AtBars {
+    uint64_t kv_full[ST], kv_empty[ST];
+    uint64_t q_full[NQB], q_empty[NQB];
+    uint64_t s_full[NSB], s_empty[NSB];
+    uint64_t p_full[NPB], p_empty[NPB];
+    uint64_t o_full, o_empty;
+    uint64_t i_full[AT_IRING], i_empty[AT_IRING];
+    uint64_t drain;
+    int i_ring[AT_IRING];
+    int abort_flag;
+};
+
 template <int HD>
-__global__ void __launch_bounds__(AT_THREADS, 1)
+__global__ void __launch_bounds__(AtCfg<HD>::THREADS, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmKc,
                const __grid_constant__ CUtensorMap tmVc, const __grid_constant__ CUtensorMap tmKb,
                const __grid_constant__ CUtensorMap tmVb, const AtArgs a, const DevErr err) {
     using Cfg = AtCfg<HD>;
-    constexpr int ST = Cfg::STAGES;
+    constexpr int ST = Cfg::STAGES, NQB = Cfg::NQB, NPB = Cfg::NPB, NSB = Cfg::NSB;
+    using Bars = AtBars<ST, NQB, NPB, NSB>;
+    static_assert(sizeof(Bars) + 8 <= Cfg::BAR_BYTES, "barrier area");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* sQ = sm;                                   // [2][Q_BYTES]
-    uint8_t* sP = sQ + 2 * Cfg::Q_BYTES;                // [2][P_BYTES]
-    uint8_t* sKV = sP + 2 * Cfg::P_BYTES;               // [ST][K tile, V tile]
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sKV + ST * 2 * Cfg::T_BYTES);
-    uint64_t* kv_full = bars;                           // [ST]
-    uint64_t* kv_empty = kv_full + ST;                  // [ST]
-    uint64_t* q_full = kv_empty + ST;                   // [2]
-    uint64_t* q_empty = q_full + 2;                     // [2]
-    uint64_t* s_full = q_empty + 2;                     // [2]
-    uint64_t* s_empty = s_full + 2;                     // [2]
-    uint64_t* p_full = s_empty + 2;                     // [2]
-    uint64_t* p_empty = p_full + 2;                     // [2]
-    uint64_t* o_full = p_empty + 2;                     // [2]
-    uint64_t* o_empty = o_full + 2;                     // [2]
-    uint64_t* i_full = o_empty + 2;                     // [AT_IRING]
-    uint64_t* i_empty = i_full + AT_IRING;              // [AT_IRING]
-    uint64_t* drain = i_empty + AT_IRING;
-    int* i_ring = reinterpret_cast<int*>(drain + 1);    // [AT_IRING]
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(i_ring + AT_IRING);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sm + Cfg::NP * Cfg::PIPE_BYTES + Cfg::NP * Cfg::BAR_BYTES - 8);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int pp = warp / 6;          // this warp's pipeline
+    const int role = warp % 6;        // 0 producer, 1 MMA, 2..5 softmax
+    uint8_t* pbase = sm + pp * Cfg::PIPE_BYTES;
+    uint8_t* sQ = pbase;                                // [NQB][Q_BYTES]
+    uint8_t* sP = sQ + NQB * Cfg::Q_BYTES;              // [NPB][P_BYTES]
+    uint8_t* sKV = sP + NPB * Cfg::P_BYTES;             // [ST][K tile, V tile]
+    Bars& bb = *reinterpret_cast<Bars*>(sm + Cfg::NP * Cfg::PIPE_BYTES + pp * Cfg::BAR_BYTES);
+    volatile int* abort_flag = &bb.abort_flag;
+    // For R <= 64 the query rows of pipeline 0 sit in MMA rows 64..127 and those
+    // of pipeline 1 in rows 0..63, so the active softmax warps of the two
+    // pipelines use all four TMEM lane quadrants (SM sub-partitions).
+    const int rb = a.R <= 64 ? (pp == 0 ? 64 : 0) : 0;
 
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < ST; ++s) { mbar_init(&kv_full[s], 1); mbar_init(&kv_empty[s], 1); }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(&q_full[b], 1); mbar_init(&q_empty[b], 1);
-            mbar_init(&s_full[b], 1); mbar_init(&s_empty[b], 128);
-            mbar_init(&p_full[b], 128); mbar_init(&p_empty[b], 1);
-            mbar_init(&o_full[b], 1); mbar_init(&o_empty[b], 128);
-        }
-        for (int r = 0; r < AT_IRING; ++r) { mbar_init(&i_full[r], 1); mbar_init(&i_empty[r], 1 + 4); }
-        mbar_init(drain, 1);
-        *abort_flag = 0;
+    if ((threadIdx.x % 192) == 0) {
+        for (int s = 0; s < ST; ++s) { mbar_init(&bb.kv_full[s], 1); mbar_init(&bb.kv_empty[s], 1); }
+        for (int b = 0; b < NQB; ++b) { mbar_init(&bb.q_full[b], 1); mbar_init(&bb.q_empty[b], 1); }
+        for (int b = 0; b < NSB; ++b) { mbar_init(&bb.s_full[b], 1); mbar_init(&bb.s_empty[b], 128); }
+        for (int b = 0; b < NPB; ++b) { mbar_init(&bb.p_full[b], 128); mbar_init(&bb.p_empty[b], 1); }
+        mbar_init(&bb.o_full, 1); mbar_init(&bb.o_empty, 128);
+        for (int r = 0; r < AT_IRING; ++r) { mbar_init(&bb.i_full[r], 1); mbar_init(&bb.i_empty[r], 1 + 4); }
+        mbar_init(&bb.drain, 1);
+        bb.abort_flag = 0;
         fence_barrier_init();
     }
-    // Zero both Q buffers: rows R..127 stay zero (TMA writes only the R real rows).
-    for (int i = threadIdx.x; i < 2 * Cfg::Q_BYTES / 16; i += AT_THREADS)
-        reinterpret_cast<uint4*>(sQ)[i] = make_uint4(0, 0, 0, 0);
+    // Zero the Q buffers: MMA rows without a query row stay zero (TMA writes only the R real rows).
+    for (int i = threadIdx.x; i < Cfg::NP * Cfg::PIPE_BYTES / 16; i += Cfg::THREADS) {
+        const int off = i * 16 % Cfg::PIPE_BYTES;
+        if (off < NQB * Cfg::Q_BYTES) *reinterpret_cast<uint4*>(sm + i * 16) = make_uint4(0, 0, 0, 0);
+    }
     fence_proxy_async_smem();
     if (warp == 0 && lane == 0) {
         prefetch_tensormap(&tmQ); prefetch_tensormap(&tmKc); prefetch_tensormap(&tmVc);
@@ -168,12 +182,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem_base = *tmem_holder;
+    const uint32_t tmem_base = *tmem_holder + pp * Cfg::PIPE_COLS;
 
-    if (warp == 0) {
+    if (role == 0) {
         if (lane == 0) {
             // ------------------------------------------ scheduler + TMA producer
-            int icount = 0, tcount = 0, q_loads = 0;
+            int icount = 0, tcount = 0;
             uint32_t kv_fills = 0;
             bool aborted = false;
             while (true) {
@@ -185,23 +199,22 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                     if (at_decode(a, c, x)) { it = c; break; }
                 }
                 const int r = icount % AT_IRING;
-                if (*abort_flag || !mbar_wait(&i_empty[r], ((icount / AT_IRING) & 1) ^ 1, err)) { aborted = true; break; }
-                i_ring[r] = it;
-                mbar_arrive(&i_full[r]);
+                if (*abort_flag || !mbar_wait(&bb.i_empty[r], ((icount / AT_IRING) & 1) ^ 1, err)) { aborted = true; break; }
+                bb.i_ring[r] = it;
+                mbar_arrive(&bb.i_full[r]);
                 if (it < 0) break;
-                const int qb = icount & 1;
-                if (*abort_flag || !mbar_wait(&q_empty[qb], ((icount >> 1) & 1) ^ 1, err)) { aborted = true; break; }
-                mbar_arrive_expect_tx(&q_full[qb], a.R * HD * 2);
+                const int qb = icount % NQB;
+                if (*abort_flag || !mbar_wait(&bb.q_empty[qb], ((icount / NQB) & 1) ^ 1, err)) { aborted = true; break; }
+                mbar_arrive_expect_tx(&bb.q_full[qb], a.R * HD * 2);
                 #pragma unroll
                 for (int kb = 0; kb < Cfg::KB; ++kb)
-                    tma_load_3d(sQ + qb * Cfg::Q_BYTES + kb * Cfg::QKB_BYTES + a.rb * 128, &tmQ, kb * 64, x.g * a.G,
-                                x.n * a.B, &q_full[qb]);
-                ++q_loads;
+                    tma_load_3d(sQ + qb * Cfg::Q_BYTES + kb * Cfg::QKB_BYTES + rb * 128, &tmQ, kb * 64, x.g * a.G,
+                                x.n * a.B, &bb.q_full[qb]);
                 const int nt = x.nctx + x.blk;
                 for (int t = 0; t < nt && !aborted; ++t) {
                     const int s = tcount % ST;
-                    if (*abort_flag || !mbar_wait(&kv_empty[s], ((tcount / ST) & 1) ^ 1, err)) { aborted = true; break; }
-                    mbar_arrive_expect_tx(&kv_full[s], 2 * Cfg::T_BYTES);
+                    if (*abort_flag || !mbar_wait(&bb.kv_empty[s], ((tcount / ST) & 1) ^ 1, err)) { aborted = true; break; }
+                    mbar_arrive_expect_tx(&bb.kv_full[s], 2 * Cfg::T_BYTES);
                     uint8_t* dK = sKV + s * 2 * Cfg::T_BYTES;
                     uint8_t* dV = dK + Cfg::T_BYTES;
                     const bool ctx = t < x.nctx;
@@ -209,8 +222,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                     #pragma unroll
                     for (int kb = 0; kb < Cfg::KB; ++kb) {
                         const int col = x.g * HD + kb * 64;
-                        tma_load_2d(dK + kb * Cfg::TKB_BYTES, ctx ? &tmKc : &tmKb, col, row, &kv_full[s]);
-                        tma_load_2d(dV + kb * Cfg::TKB_BYTES, ctx ? &tmVc : &tmVb, col, row, &kv_full[s]);
+                        tma_load_2d(dK + kb * Cfg::TKB_BYTES, ctx ? &tmKc : &tmKb, col, row, &bb.kv_full[s]);
+                        tma_load_2d(dV + kb * Cfg::TKB_BYTES, ctx ? &tmVc : &tmVb, col, row, &bb.kv_full[s]);
                     }
                     kv_fills |= 1u << s;
                     ++tcount;
@@ -225,15 +238,16 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                 for (int s = 0; s < ST; ++s) {
                     if (!(kv_fills & (1u << s))) continue;
                     const int last = tcount - 1 - ((tcount - 1 - s) % ST + ST) % ST;   // latest tile using stage s
-                    mbar_wait(&kv_full[s], (last / ST) & 1, err);
+                    mbar_wait(&bb.kv_full[s], (last / ST) & 1, err);
                 }
-                for (int qb = 0; qb < 2 && qb < q_loads; ++qb) {
-                    const int last = q_loads - 1 - ((q_loads - 1 - qb) & 1);   // latest load into buffer qb
-                    mbar_wait(&q_full[qb], (last >> 1) & 1, err);
+                // the Q load of the item being filled (icount) has been issued
+                for (int b = 0; b < NQB; ++b) {
+                    const int last = icount - ((icount - b) % NQB + NQB) % NQB;
+                    if (last >= 0) mbar_wait(&bb.q_full[b], (last / NQB) & 1, err);
                 }
             }
         }
-    } else if (warp == 1) {
+    } else if (role == 1) {
         if (lane == 0) {
             // ------------------------------------------------------ MMA issuer
             constexpr uint32_t idesc_s = idesc_bf16(AT_M, AT_KT);
@@ -241,55 +255,53 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
             int icount = 0, tcount = 0;
             bool aborted = false, issued = false;
             // the P V product of the previous tile waits until its P is ready
-            int pv_t = -1, pv_first = 0, pv_last = 0, pv_ob = 0, pv_oi = 0;
+            int pv_t = -1, pv_first = 0, pv_last = 0, pv_oi = 0;
             auto issue_pv = [&]() -> bool {
-                const int b = pv_t & 1;
-                if (*abort_flag || !mbar_wait(&p_full[b], (pv_t >> 1) & 1, err)) return false;
-                if (pv_first && !mbar_wait(&o_empty[pv_ob], ((pv_oi >> 1) & 1) ^ 1, err)) return false;
+                const int pb = pv_t % NPB;
+                if (*abort_flag || !mbar_wait(&bb.p_full[pb], (pv_t / NPB) & 1, err)) return false;
+                if (pv_first && !mbar_wait(&bb.o_empty, (pv_oi & 1) ^ 1, err)) return false;
                 tc_fence_after();
                 const int s = pv_t % ST;
                 const uint32_t vaddr = smem_u32(sKV + s * 2 * Cfg::T_BYTES + Cfg::T_BYTES);
-                const uint64_t pd = sw128_desc(smem_u32(sP + b * Cfg::P_BYTES));
-                const uint32_t o_tmem = tmem_base + Cfg::O_COL + pv_ob * HD;
+                const uint64_t pd = sw128_desc(smem_u32(sP + pb * Cfg::P_BYTES));
                 #pragma unroll
                 for (int j = 0; j < AT_KT / 16; ++j)
-                    mma_bf16(o_tmem, pd + 2 * j, sw128_desc_mn(vaddr + j * 16 * 128, Cfg::TKB_BYTES, 1024), idesc_o,
-                             (pv_first && j == 0) ? 0 : 1);
+                    mma_bf16(tmem_base + Cfg::O_COL, pd + 2 * j, sw128_desc_mn(vaddr + j * 16 * 128, Cfg::TKB_BYTES, 1024),
+                             idesc_o, (pv_first && j == 0) ? 0 : 1);
                 issued = true;
-                mma_commit(&kv_empty[s]);
-                mma_commit(&p_empty[b]);
-                if (pv_last) mma_commit(&o_full[pv_ob]);
+                mma_commit(&bb.kv_empty[s]);
+                mma_commit(&bb.p_empty[pb]);
+                if (pv_last) mma_commit(&bb.o_full);
                 pv_t = -1;
                 return true;
             };
             while (!aborted) {
                 const int r = icount % AT_IRING;
-                if (*abort_flag || !mbar_wait(&i_full[r], (icount / AT_IRING) & 1, err)) { aborted = true; break; }
-                const int it = i_ring[r];
-                mbar_arrive(&i_empty[r]);
+                if (*abort_flag || !mbar_wait(&bb.i_full[r], (icount / AT_IRING) & 1, err)) { aborted = true; break; }
+                const int it = bb.i_ring[r];
+                mbar_arrive(&bb.i_empty[r]);
                 if (it < 0) break;
                 AtItem x;
                 at_decode(a, it, x);
-                const int qb = icount & 1;
-                if (*abort_flag || !mbar_wait(&q_full[qb], (icount >> 1) & 1, err)) { aborted = true; break; }
+                const int qb = icount % NQB;
+                if (*abort_flag || !mbar_wait(&bb.q_full[qb], (icount / NQB) & 1, err)) { aborted = true; break; }
                 const uint32_t qaddr = smem_u32(sQ + qb * Cfg::Q_BYTES);
                 const int nt = x.nctx + x.blk;
                 for (int t = 0; t < nt; ++t) {
-                    const int s = tcount % ST, b = tcount & 1;
-                    if (*abort_flag || !mbar_wait(&kv_full[s], (tcount / ST) & 1, err) ||
-                        !mbar_wait(&s_empty[b], ((tcount >> 1) & 1) ^ 1, err)) { aborted = true; break; }
+                    const int s = tcount % ST, b = tcount % NSB;
+                    if (*abort_flag || !mbar_wait(&bb.kv_full[s], (tcount / ST) & 1, err) ||
+                        !mbar_wait(&bb.s_empty[b], ((tcount / NSB) & 1) ^ 1, err)) { aborted = true; break; }
                     tc_fence_after();
                     const uint32_t kaddr = smem_u32(sKV + s * 2 * Cfg::T_BYTES);
-                    const uint32_t s_tmem = tmem_base + b * AT_KT;
                     #pragma unroll
                     for (int j = 0; j < HD / 16; ++j)
-                        mma_bf16(s_tmem, sw128_desc(qaddr + (j >> 2) * Cfg::QKB_BYTES + (j & 3) * 32),
+                        mma_bf16(tmem_base + b * AT_KT, sw128_desc(qaddr + (j >> 2) * Cfg::QKB_BYTES + (j & 3) * 32),
                                  sw128_desc(kaddr + (j >> 2) * Cfg::TKB_BYTES + (j & 3) * 32), idesc_s, j > 0);
                     issued = true;
-                    mma_commit(&s_full[b]);
-                    if (t == nt - 1) mma_commit(&q_empty[qb]);
+                    mma_commit(&bb.s_full[b]);
+                    if (t == nt - 1) mma_commit(&bb.q_empty[qb]);
                     if (pv_t >= 0 && !issue_pv()) { aborted = true; break; }
-                    pv_t = tcount; pv_first = t == 0; pv_last = t == nt - 1; pv_ob = icount & 1; pv_oi = icount;
+                    pv_t = tcount; pv_first = t == 0; pv_last = t == nt - 1; pv_oi = icount;
                     ++tcount;
                 }
                 if (aborted) break;
@@ -299,8 +311,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
             if (aborted) {
                 *abort_flag = 1;
                 if (issued) {   // let issued MMAs finish before TMEM is released
-                    mma_commit(drain);
-                    mbar_wait(drain, 0, err);
+                    mma_commit(&bb.drain);
+                    mbar_wait(&bb.drain, 0, err);
                 }
             }
         }
@@ -308,40 +320,39 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         // ------------------------------- softmax + epilogue: one row per thread
         const int q4 = warp & 3;
         const int lrow = q4 * 32 + lane;                     // TMEM lane = MMA row
-        const int row = lrow - a.rb;                         // query row of the item (R of them)
-        const bool pad = q4 * 32 + 32 <= a.rb || q4 * 32 >= a.rb + a.R;   // warp holds padding rows only
+        const int row = lrow - rb;                           // query row of the item (R of them)
+        const bool pad = q4 * 32 + 32 <= rb || q4 * 32 >= rb + a.R;   // warp holds padding rows only
         const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
+        const int stid = threadIdx.x - pp * 192 - 64;        // 0..127 within the pipeline's softmax warps
         int icount = 0, tcount = 0;
         bool ok = true;
         while (ok) {
             const int r = icount % AT_IRING;
-            ok = mbar_wait(&i_full[r], (icount / AT_IRING) & 1, err);
+            ok = mbar_wait(&bb.i_full[r], (icount / AT_IRING) & 1, err);
             if (!__all_sync(0xFFFFFFFFu, ok) || __any_sync(0xFFFFFFFFu, *abort_flag != 0)) { ok = false; break; }
-            const int it = i_ring[r];
+            const int it = bb.i_ring[r];
             __syncwarp();
-            if (lane == 0) mbar_arrive(&i_empty[r]);
+            if (lane == 0) mbar_arrive(&bb.i_empty[r]);
             if (it < 0) break;
             AtItem x;
             at_decode(a, it, x);
-            const int ob = icount & 1;
             const int nt = x.nctx + x.blk;
             float m_run = -INFINITY, l_run = 0.f;
             for (int t = 0; t < nt; ++t) {
-                const int b = tcount & 1;
-                ok = mbar_wait(&s_full[b], (tcount >> 1) & 1, err);
+                const int b = tcount % NSB, pb = tcount % NPB;
+                ok = mbar_wait(&bb.s_full[b], (tcount / NSB) & 1, err);
                 if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }   // also reconverges the warp
                 tc_fence_after();
                 int v0, v1;
                 at_tile_range(x, t, v0, v1);
+                uint32_t pk[AT_KT / 2];
                 if (pad) {   // nothing to compute; the MMA's padding rows of P may hold anything
-                    mbar_arrive(&s_empty[b]);
-                    goto zero_v;
-                }
-                {
+                    mbar_arrive(&bb.s_empty[b]);
+                } else {
                 float s[AT_KT];
                 tmem_ld64(tmem_base + lane_off + b * AT_KT, s);
                 tc_fence_before();
-                mbar_arrive(&s_empty[b]);
+                mbar_arrive(&bb.s_empty[b]);
                 if (v0 > 0 || v1 < AT_KT) {   // edge tile (warp-uniform): keys outside [v0, v1) do not exist
                     #pragma unroll
                     for (int j = 0; j < AT_KT; ++j)
@@ -362,7 +373,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                     if (__any_sync(0xFFFFFFFFu, need)) {
                         // O of this item holds the P V products up to the previous tile: wait for the last one
                         const int tp = tcount - 1;
-                        ok = mbar_wait(&p_empty[tp & 1], (tp >> 1) & 1, err);
+                        ok = mbar_wait(&bb.p_empty[tp % NPB], (tp / NPB) & 1, err);
                         if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
                         tc_fence_after();
                         const float m_new = need ? mt : m_run;
@@ -370,10 +381,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                         #pragma unroll 1
                         for (int c = 0; c < HD; c += 32) {
                             float o[32];
-                            tmem_ld32(tmem_base + lane_off + Cfg::O_COL + ob * HD + c, o);
+                            tmem_ld32(tmem_base + lane_off + Cfg::O_COL + c, o);
                             #pragma unroll
                             for (int j = 0; j < 32; ++j) o[j] *= alpha;
-                            tmem_st32(tmem_base + lane_off + Cfg::O_COL + ob * HD + c, o);
+                            tmem_st32(tmem_base + lane_off + Cfg::O_COL + c, o);
                         }
                         tmem_st_wait();
                         tc_fence_before();
@@ -383,7 +394,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                 }
                 // p = 2^(s * scale - m): one FMA and one SFU op per score; four partial sums
                 float l4[4] = {0.f, 0.f, 0.f, 0.f};
-                uint32_t pk[AT_KT / 2];
                 const float neg_m = -m_run;
                 #pragma unroll
                 for (int j = 0; j < AT_KT; j += 2) {
@@ -393,27 +403,30 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                     pk[j / 2] = pack_bf16(p0, p1);
                 }
                 l_run += (l4[0] + l4[1]) + (l4[2] + l4[3]);
-                // P buffer b is free once the P V product of tile tcount - 2 is done
-                if (tcount >= 2) {
-                    ok = mbar_wait(&p_empty[b], ((tcount >> 1) & 1) ^ 1, err);
+                }
+                // P buffer pb is free once the P V product of tile tcount - NPB is done.  Every
+                // warp waits, padding ones included: an arrival on p_full must never run ahead
+                // into the phase of a later tile.
+                if (tcount >= NPB) {
+                    ok = mbar_wait(&bb.p_empty[pb], ((tcount / NPB) & 1) ^ 1, err);
                     if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
                 }
-                uint8_t* prow = sP + b * Cfg::P_BYTES + lrow * 128;
-                #pragma unroll
-                for (int c = 0; c < 8; ++c)
-                    *reinterpret_cast<uint4*>(prow + ((c ^ (lrow & 7)) << 4)) =
-                        make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+                if (!pad) {
+                    uint8_t* prow = sP + pb * Cfg::P_BYTES + lrow * 128;
+                    #pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        *reinterpret_cast<uint4*>(prow + ((c ^ (lrow & 7)) << 4)) =
+                            make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
                 }
-            zero_v:
                 // Rows of the V tile outside [v0, v1) may hold anything (cache rows past
                 // the sequence's length): zero them, so that 0 * V adds exactly nothing.
                 if (v0 > 0 || v1 < AT_KT) {
                     // the tile's copies have landed (its MMA has read K); the stage is not
                     // refilled before this tile's P V product, which waits for these writes
-                    ok = mbar_wait(&kv_full[tcount % ST], (tcount / ST) & 1, err);
+                    ok = mbar_wait(&bb.kv_full[tcount % ST], (tcount / ST) & 1, err);
                     if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
                     uint8_t* vt = sKV + (tcount % ST) * 2 * Cfg::T_BYTES + Cfg::T_BYTES;
-                    for (int i = threadIdx.x - 64; i < AT_KT * Cfg::KB * 8; i += 128) {
+                    for (int i = stid; i < AT_KT * Cfg::KB * 8; i += 128) {
                         const int kr = (i >> 3) % AT_KT;
                         if (kr >= v0 && kr < v1) continue;
                         *reinterpret_cast<uint4*>(vt + (i >> 3) / AT_KT * Cfg::TKB_BYTES + kr * 128 + (i & 7) * 16) =
@@ -421,15 +434,15 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                     }
                 }
                 fence_proxy_async_smem();
-                mbar_arrive(&p_full[b]);
+                mbar_arrive(&bb.p_full[pb]);
                 ++tcount;
             }
             if (!ok) break;
             // ---- epilogue of the item
-            ok = mbar_wait(&o_full[ob], (icount >> 1) & 1, err);
+            ok = mbar_wait(&bb.o_full, icount & 1, err);
             if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
             tc_fence_after();
-            const bool real = row >= 0 && row < a.R;   // other MMA rows are zero padding
+            const bool real = row >= 0 && row < a.R;   // other MMA rows are padding
             const int64_t NQ = (int64_t)a.N * a.B * a.Hq;
             const int64_t qrow = real ? (int64_t)(x.n * a.B + row / a.G) * a.Hq + x.g * a.G + row % a.G : 0;
             const float inv = 1.f / l_run;
@@ -437,7 +450,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
             for (int c = 0; c < HD && !pad; c += 32) {
                 float o[32];
                 __syncwarp();
-                tmem_ld32(tmem_base + lane_off + Cfg::O_COL + ob * HD + c, o);
+                tmem_ld32(tmem_base + lane_off + Cfg::O_COL + c, o);
                 if (!real) continue;
                 if (x.direct) {
                     uint4* dst = reinterpret_cast<uint4*>(a.O + qrow * HD + c);
@@ -457,8 +470,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
             }
             __syncwarp();
             tc_fence_before();
-            mbar_arrive(&o_empty[ob]);
-            if (real && !x.direct) a.lse[(int64_t)x.s * NQ + qrow] = m_run + log2f(l_run);
+            mbar_arrive(&bb.o_empty);
+            if (real && !pad && !x.direct) a.lse[(int64_t)x.s * NQ + qrow] = m_run + log2f(l_run);
             ++icount;
         }
         if (!ok) *abort_flag = 1;
@@ -467,7 +480,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+        tmem_dealloc(*tmem_holder, Cfg::TMEM_COLS);
     }
 }
 
@@ -611,7 +624,6 @@ dfl_status attn_tc(const void* Q, const void* Kc, const void* Vc, const void* Kb
     const bool ragged = ctx_len != nullptr;
     AtArgs a{};
     a.N = N; a.B = B; a.Hq = Hq; a.Hkv = Hkv; a.G = Hq / Hkv; a.R = B * a.G;
-    a.rb = a.R <= 64 ? 64 : 0;
     a.C = C; a.C_stride = ragged ? C_stride : C; a.ctx_len = ctx_len;
     a.kps = attn_tc_kps(N, C, B, Hkv, ragged);
     a.S = (C + B + a.kps - 1) / a.kps;
@@ -643,16 +655,17 @@ dfl_status attn_tc(const void* Q, const void* Kc, const void* Vc, const void* Kb
         if (cudaMemsetAsync(a.counter, 0, sizeof(int), st) != cudaSuccess) return DFL_ERR_CUDA;
         const int grid = std::min(ctx->sm_count, a.items);
         const DevErr err = dev_err(ctx);
-        auto run = [&](auto kern, int smem, int slot) -> dfl_status {
+        auto run = [&](auto kern, int smem, int threads, int slot) -> dfl_status {
             if (!ctx->attn_attr_set[slot]) {
                 if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
                     return DFL_ERR_CUDA;
                 ctx->attn_attr_set[slot] = true;
             }
-            kern<<<grid, AT_THREADS, smem, st>>>(mq, mkc, mvc, mkb, mvb, a, err);
+            kern<<<grid, threads, smem, st>>>(mq, mkc, mvc, mkb, mvb, a, err);
             return last_launch();
         };
-        rc = hd == 128 ? run(attn_tc_kernel<128>, AtCfg<128>::SMEM, 1) : run(attn_tc_kernel<64>, AtCfg<64>::SMEM, 0);
+        rc = hd == 128 ? run(attn_tc_kernel<128>, AtCfg<128>::SMEM, AtCfg<128>::THREADS, 1)
+                       : run(attn_tc_kernel<64>, AtCfg<64>::SMEM, AtCfg<64>::THREADS, 0);
     }
     if (rc != DFL_OK || a.S == 1) return rc;
     ProfScope ps("attn_combine", st);
