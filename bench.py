@@ -114,7 +114,7 @@ def source_hash(files):
 KERNEL_SOURCES = {
     "gemm_ctx_kv": ["gemm_tc.cuh", "gemm_tc.cu"], "gemm_block_qkv": ["gemm_tc.cuh", "gemm_tc.cu"],
     "gemm_o_proj": ["gemm_tc.cuh", "gemm_tc.cu"], "gemm_lm_head": ["gemm_tc.cuh", "gemm_tc.cu"],
-    "mix_rmsnorm_bf16": ["mix_rmsnorm.cu"], "attn_bf16": ["block_attn.cu"],
+    "mix_rmsnorm_bf16": ["mix_rmsnorm.cu"], "attn_bf16": ["block_attn.cu"], "attn_tc": ["block_attn_tc.cu"],
     "verifier_row_stats": ["self_select.cu"],
 }
 

@@ -119,21 +119,28 @@ __device__ __forceinline__ void epi_store(const GemmShape& sh, const GemmEpi& ep
     const int hd = ep.hd;
     const int half = hd >> 1;
     const int pos = !ok ? 0 : (ep.row_pos ? ep.row_pos[row] : ep.pos_off + row % ep.rows_per_seq);
-    const float2* cs = reinterpret_cast<const float2*>(ep.rope) + (int64_t)pos * half;
+    const float4* cs = reinterpret_cast<const float4*>(ep.rope + (int64_t)pos * hd);   // (cos, sin) pairs
+    // One chunk of 32 rotation pairs at a time: its cos/sin (256 contiguous
+    // bytes of the thread's position) are loaded once, 16 bytes per load, and
+    // serve every head of the tile.
     #pragma unroll 1
-    for (int h0 = 0; h0 < BN; h0 += hd) {
+    for (int c = 0; c < half; c += 32) {
+        float4 t[16];
+        #pragma unroll
+        for (int j = 0; j < 16; ++j) t[j] = ok ? __ldg(cs + c / 2 + j) : make_float4(1.f, 0.f, 1.f, 0.f);
         #pragma unroll 1
-        for (int c = 0; c < half; c += 32) {
+        for (int h0 = 0; h0 < BN; h0 += hd) {
             float x[32], y[32];
             tmem_ld32(tbase + h0 + c, x);
             tmem_ld32(tbase + h0 + c + half, y);
             if (ok) {
                 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const float2 t = __ldg(cs + c + j);
-                    const float a = x[j], b = y[j];
-                    x[j] = a * t.x - b * t.y;
-                    y[j] = b * t.x + a * t.y;
+                for (int j = 0; j < 16; ++j) {
+                    const float a0 = x[2 * j], b0 = y[2 * j], a1 = x[2 * j + 1], b1 = y[2 * j + 1];
+                    x[2 * j] = a0 * t[j].x - b0 * t[j].y;
+                    y[2 * j] = b0 * t[j].x + a0 * t[j].y;
+                    x[2 * j + 1] = a1 * t[j].z - b1 * t[j].w;
+                    y[2 * j + 1] = b1 * t[j].z + a1 * t[j].w;
                 }
                 store_bf16x32(out + h0 + c, x);
                 store_bf16x32(out + h0 + c + half, y);
@@ -148,17 +155,28 @@ __device__ __forceinline__ void epi_resid(const GemmShape& sh, const GemmEpi& ep
     const bool ok = row < sh.M;
     float* out = ep.resid + (int64_t)(ok ? row : 0) * ep.ld_resid + n0;
     #pragma unroll 1
-    for (int c = 0; c < BN / 32; ++c) {
-        float v[32];
+    for (int c = 0; c < BN / 32; c += 2) {
+        const bool in0 = ok && n0 + c * 32 < sh.N, in1 = ok && n0 + c * 32 + 32 < sh.N;
+        float4* p = reinterpret_cast<float4*>(out + c * 32);
+        float4 r[16];
+        #pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            r[q] = in0 ? p[q] : make_float4(0.f, 0.f, 0.f, 0.f);
+            r[8 + q] = in1 ? p[8 + q] : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        float v[32], w[32];
         tmem_ld32(tbase + c * 32, v);
-        if (ok && n0 + c * 32 < sh.N) {
-            float4* p = reinterpret_cast<float4*>(out + c * 32);
-            #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                float4 o = p[q];
-                o.x += v[4 * q + 0]; o.y += v[4 * q + 1]; o.z += v[4 * q + 2]; o.w += v[4 * q + 3];
-                p[q] = o;
-            }
+        tmem_ld32(tbase + c * 32 + 32, w);
+        #pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            r[q].x += v[4 * q + 0]; r[q].y += v[4 * q + 1]; r[q].z += v[4 * q + 2]; r[q].w += v[4 * q + 3];
+            r[8 + q].x += w[4 * q + 0]; r[8 + q].y += w[4 * q + 1];
+            r[8 + q].z += w[4 * q + 2]; r[8 + q].w += w[4 * q + 3];
+        }
+        #pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            if (in0) p[q] = r[q];
+            if (in1) p[8 + q] = r[8 + q];
         }
     }
 }
