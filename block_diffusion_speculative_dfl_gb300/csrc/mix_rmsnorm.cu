@@ -6,15 +6,20 @@
 // x = sum_i softmax(mix_l)_i H_i[r].  All D draft layers come from one read of
 // H, so the stack is streamed from HBM once per draft step.
 //
-// bf16 kernel: per row, TMA bulk copies stage the L slices H_i[r] in shared
-// memory (two rows in flight when they fit), and the D normalised rows are
-// staged in shared memory and written back with one bulk copy each.  The L -> D mixing is a tiny matrix product per
-// group of positions, run on the tensor cores with mma.sync m16n8k16: A holds
-// the mixing weights (rows 0..7 the bf16-rounded weight of draft layer
-// 0..7, rows 8..15 the bf16 remainder, so hi + lo carries the fp32 weight
-// to ~2^-16), B holds the bf16 hidden states (exact), accumulation is fp32.
-// The products of bf16 values are exact in fp32, so the result equals the
-// fp32 mixture up to accumulation rounding.
+// bf16 kernel: a persistent CTA per SM streams rows through a ring of up to
+// four shared-memory stages (one TMA bulk copy per target layer slice), and
+// two teams of 16 warps work on alternate rows, so one team's arithmetic
+// overlaps the other's waits.  Per row each warp mixes its span of positions
+// twice: once for the sum of squares, then (after the team's barrier) with
+// the weights scaled by the row's rsqrt factor, writing the bf16 result over
+// its consumed input in place and copying it out with 16-byte stores.  The
+// L -> D mixing is a tiny matrix product per group of 16 positions, run on
+// the tensor cores with mma.sync m16n8k16: A holds the mixing weights (rows
+// 0..7 the bf16-rounded weight of draft layer 0..7, rows 8..15 the bf16
+// remainder, so hi + lo carries the fp32 weight to ~2^-16), B holds the bf16
+// hidden states (exact), accumulation is fp32.  The products of bf16 values
+// are exact in fp32, so the result equals the fp32 mixture up to
+// accumulation rounding.
 //
 // fp32 kernel: plain FFMA mixture, one CTA per row.
 #include "internal.h"
@@ -23,11 +28,14 @@ namespace dfl {
 
 namespace {
 
-constexpr int MIX_WARPS = 16;
-constexpr int MIX_THREADS = MIX_WARPS * 32;
-constexpr int MIX_MAXG = 20;            // 16-position groups per warp -> d <= 5120
-constexpr int MIX_GCOLS = 4 * MIX_MAXG;  // TMEM columns of gains per thread
-constexpr int MIX_TMEM_COLS = 512;       // 4 column blocks of MIX_GCOLS, rounded to a power of two
+constexpr int MIX_TEAMS = 2;               // teams of warps working on alternate rows
+constexpr int MIX_TEAM_WARPS = 16;
+constexpr int MIX_THREADS = MIX_TEAMS * MIX_TEAM_WARPS * 32;
+constexpr int MIX_MAXG = 20;               // 16-position groups per warp -> d <= 5120
+constexpr int MIX_GCOLS = 4 * MIX_MAXG;    // TMEM columns of gains per thread
+constexpr int MIX_TMEM_COLS = 512;         // 4 column blocks of MIX_GCOLS, rounded to a power of two
+constexpr int MIX_MAXSTAGE = 4;            // rows staged at most
+constexpr int MIX_ZERO_BYTES = 128 + MIX_MAXG * 32;   // zero rows read in place of target layers >= L
 
 __device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
                                               uint32_t& r3) {
@@ -60,6 +68,21 @@ __device__ __forceinline__ void split_bf16(float a, uint16_t& hi, uint16_t& lo) 
     lo = *reinterpret_cast<const uint16_t*>(&l);
 }
 
+// Barrier over the `count` threads of named barrier `id` that also returns
+// whether `pred` holds in every one of them.
+__device__ __forceinline__ bool team_sync_and(int id, int count, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 q, %1, 0;\n\t"
+        "barrier.cta.red.and.pred p, %2, %3, q;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r) : "r"((uint32_t)pred), "r"(id), "r"(count) : "memory");
+    return r != 0;
+}
+
+__device__ __forceinline__ void team_sync(int id, int count) {
+    asm volatile("barrier.cta.sync %0, %1;" :: "r"(id), "r"(count) : "memory");
+}
+
 struct MixArgs {
     const __nv_bfloat16* H;
     int64_t layer_stride;
@@ -74,205 +97,268 @@ struct MixArgs {
     int64_t xc_stride;
 };
 
-// Shared-memory plan of the bf16 kernel: `nstage` input stages of L padded
-// slabs, one output stage of D padded slabs, the zero row, the reduction
-// array and the barriers.  Slabs are padded by 16 bytes so that the rows of
-// one ldmatrix (8 layers) and the bf16x2 writes of one warp (8 draft layers)
-// fall on distinct banks.
+// Shared-memory plan of the bf16 kernel: `nstage` row stages of max(L, D)
+// padded slabs (the L input slabs, overwritten in place by the D output
+// slabs), the zero row, the per-team reduction arrays and the barriers.
+// Slabs are padded by 16 bytes so that the rows of one ldmatrix (8 layers)
+// and the bf16x2 writes of one warp (8 draft layers) fall on distinct banks.
 struct MixSmem {
-    int slab, stage_bytes, out_bytes, nstage, total;
+    int slab, stage_bytes, nstage, total;
 };
 
 __host__ __device__ inline MixSmem mix_smem_plan(int L, int D, int d, int nstage) {
     MixSmem m;
     m.slab = d * 2 + 16;
-    m.stage_bytes = ((L * m.slab + 127) / 128) * 128;
-    m.out_bytes = ((D * m.slab + 127) / 128) * 128;
+    m.stage_bytes = (((L > D ? L : D) * m.slab + 127) / 128) * 128;
     m.nstage = nstage;
-    m.total = 128 + nstage * m.stage_bytes + m.out_bytes + 128 + MIX_WARPS * 8 * 4 + 2 * 8 + 16;
+    m.total = 128 + nstage * m.stage_bytes + MIX_ZERO_BYTES + MIX_TEAMS * MIX_TEAM_WARPS * 8 * 4 +
+              MIX_MAXSTAGE * 2 * 8 + 16;
     return m;
 }
 
-__device__ __forceinline__ void bulk_s2g(void* dst, const void* src, uint32_t bytes) {
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
-                 :: "l"(dst), "r"(smem_u32(src)), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
+// One persistent CTA per SM, two teams of 16 warps.  The CTA's rows are
+// numbered k = 0, 1, ...; row k sits in stage k % nstage and is processed by
+// team k % 2, so one team's arithmetic overlaps the other's waits.  Per row,
+// each warp owns a contiguous span of at most GPW 16-position groups:
+//   pass 1  mix its span on the tensor cores, sum of squares per draft layer;
+//   team barrier (partial sums of every warp);
+//   pass 2  mix again with the weights scaled by rsqrt(mean + eps) (the
+//           product comes out normalised), apply the gain and write the bf16
+//           result over the consumed input slabs of its span (draft layer l
+//           into slab l), then copy its span of the D output rows to global
+//           memory with 16-byte stores;
+//   team barrier, after which the stage is refilled with row k + nstage.
+// Recomputing the mixture (pass 2) costs a few tensor-core instructions and
+// keeps nothing live across the barrier, which leaves room for two teams.
+// GPW is a compile-time bound so that both passes unroll completely.
+template <int GPW>
 __global__ void __launch_bounds__(MIX_THREADS, 1) mix_rmsnorm_bf16_kernel(const MixArgs a, const int nstage,
                                                                          const DevErr err) {
+    static_assert(GPW % 4 == 0 && GPW <= MIX_MAXG, "group bound");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
     const MixSmem P = mix_smem_plan(a.L, a.D, a.d, nstage);
-    uint8_t* in0 = smem;                                   // stage s at in0 + s * stage_bytes
-    uint8_t* out = smem + nstage * P.stage_bytes;          // D padded output slabs
-    uint8_t* zero_row = out + P.out_bytes;                 // 16 zero bytes
-    float* red = reinterpret_cast<float*>(zero_row + 128); // [MIX_WARPS][8]
-    uint64_t* full = reinterpret_cast<uint64_t*>(red + MIX_WARPS * 8);
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(full + 2);
+    uint8_t* in0 = smem;                                       // stage s at in0 + s * stage_bytes
+    uint8_t* zero_rows = smem + nstage * P.stage_bytes;        // MIX_ZERO_BYTES of zeros
+    float* red = reinterpret_cast<float*>(zero_rows + MIX_ZERO_BYTES);   // [team][warp][8]
+    uint64_t* full = reinterpret_cast<uint64_t*>(red + MIX_TEAMS * MIX_TEAM_WARPS * 8);
+    int* fills = reinterpret_cast<int*>(full + MIX_MAXSTAGE);   // copies issued per stage
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(fills + 2 * MIX_MAXSTAGE);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int team = warp / MIX_TEAM_WARPS, tw = warp % MIX_TEAM_WARPS;
+    const int bar_id = 1 + team, bar_n = MIX_TEAM_WARPS * 32;
     const uint32_t tx_bytes = (uint32_t)a.L * (uint32_t)a.d * 2u;
     const uint32_t row_bytes = (uint32_t)a.d * 2u;
 
     if (tid == 0) {
-        for (int q = 0; q < nstage; ++q) mbar_init(&full[q], 1);
+        for (int q = 0; q < nstage; ++q) { mbar_init(&full[q], 1); fills[q] = 0; }
         fence_barrier_init();
     }
-    if (tid < 4) reinterpret_cast<uint32_t*>(zero_row)[tid] = 0u;
-    // The RMSNorm gains do not change from row to row: each thread keeps the
-    // 4 * MIX_MAXG gains of the positions it writes in its own TMEM lane
-    // (quadrant warp % 4, column block warp / 4) instead of re-reading them
-    // from L2 for every row.
+    for (int i = tid; i < MIX_ZERO_BYTES / 4; i += MIX_THREADS) reinterpret_cast<uint32_t*>(zero_rows)[i] = 0u;
+    // The RMSNorm gains do not change from row to row: warp tw of either team
+    // finds the 4 * GPW gains of the positions it writes in TMEM lane quadrant
+    // tw % 4, column block tw / 4 (written once, by team 0).
     if (warp == 0) { tmem_alloc(tmem_holder, MIX_TMEM_COLS); tmem_relinquish(); }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tgain = *tmem_holder + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)((warp >> 2) * MIX_GCOLS);
+    const uint32_t tgain = *tmem_holder + ((uint32_t)(32 * (tw & 3)) << 16) + (uint32_t)((tw >> 2) * MIX_GCOLS);
 
-    uint32_t fills0 = 0u, fills1 = 0u;   // copies issued per stage (thread 0 only)
-    auto issue = [&](int64_t row, int s) {
-        if (s) ++fills1; else ++fills0;
+    // Row k of this CTA.
+    auto row_of = [&](int k) -> int64_t { return blockIdx.x + (int64_t)k * gridDim.x; };
+    auto issue = [&](int k) {   // one thread: stage row k's L slices
+        const int s = k % nstage;
+        const int64_t row = row_of(k);
         uint8_t* dst = in0 + s * P.stage_bytes;
+        ++fills[s];
         mbar_arrive_expect_tx(&full[s], tx_bytes);
         for (int i = 0; i < a.L; ++i)
             bulk_g2s(dst + i * P.slab, a.H + i * a.layer_stride + row * a.d, row_bytes, &full[s]);
     };
     if (tid == 0)
         for (int q = 0; q < nstage; ++q)
-            if (blockIdx.x + (int64_t)q * gridDim.x < a.rows) issue(blockIdx.x + (int64_t)q * gridDim.x, q);
+            if (row_of(q) < a.rows) issue(q);
 
-    // A fragments: mixing weights of draft layer l = lane/4 (hi rows 0..7, lo rows 8..15).
-    uint32_t afrag[4];
+    // A fragments: mixing weights of draft layer l = lane/4 (hi rows 0..7, lo
+    // rows 8..15) for target layers k0, k0+1, k0+8, k0+9.
+    float wts[4];
     {
         const int l = lane >> 2;
         const int k0 = 2 * (lane & 3);
-        uint16_t hi[4], lo[4];
         const int ks[4] = {k0, k0 + 1, k0 + 8, k0 + 9};
         #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const float w = (l < a.D && ks[j] < a.L) ? mix_weight(a.mix_logits, a.L, l, ks[j]) : 0.f;
-            split_bf16(w, hi[j], lo[j]);
-        }
-        afrag[0] = (uint32_t)hi[0] | ((uint32_t)hi[1] << 16);   // row l,   k0..k0+1
-        afrag[1] = (uint32_t)lo[0] | ((uint32_t)lo[1] << 16);   // row l+8, k0..k0+1
-        afrag[2] = (uint32_t)hi[2] | ((uint32_t)hi[3] << 16);   // row l,   k0+8..k0+9
-        afrag[3] = (uint32_t)lo[2] | ((uint32_t)lo[3] << 16);   // row l+8, k0+8..k0+9
+        for (int j = 0; j < 4; ++j) wts[j] = (l < a.D && ks[j] < a.L) ? mix_weight(a.mix_logits, a.L, l, ks[j]) : 0.f;
     }
+    auto make_frag = [&](float scale, uint32_t (&f)[4]) {
+        uint16_t hi[4], lo[4];
+        #pragma unroll
+        for (int j = 0; j < 4; ++j) split_bf16(wts[j] * scale, hi[j], lo[j]);
+        f[0] = (uint32_t)hi[0] | ((uint32_t)hi[1] << 16);   // row l,   k0..k0+1
+        f[1] = (uint32_t)lo[0] | ((uint32_t)lo[1] << 16);   // row l+8, k0..k0+1
+        f[2] = (uint32_t)hi[2] | ((uint32_t)hi[3] << 16);   // row l,   k0+8..k0+9
+        f[3] = (uint32_t)lo[2] | ((uint32_t)lo[3] << 16);   // row l+8, k0+8..k0+9
+    };
+    uint32_t afrag[4];
+    make_frag(1.f, afrag);
 
-    // ldmatrix row owned by this thread: matrix lane/8 -> (k half, position half)
+    const int groups = a.d / 16;
+    // Warp tw owns the contiguous groups [g0, g0 + ng) (16 positions each).
+    const int gpw = (groups + MIX_TEAM_WARPS - 1) / MIX_TEAM_WARPS;
+    const int g0 = min(tw * gpw, groups);
+    const int ng = min(gpw, groups - g0);
+    const int l_out = lane >> 2;
+    const int n = 2 * (lane & 3);
+    const bool writes = l_out < a.D;
+    // ldmatrix row of this thread (matrix lane/8 -> k half, position half): target
+    // layer my_k of the stage, or the zero rows, at byte offset j * 32 for group g0 + j.
     const int my_k = ((lane >> 3) & 1) * 8 + (lane & 7);
     const int my_off = (lane >> 4) * 8;
-    const int groups = a.d / 16;
-    const int l_out = lane >> 2;
-    const bool writes = l_out < a.D;
-    const float* gain_l = a.gain + (int64_t)(writes ? l_out : 0) * a.d;
-    uint8_t* out_l = out + l_out * P.slab;
-    const uint32_t zero_addr = smem_u32(zero_row);
-    {
-        const int n = 2 * (lane & 3);
-        #pragma unroll
-        for (int c = 0; c < MIX_MAXG / 4; ++c) {
+    const bool k_real = my_k < a.L;
+    const uint32_t zero_addr = smem_u32(zero_rows);
+    const uint32_t ld_rel = (uint32_t)(my_k * P.slab + (g0 * 16 + my_off) * 2);
+    // write position of this thread in its span: draft layer l_out, positions n, n+1 (+8) of each group
+    const uint32_t st_rel = (uint32_t)(l_out * P.slab + (g0 * 16 + n) * 2);
+    if (MIX_TEAMS > 1 && team == 0) {
+        const float* gain_l = a.gain + (int64_t)(writes ? l_out : 0) * a.d;
+        #pragma unroll 1
+        for (int c = 0; c < GPW / 4; ++c) {
             uint32_t gv[16];
             #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                const int g = warp + (4 * c + q) * MIX_WARPS;
-                float2 g0 = make_float2(0.f, 0.f), g1 = make_float2(0.f, 0.f);
-                if (writes && g < groups) {
-                    g0 = __ldg(reinterpret_cast<const float2*>(gain_l + g * 16 + n));
-                    g1 = __ldg(reinterpret_cast<const float2*>(gain_l + g * 16 + n + 8));
+                const int j = 4 * c + q;
+                float2 ga = make_float2(0.f, 0.f), gb = make_float2(0.f, 0.f);
+                if (writes && j < ng) {
+                    ga = __ldg(reinterpret_cast<const float2*>(gain_l + (g0 + j) * 16 + n));
+                    gb = __ldg(reinterpret_cast<const float2*>(gain_l + (g0 + j) * 16 + n + 8));
                 }
-                gv[4 * q + 0] = __float_as_uint(g0.x);
-                gv[4 * q + 1] = __float_as_uint(g0.y);
-                gv[4 * q + 2] = __float_as_uint(g1.x);
-                gv[4 * q + 3] = __float_as_uint(g1.y);
+                gv[4 * q + 0] = __float_as_uint(ga.x);
+                gv[4 * q + 1] = __float_as_uint(ga.y);
+                gv[4 * q + 2] = __float_as_uint(gb.x);
+                gv[4 * q + 3] = __float_as_uint(gb.y);
             }
             tmem_st16(tgain + 16 * c, gv);
         }
         tmem_st_wait();
     }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
 
-    int it = 0;
-    for (int64_t row = blockIdx.x; row < a.rows; row += gridDim.x, ++it) {
-        const int s = (nstage == 2) ? (it & 1) : 0;
-        const uint32_t par = (nstage == 2) ? ((it >> 1) & 1) : (it & 1);
-        const bool ok = mbar_wait(&full[s], par, err);
-        if (!__syncthreads_and(ok)) {
-            // A bounded wait ran out (error recorded): let issued copies land, then leave.
-            if (tid == 0) {
-                if (fills0) mbar_wait(&full[0], (fills0 - 1) & 1, err);
-                if (fills1) mbar_wait(&full[1], (fills1 - 1) & 1, err);
-            }
-            break;
-        }
-        const uint32_t stage_addr = smem_u32(in0) + (uint32_t)(s * P.stage_bytes);
-        const uint32_t base = my_k < a.L ? stage_addr + (uint32_t)(my_k * P.slab) : zero_addr;
-        const uint32_t step = my_k < a.L ? 2u : 0u;
-        float v[MIX_MAXG][4];
+    // mixture of group j of the span: v = (pos n, n+1, n+8, n+9) of draft layer l_out
+    auto mix_group = [&](const uint32_t (&af)[4], uint32_t addr, float (&v)[4]) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_trans(addr, b0, b1, b2, b3);
+        float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+        mma_16816(c0, af, b0, b1);
+        mma_16816(c1, af, b2, b3);
+        v[0] = c0[0] + c0[2];   // hi + lo weight rows
+        v[1] = c0[1] + c0[3];
+        v[2] = c1[0] + c1[2];
+        v[3] = c1[1] + c1[3];
+    };
+
+    // With a single stage (very wide rows) only team 0 works.
+    const int tstep = nstage >= 2 ? MIX_TEAMS : 1;
+    const bool leader = tw == 0 && lane == 0;
+    const bool full_span = ng == GPW;   // warp-uniform; false only for the last warps of ragged widths
+    bool ok = true;
+    int s = team % nstage;
+    uint32_t par = (uint32_t)(team / nstage) & 1u;
+    for (int k = team; team < tstep && row_of(k) < a.rows; k += tstep) {
+        const int64_t row = row_of(k);
+        ok = mbar_wait(&full[s], par, err);
+        uint8_t* stage = in0 + s * P.stage_bytes;
+        const uint32_t stage_addr = smem_u32(stage);
+        // ldmatrix address of group 0 of the span; group j is 32 bytes further.
+        // A zero row sits in the same bank slot (address mod 128) as the real
+        // row it replaces, so the 8 rows of every 8x8 matrix hit distinct banks.
+        const uint32_t ld0 = k_real ? stage_addr + ld_rel : zero_addr + (ld_rel & 127u);
+        // ---- pass 1: sum of squares of this warp's span, per draft layer
         float ss = 0.f;
-        #pragma unroll
-        for (int j = 0; j < MIX_MAXG; ++j) {
-            const int g = warp + j * MIX_WARPS;
-            v[j][0] = v[j][1] = v[j][2] = v[j][3] = 0.f;
-            if (g < groups) {
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4_trans(base + step * (uint32_t)(g * 16 + my_off), b0, b1, b2, b3);
-                float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
-                mma_16816(c0, afrag, b0, b1);
-                mma_16816(c1, afrag, b2, b3);
-                v[j][0] = c0[0] + c0[2];
-                v[j][1] = c0[1] + c0[3];
-                v[j][2] = c1[0] + c1[2];
-                v[j][3] = c1[1] + c1[3];
-                ss += v[j][0] * v[j][0] + v[j][1] * v[j][1] + v[j][2] * v[j][2] + v[j][3] * v[j][3];
+        if (ok) {
+            if (full_span) {
+                #pragma unroll 1
+                for (int c = 0; c < GPW / 4; ++c) {
+                    const uint32_t ldc = ld0 + 128u * c;
+                    #pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        float v[4];
+                        mix_group(afrag, ldc + 32u * q, v);
+                        ss += v[0] * v[0] + v[1] * v[1] + v[2] * v[2] + v[3] * v[3];
+                    }
+                }
+            } else {
+                #pragma unroll 1
+                for (int j = 0; j < ng; ++j) {
+                    float v[4];
+                    mix_group(afrag, ld0 + 32u * j, v);
+                    ss += v[0] * v[0] + v[1] * v[1] + v[2] * v[2] + v[3] * v[3];
+                }
             }
         }
         ss += __shfl_xor_sync(0xFFFFFFFFu, ss, 1);
         ss += __shfl_xor_sync(0xFFFFFFFFu, ss, 2);
-        if ((lane & 3) == 0) red[warp * 8 + l_out] = ss;
-        if (tid == 0) bulk_wait_read0();   // previous row's output stage has been read out
-        __syncthreads();                    // stage s consumed; partial sums visible; output stage free
-        if (tid == 0 && row + (int64_t)nstage * gridDim.x < a.rows) issue(row + (int64_t)nstage * gridDim.x, s);
+        if ((lane & 3) == 0) red[(team * MIX_TEAM_WARPS + tw) * 8 + l_out] = ss;
+        if (!team_sync_and(bar_id, bar_n, ok)) break;   // a bounded wait ran out (error recorded)
         float tot = 0.f;
         #pragma unroll
-        for (int w = 0; w < MIX_WARPS; ++w) tot += red[w * 8 + l_out];
+        for (int w = 0; w < MIX_TEAM_WARPS; ++w) tot += red[(team * MIX_TEAM_WARPS + w) * 8 + l_out];
         const float rs = rsqrtf(tot / (float)a.d + a.eps);
-        {
-            const int n = 2 * (lane & 3);
+        uint32_t afrag_n[4];
+        make_frag(rs, afrag_n);
+        // ---- pass 2: normalised bf16 output over the consumed input of the span.
+        // The collective mma.sync consumes every lane's ldmatrix result, so a
+        // group's input has been read in full before any lane overwrites it.
+        #pragma unroll 1
+        for (int c = 0; 4 * c < ng; ++c) {
+            float gv[16];
+            tmem_ld16(tgain + 16 * c, gv);
+            const uint32_t ldc = ld0 + 128u * c;
+            uint8_t* outc = stage + st_rel + 128 * c;
             #pragma unroll
-            for (int c = 0; c < MIX_MAXG / 4; ++c) {
-                if (warp + 4 * c * MIX_WARPS >= groups) break;   // warp-uniform
-                float gv[16];
-                tmem_ld16(tgain + 16 * c, gv);
-                if (writes) {
-                    #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const int j = 4 * c + q;
-                        const int g = warp + j * MIX_WARPS;
-                        if (g < groups) {
-                            const int p = g * 16 + n;
-                            *reinterpret_cast<uint32_t*>(out_l + p * 2) =
-                                pack_bf16(v[j][0] * rs * gv[4 * q], v[j][1] * rs * gv[4 * q + 1]);
-                            *reinterpret_cast<uint32_t*>(out_l + (p + 8) * 2) =
-                                pack_bf16(v[j][2] * rs * gv[4 * q + 2], v[j][3] * rs * gv[4 * q + 3]);
-                        }
+            for (int q = 0; q < 4; ++q) {
+                if (full_span || 4 * c + q < ng) {
+                    float v[4];
+                    mix_group(afrag_n, ldc + 32u * q, v);
+                    if (writes) {
+                        *reinterpret_cast<uint32_t*>(outc + 32 * q) = pack_bf16(v[0] * gv[4 * q], v[1] * gv[4 * q + 1]);
+                        *reinterpret_cast<uint32_t*>(outc + 32 * q + 16) =
+                            pack_bf16(v[2] * gv[4 * q + 2], v[3] * gv[4 * q + 3]);
                     }
                 }
             }
         }
-        fence_proxy_async_smem();   // make the output stage visible to the bulk copies
-        __syncthreads();
-        if (tid == 0) {
-            for (int l = 0; l < a.D; ++l)
-                bulk_s2g(a.Xc + l * a.xc_stride + row * a.d, out + l * P.slab, row_bytes);
-            bulk_commit();
+        // Copy the span's D output rows out: 16 bytes per lane, ng * 32 contiguous bytes per row.
+        __syncwarp();
+        {
+            const uint8_t* src = stage + g0 * 32;
+            __nv_bfloat16* dst = a.Xc + row * a.d + g0 * 16;
+            for (int l = 0; l < a.D; ++l) {
+                for (int c = lane; c < 2 * ng; c += 32)
+                    *reinterpret_cast<uint4*>(dst + c * 8) = *reinterpret_cast<const uint4*>(src + c * 16);
+                src += P.slab;
+                dst += a.xc_stride;
+            }
         }
+        // The stage's next contents come from TMA (the async proxy): order this
+        // warp's shared-memory accesses before that write, then refill once
+        // every warp is done with the stage.
+        fence_proxy_async_smem();
+        team_sync(bar_id, bar_n);
+        if (leader && row_of(k + nstage) < a.rows) issue(k + nstage);
+        s += tstep;
+        if (s >= nstage) { s -= nstage; par ^= 1u; }
     }
-    if (tid == 0) bulk_wait0();
     tc_fence_before();
     __syncthreads();
+    if (tid == 0) {
+        // After a wait ran out: let every issued copy land before the CTA exits
+        // (the latest fill of stage q completes phase fills[q] - 1).
+        for (int q = 0; q < nstage; ++q)
+            if (fills[q]) mbar_wait(&full[q], (uint32_t)(fills[q] - 1) & 1u, err);
+    }
     if (warp == 0) {
         tc_fence_after();
         tmem_dealloc(*tmem_holder, MIX_TMEM_COLS);
@@ -341,22 +427,30 @@ extern "C" dfl_status dfl_layer_mix_rmsnorm(const void* H, int64_t layer_stride,
     if (!ctx) return DFL_ERR_NO_DEVICE;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (dt == DFL_BF16) {
-        if (d % 16 != 0 || d > 16 * MIX_WARPS * MIX_MAXG) return DFL_ERR_UNSUPPORTED_SHAPE;
-        int nstage = 2;
-        if (mix_smem_plan(L, D, d, 2).total > 227 * 1024) nstage = 1;
+        if (d % 16 != 0 || d > 16 * MIX_TEAM_WARPS * MIX_MAXG) return DFL_ERR_UNSUPPORTED_SHAPE;
+        int nstage = MIX_MAXSTAGE;   // as many rows in flight as shared memory holds
+        while (nstage > 1 && mix_smem_plan(L, D, d, nstage).total > 227 * 1024) --nstage;
         const int smem = mix_smem_plan(L, D, d, nstage).total;
         if (smem > 227 * 1024) return DFL_ERR_UNSUPPORTED_SHAPE;
+        const int gpw = (d / 16 + MIX_TEAM_WARPS - 1) / MIX_TEAM_WARPS;
+        const int gi = gpw <= 4 ? 0 : gpw <= 8 ? 1 : gpw <= 12 ? 2 : gpw <= 16 ? 3 : 4;
+        using KernFn = void (*)(const MixArgs, const int, const DevErr);
+        static const KernFn kerns[5] = {mix_rmsnorm_bf16_kernel<4>, mix_rmsnorm_bf16_kernel<8>,
+                                        mix_rmsnorm_bf16_kernel<12>, mix_rmsnorm_bf16_kernel<16>,
+                                        mix_rmsnorm_bf16_kernel<20>};
+        const KernFn kern = kerns[gi];
         if (!ctx->mix_attr_set) {
-            if (cudaFuncSetAttribute(mix_rmsnorm_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     227 * 1024) != cudaSuccess)
-                return DFL_ERR_CUDA;
+            for (int i = 0; i < 5; ++i)
+                if (cudaFuncSetAttribute(kerns[i], cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) !=
+                    cudaSuccess)
+                    return DFL_ERR_CUDA;
             ctx->mix_attr_set = true;
         }
         MixArgs a{static_cast<const __nv_bfloat16*>(H), layer_stride, L, rows, d, D, mix_logits, gain, eps,
                   static_cast<__nv_bfloat16*>(Xc), xc_layer_stride};
         const int64_t grid = rows < ctx->sm_count ? rows : ctx->sm_count;
         ProfScope ps("mix_rmsnorm_bf16", st);
-        mix_rmsnorm_bf16_kernel<<<(unsigned)grid, MIX_THREADS, smem, st>>>(a, nstage, dev_err(ctx));
+        kern<<<(unsigned)grid, MIX_THREADS, smem, st>>>(a, nstage, dev_err(ctx));
         return last_launch();
     }
     const size_t smem = (size_t)(D * L + D * 32 + (size_t)D * d) * sizeof(float);

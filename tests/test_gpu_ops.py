@@ -28,7 +28,13 @@ def _ws(nbytes):
 
 # ------------------------------------------------------------------- mix --
 
-@pytest.mark.parametrize("rows,d,L,D", [(300, 512, 9, 7), (200, 2880, 7, 8), (5, 4096, 9, 1), (149, 256, 3, 2)])
+@pytest.mark.parametrize("rows,d,L,D", [
+    (300, 512, 9, 7), (200, 2880, 7, 8), (5, 4096, 9, 1), (149, 256, 3, 2),
+    (3000, 512, 9, 7),    # ~20 rows per CTA: both teams, the stage ring wraps many times
+    (1000, 2880, 7, 8),   # more draft layers than target layers: an output-only slab per stage
+    (40, 4096, 16, 8),    # one stage fits: a single team
+    (7, 5120, 9, 8),      # the widest rows (20 groups per warp)
+])
 def test_mix_rmsnorm_bf16(rows, d, L, D):
     rng = np.random.default_rng(rows + d)
     H = rng_bf16(rng, (L, rows, d)) * rng.uniform(0.5, 2, (L, 1, 1)).astype(np.float32)
