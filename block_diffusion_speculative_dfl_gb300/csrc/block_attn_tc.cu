@@ -8,8 +8,11 @@
 // to all of that sequence's context keys and all B block keys, no mask:
 //   O = softmax(Q [Kc;Kb]^T / sqrt(hd)) [Vc;Vb].
 //
-// Work item = (split s, sequence n, K/V head g): one range of at most `kps`
-// keys of the sequence's Cn + B keys.  A persistent kernel (one CTA per SM)
+// Work item = (split s, sequence n, K/V head g, head subset h): one range of
+// at most `kps` keys of the sequence's Cn + B keys, for the Gq = G / hs query
+// heads h*Gq .. h*Gq + Gq - 1 of the group (hs = 1 unless B * G exceeds the
+// 128 MMA rows; the subsets of one group are consecutive items, so their K/V
+// tiles are read from HBM once and from L2 by the others).  A persistent kernel (one CTA per SM)
 // takes items from a global counter; empty items (past a shorter sequence's
 // keys) are skipped by the scheduler.  Per CTA:
 //   warp 0  scheduler + TMA producer: the item's Q rows (3-D box: head dim x
@@ -40,12 +43,13 @@ constexpr int AT_IRING = 4;         // scheduled items in flight between the war
 
 struct AtArgs {
     int N, B, Hq, Hkv, G, R;
+    int hs, Gq;               // head subsets per K/V head, query heads per item (R = B * Gq)
     int C;                    // context keys per sequence (the maximum when ctx_len is given)
     int C_stride;             // context rows per sequence in Kc / Vc
     const int32_t* ctx_len;   // nullable [N]
     int kps;                  // keys per item (multiple of 64)
-    int S;                    // items per (sequence, K/V head)
-    int items;                // S * N * Hkv
+    int S;                    // items per (sequence, K/V head, head subset)
+    int items;                // S * N * Hkv * hs
     int* counter;             // zeroed before the launch
     __nv_bfloat16* O;         // [N*B*Hq][hd]
     float* Opart;             // [S][N*B*Hq][hd]
@@ -77,7 +81,7 @@ struct AtCfg {
 
 // One work item, decoded identically by every warp.
 struct AtItem {
-    int n, g, s;
+    int n, g, h, s;
     int Cn;          // context keys of the sequence
     int lo, hi;      // key range [lo, hi) of the Cn + B keys
     int nctx;        // context tiles (64 keys from lo, valid below min(hi, Cn))
@@ -86,9 +90,11 @@ struct AtItem {
 };
 
 __device__ __forceinline__ bool at_decode(const AtArgs& a, int it, AtItem& x) {
-    const int units = a.N * a.Hkv;
+    const int units = a.N * a.Hkv * a.hs;
     x.s = it / units;
-    const int u = it - x.s * units;
+    int u = it - x.s * units;
+    x.h = u % a.hs;
+    u /= a.hs;
     x.n = u / a.Hkv;
     x.g = u - x.n * a.Hkv;
     x.Cn = a.ctx_len ? a.ctx_len[x.n] : a.C;
@@ -208,8 +214,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                 mbar_arrive_expect_tx(&bb.q_full[qb], a.R * HD * 2);
                 #pragma unroll
                 for (int kb = 0; kb < Cfg::KB; ++kb)
-                    tma_load_3d(sQ + qb * Cfg::Q_BYTES + kb * Cfg::QKB_BYTES + rb * 128, &tmQ, kb * 64, x.g * a.G,
-                                x.n * a.B, &bb.q_full[qb]);
+                    tma_load_3d(sQ + qb * Cfg::Q_BYTES + kb * Cfg::QKB_BYTES + rb * 128, &tmQ, kb * 64,
+                                x.g * a.G + x.h * a.Gq, x.n * a.B, &bb.q_full[qb]);
                 const int nt = x.nctx + x.blk;
                 for (int t = 0; t < nt && !aborted; ++t) {
                     const int s = tcount % ST;
@@ -250,64 +256,109 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     } else if (role == 1) {
         if (lane == 0) {
             // ------------------------------------------------------ MMA issuer
+            // Event loop: issue whichever product is ready, S = Q K^T of the
+            // next tile (its K/V landed, an S buffer free) or O += P V of the
+            // oldest tile whose P is written, so that neither waits on the
+            // other's inputs.  Tiles are numbered per pipeline; meta[] keeps,
+            // for tiles whose S is issued and whose P V is not, whether they
+            // open / close their item and the item's number.
             constexpr uint32_t idesc_s = idesc_bf16(AT_M, AT_KT);
             constexpr uint32_t idesc_o = idesc_bf16_bmn(AT_M, HD);
-            int icount = 0, tcount = 0;
+            constexpr int META = 8;
+            static_assert(META >= ST + NSB + 1, "tiles in flight between S and P V");
+            struct TileMeta { int8_t first, last; int icount; };
+            TileMeta meta[META];
+            int tcs = 0, tcp = 0;                 // tiles with S issued, with P V issued
+            int icount = 0, t_in = 0, nt = 0;     // the S side's current item, its next tile, its tiles
+            int qb = 0;
+            uint32_t qaddr = 0;
+            bool have_item = false, q_ready = false, items_done = false;
             bool aborted = false, issued = false;
-            // the P V product of the previous tile waits until its P is ready
-            int pv_t = -1, pv_first = 0, pv_last = 0, pv_oi = 0;
-            auto issue_pv = [&]() -> bool {
-                const int pb = pv_t % NPB;
-                if (*abort_flag || !mbar_wait(&bb.p_full[pb], (pv_t / NPB) & 1, err)) return false;
-                if (pv_first && !mbar_wait(&bb.o_empty, (pv_oi & 1) ^ 1, err)) return false;
-                tc_fence_after();
-                const int s = pv_t % ST;
-                const uint32_t vaddr = smem_u32(sKV + s * 2 * Cfg::T_BYTES + Cfg::T_BYTES);
-                const uint64_t pd = sw128_desc(smem_u32(sP + pb * Cfg::P_BYTES));
-                #pragma unroll
-                for (int j = 0; j < AT_KT / 16; ++j)
-                    mma_bf16(tmem_base + Cfg::O_COL, pd + 2 * j, sw128_desc_mn(vaddr + j * 16 * 128, Cfg::TKB_BYTES, 1024),
-                             idesc_o, (pv_first && j == 0) ? 0 : 1);
-                issued = true;
-                mma_commit(&bb.kv_empty[s]);
-                mma_commit(&bb.p_empty[pb]);
-                if (pv_last) mma_commit(&bb.o_full);
-                pv_t = -1;
-                return true;
-            };
-            while (!aborted) {
-                const int r = icount % AT_IRING;
-                if (*abort_flag || !mbar_wait(&bb.i_full[r], (icount / AT_IRING) & 1, err)) { aborted = true; break; }
-                const int it = bb.i_ring[r];
-                mbar_arrive(&bb.i_empty[r]);
-                if (it < 0) break;
-                AtItem x;
-                at_decode(a, it, x);
-                const int qb = icount % NQB;
-                if (*abort_flag || !mbar_wait(&bb.q_full[qb], (icount / NQB) & 1, err)) { aborted = true; break; }
-                const uint32_t qaddr = smem_u32(sQ + qb * Cfg::Q_BYTES);
-                const int nt = x.nctx + x.blk;
-                for (int t = 0; t < nt; ++t) {
-                    const int s = tcount % ST, b = tcount % NSB;
-                    if (*abort_flag || !mbar_wait(&bb.kv_full[s], (tcount / ST) & 1, err) ||
-                        !mbar_wait(&bb.s_empty[b], ((tcount / NSB) & 1) ^ 1, err)) { aborted = true; break; }
-                    tc_fence_after();
-                    const uint32_t kaddr = smem_u32(sKV + s * 2 * Cfg::T_BYTES);
-                    #pragma unroll
-                    for (int j = 0; j < HD / 16; ++j)
-                        mma_bf16(tmem_base + b * AT_KT, sw128_desc(qaddr + (j >> 2) * Cfg::QKB_BYTES + (j & 3) * 32),
-                                 sw128_desc(kaddr + (j >> 2) * Cfg::TKB_BYTES + (j & 3) * 32), idesc_s, j > 0);
-                    issued = true;
-                    mma_commit(&bb.s_full[b]);
-                    if (t == nt - 1) mma_commit(&bb.q_empty[qb]);
-                    if (pv_t >= 0 && !issue_pv()) { aborted = true; break; }
-                    pv_t = tcount; pv_first = t == 0; pv_last = t == nt - 1; pv_oi = icount;
-                    ++tcount;
+            uint64_t t_idle = globaltimer_ns();
+            while (true) {
+                bool prog = false;
+                // P V of the oldest tile whose S is issued
+                if (tcp < tcs) {
+                    const TileMeta m = meta[tcp % META];
+                    const int pb = tcp % NPB;
+                    if (mbar_test(&bb.p_full[pb], (tcp / NPB) & 1) &&
+                        (!m.first || mbar_test(&bb.o_empty, (m.icount & 1) ^ 1))) {
+                        tc_fence_after();
+                        const int s = tcp % ST;
+                        const uint32_t vaddr = smem_u32(sKV + s * 2 * Cfg::T_BYTES + Cfg::T_BYTES);
+                        const uint64_t pd = sw128_desc(smem_u32(sP + pb * Cfg::P_BYTES));
+                        #pragma unroll
+                        for (int j = 0; j < AT_KT / 16; ++j)
+                            mma_bf16(tmem_base + Cfg::O_COL, pd + 2 * j,
+                                     sw128_desc_mn(vaddr + j * 16 * 128, Cfg::TKB_BYTES, 1024), idesc_o,
+                                     (m.first && j == 0) ? 0 : 1);
+                        issued = true;
+                        mma_commit(&bb.kv_empty[s]);
+                        mma_commit(&bb.p_empty[pb]);
+                        if (m.last) mma_commit(&bb.o_full);
+                        ++tcp;
+                        prog = true;
+                    }
                 }
-                if (aborted) break;
-                ++icount;
+                // the next item of the S side
+                if (!have_item && !items_done) {
+                    const int r = icount % AT_IRING;
+                    if (mbar_test(&bb.i_full[r], (icount / AT_IRING) & 1)) {
+                        const int it = bb.i_ring[r];
+                        mbar_arrive(&bb.i_empty[r]);
+                        if (it < 0) {
+                            items_done = true;
+                        } else {
+                            AtItem x;
+                            at_decode(a, it, x);
+                            nt = x.nctx + x.blk;
+                            t_in = 0;
+                            qb = icount % NQB;
+                            qaddr = smem_u32(sQ + qb * Cfg::Q_BYTES);
+                            have_item = true;
+                            q_ready = false;
+                        }
+                        prog = true;
+                    }
+                }
+                if (have_item && !q_ready && mbar_test(&bb.q_full[qb], (icount / NQB) & 1)) { q_ready = true; prog = true; }
+                // S of the next tile
+                if (have_item && q_ready) {
+                    const int s = tcs % ST, b = tcs % NSB;
+                    if (mbar_test(&bb.kv_full[s], (tcs / ST) & 1) && mbar_test(&bb.s_empty[b], ((tcs / NSB) & 1) ^ 1)) {
+                        tc_fence_after();
+                        const uint32_t kaddr = smem_u32(sKV + s * 2 * Cfg::T_BYTES);
+                        #pragma unroll
+                        for (int j = 0; j < HD / 16; ++j)
+                            mma_bf16(tmem_base + b * AT_KT, sw128_desc(qaddr + (j >> 2) * Cfg::QKB_BYTES + (j & 3) * 32),
+                                     sw128_desc(kaddr + (j >> 2) * Cfg::TKB_BYTES + (j & 3) * 32), idesc_s, j > 0);
+                        issued = true;
+                        mma_commit(&bb.s_full[b]);
+                        meta[tcs % META] = TileMeta{(int8_t)(t_in == 0), (int8_t)(t_in == nt - 1), icount};
+                        if (t_in == nt - 1) {
+                            mma_commit(&bb.q_empty[qb]);
+                            have_item = false;
+                            ++icount;
+                        }
+                        ++t_in;
+                        ++tcs;
+                        prog = true;
+                    }
+                }
+                if (items_done && tcp == tcs) break;
+                if (prog) {
+                    t_idle = globaltimer_ns();
+                    continue;
+                }
+                // Nothing ready: yield the issue slots (the softmax warps share this SM
+                // sub-partition) before polling again.
+                __nanosleep(20);
+                if (*abort_flag || globaltimer_ns() - t_idle > err.limit_ns) {
+                    if (!*abort_flag) record_error(err, DFL_ERR_TIMEOUT);
+                    aborted = true;
+                    break;
+                }
             }
-            if (!aborted && pv_t >= 0 && !issue_pv()) aborted = true;
             if (aborted) {
                 *abort_flag = 1;
                 if (issued) {   // let issued MMAs finish before TMEM is released
@@ -444,7 +495,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
             tc_fence_after();
             const bool real = row >= 0 && row < a.R;   // other MMA rows are padding
             const int64_t NQ = (int64_t)a.N * a.B * a.Hq;
-            const int64_t qrow = real ? (int64_t)(x.n * a.B + row / a.G) * a.Hq + x.g * a.G + row % a.G : 0;
+            const int64_t qrow =
+                real ? (int64_t)(x.n * a.B + row / a.Gq) * a.Hq + x.g * a.G + x.h * a.Gq + row % a.Gq : 0;
             const float inv = 1.f / l_run;
             #pragma unroll 1
             for (int c = 0; c < HD && !pad; c += 32) {
@@ -541,7 +593,7 @@ bool at_map_2d(CUtensorMap* m, const void* base, int64_t rows, int cols, int box
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Q [N*B][Hq][hd] as (hd, Hq, N*B); box = 64 x G heads x B block rows.
+// Q [N*B][Hq][hd] as (hd, Hq, N*B); box = 64 x G (query heads of one item) x B block rows.
 bool at_map_q(CUtensorMap* m, const void* base, int NB, int Hq, int hd, int G, int B) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return false;
@@ -558,11 +610,18 @@ constexpr int AT_SLOTS = 152;   // one persistent CTA per SM of a GB300
 
 }  // namespace
 
+// Head subsets per K/V head: the fewest that give at most 128 query rows per item.
+int at_head_subsets(int B, int G) {
+    for (int hs = 1; hs <= G; ++hs)
+        if (G % hs == 0 && B * (G / hs) <= AT_M) return hs;
+    return 0;
+}
+
 bool attn_tc_supported(int B, int Hq, int Hkv, int hd) {
     if (hd != 64 && hd != 128) return false;
     if (Hkv <= 0 || Hq % Hkv != 0) return false;
     const int G = Hq / Hkv;
-    return B >= 1 && B <= AT_KT && G <= 256 && B * G <= AT_M;
+    return B >= 1 && B <= AT_KT && G <= 256 && at_head_subsets(B, G) > 0;
 }
 
 // Keys per item.  Makespan model over 152 persistent CTAs, in units of one
@@ -573,8 +632,7 @@ bool attn_tc_supported(int B, int Hq, int Hkv, int hd) {
 // over [0, C] and items are handed out dynamically: total work / 152 + half an
 // item.  Depends on the shape only, so workspace sizes do not depend on the
 // device.
-int attn_tc_kps(int N, int C, int B, int Hkv, bool ragged) {
-    const int units = N * Hkv;
+int attn_tc_kps(int units, int C, int B, bool ragged) {
     const int ktiles = (C + B + AT_KT - 1) / AT_KT;
     int best_kps = ktiles * AT_KT;
     double best = 1e30;
@@ -608,7 +666,7 @@ int attn_tc_kps(int N, int C, int B, int Hkv, bool ragged) {
 }
 
 size_t attn_tc_ws_bytes(int N, int C, int B, int Hq, int Hkv, int hd, bool ragged) {
-    const int kps = attn_tc_kps(N, C, B, Hkv, ragged);
+    const int kps = attn_tc_kps(N * Hkv * at_head_subsets(B, Hq / Hkv), C, B, ragged);
     const int S = (C + B + kps - 1) / kps;
     const size_t NQ = (size_t)N * B * Hq;
     size_t b = 256;   // item counter
@@ -623,11 +681,12 @@ dfl_status attn_tc(const void* Q, const void* Kc, const void* Vc, const void* Kb
     if (!ctx) return DFL_ERR_NO_DEVICE;
     const bool ragged = ctx_len != nullptr;
     AtArgs a{};
-    a.N = N; a.B = B; a.Hq = Hq; a.Hkv = Hkv; a.G = Hq / Hkv; a.R = B * a.G;
+    a.N = N; a.B = B; a.Hq = Hq; a.Hkv = Hkv; a.G = Hq / Hkv;
+    a.hs = at_head_subsets(B, a.G); a.Gq = a.G / a.hs; a.R = B * a.Gq;
     a.C = C; a.C_stride = ragged ? C_stride : C; a.ctx_len = ctx_len;
-    a.kps = attn_tc_kps(N, C, B, Hkv, ragged);
+    a.kps = attn_tc_kps(N * Hkv * a.hs, C, B, ragged);
     a.S = (C + B + a.kps - 1) / a.kps;
-    a.items = a.S * N * Hkv;
+    a.items = a.S * N * Hkv * a.hs;
     const size_t NQ = (size_t)N * B * Hq;
     uint8_t* p = static_cast<uint8_t*>(ws);
     a.counter = reinterpret_cast<int*>(p);
@@ -644,7 +703,7 @@ dfl_status attn_tc(const void* Q, const void* Kc, const void* Vc, const void* Kb
     const int64_t ctx_rows = (int64_t)N * a.C_stride;
     const void* kc = C > 0 ? Kc : Kb;   // an empty context is never read; any valid map serves
     const void* vc = C > 0 ? Vc : Vb;
-    if (!at_map_q(&mq, Q, N * B, Hq, hd, a.G, B) ||
+    if (!at_map_q(&mq, Q, N * B, Hq, hd, a.Gq, B) ||
         !at_map_2d(&mkc, kc, C > 0 ? ctx_rows : (int64_t)N * B, kv, AT_KT) ||
         !at_map_2d(&mvc, vc, C > 0 ? ctx_rows : (int64_t)N * B, kv, AT_KT) ||
         !at_map_2d(&mkb, Kb, (int64_t)N * B, kv, AT_KT) || !at_map_2d(&mvb, Vb, (int64_t)N * B, kv, AT_KT))

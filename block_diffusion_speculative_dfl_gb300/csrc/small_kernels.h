@@ -41,7 +41,7 @@ int attn_splits(int N, int C, int B, int Hkv);
 size_t attn_ws_bytes(int N, int C, int B, int Hq, int Hkv, int hd, bool ragged = false);
 // tcgen05 attention (block_attn_tc.cu): shapes it serves, its scratch, launch.
 bool attn_tc_supported(int B, int Hq, int Hkv, int hd);
-int attn_tc_kps(int N, int C, int B, int Hkv, bool ragged);
+int attn_tc_kps(int units, int C, int B, bool ragged);   // units: (sequence, K/V head, head subset)
 size_t attn_tc_ws_bytes(int N, int C, int B, int Hq, int Hkv, int hd, bool ragged);
 dfl_status attn_tc(const void* Q, const void* Kc, const void* Vc, const void* Kb, const void* Vb, int N, int C,
                    int B, int Hq, int Hkv, int hd, void* O, void* ws, cudaStream_t st, const int32_t* ctx_len,

@@ -162,6 +162,8 @@ def test_rope_table_matches_oracle():
     (1, 300, 64, 4, 2, 128, 256),     # 128 query rows per unit (the padded MMA tile full)
     (2, 1000, 8, 8, 4, 64, 256),      # hd 64, several items per sequence
     (32, 2048, 16, 32, 8, 128, 512),  # the Qwen3-8B drafter's attention shape
+    (16, 1024, 33, 32, 8, 128, 512),  # the self-selection window: 132 rows per K/V head, two head subsets
+    (3, 500, 24, 48, 4, 64, 256),     # 288 rows per K/V head: three head subsets of 96 rows
 ])
 def test_block_attn_bf16(N, C, B, Hq, Hkv, hd, d):
     rng = np.random.default_rng(N * 7 + C)
