@@ -148,17 +148,23 @@ __global__ void __launch_bounds__(XT) tv_alpha_kernel(const float* logits, const
             lv[q] = lse_v[row];
         }
         if ((V & 7) == 0) {
+            // exp(a - b) = 2^(a log2(e) - b log2(e)): one FMA and one SFU op per element
+            constexpr float L2E = 1.4426950408889634f;
+            const float zs = inv_T * L2E, zo = -lz * L2E;
+            float vo[8];
+            #pragma unroll
+            for (int q = 0; q < 8; ++q) vo[q] = -lv[q] * L2E;
             for (int c = threadIdx.x; c < V / 8; c += XT) {
                 float zz[8], qx[8];
                 load8<false>(z, c, zz);
                 #pragma unroll
-                for (int e = 0; e < 8; ++e) qx[e] = expf(zz[e] * inv_T - lz);
+                for (int e = 0; e < 8; ++e) qx[e] = ex2_ftz(fmaf(zz[e], zs, zo));
                 #pragma unroll
                 for (int q = 0; q < 8; ++q) {
                     float vv[8];
                     load8<BF16>(vr[q], c, vv);
                     #pragma unroll
-                    for (int e = 0; e < 8; ++e) acc[q] += fabsf(expf(vv[e] - lv[q]) - qx[e]);
+                    for (int e = 0; e < 8; ++e) acc[q] += fabsf(ex2_ftz(fmaf(vv[e], L2E, vo[q])) - qx[e]);
                 }
             }
         } else {

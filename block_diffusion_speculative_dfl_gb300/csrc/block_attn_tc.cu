@@ -20,14 +20,19 @@
 //           of the context cache, then one tile of the block's own keys;
 //   warp 1  MMA issuer: S = Q K^T (M = 128 padded query rows, N = 64 keys,
 //           K = hd) into a double-buffered TMEM tile, then O += P V (K = 64
-//           keys, N = hd, V read MN-major straight from its TMA tile) into a
-//           double-buffered TMEM accumulator;
+//           keys, N = hd; P read from TMEM, V read MN-major straight from its
+//           TMA tile) into a TMEM accumulator, each issued as soon as its
+//           inputs are ready;
 //   warps 2-5  one query row per thread (TMEM lane): masked online softmax
 //           in base 2 with lazy rescaling (O is rescaled in TMEM only when a
-//           row maximum grows by more than 2^8), P written to shared memory
-//           as bf16 in the 128-byte-swizzled K-major layout the MMA reads,
-//           and the item's epilogue (bf16 output, or fp32 partial + log-sum-
-//           exp when the sequence's keys span several items).
+//           row maximum grows by more than 2^8), P written as bf16 over the
+//           first half of the tile's own S columns (the A operand of P V), and
+//           the item's epilogue (bf16 output, or fp32 partial + log-sum-exp
+//           when the sequence's keys span several items).
+// When both pipelines' query rows fit in 64 MMA rows each, they share one Q
+// buffer (pipeline 0's rows in MMA rows 64..127, pipeline 1's in 0..63: each
+// pipeline's MMA reads the other's rows as its padding rows, whose results are
+// never used), and the shared memory saved goes to deeper K/V rings.
 // A combine kernel merges the partials of multi-item sequences.
 #include "internal.h"
 #include "small_kernels.h"
@@ -57,26 +62,26 @@ struct AtArgs {
     float scale_log2;         // log2(e) / sqrt(hd)
 };
 
-template <int HD>
+template <int HD, bool SHQ>
 struct AtCfg {
     static constexpr int NP = 2;                       // independent pipelines per CTA (two items in flight)
     static constexpr int KB = HD / 64;                 // 64-element K-blocks of a head row
     static constexpr int Q_BYTES = AT_M * HD * 2;      // one Q buffer
     static constexpr int QKB_BYTES = AT_M * 128;       // one K-block of Q (128 rows x 128 B)
-    static constexpr int P_BYTES = AT_M * AT_KT * 2;   // one P buffer
     static constexpr int T_BYTES = AT_KT * HD * 2;     // one K or V tile
     static constexpr int TKB_BYTES = AT_KT * 128;      // one K-block of a K/V tile
     static constexpr int NQB = 1;                      // Q buffers per pipeline
-    static constexpr int NPB = HD == 128 ? 1 : 2;      // P buffers per pipeline
-    static constexpr int NSB = 2;                      // S buffers (TMEM) per pipeline
-    static constexpr int STAGES = HD == 128 ? 2 : 4;   // K/V stages per pipeline
-    static constexpr int PIPE_BYTES = NQB * Q_BYTES + NPB * P_BYTES + STAGES * 2 * T_BYTES;
+    static constexpr int NSB = 2;                      // S (and P) buffers in TMEM per pipeline
+    static constexpr int Q_TOTAL = SHQ ? Q_BYTES : NP * Q_BYTES;
+    static constexpr int STAGES = HD == 128 ? (SHQ ? 3 : 2) : 6;   // K/V stages per pipeline
+    static constexpr int RING_BYTES = STAGES * 2 * T_BYTES;
     static constexpr int O_COL = NSB * AT_KT;          // per pipeline: S buffers from column 0, O after them
     static constexpr int PIPE_COLS = 256;              // TMEM columns per pipeline
     static constexpr int TMEM_COLS = NP * PIPE_COLS;
     static constexpr int THREADS = NP * 192;
     static constexpr int BAR_BYTES = 512;              // barriers and scheduler slots per pipeline
-    static constexpr int SMEM = 1024 + NP * (PIPE_BYTES + BAR_BYTES);
+    static constexpr int SMEM = 1024 + Q_TOTAL + NP * (RING_BYTES + BAR_BYTES);
+    static_assert(SMEM <= 227 * 1024, "shared memory");
 };
 
 // One work item, decoded identically by every warp.
@@ -123,12 +128,12 @@ __device__ __forceinline__ void at_tile_range(const AtItem& x, int t, int& v0, i
 }
 
 // Barriers and scheduler slots of one pipeline.
-template <int ST, int NQB, int NPB, int NSB>
+template <int ST, int NQB, int NSB>
 struct AtBars {
     uint64_t kv_full[ST], kv_empty[ST];
     uint64_t q_full[NQB], q_empty[NQB];
-    uint64_t s_full[NSB], s_empty[NSB];
-    uint64_t p_full[NPB], p_empty[NPB];
+    uint64_t s_full[NSB], s_empty[NSB];   // s_empty: the P V product that read the buffer's P is done
+    uint64_t p_full[NSB];                 // P of the buffer written by all 128 softmax threads
     uint64_t o_full, o_empty;
     uint64_t i_full[AT_IRING], i_empty[AT_IRING];
     uint64_t drain;
@@ -136,27 +141,26 @@ struct AtBars {
     int abort_flag;
 };
 
-template <int HD>
-__global__ void __launch_bounds__(AtCfg<HD>::THREADS, 1)
+template <int HD, bool SHQ>
+__global__ void __launch_bounds__(AtCfg<HD, SHQ>::THREADS, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmKc,
                const __grid_constant__ CUtensorMap tmVc, const __grid_constant__ CUtensorMap tmKb,
                const __grid_constant__ CUtensorMap tmVb, const AtArgs a, const DevErr err) {
-    using Cfg = AtCfg<HD>;
-    constexpr int ST = Cfg::STAGES, NQB = Cfg::NQB, NPB = Cfg::NPB, NSB = Cfg::NSB;
-    using Bars = AtBars<ST, NQB, NPB, NSB>;
+    using Cfg = AtCfg<HD, SHQ>;
+    constexpr int ST = Cfg::STAGES, NQB = Cfg::NQB, NSB = Cfg::NSB;
+    using Bars = AtBars<ST, NQB, NSB>;
     static_assert(sizeof(Bars) + 8 <= Cfg::BAR_BYTES, "barrier area");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sm + Cfg::NP * Cfg::PIPE_BYTES + Cfg::NP * Cfg::BAR_BYTES - 8);
+    uint8_t* bar_base = sm + Cfg::Q_TOTAL + Cfg::NP * Cfg::RING_BYTES;
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bar_base + Cfg::NP * Cfg::BAR_BYTES - 8);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int pp = warp / 6;          // this warp's pipeline
     const int role = warp % 6;        // 0 producer, 1 MMA, 2..5 softmax
-    uint8_t* pbase = sm + pp * Cfg::PIPE_BYTES;
-    uint8_t* sQ = pbase;                                // [NQB][Q_BYTES]
-    uint8_t* sP = sQ + NQB * Cfg::Q_BYTES;              // [NPB][P_BYTES]
-    uint8_t* sKV = sP + NPB * Cfg::P_BYTES;             // [ST][K tile, V tile]
-    Bars& bb = *reinterpret_cast<Bars*>(sm + Cfg::NP * Cfg::PIPE_BYTES + pp * Cfg::BAR_BYTES);
+    uint8_t* sQ = sm + (SHQ ? 0 : pp * Cfg::Q_BYTES);                   // this pipeline's Q buffer
+    uint8_t* sKV = sm + Cfg::Q_TOTAL + pp * Cfg::RING_BYTES;             // [ST][K tile, V tile]
+    Bars& bb = *reinterpret_cast<Bars*>(bar_base + pp * Cfg::BAR_BYTES);
     volatile int* abort_flag = &bb.abort_flag;
     // For R <= 64 the query rows of pipeline 0 sit in MMA rows 64..127 and those
     // of pipeline 1 in rows 0..63, so the active softmax warps of the two
@@ -166,8 +170,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     if ((threadIdx.x % 192) == 0) {
         for (int s = 0; s < ST; ++s) { mbar_init(&bb.kv_full[s], 1); mbar_init(&bb.kv_empty[s], 1); }
         for (int b = 0; b < NQB; ++b) { mbar_init(&bb.q_full[b], 1); mbar_init(&bb.q_empty[b], 1); }
-        for (int b = 0; b < NSB; ++b) { mbar_init(&bb.s_full[b], 1); mbar_init(&bb.s_empty[b], 128); }
-        for (int b = 0; b < NPB; ++b) { mbar_init(&bb.p_full[b], 128); mbar_init(&bb.p_empty[b], 1); }
+        for (int b = 0; b < NSB; ++b) {
+            mbar_init(&bb.s_full[b], 1); mbar_init(&bb.s_empty[b], 1); mbar_init(&bb.p_full[b], 128);
+        }
         mbar_init(&bb.o_full, 1); mbar_init(&bb.o_empty, 128);
         for (int r = 0; r < AT_IRING; ++r) { mbar_init(&bb.i_full[r], 1); mbar_init(&bb.i_empty[r], 1 + 4); }
         mbar_init(&bb.drain, 1);
@@ -175,10 +180,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         fence_barrier_init();
     }
     // Zero the Q buffers: MMA rows without a query row stay zero (TMA writes only the R real rows).
-    for (int i = threadIdx.x; i < Cfg::NP * Cfg::PIPE_BYTES / 16; i += Cfg::THREADS) {
-        const int off = i * 16 % Cfg::PIPE_BYTES;
-        if (off < NQB * Cfg::Q_BYTES) *reinterpret_cast<uint4*>(sm + i * 16) = make_uint4(0, 0, 0, 0);
-    }
+    for (int i = threadIdx.x; i < Cfg::Q_TOTAL / 16; i += Cfg::THREADS)
+        *reinterpret_cast<uint4*>(sm + i * 16) = make_uint4(0, 0, 0, 0);
     fence_proxy_async_smem();
     if (warp == 0 && lane == 0) {
         prefetch_tensormap(&tmQ); prefetch_tensormap(&tmKc); prefetch_tensormap(&tmVc);
@@ -264,7 +267,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
             // open / close their item and the item's number.
             constexpr uint32_t idesc_s = idesc_bf16(AT_M, AT_KT);
             constexpr uint32_t idesc_o = idesc_bf16_bmn(AT_M, HD);
-            constexpr int META = 8;
+            constexpr int META = 16;
             static_assert(META >= ST + NSB + 1, "tiles in flight between S and P V");
             struct TileMeta { int8_t first, last; int icount; };
             TileMeta meta[META];
@@ -280,21 +283,22 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                 // P V of the oldest tile whose S is issued
                 if (tcp < tcs) {
                     const TileMeta m = meta[tcp % META];
-                    const int pb = tcp % NPB;
-                    if (mbar_test(&bb.p_full[pb], (tcp / NPB) & 1) &&
+                    const int b = tcp % NSB;
+                    if (mbar_test(&bb.p_full[b], (tcp / NSB) & 1) &&
                         (!m.first || mbar_test(&bb.o_empty, (m.icount & 1) ^ 1))) {
                         tc_fence_after();
                         const int s = tcp % ST;
                         const uint32_t vaddr = smem_u32(sKV + s * 2 * Cfg::T_BYTES + Cfg::T_BYTES);
-                        const uint64_t pd = sw128_desc(smem_u32(sP + pb * Cfg::P_BYTES));
+                        // P (bf16, 2 per column) sits in the first 32 columns of S buffer b:
+                        // 16 keys per MMA = 8 columns
                         #pragma unroll
                         for (int j = 0; j < AT_KT / 16; ++j)
-                            mma_bf16(tmem_base + Cfg::O_COL, pd + 2 * j,
-                                     sw128_desc_mn(vaddr + j * 16 * 128, Cfg::TKB_BYTES, 1024), idesc_o,
-                                     (m.first && j == 0) ? 0 : 1);
+                            mma_bf16_ts(tmem_base + Cfg::O_COL, tmem_base + b * AT_KT + 8 * j,
+                                        sw128_desc_mn(vaddr + j * 16 * 128, Cfg::TKB_BYTES, 1024), idesc_o,
+                                        (m.first && j == 0) ? 0 : 1);
                         issued = true;
                         mma_commit(&bb.kv_empty[s]);
-                        mma_commit(&bb.p_empty[pb]);
+                        mma_commit(&bb.s_empty[b]);
                         if (m.last) mma_commit(&bb.o_full);
                         ++tcp;
                         prog = true;
@@ -350,9 +354,19 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                     t_idle = globaltimer_ns();
                     continue;
                 }
-                // Nothing ready: yield the issue slots (the softmax warps share this SM
-                // sub-partition) before polling again.
-                __nanosleep(20);
+                // Nothing ready: suspend on the barrier of the event most likely next
+                // (P of the oldest pending tile, else the next K/V tile, Q or item) rather
+                // than spin, since a softmax warp shares this SM sub-partition; it wakes
+                // as soon as that phase completes, and the loop then tests everything.
+                if (tcp < tcs) {
+                    mbar_try_wait_for(&bb.p_full[tcp % NSB], (tcp / NSB) & 1, 2000);
+                } else if (have_item && q_ready) {
+                    mbar_try_wait_for(&bb.kv_full[tcs % ST], (tcs / ST) & 1, 2000);
+                } else if (have_item) {
+                    mbar_try_wait_for(&bb.q_full[qb], (icount / NQB) & 1, 2000);
+                } else if (!items_done) {
+                    mbar_try_wait_for(&bb.i_full[icount % AT_IRING], (icount / AT_IRING) & 1, 2000);
+                }
                 if (*abort_flag || globaltimer_ns() - t_idle > err.limit_ns) {
                     if (!*abort_flag) record_error(err, DFL_ERR_TIMEOUT);
                     aborted = true;
@@ -390,20 +404,16 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
             const int nt = x.nctx + x.blk;
             float m_run = -INFINITY, l_run = 0.f;
             for (int t = 0; t < nt; ++t) {
-                const int b = tcount % NSB, pb = tcount % NPB;
+                const int b = tcount % NSB;
                 ok = mbar_wait(&bb.s_full[b], (tcount / NSB) & 1, err);
                 if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }   // also reconverges the warp
                 tc_fence_after();
                 int v0, v1;
                 at_tile_range(x, t, v0, v1);
+                if (!pad) {   // padding rows: nothing to compute; their P columns may hold anything
                 uint32_t pk[AT_KT / 2];
-                if (pad) {   // nothing to compute; the MMA's padding rows of P may hold anything
-                    mbar_arrive(&bb.s_empty[b]);
-                } else {
                 float s[AT_KT];
                 tmem_ld64(tmem_base + lane_off + b * AT_KT, s);
-                tc_fence_before();
-                mbar_arrive(&bb.s_empty[b]);
                 if (v0 > 0 || v1 < AT_KT) {   // edge tile (warp-uniform): keys outside [v0, v1) do not exist
                     #pragma unroll
                     for (int j = 0; j < AT_KT; ++j)
@@ -424,7 +434,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                     if (__any_sync(0xFFFFFFFFu, need)) {
                         // O of this item holds the P V products up to the previous tile: wait for the last one
                         const int tp = tcount - 1;
-                        ok = mbar_wait(&bb.p_empty[tp % NPB], (tp / NPB) & 1, err);
+                        ok = mbar_wait(&bb.s_empty[tp % NSB], (tp / NSB) & 1, err);
                         if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
                         tc_fence_after();
                         const float m_new = need ? mt : m_run;
@@ -454,20 +464,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                     pk[j / 2] = pack_bf16(p0, p1);
                 }
                 l_run += (l4[0] + l4[1]) + (l4[2] + l4[3]);
-                }
-                // P buffer pb is free once the P V product of tile tcount - NPB is done.  Every
-                // warp waits, padding ones included: an arrival on p_full must never run ahead
-                // into the phase of a later tile.
-                if (tcount >= NPB) {
-                    ok = mbar_wait(&bb.p_empty[pb], ((tcount / NPB) & 1) ^ 1, err);
-                    if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
-                }
-                if (!pad) {
-                    uint8_t* prow = sP + pb * Cfg::P_BYTES + lrow * 128;
-                    #pragma unroll
-                    for (int c = 0; c < 8; ++c)
-                        *reinterpret_cast<uint4*>(prow + ((c ^ (lrow & 7)) << 4)) =
-                            make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+                // P over the first half of this tile's S columns (this thread's own lane, whose
+                // S it has already read): the A operand of the P V product
+                tmem_st32u(tmem_base + lane_off + b * AT_KT, pk);
+                tmem_st_wait();
                 }
                 // Rows of the V tile outside [v0, v1) may hold anything (cache rows past
                 // the sequence's length): zero them, so that 0 * V adds exactly nothing.
@@ -483,9 +483,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                         *reinterpret_cast<uint4*>(vt + (i >> 3) / AT_KT * Cfg::TKB_BYTES + kr * 128 + (i & 7) * 16) =
                             make_uint4(0, 0, 0, 0);
                     }
+                    fence_proxy_async_smem();   // visible to the P V product's operand reads
                 }
-                fence_proxy_async_smem();
-                mbar_arrive(&bb.p_full[pb]);
+                tc_fence_before();
+                mbar_arrive(&bb.p_full[b]);
                 ++tcount;
             }
             if (!ok) break;
@@ -723,8 +724,14 @@ dfl_status attn_tc(const void* Q, const void* Kc, const void* Vc, const void* Kb
             kern<<<grid, threads, smem, st>>>(mq, mkc, mvc, mkb, mvb, a, err);
             return last_launch();
         };
-        rc = hd == 128 ? run(attn_tc_kernel<128>, AtCfg<128>::SMEM, AtCfg<128>::THREADS, 1)
-                       : run(attn_tc_kernel<64>, AtCfg<64>::SMEM, AtCfg<64>::THREADS, 0);
+        // the two pipelines share one Q buffer when each item has at most 64 query rows
+        const bool shq = a.R <= 64;
+        if (hd == 128)
+            rc = shq ? run(attn_tc_kernel<128, true>, AtCfg<128, true>::SMEM, AtCfg<128, true>::THREADS, 3)
+                     : run(attn_tc_kernel<128, false>, AtCfg<128, false>::SMEM, AtCfg<128, false>::THREADS, 1);
+        else
+            rc = shq ? run(attn_tc_kernel<64, true>, AtCfg<64, true>::SMEM, AtCfg<64, true>::THREADS, 2)
+                     : run(attn_tc_kernel<64, false>, AtCfg<64, false>::SMEM, AtCfg<64, false>::THREADS, 0);
     }
     if (rc != DFL_OK || a.S == 1) return rc;
     ProfScope ps("attn_combine", st);

@@ -17,7 +17,7 @@ struct DeviceCtx {
     int* err_word = nullptr;       // device address of this device's error word
     bool gemm_attr_set[16] = {};   // max-dynamic-smem set for gemm instantiations
     bool mix_attr_set = false;
-    bool attn_attr_set[2] = {};    // tcgen05 attention, head dim 64 / 128
+    bool attn_attr_set[4] = {};    // tcgen05 attention: head dim 64 / 128, own / shared Q buffer
 };
 
 // Context of the current device (initialised on first use); nullptr if no

@@ -23,6 +23,7 @@ namespace dfl {
 namespace {
 
 constexpr int RS_THREADS = 256;
+constexpr float kLog2e = 1.4426950408889634f;
 
 struct RowStat {
     float m;    // running max
@@ -80,7 +81,47 @@ __global__ void __launch_bounds__(RS_THREADS) verifier_row_stats_kernel(const vo
     const bool vec = (V % 8) == 0;
     if (vec) {
         const int chunks = V / 8;
-        for (int c = threadIdx.x; c < chunks; c += RS_THREADS) {
+        int c = threadIdx.x;
+        if constexpr (BF16) {
+            // Four 16-byte loads in flight per thread: chunks c, c + T, c + 2T, c + 3T
+            // (increasing indices, so the first maximum found is the lowest).
+            for (; c + 3 * RS_THREADS < chunks; c += 4 * RS_THREADS) {
+                uint4 u[4];
+                #pragma unroll
+                for (int q = 0; q < 4; ++q) u[q] = __ldg(reinterpret_cast<const uint4*>(row) + c + q * RS_THREADS);
+                float x[4][8];
+                #pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    x[q][0] = bf16lo(u[q].x); x[q][1] = bf16hi(u[q].x); x[q][2] = bf16lo(u[q].y); x[q][3] = bf16hi(u[q].y);
+                    x[q][4] = bf16lo(u[q].z); x[q][5] = bf16hi(u[q].z); x[q][6] = bf16lo(u[q].w); x[q][7] = bf16hi(u[q].w);
+                }
+                float vm = x[0][0];
+                #pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    #pragma unroll
+                    for (int j = 0; j < 8; ++j) vm = fmaxf(vm, x[q][j]);
+                if (vm > st.m) {
+                    st.s = st.m == -INFINITY ? 0.f : st.s * ex2_ftz((st.m - vm) * kLog2e);
+                    st.m = vm;
+                    int f = -1;
+                    #pragma unroll
+                    for (int q = 3; q >= 0; --q)
+                        #pragma unroll
+                        for (int j = 7; j >= 0; --j)
+                            if (x[q][j] == vm) f = (c + q * RS_THREADS) * 8 + j;
+                    st.idx = f;
+                }
+                // exp(x - m) = 2^(x log2(e) - m log2(e)): one FMA and one SFU op per element
+                const float nml = -st.m * kLog2e;
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                #pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    #pragma unroll
+                    for (int j = 0; j < 8; ++j) acc[q] += ex2_ftz(fmaf(x[q][j], kLog2e, nml));
+                st.s += (acc[0] + acc[1]) + (acc[2] + acc[3]);
+            }
+        }
+        for (; c < chunks; c += RS_THREADS) {
             float x[8];
             if constexpr (BF16) {
                 const uint4 u = reinterpret_cast<const uint4*>(row)[c];
