@@ -113,6 +113,7 @@ def source_hash(files):
 # kernel trace name -> source files its code lives in (for the traffic record)
 KERNEL_SOURCES = {
     "gemm_ctx_kv": ["gemm_tc.cuh", "gemm_tc.cu"], "gemm_block_qkv": ["gemm_tc.cuh", "gemm_tc.cu"],
+    "gemm_kv_qkv": ["gemm_tc.cuh", "gemm_tc.cu"], "gemm_kv_qkv_append": ["gemm_tc.cuh", "gemm_tc.cu"],
     "gemm_o_proj": ["gemm_tc.cuh", "gemm_tc.cu"], "gemm_lm_head": ["gemm_tc.cuh", "gemm_tc.cu"],
     "mix_rmsnorm_bf16": ["mix_rmsnorm.cu"], "attn_bf16": ["block_attn.cu"], "attn_tc": ["block_attn_tc.cu"],
     "verifier_row_stats": ["self_select.cu"],
@@ -154,6 +155,9 @@ def kernel_work(w, ctx_lens=None):
         "attn_tc": (4.0 * B * Hq * keys * hd, 2.0 * (2 * keys * kv + 2 * rows_b * qd)),
         "gemm_o_proj": (2.0 * rows_b * d * qd, 2.0 * (rows_b * qd + d * qd) + 8.0 * rows_b * d),
     }
+    # the context and block projections of a layer run as one grouped launch
+    both = "gemm_kv_qkv_append" if w.R > 0 else "gemm_kv_qkv"
+    work[both] = tuple(a + b for a, b in zip(work[ctx], work["gemm_block_qkv"]))
     if w.F > 0:
         M = rows_b
         work["gemm_ffn_gate_up"] = (2.0 * M * 2 * w.F * d, 2.0 * (M * d + 2 * w.F * d + M * w.F))

@@ -220,41 +220,41 @@ dfl_status dual_kv_proj_bf16(DeviceCtx* ctx, const void* Xc, int64_t ctx_M, int 
     void* Xn = ws;
     if ((rc = rmsnorm_rows(Xb, d, (int64_t)N * B, 1, 1, 0, blk_gain, eps, Xn, true, st)) != DFL_OK) return rc;
 
-    if (ctx_M > 0) {   // context rows: [Kc | Vc] = Xc [Wkc ; Wvc]^T
-        GemmArgs g{};
-        g.A = Xc; g.M = ctx_M; g.K = d;
-        g.B[0] = Wkc; g.B[1] = Wvc; g.b_rows[0] = kv; g.b_rows[1] = kv;
-        g.b_begin[0] = 0; g.b_begin[1] = kv; g.nb = 2; g.N = 2 * kv;
-        g.bn = (kv % 256 == 0) ? 256 : 128;
-        g.m_inner = 0;
-        g.epi = EPI_STORE;
-        g.ep.seg[0] = GemmSeg{Kc, 0, kv, rope != nullptr};
-        g.ep.seg[1] = GemmSeg{Vc, kv, kv, 0};
-        g.ep.nseg = 2;
-        g.ep.rope = rope; g.ep.hd = hd; g.ep.rows_per_seq = ctx_per; g.ep.pos_off = 0;
-        if (plan) { g.ep.row_pos = plan->ctx_pos; g.ep.row_dst = plan->ctx_dst; }
-        g.tag = plan ? "gemm_ctx_kv_append" : "gemm_ctx_kv";
-        if ((rc = gemm_tc(ctx, g, st)) != DFL_OK) return rc;
-    }
-    {   // block rows: [Q | Kb | Vb] = Xn [Wq ; Wkb ; Wvb]^T
-        GemmArgs g{};
-        g.A = Xn; g.M = N * B; g.K = d;
-        g.B[0] = Wq; g.B[1] = Wkb; g.B[2] = Wvb;
-        g.b_rows[0] = qd; g.b_rows[1] = kv; g.b_rows[2] = kv;
-        g.b_begin[0] = 0; g.b_begin[1] = qd; g.b_begin[2] = qd + kv; g.nb = 3; g.N = qd + 2 * kv;
-        g.bn = 0;   // chosen per shape
-        g.m_inner = 1;
-        g.epi = EPI_STORE;
-        g.ep.seg[0] = GemmSeg{Q, 0, qd, rope != nullptr};
-        g.ep.seg[1] = GemmSeg{Kb, qd, kv, rope != nullptr};
-        g.ep.seg[2] = GemmSeg{Vb, qd + kv, kv, 0};
-        g.ep.nseg = 3;
-        g.ep.rope = rope; g.ep.hd = hd; g.ep.rows_per_seq = B; g.ep.pos_off = ctx_per;
-        if (plan) g.ep.row_pos = plan->blk_pos;
-        g.tag = "gemm_block_qkv";
-        if ((rc = gemm_tc(ctx, g, st)) != DFL_OK) return rc;
-    }
-    return DFL_OK;
+    // block rows: [Q | Kb | Vb] = Xn [Wq ; Wkb ; Wvb]^T
+    GemmArgs gb{};
+    gb.A = Xn; gb.M = N * B; gb.K = d;
+    gb.B[0] = Wq; gb.B[1] = Wkb; gb.B[2] = Wvb;
+    gb.b_rows[0] = qd; gb.b_rows[1] = kv; gb.b_rows[2] = kv;
+    gb.b_begin[0] = 0; gb.b_begin[1] = qd; gb.b_begin[2] = qd + kv; gb.nb = 3; gb.N = qd + 2 * kv;
+    gb.bn = 0;   // chosen per shape
+    gb.m_inner = 1;
+    gb.epi = EPI_STORE;
+    gb.ep.seg[0] = GemmSeg{Q, 0, qd, rope != nullptr};
+    gb.ep.seg[1] = GemmSeg{Kb, qd, kv, rope != nullptr};
+    gb.ep.seg[2] = GemmSeg{Vb, qd + kv, kv, 0};
+    gb.ep.nseg = 3;
+    gb.ep.rope = rope; gb.ep.hd = hd; gb.ep.rows_per_seq = B; gb.ep.pos_off = ctx_per;
+    if (plan) gb.ep.row_pos = plan->blk_pos;
+    gb.tag = "gemm_block_qkv";
+    if (ctx_M <= 0) return gemm_tc(ctx, gb, st);
+
+    // context rows: [Kc | Vc] = Xc [Wkc ; Wvc]^T
+    GemmArgs gc{};
+    gc.A = Xc; gc.M = ctx_M; gc.K = d;
+    gc.B[0] = Wkc; gc.B[1] = Wvc; gc.b_rows[0] = kv; gc.b_rows[1] = kv;
+    gc.b_begin[0] = 0; gc.b_begin[1] = kv; gc.nb = 2; gc.N = 2 * kv;
+    gc.bn = (kv % 256 == 0) ? 256 : 128;
+    gc.m_inner = 0;
+    gc.epi = EPI_STORE;
+    gc.ep.seg[0] = GemmSeg{Kc, 0, kv, rope != nullptr};
+    gc.ep.seg[1] = GemmSeg{Vc, kv, kv, 0};
+    gc.ep.nseg = 2;
+    gc.ep.rope = rope; gc.ep.hd = hd; gc.ep.rows_per_seq = ctx_per; gc.ep.pos_off = 0;
+    if (plan) { gc.ep.row_pos = plan->ctx_pos; gc.ep.row_dst = plan->ctx_dst; }
+    gc.tag = plan ? "gemm_ctx_kv_append" : "gemm_ctx_kv";
+    // One launch for both: the block projection's weights stream from HBM on a
+    // few SMs while the others work on context tiles (block tiles first).
+    return gemm_tc2(ctx, gb, gc, plan ? "gemm_kv_qkv_append" : "gemm_kv_qkv", st);
 }
 
 // bf16 block attention and output projection, Xb += Attn(Q, [Kc;Kb], [Vc;Vb]) Wo^T.

@@ -35,8 +35,8 @@ bool make_map(CUtensorMap* m, const void* base, int rows, int K, int box_rows) {
 }
 
 template <int BN, int EPI, int CM>
-dfl_status launch(DeviceCtx* ctx, const GemmArgs& g, const GemmShape& sh, const CUtensorMap (&mb)[3],
-                  const CUtensorMap& ma, cudaStream_t st, int slot) {
+dfl_status launch(DeviceCtx* ctx, const GemmProb& p0, const GemmProb& p1, int nprob, const char* tag,
+                  cudaStream_t st, int slot) {
     auto kern = gemm_tc_kernel<BN, EPI, CM>;
     if (!ctx->gemm_attr_set[slot]) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, GemmCfg<BN>::SMEM) !=
@@ -46,7 +46,8 @@ dfl_status launch(DeviceCtx* ctx, const GemmArgs& g, const GemmShape& sh, const 
             return DFL_ERR_CUDA;
         ctx->gemm_attr_set[slot] = true;
     }
-    const int tiles = ((sh.tiles_m + CM - 1) / CM) * sh.tiles_n;
+    int tiles = ((p0.sh.tiles_m + CM - 1) / CM) * p0.sh.tiles_n;
+    if (nprob > 1) tiles += ((p1.sh.tiles_m + CM - 1) / CM) * p1.sh.tiles_n;
     const int max_clusters = ctx->sm_count / CM;
     const int grid = (tiles < max_clusters ? tiles : max_clusters) * CM;
     cudaLaunchConfig_t cfg = {};
@@ -62,16 +63,16 @@ dfl_status launch(DeviceCtx* ctx, const GemmArgs& g, const GemmShape& sh, const 
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     const DevErr err = dev_err(ctx);
-    ProfScope ps(g.tag ? g.tag : "gemm_tc", st);
-    if (cudaLaunchKernelEx(&cfg, kern, ma, mb[0], mb[1], mb[2], sh, g.ep, err) != cudaSuccess) return DFL_ERR_CUDA;
+    ProfScope ps(tag ? tag : "gemm_tc", st);
+    if (cudaLaunchKernelEx(&cfg, kern, p0, p1, nprob, err) != cudaSuccess) return DFL_ERR_CUDA;
     return last_launch();
 }
 
 template <int BN, int EPI>
-dfl_status launch_cm(DeviceCtx* ctx, const GemmArgs& g, const GemmShape& sh, const CUtensorMap (&mb)[3],
-                     const CUtensorMap& ma, cudaStream_t st, int slot, int cm) {
-    if (cm == 2) return launch<BN, EPI, 2>(ctx, g, sh, mb, ma, st, slot + 8);
-    return launch<BN, EPI, 1>(ctx, g, sh, mb, ma, st, slot);
+dfl_status launch_cm(DeviceCtx* ctx, const GemmProb& p0, const GemmProb& p1, int nprob, const char* tag,
+                     cudaStream_t st, int slot, int cm) {
+    if (cm == 2) return launch<BN, EPI, 2>(ctx, p0, p1, nprob, tag, st, slot + 8);
+    return launch<BN, EPI, 1>(ctx, p0, p1, nprob, tag, st, slot);
 }
 
 }  // namespace
@@ -96,14 +97,14 @@ static int pick_bn(const GemmArgs& g, int sm_count) {
     return cost(256) <= cost(128) ? 256 : 128;
 }
 
-dfl_status gemm_tc(DeviceCtx* ctx, const GemmArgs& g_in, cudaStream_t st) {
-    GemmArgs g = g_in;
-    if (g.bn == 0) g.bn = pick_bn(g, ctx->sm_count);
+// Validated problem of one GEMM for tile width bn and cluster size cm.
+static dfl_status build_prob(const GemmArgs& g, int cm, GemmProb& P) {
     if (g.M <= 0 || g.N <= 0 || g.K <= 0) return DFL_ERR_INVALID_ARG;
     if (g.K % 8 != 0 || !aligned16(g.A)) return DFL_ERR_MISALIGNED;
     if (g.bn != 128 && g.bn != 256) return DFL_ERR_UNSUPPORTED_SHAPE;
     if (g.nb < 1 || g.nb > 3) return DFL_ERR_INVALID_ARG;
-    GemmShape sh{};
+    GemmShape& sh = P.sh;
+    sh = GemmShape{};
     sh.M = g.M; sh.N = g.N; sh.K = g.K;
     sh.tiles_m = (g.M + GEMM_BM - 1) / GEMM_BM;
     sh.tiles_n = (g.N + g.bn - 1) / g.bn;
@@ -112,30 +113,73 @@ dfl_status gemm_tc(DeviceCtx* ctx, const GemmArgs& g_in, cudaStream_t st) {
     sh.nb = g.nb;
     sh.split_b = g.split_b;
     if (g.split_b && (g.nb != 2 || (g.N / 2) % (g.bn / 2) != 0)) return DFL_ERR_UNSUPPORTED_SHAPE;
-    // Pair the M-tiles of each N-tile in 2-CTA clusters (B tile multicast) when
-    // there is more than one M-tile.
-    const int cm = sh.tiles_m >= 2 ? 2 : 1;
-    CUtensorMap ma, mb[3];
-    if (!make_map(&ma, g.A, g.M, g.K, GEMM_BM)) return DFL_ERR_CUDA;
+    if (!make_map(&P.a, g.A, g.M, g.K, GEMM_BM)) return DFL_ERR_CUDA;
     for (int j = 0; j < 3; ++j) {
         const int jj = j < g.nb ? j : 0;
         if (!aligned16(g.B[jj])) return DFL_ERR_MISALIGNED;
         // every tile of BN columns must come from one B map
         if (j < g.nb && !g.split_b && (g.b_begin[j] % g.bn != 0)) return DFL_ERR_UNSUPPORTED_SHAPE;
-        if (!make_map(&mb[j], g.B[jj], g.b_rows[jj], g.K, g.split_b ? g.bn / 2 : g.bn / cm)) return DFL_ERR_CUDA;
+        if (!make_map(&P.b[j], g.B[jj], g.b_rows[jj], g.K, g.split_b ? g.bn / 2 : g.bn / cm)) return DFL_ERR_CUDA;
         sh.b_begin[j] = g.b_begin[jj];
     }
-    const int slot = (g.bn == 256 ? 0 : 4) + g.epi;
-    if (g.bn == 256) {
-        if (g.epi == EPI_STORE) return launch_cm<256, EPI_STORE>(ctx, g, sh, mb, ma, st, slot, cm);
-        if (g.epi == EPI_RESID) return launch_cm<256, EPI_RESID>(ctx, g, sh, mb, ma, st, slot, cm);
-        if (g.epi == EPI_SWIGLU) return launch_cm<256, EPI_SWIGLU>(ctx, g, sh, mb, ma, st, slot, cm);
-        return launch_cm<256, EPI_ARGMAX>(ctx, g, sh, mb, ma, st, slot, cm);
+    P.ep = g.ep;
+    return DFL_OK;
+}
+
+static dfl_status launch_probs(DeviceCtx* ctx, const GemmProb& p0, const GemmProb& p1, int nprob, int bn, int epi,
+                               int cm, const char* tag, cudaStream_t st) {
+    const int slot = (bn == 256 ? 0 : 4) + epi;
+    if (bn == 256) {
+        if (epi == EPI_STORE) return launch_cm<256, EPI_STORE>(ctx, p0, p1, nprob, tag, st, slot, cm);
+        if (epi == EPI_RESID) return launch_cm<256, EPI_RESID>(ctx, p0, p1, nprob, tag, st, slot, cm);
+        if (epi == EPI_SWIGLU) return launch_cm<256, EPI_SWIGLU>(ctx, p0, p1, nprob, tag, st, slot, cm);
+        return launch_cm<256, EPI_ARGMAX>(ctx, p0, p1, nprob, tag, st, slot, cm);
     }
-    if (g.epi == EPI_STORE) return launch_cm<128, EPI_STORE>(ctx, g, sh, mb, ma, st, slot, cm);
-    if (g.epi == EPI_RESID) return launch_cm<128, EPI_RESID>(ctx, g, sh, mb, ma, st, slot, cm);
-    if (g.epi == EPI_SWIGLU) return launch_cm<128, EPI_SWIGLU>(ctx, g, sh, mb, ma, st, slot, cm);
-    return launch_cm<128, EPI_ARGMAX>(ctx, g, sh, mb, ma, st, slot, cm);
+    if (epi == EPI_STORE) return launch_cm<128, EPI_STORE>(ctx, p0, p1, nprob, tag, st, slot, cm);
+    if (epi == EPI_RESID) return launch_cm<128, EPI_RESID>(ctx, p0, p1, nprob, tag, st, slot, cm);
+    if (epi == EPI_SWIGLU) return launch_cm<128, EPI_SWIGLU>(ctx, p0, p1, nprob, tag, st, slot, cm);
+    return launch_cm<128, EPI_ARGMAX>(ctx, p0, p1, nprob, tag, st, slot, cm);
+}
+
+dfl_status gemm_tc(DeviceCtx* ctx, const GemmArgs& g_in, cudaStream_t st) {
+    GemmArgs g = g_in;
+    if (g.bn == 0) g.bn = pick_bn(g, ctx->sm_count);
+    // Pair the M-tiles of each N-tile in 2-CTA clusters (B tile multicast) when
+    // there is more than one M-tile.
+    const int cm = (g.M + GEMM_BM - 1) / GEMM_BM >= 2 ? 2 : 1;
+    GemmProb P;
+    dfl_status rc = build_prob(g, cm, P);
+    if (rc != DFL_OK) return rc;
+    return launch_probs(ctx, P, P, 1, g.bn, g.epi, cm, g.tag, st);
+}
+
+// Two independent GEMMs in one launch (same epilogue kind; problem 0's tiles
+// first), with a tile width and cluster shape both accept; two launches when
+// there is none.
+dfl_status gemm_tc2(DeviceCtx* ctx, const GemmArgs& g0_in, const GemmArgs& g1_in, const char* tag, cudaStream_t st) {
+    GemmArgs g0 = g0_in, g1 = g1_in;
+    // One tile width for both: 256 when every B segment of both allows it (a
+    // grouped launch has enough tiles either way), else 128.
+    auto allows = [](const GemmArgs& g, int bn) {
+        if (g.bn != 0) return g.bn == bn;
+        if (g.split_b) return (g.N / 2) % (bn / 2) == 0;
+        for (int j = 0; j < g.nb; ++j) if (g.b_begin[j] % bn != 0) return false;
+        return true;
+    };
+    const int bn = allows(g0, 256) && allows(g1, 256) ? 256 : allows(g0, 128) && allows(g1, 128) ? 128 : 0;
+    // Clusters of two only when both problems have at least two M-tiles.
+    const int cm0 = (g0.M + GEMM_BM - 1) / GEMM_BM >= 2 ? 2 : 1, cm1 = (g1.M + GEMM_BM - 1) / GEMM_BM >= 2 ? 2 : 1;
+    const int cm = cm0 < cm1 ? cm0 : cm1;
+    if (bn == 0 || g0.epi != g1.epi) {
+        dfl_status rc = gemm_tc(ctx, g0, st);
+        return rc != DFL_OK ? rc : gemm_tc(ctx, g1, st);
+    }
+    g0.bn = g1.bn = bn;
+    GemmProb P0, P1;
+    dfl_status rc = build_prob(g0, cm, P0);
+    if (rc == DFL_OK) rc = build_prob(g1, cm, P1);
+    if (rc != DFL_OK) return rc;
+    return launch_probs(ctx, P0, P1, 2, bn, g0.epi, cm, tag, st);
 }
 
 }  // namespace dfl

@@ -61,6 +61,18 @@ struct GemmShape {
     int split_b;         // B tile = [BN/2 rows of map 0 ; BN/2 rows of map 1] at rows tn * BN/2
 };
 
+// One GEMM of a launch: its tensor maps (A, up to three B segments), shape and
+// epilogue.  A launch runs one or two problems with the same tile width,
+// epilogue kind and cluster shape as one persistent tile sequence (problem 0's
+// tiles first), so that a small problem streams its weights while other SMs
+// work on a large one.
+struct GemmProb {
+    CUtensorMap a;
+    CUtensorMap b[3];
+    GemmShape sh;
+    GemmEpi ep;
+};
+
 constexpr int GEMM_BM = 128;
 constexpr int GEMM_BK = 64;
 constexpr int GEMM_THREADS = 192;
@@ -257,9 +269,8 @@ __device__ __forceinline__ void epi_swiglu(const GemmShape& sh, const GemmEpi& e
 
 template <int BN, int EPI, int CM>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
-gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
-               const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmB2,
-               const GemmShape sh, const GemmEpi ep, const DevErr err) {
+gemm_tc_kernel(const __grid_constant__ GemmProb p0, const __grid_constant__ GemmProb p1, const int nprob,
+               const DevErr err) {
     using Cfg = GemmCfg<BN>;
     constexpr int STAGES = Cfg::STAGES;
     extern __shared__ uint8_t smem_raw[];
@@ -279,8 +290,16 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 
     const uint32_t crank = (CM > 1) ? cluster_ctarank() : 0u;
     const int cid = blockIdx.x / CM, nclusters = gridDim.x / CM;
-    const int tiles_mc = (sh.tiles_m + CM - 1) / CM;
     constexpr uint16_t kPair = (1u << CM) - 1u;
+    // cluster tiles of each problem; tile t of the launch belongs to problem 0 if t < T0
+    const int tmc0 = (p0.sh.tiles_m + CM - 1) / CM, tmc1 = (p1.sh.tiles_m + CM - 1) / CM;
+    const int T0 = tmc0 * p0.sh.tiles_n;
+    const int total = T0 + (nprob > 1 ? tmc1 * p1.sh.tiles_n : 0);
+    auto locate = [&](int t, const GemmProb*& P, int& tmc, int& tn) {
+        const bool second = t >= T0;
+        P = second ? &p1 : &p0;
+        tile_coords(P->sh, second ? tmc1 : tmc0, second ? t - T0 : t, tmc, tn);
+    };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], CM); }
@@ -290,17 +309,17 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         fence_barrier_init();
     }
     if (warp == 0 && lane == 0) {
-        prefetch_tensormap(&tmA);
-        prefetch_tensormap(&tmB0);
-        if (sh.nb > 1) prefetch_tensormap(&tmB1);
-        if (sh.nb > 2) prefetch_tensormap(&tmB2);
+        for (int q = 0; q < nprob; ++q) {
+            const GemmProb& P = q ? p1 : p0;
+            prefetch_tensormap(&P.a);
+            for (int j = 0; j < P.sh.nb; ++j) prefetch_tensormap(&P.b[j]);
+        }
     }
     if (warp == 1) { tmem_alloc(tmem_holder, Cfg::TMEM_COLS); tmem_relinquish(); }
     tc_fence_before();
     if (CM > 1) cluster_sync(); else __syncthreads();   // peers' barriers are initialised before any multicast
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
-    const int total = tiles_mc * sh.tiles_n;
 
     if (warp == 0) {
         if (lane == 0) {
@@ -310,26 +329,28 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             uint32_t fills = 0;   // bit s: stage s has been filled at least once
             bool aborted = false;
             for (int t = cid; t < total && !aborted; t += nclusters) {
+                const GemmProb* P;
                 int tmc, tn;
-                tile_coords(sh, tiles_mc, t, tmc, tn);
+                locate(t, P, tmc, tn);
+                const GemmShape& sh = P->sh;
                 const int m0 = (tmc * CM + (int)crank) * GEMM_BM, n0 = tn * BN;
-                const CUtensorMap* mb = &tmB0;
+                const CUtensorMap* mb = &P->b[0];
                 int nb0 = n0;
-                if (sh.nb > 2 && n0 >= sh.b_begin[2]) { mb = &tmB2; nb0 = n0 - sh.b_begin[2]; }
-                else if (sh.nb > 1 && n0 >= sh.b_begin[1]) { mb = &tmB1; nb0 = n0 - sh.b_begin[1]; }
+                if (sh.nb > 2 && n0 >= sh.b_begin[2]) { mb = &P->b[2]; nb0 = n0 - sh.b_begin[2]; }
+                else if (sh.nb > 1 && n0 >= sh.b_begin[1]) { mb = &P->b[1]; nb0 = n0 - sh.b_begin[1]; }
                 for (int kb = 0; kb < sh.num_kb; ++kb) {
                     if (*abort_flag || !mbar_wait(&empty[stage], phase ^ 1, err)) { aborted = true; break; }
                     mbar_arrive_expect_tx(&full[stage], Cfg::A_BYTES + Cfg::B_BYTES);
-                    tma_load_2d(sA + stage * Cfg::A_BYTES, &tmA, kb * GEMM_BK, m0, &full[stage]);
+                    tma_load_2d(sA + stage * Cfg::A_BYTES, &P->a, kb * GEMM_BK, m0, &full[stage]);
                     if (sh.split_b) {   // [gate half (map 0) ; up half (map 1)] of the same features
                         const int fr = tn * (BN / 2);
                         if (CM == 1) {
-                            tma_load_2d(sB + stage * Cfg::B_BYTES, &tmB0, kb * GEMM_BK, fr, &full[stage]);
-                            tma_load_2d(sB + stage * Cfg::B_BYTES + Cfg::B_BYTES / 2, &tmB1, kb * GEMM_BK, fr,
+                            tma_load_2d(sB + stage * Cfg::B_BYTES, &P->b[0], kb * GEMM_BK, fr, &full[stage]);
+                            tma_load_2d(sB + stage * Cfg::B_BYTES + Cfg::B_BYTES / 2, &P->b[1], kb * GEMM_BK, fr,
                                         &full[stage]);
                         } else {
                             tma_load_2d_mc(sB + stage * Cfg::B_BYTES + crank * (Cfg::B_BYTES / 2),
-                                           crank ? &tmB1 : &tmB0, kb * GEMM_BK, fr, &full[stage], kPair);
+                                           crank ? &P->b[1] : &P->b[0], kb * GEMM_BK, fr, &full[stage], kPair);
                         }
                     } else if (CM == 1) {
                         tma_load_2d(sB + stage * Cfg::B_BYTES, mb, kb * GEMM_BK, nb0, &full[stage]);
@@ -364,10 +385,11 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             bool aborted = false;
             bool issued = false;
             for (int t = cid; t < total && !aborted; t += nclusters) {
+                const int num_kb = (t >= T0 ? p1 : p0).sh.num_kb;
                 if (*abort_flag || !mbar_wait(&tempty[acc], acc_phase ^ 1, err)) { aborted = true; break; }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
-                for (int kb = 0; kb < sh.num_kb; ++kb) {
+                for (int kb = 0; kb < num_kb; ++kb) {
                     if (*abort_flag || !mbar_wait(&full[stage], phase, err)) { aborted = true; break; }
                     tc_fence_after();
                     const uint64_t ad = sw128_desc(smem_u32(sA + stage * Cfg::A_BYTES));
@@ -403,14 +425,15 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             const bool ready = mbar_wait(&tfull[acc], acc_phase, err);
             if (!__all_sync(0xFFFFFFFFu, ready)) { *abort_flag = 1; break; }
             tc_fence_after();
+            const GemmProb* P;
             int tmc, tn;
-            tile_coords(sh, tiles_mc, t, tmc, tn);
+            locate(t, P, tmc, tn);
             const int row = (tmc * CM + (int)crank) * GEMM_BM + q * 32 + lane;
             const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
-            if (EPI == EPI_STORE) epi_store<BN>(sh, ep, tbase, row, tn * BN);
-            else if (EPI == EPI_RESID) epi_resid<BN>(sh, ep, tbase, row, tn * BN);
-            else if (EPI == EPI_SWIGLU) epi_swiglu<BN>(sh, ep, tbase, row, tn);
-            else epi_argmax<BN>(sh, ep, tbase, row, tn * BN, tn);
+            if (EPI == EPI_STORE) epi_store<BN>(P->sh, P->ep, tbase, row, tn * BN);
+            else if (EPI == EPI_RESID) epi_resid<BN>(P->sh, P->ep, tbase, row, tn * BN);
+            else if (EPI == EPI_SWIGLU) epi_swiglu<BN>(P->sh, P->ep, tbase, row, tn);
+            else epi_argmax<BN>(P->sh, P->ep, tbase, row, tn * BN, tn);
             tc_fence_before();
             mbar_arrive(&tempty[acc]);
             acc ^= 1;

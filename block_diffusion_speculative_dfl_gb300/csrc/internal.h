@@ -64,6 +64,9 @@ struct GemmArgs {
 };
 
 dfl_status gemm_tc(DeviceCtx* ctx, const GemmArgs& g, cudaStream_t st);
+// Two independent GEMMs in one persistent launch (problem g0's tiles first),
+// traced as `tag`; two launches when no tile width suits both.
+dfl_status gemm_tc2(DeviceCtx* ctx, const GemmArgs& g0, const GemmArgs& g1, const char* tag, cudaStream_t st);
 
 // The driver's cuTensorMapEncodeTiled (resolved once; nullptr if unavailable).
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
