@@ -308,8 +308,9 @@ dfl_status sample_rows(const float* logits, int64_t ld, const float* pmax, const
 }
 
 // Per-tile partials from materialised fp32 logits (the fp32 path): max,
-// lowest argmax and fp64 sum of expf((z - max) * inv_T) in column order,
-// exactly as the tensor-core GEMM epilogue forms them.  Thread per (row, tile).
+// lowest argmax and sum of expf((z - max) * inv_T) in column order (groups
+// of four in fp32, groups in fp64), exactly as the tensor-core GEMM epilogue
+// forms them.  Thread per (row, tile).
 __global__ void tile_partials_kernel(const float* logits, int64_t ld, int64_t M, int V, int bn, int tiles,
                                      float inv_T, float* pmax, int* pidx, double* psum) {
     const int64_t id = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
@@ -323,7 +324,11 @@ __global__ void tile_partials_kernel(const float* logits, int64_t ld, int64_t M,
     for (int v = 0; v < vmax; ++v)
         if (z[v] > best) { best = z[v]; bi = t * bn + v; }
     double s = 0.0;
-    for (int v = 0; v < vmax; ++v) s += (double)expf((z[v] - best) * inv_T);
+    for (int v = 0; v < vmax; v += 4) {   // groups of four added pairwise in fp32, as the GEMM epilogue does
+        float e[4];
+        for (int q = 0; q < 4; ++q) e[q] = v + q < vmax ? expf((z[v + q] - best) * inv_T) : 0.f;
+        s += (double)((e[0] + e[1]) + (e[2] + e[3]));
+    }
     pmax[id] = best;
     pidx[id] = bi;
     if (psum) psum[id] = s;
