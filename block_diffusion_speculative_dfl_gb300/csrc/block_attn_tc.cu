@@ -15,10 +15,13 @@
 // tiles are read from HBM once and from L2 by the others).  A persistent kernel (one CTA per SM)
 // takes items from a global counter; empty items (past a shorter sequence's
 // keys) are skipped by the scheduler.  Per CTA:
-//   warp 0  scheduler + TMA producer: the item's Q rows (3-D box: head dim x
-//           G heads x B block rows, zero rows up to 128) and 64-key K/V tiles
-//           of the context cache, then one tile of the block's own keys;
-//   warp 1  MMA issuer: S = Q K^T (M = 128 padded query rows, N = 64 keys,
+//   warp 0  lane 0: scheduler + TMA producer of the item's Q rows (3-D box:
+//           head dim x G heads x B block rows, zero rows up to 128) and its
+//           64-key K tiles (context cache, then one tile of the block's own
+//           keys); lane 1: TMA producer of the matching V tiles.  K and V have
+//           rings of their own, so a K slot is refilled as soon as S has read
+//           it while its V waits for the P V product;
+//   warp 1  MMA issuer: S = Q K^T (M = 64 or 128 padded query rows, N = 64 keys,
 //           K = hd) into a double-buffered TMEM tile, then O += P V (K = 64
 //           keys, N = hd; P read from TMEM, V read MN-major straight from its
 //           TMA tile) into a TMEM accumulator, each issued as soon as its
@@ -29,10 +32,9 @@
 //           first half of the tile's own S columns (the A operand of P V), and
 //           the item's epilogue (bf16 output, or fp32 partial + log-sum-exp
 //           when the sequence's keys span several items).
-// When both pipelines' query rows fit in 64 MMA rows each, they share one Q
-// buffer (pipeline 0's rows in MMA rows 64..127, pipeline 1's in 0..63: each
-// pipeline's MMA reads the other's rows as its padding rows, whose results are
-// never used), and the shared memory saved goes to deeper K/V rings.
+// When an item has at most 64 query rows the products run with M = 64: half
+// the tensor-pipe time of M = 128 on padding rows, and half the Q buffer, so
+// the shared memory saved goes to deeper K/V rings.
 // A combine kernel merges the partials of multi-item sequences.
 #include "internal.h"
 #include "small_kernels.h"
@@ -45,6 +47,7 @@ constexpr int AT_KT = 64;           // keys per tile
 constexpr int AT_M = 128;           // MMA rows (query rows, zero-padded)
 constexpr float AT_LAZY = 8.f;      // rescale O only when a row max grows by more than this (log2 units)
 constexpr int AT_IRING = 4;         // scheduled items in flight between the warps
+static_assert((AT_IRING & (AT_IRING - 1)) == 0, "ring positions are masked");
 
 struct AtArgs {
     int N, B, Hq, Hkv, G, R;
@@ -62,21 +65,30 @@ struct AtArgs {
     float scale_log2;         // log2(e) / sqrt(hd)
 };
 
-template <int HD, bool SHQ>
+// MM: rows of the MMAs (64 when an item has at most 64 query rows, else 128).
+// An M = 64 product puts row m in TMEM lane 32 (m / 16) + m % 16: the first
+// 16 lanes of each warp's quadrant (the same for P read back as its A operand).
+template <int HD, int MM>
 struct AtCfg {
     static constexpr int NP = 2;                       // independent pipelines per CTA (two items in flight)
     static constexpr int KB = HD / 64;                 // 64-element K-blocks of a head row
-    static constexpr int Q_BYTES = AT_M * HD * 2;      // one Q buffer
-    static constexpr int QKB_BYTES = AT_M * 128;       // one K-block of Q (128 rows x 128 B)
+    static constexpr int Q_BYTES = MM * HD * 2;        // one Q buffer
+    static constexpr int QKB_BYTES = MM * 128;         // one K-block of Q (MM rows x 128 B)
     static constexpr int T_BYTES = AT_KT * HD * 2;     // one K or V tile
     static constexpr int TKB_BYTES = AT_KT * 128;      // one K-block of a K/V tile
     static constexpr int NQB = 1;                      // Q buffers per pipeline
-    static constexpr int NSB = 2;                      // S (and P) buffers in TMEM per pipeline
-    static constexpr int Q_TOTAL = SHQ ? Q_BYTES : NP * Q_BYTES;
-    static constexpr int STAGES = HD == 128 ? (SHQ ? 3 : 2) : 6;   // K/V stages per pipeline
-    static constexpr int RING_BYTES = STAGES * 2 * T_BYTES;
+    // S (and P) buffers in TMEM per pipeline: a third one, where the columns
+    // allow it, lets S run a tile further ahead of the softmax
+    static constexpr int NSB = HD == 64 ? 3 : 2;
+    static constexpr int Q_TOTAL = NP * Q_BYTES;
+    // K and V tiles have rings of their own: a K slot is free again once S has
+    // read it, a V slot only after the P V product
+    static constexpr int KST = HD == 128 ? (MM == 64 ? 3 : 2) : 6;    // K slots per pipeline
+    static constexpr int VST = KST;                                     // V slots per pipeline
+    static constexpr int RING_BYTES = (KST + VST) * T_BYTES;
     static constexpr int O_COL = NSB * AT_KT;          // per pipeline: S buffers from column 0, O after them
     static constexpr int PIPE_COLS = 256;              // TMEM columns per pipeline
+    static_assert(O_COL + HD <= PIPE_COLS, "TMEM columns");
     static constexpr int TMEM_COLS = NP * PIPE_COLS;
     static constexpr int THREADS = NP * 192;
     static constexpr int BAR_BYTES = 512;              // barriers and scheduler slots per pipeline
@@ -128,9 +140,10 @@ __device__ __forceinline__ void at_tile_range(const AtItem& x, int t, int& v0, i
 }
 
 // Barriers and scheduler slots of one pipeline.
-template <int ST, int NQB, int NSB>
+template <int KST, int VST, int NQB, int NSB>
 struct AtBars {
-    uint64_t kv_full[ST], kv_empty[ST];
+    uint64_t k_full[KST], k_empty[KST];   // k_empty: S has read the slot
+    uint64_t v_full[VST], v_empty[VST];   // v_empty: P V has read the slot
     uint64_t q_full[NQB], q_empty[NQB];
     uint64_t s_full[NSB], s_empty[NSB];   // s_empty: the P V product that read the buffer's P is done
     uint64_t p_full[NSB];                 // P of the buffer written by all 128 softmax threads
@@ -141,14 +154,23 @@ struct AtBars {
     int abort_flag;
 };
 
-template <int HD, bool SHQ>
-__global__ void __launch_bounds__(AtCfg<HD, SHQ>::THREADS, 1)
+// Position in a ring of N slots and the phase parity of its current use.
+template <int N>
+struct AtRing {
+    uint32_t i = 0, ph = 0;
+    __device__ __forceinline__ void step() {
+        if (++i == N) { i = 0; ph ^= 1u; }
+    }
+};
+
+template <int HD, int MM>
+__global__ void __launch_bounds__(AtCfg<HD, MM>::THREADS, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmKc,
                const __grid_constant__ CUtensorMap tmVc, const __grid_constant__ CUtensorMap tmKb,
                const __grid_constant__ CUtensorMap tmVb, const AtArgs a, const DevErr err) {
-    using Cfg = AtCfg<HD, SHQ>;
-    constexpr int ST = Cfg::STAGES, NQB = Cfg::NQB, NSB = Cfg::NSB;
-    using Bars = AtBars<ST, NQB, NSB>;
+    using Cfg = AtCfg<HD, MM>;
+    constexpr int KST = Cfg::KST, VST = Cfg::VST, NQB = Cfg::NQB, NSB = Cfg::NSB;
+    using Bars = AtBars<KST, VST, NQB, NSB>;
     static_assert(sizeof(Bars) + 8 <= Cfg::BAR_BYTES, "barrier area");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -158,23 +180,21 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int pp = warp / 6;          // this warp's pipeline
     const int role = warp % 6;        // 0 producer, 1 MMA, 2..5 softmax
-    uint8_t* sQ = sm + (SHQ ? 0 : pp * Cfg::Q_BYTES);                   // this pipeline's Q buffer
-    uint8_t* sKV = sm + Cfg::Q_TOTAL + pp * Cfg::RING_BYTES;             // [ST][K tile, V tile]
+    uint8_t* sQ = sm + pp * Cfg::Q_BYTES;                                // this pipeline's Q buffer
+    uint8_t* sK = sm + Cfg::Q_TOTAL + pp * Cfg::RING_BYTES;              // [KST] K tiles
+    uint8_t* sV = sK + KST * Cfg::T_BYTES;                               // [VST] V tiles
     Bars& bb = *reinterpret_cast<Bars*>(bar_base + pp * Cfg::BAR_BYTES);
     volatile int* abort_flag = &bb.abort_flag;
-    // For R <= 64 the query rows of pipeline 0 sit in MMA rows 64..127 and those
-    // of pipeline 1 in rows 0..63, so the active softmax warps of the two
-    // pipelines use all four TMEM lane quadrants (SM sub-partitions).
-    const int rb = a.R <= 64 ? (pp == 0 ? 64 : 0) : 0;
 
     if ((threadIdx.x % 192) == 0) {
-        for (int s = 0; s < ST; ++s) { mbar_init(&bb.kv_full[s], 1); mbar_init(&bb.kv_empty[s], 1); }
+        for (int s = 0; s < KST; ++s) { mbar_init(&bb.k_full[s], 1); mbar_init(&bb.k_empty[s], 1); }
+        for (int s = 0; s < VST; ++s) { mbar_init(&bb.v_full[s], 1); mbar_init(&bb.v_empty[s], 1); }
         for (int b = 0; b < NQB; ++b) { mbar_init(&bb.q_full[b], 1); mbar_init(&bb.q_empty[b], 1); }
         for (int b = 0; b < NSB; ++b) {
             mbar_init(&bb.s_full[b], 1); mbar_init(&bb.s_empty[b], 1); mbar_init(&bb.p_full[b], 128);
         }
         mbar_init(&bb.o_full, 1); mbar_init(&bb.o_empty, 128);
-        for (int r = 0; r < AT_IRING; ++r) { mbar_init(&bb.i_full[r], 1); mbar_init(&bb.i_empty[r], 1 + 4); }
+        for (int r = 0; r < AT_IRING; ++r) { mbar_init(&bb.i_full[r], 1); mbar_init(&bb.i_empty[r], 1 + 1 + 4); }
         mbar_init(&bb.drain, 1);
         bb.abort_flag = 0;
         fence_barrier_init();
@@ -195,9 +215,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
 
     if (role == 0) {
         if (lane == 0) {
-            // ------------------------------------------ scheduler + TMA producer
+            // ---------------------------------------- scheduler + TMA producer of Q and K
             int icount = 0, tcount = 0;
-            uint32_t kv_fills = 0;
+            uint32_t k_fills = 0;
             bool aborted = false;
             while (true) {
                 int it = -1;
@@ -217,24 +237,20 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                 mbar_arrive_expect_tx(&bb.q_full[qb], a.R * HD * 2);
                 #pragma unroll
                 for (int kb = 0; kb < Cfg::KB; ++kb)
-                    tma_load_3d(sQ + qb * Cfg::Q_BYTES + kb * Cfg::QKB_BYTES + rb * 128, &tmQ, kb * 64,
+                    tma_load_3d(sQ + qb * Cfg::Q_BYTES + kb * Cfg::QKB_BYTES, &tmQ, kb * 64,
                                 x.g * a.G + x.h * a.Gq, x.n * a.B, &bb.q_full[qb]);
                 const int nt = x.nctx + x.blk;
                 for (int t = 0; t < nt && !aborted; ++t) {
-                    const int s = tcount % ST;
-                    if (*abort_flag || !mbar_wait(&bb.kv_empty[s], ((tcount / ST) & 1) ^ 1, err)) { aborted = true; break; }
-                    mbar_arrive_expect_tx(&bb.kv_full[s], 2 * Cfg::T_BYTES);
-                    uint8_t* dK = sKV + s * 2 * Cfg::T_BYTES;
-                    uint8_t* dV = dK + Cfg::T_BYTES;
+                    const int s = tcount % KST;
+                    if (*abort_flag || !mbar_wait(&bb.k_empty[s], ((tcount / KST) & 1) ^ 1, err)) { aborted = true; break; }
+                    mbar_arrive_expect_tx(&bb.k_full[s], Cfg::T_BYTES);
                     const bool ctx = t < x.nctx;
                     const int row = ctx ? x.n * a.C_stride + x.lo + t * AT_KT : x.n * a.B;
                     #pragma unroll
-                    for (int kb = 0; kb < Cfg::KB; ++kb) {
-                        const int col = x.g * HD + kb * 64;
-                        tma_load_2d(dK + kb * Cfg::TKB_BYTES, ctx ? &tmKc : &tmKb, col, row, &bb.kv_full[s]);
-                        tma_load_2d(dV + kb * Cfg::TKB_BYTES, ctx ? &tmVc : &tmVb, col, row, &bb.kv_full[s]);
-                    }
-                    kv_fills |= 1u << s;
+                    for (int kb = 0; kb < Cfg::KB; ++kb)
+                        tma_load_2d(sK + s * Cfg::T_BYTES + kb * Cfg::TKB_BYTES, ctx ? &tmKc : &tmKb, x.g * HD + kb * 64,
+                                    row, &bb.k_full[s]);
+                    k_fills |= 1u << s;
                     ++tcount;
                 }
                 if (aborted) break;
@@ -243,16 +259,55 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
             if (aborted) {
                 *abort_flag = 1;
                 // let issued copies land before the CTA exits: the latest fill of
-                // each buffer has the parity of its fill count
-                for (int s = 0; s < ST; ++s) {
-                    if (!(kv_fills & (1u << s))) continue;
-                    const int last = tcount - 1 - ((tcount - 1 - s) % ST + ST) % ST;   // latest tile using stage s
-                    mbar_wait(&bb.kv_full[s], (last / ST) & 1, err);
+                // each slot has the parity of its fill count
+                for (int s = 0; s < KST; ++s) {
+                    if (!(k_fills & (1u << s))) continue;
+                    const int last = tcount - 1 - ((tcount - 1 - s) % KST + KST) % KST;   // latest tile using slot s
+                    mbar_wait(&bb.k_full[s], (last / KST) & 1, err);
                 }
                 // the Q load of the item being filled (icount) has been issued
                 for (int b = 0; b < NQB; ++b) {
                     const int last = icount - ((icount - b) % NQB + NQB) % NQB;
                     if (last >= 0) mbar_wait(&bb.q_full[b], (last / NQB) & 1, err);
+                }
+            }
+        } else if (lane == 1) {
+            // ------------------------------------------------- TMA producer of V
+            // follows the scheduled items like the consumers, as far ahead as the V ring allows
+            int icount = 0, tcount = 0;
+            uint32_t v_fills = 0;
+            bool aborted = false;
+            while (true) {
+                const int r = icount % AT_IRING;
+                if (*abort_flag || !mbar_wait(&bb.i_full[r], (icount / AT_IRING) & 1, err)) { aborted = true; break; }
+                const int it = bb.i_ring[r];
+                mbar_arrive(&bb.i_empty[r]);
+                if (it < 0) break;
+                AtItem x;
+                at_decode(a, it, x);
+                const int nt = x.nctx + x.blk;
+                for (int t = 0; t < nt && !aborted; ++t) {
+                    const int s = tcount % VST;
+                    if (*abort_flag || !mbar_wait(&bb.v_empty[s], ((tcount / VST) & 1) ^ 1, err)) { aborted = true; break; }
+                    mbar_arrive_expect_tx(&bb.v_full[s], Cfg::T_BYTES);
+                    const bool ctx = t < x.nctx;
+                    const int row = ctx ? x.n * a.C_stride + x.lo + t * AT_KT : x.n * a.B;
+                    #pragma unroll
+                    for (int kb = 0; kb < Cfg::KB; ++kb)
+                        tma_load_2d(sV + s * Cfg::T_BYTES + kb * Cfg::TKB_BYTES, ctx ? &tmVc : &tmVb, x.g * HD + kb * 64,
+                                    row, &bb.v_full[s]);
+                    v_fills |= 1u << s;
+                    ++tcount;
+                }
+                if (aborted) break;
+                ++icount;
+            }
+            if (aborted) {
+                *abort_flag = 1;
+                for (int s = 0; s < VST; ++s) {
+                    if (!(v_fills & (1u << s))) continue;
+                    const int last = tcount - 1 - ((tcount - 1 - s) % VST + VST) % VST;
+                    mbar_wait(&bb.v_full[s], (last / VST) & 1, err);
                 }
             }
         }
@@ -262,51 +317,64 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
             // Event loop: issue whichever product is ready, S = Q K^T of the
             // next tile (its K/V landed, an S buffer free) or O += P V of the
             // oldest tile whose P is written, so that neither waits on the
-            // other's inputs.  Tiles are numbered per pipeline; meta[] keeps,
+            // other's inputs.  Tiles are numbered per pipeline; `meta` keeps,
             // for tiles whose S is issued and whose P V is not, whether they
-            // open / close their item and the item's number.
-            constexpr uint32_t idesc_s = idesc_bf16(AT_M, AT_KT);
-            constexpr uint32_t idesc_o = idesc_bf16_bmn(AT_M, HD);
+            // open / close their item and the parity of the item's number: 4
+            // bits per tile in one register (an indexed array would live in
+            // local memory, whose loads queue behind this SM's TMA traffic).
+            // The loop is one thread's serial chain, so ring positions and phases are
+            // stepped incrementally (no division by the ring sizes) and the barrier
+            // tests of one decision are issued together before they are used.
+            constexpr uint32_t idesc_s = idesc_bf16(MM, AT_KT);
+            constexpr uint32_t idesc_o = idesc_bf16_bmn(MM, HD);
             constexpr int META = 16;
-            static_assert(META >= ST + NSB + 1, "tiles in flight between S and P V");
-            struct TileMeta { int8_t first, last; int icount; };
-            TileMeta meta[META];
+            static_assert(META >= KST + NSB + 1, "tiles in flight between S and P V");
+            constexpr uint32_t M_FIRST = 1, M_LAST = 2, M_ODD = 4;
+            uint64_t meta = 0;
             int tcs = 0, tcp = 0;                 // tiles with S issued, with P V issued
             int icount = 0, t_in = 0, nt = 0;     // the S side's current item, its next tile, its tiles
-            int qb = 0;
-            uint32_t qaddr = 0;
+            AtRing<KST> ks;                       // K slot of tile tcs
+            AtRing<NSB> sb;                       // S buffer of tile tcs
+            AtRing<NSB> pb;                       // S / P buffer of tile tcp
+            AtRing<VST> vs;                       // V slot of tile tcp
+            const uint32_t sK32 = smem_u32(sK), sV32 = smem_u32(sV), qaddr = smem_u32(sQ);
             bool have_item = false, q_ready = false, items_done = false;
             bool aborted = false, issued = false;
-            uint64_t t_idle = globaltimer_ns();
+            // timeout of an idle stretch: the timer is read on every 8th idle pass
+            uint64_t t_idle = 0;
+            uint32_t nidle = 0;
+            static_assert(NQB == 1, "one Q buffer per pipeline");
             while (true) {
                 bool prog = false;
                 // P V of the oldest tile whose S is issued
                 if (tcp < tcs) {
-                    const TileMeta m = meta[tcp % META];
-                    const int b = tcp % NSB;
-                    if (mbar_test(&bb.p_full[b], (tcp / NSB) & 1) &&
-                        (!m.first || mbar_test(&bb.o_empty, (m.icount & 1) ^ 1))) {
+                    const uint32_t m = (uint32_t)(meta >> (4 * (tcp & (META - 1)))) & 0xFu;
+                    const bool p_ok = mbar_test(&bb.p_full[pb.i], pb.ph);
+                    const bool v_ok = mbar_test(&bb.v_full[vs.i], vs.ph);
+                    const bool o_ok = !(m & M_FIRST) || mbar_test(&bb.o_empty, ((m & M_ODD) ? 1u : 0u) ^ 1u);
+                    if (p_ok && v_ok && o_ok) {
                         tc_fence_after();
-                        const int s = tcp % ST;
-                        const uint32_t vaddr = smem_u32(sKV + s * 2 * Cfg::T_BYTES + Cfg::T_BYTES);
-                        // P (bf16, 2 per column) sits in the first 32 columns of S buffer b:
+                        const uint32_t vaddr = sV32 + vs.i * Cfg::T_BYTES;
+                        // P (bf16, 2 per column) sits in the first 32 columns of S buffer pb:
                         // 16 keys per MMA = 8 columns
                         #pragma unroll
                         for (int j = 0; j < AT_KT / 16; ++j)
-                            mma_bf16_ts(tmem_base + Cfg::O_COL, tmem_base + b * AT_KT + 8 * j,
+                            mma_bf16_ts(tmem_base + Cfg::O_COL, tmem_base + pb.i * AT_KT + 8 * j,
                                         sw128_desc_mn(vaddr + j * 16 * 128, Cfg::TKB_BYTES, 1024), idesc_o,
-                                        (m.first && j == 0) ? 0 : 1);
+                                        ((m & M_FIRST) && j == 0) ? 0 : 1);
                         issued = true;
-                        mma_commit(&bb.kv_empty[s]);
-                        mma_commit(&bb.s_empty[b]);
-                        if (m.last) mma_commit(&bb.o_full);
+                        mma_commit(&bb.v_empty[vs.i]);
+                        mma_commit(&bb.s_empty[pb.i]);
+                        if (m & M_LAST) mma_commit(&bb.o_full);
+                        pb.step();
+                        vs.step();
                         ++tcp;
                         prog = true;
                     }
                 }
                 // the next item of the S side
                 if (!have_item && !items_done) {
-                    const int r = icount % AT_IRING;
+                    const int r = icount & (AT_IRING - 1);
                     if (mbar_test(&bb.i_full[r], (icount / AT_IRING) & 1)) {
                         const int it = bb.i_ring[r];
                         mbar_arrive(&bb.i_empty[r]);
@@ -317,33 +385,39 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                             at_decode(a, it, x);
                             nt = x.nctx + x.blk;
                             t_in = 0;
-                            qb = icount % NQB;
-                            qaddr = smem_u32(sQ + qb * Cfg::Q_BYTES);
                             have_item = true;
                             q_ready = false;
                         }
                         prog = true;
                     }
                 }
-                if (have_item && !q_ready && mbar_test(&bb.q_full[qb], (icount / NQB) & 1)) { q_ready = true; prog = true; }
+                if (have_item && !q_ready && mbar_test(&bb.q_full[0], icount & 1)) { q_ready = true; prog = true; }
                 // S of the next tile
                 if (have_item && q_ready) {
-                    const int s = tcs % ST, b = tcs % NSB;
-                    if (mbar_test(&bb.kv_full[s], (tcs / ST) & 1) && mbar_test(&bb.s_empty[b], ((tcs / NSB) & 1) ^ 1)) {
+                    const bool k_ok = mbar_test(&bb.k_full[ks.i], ks.ph);
+                    const bool s_ok = mbar_test(&bb.s_empty[sb.i], sb.ph ^ 1);
+                    if (k_ok && s_ok) {
                         tc_fence_after();
-                        const uint32_t kaddr = smem_u32(sKV + s * 2 * Cfg::T_BYTES);
+                        const uint32_t kaddr = sK32 + ks.i * Cfg::T_BYTES;
                         #pragma unroll
                         for (int j = 0; j < HD / 16; ++j)
-                            mma_bf16(tmem_base + b * AT_KT, sw128_desc(qaddr + (j >> 2) * Cfg::QKB_BYTES + (j & 3) * 32),
+                            mma_bf16(tmem_base + sb.i * AT_KT, sw128_desc(qaddr + (j >> 2) * Cfg::QKB_BYTES + (j & 3) * 32),
                                      sw128_desc(kaddr + (j >> 2) * Cfg::TKB_BYTES + (j & 3) * 32), idesc_s, j > 0);
                         issued = true;
-                        mma_commit(&bb.s_full[b]);
-                        meta[tcs % META] = TileMeta{(int8_t)(t_in == 0), (int8_t)(t_in == nt - 1), icount};
-                        if (t_in == nt - 1) {
-                            mma_commit(&bb.q_empty[qb]);
+                        mma_commit(&bb.k_empty[ks.i]);
+                        mma_commit(&bb.s_full[sb.i]);
+                        const int sh = 4 * (tcs & (META - 1));
+                        const bool last = t_in == nt - 1;
+                        meta = (meta & ~(0xFull << sh)) |
+                               ((uint64_t)((t_in == 0 ? M_FIRST : 0u) | (last ? M_LAST : 0u) | ((icount & 1) ? M_ODD : 0u))
+                                << sh);
+                        if (last) {
+                            mma_commit(&bb.q_empty[0]);
                             have_item = false;
                             ++icount;
                         }
+                        ks.step();
+                        sb.step();
                         ++t_in;
                         ++tcs;
                         prog = true;
@@ -351,23 +425,32 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                 }
                 if (items_done && tcp == tcs) break;
                 if (prog) {
-                    t_idle = globaltimer_ns();
+                    nidle = 0;
                     continue;
                 }
                 // Nothing ready: suspend on the barrier of the event most likely next
-                // (P of the oldest pending tile, else the next K/V tile, Q or item) rather
-                // than spin, since a softmax warp shares this SM sub-partition; it wakes
+                // (P, then V, of the oldest pending tile, else the next K tile, Q or item) rather
+                // than spin, since softmax warps share this SM sub-partition; it wakes
                 // as soon as that phase completes, and the loop then tests everything.
                 if (tcp < tcs) {
-                    mbar_try_wait_for(&bb.p_full[tcp % NSB], (tcp / NSB) & 1, 2000);
+                    if (mbar_test(&bb.p_full[pb.i], pb.ph))
+                        mbar_try_wait_for(&bb.v_full[vs.i], vs.ph, 2000);
+                    else
+                        mbar_try_wait_for(&bb.p_full[pb.i], pb.ph, 2000);
                 } else if (have_item && q_ready) {
-                    mbar_try_wait_for(&bb.kv_full[tcs % ST], (tcs / ST) & 1, 2000);
+                    mbar_try_wait_for(&bb.k_full[ks.i], ks.ph, 2000);
                 } else if (have_item) {
-                    mbar_try_wait_for(&bb.q_full[qb], (icount / NQB) & 1, 2000);
+                    mbar_try_wait_for(&bb.q_full[0], icount & 1, 2000);
                 } else if (!items_done) {
-                    mbar_try_wait_for(&bb.i_full[icount % AT_IRING], (icount / AT_IRING) & 1, 2000);
+                    mbar_try_wait_for(&bb.i_full[icount & (AT_IRING - 1)], (icount / AT_IRING) & 1, 2000);
                 }
-                if (*abort_flag || globaltimer_ns() - t_idle > err.limit_ns) {
+                bool late = false;
+                if ((nidle++ & 7u) == 0) {
+                    const uint64_t now = globaltimer_ns();
+                    if (nidle == 1) t_idle = now;
+                    else late = now - t_idle > err.limit_ns;
+                }
+                if (*abort_flag || late) {
                     if (!*abort_flag) record_error(err, DFL_ERR_TIMEOUT);
                     aborted = true;
                     break;
@@ -384,9 +467,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     } else {
         // ------------------------------- softmax + epilogue: one row per thread
         const int q4 = warp & 3;
-        const int lrow = q4 * 32 + lane;                     // TMEM lane = MMA row
-        const int row = lrow - rb;                           // query row of the item (R of them)
-        const bool pad = q4 * 32 + 32 <= rb || q4 * 32 >= rb + a.R;   // warp holds padding rows only
+        // query row of the item held by this thread's TMEM lane (R of them; others are padding)
+        const int row = MM == 64 ? (lane < 16 ? 16 * q4 + lane : -1) : q4 * 32 + lane;
+        const bool pad = (MM == 64 ? 16 : 32) * q4 >= a.R;   // warp-uniform: padding rows only
+        const bool live = MM == 128 || lane < 16;            // this lane holds an MMA row (maybe padding)
         const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
         const int stid = threadIdx.x - pp * 192 - 64;        // 0..127 within the pipeline's softmax warps
         int icount = 0, tcount = 0;
@@ -430,7 +514,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                 if (t == 0) {
                     m_run = mt;
                 } else {
-                    const bool need = mt > m_run + AT_LAZY;
+                    const bool need = live && mt > m_run + AT_LAZY;
                     if (__any_sync(0xFFFFFFFFu, need)) {
                         // O of this item holds the P V products up to the previous tile: wait for the last one
                         const int tp = tcount - 1;
@@ -472,11 +556,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                 // Rows of the V tile outside [v0, v1) may hold anything (cache rows past
                 // the sequence's length): zero them, so that 0 * V adds exactly nothing.
                 if (v0 > 0 || v1 < AT_KT) {
-                    // the tile's copies have landed (its MMA has read K); the stage is not
-                    // refilled before this tile's P V product, which waits for these writes
-                    ok = mbar_wait(&bb.kv_full[tcount % ST], (tcount / ST) & 1, err);
+                    // the V tile has landed; its slot is not refilled before this
+                    // tile's P V product, which waits for these writes
+                    ok = mbar_wait(&bb.v_full[tcount % VST], (tcount / VST) & 1, err);
                     if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
-                    uint8_t* vt = sKV + (tcount % ST) * 2 * Cfg::T_BYTES + Cfg::T_BYTES;
+                    uint8_t* vt = sV + (tcount % VST) * Cfg::T_BYTES;
                     for (int i = stid; i < AT_KT * Cfg::KB * 8; i += 128) {
                         const int kr = (i >> 3) % AT_KT;
                         if (kr >= v0 && kr < v1) continue;
@@ -724,14 +808,14 @@ dfl_status attn_tc(const void* Q, const void* Kc, const void* Vc, const void* Kb
             kern<<<grid, threads, smem, st>>>(mq, mkc, mvc, mkb, mvb, a, err);
             return last_launch();
         };
-        // the two pipelines share one Q buffer when each item has at most 64 query rows
-        const bool shq = a.R <= 64;
+        // M = 64 products when each item has at most 64 query rows
+        const bool m64 = a.R <= 64;
         if (hd == 128)
-            rc = shq ? run(attn_tc_kernel<128, true>, AtCfg<128, true>::SMEM, AtCfg<128, true>::THREADS, 3)
-                     : run(attn_tc_kernel<128, false>, AtCfg<128, false>::SMEM, AtCfg<128, false>::THREADS, 1);
+            rc = m64 ? run(attn_tc_kernel<128, 64>, AtCfg<128, 64>::SMEM, AtCfg<128, 64>::THREADS, 3)
+                     : run(attn_tc_kernel<128, 128>, AtCfg<128, 128>::SMEM, AtCfg<128, 128>::THREADS, 1);
         else
-            rc = shq ? run(attn_tc_kernel<64, true>, AtCfg<64, true>::SMEM, AtCfg<64, true>::THREADS, 2)
-                     : run(attn_tc_kernel<64, false>, AtCfg<64, false>::SMEM, AtCfg<64, false>::THREADS, 0);
+            rc = m64 ? run(attn_tc_kernel<64, 64>, AtCfg<64, 64>::SMEM, AtCfg<64, 64>::THREADS, 2)
+                     : run(attn_tc_kernel<64, 128>, AtCfg<64, 128>::SMEM, AtCfg<64, 128>::THREADS, 0);
     }
     if (rc != DFL_OK || a.S == 1) return rc;
     ProfScope ps("attn_combine", st);

@@ -6,8 +6,9 @@
 `mix` runs dfl_layer_mix_rmsnorm on H[L][rows][d] (rows = N * C unless
 --rows is given); `attn` runs dfl_block_attn (attention and output
 projection) on the workload's N, C, B, heads and head dim.  Inputs are
-random bf16 tensors on the device; a 256 MB buffer is written between
-launches so the inputs come from HBM.  Prints one JSON line with the
+random bf16 tensors on the device; between launches a 256 MB buffer is
+written and another read, so the inputs come from HBM and no dirty line of
+the flush is written back during the timed launch.  Prints one JSON line with the
 library's own per-kernel trace (CUDA events around each launch), in µs per
 launch, and the achieved bandwidth of the main kernel.  Two untimed launches
 come first, so under a profiler `-s 2 -c 1` selects a warm launch.
@@ -33,14 +34,22 @@ def _peak_gbs() -> float:
         return 6800.0
 
 
+def _flush(w: torch.Tensor, r: torch.Tensor) -> None:
+    # write one buffer larger than L2, then read another: the read evicts the
+    # dirty lines, so their write-back does not land in the timed launch
+    w.zero_()
+    r.sum()
+
+
 def _timed(call, iters: int) -> dict:
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    w = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    r = torch.ones(64 << 20, dtype=torch.int32, device="cuda")
     for _ in range(2):
         call()
     torch.cuda.synchronize()
     dfl.dfl_profile_enable(True)
     for _ in range(iters):
-        flush.zero_()
+        _flush(w, r)
         call()
     torch.cuda.synchronize()
     dfl.dfl_profile_enable(False)
