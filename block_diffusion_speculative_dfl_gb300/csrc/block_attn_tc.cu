@@ -85,6 +85,7 @@ struct AtCfg {
     // read it, a V slot only after the P V product
     static constexpr int KST = HD == 128 ? (MM == 64 ? 3 : 2) : 6;    // K slots per pipeline
     static constexpr int VST = KST;                                     // V slots per pipeline
+    static_assert(KST >= NSB && VST >= NSB, "completion barriers are shared by the K / V slots and S buffers");
     static constexpr int RING_BYTES = (KST + VST) * T_BYTES;
     static constexpr int O_COL = NSB * AT_KT;          // per pipeline: S buffers from column 0, O after them
     static constexpr int PIPE_COLS = 256;              // TMEM columns per pipeline
@@ -142,10 +143,15 @@ __device__ __forceinline__ void at_tile_range(const AtItem& x, int t, int& v0, i
 // Barriers and scheduler slots of one pipeline.
 template <int KST, int VST, int NQB, int NSB>
 struct AtBars {
-    uint64_t k_full[KST], k_empty[KST];   // k_empty: S has read the slot
-    uint64_t v_full[VST], v_empty[VST];   // v_empty: P V has read the slot
+    // One completion barrier per product and slot: s_done[t % KST] completes when
+    // S of tile t is done (its K slot is free, its S is ready for the softmax);
+    // pv_done[t % VST] when P V of tile t is done (its V slot and S buffer are
+    // free, O holds it).  A waiter for tile t's phase always knows that the
+    // slot's previous phase (tile t - ring size) has completed, so the parity
+    // test cannot mistake it.
+    uint64_t k_full[KST], s_done[KST];
+    uint64_t v_full[VST], pv_done[VST];
     uint64_t q_full[NQB], q_empty[NQB];
-    uint64_t s_full[NSB], s_empty[NSB];   // s_empty: the P V product that read the buffer's P is done
     uint64_t p_full[NSB];                 // P of the buffer written by all 128 softmax threads
     uint64_t o_full, o_empty;
     uint64_t i_full[AT_IRING], i_empty[AT_IRING];
@@ -187,12 +193,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     volatile int* abort_flag = &bb.abort_flag;
 
     if ((threadIdx.x % 192) == 0) {
-        for (int s = 0; s < KST; ++s) { mbar_init(&bb.k_full[s], 1); mbar_init(&bb.k_empty[s], 1); }
-        for (int s = 0; s < VST; ++s) { mbar_init(&bb.v_full[s], 1); mbar_init(&bb.v_empty[s], 1); }
+        for (int s = 0; s < KST; ++s) { mbar_init(&bb.k_full[s], 1); mbar_init(&bb.s_done[s], 1); }
+        for (int s = 0; s < VST; ++s) { mbar_init(&bb.v_full[s], 1); mbar_init(&bb.pv_done[s], 1); }
         for (int b = 0; b < NQB; ++b) { mbar_init(&bb.q_full[b], 1); mbar_init(&bb.q_empty[b], 1); }
-        for (int b = 0; b < NSB; ++b) {
-            mbar_init(&bb.s_full[b], 1); mbar_init(&bb.s_empty[b], 1); mbar_init(&bb.p_full[b], 128);
-        }
+        for (int b = 0; b < NSB; ++b) mbar_init(&bb.p_full[b], 128);
         mbar_init(&bb.o_full, 1); mbar_init(&bb.o_empty, 128);
         for (int r = 0; r < AT_IRING; ++r) { mbar_init(&bb.i_full[r], 1); mbar_init(&bb.i_empty[r], 1 + 1 + 4); }
         mbar_init(&bb.drain, 1);
@@ -242,7 +246,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                 const int nt = x.nctx + x.blk;
                 for (int t = 0; t < nt && !aborted; ++t) {
                     const int s = tcount % KST;
-                    if (*abort_flag || !mbar_wait(&bb.k_empty[s], ((tcount / KST) & 1) ^ 1, err)) { aborted = true; break; }
+                    if (*abort_flag || !mbar_wait(&bb.s_done[s], ((tcount / KST) & 1) ^ 1, err)) { aborted = true; break; }
                     mbar_arrive_expect_tx(&bb.k_full[s], Cfg::T_BYTES);
                     const bool ctx = t < x.nctx;
                     const int row = ctx ? x.n * a.C_stride + x.lo + t * AT_KT : x.n * a.B;
@@ -288,7 +292,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                 const int nt = x.nctx + x.blk;
                 for (int t = 0; t < nt && !aborted; ++t) {
                     const int s = tcount % VST;
-                    if (*abort_flag || !mbar_wait(&bb.v_empty[s], ((tcount / VST) & 1) ^ 1, err)) { aborted = true; break; }
+                    if (*abort_flag || !mbar_wait(&bb.pv_done[s], ((tcount / VST) & 1) ^ 1, err)) { aborted = true; break; }
                     mbar_arrive_expect_tx(&bb.v_full[s], Cfg::T_BYTES);
                     const bool ctx = t < x.nctx;
                     const int row = ctx ? x.n * a.C_stride + x.lo + t * AT_KT : x.n * a.B;
@@ -335,6 +339,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
             int icount = 0, t_in = 0, nt = 0;     // the S side's current item, its next tile, its tiles
             AtRing<KST> ks;                       // K slot of tile tcs
             AtRing<NSB> sb;                       // S buffer of tile tcs
+            AtRing<VST> pe;                       // V slot of tile tcs - NSB (whose P V frees sb)
             AtRing<NSB> pb;                       // S / P buffer of tile tcp
             AtRing<VST> vs;                       // V slot of tile tcp
             const uint32_t sK32 = smem_u32(sK), sV32 = smem_u32(sV), qaddr = smem_u32(sQ);
@@ -363,8 +368,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                                         sw128_desc_mn(vaddr + j * 16 * 128, Cfg::TKB_BYTES, 1024), idesc_o,
                                         ((m & M_FIRST) && j == 0) ? 0 : 1);
                         issued = true;
-                        mma_commit(&bb.v_empty[vs.i]);
-                        mma_commit(&bb.s_empty[pb.i]);
+                        mma_commit(&bb.pv_done[vs.i]);
                         if (m & M_LAST) mma_commit(&bb.o_full);
                         pb.step();
                         vs.step();
@@ -395,7 +399,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                 // S of the next tile
                 if (have_item && q_ready) {
                     const bool k_ok = mbar_test(&bb.k_full[ks.i], ks.ph);
-                    const bool s_ok = mbar_test(&bb.s_empty[sb.i], sb.ph ^ 1);
+                    // S buffer sb is free once P V of tile tcs - NSB is done; that product
+                    // must have been issued first (then the V slot's previous phase is done)
+                    const bool s_ok = tcs < NSB || (tcp > tcs - NSB && mbar_test(&bb.pv_done[pe.i], pe.ph));
                     if (k_ok && s_ok) {
                         tc_fence_after();
                         const uint32_t kaddr = sK32 + ks.i * Cfg::T_BYTES;
@@ -404,8 +410,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                             mma_bf16(tmem_base + sb.i * AT_KT, sw128_desc(qaddr + (j >> 2) * Cfg::QKB_BYTES + (j & 3) * 32),
                                      sw128_desc(kaddr + (j >> 2) * Cfg::TKB_BYTES + (j & 3) * 32), idesc_s, j > 0);
                         issued = true;
-                        mma_commit(&bb.k_empty[ks.i]);
-                        mma_commit(&bb.s_full[sb.i]);
+                        mma_commit(&bb.s_done[ks.i]);
                         const int sh = 4 * (tcs & (META - 1));
                         const bool last = t_in == nt - 1;
                         meta = (meta & ~(0xFull << sh)) |
@@ -416,6 +421,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                             have_item = false;
                             ++icount;
                         }
+                        if (tcs >= NSB) pe.step();
                         ks.step();
                         sb.step();
                         ++t_in;
@@ -489,7 +495,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
             float m_run = -INFINITY, l_run = 0.f;
             for (int t = 0; t < nt; ++t) {
                 const int b = tcount % NSB;
-                ok = mbar_wait(&bb.s_full[b], (tcount / NSB) & 1, err);
+                ok = mbar_wait(&bb.s_done[tcount % KST], (tcount / KST) & 1, err);
                 if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }   // also reconverges the warp
                 tc_fence_after();
                 int v0, v1;
@@ -518,7 +524,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                     if (__any_sync(0xFFFFFFFFu, need)) {
                         // O of this item holds the P V products up to the previous tile: wait for the last one
                         const int tp = tcount - 1;
-                        ok = mbar_wait(&bb.s_empty[tp % NSB], (tp / NSB) & 1, err);
+                        ok = mbar_wait(&bb.pv_done[tp % VST], (tp / VST) & 1, err);
                         if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
                         tc_fence_after();
                         const float m_new = need ? mt : m_run;
