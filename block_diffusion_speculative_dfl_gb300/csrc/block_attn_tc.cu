@@ -155,7 +155,7 @@ struct AtBars {
     uint64_t p_full[NSB];                 // P of the buffer written by all 128 softmax threads
     uint64_t o_full, o_empty;
     uint64_t i_full[AT_IRING], i_empty[AT_IRING];
-    uint64_t drain;
+    uint64_t drain, drain2;               // abort: the S / P V issuer's MMAs are done
     int i_ring[AT_IRING];
     int abort_flag;
 };
@@ -198,8 +198,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         for (int b = 0; b < NQB; ++b) { mbar_init(&bb.q_full[b], 1); mbar_init(&bb.q_empty[b], 1); }
         for (int b = 0; b < NSB; ++b) mbar_init(&bb.p_full[b], 128);
         mbar_init(&bb.o_full, 1); mbar_init(&bb.o_empty, 128);
-        for (int r = 0; r < AT_IRING; ++r) { mbar_init(&bb.i_full[r], 1); mbar_init(&bb.i_empty[r], 1 + 1 + 4); }
+        for (int r = 0; r < AT_IRING; ++r) { mbar_init(&bb.i_full[r], 1); mbar_init(&bb.i_empty[r], 1 + 2 + 4); }   // V producer, two MMA issuers, four softmax warps
         mbar_init(&bb.drain, 1);
+        mbar_init(&bb.drain2, 1);
         bb.abort_flag = 0;
         fence_barrier_init();
     }
@@ -316,151 +317,52 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
             }
         }
     } else if (role == 1) {
+        // Two MMA issuers, each a plain sequence of waits: lane 0 issues S = Q K^T of
+        // every tile as soon as its K has landed and its S buffer is free (up to NSB
+        // tiles ahead of the softmax); lane 1 issues O += P V of every tile as soon as
+        // its P is written and its V has landed.  Each follows the scheduled items.
+        constexpr uint32_t idesc_s = idesc_bf16(MM, AT_KT);
+        constexpr uint32_t idesc_o = idesc_bf16_bmn(MM, HD);
+        static_assert(NQB == 1, "one Q buffer per pipeline");
         if (lane == 0) {
-            // ------------------------------------------------------ MMA issuer
-            // Event loop: issue whichever product is ready, S = Q K^T of the
-            // next tile (its K/V landed, an S buffer free) or O += P V of the
-            // oldest tile whose P is written, so that neither waits on the
-            // other's inputs.  Tiles are numbered per pipeline; `meta` keeps,
-            // for tiles whose S is issued and whose P V is not, whether they
-            // open / close their item and the parity of the item's number: 4
-            // bits per tile in one register (an indexed array would live in
-            // local memory, whose loads queue behind this SM's TMA traffic).
-            // The loop is one thread's serial chain, so ring positions and phases are
-            // stepped incrementally (no division by the ring sizes) and the barrier
-            // tests of one decision are issued together before they are used.
-            constexpr uint32_t idesc_s = idesc_bf16(MM, AT_KT);
-            constexpr uint32_t idesc_o = idesc_bf16_bmn(MM, HD);
-            constexpr int META = 16;
-            static_assert(META >= KST + NSB + 1, "tiles in flight between S and P V");
-            constexpr uint32_t M_FIRST = 1, M_LAST = 2, M_ODD = 4;
-            uint64_t meta = 0;
-            int tcs = 0, tcp = 0;                 // tiles with S issued, with P V issued
-            int icount = 0, t_in = 0, nt = 0;     // the S side's current item, its next tile, its tiles
-            AtRing<KST> ks;                       // K slot of tile tcs
-            AtRing<NSB> sb;                       // S buffer of tile tcs
-            AtRing<VST> pe;                       // V slot of tile tcs - NSB (whose P V frees sb)
-            AtRing<NSB> pb;                       // S / P buffer of tile tcp
-            AtRing<VST> vs;                       // V slot of tile tcp
-            const uint32_t sK32 = smem_u32(sK), sV32 = smem_u32(sV), qaddr = smem_u32(sQ);
-            bool have_item = false, q_ready = false, items_done = false;
+            // ------------------------------------------------------ S issuer
+            AtRing<KST> ks;                       // K slot of tile tcount
+            AtRing<NSB> sb;                       // S buffer of tile tcount
+            AtRing<VST> pe;                       // V slot of tile tcount - NSB (whose P V frees sb)
+            const uint32_t sK32 = smem_u32(sK), qaddr = smem_u32(sQ);
+            int icount = 0, tcount = 0;
             bool aborted = false, issued = false;
-            // timeout of an idle stretch: the timer is read on every 8th idle pass
-            uint64_t t_idle = 0;
-            uint32_t nidle = 0;
-            static_assert(NQB == 1, "one Q buffer per pipeline");
-            while (true) {
-                bool prog = false;
-                // P V of the oldest tile whose S is issued
-                if (tcp < tcs) {
-                    const uint32_t m = (uint32_t)(meta >> (4 * (tcp & (META - 1)))) & 0xFu;
-                    const bool p_ok = mbar_test(&bb.p_full[pb.i], pb.ph);
-                    const bool v_ok = mbar_test(&bb.v_full[vs.i], vs.ph);
-                    const bool o_ok = !(m & M_FIRST) || mbar_test(&bb.o_empty, ((m & M_ODD) ? 1u : 0u) ^ 1u);
-                    if (p_ok && v_ok && o_ok) {
-                        tc_fence_after();
-                        const uint32_t vaddr = sV32 + vs.i * Cfg::T_BYTES;
-                        // P (bf16, 2 per column) sits in the first 32 columns of S buffer pb:
-                        // 16 keys per MMA = 8 columns
-                        #pragma unroll
-                        for (int j = 0; j < AT_KT / 16; ++j)
-                            mma_bf16_ts(tmem_base + Cfg::O_COL, tmem_base + pb.i * AT_KT + 8 * j,
-                                        sw128_desc_mn(vaddr + j * 16 * 128, Cfg::TKB_BYTES, 1024), idesc_o,
-                                        ((m & M_FIRST) && j == 0) ? 0 : 1);
-                        issued = true;
-                        mma_commit(&bb.pv_done[vs.i]);
-                        if (m & M_LAST) mma_commit(&bb.o_full);
-                        pb.step();
-                        vs.step();
-                        ++tcp;
-                        prog = true;
-                    }
+            while (!aborted) {
+                const int r = icount & (AT_IRING - 1);
+                if (*abort_flag || !mbar_wait(&bb.i_full[r], (icount / AT_IRING) & 1, err)) { aborted = true; break; }
+                const int it = bb.i_ring[r];
+                mbar_arrive(&bb.i_empty[r]);
+                if (it < 0) break;
+                AtItem x;
+                at_decode(a, it, x);
+                const int nt = x.nctx + x.blk;
+                if (!mbar_wait(&bb.q_full[0], icount & 1, err)) { aborted = true; break; }
+                for (int t = 0; t < nt; ++t) {
+                    // S buffer sb is free once P V of tile tcount - NSB is done; this
+                    // thread waited for P V of tile tcount - NSB - VST before issuing
+                    // S of tile tcount - VST, so the V slot's previous phase is done
+                    if (*abort_flag || !mbar_wait(&bb.k_full[ks.i], ks.ph, err) ||
+                        (tcount >= NSB && !mbar_wait(&bb.pv_done[pe.i], pe.ph, err))) { aborted = true; break; }
+                    tc_fence_after();
+                    const uint32_t kaddr = sK32 + ks.i * Cfg::T_BYTES;
+                    #pragma unroll
+                    for (int j = 0; j < HD / 16; ++j)
+                        mma_bf16(tmem_base + sb.i * AT_KT, sw128_desc(qaddr + (j >> 2) * Cfg::QKB_BYTES + (j & 3) * 32),
+                                 sw128_desc(kaddr + (j >> 2) * Cfg::TKB_BYTES + (j & 3) * 32), idesc_s, j > 0);
+                    issued = true;
+                    mma_commit(&bb.s_done[ks.i]);
+                    if (t == nt - 1) mma_commit(&bb.q_empty[0]);
+                    if (tcount >= NSB) pe.step();
+                    ks.step();
+                    sb.step();
+                    ++tcount;
                 }
-                // the next item of the S side
-                if (!have_item && !items_done) {
-                    const int r = icount & (AT_IRING - 1);
-                    if (mbar_test(&bb.i_full[r], (icount / AT_IRING) & 1)) {
-                        const int it = bb.i_ring[r];
-                        mbar_arrive(&bb.i_empty[r]);
-                        if (it < 0) {
-                            items_done = true;
-                        } else {
-                            AtItem x;
-                            at_decode(a, it, x);
-                            nt = x.nctx + x.blk;
-                            t_in = 0;
-                            have_item = true;
-                            q_ready = false;
-                        }
-                        prog = true;
-                    }
-                }
-                if (have_item && !q_ready && mbar_test(&bb.q_full[0], icount & 1)) { q_ready = true; prog = true; }
-                // S of the next tile
-                if (have_item && q_ready) {
-                    const bool k_ok = mbar_test(&bb.k_full[ks.i], ks.ph);
-                    // S buffer sb is free once P V of tile tcs - NSB is done; that product
-                    // must have been issued first (then the V slot's previous phase is done)
-                    const bool s_ok = tcs < NSB || (tcp > tcs - NSB && mbar_test(&bb.pv_done[pe.i], pe.ph));
-                    if (k_ok && s_ok) {
-                        tc_fence_after();
-                        const uint32_t kaddr = sK32 + ks.i * Cfg::T_BYTES;
-                        #pragma unroll
-                        for (int j = 0; j < HD / 16; ++j)
-                            mma_bf16(tmem_base + sb.i * AT_KT, sw128_desc(qaddr + (j >> 2) * Cfg::QKB_BYTES + (j & 3) * 32),
-                                     sw128_desc(kaddr + (j >> 2) * Cfg::TKB_BYTES + (j & 3) * 32), idesc_s, j > 0);
-                        issued = true;
-                        mma_commit(&bb.s_done[ks.i]);
-                        const int sh = 4 * (tcs & (META - 1));
-                        const bool last = t_in == nt - 1;
-                        meta = (meta & ~(0xFull << sh)) |
-                               ((uint64_t)((t_in == 0 ? M_FIRST : 0u) | (last ? M_LAST : 0u) | ((icount & 1) ? M_ODD : 0u))
-                                << sh);
-                        if (last) {
-                            mma_commit(&bb.q_empty[0]);
-                            have_item = false;
-                            ++icount;
-                        }
-                        if (tcs >= NSB) pe.step();
-                        ks.step();
-                        sb.step();
-                        ++t_in;
-                        ++tcs;
-                        prog = true;
-                    }
-                }
-                if (items_done && tcp == tcs) break;
-                if (prog) {
-                    nidle = 0;
-                    continue;
-                }
-                // Nothing ready: suspend on the barrier of the event most likely next
-                // (P, then V, of the oldest pending tile, else the next K tile, Q or item) rather
-                // than spin, since softmax warps share this SM sub-partition; it wakes
-                // as soon as that phase completes, and the loop then tests everything.
-                if (tcp < tcs) {
-                    if (mbar_test(&bb.p_full[pb.i], pb.ph))
-                        mbar_try_wait_for(&bb.v_full[vs.i], vs.ph, 2000);
-                    else
-                        mbar_try_wait_for(&bb.p_full[pb.i], pb.ph, 2000);
-                } else if (have_item && q_ready) {
-                    mbar_try_wait_for(&bb.k_full[ks.i], ks.ph, 2000);
-                } else if (have_item) {
-                    mbar_try_wait_for(&bb.q_full[0], icount & 1, 2000);
-                } else if (!items_done) {
-                    mbar_try_wait_for(&bb.i_full[icount & (AT_IRING - 1)], (icount / AT_IRING) & 1, 2000);
-                }
-                bool late = false;
-                if ((nidle++ & 7u) == 0) {
-                    const uint64_t now = globaltimer_ns();
-                    if (nidle == 1) t_idle = now;
-                    else late = now - t_idle > err.limit_ns;
-                }
-                if (*abort_flag || late) {
-                    if (!*abort_flag) record_error(err, DFL_ERR_TIMEOUT);
-                    aborted = true;
-                    break;
-                }
+                ++icount;
             }
             if (aborted) {
                 *abort_flag = 1;
@@ -469,14 +371,69 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                     mbar_wait(&bb.drain, 0, err);
                 }
             }
+        } else if (lane == 1) {
+            // ------------------------------------------------------ P V issuer
+            AtRing<NSB> pb;                       // S / P buffer of tile tcount
+            AtRing<VST> vs;                       // V slot of tile tcount
+            const uint32_t sV32 = smem_u32(sV);
+            int icount = 0;
+            bool aborted = false, issued = false;
+            while (!aborted) {
+                const int r = icount & (AT_IRING - 1);
+                if (*abort_flag || !mbar_wait(&bb.i_full[r], (icount / AT_IRING) & 1, err)) { aborted = true; break; }
+                const int it = bb.i_ring[r];
+                mbar_arrive(&bb.i_empty[r]);
+                if (it < 0) break;
+                AtItem x;
+                at_decode(a, it, x);
+                const int nt = x.nctx + x.blk;
+                // O is free once the previous item's epilogue has read it
+                if (!mbar_wait(&bb.o_empty, (icount & 1) ^ 1, err)) { aborted = true; break; }
+                for (int t = 0; t < nt; ++t) {
+                    if (*abort_flag || !mbar_wait(&bb.p_full[pb.i], pb.ph, err) || !mbar_wait(&bb.v_full[vs.i], vs.ph, err)) {
+                        aborted = true;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t vaddr = sV32 + vs.i * Cfg::T_BYTES;
+                    // P (bf16, 2 per column) sits in the first 32 columns of S buffer pb:
+                    // 16 keys per MMA = 8 columns
+                    #pragma unroll
+                    for (int j = 0; j < AT_KT / 16; ++j)
+                        mma_bf16_ts(tmem_base + Cfg::O_COL, tmem_base + pb.i * AT_KT + 8 * j,
+                                    sw128_desc_mn(vaddr + j * 16 * 128, Cfg::TKB_BYTES, 1024), idesc_o,
+                                    (t == 0 && j == 0) ? 0 : 1);
+                    issued = true;
+                    mma_commit(&bb.pv_done[vs.i]);
+                    if (t == nt - 1) mma_commit(&bb.o_full);
+                    pb.step();
+                    vs.step();
+                }
+                ++icount;
+            }
+            if (aborted) {
+                *abort_flag = 1;
+                if (issued) {
+                    mma_commit(&bb.drain2);
+                    mbar_wait(&bb.drain2, 0, err);
+                }
+            }
         }
     } else {
-        // ------------------------------- softmax + epilogue: one row per thread
+        // ---------------------------------------------------- softmax + epilogue
+        // M = 128: one query row per thread (its TMEM lane) with all 64 keys of a
+        // tile and all of O's columns.  M = 64: the 16 rows of the warp's quadrant
+        // are shared by its 32 threads (half-split TMEM accesses): thread t holds
+        // row 16 q + t % 16, keys [32 (t / 16), + 32) of each tile and half of O's
+        // columns; the two halves of a row meet by one shuffle.
+        constexpr bool HALF = MM == 64;
+        constexpr int KPT = HALF ? AT_KT / 2 : AT_KT;   // keys per thread and tile
+        constexpr int OPT = HALF ? HD / 2 : HD;         // O columns per thread
         const int q4 = warp & 3;
-        // query row of the item held by this thread's TMEM lane (R of them; others are padding)
-        const int row = MM == 64 ? (lane < 16 ? 16 * q4 + lane : -1) : q4 * 32 + lane;
-        const bool pad = (MM == 64 ? 16 : 32) * q4 >= a.R;   // warp-uniform: padding rows only
-        const bool live = MM == 128 || lane < 16;            // this lane holds an MMA row (maybe padding)
+        const int hh = HALF ? lane >> 4 : 0;            // this thread's half of the keys and of O
+        // query row of the item held by this thread (R of them; the others are padding)
+        const int row = HALF ? 16 * q4 + (lane & 15) : 32 * q4 + lane;
+        const bool pad = (HALF ? 16 : 32) * q4 >= a.R;  // warp-uniform: padding rows only
         const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
         const int stid = threadIdx.x - pp * 192 - 64;        // 0..127 within the pipeline's softmax warps
         int icount = 0, tcount = 0;
@@ -501,26 +458,29 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                 int v0, v1;
                 at_tile_range(x, t, v0, v1);
                 if (!pad) {   // padding rows: nothing to compute; their P columns may hold anything
-                uint32_t pk[AT_KT / 2];
-                float s[AT_KT];
-                tmem_ld64(tmem_base + lane_off + b * AT_KT, s);
+                uint32_t pk[KPT / 2];
+                float s[KPT];
+                if constexpr (HALF) tmem_ld32_hx2<AT_KT / 2>(tmem_base + lane_off + b * AT_KT, s);
+                else tmem_ld64(tmem_base + lane_off + b * AT_KT, s);
+                const int k0 = hh * KPT;      // this thread's first key of the tile
                 if (v0 > 0 || v1 < AT_KT) {   // edge tile (warp-uniform): keys outside [v0, v1) do not exist
                     #pragma unroll
-                    for (int j = 0; j < AT_KT; ++j)
-                        if (j < v0 || j >= v1) s[j] = -INFINITY;
+                    for (int j = 0; j < KPT; ++j)
+                        if (k0 + j < v0 || k0 + j >= v1) s[j] = -INFINITY;
                 }
                 // row maximum of the raw scores (scale > 0 commutes with max), four partial chains
                 float m4[4] = {s[0], s[1], s[2], s[3]};
                 #pragma unroll
-                for (int j = 4; j < AT_KT; j += 4) {
+                for (int j = 4; j < KPT; j += 4) {
                     m4[0] = fmaxf(m4[0], s[j]); m4[1] = fmaxf(m4[1], s[j + 1]);
                     m4[2] = fmaxf(m4[2], s[j + 2]); m4[3] = fmaxf(m4[3], s[j + 3]);
                 }
-                const float mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * a.scale_log2;
+                float mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * a.scale_log2;
+                if constexpr (HALF) mt = fmaxf(mt, __shfl_xor_sync(0xFFFFFFFFu, mt, 16));
                 if (t == 0) {
                     m_run = mt;
                 } else {
-                    const bool need = live && mt > m_run + AT_LAZY;
+                    const bool need = mt > m_run + AT_LAZY;
                     if (__any_sync(0xFFFFFFFFu, need)) {
                         // O of this item holds the P V products up to the previous tile: wait for the last one
                         const int tp = tcount - 1;
@@ -530,12 +490,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                         const float m_new = need ? mt : m_run;
                         const float alpha = exp2f(m_run - m_new);
                         #pragma unroll 1
-                        for (int c = 0; c < HD; c += 32) {
+                        for (int c = 0; c < OPT; c += 32) {
                             float o[32];
-                            tmem_ld32(tmem_base + lane_off + Cfg::O_COL + c, o);
+                            if constexpr (HALF) tmem_ld32_hx2<HD / 2>(tmem_base + lane_off + Cfg::O_COL + c, o);
+                            else tmem_ld32(tmem_base + lane_off + Cfg::O_COL + c, o);
                             #pragma unroll
                             for (int j = 0; j < 32; ++j) o[j] *= alpha;
-                            tmem_st32(tmem_base + lane_off + Cfg::O_COL + c, o);
+                            if constexpr (HALF) tmem_st32_hx2<HD / 2>(tmem_base + lane_off + Cfg::O_COL + c, o);
+                            else tmem_st32(tmem_base + lane_off + Cfg::O_COL + c, o);
                         }
                         tmem_st_wait();
                         tc_fence_before();
@@ -547,7 +509,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                 float l4[4] = {0.f, 0.f, 0.f, 0.f};
                 const float neg_m = -m_run;
                 #pragma unroll
-                for (int j = 0; j < AT_KT; j += 2) {
+                for (int j = 0; j < KPT; j += 2) {
                     const float p0 = ex2_ftz(fmaf(s[j], a.scale_log2, neg_m));
                     const float p1 = ex2_ftz(fmaf(s[j + 1], a.scale_log2, neg_m));
                     l4[(j >> 1) & 3] += p0 + p1;
@@ -555,8 +517,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                 }
                 l_run += (l4[0] + l4[1]) + (l4[2] + l4[3]);
                 // P over the first half of this tile's S columns (this thread's own lane, whose
-                // S it has already read): the A operand of the P V product
-                tmem_st32u(tmem_base + lane_off + b * AT_KT, pk);
+                // S it has already read): the A operand of the P V product; key k of a row
+                // in column k / 2
+                if constexpr (HALF) tmem_st16u_hx2<AT_KT / 4>(tmem_base + lane_off + b * AT_KT, pk);
+                else tmem_st32u(tmem_base + lane_off + b * AT_KT, pk);
                 tmem_st_wait();
                 }
                 // Rows of the V tile outside [v0, v1) may hold anything (cache rows past
@@ -584,17 +548,21 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
             ok = mbar_wait(&bb.o_full, icount & 1, err);
             if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
             tc_fence_after();
-            const bool real = row >= 0 && row < a.R;   // other MMA rows are padding
+            const bool real = row < a.R;   // other MMA rows are padding
             const int64_t NQ = (int64_t)a.N * a.B * a.Hq;
             const int64_t qrow =
                 real ? (int64_t)(x.n * a.B + row / a.Gq) * a.Hq + x.g * a.G + x.h * a.Gq + row % a.Gq : 0;
-            const float inv = 1.f / l_run;
+            float l_tot = l_run;   // the row's sum over all keys
+            if constexpr (HALF) l_tot += __shfl_xor_sync(0xFFFFFFFFu, l_run, 16);
+            const float inv = 1.f / l_tot;
             #pragma unroll 1
-            for (int c = 0; c < HD && !pad; c += 32) {
+            for (int c0 = 0; c0 < OPT && !pad; c0 += 32) {
                 float o[32];
                 __syncwarp();
-                tmem_ld32(tmem_base + lane_off + Cfg::O_COL + c, o);
+                if constexpr (HALF) tmem_ld32_hx2<HD / 2>(tmem_base + lane_off + Cfg::O_COL + c0, o);
+                else tmem_ld32(tmem_base + lane_off + Cfg::O_COL + c0, o);
                 if (!real) continue;
+                const int c = hh * OPT + c0;   // O column of o[0]
                 if (x.direct) {
                     uint4* dst = reinterpret_cast<uint4*>(a.O + qrow * HD + c);
                     #pragma unroll
@@ -614,7 +582,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
             __syncwarp();
             tc_fence_before();
             mbar_arrive(&bb.o_empty);
-            if (real && !pad && !x.direct) a.lse[(int64_t)x.s * NQ + qrow] = m_run + log2f(l_run);
+            if (real && !pad && !x.direct && hh == 0) a.lse[(int64_t)x.s * NQ + qrow] = m_run + log2f(l_tot);
             ++icount;
         }
         if (!ok) *abort_flag = 1;
