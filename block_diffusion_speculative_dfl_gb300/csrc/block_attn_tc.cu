@@ -21,20 +21,22 @@
 //           keys); lane 1: TMA producer of the matching V tiles.  K and V have
 //           rings of their own, so a K slot is refilled as soon as S has read
 //           it while its V waits for the P V product;
-//   warp 1  MMA issuer: S = Q K^T (M = 64 or 128 padded query rows, N = 64 keys,
-//           K = hd) into a double-buffered TMEM tile, then O += P V (K = 64
+//   warp 1  lane 0: issues S = Q K^T (M = 64 or 128 padded query rows, N = 64
+//           keys, K = hd) into one of NSB TMEM buffers as soon as the K tile
+//           has landed and the buffer is free; lane 1: issues O += P V (K = 64
 //           keys, N = hd; P read from TMEM, V read MN-major straight from its
-//           TMA tile) into a TMEM accumulator, each issued as soon as its
-//           inputs are ready;
-//   warps 2-5  one query row per thread (TMEM lane): masked online softmax
-//           in base 2 with lazy rescaling (O is rescaled in TMEM only when a
-//           row maximum grows by more than 2^8), P written as bf16 over the
-//           first half of the tile's own S columns (the A operand of P V), and
-//           the item's epilogue (bf16 output, or fp32 partial + log-sum-exp
-//           when the sequence's keys span several items).
-// When an item has at most 64 query rows the products run with M = 64: half
-// the tensor-pipe time of M = 128 on padding rows, and half the Q buffer, so
-// the shared memory saved goes to deeper K/V rings.
+//           TMA tile) into a TMEM accumulator as soon as P is written and V has
+//           landed;
+//   warps 2-5  masked online softmax in base 2 with lazy rescaling (O is
+//           rescaled in TMEM only when a row maximum grows by more than 2^8),
+//           P written as bf16 over the first half of the tile's own S columns
+//           (the A operand of P V), and the item's epilogue (bf16 output, or
+//           fp32 partial + log-sum-exp when the sequence's keys span several
+//           items).  At M = 128 each thread owns one row (its TMEM lane); at
+//           M = 64 the 16 rows of a warp's quadrant are split over its 32
+//           threads, each with half of a row's keys and of O.
+// When an item has at most 64 query rows the products run with M = 64: the
+// Q buffer halves, so the shared memory saved goes to deeper K/V rings.
 // A combine kernel merges the partials of multi-item sequences.
 #include "internal.h"
 #include "small_kernels.h"
