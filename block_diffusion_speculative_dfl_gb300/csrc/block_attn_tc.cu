@@ -14,19 +14,19 @@
 // 128 MMA rows; the subsets of one group are consecutive items, so their K/V
 // tiles are read from HBM once and from L2 by the others).  A persistent kernel (one CTA per SM)
 // takes items from a global counter; empty items (past a shorter sequence's
-// keys) are skipped by the scheduler.  Per CTA:
-//   warp 0  lane 0: scheduler + TMA producer of the item's Q rows (3-D box:
-//           head dim x G heads x B block rows, zero rows up to 128) and its
-//           64-key K tiles (context cache, then one tile of the block's own
-//           keys); lane 1: TMA producer of the matching V tiles.  K and V have
-//           rings of their own, so a K slot is refilled as soon as S has read
-//           it while its V waits for the P V product;
-//   warp 1  lane 0: issues S = Q K^T (M = 64 or 128 padded query rows, N = 64
-//           keys, K = hd) into one of NSB TMEM buffers as soon as the K tile
-//           has landed and the buffer is free; lane 1: issues O += P V (K = 64
-//           keys, N = hd; P read from TMEM, V read MN-major straight from its
-//           TMA tile) into a TMEM accumulator as soon as P is written and V has
-//           landed;
+// keys) are skipped by the scheduler.  Per CTA, two pipelines of 8 warps:
+//   warp 0  scheduler + TMA producer of the item's Q rows (3-D box: head dim x
+//           G heads x B block rows, zero rows up to 128) and its 64-key K
+//           tiles (context cache, then one tile of the block's own keys);
+//   warp 7  TMA producer of the matching V tiles.  K and V have rings of
+//           their own, so a K slot is refilled as soon as S has read it while
+//           its V waits for the P V product;
+//   warp 1  issues S = Q K^T (M = 64 or 128 padded query rows, N = 64 keys,
+//           K = hd) into one of NSB TMEM buffers as soon as the K tile has
+//           landed and the buffer is free;
+//   warp 6  issues O += P V (K = 64 keys, N = hd; P read from TMEM, V read
+//           MN-major straight from its TMA tile) into a TMEM accumulator as
+//           soon as P is written and V has landed;
 //   warps 2-5  masked online softmax in base 2 with lazy rescaling (O is
 //           rescaled in TMEM only when a row maximum grows by more than 2^8),
 //           P written as bf16 over the first half of the tile's own S columns
@@ -49,6 +49,11 @@ constexpr int AT_KT = 64;           // keys per tile
 constexpr int AT_M = 128;           // MMA rows (query rows, zero-padded)
 constexpr float AT_LAZY = 8.f;      // rescale O only when a row max grows by more than this (log2 units)
 constexpr int AT_IRING = 4;         // scheduled items in flight between the warps
+// Warps per pipeline, one role each: 0 scheduler + Q/K producer, 1 S issuer,
+// 2..5 softmax, 6 P V issuer, 7 V producer.  A role that blocks on barriers
+// has a warp of its own: lanes of one warp waiting on different barriers hold
+// one another up.
+constexpr int AT_WPP = 8;
 static_assert((AT_IRING & (AT_IRING - 1)) == 0, "ring positions are masked");
 
 struct AtArgs {
@@ -93,7 +98,7 @@ struct AtCfg {
     static constexpr int PIPE_COLS = 256;              // TMEM columns per pipeline
     static_assert(O_COL + HD <= PIPE_COLS, "TMEM columns");
     static constexpr int TMEM_COLS = NP * PIPE_COLS;
-    static constexpr int THREADS = NP * 192;
+    static constexpr int THREADS = NP * AT_WPP * 32;
     static constexpr int BAR_BYTES = 512;              // barriers and scheduler slots per pipeline
     static constexpr int SMEM = 1024 + Q_TOTAL + NP * (RING_BYTES + BAR_BYTES);
     static_assert(SMEM <= 227 * 1024, "shared memory");
@@ -186,15 +191,15 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bar_base + Cfg::NP * Cfg::BAR_BYTES - 8);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int pp = warp / 6;          // this warp's pipeline
-    const int role = warp % 6;        // 0 producer, 1 MMA, 2..5 softmax
+    const int pp = warp / AT_WPP;     // this warp's pipeline
+    const int role = warp % AT_WPP;   // see AT_WPP
     uint8_t* sQ = sm + pp * Cfg::Q_BYTES;                                // this pipeline's Q buffer
     uint8_t* sK = sm + Cfg::Q_TOTAL + pp * Cfg::RING_BYTES;              // [KST] K tiles
     uint8_t* sV = sK + KST * Cfg::T_BYTES;                               // [VST] V tiles
     Bars& bb = *reinterpret_cast<Bars*>(bar_base + pp * Cfg::BAR_BYTES);
     volatile int* abort_flag = &bb.abort_flag;
 
-    if ((threadIdx.x % 192) == 0) {
+    if ((threadIdx.x % (AT_WPP * 32)) == 0) {
         for (int s = 0; s < KST; ++s) { mbar_init(&bb.k_full[s], 1); mbar_init(&bb.s_done[s], 1); }
         for (int s = 0; s < VST; ++s) { mbar_init(&bb.v_full[s], 1); mbar_init(&bb.pv_done[s], 1); }
         for (int b = 0; b < NQB; ++b) { mbar_init(&bb.q_full[b], 1); mbar_init(&bb.q_empty[b], 1); }
@@ -220,8 +225,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder + pp * Cfg::PIPE_COLS;
 
-    if (role == 0) {
-        if (lane == 0) {
+    if (role == 0 || role == 7) {
+        if (role == 0 && lane == 0) {
             // ---------------------------------------- scheduler + TMA producer of Q and K
             int icount = 0, tcount = 0;
             uint32_t k_fills = 0;
@@ -278,7 +283,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                     if (last >= 0) mbar_wait(&bb.q_full[b], (last / NQB) & 1, err);
                 }
             }
-        } else if (lane == 1) {
+        } else if (role == 7 && lane == 0) {
             // ------------------------------------------------- TMA producer of V
             // follows the scheduled items like the consumers, as far ahead as the V ring allows
             int icount = 0, tcount = 0;
@@ -318,15 +323,15 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                 }
             }
         }
-    } else if (role == 1) {
-        // Two MMA issuers, each a plain sequence of waits: lane 0 issues S = Q K^T of
+    } else if (role == 1 || role == 6) {
+        // Two MMA issuers, each a plain sequence of waits: warp 1 issues S = Q K^T of
         // every tile as soon as its K has landed and its S buffer is free (up to NSB
-        // tiles ahead of the softmax); lane 1 issues O += P V of every tile as soon as
+        // tiles ahead of the softmax); warp 6 issues O += P V of every tile as soon as
         // its P is written and its V has landed.  Each follows the scheduled items.
         constexpr uint32_t idesc_s = idesc_bf16(MM, AT_KT);
         constexpr uint32_t idesc_o = idesc_bf16_bmn(MM, HD);
         static_assert(NQB == 1, "one Q buffer per pipeline");
-        if (lane == 0) {
+        if (role == 1 && lane == 0) {
             // ------------------------------------------------------ S issuer
             AtRing<KST> ks;                       // K slot of tile tcount
             AtRing<NSB> sb;                       // S buffer of tile tcount
@@ -373,7 +378,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                     mbar_wait(&bb.drain, 0, err);
                 }
             }
-        } else if (lane == 1) {
+        } else if (role == 6 && lane == 0) {
             // ------------------------------------------------------ P V issuer
             AtRing<NSB> pb;                       // S / P buffer of tile tcount
             AtRing<VST> vs;                       // V slot of tile tcount
@@ -437,7 +442,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         const int row = HALF ? 16 * q4 + (lane & 15) : 32 * q4 + lane;
         const bool pad = (HALF ? 16 : 32) * q4 >= a.R;  // warp-uniform: padding rows only
         const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
-        const int stid = threadIdx.x - pp * 192 - 64;        // 0..127 within the pipeline's softmax warps
+        const int stid = threadIdx.x - pp * AT_WPP * 32 - 64;        // 0..127 within the pipeline's softmax warps
         int icount = 0, tcount = 0;
         bool ok = true;
         while (ok) {
