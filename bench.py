@@ -42,6 +42,7 @@ class L2Flush:
     L2 that holds none of its inputs and nothing left to write back."""
 
     def __init__(self) -> None:
+        import torch
         self.w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
         self.r = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.int32, device="cuda")
 
