@@ -164,6 +164,8 @@ def test_rope_table_matches_oracle():
     (32, 2048, 16, 32, 8, 128, 512),  # the Qwen3-8B drafter's attention shape
     (16, 1024, 33, 32, 8, 128, 512),  # the self-selection window: 132 rows per K/V head, two head subsets
     (3, 500, 24, 48, 4, 64, 256),     # 288 rows per K/V head: three head subsets of 96 rows
+    (3, 150, 12, 4, 2, 128, 256),     # M = 64 with 24 rows: a quadrant with 8 rows and 8 padding rows
+    (2, 90, 16, 6, 2, 64, 192),       # M = 64, hd 64, group 3: 48 rows, one padding warp
 ])
 def test_block_attn_bf16(N, C, B, Hq, Hkv, hd, d):
     rng = np.random.default_rng(N * 7 + C)
