@@ -189,6 +189,35 @@ def test_block_attn_bf16(N, C, B, Hq, Hkv, hd, d):
     assert_bf16_close(got - Xb, ref - Xb, "O Wo^T")
 
 
+@pytest.mark.parametrize("N,C,B,Hq,Hkv,hd,d", [
+    (8, 2048, 16, 32, 8, 128, 512),   # M = 64, hd 128, one item per pipeline
+    (8, 1500, 8, 64, 8, 64, 256),     # M = 64, hd 64, three S buffers
+    (4, 1024, 33, 32, 8, 128, 512),   # M = 128, two head subsets
+    (1, 700, 16, 32, 8, 128, 512),    # key ranges split over items, combine kernel
+])
+def test_block_attn_bitwise_reproducible(N, C, B, Hq, Hkv, hd, d):
+    # Items are taken from a global counter in whatever order the CTAs get to
+    # it, but each item's arithmetic and the combine's order are fixed: every
+    # launch must produce the same bits.
+    rng = np.random.default_rng(N * 13 + C)
+    Q = dev(rng_bf16(rng, (N * B, Hq, hd)), "bf16")
+    Kc, Vc = dev(rng_bf16(rng, (N * C, Hkv, hd)), "bf16"), dev(rng_bf16(rng, (N * C, Hkv, hd)), "bf16")
+    Kb, Vb = dev(rng_bf16(rng, (N * B, Hkv, hd)), "bf16"), dev(rng_bf16(rng, (N * B, Hkv, hd)), "bf16")
+    Wo = dev(rng_bf16(rng, (d, Hq * hd), (Hq * hd) ** -0.5), "bf16")
+    wsb = dfl.workspace_size(dfl.DFL_OP_BLOCK_ATTN, N=N, C=C, B=B, Hq=Hq, Hkv=Hkv, hd=hd, d=d, dtype=dfl.DFL_BF16)
+    ws = _ws(wsb)
+    first = None
+    for _ in range(8):
+        Xb_d = dev(np.zeros((N * B, d), np.float32))
+        dfl.dfl_block_attn(Q, Kc, Vc, Kb, Vb, N, C, B, Hq, Hkv, hd, dfl.DFL_BF16, Wo, d, Xb_d, ws, wsb)
+        got = host(Xb_d)
+        assert np.all(np.isfinite(got))
+        if first is None:
+            first = got
+        else:
+            assert np.array_equal(got.view(np.uint32), first.view(np.uint32))
+
+
 def test_block_attn_f32():
     N, C, B, Hq, Hkv, hd, d = 1, 64, 16, 4, 4, 64, 256
     rng = np.random.default_rng(11)
