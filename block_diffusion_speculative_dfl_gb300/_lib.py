@@ -16,6 +16,7 @@ DFL_ERR_WORKSPACE, DFL_ERR_CUDA, DFL_ERR_TIMEOUT, DFL_ERR_NO_DEVICE = 4, 5, 6, 7
 DFL_F32, DFL_BF16 = 0, 1
 DFL_OP_DUAL_KV_PROJ, DFL_OP_BLOCK_ATTN, DFL_OP_LM_HEAD, DFL_OP_SELF_SELECT, DFL_OP_DRAFT_STEP = 1, 2, 3, 4, 5
 DFL_OP_TV_ACCEPTANCE, DFL_OP_SPEC_ACCEPT, DFL_OP_BLOCK_FFN, DFL_OP_DRAFT_STEP_CACHED = 6, 7, 8, 9
+DFL_OP_DRAFT_STEP_HOST = 10
 
 # Every function the header declares; tests check each is exported.
 EXPORTED = ("dfl_version", "dfl_status_string", "dfl_workspace_size", "dfl_rope_table",
@@ -23,7 +24,7 @@ EXPORTED = ("dfl_version", "dfl_status_string", "dfl_workspace_size", "dfl_rope_
             "dfl_greedy_accept", "dfl_self_select", "dfl_draft_step", "dfl_get_device_error",
             "dfl_set_wait_limit_ns", "dfl_selftest_bounded_wait", "dfl_profile_enable", "dfl_profile_report",
             "dfl_self_select_noalloc", "dfl_tv_acceptance", "dfl_spec_accept", "dfl_block_ffn",
-            "dfl_draft_step_cached")
+            "dfl_draft_step_cached", "dfl_draft_step_host")
 
 
 class DflError(RuntimeError):
@@ -79,6 +80,7 @@ _SIGS = {
     "dfl_self_select": ([_P, _I32, _P, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _SZ, _P], _I32),
     "dfl_draft_step": ([C.POINTER(StepArgs), _P, _SZ, _P], _I32),
     "dfl_draft_step_cached": ([C.POINTER(StepArgs), C.POINTER(CtxCache), _P, _SZ, _P], _I32),
+    "dfl_draft_step_host": ([C.POINTER(StepArgs), _P, _I32, _P, _SZ, _P], _I32),
     "dfl_get_device_error": ([_P, C.POINTER(_I32)], _I32),
     "dfl_set_wait_limit_ns": ([C.c_uint64], _I32),
     "dfl_selftest_bounded_wait": ([C.c_uint64, _P, _P], _I32),
@@ -195,6 +197,11 @@ def dfl_self_select(vlog, dt, drafts, N, K, G, V, scores, selected, accept_len, 
 
 def dfl_draft_step(args: StepArgs, ws, ws_bytes, stream=None):
     _check("dfl_draft_step", load().dfl_draft_step(C.byref(args), ptr(ws), ws_bytes, _stream(stream)))
+
+
+def dfl_draft_step_host(args: StepArgs, H_dev, chunks, ws, ws_bytes, stream=None):
+    _check("dfl_draft_step_host",
+           load().dfl_draft_step_host(C.byref(args), ptr(H_dev), int(chunks), ptr(ws), ws_bytes, _stream(stream)))
 
 
 def dfl_draft_step_cached(args: StepArgs, cache: CtxCache, ws, ws_bytes, stream=None):

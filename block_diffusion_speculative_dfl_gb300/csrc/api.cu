@@ -85,6 +85,16 @@ size_t ws_lm_head(int N, int B, int row0, int d, int V, int dt, bool logits_miss
 // drafts, then scratch shared by the calls in turn.  The cached step mixes
 // and projects R rows per sequence, keeps K/V in the caller's cache (C is its
 // capacity) and, when sampling, lends the feature area to the logits.
+size_t step_ws_bytes(const dfl_shape& s, bool cached);
+
+// Host-input step: the plain step's workspace, then the context K/V of layers
+// 1..D-1 (layer 0's are the plain step's Kc / Vc).
+size_t kv_layer_bytes(const dfl_shape& s) { return al256((size_t)s.N * s.C * s.Hkv * s.hd * 2); }
+size_t step_host_ws_bytes(const dfl_shape& s) {
+    if (s.dtype != DFL_BF16 || s.D < 1) return 0;
+    return step_ws_bytes(s, false) + (size_t)(s.D - 1) * 2 * kv_layer_bytes(s);
+}
+
 size_t step_ws_bytes(const dfl_shape& s, bool cached) {
     if (cached && (s.dtype != DFL_BF16 || s.R < 1)) return 0;
     const size_t e = esz(s.dtype);
@@ -149,6 +159,7 @@ extern "C" size_t dfl_workspace_size(dfl_op op, const dfl_shape* s) {
         case DFL_OP_BLOCK_FFN: return s->F > 0 ? ws_block_ffn(s->N, s->B, s->d, s->F, s->dtype) : 0;
         case DFL_OP_DRAFT_STEP: return step_ws_bytes(*s, false);
         case DFL_OP_DRAFT_STEP_CACHED: return step_ws_bytes(*s, true);
+        case DFL_OP_DRAFT_STEP_HOST: return step_host_ws_bytes(*s);
     }
     return 0;
 }
@@ -210,6 +221,27 @@ struct KvRowPlan {
 // Without a plan, context row r sits at position r % ctx_per and block row r
 // at ctx_per + r % B; with one, the plan gives positions and context rows go
 // to plan->ctx_dst (rows < 0 dropped).
+// Context rows: [Kc | Vc] = Xc [Wkc ; Wvc]^T with rotary on Kc; row r of the
+// call sits at position r % ctx_per (or at plan->ctx_pos[r]).
+GemmArgs ctx_kv_args(const void* Xc, int64_t ctx_M, int ctx_per, int d, const void* Wkc, const void* Wvc, int Hkv,
+                     int hd, const float* rope, void* Kc, void* Vc, const KvRowPlan* plan) {
+    const int kv = Hkv * hd;
+    GemmArgs gc{};
+    gc.A = Xc; gc.M = (int)ctx_M; gc.K = d;
+    gc.B[0] = Wkc; gc.B[1] = Wvc; gc.b_rows[0] = kv; gc.b_rows[1] = kv;
+    gc.b_begin[0] = 0; gc.b_begin[1] = kv; gc.nb = 2; gc.N = 2 * kv;
+    gc.bn = (kv % 256 == 0) ? 256 : 128;
+    gc.m_inner = 0;
+    gc.epi = EPI_STORE;
+    gc.ep.seg[0] = GemmSeg{Kc, 0, kv, rope != nullptr};
+    gc.ep.seg[1] = GemmSeg{Vc, kv, kv, 0};
+    gc.ep.nseg = 2;
+    gc.ep.rope = rope; gc.ep.hd = hd; gc.ep.rows_per_seq = ctx_per; gc.ep.pos_off = 0;
+    if (plan) { gc.ep.row_pos = plan->ctx_pos; gc.ep.row_dst = plan->ctx_dst; }
+    gc.tag = plan ? "gemm_ctx_kv_append" : "gemm_ctx_kv";
+    return gc;
+}
+
 dfl_status dual_kv_proj_bf16(DeviceCtx* ctx, const void* Xc, int64_t ctx_M, int ctx_per, const float* Xb, int N,
                              int B, int d, const float* blk_gain, float eps, const void* Wq, const void* Wkc,
                              const void* Wvc, const void* Wkb, const void* Wvb, int Hq, int Hkv, int hd,
@@ -238,20 +270,7 @@ dfl_status dual_kv_proj_bf16(DeviceCtx* ctx, const void* Xc, int64_t ctx_M, int 
     gb.tag = "gemm_block_qkv";
     if (ctx_M <= 0) return gemm_tc(ctx, gb, st);
 
-    // context rows: [Kc | Vc] = Xc [Wkc ; Wvc]^T
-    GemmArgs gc{};
-    gc.A = Xc; gc.M = ctx_M; gc.K = d;
-    gc.B[0] = Wkc; gc.B[1] = Wvc; gc.b_rows[0] = kv; gc.b_rows[1] = kv;
-    gc.b_begin[0] = 0; gc.b_begin[1] = kv; gc.nb = 2; gc.N = 2 * kv;
-    gc.bn = (kv % 256 == 0) ? 256 : 128;
-    gc.m_inner = 0;
-    gc.epi = EPI_STORE;
-    gc.ep.seg[0] = GemmSeg{Kc, 0, kv, rope != nullptr};
-    gc.ep.seg[1] = GemmSeg{Vc, kv, kv, 0};
-    gc.ep.nseg = 2;
-    gc.ep.rope = rope; gc.ep.hd = hd; gc.ep.rows_per_seq = ctx_per; gc.ep.pos_off = 0;
-    if (plan) { gc.ep.row_pos = plan->ctx_pos; gc.ep.row_dst = plan->ctx_dst; }
-    gc.tag = plan ? "gemm_ctx_kv_append" : "gemm_ctx_kv";
+    const GemmArgs gc = ctx_kv_args(Xc, ctx_M, ctx_per, d, Wkc, Wvc, Hkv, hd, rope, Kc, Vc, plan);
     // One launch for both: the block projection's weights stream from HBM on a
     // few SMs while the others work on context tiles (block tiles first).
     return gemm_tc2(ctx, gb, gc, plan ? "gemm_kv_qkv_append" : "gemm_kv_qkv", st);
@@ -517,8 +536,18 @@ namespace {
 
 // The whole draft step; with `cache`, the incremental form over the caller's
 // context K/V cache (args->C its capacity, args->H the R new rows per sequence).
-dfl_status draft_step_impl(const dfl_step_args* a, const dfl_ctx_cache* cache, void* ws, size_t ws_bytes,
-                           dfl_stream stream) {
+// Shapes the bf16 tensor-core path of a step takes (TMA strides, tile widths).
+dfl_status step_bf16_shape(const dfl_step_args* a) {
+    if (a->Hq <= 0 || a->Hkv <= 0 || a->Hq % a->Hkv != 0 || (a->hd != 64 && a->hd != 128))
+        return DFL_ERR_UNSUPPORTED_SHAPE;
+    if ((a->Hkv * a->hd) % 128 != 0 || (a->Hq * a->hd) % 128 != 0 || a->d % 32 != 0)
+        return DFL_ERR_UNSUPPORTED_SHAPE;
+    if (a->rope && !aligned16(a->rope)) return DFL_ERR_MISALIGNED;
+    return DFL_OK;
+}
+
+// Host-side checks of a step's arguments (no launch).
+dfl_status step_check(const dfl_step_args* a, const dfl_ctx_cache* cache, const void* ws) {
     if (!a || !ws) return DFL_ERR_INVALID_ARG;
     const int dt = a->dtype;
     if (dt != DFL_F32 && dt != DFL_BF16) return DFL_ERR_INVALID_ARG;
@@ -547,16 +576,28 @@ dfl_status draft_step_impl(const dfl_step_args* a, const dfl_ctx_cache* cache, v
         if ((int64_t)a->N * a->C >= (int64_t)1 << 31) return DFL_ERR_UNSUPPORTED_SHAPE;
         if (!aligned16(cache->K) || !aligned16(cache->V) || (cache->layer_stride * 2) % 16 != 0)
             return DFL_ERR_MISALIGNED;
-        if (a->Hq <= 0 || a->Hkv <= 0 || a->Hq % a->Hkv != 0 || (a->hd != 64 && a->hd != 128))
-            return DFL_ERR_UNSUPPORTED_SHAPE;
-        if ((a->Hkv * a->hd) % 128 != 0 || (a->Hq * a->hd) % 128 != 0 || a->d % 32 != 0)
-            return DFL_ERR_UNSUPPORTED_SHAPE;
-        if (a->rope && !aligned16(a->rope)) return DFL_ERR_MISALIGNED;
+        return step_bf16_shape(a);
     }
+    return DFL_OK;
+}
+
+dfl_shape step_shape(const dfl_step_args* a, const dfl_ctx_cache* cache) {
     dfl_shape s{};
     s.N = a->N; s.C = a->C; s.B = a->B; s.d = a->d; s.Hq = a->Hq; s.Hkv = a->Hkv; s.hd = a->hd; s.D = a->D;
-    s.L = a->L; s.V = a->V; s.K = a->sample ? a->sample->K : 0; s.G = a->B - 1; s.row0 = 1; s.dtype = dt;
+    s.L = a->L; s.V = a->V; s.K = a->sample ? a->sample->K : 0; s.G = a->B - 1; s.row0 = 1; s.dtype = a->dtype;
     s.F = a->F; s.R = cache ? cache->R : 0;
+    return s;
+}
+
+dfl_status step_tail(const dfl_step_args* a, const dfl_shape& s, uint8_t* Xc, size_t xc_bytes, int32_t* samples,
+                     uint8_t* sub, size_t sub_bytes, dfl_stream stream);
+
+dfl_status draft_step_impl(const dfl_step_args* a, const dfl_ctx_cache* cache, void* ws, size_t ws_bytes,
+                           dfl_stream stream) {
+    dfl_status rc = step_check(a, cache, ws);
+    if (rc != DFL_OK) return rc;
+    const int dt = a->dtype;
+    const dfl_shape s = step_shape(a, cache);
     if (ws_bytes < step_ws_bytes(s, cache != nullptr)) return DFL_ERR_WORKSPACE;
     if (!aligned16(ws)) return DFL_ERR_MISALIGNED;
     DeviceCtx* dctx = current_ctx();
@@ -592,7 +633,6 @@ dfl_status draft_step_impl(const dfl_step_args* a, const dfl_ctx_cache* cache, v
     if (a->V > 0) carve(p, (size_t)N * (B - 1) * 4);
     uint8_t* sub = p;
     const size_t sub_bytes = ws_bytes - (size_t)(sub - static_cast<uint8_t*>(ws));
-    dfl_status rc;
 
     {
     ProfScope ps("copy_block_init", st);
@@ -634,6 +674,17 @@ dfl_status draft_step_impl(const dfl_step_args* a, const dfl_ctx_cache* cache, v
                                             w.W2, a->F, sub, sub_bytes, stream)) != DFL_OK)
             return rc;
     }
+    return step_tail(a, s, Xc, xc_bytes, samples, sub, sub_bytes, stream);
+}
+
+// LM head and acceptance epilogue of a step (a7 onwards), on the final Xb.
+dfl_status step_tail(const dfl_step_args* a, const dfl_shape& s, uint8_t* Xc, size_t xc_bytes, int32_t* samples,
+                     uint8_t* sub, size_t sub_bytes, dfl_stream stream) {
+    const int dt = a->dtype;
+    const dfl_dtype ddt = static_cast<dfl_dtype>(dt);
+    const int N = a->N, B = a->B, d = a->d;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    dfl_status rc;
     if (a->V == 0) return DFL_OK;
     float* logits = a->logits;
     if (!logits && a->sample) {   // sampling walks the logits; borrow the Xc area (no longer needed)
@@ -669,11 +720,116 @@ dfl_status draft_step_impl(const dfl_step_args* a, const dfl_ctx_cache* cache, v
     return DFL_OK;
 }
 
+// dfl_draft_step_host: the copy of H in groups of whole sequences on the
+// device's copy stream, each group's mix and context projections (all
+// layers) as soon as it has landed, then the block path and the tail.
+dfl_status draft_step_host_impl(const dfl_step_args* a, void* H_dev, int chunks, void* ws, size_t ws_bytes,
+                                dfl_stream stream) {
+    dfl_status rc = step_check(a, nullptr, ws);
+    if (rc != DFL_OK) return rc;
+    if (!H_dev || chunks < 1) return DFL_ERR_INVALID_ARG;
+    if (a->dtype != DFL_BF16) return DFL_ERR_UNSUPPORTED_SHAPE;
+    if ((rc = step_bf16_shape(a)) != DFL_OK) return rc;
+    if (!aligned16(H_dev) || (a->h_layer_stride * 2) % 16 != 0 || a->d % 8 != 0) return DFL_ERR_MISALIGNED;
+    if (a->h_layer_stride < (int64_t)a->N * a->C * a->d) return DFL_ERR_INVALID_ARG;
+    const dfl_shape s = step_shape(a, nullptr);
+    const size_t plain_bytes = step_ws_bytes(s, false);
+    if (ws_bytes < step_host_ws_bytes(s)) return DFL_ERR_WORKSPACE;
+    DeviceCtx* dctx = current_ctx();
+    if (!dctx) return DFL_ERR_NO_DEVICE;
+    if (!dctx->copy_st) {
+        if (cudaStreamCreateWithFlags(&dctx->copy_st, cudaStreamNonBlocking) != cudaSuccess) return DFL_ERR_CUDA;
+        for (cudaEvent_t& e : dctx->copy_ev)
+            if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return DFL_ERR_CUDA;
+    }
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int N = a->N, C = a->C, B = a->B, d = a->d, L = a->L, D = a->D;
+    const int kv = a->Hkv * a->hd;
+    const int64_t ctx_rows = (int64_t)N * C;
+    // the plain step's carve, then layers 1..D-1's context K/V past its end
+    uint8_t* p = static_cast<uint8_t*>(ws);
+    const size_t xc_bytes = (size_t)D * ctx_rows * d * 2;
+    uint8_t* Xc = carve(p, xc_bytes);
+    void* Q = carve(p, (size_t)N * B * a->Hq * a->hd * 2);
+    uint8_t* Kc0 = carve(p, (size_t)ctx_rows * kv * 2);
+    uint8_t* Vc0 = carve(p, (size_t)ctx_rows * kv * 2);
+    void* Kb = carve(p, (size_t)N * B * kv * 2);
+    void* Vb = carve(p, (size_t)N * B * kv * 2);
+    int32_t* samples = a->samples;
+    if (a->V > 0 && s.K > 0) {
+        int32_t* own = reinterpret_cast<int32_t*>(carve(p, (size_t)N * s.K * (B - 1) * 4));
+        if (!samples) samples = own;
+    }
+    if (a->V > 0) carve(p, (size_t)N * (B - 1) * 4);
+    uint8_t* sub = p;
+    const size_t sub_bytes = plain_bytes - (size_t)(sub - static_cast<uint8_t*>(ws));
+    uint8_t* extra = static_cast<uint8_t*>(ws) + plain_bytes;
+    auto kc_of = [&](int l) { return l == 0 ? Kc0 : extra + (size_t)(l - 1) * 2 * kv_layer_bytes(s); };
+    auto vc_of = [&](int l) { return l == 0 ? Vc0 : kc_of(l) + kv_layer_bytes(s); };
+
+    {
+    ProfScope ps("copy_block_init", st);
+    if (cudaMemcpyAsync(a->Xb, a->Xb0, (size_t)N * B * d * sizeof(float), cudaMemcpyDeviceToDevice, st) !=
+        cudaSuccess)
+        return DFL_ERR_CUDA;
+    }
+    // H_dev may still be read by work queued earlier on `stream`
+    cudaEvent_t* ev = dctx->copy_ev;
+    if (cudaEventRecord(ev[DeviceCtx::MAX_H_CHUNKS], st) != cudaSuccess ||
+        cudaStreamWaitEvent(dctx->copy_st, ev[DeviceCtx::MAX_H_CHUNKS], 0) != cudaSuccess)
+        return DFL_ERR_CUDA;
+    const int nch = std::min(std::min(chunks, N), DeviceCtx::MAX_H_CHUNKS);
+    const int per = (N + nch - 1) / nch;
+    const uint8_t* Hh = static_cast<const uint8_t*>(a->H);
+    uint8_t* Hd = static_cast<uint8_t*>(H_dev);
+    const size_t lstride = (size_t)a->h_layer_stride * 2;
+    for (int c = 0; c * per < N; ++c) {
+        const int n0 = c * per, n1 = std::min(N, n0 + per);
+        const int64_t r0 = (int64_t)n0 * C, rows = (int64_t)(n1 - n0) * C;
+        const size_t off = (size_t)r0 * d * 2, bytes = (size_t)rows * d * 2;
+        for (int i = 0; i < L; ++i)
+            if (cudaMemcpyAsync(Hd + i * lstride + off, Hh + i * lstride + off, bytes, cudaMemcpyHostToDevice,
+                                dctx->copy_st) != cudaSuccess)
+                return DFL_ERR_CUDA;
+        if (cudaEventRecord(ev[c], dctx->copy_st) != cudaSuccess || cudaStreamWaitEvent(st, ev[c], 0) != cudaSuccess)
+            return DFL_ERR_CUDA;
+        if ((rc = dfl_layer_mix_rmsnorm(Hd + off, a->h_layer_stride, L, rows, d, DFL_BF16, D, a->mix_logits,
+                                        a->mix_gain, a->eps, Xc + off, ctx_rows * d, stream)) != DFL_OK)
+            return rc;
+        for (int l = 0; l < D; ++l) {   // context rows start at a sequence: position = row % C
+            const dfl_layer_weights& w = a->layers[l];
+            const GemmArgs gc = ctx_kv_args(Xc + (size_t)l * ctx_rows * d * 2 + off, rows, C, d, w.Wkc, w.Wvc,
+                                            a->Hkv, a->hd, a->rope, kc_of(l) + (size_t)r0 * kv * 2,
+                                            vc_of(l) + (size_t)r0 * kv * 2, nullptr);
+            if ((rc = gemm_tc(dctx, gc, st)) != DFL_OK) return rc;
+        }
+    }
+    for (int l = 0; l < D; ++l) {
+        const dfl_layer_weights& w = a->layers[l];
+        if ((rc = dual_kv_proj_bf16(dctx, nullptr, 0, C, a->Xb, N, B, d, a->blk_gain + (size_t)l * d, a->eps, w.Wq,
+                                    w.Wkc, w.Wvc, w.Wkb, w.Wvb, a->Hq, a->Hkv, a->hd, a->rope, Q, nullptr, nullptr, Kb,
+                                    Vb, sub, nullptr, st)) != DFL_OK)
+            return rc;
+        if ((rc = block_attn_bf16(dctx, Q, kc_of(l), vc_of(l), Kb, Vb, N, C, B, a->Hq, a->Hkv, a->hd, w.Wo, d, a->Xb,
+                                  sub, nullptr, C, st)) != DFL_OK)
+            return rc;
+        if (a->F > 0 && (rc = dfl_block_ffn(a->Xb, N, B, d, DFL_BF16, a->ffn_gain + (size_t)l * d, a->eps, w.W1,
+                                            w.W3, w.W2, a->F, sub, sub_bytes, stream)) != DFL_OK)
+            return rc;
+    }
+    return step_tail(a, s, Xc, xc_bytes, samples, sub, sub_bytes, stream);
+}
+
 }  // namespace
 }  // namespace dfl
 
 extern "C" dfl_status dfl_draft_step(const dfl_step_args* a, void* ws, size_t ws_bytes, dfl_stream stream) {
     return draft_step_impl(a, nullptr, ws, ws_bytes, stream);
+}
+
+extern "C" dfl_status dfl_draft_step_host(const dfl_step_args* a, void* H_dev, int32_t chunks, void* ws,
+                                          size_t ws_bytes, dfl_stream stream) {
+    return draft_step_host_impl(a, H_dev, chunks, ws, ws_bytes, stream);
 }
 
 extern "C" dfl_status dfl_draft_step_cached(const dfl_step_args* a, const dfl_ctx_cache* cache, void* ws,

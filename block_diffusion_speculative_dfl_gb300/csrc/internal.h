@@ -17,7 +17,11 @@ struct DeviceCtx {
     int* err_word = nullptr;       // device address of this device's error word
     bool gemm_attr_set[16] = {};   // max-dynamic-smem set for gemm instantiations
     bool mix_attr_set = false;
-    bool attn_attr_set[4] = {};    // tcgen05 attention: head dim 64 / 128, own / shared Q buffer
+    bool attn_attr_set[4] = {};    // tcgen05 attention: head dim 64 / 128, M = 64 / 128 products
+    // Host-input draft step: a copy stream and events, created on first use.
+    static constexpr int MAX_H_CHUNKS = 16;
+    cudaStream_t copy_st = nullptr;
+    cudaEvent_t copy_ev[MAX_H_CHUNKS + 1] = {};
 };
 
 // Context of the current device (initialised on first use); nullptr if no

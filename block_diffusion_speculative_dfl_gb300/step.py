@@ -130,16 +130,32 @@ class DraftModel:
         self._last_args = self._args(H, Xb0, target, vlog)
         _lib.dfl_draft_step(self._last_args, self.ws, self.ws_bytes, stream)
 
-    def step_from_host(self, H_host, Xb0_host, target_host=None, vlog_host=None, dev_in=None, stream=None):
+    def _step_host(self, H_host, H_dev, Xb0, target, vlog, chunks, stream):
+        """``dfl_draft_step_host``: H from (pinned) host memory through ``H_dev``."""
+        s = self.shape
+        need = _lib.workspace_size(_lib.DFL_OP_DRAFT_STEP_HOST, N=s.N, C=s.C, B=s.B, d=s.d, Hq=s.Hq, Hkv=s.Hkv,
+                                   hd=s.hd, D=s.D, L=s.L, V=s.V, K=s.K, G=s.B - 1, row0=1, dtype=s.dt, F=s.F)
+        if need > self.ws_bytes:   # the context K/V of every layer is kept: a larger workspace
+            self.ws = torch.empty(need, dtype=torch.uint8, device=self.Xb.device)
+            self.ws_bytes = need
+        self._last_args = self._args(H_host, Xb0, target, vlog)
+        _lib.dfl_draft_step_host(self._last_args, H_dev, chunks, self.ws, self.ws_bytes, stream)
+
+    def step_from_host(self, H_host, Xb0_host, target_host=None, vlog_host=None, dev_in=None, stream=None,
+                       chunks=8):
         """End-to-end step: copy pinned host inputs in, run, copy results out.
 
         ``dev_in`` is a dict of preallocated device buffers with the inputs'
         shapes (allocated on first use).  Returns host tensors of the
-        per-sequence results.
+        per-sequence results.  For a bf16 model with pinned ``H_host`` the
+        hidden states go through ``dfl_draft_step_host``: copied in ``chunks``
+        groups of sequences while the groups already in are mixed and
+        projected (``chunks=0``: one copy, then the device step).
         """
         st = stream or torch.cuda.current_stream()
         if dev_in is None:
             dev_in = {}
+        overlap = chunks > 0 and self.shape.dt == DFL_BF16 and H_host.is_pinned()
         ins = {"H": H_host, "Xb0": Xb0_host, "target": target_host, "vlog": vlog_host}
         with torch.cuda.stream(st):
             for k, h in ins.items():
@@ -147,8 +163,13 @@ class DraftModel:
                     continue
                 if k not in dev_in:
                     dev_in[k] = torch.empty(h.shape, dtype=h.dtype, device=self.Xb.device)
-                dev_in[k].copy_(h, non_blocking=True)
-            self.step(dev_in["H"], dev_in["Xb0"], dev_in.get("target"), dev_in.get("vlog"), stream=st)
+                if not (overlap and k == "H"):
+                    dev_in[k].copy_(h, non_blocking=True)
+            if overlap:
+                self._step_host(H_host, dev_in["H"], dev_in["Xb0"], dev_in.get("target"), dev_in.get("vlog"),
+                                chunks, st)
+            else:
+                self.step(dev_in["H"], dev_in["Xb0"], dev_in.get("target"), dev_in.get("vlog"), stream=st)
             out = {"accept_len": self.accept_len.to("cpu", non_blocking=True),
                    "bonus": self.bonus.to("cpu", non_blocking=True)}
             if self.draft is not None:

@@ -87,7 +87,8 @@ typedef enum dfl_op {
     DFL_OP_TV_ACCEPTANCE = 6,
     DFL_OP_SPEC_ACCEPT = 7,
     DFL_OP_BLOCK_FFN = 8,
-    DFL_OP_DRAFT_STEP_CACHED = 9
+    DFL_OP_DRAFT_STEP_CACHED = 9,
+    DFL_OP_DRAFT_STEP_HOST = 10
 } dfl_op;
 
 /* Library version string (static storage). */
@@ -394,6 +395,28 @@ typedef struct dfl_step_args {
  */
 dfl_status dfl_draft_step(const dfl_step_args* args, void* ws, size_t ws_bytes,
                           dfl_stream stream);
+
+/*
+ * dfl_draft_step_host -- dfl_draft_step with the target hidden states in host
+ *   memory: the same results, bit for bit, as dfl_draft_step on a device copy
+ *   of args->H.  The copy is issued here, in `chunks` groups of whole
+ *   sequences on a copy stream the library owns (created on the first call),
+ *   and each group's mix and context K/V projections of all D layers run as
+ *   soon as its rows have landed, so they overlap the copy of the next group;
+ *   the block rows' projections, attention, LM head and epilogue follow the
+ *   last group.  bf16 only.
+ *   args->H   in, HOST [L][N*C][d] bf16 with args->h_layer_stride (pinned
+ *             memory, or the copies are not asynchronous)
+ *   H_dev     device buffer of the same layout, overwritten (the copy stream
+ *             first waits for the work already queued on `stream`)
+ *   chunks    1..16 groups (at most N)
+ *   ws        dfl_workspace_size(DFL_OP_DRAFT_STEP_HOST) bytes: the step's
+ *             workspace plus the context K/V of every layer
+ *   Errors: as dfl_draft_step; UNSUPPORTED_SHAPE for fp32 or shapes the bf16
+ *   tensor-core path does not take.
+ */
+dfl_status dfl_draft_step_host(const dfl_step_args* args, void* H_dev, int32_t chunks, void* ws, size_t ws_bytes,
+                               dfl_stream stream);
 
 /* Per-layer context K/V cache of a batch of sequences.  Host struct; the
  * tensors are device memory owned by the caller. */

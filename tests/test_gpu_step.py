@@ -181,6 +181,30 @@ def test_step_from_host_matches_device_step():
     assert np.array_equal(out["accept_len"].numpy(), geometric_prefix(w))
 
 
+@pytest.mark.parametrize("F,chunks", [(0, 1), (0, 2), (0, 5), (0, 16), (384, 3)])
+def test_host_input_step_is_bitwise_the_device_step(F, chunks):
+    # dfl_draft_step_host copies H in groups of sequences and mixes / projects
+    # each group as it lands: every row's arithmetic is the device step's, so
+    # the residual stream and the drafts must agree bit for bit.
+    w = Workload("hoststep", N=5, d=256, Hq=4, Hkv=2, hd=128, D=3, L=4, B=16, C=96, V=1500, dtype="bf16", seed=59,
+                 geom_p=0.3, F=F)
+    model, _ = _model(w)
+    H_host = torch.from_numpy(gen_hidden(w, as_bits=True).view(np.int16)).view(torch.bfloat16).pin_memory()
+    X0 = torch.from_numpy(gen_block_init(w)).cuda()
+    model.want_logits(True)
+    model.step(H_host.cuda(), X0)
+    torch.cuda.synchronize()
+    Xb_ref, drafts, z_ref = host(model.Xb).copy(), host(model.draft).copy(), host(model.logits).copy()
+    H_dev = torch.empty(H_host.shape, dtype=torch.bfloat16, device="cuda")
+    model.Xb.zero_()
+    model._step_host(H_host, H_dev, X0, None, None, chunks, torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    assert np.array_equal(host(model.Xb).view(np.uint32), Xb_ref.view(np.uint32))
+    assert np.array_equal(host(model.logits).view(np.uint32), z_ref.view(np.uint32))
+    assert np.array_equal(host(model.draft), drafts)
+    assert np.array_equal(host(H_dev.view(torch.int16)), H_host.view(torch.int16).numpy())
+
+
 # ---------------------------------------------------------- full sizes --
 
 def test_qwen3_8b_single_layer_full_size():
