@@ -281,12 +281,14 @@ dfl_status dual_kv_proj_bf16(DeviceCtx* ctx, const void* Xc, int64_t ctx_M, int 
 // and C_stride the context rows per sequence of Kc / Vc.
 dfl_status block_attn_bf16(DeviceCtx* ctx, const void* Q, const void* Kc, const void* Vc, const void* Kb,
                            const void* Vb, int N, int C, int B, int Hq, int Hkv, int hd, const void* Wo, int d,
-                           float* Xb, void* ws, const int32_t* ctx_len, int C_stride, cudaStream_t st) {
+                           float* Xb, void* ws, const int32_t* ctx_len, int C_stride, cudaStream_t st,
+                           int policy_N = 0) {
     const int qd = Hq * hd;
     dfl_status rc;
     uint8_t* p = static_cast<uint8_t*>(ws);
     void* O = carve(p, (size_t)N * B * qd * 2);
-    if ((rc = attn_bf16(Q, Kc, Vc, Kb, Vb, N, C, B, Hq, Hkv, hd, O, p, st, ctx_len, C_stride)) != DFL_OK) return rc;
+    if ((rc = attn_bf16(Q, Kc, Vc, Kb, Vb, N, C, B, Hq, Hkv, hd, O, p, st, ctx_len, C_stride, policy_N)) != DFL_OK)
+        return rc;
     GemmArgs g{};   // Xb += O Wo^T
     g.A = O; g.M = N * B; g.K = qd;
     g.B[0] = Wo; g.b_rows[0] = d; g.b_begin[0] = 0; g.nb = 1; g.N = d;
@@ -778,6 +780,11 @@ dfl_status draft_step_host_impl(const dfl_step_args* a, void* H_dev, int chunks,
     if (cudaEventRecord(ev[DeviceCtx::MAX_H_CHUNKS], st) != cudaSuccess ||
         cudaStreamWaitEvent(dctx->copy_st, ev[DeviceCtx::MAX_H_CHUNKS], 0) != cudaSuccess)
         return DFL_ERR_CUDA;
+    // Sequences are independent: with greedy drafts (no sampling epilogue) each
+    // group also runs its block path, LM head and acceptance as soon as its
+    // context is projected (the attention splits keys as for the whole batch,
+    // so every group's arithmetic is the whole-batch step's).
+    const bool group_tail = !a->sample && !a->vlog && (!a->logits || ((size_t)(a->B - 1) * a->V) % 4 == 0);
     const int nch = std::min(std::min(chunks, N), DeviceCtx::MAX_H_CHUNKS);
     const int per = (N + nch - 1) / nch;
     const uint8_t* Hh = static_cast<const uint8_t*>(a->H);
@@ -803,7 +810,33 @@ dfl_status draft_step_host_impl(const dfl_step_args* a, void* H_dev, int chunks,
                                             vc_of(l) + (size_t)r0 * kv * 2, nullptr);
             if ((rc = gemm_tc(dctx, gc, st)) != DFL_OK) return rc;
         }
+        if (!group_tail) continue;
+        const int Nc = n1 - n0;
+        float* Xb_c = a->Xb + (size_t)n0 * B * d;
+        for (int l = 0; l < D; ++l) {
+            const dfl_layer_weights& w = a->layers[l];
+            if ((rc = dual_kv_proj_bf16(dctx, nullptr, 0, C, Xb_c, Nc, B, d, a->blk_gain + (size_t)l * d, a->eps,
+                                        w.Wq, w.Wkc, w.Wvc, w.Wkb, w.Wvb, a->Hq, a->Hkv, a->hd, a->rope, Q, nullptr,
+                                        nullptr, Kb, Vb, sub, nullptr, st)) != DFL_OK)
+                return rc;
+            if ((rc = block_attn_bf16(dctx, Q, kc_of(l) + (size_t)r0 * kv * 2, vc_of(l) + (size_t)r0 * kv * 2, Kb, Vb,
+                                      Nc, C, B, a->Hq, a->Hkv, a->hd, w.Wo, d, Xb_c, sub, nullptr, C, st, N)) != DFL_OK)
+                return rc;
+            if (a->F > 0 && (rc = dfl_block_ffn(Xb_c, Nc, B, d, DFL_BF16, a->ffn_gain + (size_t)l * d, a->eps, w.W1,
+                                                w.W3, w.W2, a->F, sub, sub_bytes, stream)) != DFL_OK)
+                return rc;
+        }
+        if (a->V == 0) continue;
+        const size_t G = (size_t)(B - 1);
+        if ((rc = dfl_lm_head_argmax(Xb_c, Nc, B, 1, d, DFL_BF16, a->final_gain, a->eps, a->W_lm, a->V,
+                                     a->draft + (size_t)n0 * G, a->logits ? a->logits + (size_t)n0 * G * a->V : nullptr,
+                                     nullptr, nullptr, sub, sub_bytes, stream)) != DFL_OK)
+            return rc;
+        if (a->target && (rc = dfl_greedy_accept(a->draft + (size_t)n0 * G, a->target + (size_t)n0 * B, Nc, B - 1,
+                                                 a->accept_len + n0, a->bonus + n0, stream)) != DFL_OK)
+            return rc;
     }
+    if (group_tail) return DFL_OK;
     for (int l = 0; l < D; ++l) {
         const dfl_layer_weights& w = a->layers[l];
         if ((rc = dual_kv_proj_bf16(dctx, nullptr, 0, C, a->Xb, N, B, d, a->blk_gain + (size_t)l * d, a->eps, w.Wq,

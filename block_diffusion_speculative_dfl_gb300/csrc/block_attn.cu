@@ -320,9 +320,9 @@ size_t attn_ws_bytes(int N, int C, int B, int Hq, int Hkv, int hd, bool ragged) 
 
 dfl_status attn_bf16(const void* Q, const void* Kc, const void* Vc, const void* Kb, const void* Vb, int N, int C,
                      int B, int Hq, int Hkv, int hd, void* O, void* ws, cudaStream_t st, const int32_t* ctx_len,
-                     int C_stride) {
+                     int C_stride, int policy_N) {
     if (attn_tc_supported(B, Hq, Hkv, hd)) return attn_tc(Q, Kc, Vc, Kb, Vb, N, C, B, Hq, Hkv, hd, O, ws, st, ctx_len,
-                                                          C_stride);
+                                                          C_stride, policy_N);
     AttnArgs a{};
     a.ctx_len = ctx_len;
     a.C_stride = ctx_len ? C_stride : C;
@@ -332,7 +332,7 @@ dfl_status attn_bf16(const void* Q, const void* Kc, const void* Vc, const void* 
     a.Kb = static_cast<const __nv_bfloat16*>(Kb);
     a.Vb = static_cast<const __nv_bfloat16*>(Vb);
     a.N = N; a.C = C; a.B = B; a.Hq = Hq; a.Hkv = Hkv; a.G = Hq / Hkv; a.R = B * a.G;
-    a.S = attn_splits(N, C, B, Hkv);
+    a.S = attn_splits(policy_N > 0 ? policy_N : N, C, B, Hkv);
     const int tiles = (C + B + KT - 1) / KT;
     a.keys_per_split = ((tiles + a.S - 1) / a.S) * KT;
     a.O = static_cast<__nv_bfloat16*>(O);

@@ -742,7 +742,7 @@ size_t attn_tc_ws_bytes(int N, int C, int B, int Hq, int Hkv, int hd, bool ragge
 
 dfl_status attn_tc(const void* Q, const void* Kc, const void* Vc, const void* Kb, const void* Vb, int N, int C,
                    int B, int Hq, int Hkv, int hd, void* O, void* ws, cudaStream_t st, const int32_t* ctx_len,
-                   int C_stride) {
+                   int C_stride, int policy_N) {
     DeviceCtx* ctx = current_ctx();
     if (!ctx) return DFL_ERR_NO_DEVICE;
     const bool ragged = ctx_len != nullptr;
@@ -750,7 +750,7 @@ dfl_status attn_tc(const void* Q, const void* Kc, const void* Vc, const void* Kb
     a.N = N; a.B = B; a.Hq = Hq; a.Hkv = Hkv; a.G = Hq / Hkv;
     a.hs = at_head_subsets(B, a.G); a.Gq = a.G / a.hs; a.R = B * a.Gq;
     a.C = C; a.C_stride = ragged ? C_stride : C; a.ctx_len = ctx_len;
-    a.kps = attn_tc_kps(N * Hkv * a.hs, C, B, ragged);
+    a.kps = attn_tc_kps((policy_N > 0 ? policy_N : N) * Hkv * a.hs, C, B, ragged);
     a.S = (C + B + a.kps - 1) / a.kps;
     a.items = a.S * N * Hkv * a.hs;
     const size_t NQ = (size_t)N * B * Hq;

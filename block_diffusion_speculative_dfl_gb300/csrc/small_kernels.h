@@ -45,12 +45,15 @@ int attn_tc_kps(int units, int C, int B, bool ragged);   // units: (sequence, K/
 size_t attn_tc_ws_bytes(int N, int C, int B, int Hq, int Hkv, int hd, bool ragged);
 dfl_status attn_tc(const void* Q, const void* Kc, const void* Vc, const void* Kb, const void* Vb, int N, int C,
                    int B, int Hq, int Hkv, int hd, void* O, void* ws, cudaStream_t st, const int32_t* ctx_len,
-                   int C_stride);
+                   int C_stride, int policy_N = 0);
 // ctx_len (nullable, device [N]): per-sequence context keys, with C the
 // maximum (C_stride context rows per sequence in Kc / Vc).
 dfl_status attn_bf16(const void* Q, const void* Kc, const void* Vc, const void* Kb, const void* Vb, int N, int C,
                      int B, int Hq, int Hkv, int hd, void* O, void* ws, cudaStream_t st,
-                     const int32_t* ctx_len = nullptr, int C_stride = 0);
+                     const int32_t* ctx_len = nullptr, int C_stride = 0, int policy_N = 0);
+// policy_N (0: N): the batch size that decides how keys are split over work
+// items, so that a call on a group of sequences splits them as a call on the
+// whole batch of policy_N sequences would (same arithmetic, same bits).
 
 // TV acceptance diagnostic and stochastic acceptance (workspace bytes)
 size_t tv_ws_bytes(int N, int K, int G);

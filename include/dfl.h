@@ -403,8 +403,9 @@ dfl_status dfl_draft_step(const dfl_step_args* args, void* ws, size_t ws_bytes,
  *   sequences on a copy stream the library owns (created on the first call),
  *   and each group's mix and context K/V projections of all D layers run as
  *   soon as its rows have landed, so they overlap the copy of the next group;
- *   the block rows' projections, attention, LM head and epilogue follow the
- *   last group.  bf16 only.
+ *   with greedy drafts (no `sample`) the group's block rows, LM head and
+ *   acceptance follow at once too (sequences are independent), otherwise
+ *   they run for all sequences after the last group.  bf16 only.
  *   args->H   in, HOST [L][N*C][d] bf16 with args->h_layer_stride (pinned
  *             memory, or the copies are not asynchronous)
  *   H_dev     device buffer of the same layout, overwritten (the copy stream
