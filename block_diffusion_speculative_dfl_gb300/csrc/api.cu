@@ -536,8 +536,6 @@ extern "C" dfl_status dfl_self_select(const void* vlog, dfl_dtype dt, const int3
 namespace dfl {
 namespace {
 
-// The whole draft step; with `cache`, the incremental form over the caller's
-// context K/V cache (args->C its capacity, args->H the R new rows per sequence).
 // Shapes the bf16 tensor-core path of a step takes (TMA strides, tile widths).
 dfl_status step_bf16_shape(const dfl_step_args* a) {
     if (a->Hq <= 0 || a->Hkv <= 0 || a->Hq % a->Hkv != 0 || (a->hd != 64 && a->hd != 128))
@@ -594,6 +592,8 @@ dfl_shape step_shape(const dfl_step_args* a, const dfl_ctx_cache* cache) {
 dfl_status step_tail(const dfl_step_args* a, const dfl_shape& s, uint8_t* Xc, size_t xc_bytes, int32_t* samples,
                      uint8_t* sub, size_t sub_bytes, dfl_stream stream);
 
+// The whole draft step; with `cache`, the incremental form over the caller's
+// context K/V cache (args->C its capacity, args->H the R new rows per sequence).
 dfl_status draft_step_impl(const dfl_step_args* a, const dfl_ctx_cache* cache, void* ws, size_t ws_bytes,
                            dfl_stream stream) {
     dfl_status rc = step_check(a, cache, ws);

@@ -67,3 +67,47 @@ def test_step_workspace_grows_with_layers(dt):
     b = dfl.workspace_size(dfl.DFL_OP_DRAFT_STEP, N=1, C=64, B=16, d=256, Hq=4, Hkv=4, hd=64, D=2, L=3, V=1000,
                            K=0, G=15, row0=1, dtype=dt)
     assert b - a >= 64 * 256 * (2 if dt else 4)
+
+
+def _host_step_args(dtype=1):
+    """A dfl_step_args whose device pointers are stand-in aligned addresses.
+
+    Only the host-side checks read it; nothing is dereferenced on the device.
+    """
+    lib = dfl._lib
+    fake = 1 << 20
+    layers = (lib.LayerWeights * 2)()
+    for w in layers:
+        for n, _ in lib.LayerWeights._fields_[:6]:
+            setattr(w, n, fake)
+    a = lib.StepArgs()
+    a.N, a.C, a.B, a.d, a.Hq, a.Hkv, a.hd, a.D, a.L, a.V, a.dtype = 2, 64, 16, 256, 4, 2, 64, 2, 3, 1000, dtype
+    a.eps, a.h_layer_stride = 1e-6, 2 * 64 * 256
+    for n in ("H", "mix_logits", "mix_gain", "blk_gain", "final_gain", "W_lm", "Xb0", "Xb", "draft"):
+        setattr(a, n, fake)
+    a.layers = layers
+    return a, layers
+
+
+def test_host_input_step_rejects_bad_arguments_on_the_host():
+    lib = dfl.load()
+    shape = dict(N=2, C=64, B=16, d=256, Hq=4, Hkv=2, hd=64, D=2, L=3, V=1000, K=0, G=15, row0=1, dtype=1)
+    need = dfl.workspace_size(dfl.DFL_OP_DRAFT_STEP_HOST, **shape)
+    assert need > dfl.workspace_size(dfl.DFL_OP_DRAFT_STEP, **shape)   # plus the context K/V of the later layers
+    fake = 1 << 20
+    a, keep = _host_step_args()
+    call = lambda args, H_dev=fake, chunks=2, ws=fake, nbytes=need: lib.dfl_draft_step_host(
+        ctypes.byref(args), H_dev, chunks, ws, nbytes, None)
+    assert call(a, H_dev=None) == 1                  # no device copy of H
+    assert call(a, chunks=0) == 1                    # at least one group
+    assert call(a, ws=None) == 1
+    assert call(a, H_dev=fake + 8) == 3              # H_dev off the 16-byte rule
+    assert call(a, nbytes=need - 1) == 4             # workspace one byte short
+    b, keep_b = _host_step_args(dtype=0)
+    assert call(b) == 2                              # fp32 has no host-input path
+    a.h_layer_stride = 2 * 64 * 256 - 8
+    assert call(a) == 1                              # layer slabs overlap
+    a.h_layer_stride, a.hd = 2 * 64 * 256, 96
+    assert call(a) == 2                              # head size without a kernel
+    a.hd, a.Xb = 64, None
+    assert call(a) == 1
