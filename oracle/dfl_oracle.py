@@ -535,19 +535,21 @@ def speculative_accept(z_rows, T: float, v_rows, x, u_acc, u_res):
     accepted the bonus token is drawn from P_{G+1} with u_res[G].  This keeps
     the verifier's distribution (the DFlare post's "proper acceptance
     procedure" for stochastic decoding).  Returns (accepted, token, margin):
-    margin is the relative distance of the deciding test or draw to its
-    boundary (how close floating point came to changing the result).
+    margin is the smallest relative distance to its boundary over every test
+    made (accepted ones included: any of them could flip the result) and the
+    final draw, i.e. how close floating point came to changing the result.
     """
     G = len(x)
+    near = np.inf
     for j in range(G):
         Q = softmax_t(z_rows[j], T)
         P = softmax_t(v_rows[j])
         q, p = Q[x[j]], P[x[j]]
+        near = min(near, abs(u_acc[j] * q - p) / max(p, 1e-300))
         if u_acc[j] * q < p:
             continue
-        acc_margin = abs(u_acc[j] * q - p) / max(p, 1e-300)
         r = np.maximum(P - Q, 0.0)
         y, m = inverse_cdf(r, u_res[j])
-        return j, y, min(acc_margin, m)
+        return j, y, min(near, m)
     y, m = inverse_cdf(softmax_t(v_rows[G]), u_res[G])
-    return G, y, m
+    return G, y, min(near, m)

@@ -540,6 +540,38 @@ def test_inverse_cdf_grid_and_margin():
     w = np.array([1.0, 0.0, 3.0])
     assert orc.inverse_cdf(w, 0.1)[0] == 0 and orc.inverse_cdf(w, 0.3)[0] == 2
     assert orc.inverse_cdf(w, 0.25)[1] == 0.0                    # exactly on a boundary
+    v, margin = orc.inverse_cdf(w, 0.6)          # u*total = 2.4 in (1, 4]: 1.4 and 1.6 away, / 4
+    assert v == 2 and abs(margin - 0.35) < 1e-15
+
+
+def test_sampling_margin_worked_example():
+    # weights (1, 1, 2), total 4, cumulative (1, 2, 4)
+    for T in (1.0, 2.0):
+        z = T * np.log([1.0, 1.0, 2.0])
+        v, margin = orc.sample_inverse_cdf(z, T, 0.3)    # 1.2: 0.2 above 1, 0.8 below 2
+        assert v == 1 and abs(margin - 0.05) < 1e-12
+        v, margin = orc.sample_inverse_cdf(z, T, 0.45)   # 1.8: 0.8 above 1, 0.2 below 2
+        assert v == 1 and abs(margin - 0.05) < 1e-12
+        v, margin = orc.sample_inverse_cdf(z, T, 0.9)    # 3.6: 1.6 above 2, 0.4 below 4
+        assert v == 2 and abs(margin - 0.1) < 1e-12
+
+
+def test_speculative_accept_margin_worked_example():
+    # Q = (1/2, 1/2), P_1 = (0.2, 0.8), P_2 = (0.25, 0.75); draft token 0 (q = 1/2, p = 0.2)
+    z, v1, v2 = np.zeros(2), np.log([0.2, 0.8]), np.log([0.25, 0.75])
+    run = lambda ua, ur: orc.speculative_accept([z], 1.0, [v1, v2], [0], [ua], ur)
+    # rejected (0.3 >= 0.2, test 0.5 away); residual (0, 0.3) at 0.06: 0.2 of it away
+    a, y, m = run(0.6, [0.2, 0.5])
+    assert (a, y) == (0, 1) and abs(m - 0.2) < 1e-12
+    # rejected closer to the boundary (0.225 vs 0.2: 0.125 of p)
+    a, y, m = run(0.45, [0.2, 0.5])
+    assert (a, y) == (0, 1) and abs(m - 0.125) < 1e-12
+    # accepted (0.15 < 0.2, 0.25 away); bonus from P_2 at 0.4: 0.15 away
+    a, y, m = run(0.3, [0.5, 0.4])
+    assert (a, y) == (1, 1) and abs(m - 0.15) < 1e-12
+    # accepted close to the boundary (0.19 vs 0.2): the accepted test sets the margin
+    a, y, m = run(0.38, [0.5, 0.4])
+    assert (a, y) == (1, 1) and abs(m - 0.05) < 1e-12
 
 
 def _spec_output_distribution(z, T, v, n_grid=400):
@@ -600,6 +632,18 @@ def test_uniform_streams_are_distinct():
     a = orc.draw_uniform_stream(7, 1, 2, 0, 0)
     assert a == orc.draw_uniform(7, 1, 2, 0)
     assert len({orc.draw_uniform_stream(7, 1, 2, 0, s) for s in range(3)}) == 3
+
+
+@pytest.mark.parametrize("case", _golden_philox())
+def test_uniform_counter_words_follow_the_known_answers(case):
+    # (sequence, window row, draft, stream) are counter words 0..3 and the seed's
+    # low/high halves key words 0/1: the published vectors fix the mapping.
+    c, k, x = case
+    seed = k[0] | (k[1] << 32)
+    want = ((x[0] >> 8) + 0.5) * 2.0 ** -24
+    assert orc.draw_uniform_stream(seed, c[0], c[1], c[2], c[3]) == want
+    if c[3] == 0:
+        assert orc.draw_uniform(seed, c[0], c[1], c[2]) == want
 
 
 
