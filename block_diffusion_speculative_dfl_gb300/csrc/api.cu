@@ -739,10 +739,20 @@ dfl_status draft_step_host_impl(const dfl_step_args* a, void* H_dev, int chunks,
     if (ws_bytes < step_host_ws_bytes(s)) return DFL_ERR_WORKSPACE;
     DeviceCtx* dctx = current_ctx();
     if (!dctx) return DFL_ERR_NO_DEVICE;
-    if (!dctx->copy_st) {
-        if (cudaStreamCreateWithFlags(&dctx->copy_st, cudaStreamNonBlocking) != cudaSuccess) return DFL_ERR_CUDA;
-        for (cudaEvent_t& e : dctx->copy_ev)
-            if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return DFL_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(dctx->host_mu);
+    if (!dctx->copy_st) {   // all or nothing: a failed creation leaves nothing half made
+        cudaStream_t cs = nullptr;
+        cudaEvent_t ev[DeviceCtx::MAX_H_CHUNKS + 1] = {};
+        bool ok = cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking) == cudaSuccess;
+        for (cudaEvent_t& e : ev) ok = ok && cudaEventCreateWithFlags(&e, cudaEventDisableTiming) == cudaSuccess;
+        if (!ok) {
+            for (cudaEvent_t e : ev)
+                if (e) cudaEventDestroy(e);
+            if (cs) cudaStreamDestroy(cs);
+            return DFL_ERR_CUDA;
+        }
+        for (int i = 0; i <= DeviceCtx::MAX_H_CHUNKS; ++i) dctx->copy_ev[i] = ev[i];
+        dctx->copy_st = cs;
     }
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const int N = a->N, C = a->C, B = a->B, d = a->d, L = a->L, D = a->D;

@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "../../include/dfl.h"
 #include "gemm_tc.cuh"
 
@@ -19,7 +21,10 @@ struct DeviceCtx {
     bool mix_attr_set = false;
     bool attn_attr_set[4] = {};    // tcgen05 attention: head dim 64 / 128, M = 64 / 128 products
     // Host-input draft step: a copy stream and events, created on first use.
+    // host_mu is held while a call issues its work: the events are shared, and
+    // a wait must see the record its own call made.
     static constexpr int MAX_H_CHUNKS = 16;
+    std::mutex host_mu;
     cudaStream_t copy_st = nullptr;
     cudaEvent_t copy_ev[MAX_H_CHUNKS + 1] = {};
 };

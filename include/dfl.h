@@ -410,9 +410,12 @@ dfl_status dfl_draft_step(const dfl_step_args* args, void* ws, size_t ws_bytes,
  *             memory, or the copies are not asynchronous)
  *   H_dev     device buffer of the same layout, overwritten (the copy stream
  *             first waits for the work already queued on `stream`)
- *   chunks    1..16 groups (at most N)
+ *   chunks    number of groups, >= 1 (above min(N, 16) it is taken as that)
  *   ws        dfl_workspace_size(DFL_OP_DRAFT_STEP_HOST) bytes: the step's
  *             workspace plus the context K/V of every layer
+ *   Calls on one device from several host threads are issued one at a time
+ *   (they share the copy stream and its events); their work still runs on
+ *   their own streams.
  *   Errors: as dfl_draft_step; UNSUPPORTED_SHAPE for fp32 or shapes the bf16
  *   tensor-core path does not take.
  */
