@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "../../include/dfl.h"
@@ -17,9 +18,11 @@ struct DeviceCtx {
     int device = -1;
     int sm_count = 0;
     int* err_word = nullptr;       // device address of this device's error word
-    bool gemm_attr_set[16] = {};   // max-dynamic-smem set for gemm instantiations
-    bool mix_attr_set = false;
-    bool attn_attr_set[4] = {};    // tcgen05 attention: head dim 64 / 128, M = 64 / 128 products
+    // max-dynamic-smem attribute set (atomic: calls may come from several
+    // host threads; setting it twice is harmless)
+    std::atomic<bool> gemm_attr_set[16] = {};   // gemm instantiations
+    std::atomic<bool> mix_attr_set{false};
+    std::atomic<bool> attn_attr_set[4] = {};    // tcgen05 attention: head dim 64 / 128, M = 64 / 128 products
     // Host-input draft step: a copy stream and events, created on first use.
     // host_mu is held while a call issues its work: the events are shared, and
     // a wait must see the record its own call made.
