@@ -111,3 +111,22 @@ def test_host_input_step_rejects_bad_arguments_on_the_host():
     assert call(a) == 2                              # head size without a kernel
     a.hd, a.Xb = 64, None
     assert call(a) == 1
+
+
+def test_header_is_plain_c_and_links(tmp_path):
+    # A C99 program (tests/c_abi_host_calls.c) built with -pedantic -Werror
+    # against include/dfl.h and libdfl.so, run on the host.
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    dfl.build()
+    root = os.path.dirname(os.path.dirname(__file__))
+    libdir = os.path.dirname(dfl.LIB)
+    exe = str(tmp_path / "host_calls")
+    subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror", "-I", os.path.join(root, "include"),
+                    os.path.join(root, "tests", "c_abi_host_calls.c"), "-L", libdir, "-ldfl",
+                    "-Wl,-rpath," + libdir, "-o", exe], check=True)
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0 and r.stdout.strip() == "ok", r.stderr
