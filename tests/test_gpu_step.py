@@ -205,6 +205,37 @@ def test_host_input_step_is_bitwise_the_device_step(F, chunks):
     assert np.array_equal(host(H_dev.view(torch.int16)), H_host.view(torch.int16).numpy())
 
 
+def test_step_replays_from_a_cuda_graph():
+    # A call neither allocates nor synchronises and its pointers and launch
+    # shapes are fixed for a shape, so a step captured once into a CUDA graph
+    # replays the eager step bit for bit.
+    w = Workload("graph", N=3, d=256, Hq=4, Hkv=2, hd=128, D=2, L=3, B=16, C=96, V=1500, dtype="bf16", seed=61,
+                 geom_p=0.3)
+    model, _ = _model(w)
+    model.want_logits(True)
+    H = _hidden_dev(w)
+    X0 = torch.from_numpy(gen_block_init(w)).cuda()
+    model.step(H, X0)
+    torch.cuda.synchronize()
+    target = torch.from_numpy(plant_targets(w, host(model.draft))).cuda()
+    model.step(H, X0, target=target)   # eager, outside any capture
+    torch.cuda.synchronize()
+    ref = {k: host(getattr(model, k)).copy() for k in ("Xb", "logits", "draft", "accept_len", "bonus")}
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        model.step(H, X0, target=target)
+    for k in ref:
+        getattr(model, k).zero_()
+    torch.cuda.synchronize()
+    for _ in range(2):
+        g.replay()
+        torch.cuda.synchronize()
+        for k, v in ref.items():
+            got = host(getattr(model, k))
+            assert np.array_equal(got.view(np.uint32), v.view(np.uint32)), k
+    assert np.array_equal(ref["accept_len"], geometric_prefix(w))
+
+
 # ---------------------------------------------------------- full sizes --
 
 def test_qwen3_8b_single_layer_full_size():
