@@ -94,7 +94,8 @@ typedef enum dfl_op {
 /* Library version string (static storage). */
 const char* dfl_version(void);
 
-/* Message for a status code (static storage). */
+/* Message for a status code (static storage); "unknown status" for a code
+ * outside dfl_status. */
 const char* dfl_status_string(dfl_status s);
 
 /* Bytes of scratch the operation needs for this shape; 0 if it needs none or
@@ -466,13 +467,16 @@ dfl_status dfl_draft_step_cached(const dfl_step_args* args, const dfl_ctx_cache*
 dfl_status dfl_get_device_error(dfl_stream stream, int32_t* code);
 
 /* Upper bound, in nanoseconds, on any single device-side wait (mbarrier or
- * flag) in subsequently launched kernels.  Default 2e9 (2 s). */
+ * flag) in subsequently launched kernels.  Default 2e9 (2 s); process-wide.
+ * Errors: INVALID_ARG for 0. */
 dfl_status dfl_set_wait_limit_ns(uint64_t ns);
 
 /* Self-test of the bounded wait: launches one block that waits on an
  * mbarrier no thread arrives at, for at most limit_ns; the kernel records
  * DFL_ERR_TIMEOUT in *status_out (device int32) and returns.  Used by tests
- * to show that a wait which runs out leaves the context usable. */
+ * to show that a wait which runs out leaves the context usable.
+ * Errors: INVALID_ARG (status_out NULL, limit_ns 0 or above 1e10),
+ * NO_DEVICE, CUDA. */
 dfl_status dfl_selftest_bounded_wait(uint64_t limit_ns, int32_t* status_out,
                                      dfl_stream stream);
 
