@@ -4,6 +4,7 @@
 #include <atomic>
 #include <cstdio>
 #include <cstring>
+#include <initializer_list>
 #include <mutex>
 #include <string>
 #include <vector>
@@ -146,7 +147,10 @@ extern "C" const char* dfl_status_string(dfl_status s) {
 }
 
 extern "C" size_t dfl_workspace_size(dfl_op op, const dfl_shape* s) {
-    if (!s) return 0;
+    if (!s || (s->dtype != DFL_F32 && s->dtype != DFL_BF16)) return 0;
+    // every size is a count: a negative one makes the shape invalid
+    for (int32_t v : {s->N, s->C, s->B, s->d, s->Hq, s->Hkv, s->hd, s->D, s->L, s->V, s->K, s->G, s->row0, s->F, s->R})
+        if (v < 0) return 0;
     switch (op) {
         case DFL_OP_DUAL_KV_PROJ: return ws_dual_kv_proj(s->N, s->B, s->d, s->dtype);
         case DFL_OP_BLOCK_ATTN: return ws_block_attn(s->N, s->C, s->B, s->Hq, s->Hkv, s->hd, s->dtype);

@@ -130,3 +130,27 @@ def test_header_is_plain_c_and_links(tmp_path):
                     "-Wl,-rpath," + libdir, "-o", exe], check=True)
     r = subprocess.run([exe], capture_output=True, text=True, timeout=120)
     assert r.returncode == 0 and r.stdout.strip() == "ok", r.stderr
+
+
+_OPS = ["DFL_OP_DUAL_KV_PROJ", "DFL_OP_BLOCK_ATTN", "DFL_OP_LM_HEAD", "DFL_OP_SELF_SELECT", "DFL_OP_DRAFT_STEP",
+        "DFL_OP_TV_ACCEPTANCE", "DFL_OP_SPEC_ACCEPT", "DFL_OP_BLOCK_FFN", "DFL_OP_DRAFT_STEP_CACHED",
+        "DFL_OP_DRAFT_STEP_HOST"]
+_SHAPE = dict(N=3, C=96, B=16, d=256, Hq=4, Hkv=2, hd=128, D=2, L=3, V=1500, K=4, G=15, row0=1, dtype=1, F=384, R=8)
+
+
+@pytest.mark.parametrize("op", _OPS)
+def test_workspace_size_is_zero_for_invalid_shapes(op):
+    code = getattr(dfl._lib, op)
+    ok = dfl.workspace_size(code, **_SHAPE)
+    assert 0 < ok < 1 << 32
+    assert dfl.workspace_size(code, **dict(_SHAPE, dtype=7)) == 0
+    for k in _SHAPE:
+        if k != "dtype":
+            assert dfl.workspace_size(code, **dict(_SHAPE, **{k: -1})) == 0, k
+
+
+@pytest.mark.parametrize("op", ["DFL_OP_DRAFT_STEP", "DFL_OP_DRAFT_STEP_CACHED", "DFL_OP_DRAFT_STEP_HOST"])
+def test_step_workspace_grows_with_the_batch(op):
+    code = getattr(dfl._lib, op)
+    sizes = [dfl.workspace_size(code, **dict(_SHAPE, N=n)) for n in (1, 2, 4, 8)]
+    assert all(a < b for a, b in zip(sizes, sizes[1:])), sizes
