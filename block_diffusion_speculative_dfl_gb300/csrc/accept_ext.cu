@@ -399,6 +399,8 @@ extern "C" dfl_status dfl_tv_acceptance(const float* logits, float T, const void
         !(T > 0.f))
         return DFL_ERR_INVALID_ARG;
     if (dt != DFL_F32 && dt != DFL_BF16) return DFL_ERR_INVALID_ARG;
+    // rows are read with 16-byte loads when V % 8 == 0
+    if (!aligned16(logits) || !aligned16(vlog) || !aligned16(ws)) return DFL_ERR_MISALIGNED;
     if (ws_bytes < tv_ws_bytes(N, K, G)) return DFL_ERR_WORKSPACE;
     if (!current_ctx()) return DFL_ERR_NO_DEVICE;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -427,6 +429,7 @@ extern "C" dfl_status dfl_spec_accept(const float* logits, float T, const void* 
         G > 1024 || V <= 0 || !(T > 0.f))
         return DFL_ERR_INVALID_ARG;
     if (dt != DFL_F32 && dt != DFL_BF16) return DFL_ERR_INVALID_ARG;
+    if (!aligned16(logits) || !aligned16(vlog) || !aligned16(ws)) return DFL_ERR_MISALIGNED;
     if (ws_bytes < spec_ws_bytes(N, G, V)) return DFL_ERR_WORKSPACE;
     if (!current_ctx()) return DFL_ERR_NO_DEVICE;
     cudaStream_t st = static_cast<cudaStream_t>(stream);

@@ -573,6 +573,24 @@ dfl_status step_check(const dfl_step_args* a, const dfl_ctx_cache* cache, const 
         if (!w.Wq || !w.Wkc || !w.Wvc || !w.Wkb || !w.Wvb || !w.Wo) return DFL_ERR_INVALID_ARG;
         if (a->F > 0 && (!w.W1 || !w.W3 || !w.W2)) return DFL_ERR_INVALID_ARG;
     }
+    // Shape rules of the calls the step makes that hold for every dtype (each
+    // with the status that call returns), checked before the first launch.
+    if (a->L > 16 || a->Hq <= 0 || a->Hkv <= 0 || a->hd <= 0 || a->Hq % a->Hkv != 0) return DFL_ERR_INVALID_ARG;
+    const int64_t h_rows = (int64_t)a->N * (cache ? cache->R : a->C);
+    if (a->L > 1 && a->h_layer_stride < h_rows * a->d) return DFL_ERR_INVALID_ARG;
+    if (a->d % 8 != 0 || a->hd % 8 != 0 || a->F % 8 != 0 || a->h_layer_stride % 8 != 0)
+        return DFL_ERR_MISALIGNED;
+    // The 16-byte rule of every kernel the step launches, likewise.
+    const void* al[] = {ws, a->Xb, a->mix_gain, a->blk_gain, a->final_gain, a->W_lm, a->rope, a->ffn_gain,
+                        a->logits, a->vlog};
+    for (const void* q : al)
+        if (q && !aligned16(q)) return DFL_ERR_MISALIGNED;
+    for (int l = 0; l < a->D; ++l) {
+        const dfl_layer_weights& w = a->layers[l];
+        const void* wl[] = {w.Wq, w.Wkc, w.Wvc, w.Wkb, w.Wvb, w.Wo, w.W1, w.W3, w.W2};
+        for (const void* q : wl)
+            if (q && !aligned16(q)) return DFL_ERR_MISALIGNED;
+    }
     if (cache) {
         if (dt != DFL_BF16) return DFL_ERR_UNSUPPORTED_SHAPE;
         if (!cache->K || !cache->V || !cache->ctx_len || !cache->n_new || cache->R < 1) return DFL_ERR_INVALID_ARG;
@@ -602,6 +620,7 @@ dfl_status draft_step_impl(const dfl_step_args* a, const dfl_ctx_cache* cache, v
                            dfl_stream stream) {
     dfl_status rc = step_check(a, cache, ws);
     if (rc != DFL_OK) return rc;
+    if (!aligned16(a->H)) return DFL_ERR_MISALIGNED;   // read by the mix's bulk copies
     const int dt = a->dtype;
     const dfl_shape s = step_shape(a, cache);
     if (ws_bytes < step_ws_bytes(s, cache != nullptr)) return DFL_ERR_WORKSPACE;

@@ -282,7 +282,7 @@ dfl_status dfl_self_select_noalloc(const void* vlog, dfl_dtype dt, const int32_t
  *   alpha   out, fp32 [N][K][G]; tokens_per_draft out (nullable) fp32 [N][K]
  *   ws      dfl_workspace_size(DFL_OP_TV_ACCEPTANCE) bytes (row log-sum-exps)
  *   Errors: INVALID_ARG (K outside 1..64, G outside 1..1024, T <= 0),
- *   WORKSPACE.
+ *   MISALIGNED (logits, vlog or ws), WORKSPACE.
  */
 dfl_status dfl_tv_acceptance(const float* logits, float T, const void* vlog, dfl_dtype dt,
                              int32_t N, int32_t K, int32_t G, int32_t V, float* alpha,
@@ -305,7 +305,7 @@ dfl_status dfl_tv_acceptance(const float* logits, float T, const void* vlog, dfl
  *           draft 0); a token outside [0, V) is rejected
  *   accept_len out, int32 [N] (accepted drafts, 0..G); next_token out, int32 [N]
  *   ws      dfl_workspace_size(DFL_OP_SPEC_ACCEPT) bytes (N, G and V of the shape)
- *   Errors: INVALID_ARG, WORKSPACE.
+ *   Errors: INVALID_ARG, MISALIGNED (logits, vlog or ws), WORKSPACE.
  */
 dfl_status dfl_spec_accept(const float* logits, float T, const void* vlog, dfl_dtype dt,
                            const int32_t* drafts, const int32_t* sel, int32_t N, int32_t K,
@@ -391,8 +391,12 @@ typedef struct dfl_step_args {
  *   (whose results replace accept_len/bonus).  V == 0 stops after the layers.
  *   ws: dfl_workspace_size(DFL_OP_DRAFT_STEP) bytes holding the mixed context
  *   features of all D layers and each layer's Q/K/V.
- *   Errors: those of the calls it makes; nothing is launched on a host-side
- *   argument error.
+ *   Errors: those of the calls it makes.  Null pointers, sizes, the 16-byte
+ *   rule of every pointer and the shape rules that hold for both dtypes are
+ *   checked before anything is launched.  A shape that one kernel does not
+ *   take (UNSUPPORTED_SHAPE, e.g. a bf16 width outside a tile rule) can be
+ *   found after earlier calls of the step were queued; the outputs are then
+ *   undefined.
  */
 dfl_status dfl_draft_step(const dfl_step_args* args, void* ws, size_t ws_bytes,
                           dfl_stream stream);

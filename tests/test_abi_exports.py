@@ -154,3 +154,100 @@ def test_step_workspace_grows_with_the_batch(op):
     code = getattr(dfl._lib, op)
     sizes = [dfl.workspace_size(code, **dict(_SHAPE, N=n)) for n in (1, 2, 4, 8)]
     assert all(a < b for a, b in zip(sizes, sizes[1:])), sizes
+
+
+_FAKE = 1 << 20   # stand-in device address (16-byte aligned); never dereferenced here
+
+
+def _no_device(lib):
+    # The sweep below passes stand-in addresses: it runs only where the library
+    # finds no usable device, so that a call that passes its host checks stops
+    # at NO_DEVICE instead of launching.
+    code = ctypes.c_int32(0)
+    return lib.dfl_get_device_error(None, ctypes.byref(code)) == 7
+
+
+def _entry_points():
+    """(function, valid arguments, indices of the pointers that may not be NULL,
+    indices of those read or written with 16-byte or TMA accesses)."""
+    sz = lambda op, **k: dfl.workspace_size(op, **k)
+    F = _FAKE
+    s = dict(N=2, C=64, B=16, d=256, Hq=4, Hkv=2, hd=128, dtype=1)
+    ws_kv = sz(dfl.DFL_OP_DUAL_KV_PROJ, **s)
+    ws_at = sz(dfl.DFL_OP_BLOCK_ATTN, **s)
+    ws_lm = sz(dfl.DFL_OP_LM_HEAD, N=2, B=16, row0=1, d=256, V=1000, dtype=1)
+    ws_sel = sz(dfl.DFL_OP_SELF_SELECT, N=2, K=4, G=8, V=1000, dtype=1)
+    ws_tv = sz(dfl.DFL_OP_TV_ACCEPTANCE, N=2, K=4, G=8, V=1000, dtype=1)
+    ws_sp = sz(dfl.DFL_OP_SPEC_ACCEPT, N=2, K=4, G=8, V=1000, dtype=1)
+    ws_ffn = sz(dfl.DFL_OP_BLOCK_FFN, N=2, B=16, d=256, F=384, dtype=1)
+    return [
+        ("dfl_rope_table", [F, 80, 128, 1e6, None], [0], []),
+        ("dfl_layer_mix_rmsnorm", [F, 64 * 256, 3, 64, 256, 1, 2, F, F, 1e-6, F, 64 * 256, None], [0, 7, 8, 10], [0, 8, 10]),
+        ("dfl_dual_kv_proj", [F, F, 2, 64, 16, 256, 1, F, 1e-6, F, F, F, F, F, 4, 2, 128, None,
+                              F, F, F, F, F, F, ws_kv, None], [0, 1, 7, 9, 10, 11, 12, 13, 18, 19, 20, 21, 22, 23],
+         [0, 1, 7, 9, 10, 11, 12, 13, 18, 19, 20, 21, 22, 23]),
+        ("dfl_block_attn", [F, F, F, F, F, 2, 64, 16, 4, 2, 128, 1, F, 256, F, F, ws_at, None],
+         [0, 1, 2, 3, 4, 12, 14, 15], [0, 1, 2, 3, 4, 12, 14, 15]),
+        ("dfl_lm_head_argmax", [F, 2, 16, 1, 256, 1, F, 1e-6, F, 1000, F, None, None, None, F, ws_lm, None],
+         [0, 6, 8, 10, 14], [0, 6, 8, 14]),
+        ("dfl_greedy_accept", [F, F, 2, 15, F, F, None], [0, 1, 4, 5], []),
+        ("dfl_self_select", [F, 1, F, 2, 4, 8, 1000, F, F, F, F, F, ws_sel, None], [0, 2, 7, 8, 9, 10, 11], [0, 11]),
+        ("dfl_self_select_noalloc", [F, 1, F, 2, 4, 8, 1000, F, F, F, F, None], [0, 2, 7, 8, 9, 10], [0]),
+        ("dfl_tv_acceptance", [F, 1.5, F, 1, 2, 4, 8, 1000, F, None, F, ws_tv, None], [0, 2, 8, 10], [0, 2, 10]),
+        ("dfl_spec_accept", [F, 1.5, F, 1, F, None, 2, 4, 8, 1000, 7, F, F, F, ws_sp, None], [0, 2, 4, 11, 12, 13], [0, 2, 13]),
+        ("dfl_block_ffn", [F, 2, 16, 256, 1, F, 1e-6, F, F, F, 384, F, ws_ffn, None], [0, 5, 7, 8, 9, 11], [0, 5, 7, 8, 9, 11]),
+    ]
+
+
+@pytest.mark.parametrize("name,args,required,vec", _entry_points(), ids=lambda v: v if isinstance(v, str) else "")
+def test_every_required_pointer_is_checked_on_the_host(name, args, required, vec):
+    lib = dfl.load()
+    if not _no_device(lib):
+        pytest.skip("a usable device is present: the sweep's stand-in addresses must not reach a launch")
+    fn = getattr(lib, name)
+    assert fn(*args) == 7, "valid arguments should pass every host check and stop at NO_DEVICE"
+    for i in required:
+        bad = list(args)
+        bad[i] = None
+        assert fn(*bad) == 1, f"{name}: NULL argument {i} not rejected on the host"
+    for i in vec:   # 8 bytes off: vector loads and TMA copies would fault, so the host refuses it
+        bad = list(args)
+        bad[i] = args[i] + 8
+        assert fn(*bad) == 3, f"{name}: misaligned argument {i} not rejected on the host"
+
+
+def test_step_refuses_a_misaligned_pointer_before_any_launch():
+    lib = dfl.load()
+    if not _no_device(lib):
+        pytest.skip("a usable device is present: the stand-in addresses must not reach a launch")
+    a, layers = _host_step_args()
+    need = dfl.workspace_size(dfl.DFL_OP_DRAFT_STEP, N=2, C=64, B=16, d=256, Hq=4, Hkv=2, hd=64, D=2, L=3, V=1000,
+                              K=0, G=15, row0=1, dtype=1)
+    step = lambda: lib.dfl_draft_step(ctypes.byref(a), _FAKE, need, None)
+    assert step() == 7
+    for name in ("H", "Xb", "mix_gain", "blk_gain", "final_gain", "W_lm"):
+        setattr(a, name, _FAKE + 8)
+        assert step() == 3, name
+        setattr(a, name, _FAKE)
+    for name in ("Wq", "Wkc", "Wvc", "Wkb", "Wvb", "Wo"):
+        setattr(layers[1], name, _FAKE + 8)
+        assert step() == 3, name
+        setattr(layers[1], name, _FAKE)
+    assert lib.dfl_draft_step(ctypes.byref(a), _FAKE + 8, need, None) == 3   # workspace
+    assert step() == 7
+
+
+@pytest.mark.parametrize("field,value,status", [("L", 17, 1), ("Hq", 3, 1), ("hd", 60, 3), ("d", 260, 3),
+                                                ("h_layer_stride", 2 * 64 * 256 - 8, 1),
+                                                ("h_layer_stride", 2 * 64 * 256 + 4, 3)])
+def test_step_refuses_a_bad_shape_before_any_launch(field, value, status):
+    lib = dfl.load()
+    if not _no_device(lib):
+        pytest.skip("a usable device is present: the stand-in addresses must not reach a launch")
+    a, layers = _host_step_args()
+    need = dfl.workspace_size(dfl.DFL_OP_DRAFT_STEP, N=2, C=64, B=16, d=260, Hq=4, Hkv=2, hd=64, D=2, L=17,
+                              V=1000, K=0, G=15, row0=1, dtype=1)
+    setattr(a, field, value)
+    if field == "d":
+        a.h_layer_stride = 2 * 64 * 264   # large enough, so that only d itself is wrong
+    assert lib.dfl_draft_step(ctypes.byref(a), _FAKE, need, None) == status
