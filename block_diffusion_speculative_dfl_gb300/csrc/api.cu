@@ -317,6 +317,7 @@ extern "C" dfl_status dfl_dual_kv_proj(const void* Xc, const float* Xb, int32_t 
     if (N <= 0 || C < 0 || B <= 0 || d <= 0 || Hq <= 0 || Hkv <= 0 || hd <= 0 || Hq % Hkv != 0)
         return DFL_ERR_INVALID_ARG;
     if (dt != DFL_F32 && dt != DFL_BF16) return DFL_ERR_INVALID_ARG;
+    if (!rows_fit((int64_t)N * C) || !rows_fit((int64_t)N * B)) return DFL_ERR_UNSUPPORTED_SHAPE;
     if (!Xb || !blk_gain || !Wq || !Wkb || !Wvb || !Q || !Kb || !Vb || !ws) return DFL_ERR_INVALID_ARG;
     if (C > 0 && (!Xc || !Wkc || !Wvc || !Kc || !Vc)) return DFL_ERR_INVALID_ARG;
     if (rope && (hd & 1)) return DFL_ERR_INVALID_ARG;
@@ -380,6 +381,7 @@ extern "C" dfl_status dfl_block_attn(const void* Q, const void* Kc, const void* 
     if (N <= 0 || C < 0 || B <= 0 || d <= 0 || Hq <= 0 || Hkv <= 0 || hd <= 0 || Hq % Hkv != 0)
         return DFL_ERR_INVALID_ARG;
     if (dt != DFL_F32 && dt != DFL_BF16) return DFL_ERR_INVALID_ARG;
+    if (!rows_fit((int64_t)N * C) || !rows_fit((int64_t)N * B)) return DFL_ERR_UNSUPPORTED_SHAPE;
     if (!Q || !Kb || !Vb || !Wo || !Xb || !ws || (C > 0 && (!Kc || !Vc))) return DFL_ERR_INVALID_ARG;
     const void* ptrs[] = {Q, Kb, Vb, Wo, Xb, ws, C > 0 ? Kc : Q, C > 0 ? Vc : Q};
     for (const void* p : ptrs) if (!aligned16(p)) return DFL_ERR_MISALIGNED;
@@ -413,6 +415,7 @@ extern "C" dfl_status dfl_block_ffn(float* Xb, int32_t N, int32_t B, int32_t d, 
     if (!Xb || !ffn_gain || !W1 || !W3 || !W2 || !ws || N <= 0 || B <= 0 || d <= 0 || F <= 0)
         return DFL_ERR_INVALID_ARG;
     if (dt != DFL_F32 && dt != DFL_BF16) return DFL_ERR_INVALID_ARG;
+    if (!rows_fit((int64_t)N * B)) return DFL_ERR_UNSUPPORTED_SHAPE;
     const void* ptrs[] = {Xb, ffn_gain, W1, W3, W2, ws};
     for (const void* p : ptrs) if (!aligned16(p)) return DFL_ERR_MISALIGNED;
     if (d % 8 != 0 || F % 8 != 0) return DFL_ERR_MISALIGNED;
@@ -471,6 +474,7 @@ extern "C" dfl_status dfl_lm_head_argmax(const float* Xb, int32_t N, int32_t B, 
                                          size_t ws_bytes, dfl_stream stream) {
     if (N <= 0 || B <= 0 || row0 < 0 || row0 >= B || d <= 0 || V <= 0) return DFL_ERR_INVALID_ARG;
     if (dt != DFL_F32 && dt != DFL_BF16) return DFL_ERR_INVALID_ARG;
+    if (!rows_fit((int64_t)N * B)) return DFL_ERR_UNSUPPORTED_SHAPE;
     if (!Xb || !final_gain || !W_lm || !argmax_out || !ws) return DFL_ERR_INVALID_ARG;
     if (sp && (sp->K < 1 || sp->K > 64 || !(sp->T > 0.f) || !samples_out)) return DFL_ERR_INVALID_ARG;
     if (sp && dt == DFL_BF16 && !logits_out) return DFL_ERR_INVALID_ARG;
@@ -577,6 +581,8 @@ dfl_status step_check(const dfl_step_args* a, const dfl_ctx_cache* cache, const 
     // with the status that call returns), checked before the first launch.
     if (a->L > 16 || a->Hq <= 0 || a->Hkv <= 0 || a->hd <= 0 || a->Hq % a->Hkv != 0) return DFL_ERR_INVALID_ARG;
     const int64_t h_rows = (int64_t)a->N * (cache ? cache->R : a->C);
+    if (!rows_fit(h_rows) || !rows_fit((int64_t)a->N * a->C) || !rows_fit((int64_t)a->N * a->B))
+        return DFL_ERR_UNSUPPORTED_SHAPE;
     if (a->L > 1 && a->h_layer_stride < h_rows * a->d) return DFL_ERR_INVALID_ARG;
     if (a->d % 8 != 0 || a->hd % 8 != 0 || a->F % 8 != 0 || a->h_layer_stride % 8 != 0)
         return DFL_ERR_MISALIGNED;

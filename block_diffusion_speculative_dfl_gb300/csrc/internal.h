@@ -41,6 +41,8 @@ uint64_t wait_limit_ns();
 inline dfl_status cuda_status(cudaError_t e) { return e == cudaSuccess ? DFL_OK : DFL_ERR_CUDA; }
 inline dfl_status last_launch() { return cuda_status(cudaGetLastError()); }
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+// Row counts index TMA coordinates and GEMM extents, which are 32-bit.
+inline bool rows_fit(int64_t rows) { return rows < ((int64_t)1 << 31); }
 
 // --------------------------------------------------------------- tracing --
 

@@ -30,7 +30,11 @@
  *              bf16 tensors hold raw bf16 bits (2 bytes per element).
  *              The block residual stream Xb is always fp32.
  *   Alignment  Every tensor pointer must be 16-byte aligned and d, hd,
- *              Hq*hd a multiple of 8, else DFL_ERR_MISALIGNED.
+ *              Hq*hd a multiple of 8, else DFL_ERR_MISALIGNED (checked for
+ *              every pointer a 16-byte or TMA access reads or writes).
+ *   Sizes      Row counts (N*C context rows, N*B block rows) stay below 2^31:
+ *              TMA coordinates and GEMM extents are 32-bit, so larger ones
+ *              return DFL_ERR_UNSUPPORTED_SHAPE.
  *   Errors     Argument checks run on the host before any launch and return
  *              a non-zero dfl_status with nothing launched.  A launch failure
  *              returns DFL_ERR_CUDA.  Kernels never trap: a bounded wait that

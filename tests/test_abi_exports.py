@@ -251,3 +251,20 @@ def test_step_refuses_a_bad_shape_before_any_launch(field, value, status):
     if field == "d":
         a.h_layer_stride = 2 * 64 * 264   # large enough, so that only d itself is wrong
     assert lib.dfl_draft_step(ctypes.byref(a), _FAKE, need, None) == status
+
+
+def test_row_counts_beyond_32_bits_are_refused():
+    # TMA coordinates and GEMM extents are 32-bit: N*C or N*B of 2^31 rows and
+    # more is an unsupported shape, refused on the host.
+    lib = dfl.load()
+    if not _no_device(lib):
+        pytest.skip("a usable device is present: the stand-in addresses must not reach a launch")
+    F = _FAKE
+    big_n, big_c = 1 << 20, 1 << 11
+    assert lib.dfl_block_attn(F, F, F, F, F, big_n, big_c, 16, 4, 2, 128, 1, F, 256, F, F, 1 << 40, None) == 2
+    assert lib.dfl_dual_kv_proj(F, F, big_n, big_c, 16, 256, 1, F, 1e-6, F, F, F, F, F, 4, 2, 128, None,
+                                F, F, F, F, F, F, 1 << 40, None) == 2
+    assert lib.dfl_block_ffn(F, 1 << 27, 16, 256, 1, F, 1e-6, F, F, F, 384, F, 1 << 40, None) == 2
+    a, layers = _host_step_args()
+    a.N, a.C, a.h_layer_stride = big_n, big_c, big_n * big_c * 256
+    assert lib.dfl_draft_step(ctypes.byref(a), F, 1 << 50, None) == 2
