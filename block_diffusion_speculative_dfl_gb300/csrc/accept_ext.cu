@@ -395,6 +395,7 @@ using namespace dfl;
 extern "C" dfl_status dfl_tv_acceptance(const float* logits, float T, const void* vlog, dfl_dtype dt, int32_t N,
                                         int32_t K, int32_t G, int32_t V, float* alpha, float* tokens_per_draft,
                                         void* ws, size_t ws_bytes, dfl_stream stream) {
+    const dfl::ApiRange nvtx_range("dfl_tv_acceptance");
     if (!logits || !vlog || !alpha || !ws || N <= 0 || K < 1 || K > 64 || G < 1 || G > 1024 || V <= 0 ||
         !(T > 0.f))
         return DFL_ERR_INVALID_ARG;
@@ -425,6 +426,7 @@ extern "C" dfl_status dfl_spec_accept(const float* logits, float T, const void* 
                                       const int32_t* drafts, const int32_t* sel, int32_t N, int32_t K, int32_t G,
                                       int32_t V, uint64_t seed, int32_t* accept_len, int32_t* next_token, void* ws,
                                       size_t ws_bytes, dfl_stream stream) {
+    const dfl::ApiRange nvtx_range("dfl_spec_accept");
     if (!logits || !vlog || !drafts || !accept_len || !next_token || !ws || N <= 0 || K < 1 || K > 64 || G < 1 ||
         G > 1024 || V <= 0 || !(T > 0.f))
         return DFL_ERR_INVALID_ARG;

@@ -194,6 +194,7 @@ extern "C" dfl_status dfl_selftest_bounded_wait(uint64_t limit_ns, int32_t* stat
 }
 
 extern "C" dfl_status dfl_rope_table(float* table, int32_t P, int32_t hd, double theta, dfl_stream stream) {
+    const dfl::ApiRange nvtx_range("dfl_rope_table");
     if (!table || P <= 0 || hd <= 0 || (hd & 1) || !(theta > 0.0)) return DFL_ERR_INVALID_ARG;
     if (!current_ctx()) return DFL_ERR_NO_DEVICE;
     return rope_table(table, P, hd, theta, static_cast<cudaStream_t>(stream));
@@ -201,6 +202,7 @@ extern "C" dfl_status dfl_rope_table(float* table, int32_t P, int32_t hd, double
 
 extern "C" dfl_status dfl_greedy_accept(const int32_t* draft, const int32_t* target, int32_t N, int32_t n,
                                         int32_t* accept_len, int32_t* bonus, dfl_stream stream) {
+    const dfl::ApiRange nvtx_range("dfl_greedy_accept");
     if (!target || !accept_len || !bonus || N <= 0 || n < 0 || n > 1024 || (n > 0 && !draft))
         return DFL_ERR_INVALID_ARG;
     if (!current_ctx()) return DFL_ERR_NO_DEVICE;
@@ -314,6 +316,7 @@ extern "C" dfl_status dfl_dual_kv_proj(const void* Xc, const float* Xb, int32_t 
                                        int32_t Hq, int32_t Hkv, int32_t hd, const float* rope, void* Q, void* Kc,
                                        void* Vc, void* Kb, void* Vb, void* ws, size_t ws_bytes,
                                        dfl_stream stream) {
+    const dfl::ApiRange nvtx_range("dfl_dual_kv_proj");
     if (N <= 0 || C < 0 || B <= 0 || d <= 0 || Hq <= 0 || Hkv <= 0 || hd <= 0 || Hq % Hkv != 0)
         return DFL_ERR_INVALID_ARG;
     if (dt != DFL_F32 && dt != DFL_BF16) return DFL_ERR_INVALID_ARG;
@@ -378,6 +381,7 @@ extern "C" dfl_status dfl_block_attn(const void* Q, const void* Kc, const void* 
                                      int32_t N, int32_t C, int32_t B, int32_t Hq, int32_t Hkv, int32_t hd,
                                      dfl_dtype dt, const void* Wo, int32_t d, float* Xb, void* ws, size_t ws_bytes,
                                      dfl_stream stream) {
+    const dfl::ApiRange nvtx_range("dfl_block_attn");
     if (N <= 0 || C < 0 || B <= 0 || d <= 0 || Hq <= 0 || Hkv <= 0 || hd <= 0 || Hq % Hkv != 0)
         return DFL_ERR_INVALID_ARG;
     if (dt != DFL_F32 && dt != DFL_BF16) return DFL_ERR_INVALID_ARG;
@@ -412,6 +416,7 @@ extern "C" dfl_status dfl_block_attn(const void* Q, const void* Kc, const void* 
 extern "C" dfl_status dfl_block_ffn(float* Xb, int32_t N, int32_t B, int32_t d, dfl_dtype dt, const float* ffn_gain,
                                     float eps, const void* W1, const void* W3, const void* W2, int32_t F, void* ws,
                                     size_t ws_bytes, dfl_stream stream) {
+    const dfl::ApiRange nvtx_range("dfl_block_ffn");
     if (!Xb || !ffn_gain || !W1 || !W3 || !W2 || !ws || N <= 0 || B <= 0 || d <= 0 || F <= 0)
         return DFL_ERR_INVALID_ARG;
     if (dt != DFL_F32 && dt != DFL_BF16) return DFL_ERR_INVALID_ARG;
@@ -472,6 +477,7 @@ extern "C" dfl_status dfl_lm_head_argmax(const float* Xb, int32_t N, int32_t B, 
                                          int32_t V, int32_t* argmax_out, float* logits_out,
                                          const dfl_sample_params* sp, int32_t* samples_out, void* ws,
                                          size_t ws_bytes, dfl_stream stream) {
+    const dfl::ApiRange nvtx_range("dfl_lm_head_argmax");
     if (N <= 0 || B <= 0 || row0 < 0 || row0 >= B || d <= 0 || V <= 0) return DFL_ERR_INVALID_ARG;
     if (dt != DFL_F32 && dt != DFL_BF16) return DFL_ERR_INVALID_ARG;
     if (!rows_fit((int64_t)N * B)) return DFL_ERR_UNSUPPORTED_SHAPE;
@@ -529,6 +535,7 @@ extern "C" dfl_status dfl_lm_head_argmax(const float* Xb, int32_t N, int32_t B, 
 extern "C" dfl_status dfl_self_select(const void* vlog, dfl_dtype dt, const int32_t* drafts, int32_t N, int32_t K,
                                       int32_t G, int32_t V, float* scores, int32_t* selected, int32_t* accept_len,
                                       int32_t* bonus, void* ws, size_t ws_bytes, dfl_stream stream) {
+    const dfl::ApiRange nvtx_range("dfl_self_select");
     if (N <= 0 || K < 1 || K > 64 || G < 1 || G > 1024 || V <= 0) return DFL_ERR_INVALID_ARG;
     if (dt != DFL_F32 && dt != DFL_BF16) return DFL_ERR_INVALID_ARG;
     if (!vlog || !drafts || !scores || !selected || !accept_len || !bonus || !ws) return DFL_ERR_INVALID_ARG;
@@ -896,16 +903,19 @@ dfl_status draft_step_host_impl(const dfl_step_args* a, void* H_dev, int chunks,
 }  // namespace dfl
 
 extern "C" dfl_status dfl_draft_step(const dfl_step_args* a, void* ws, size_t ws_bytes, dfl_stream stream) {
+    const dfl::ApiRange nvtx_range("dfl_draft_step");
     return draft_step_impl(a, nullptr, ws, ws_bytes, stream);
 }
 
 extern "C" dfl_status dfl_draft_step_host(const dfl_step_args* a, void* H_dev, int32_t chunks, void* ws,
                                           size_t ws_bytes, dfl_stream stream) {
+    const dfl::ApiRange nvtx_range("dfl_draft_step_host");
     return draft_step_host_impl(a, H_dev, chunks, ws, ws_bytes, stream);
 }
 
 extern "C" dfl_status dfl_draft_step_cached(const dfl_step_args* a, const dfl_ctx_cache* cache, void* ws,
                                             size_t ws_bytes, dfl_stream stream) {
+    const dfl::ApiRange nvtx_range("dfl_draft_step_cached");
     if (!cache) return DFL_ERR_INVALID_ARG;
     return draft_step_impl(a, cache, ws, ws_bytes, stream);
 }

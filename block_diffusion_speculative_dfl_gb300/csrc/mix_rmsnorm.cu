@@ -415,6 +415,7 @@ extern "C" dfl_status dfl_layer_mix_rmsnorm(const void* H, int64_t layer_stride,
                                             int32_t d, dfl_dtype dt, int32_t D, const float* mix_logits,
                                             const float* gain, float eps, void* Xc, int64_t xc_layer_stride,
                                             dfl_stream stream) {
+    const dfl::ApiRange nvtx_range("dfl_layer_mix_rmsnorm");
     if (!H || !mix_logits || !gain || !Xc) return DFL_ERR_INVALID_ARG;
     if (L < 1 || L > 16 || D < 1 || D > 8 || rows <= 0 || d <= 0) return DFL_ERR_INVALID_ARG;
     if (layer_stride < rows * d && L > 1) return DFL_ERR_INVALID_ARG;

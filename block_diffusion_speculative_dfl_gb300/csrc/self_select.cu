@@ -299,6 +299,7 @@ dfl_status noalloc_scratch(void** out) {
 extern "C" dfl_status dfl_self_select_noalloc(const void* vlog, dfl_dtype dt, const int32_t* drafts, int32_t N,
                                               int32_t K, int32_t G, int32_t V, float* scores, int32_t* selected,
                                               int32_t* accept_len, int32_t* bonus, dfl_stream stream) {
+    const dfl::ApiRange nvtx_range("dfl_self_select_noalloc");
     using namespace dfl;
     if (N <= 0 || K < 1 || K > 64 || G < 1 || G > 1024 || V <= 0) return DFL_ERR_INVALID_ARG;
     if (dt != DFL_F32 && dt != DFL_BF16) return DFL_ERR_INVALID_ARG;
