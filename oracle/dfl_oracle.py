@@ -82,6 +82,30 @@ def mix_rmsnorm(H, mix_logits, gain, eps: float) -> np.ndarray:
     return rmsnorm(x, gain, eps)
 
 
+def fc_fuse(H, W_fc, gain, eps: float) -> np.ndarray:
+    """DFlash's shared context representation: one FC over L target layers.
+
+    DFlash article, "Writing a whole block in one forward pass": hidden
+    features taken from several target layers are fused by a light
+    projection and injected into the K/V of every draft layer; the DFlare
+    post ("Per-draft-layer mixing") describes the same baseline as a fully
+    connected layer that fuses the target features into one common
+    representation, which DFlare replaces by per-layer softmax mixes.
+
+    Reading: the L hidden states of a position are concatenated layer by
+    layer into one vector of L*d values, W_fc [d][L*d] (no bias) maps it to d
+    features, and an RMSNorm with gain ``gain`` follows (the normalisation
+    DFlare keeps after its own mixture).  H is [L][rows][d]; the result is
+    [rows][d], shared by every draft layer.
+    """
+    H = np.asarray(H, dtype=F64)
+    L, rows, d = H.shape
+    cat = np.empty((rows, L * d), dtype=F64)
+    for i in range(L):
+        cat[:, i * d:(i + 1) * d] = H[i]
+    return rmsnorm(cat @ np.asarray(W_fc, dtype=F64).T, gain, eps)
+
+
 # ---------------------------------------------------------------------------
 # Rotary positions (reading: the pages give no position scheme)
 # ---------------------------------------------------------------------------
@@ -159,7 +183,7 @@ def attention(Q, K, V, visible) -> np.ndarray:
 # ---------------------------------------------------------------------------
 
 def draft_layer(Xb, Hn, mix_logits, g_mix, g_blk, W: dict, shape: dict,
-                eps: float, theta: float) -> dict:
+                eps: float, theta: float, Xc=None) -> dict:
     """One block-diffusion draft layer for one sequence.
 
     Xb [B][d] is the block's residual stream (row 0 the anchor token, rows
@@ -179,13 +203,18 @@ def draft_layer(Xb, Hn, mix_logits, g_mix, g_blk, W: dict, shape: dict,
     before its projections (pre-norm, gain g_blk); the layer ends with an
     output projection Wo added to the residual stream; there is no FFN;
     rotary positions 0..C-1 for context and C..C+B-1 for the block.
+    ``Xc`` [C][d], when given, replaces the layer's own mixture as the
+    context features (the DFlash form, where one fused representation of the
+    target features serves every draft layer; see ``fc_fuse``).
     Returns every intermediate for per-tensor comparison.
     """
     B, d = Xb.shape
-    C = Hn.shape[1]
     Hq, Hkv, hd = shape["Hq"], shape["Hkv"], shape["hd"]
     Xb = np.asarray(Xb, dtype=F64)
-    Xc = mix_rmsnorm(Hn, mix_logits, g_mix, eps)
+    if Xc is None:
+        Xc = mix_rmsnorm(Hn, mix_logits, g_mix, eps)
+    Xc = np.asarray(Xc, dtype=F64)
+    C = Xc.shape[0]
     Xn = rmsnorm(Xb, g_blk, eps)
     f = {k: np.asarray(v, dtype=F64) for k, v in W.items()}
     Q = (Xn @ f["Wq"].T).reshape(B, Hq, hd)
@@ -251,16 +280,21 @@ def argmax_lowest(z) -> np.ndarray:
 
 
 def draft_forward(Xb0, Hn, mix, g_mix, g_blk, layers, shape: dict,
-                  eps: float, theta: float, keep_layers: bool = False) -> dict:
+                  eps: float, theta: float, keep_layers: bool = False, fused=None) -> dict:
     """All D draft layers of one sequence (one single-pass block forward).
 
     DFlare post, "Generating candidates in parallel": one forward predicts
-    every mask position.  ``layers`` is a list of D weight dicts.
+    every mask position.  ``layers`` is a list of D weight dicts.  With
+    ``fused`` = (W_fc, g_fc) the context features of every layer are the one
+    DFlash fusion ``fc_fuse(Hn, W_fc, g_fc)`` instead of per-layer mixtures
+    (``mix`` and ``g_mix`` are then unused).
     """
     Xb = np.asarray(Xb0, dtype=F64)
+    Xc = None if fused is None else fc_fuse(Hn, fused[0], fused[1], eps)
     per_layer = []
     for l, W in enumerate(layers):
-        out = draft_layer(Xb, Hn, mix[l], g_mix[l], g_blk[l], W, shape, eps, theta)
+        out = draft_layer(Xb, Hn, None if fused else mix[l], None if fused else g_mix[l], g_blk[l], W, shape,
+                          eps, theta, Xc=Xc)
         Xb = out["Xb"]
         per_layer.append(out if keep_layers else {"Xb": Xb})
     return {"Xb": Xb, "layers": per_layer}
@@ -553,3 +587,136 @@ def speculative_accept(z_rows, T: float, v_rows, x, u_acc, u_res):
         return j, y, min(near, m)
     y, m = inverse_cdf(softmax_t(v_rows[G]), u_res[G])
     return G, y, min(near, m)
+
+
+# ---------------------------------------------------------------------------
+# Sets of legitimate results where floating point may decide a draw or a test
+# (used by the parity tests; the decisions themselves are the functions above)
+# ---------------------------------------------------------------------------
+
+def _nearest_nonempty(w, i: int, step: int):
+    """First index from i in direction ``step`` whose weight is positive."""
+    while 0 <= i < len(w):
+        if w[i] > 0.0:
+            return i
+        i += step
+    return None
+
+
+def inverse_cdf_outcomes(w, u: float, band: float) -> set:
+    """Every index an inverse-CDF draw of weights w at u may legitimately give.
+
+    The draw is the smallest index whose cumulative weight exceeds u * total
+    (``inverse_cdf``).  An implementation whose cumulative sums differ from
+    the exact ones by less than ``band`` * total can only move a target that
+    lies within that distance of a boundary into the interval on the other
+    side of it: the set holds the exact index and, for each boundary closer
+    than ``band`` * total, the nearest index with positive weight on the far
+    side of that boundary.
+    """
+    w = np.asarray(w, dtype=F64)
+    cdf = np.cumsum(w)
+    total = cdf[-1]
+    t = u * total
+    v = min(int(np.searchsorted(cdf, t, side="right")), len(w) - 1)
+    out = {v}
+    lo = cdf[v - 1] if v > 0 else 0.0
+    if v > 0 and t - lo < band * total:
+        j = _nearest_nonempty(w, v - 1, -1)
+        if j is not None:
+            out.add(j)
+    if cdf[v] - t < band * total:
+        j = _nearest_nonempty(w, v + 1, +1)
+        if j is not None:
+            out.add(j)
+    return out
+
+
+def sample_inverse_cdf_outcomes(z, T: float, u: float, band: float) -> set:
+    """``inverse_cdf_outcomes`` of the weights exp((z - max z) / T) that
+    ``sample_inverse_cdf`` draws from."""
+    z = np.asarray(z, dtype=F64)
+    return inverse_cdf_outcomes(np.exp((z - z.max()) / T), u, band)
+
+
+def speculative_accept_outcomes(z_rows, T: float, v_rows, x, u_acc, u_res,
+                                band_test: float, band_draw: float) -> set:
+    """Every (accepted, token) that ``speculative_accept`` may legitimately give.
+
+    Follows the same rule position by position.  A test u * Q(x_j) < P(x_j)
+    whose two sides differ by less than ``band_test`` * P(x_j) may go either
+    way, so both branches are followed; each final draw contributes its
+    ``inverse_cdf_outcomes`` with ``band_draw``.
+    """
+    G = len(x)
+    out = set()
+
+    def walk(j):
+        if j == G:
+            for y in inverse_cdf_outcomes(softmax_t(v_rows[G]), u_res[G], band_draw):
+                out.add((G, y))
+            return
+        Q = softmax_t(z_rows[j], T)
+        P = softmax_t(v_rows[j])
+        q, p = Q[x[j]], P[x[j]]
+        accept = u_acc[j] * q < p
+        ambiguous = abs(u_acc[j] * q - p) < band_test * max(p, 1e-300)
+        if accept or ambiguous:
+            walk(j + 1)
+        if not accept or ambiguous:
+            r = np.maximum(P - Q, 0.0)
+            if r.sum() > 0.0:
+                for y in inverse_cdf_outcomes(r, u_res[j], band_draw):
+                    out.add((j, y))
+
+    walk(0)
+    return out
+
+
+# ---------------------------------------------------------------------------
+# Sampled-greedy acceptance (SpecDiff-2 notes, "Streak-Distillation",
+# "Self-Selection Acceptance")
+# ---------------------------------------------------------------------------
+
+def sampled_greedy_accept(v_rows, x, u):
+    """Greedy acceptance against verifier samples instead of its argmax.
+
+    Reading of the SpecDiff-2 notes' greedy-acceptance rule at temperature
+    above zero: at window position j the verifier draws its own token y_j
+    from P_j = softmax(v_j) (inverse CDF at u[j]), and the draft token x_j is
+    accepted while it equals y_j.  At the first mismatch the verifier's own
+    sample y_j is the committed token; when all G drafts are accepted the
+    bonus is the sample y_G of row G.  Draft probabilities play no part (the
+    section's point that the rule needs no drafter calibration), every
+    committed token is a verifier sample (lossless), and the expected number
+    accepted is sum_m prod_{j<=m} P_j(x_j), the streak equation of
+    "Streak-Distillation".  v_rows [G+1][V], x [G], u [G+1].
+    Returns (accepted, token, margin), margin being the smallest relative
+    distance of any draw made to a CDF boundary.
+    """
+    G = len(x)
+    near = np.inf
+    for j in range(G + 1):
+        y, m = inverse_cdf(softmax_t(v_rows[j]), u[j])
+        near = min(near, m)
+        if j == G or y != int(x[j]):
+            return j, y, near
+    raise AssertionError("unreachable")
+
+
+def sampled_greedy_outcomes(v_rows, x, u, band: float) -> set:
+    """Every (accepted, token) that ``sampled_greedy_accept`` may legitimately
+    give when each draw may move across a boundary closer than ``band``."""
+    G = len(x)
+    out = set()
+
+    def walk(j):
+        ys = inverse_cdf_outcomes(softmax_t(v_rows[j]), u[j], band)
+        for y in ys:
+            if j < G and y == int(x[j]):
+                walk(j + 1)
+            else:
+                out.add((j, y))
+
+    walk(0)
+    return out

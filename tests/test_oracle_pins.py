@@ -752,3 +752,218 @@ def test_cached_step_block_positions_follow_the_context_length():
     assert not np.allclose(k_at_0, k_at_5)
     # rotation keeps each rotated pair's norm
     assert np.allclose(np.linalg.norm(k_at_0), np.linalg.norm(k_at_5), atol=1e-12)
+
+
+# --------------------------------------------- DFlash single-FC fusion --
+
+def _fuse_inputs(seed=81, L=3, rows=5, d=6):
+    rng = np.random.default_rng(seed)
+    H = rng.normal(size=(L, rows, d)) * rng.uniform(0.5, 2.0, size=(L, 1, 1))
+    g = rng.uniform(0.5, 1.5, size=d)
+    return rng, H, g
+
+
+def test_fc_fuse_with_scaled_identity_blocks_is_the_softmax_mix():
+    # W_fc = [a_1 I | ... | a_L I] is the FC form of a mixture with ratios a:
+    # it must give the (separately pinned) mix + RMSNorm of the same ratios.
+    rng, H, g = _fuse_inputs()
+    L, _, d = H.shape
+    logits = rng.normal(size=L)
+    a = orc.mix_weights(logits)
+    W = np.concatenate([a[i] * np.eye(d) for i in range(L)], axis=1)
+    assert np.allclose(orc.fc_fuse(H, W, g, 1e-6), orc.mix_rmsnorm(H, logits, g, 1e-6), atol=1e-13)
+
+
+@pytest.mark.parametrize("i", [0, 2])
+def test_fc_fuse_selecting_one_layer_is_its_rmsnorm(i):
+    _, H, g = _fuse_inputs()
+    L, _, d = H.shape
+    W = np.zeros((d, L * d))
+    W[:, i * d:(i + 1) * d] = np.eye(d)
+    x = H[i]
+    ref = x / np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + 1e-6) * g
+    assert np.allclose(orc.fc_fuse(H, W, g, 1e-6), ref, atol=1e-13)
+
+
+def test_fc_fuse_output_features_and_layer_order():
+    # Output feature o reads row o of W_fc; swapping two target layers
+    # together with their column blocks of W_fc changes nothing, swapping
+    # only the layers does; the norm makes a common scale of H irrelevant.
+    rng, H, g = _fuse_inputs(seed=82)
+    L, _, d = H.shape
+    W = rng.normal(size=(d, L * d)) / np.sqrt(L * d)
+    base = orc.fc_fuse(H, W, np.ones(d), 1e-12)
+    perm = [2, 0, 1]
+    Wp = np.concatenate([W[:, p * d:(p + 1) * d] for p in perm], axis=1)
+    assert np.allclose(orc.fc_fuse(H[perm], Wp, np.ones(d), 1e-12), base, atol=1e-12)
+    assert not np.allclose(orc.fc_fuse(H[perm], W, np.ones(d), 1e-12), base, atol=1e-3)
+    assert np.allclose(orc.fc_fuse(7.0 * H, W, np.ones(d), 1e-12), base, atol=1e-12)
+    # one output feature from a hand-computed dot product of the concatenation
+    cat = np.concatenate([H[i] for i in range(L)], axis=1)
+    pre = cat @ W.T
+    r0 = pre[0] / np.sqrt(np.mean(pre[0] ** 2) + 1e-6)
+    assert np.allclose(orc.fc_fuse(H, W, np.ones(d), 1e-6)[0], r0, atol=1e-13)
+
+
+def test_fused_forward_shares_one_representation_across_layers():
+    # With the scaled-identity FC, a one-layer fused forward equals the mixed
+    # forward of the same ratios; with two layers every layer reads the same
+    # context features (the mix logits, unused, may be anything).
+    t = _two_layer_drafter()
+    L, _, d = t["Hn"].shape
+    a = orc.mix_weights(t["mix"][0])
+    W = np.concatenate([a[i] * np.eye(d) for i in range(L)], axis=1)
+    one = orc.draft_forward(t["Xb"], t["Hn"], t["mix"][:1], t["g_mix"][:1], t["g_blk"][:1], t["layers"][:1],
+                            t["shape"], 1e-6, 100.0)
+    fused1 = orc.draft_forward(t["Xb"], t["Hn"], None, None, t["g_blk"][:1], t["layers"][:1], t["shape"], 1e-6,
+                               100.0, fused=(W, t["g_mix"][0]))
+    assert np.allclose(one["Xb"], fused1["Xb"], atol=1e-12)
+    fused2 = orc.draft_forward(t["Xb"], t["Hn"], None, None, t["g_blk"], t["layers"], t["shape"], 1e-6, 100.0,
+                               keep_layers=True, fused=(W, t["g_mix"][0]))
+    mixed = orc.draft_forward(t["Xb"], t["Hn"], [t["mix"][0]] * 2, [t["g_mix"][0]] * 2, t["g_blk"], t["layers"],
+                              t["shape"], 1e-6, 100.0)
+    assert np.allclose(fused2["layers"][0]["Xc"], fused2["layers"][1]["Xc"])
+    assert np.allclose(fused2["Xb"], mixed["Xb"], atol=1e-12)
+
+
+# ------------------------------- legitimate outcomes near a boundary --
+
+def test_inverse_cdf_outcomes_worked_cases():
+    w = np.array([1.0, 0.0, 3.0])                 # cumulative (1, 1, 4)
+    assert orc.inverse_cdf_outcomes(w, 0.1, 1e-6) == {0}
+    # exactly on the boundary 1: the empty interval of index 1 is skipped
+    assert orc.inverse_cdf_outcomes(w, 0.25, 1e-6) == {0, 2}
+    # 2.4 is 1.4 above 1 and 1.6 below 4 (0.35 and 0.4 of the total)
+    assert orc.inverse_cdf_outcomes(w, 0.6, 0.3) == {2}
+    assert orc.inverse_cdf_outcomes(w, 0.6, 0.36) == {0, 2}
+    w = np.array([1.0, 1.0, 2.0])                 # cumulative (1, 2, 4)
+    assert orc.inverse_cdf_outcomes(w, 0.4975, 0.01) == {1, 2}    # 1.99: 0.01 below 2
+    assert orc.inverse_cdf_outcomes(w, 0.4975, 0.002) == {1}
+    assert orc.inverse_cdf_outcomes(w, 0.2525, 0.01) == {0, 1}    # 1.01: 0.01 above 1
+    # the top boundary has no interval above it
+    assert orc.inverse_cdf_outcomes(w, 0.999999, 0.01) == {2}
+
+
+def test_inverse_cdf_outcomes_hold_every_perturbed_draw():
+    # Cumulative sums off by less than the band (relative to the total) can
+    # only give draws inside the set, and the set's extra members are reached
+    # by some such perturbation.
+    rng = np.random.default_rng(83)
+    band = 1e-3
+    hits = 0
+    for _ in range(400):
+        V = int(rng.integers(2, 9))
+        w = rng.uniform(0, 1, V) * (rng.uniform(0, 1, V) > 0.2)
+        if w.sum() == 0:
+            continue
+        # targets often near a boundary
+        cdf = np.cumsum(w) / w.sum()
+        b = cdf[int(rng.integers(0, V))]
+        u = float(np.clip(b + rng.uniform(-2 * band, 2 * band), 1e-9, 1 - 1e-9))
+        legit = orc.inverse_cdf_outcomes(w, u, band)
+        seen = set()
+        for _ in range(60):
+            noise = rng.uniform(-0.45 * band, 0.45 * band, V) * w.sum() / V
+            wp = np.maximum(w + noise * (w > 0), 0.0)
+            seen.add(orc.inverse_cdf(wp, u)[0])
+        assert seen <= legit, (w, u, seen, legit)
+        hits += len(legit) > 1
+    assert hits > 50
+
+
+def test_sample_outcomes_use_the_temperature():
+    T = 2.0
+    z = T * np.log([1.0, 1.0, 2.0])
+    assert orc.sample_inverse_cdf_outcomes(z, T, 0.4975, 0.01) == {1, 2}
+    assert orc.sample_inverse_cdf_outcomes(z, 1.0, 0.4975, 0.01) == {2}   # weights (1, 1, 4): 2.985 of 6
+
+
+def test_speculative_outcomes_follow_both_branches_of_a_tied_test():
+    # Q = (1/2, 1/2), P_1 = (0.2, 0.8), P_2 = (0.25, 0.75); draft token 0
+    z, v1, v2 = np.zeros(2), np.log([0.2, 0.8]), np.log([0.25, 0.75])
+    out = lambda ua, ur: orc.speculative_accept_outcomes([z], 1.0, [v1, v2], [0], [ua], ur, 1e-6, 1e-6)
+    assert out(0.6, [0.2, 0.5]) == {(0, 1)}                  # clear rejection
+    assert out(0.3, [0.5, 0.4]) == {(1, 1)}                  # clear acceptance, bonus 1
+    assert out(0.3, [0.5, 0.1]) == {(1, 0)}                  # bonus 0 (0.1 < 0.25)
+    # u q = 0.2 = p exactly: accepted or rejected are both legitimate
+    assert out(0.4, [0.2, 0.1]) == {(0, 1), (1, 0)}
+    # a bonus draw on its boundary (0.25) may give either token
+    assert out(0.3, [0.5, 0.25]) == {(1, 0), (1, 1)}
+
+
+def test_speculative_outcomes_hold_the_exact_result_and_perturbations():
+    rng = np.random.default_rng(84)
+    for _ in range(200):
+        G, V, T = int(rng.integers(1, 4)), int(rng.integers(2, 6)), 1.3
+        z = rng.normal(size=(G, V))
+        v = np.vstack([z / T, rng.normal(size=(1, V))]) + rng.normal(size=(G + 1, V)) * 0.3
+        x = rng.integers(0, V, G)
+        ua, ur = rng.uniform(size=G), rng.uniform(size=G + 1)
+        legit = orc.speculative_accept_outcomes(z, T, v, x, ua, ur, 1e-4, 1e-4)
+        a, y, m = orc.speculative_accept(z, T, v, x, ua, ur)
+        assert (a, y) in legit
+        if m >= 1e-4:
+            assert legit == {(a, y)}
+        vp = v + rng.uniform(-1e-8, 1e-8, v.shape)
+        assert orc.speculative_accept(z, T, vp, x, ua, ur)[:2] in legit
+
+
+# ------------------------------------------ sampled-greedy acceptance --
+
+def _midpoint_u(P_row, y):
+    c = np.cumsum(P_row)
+    lo = c[y - 1] if y > 0 else 0.0
+    return (lo + c[y]) / 2 / c[-1]
+
+
+@pytest.mark.parametrize("V,G", [(2, 1), (3, 2), (3, 3), (4, 2)])
+def test_sampled_greedy_expected_acceptance_is_the_streak_score(V, G):
+    # Enumerate every verifier sample y in V^(G+1) (each u_j at the middle of
+    # y_j's CDF interval, weight prod P_j(y_j)).  The expected number
+    # accepted is the streak equation of p_j = P_j(x_j), and the first
+    # committed token is distributed as P_1 (the rule is lossless).
+    rng = np.random.default_rng(V * 100 + G)
+    v = rng.normal(size=(G + 1, V)) * 1.5
+    P = np.exp(v) / np.exp(v).sum(axis=-1, keepdims=True)
+    x = rng.integers(0, V, G)
+    expect, first = 0.0, np.zeros(V)
+    for y in itertools.product(range(V), repeat=G + 1):
+        prob = np.prod([P[j, y[j]] for j in range(G + 1)])
+        u = [_midpoint_u(P[j], y[j]) for j in range(G + 1)]
+        a, tok, _ = orc.sampled_greedy_accept(v, x, u)
+        expect += prob * a
+        first[x[0] if a > 0 else tok] += prob
+    assert abs(expect - orc.streak_score([P[j, x[j]] for j in range(G)])) < 1e-12
+    assert np.allclose(first, P[0], atol=1e-12)
+
+
+def test_sampled_greedy_with_certain_verifier_is_the_greedy_rule():
+    # A verifier sure of its token (one-hot rows) samples its argmax, so the
+    # rule reduces to the DFlare post's greedy rule against the argmax.
+    rng = np.random.default_rng(85)
+    for _ in range(50):
+        G, V = 5, 7
+        t = rng.integers(0, V, G + 1)
+        v = np.full((G + 1, V), -1e4)
+        v[np.arange(G + 1), t] = 0.0
+        x = t[:G].copy()
+        cut = int(rng.integers(0, G + 1))
+        if cut < G:
+            x[cut] = (x[cut] + 1) % V
+        u = rng.uniform(size=G + 1)
+        a, tok, _ = orc.sampled_greedy_accept(v, x, u)
+        assert (a, tok) == orc.greedy_accept(x, t)
+
+
+def test_sampled_greedy_worked_case_and_outcomes():
+    # P_1 = P_2 = (0.5, 0.25, 0.25): CDF (0.5, 0.75, 1)
+    v = np.log(np.array([[0.5, 0.25, 0.25]] * 3))
+    x = [0, 2]
+    assert orc.sampled_greedy_accept(v, x, [0.2, 0.9, 0.3])[:2] == (2, 0)    # y = (0, 2), bonus 0
+    assert orc.sampled_greedy_accept(v, x, [0.2, 0.6, 0.3])[:2] == (1, 1)    # y_2 = 1 != 2
+    assert orc.sampled_greedy_accept(v, x, [0.7, 0.9, 0.3])[:2] == (0, 1)    # y_1 = 1 != 0
+    a, tok, m = orc.sampled_greedy_accept(v, x, [0.2, 0.6, 0.3])
+    assert abs(m - 0.1) < 1e-12                      # 0.6 is 0.1 above the boundary 0.5 (0.2 is 0.2 from 0)
+    assert orc.sampled_greedy_outcomes(v, x, [0.2, 0.6, 0.3], 1e-6) == {(1, 1)}
+    # y_1 on the boundary 0.5: token 0 (accept, then y_2 = 2, bonus 0) or token 1 (reject)
+    assert orc.sampled_greedy_outcomes(v, x, [0.5, 0.9, 0.3], 1e-6) == {(2, 0), (0, 1)}
