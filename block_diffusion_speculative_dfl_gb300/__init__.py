@@ -14,7 +14,8 @@ from ._lib import (DflError, load, version, status_string, workspace_size, ptr, 
                    dfl_profile_enable, dfl_profile_report, dfl_self_select_noalloc,
                    dfl_tv_acceptance, dfl_spec_accept, DFL_OP_TV_ACCEPTANCE, DFL_OP_SPEC_ACCEPT,
                    dfl_block_ffn, DFL_OP_BLOCK_FFN, dfl_draft_step_cached, DFL_OP_DRAFT_STEP_CACHED,
-                   dfl_draft_step_host, DFL_OP_DRAFT_STEP_HOST, CtxCache)
+                   dfl_draft_step_host, DFL_OP_DRAFT_STEP_HOST, CtxCache, dfl_fc_fuse, DFL_OP_FC_FUSE,
+                   dfl_sampled_greedy_accept, DFL_OP_SAMPLED_GREEDY, dfl_philox4x32_10)
 from .step import DraftShape, DraftModel, CachedDraftModel
 
 __all__ = [n for n in dir() if not n.startswith("_")]

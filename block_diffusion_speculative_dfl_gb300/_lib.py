@@ -16,7 +16,7 @@ DFL_ERR_WORKSPACE, DFL_ERR_CUDA, DFL_ERR_TIMEOUT, DFL_ERR_NO_DEVICE = 4, 5, 6, 7
 DFL_F32, DFL_BF16 = 0, 1
 DFL_OP_DUAL_KV_PROJ, DFL_OP_BLOCK_ATTN, DFL_OP_LM_HEAD, DFL_OP_SELF_SELECT, DFL_OP_DRAFT_STEP = 1, 2, 3, 4, 5
 DFL_OP_TV_ACCEPTANCE, DFL_OP_SPEC_ACCEPT, DFL_OP_BLOCK_FFN, DFL_OP_DRAFT_STEP_CACHED = 6, 7, 8, 9
-DFL_OP_DRAFT_STEP_HOST = 10
+DFL_OP_DRAFT_STEP_HOST, DFL_OP_FC_FUSE, DFL_OP_SAMPLED_GREEDY = 10, 11, 12
 
 # Every function the header declares; tests check each is exported.
 EXPORTED = ("dfl_version", "dfl_status_string", "dfl_workspace_size", "dfl_rope_table",
@@ -24,7 +24,8 @@ EXPORTED = ("dfl_version", "dfl_status_string", "dfl_workspace_size", "dfl_rope_
             "dfl_greedy_accept", "dfl_self_select", "dfl_draft_step", "dfl_get_device_error",
             "dfl_set_wait_limit_ns", "dfl_selftest_bounded_wait", "dfl_profile_enable", "dfl_profile_report",
             "dfl_self_select_noalloc", "dfl_tv_acceptance", "dfl_spec_accept", "dfl_block_ffn",
-            "dfl_draft_step_cached", "dfl_draft_step_host")
+            "dfl_draft_step_cached", "dfl_draft_step_host", "dfl_fc_fuse", "dfl_sampled_greedy_accept",
+            "dfl_philox4x32_10")
 
 
 class DflError(RuntimeError):
@@ -39,7 +40,7 @@ class SampleParams(C.Structure):
 
 class Shape(C.Structure):
     _fields_ = [(n, C.c_int32) for n in ("N", "C", "B", "d", "Hq", "Hkv", "hd", "D", "L", "V", "K", "G", "row0",
-                                         "dtype", "F", "R")]
+                                         "dtype", "F", "R", "fc")]
 
 
 class LayerWeights(C.Structure):
@@ -55,7 +56,8 @@ class StepArgs(C.Structure):
                                            "bonus")] +
                 [("sample", C.POINTER(SampleParams))] +
                 [(n, C.c_void_p) for n in ("samples", "vlog", "scores", "selected", "tv_alpha", "tv_tokens")] +
-                [("accept_rule", C.c_int32), ("accept_seed", C.c_uint64), ("F", C.c_int32), ("ffn_gain", C.c_void_p)])
+                [("accept_rule", C.c_int32), ("accept_seed", C.c_uint64), ("F", C.c_int32), ("ffn_gain", C.c_void_p)] +
+                [("W_fc", C.c_void_p), ("fc_gain", C.c_void_p)])
 
 
 class CtxCache(C.Structure):
@@ -90,6 +92,10 @@ _SIGS = {
     "dfl_tv_acceptance": ([_P, _F, _P, _I32, _I32, _I32, _I32, _I32, _P, _P, _P, _SZ, _P], _I32),
     "dfl_spec_accept": ([_P, _F, _P, _I32, _P, _P, _I32, _I32, _I32, _I32, C.c_uint64, _P, _P, _P, _SZ, _P], _I32),
     "dfl_block_ffn": ([_P, _I32, _I32, _I32, _I32, _P, _F, _P, _P, _P, _I32, _P, _SZ, _P], _I32),
+    "dfl_fc_fuse": ([_P, _I64, _I32, _I64, _I32, _I32, _P, _P, _F, _P, _P, _SZ, _P], _I32),
+    "dfl_sampled_greedy_accept": ([_P, _I32, _P, _P, _I32, _I32, _I32, _I32, C.c_uint64, _P, _P, _P, _SZ, _P],
+                                  _I32),
+    "dfl_philox4x32_10": ([_P, _I32, _P, _P], _I32),
 }
 
 _lib = None
@@ -261,3 +267,20 @@ def dfl_block_ffn(Xb, N, B, d, dt, ffn_gain, eps, W1, W3, W2, F, ws, ws_bytes, s
     _check("dfl_block_ffn",
            load().dfl_block_ffn(ptr(Xb), N, B, d, dt, ptr(ffn_gain), eps, ptr(W1), ptr(W3), ptr(W2), F, ptr(ws),
                                 ws_bytes, _stream(stream)))
+
+
+def dfl_fc_fuse(H, layer_stride, L, rows, d, dt, W_fc, gain, eps, Xc, ws, ws_bytes, stream=None):
+    _check("dfl_fc_fuse",
+           load().dfl_fc_fuse(ptr(H), layer_stride, L, rows, d, dt, ptr(W_fc), ptr(gain), eps, ptr(Xc), ptr(ws),
+                              ws_bytes, _stream(stream)))
+
+
+def dfl_sampled_greedy_accept(vlog, dt, drafts, sel, N, K, G, V, seed, accept_len, next_token, ws, ws_bytes,
+                              stream=None):
+    _check("dfl_sampled_greedy_accept",
+           load().dfl_sampled_greedy_accept(ptr(vlog), dt, ptr(drafts), ptr(sel), N, K, G, V, seed, ptr(accept_len),
+                                            ptr(next_token), ptr(ws), ws_bytes, _stream(stream)))
+
+
+def dfl_philox4x32_10(inp, n, out, stream=None):
+    _check("dfl_philox4x32_10", load().dfl_philox4x32_10(ptr(inp), n, ptr(out), _stream(stream)))

@@ -15,6 +15,7 @@
 #include <mutex>
 
 #include "internal.h"
+#include "philox.cuh"
 #include "small_kernels.h"
 
 namespace dfl {
@@ -22,24 +23,6 @@ namespace dfl {
 namespace {
 
 constexpr int XT = 256;   // threads per CTA
-
-// Philox4x32-10 word 0 (Salmon, Moraes, Dror & Shaw, SC'11); the sampling
-// kernel carries its own copy so that this file stands alone.
-__device__ __forceinline__ uint32_t philox0(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3, uint32_t k0,
-                                            uint32_t k1) {
-    #pragma unroll
-    for (int r = 0; r < 10; ++r) {
-        const uint32_t lo0 = 0xD2511F53u * c0, hi0 = __umulhi(0xD2511F53u, c0);
-        const uint32_t lo1 = 0xCD9E8D57u * c2, hi1 = __umulhi(0xCD9E8D57u, c2);
-        const uint32_t n0 = hi1 ^ c1 ^ k0, n2 = hi0 ^ c3 ^ k1;
-        c0 = n0; c1 = lo1; c2 = n2; c3 = lo0;
-        k0 += 0x9E3779B9u;
-        k1 += 0xBB67AE85u;
-    }
-    return c0;
-}
-
-__device__ __forceinline__ double uniform24(uint32_t x0) { return ((double)(x0 >> 8) + 0.5) * (1.0 / 16777216.0); }
 
 // Element i of a row stored as fp32 or bf16.
 template <bool BF16>
@@ -54,12 +37,23 @@ struct RowMap {
     const void* base;
     int K, J;             // drafts per sequence, rows per draft
     const int32_t* sel;   // nullable: draft 0
+    int* err;             // nullable: error word for a selection outside 0..K-1
 };
+
+// Selected draft of sequence n; one outside 0..K-1 reads draft 0 and records
+// DFL_ERR_INVALID_ARG in the error word.
+__device__ __forceinline__ int64_t sel_of(const RowMap& m, int64_t n) {
+    if (!m.sel) return 0;
+    const int32_t k = m.sel[n];
+    if (k >= 0 && k < m.K) return k;
+    if (m.err) atomicCAS(m.err, 0, DFL_ERR_INVALID_ARG);
+    return 0;
+}
 
 template <bool BF16>
 __device__ __forceinline__ const void* row_ptr(const RowMap& m, int64_t r, int V) {
     const int64_t n = r / m.J, j = r % m.J;
-    const int64_t k = m.sel ? m.sel[n] : 0;
+    const int64_t k = sel_of(m, n);
     const int64_t off = ((n * m.K + k) * m.J + j) * (int64_t)V;
     return static_cast<const uint8_t*>(m.base) + off * (BF16 ? 2 : 4);
 }
@@ -233,7 +227,7 @@ struct SpecArgs {
 
 __device__ __forceinline__ float lse_row(const SpecArgs& a, int64_t n, int j) {
     if (!a.lse_all) return a.lse_v[n * (a.G + 1) + j];
-    const int64_t k = a.vm.sel ? a.vm.sel[n] : 0;
+    const int64_t k = sel_of(a.vm, n);
     return a.lse_v[(n * a.vm.K + k) * (a.G + 1) + j];
 }
 
@@ -251,7 +245,7 @@ template <bool BF16>
 __global__ void spec_test_kernel(const SpecArgs a, int N) {
     const int64_t n = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
     if (n >= N) return;
-    const int64_t kd = a.vm.sel ? a.vm.sel[n] : 0;
+    const int64_t kd = sel_of(a.vm, n);
     const int32_t* x = a.drafts + (n * a.vm.K + kd) * a.G;
     int j = 0;
     for (; j < a.G; ++j) {
@@ -261,7 +255,7 @@ __global__ void spec_test_kernel(const SpecArgs a, int N) {
         const void* vr = row_ptr<BF16>(a.vm, n * (a.G + 1) + j, a.V);
         const double q = exp((double)(z[xj] * a.inv_T - a.lse_z[n * a.G + j]));
         const double p = exp((double)(elem<BF16>(vr, xj) - lse_row(a, n, j)));
-        const double u = uniform24(philox0((uint32_t)n, (uint32_t)j, 0u, 1u, a.key0, a.key1));
+        const double u = philox_uniform24((uint32_t)n, (uint32_t)j, 0u, 1u, a.key0, a.key1);
         if (!(u * q < p)) break;
     }
     a.stop[n] = j;
@@ -295,7 +289,7 @@ __global__ void residual_pick_kernel(const SpecArgs a, int32_t* accept_len, int3
     if (lane == 0) {
         double total = 0.0;
         for (int g = 0; g < a.ngroups; ++g) total += gs[g];
-        const double u = uniform24(philox0((uint32_t)n, (uint32_t)j, 0u, 2u, a.key0, a.key1));
+        const double u = philox_uniform24((uint32_t)n, (uint32_t)j, 0u, 2u, a.key0, a.key1);
         const double target = u * total;
         double run = 0.0;
         int g = 0;
@@ -329,7 +323,134 @@ __global__ void residual_pick_kernel(const SpecArgs a, int32_t* accept_len, int3
     }
 }
 
+// Sampled-greedy acceptance (SpecDiff-2 notes, "Self-Selection Acceptance"
+// and "Streak-Distillation", read at temperature above zero): at every
+// window position j the verifier draws its own token y_j from P_j =
+// softmax(v_j) by inverse CDF at the Philox uniform of counter (n, j, 0, 3);
+// draft token x_j is accepted while it equals y_j, and the verifier's sample
+// at the first mismatch (y_G after a fully accepted window) is the committed
+// token.  All G+1 draws of a sequence are made in parallel:
+//  1. vdraw_group_kernel: per (row, group of RG tokens) the sum of the row's
+//     weights exp(v - lse), lanes adding 8 consecutive elements per 16-byte
+//     load in fp32, the group total in fp64;
+//  2. vdraw_pick_kernel: per row, the group holding u * total (exclusive scan
+//     of the group sums) and an index-ordered fp64 walk of that group;
+//  3. sg_accept_kernel: per sequence, the first mismatch by warp ballot.
+struct SgArgs {
+    RowMap vm;            // verifier rows of the verified draft: r = n * (G+1) + j
+    const float* lse_v;   // [N][G+1], or [N][K][G+1] when lse_all
+    int lse_all;
+    int G, V;
+    uint32_t key0, key1;
+    double* gsum;         // [N*(G+1)][ngroups]
+    int32_t* y;           // [N*(G+1)] the verifier's samples
+    int ngroups;
+};
+
+__device__ __forceinline__ float sg_lse(const SgArgs& a, int64_t r) {
+    if (!a.lse_all) return a.lse_v[r];
+    const int64_t n = r / (a.G + 1), j = r % (a.G + 1);
+    const int64_t k = sel_of(a.vm, n);
+    return a.lse_v[(n * a.vm.K + k) * (a.G + 1) + j];
+}
+
+template <bool BF16>
+__global__ void vdraw_group_kernel(const SgArgs a) {
+    const int64_t r = blockIdx.x;
+    const int g = blockIdx.y * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (g >= a.ngroups) return;
+    const void* vr = row_ptr<BF16>(a.vm, r, a.V);
+    const float lse = sg_lse(a, r);
+    const int b = g * RG, e = min(a.V, b + RG);
+    float acc = 0.f;
+    if ((a.V & 7) == 0) {   // group bounds are multiples of 8
+        for (int c = b / 8 + lane; c < e / 8; c += 32) {
+            float x[8];
+            load8<BF16>(vr, c, x);
+            #pragma unroll
+            for (int q = 0; q < 8; ++q) acc += expf(x[q] - lse);
+        }
+    } else {
+        for (int i = b + lane; i < e; i += 32) acc += expf(elem<BF16>(vr, i) - lse);
+    }
+    double t = (double)acc;
+    #pragma unroll
+    for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xFFFFFFFFu, t, o);
+    if (lane == 0) a.gsum[r * a.ngroups + g] = t;
+}
+
+template <bool BF16>
+__global__ void vdraw_pick_kernel(const SgArgs a) {
+    const int64_t r = blockIdx.x;
+    const int lane = threadIdx.x;
+    const int64_t n = r / (a.G + 1);
+    const int j = (int)(r % (a.G + 1));
+    const double* gs = a.gsum + r * a.ngroups;
+    __shared__ int gsel;
+    __shared__ double rel_s;
+    if (lane == 0) {
+        double total = 0.0;
+        for (int g = 0; g < a.ngroups; ++g) total += gs[g];
+        const double target = philox_uniform24((uint32_t)n, (uint32_t)j, 0u, 3u, a.key0, a.key1) * total;
+        double run = 0.0;
+        int g = 0;
+        for (; g < a.ngroups - 1; ++g) {
+            if (run + gs[g] > target) break;
+            run += gs[g];
+        }
+        gsel = g;
+        rel_s = target - run;
+    }
+    __syncwarp();
+    const int g = gsel;
+    const double rel = rel_s;
+    const void* vr = row_ptr<BF16>(a.vm, r, a.V);
+    const float lse = sg_lse(a, r);
+    const int b0 = g * RG, b1 = min(a.V, b0 + RG);
+    double run = 0.0;
+    int pick = b1 - 1;   // a target the walk does not reach (rounding at the group's end)
+    for (int b = b0; b < b1; b += 32) {
+        double x = (b + lane < b1) ? (double)expf(elem<BF16>(vr, b + lane) - lse) : 0.0;
+        #pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const double t = __shfl_up_sync(0xFFFFFFFFu, x, o);
+            if (lane >= o) x += t;
+        }
+        const unsigned hit = __ballot_sync(0xFFFFFFFFu, b + lane < b1 && run + x > rel);
+        if (hit) { pick = b + __ffs(hit) - 1; break; }
+        run += __shfl_sync(0xFFFFFFFFu, x, 31);
+    }
+    if (lane == 0) a.y[r] = pick;
+}
+
+__global__ void sg_accept_kernel(const SgArgs a, const int32_t* drafts, int N, int32_t* accept_len,
+                                 int32_t* next_token) {
+    const int64_t n = blockIdx.x * (int64_t)(blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (n >= N) return;
+    const int64_t k = sel_of(a.vm, n);
+    const int32_t* x = drafts + (n * a.vm.K + k) * a.G;
+    const int32_t* y = a.y + n * (a.G + 1);
+    int acc = a.G;
+    for (int j0 = 0; j0 < a.G; j0 += 32) {
+        const int j = j0 + lane;
+        const unsigned miss = __ballot_sync(0xFFFFFFFFu, j < a.G && x[j] != y[j]);
+        if (miss) { acc = j0 + __ffs(miss) - 1; break; }
+    }
+    if (lane == 0) {
+        accept_len[n] = acc;
+        next_token[n] = y[acc];
+    }
+}
+
 inline size_t al256(size_t b) { return (b + 255) & ~size_t(255); }
+
+// The current device's error word (nullptr if none is current).
+inline int* err_word() {
+    DeviceCtx* c = current_ctx();
+    return c ? c->err_word : nullptr;
+}
 
 }  // namespace
 
@@ -370,7 +491,7 @@ dfl_status spec_run(const float* logits, float inv_T, const void* vlog, bool bf,
                     int32_t* next_token, const float* lse_z, const float* lse_v, bool lse_all, void* scratch,
                     cudaStream_t st) {
     ProfScope ps("spec_accept", st);
-    SpecArgs sa{logits, lse_z, inv_T, RowMap{vlog, K, G + 1, sel}, lse_v, lse_all ? 1 : 0, drafts, G, V,
+    SpecArgs sa{logits, lse_z, inv_T, RowMap{vlog, K, G + 1, sel, err_word()}, lse_v, lse_all ? 1 : 0, drafts, G, V,
                 (uint32_t)(seed & 0xFFFFFFFFu), (uint32_t)(seed >> 32), nullptr, nullptr, (V + RG - 1) / RG};
     uint8_t* p = static_cast<uint8_t*>(scratch);
     sa.stop = reinterpret_cast<int*>(p);
@@ -385,6 +506,36 @@ dfl_status spec_run(const float* logits, float inv_T, const void* vlog, bool bf,
         residual_group_kernel<false><<<ggrid, 256, 0, st>>>(sa);
         residual_pick_kernel<false><<<N, 32, 0, st>>>(sa, accept_len, next_token);
     }
+    return last_launch();
+}
+
+size_t sg_scratch_bytes(int N, int G, int V) {
+    const size_t rows = (size_t)N * (G + 1);
+    return al256(rows * 4) + al256(rows * ((V + RG - 1) / RG) * 8);
+}
+
+size_t sg_ws_bytes(int N, int G, int V) { return al256((size_t)N * (G + 1) * 4) + sg_scratch_bytes(N, G, V); }
+
+dfl_status sg_run(const void* vlog, bool bf, const int32_t* drafts, const int32_t* sel, int N, int K, int G, int V,
+                  uint64_t seed, int32_t* accept_len, int32_t* next_token, const float* lse_v, bool lse_all,
+                  void* scratch, cudaStream_t st) {
+    if ((int64_t)V > (int64_t)65535 * 8 * RG) return DFL_ERR_UNSUPPORTED_SHAPE;   // groups of a row: grid.y
+    ProfScope ps("sampled_greedy", st);
+    SgArgs sa{RowMap{vlog, K, G + 1, sel, err_word()}, lse_v, lse_all ? 1 : 0, G, V, (uint32_t)(seed & 0xFFFFFFFFu),
+              (uint32_t)(seed >> 32), nullptr, nullptr, (V + RG - 1) / RG};
+    uint8_t* p = static_cast<uint8_t*>(scratch);
+    const int64_t rows = (int64_t)N * (G + 1);
+    sa.y = reinterpret_cast<int32_t*>(p);
+    sa.gsum = reinterpret_cast<double*>(p + al256((size_t)rows * 4));
+    const dim3 ggrid((unsigned)rows, (sa.ngroups + 7) / 8);
+    if (bf) {
+        vdraw_group_kernel<true><<<ggrid, 256, 0, st>>>(sa);
+        vdraw_pick_kernel<true><<<(unsigned)rows, 32, 0, st>>>(sa);
+    } else {
+        vdraw_group_kernel<false><<<ggrid, 256, 0, st>>>(sa);
+        vdraw_pick_kernel<false><<<(unsigned)rows, 32, 0, st>>>(sa);
+    }
+    sg_accept_kernel<<<(N + 3) / 4, 128, 0, st>>>(sa, drafts, N, accept_len, next_token);
     return last_launch();
 }
 
@@ -439,7 +590,7 @@ extern "C" dfl_status dfl_spec_accept(const float* logits, float T, const void* 
     float* lse_v = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + al256((size_t)N * G * 4));
     const float inv_T = 1.0f / T;
     const bool bf = dt == DFL_BF16;
-    const RowMap vm{vlog, K, G + 1, sel};
+    const RowMap vm{vlog, K, G + 1, sel, err_word()};
     {
         ProfScope ps("row_lse", st);
         row_lse_kernel<false><<<(unsigned)(N * G), XT, 0, st>>>(RowMap{logits, 1, G, nullptr}, V, inv_T, lse_z);
@@ -450,4 +601,31 @@ extern "C" dfl_status dfl_spec_accept(const float* logits, float T, const void* 
     if (rc != DFL_OK) return rc;
     return spec_run(logits, inv_T, vlog, bf, drafts, sel, N, K, G, V, seed, accept_len, next_token, lse_z, lse_v,
                     false, static_cast<uint8_t*>(ws) + al256((size_t)N * G * 4) + al256((size_t)N * (G + 1) * 4), st);
+}
+
+extern "C" dfl_status dfl_sampled_greedy_accept(const void* vlog, dfl_dtype dt, const int32_t* drafts,
+                                                const int32_t* sel, int32_t N, int32_t K, int32_t G, int32_t V,
+                                                uint64_t seed, int32_t* accept_len, int32_t* next_token, void* ws,
+                                                size_t ws_bytes, dfl_stream stream) {
+    const dfl::ApiRange nvtx_range("dfl_sampled_greedy_accept");
+    if (!vlog || !drafts || !accept_len || !next_token || !ws || N <= 0 || K < 1 || K > 64 || G < 1 || G > 1024 ||
+        V <= 0)
+        return DFL_ERR_INVALID_ARG;
+    if (dt != DFL_F32 && dt != DFL_BF16) return DFL_ERR_INVALID_ARG;
+    if (!aligned16(vlog) || !aligned16(ws)) return DFL_ERR_MISALIGNED;
+    if (ws_bytes < sg_ws_bytes(N, G, V)) return DFL_ERR_WORKSPACE;
+    if (!current_ctx()) return DFL_ERR_NO_DEVICE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    float* lse_v = static_cast<float*>(ws);
+    const bool bf = dt == DFL_BF16;
+    {
+        ProfScope ps("row_lse", st);
+        const RowMap vm{vlog, K, G + 1, sel, err_word()};
+        if (bf) row_lse_kernel<true><<<(unsigned)(N * (G + 1)), XT, 0, st>>>(vm, V, 1.f, lse_v);
+        else row_lse_kernel<false><<<(unsigned)(N * (G + 1)), XT, 0, st>>>(vm, V, 1.f, lse_v);
+    }
+    dfl_status rc = last_launch();
+    if (rc != DFL_OK) return rc;
+    return sg_run(vlog, bf, drafts, sel, N, K, G, V, seed, accept_len, next_token, lse_v, false,
+                  static_cast<uint8_t*>(ws) + al256((size_t)N * (G + 1) * 4), st);
 }

@@ -33,12 +33,37 @@ inline uint8_t* carve(uint8_t*& p, size_t bytes) {
 }
 }  // namespace
 
+// Unique id of the CUDA context current on this thread (0 if none or unknown),
+// through the driver's cuCtxGetCurrent / cuCtxGetId.
+uint64_t current_context_id() {
+    using GetCurrentFn = CUresult (*)(CUcontext*);
+    using GetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+    static GetCurrentFn get_current = nullptr;
+    static GetIdFn get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<GetCurrentFn>(p);
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<GetIdFn>(p);
+    });
+    CUcontext c = nullptr;
+    unsigned long long id = 0;
+    if (!get_current || !get_id || get_current(&c) != CUDA_SUCCESS || !c || get_id(c, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
+
 DeviceCtx* current_ctx() {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-    if (g_ready[dev].load(std::memory_order_acquire)) return &g_ctx[dev];
+    const uint64_t cid = current_context_id();
+    if (g_ready[dev].load(std::memory_order_acquire) && cid != 0 && g_ctx[dev].ctx_id.load() == cid)
+        return &g_ctx[dev];
     std::lock_guard<std::mutex> lk(g_mu);
-    if (g_ready[dev].load(std::memory_order_relaxed)) return &g_ctx[dev];
     int major = 0, minor = 0, sms = 0;
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
@@ -46,10 +71,27 @@ DeviceCtx* current_ctx() {
         return nullptr;
     if (major != 10 || minor != 3) return nullptr;   // kernels are built for sm_103a only
     DeviceCtx& c = g_ctx[dev];
-    if (cudaGetSymbolAddress(reinterpret_cast<void**>(&c.err_word), g_dfl_error_word) != cudaSuccess)
-        return nullptr;
+    // Looking the symbol up binds the runtime's context, so its id is read after.
+    int* word = nullptr;
+    if (cudaGetSymbolAddress(reinterpret_cast<void**>(&word), g_dfl_error_word) != cudaSuccess) return nullptr;
+    const uint64_t now = current_context_id();
+    if (g_ready[dev].load(std::memory_order_relaxed) && c.ctx_id.load() == now) return &c;
+    // First use on this device, or another context than the one the entry was
+    // set up in: what belonged to the old context (function attributes, the
+    // copy stream and its events) is dropped, not destroyed -- it went with
+    // its context.
+    {
+        std::lock_guard<std::mutex> hk(c.host_mu);
+        c.copy_st = nullptr;
+        for (cudaEvent_t& e : c.copy_ev) e = nullptr;
+    }
+    for (auto& f : c.gemm_attr_set) f = false;
+    for (auto& f : c.attn_attr_set) f = false;
+    c.mix_attr_set = false;
+    c.err_word = word;
     c.device = dev;
     c.sm_count = sms;
+    c.ctx_id.store(now);
     g_ready[dev].store(true, std::memory_order_release);
     return &c;
 }
@@ -66,6 +108,9 @@ size_t ws_block_attn(int N, int C, int B, int Hq, int Hkv, int hd, int dt, bool 
     if (dt == DFL_BF16) b += al256(attn_ws_bytes(N, C, B, Hq, Hkv, hd, ragged));
     return b;
 }
+
+// fp32 pre-norm features of the DFlash fusion, [rows][d]
+size_t ws_fc_fuse(int64_t rows, int d) { return al256((size_t)rows * d * 4); }
 
 size_t ws_block_ffn(int N, int B, int d, int F, int dt) {
     const size_t M = (size_t)N * B;
@@ -100,7 +145,9 @@ size_t step_ws_bytes(const dfl_shape& s, bool cached) {
     if (cached && (s.dtype != DFL_BF16 || s.R < 1)) return 0;
     const size_t e = esz(s.dtype);
     const int64_t rows = (int64_t)s.N * (cached ? s.R : s.C);   // context rows mixed this step
-    size_t xc = (size_t)s.D * rows * s.d * e;
+    // per-layer mixtures of all D layers, or one fused representation and its
+    // fp32 pre-norm features (DFlash fusion)
+    size_t xc = s.fc ? al256((size_t)rows * s.d * e) + ws_fc_fuse(rows, s.d) : (size_t)s.D * rows * s.d * e;
     if (cached && s.V > 0 && s.K > 0) xc = std::max(xc, (size_t)s.N * (s.B - 1) * s.V * 4);
     size_t b = al256(xc);
     b += al256((size_t)s.N * s.B * s.Hq * s.hd * e);                         // Q
@@ -116,7 +163,7 @@ size_t step_ws_bytes(const dfl_shape& s, bool cached) {
             // self-selection scratch (its verifier-row LSEs are reused), drafter-row LSEs,
             // stochastic-acceptance scratch
             sub = std::max(sub, al256(select_ws_bytes(s.N, s.K, s.B - 1)) + al256((size_t)s.N * (s.B - 1) * 4) +
-                                    spec_scratch_bytes(s.N, s.V));
+                                    std::max(spec_scratch_bytes(s.N, s.V), sg_scratch_bytes(s.N, s.B - 1, s.V)));
             b += al256((size_t)s.N * s.K * (s.B - 1) * 4);                   // samples
         }
         b += al256((size_t)s.N * (s.B - 1) * 4);                             // drafts
@@ -149,7 +196,8 @@ extern "C" const char* dfl_status_string(dfl_status s) {
 extern "C" size_t dfl_workspace_size(dfl_op op, const dfl_shape* s) {
     if (!s || (s->dtype != DFL_F32 && s->dtype != DFL_BF16)) return 0;
     // every size is a count: a negative one makes the shape invalid
-    for (int32_t v : {s->N, s->C, s->B, s->d, s->Hq, s->Hkv, s->hd, s->D, s->L, s->V, s->K, s->G, s->row0, s->F, s->R})
+    for (int32_t v : {s->N, s->C, s->B, s->d, s->Hq, s->Hkv, s->hd, s->D, s->L, s->V, s->K, s->G, s->row0, s->F, s->R,
+                      s->fc})
         if (v < 0) return 0;
     switch (op) {
         case DFL_OP_DUAL_KV_PROJ: return ws_dual_kv_proj(s->N, s->B, s->d, s->dtype);
@@ -164,6 +212,8 @@ extern "C" size_t dfl_workspace_size(dfl_op op, const dfl_shape* s) {
         case DFL_OP_DRAFT_STEP: return step_ws_bytes(*s, false);
         case DFL_OP_DRAFT_STEP_CACHED: return step_ws_bytes(*s, true);
         case DFL_OP_DRAFT_STEP_HOST: return step_host_ws_bytes(*s);
+        case DFL_OP_FC_FUSE: return ws_fc_fuse((int64_t)s->N * s->C, s->d);
+        case DFL_OP_SAMPLED_GREEDY: return sg_ws_bytes(s->N, s->G, s->V);
     }
     return 0;
 }
@@ -207,6 +257,78 @@ extern "C" dfl_status dfl_greedy_accept(const int32_t* draft, const int32_t* tar
         return DFL_ERR_INVALID_ARG;
     if (!current_ctx()) return DFL_ERR_NO_DEVICE;
     return greedy_accept(draft, target, N, n, accept_len, bonus, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" dfl_status dfl_philox4x32_10(const uint32_t* in, int32_t n, uint32_t* out, dfl_stream stream) {
+    const dfl::ApiRange nvtx_range("dfl_philox4x32_10");
+    if (!in || !out || n <= 0) return DFL_ERR_INVALID_ARG;
+    if (!current_ctx()) return DFL_ERR_NO_DEVICE;
+    return philox_block(in, n, out, static_cast<cudaStream_t>(stream));
+}
+
+// ------------------------------------------------------- DFlash fusion
+
+namespace dfl {
+namespace {
+// Xc = RMSNorm([H_1 .. H_L] W_fc^T; gain): bf16 as one tensor-core GEMM over
+// K = L*d whose A tiles come from the L slabs in turn (a 3-D tensor map),
+// fp32 as L accumulating CUDA-core GEMMs; the fp32 pre-norm features F then
+// go through the row RMSNorm.
+dfl_status fc_fuse_impl(DeviceCtx* ctx, const void* H, int64_t layer_stride, int L, int64_t rows, int d, int dt,
+                        const void* W_fc, const float* gain, float eps, void* Xc, float* F, cudaStream_t st) {
+    dfl_status rc;
+    if (dt == DFL_F32) {
+        const float* h = static_cast<const float*>(H);
+        const float* w = static_cast<const float*>(W_fc);
+        for (int i = 0; i < L; ++i)
+            if ((rc = gemm_f32_ld(h + (size_t)i * layer_stride, d, w + (size_t)i * d, (int64_t)L * d, F, (int)rows,
+                                  d, d, d, i > 0, st)) != DFL_OK)
+                return rc;
+    } else {
+        GemmArgs g{};
+        g.A = H; g.M = (int)rows; g.K = L * d;
+        g.a_slabs = L; g.a_slab_stride = L > 1 ? layer_stride : (int64_t)rows * d;
+        g.B[0] = W_fc; g.b_rows[0] = d; g.b_begin[0] = 0; g.nb = 1; g.N = d;
+        g.bn = 0;
+        g.m_inner = 0;   // N-tiles innermost: the L slabs of an A row block are read from HBM once
+        g.epi = EPI_RESID;
+        g.ep.resid = F; g.ep.ld_resid = d; g.ep.resid_store = 1;
+        g.tag = "gemm_fc_fuse";
+        if ((rc = gemm_tc(ctx, g, st)) != DFL_OK) return rc;
+    }
+    return rmsnorm_rows(F, d, rows, 1, 1, 0, gain, eps, Xc, dt == DFL_BF16, st);
+}
+
+// Host-side checks shared by the entry point and the steps.
+dfl_status fc_fuse_check(const void* H, int64_t layer_stride, int L, int64_t rows, int d, int dt, const void* W_fc,
+                         const float* gain, const void* Xc) {
+    if (!H || !W_fc || !gain || !Xc || L < 1 || L > 64 || rows <= 0 || d <= 0) return DFL_ERR_INVALID_ARG;
+    if (dt != DFL_F32 && dt != DFL_BF16) return DFL_ERR_INVALID_ARG;
+    if (L > 1 && layer_stride < rows * d) return DFL_ERR_INVALID_ARG;
+    if (!rows_fit(rows) || (int64_t)L * d >= ((int64_t)1 << 31)) return DFL_ERR_UNSUPPORTED_SHAPE;
+    const void* ptrs[] = {H, W_fc, gain, Xc};
+    for (const void* p : ptrs) if (!aligned16(p)) return DFL_ERR_MISALIGNED;
+    if (d % 8 != 0 || (layer_stride * (int64_t)esz(dt)) % 16 != 0) return DFL_ERR_MISALIGNED;
+    if (dt == DFL_BF16 && d % 64 != 0) return DFL_ERR_UNSUPPORTED_SHAPE;
+    if (d > 6144) return DFL_ERR_UNSUPPORTED_SHAPE;   // the row RMSNorm keeps a row in registers
+    return DFL_OK;
+}
+}  // namespace
+}  // namespace dfl
+
+extern "C" dfl_status dfl_fc_fuse(const void* H, int64_t layer_stride, int32_t L, int64_t rows, int32_t d,
+                                  dfl_dtype dt, const void* W_fc, const float* gain, float eps, void* Xc, void* ws,
+                                  size_t ws_bytes, dfl_stream stream) {
+    const dfl::ApiRange nvtx_range("dfl_fc_fuse");
+    dfl_status rc = fc_fuse_check(H, layer_stride, L, rows, d, dt, W_fc, gain, Xc);
+    if (rc != DFL_OK) return rc;
+    if (!ws) return DFL_ERR_INVALID_ARG;
+    if (!aligned16(ws)) return DFL_ERR_MISALIGNED;
+    if (ws_bytes < ws_fc_fuse(rows, d)) return DFL_ERR_WORKSPACE;
+    DeviceCtx* ctx = current_ctx();
+    if (!ctx) return DFL_ERR_NO_DEVICE;
+    return fc_fuse_impl(ctx, H, layer_stride, L, rows, d, dt, W_fc, gain, eps, Xc, static_cast<float*>(ws),
+                        static_cast<cudaStream_t>(stream));
 }
 
 // ------------------------------------------------------- dual projection
@@ -561,6 +683,13 @@ dfl_status step_bf16_shape(const dfl_step_args* a) {
     return DFL_OK;
 }
 
+// Shape rules of the DFlash fusion in a step.
+dfl_status rc_fc_shape(const dfl_step_args* a) {
+    if ((int64_t)a->L * a->d >= ((int64_t)1 << 31) || a->d > 6144) return DFL_ERR_UNSUPPORTED_SHAPE;
+    if (a->dtype == DFL_BF16 && a->d % 64 != 0) return DFL_ERR_UNSUPPORTED_SHAPE;
+    return DFL_OK;
+}
+
 // Host-side checks of a step's arguments (no launch).
 dfl_status step_check(const dfl_step_args* a, const dfl_ctx_cache* cache, const void* ws) {
     if (!a || !ws) return DFL_ERR_INVALID_ARG;
@@ -568,8 +697,8 @@ dfl_status step_check(const dfl_step_args* a, const dfl_ctx_cache* cache, const 
     if (dt != DFL_F32 && dt != DFL_BF16) return DFL_ERR_INVALID_ARG;
     if (a->N <= 0 || a->C <= 0 || a->B < 2 || a->d <= 0 || a->D < 1 || a->D > 8 || a->L < 1 || a->V < 0)
         return DFL_ERR_INVALID_ARG;
-    if (!a->H || !a->mix_logits || !a->mix_gain || !a->blk_gain || !a->layers || !a->Xb0 || !a->Xb)
-        return DFL_ERR_INVALID_ARG;
+    if (!a->H || !a->blk_gain || !a->layers || !a->Xb0 || !a->Xb) return DFL_ERR_INVALID_ARG;
+    if (a->W_fc ? !a->fc_gain : (!a->mix_logits || !a->mix_gain)) return DFL_ERR_INVALID_ARG;
     if (a->V > 0 && (!a->W_lm || !a->final_gain || !a->draft)) return DFL_ERR_INVALID_ARG;
     if (a->target && (!a->accept_len || !a->bonus)) return DFL_ERR_INVALID_ARG;
     if (a->sample && (!a->samples || a->V == 0)) return DFL_ERR_INVALID_ARG;
@@ -577,7 +706,7 @@ dfl_status step_check(const dfl_step_args* a, const dfl_ctx_cache* cache, const 
         return DFL_ERR_INVALID_ARG;
     if ((a->tv_alpha || a->tv_tokens || a->accept_rule != 0) && !a->vlog) return DFL_ERR_INVALID_ARG;
     if (a->tv_tokens && !a->tv_alpha) return DFL_ERR_INVALID_ARG;
-    if (a->accept_rule != 0 && a->accept_rule != 1) return DFL_ERR_INVALID_ARG;
+    if (a->accept_rule < 0 || a->accept_rule > 2) return DFL_ERR_INVALID_ARG;
     if (a->F < 0 || (a->F > 0 && !a->ffn_gain)) return DFL_ERR_INVALID_ARG;
     for (int l = 0; l < a->D; ++l) {
         const dfl_layer_weights& w = a->layers[l];
@@ -591,11 +720,12 @@ dfl_status step_check(const dfl_step_args* a, const dfl_ctx_cache* cache, const 
     if (!rows_fit(h_rows) || !rows_fit((int64_t)a->N * a->C) || !rows_fit((int64_t)a->N * a->B))
         return DFL_ERR_UNSUPPORTED_SHAPE;
     if (a->L > 1 && a->h_layer_stride < h_rows * a->d) return DFL_ERR_INVALID_ARG;
+    if (a->W_fc && (rc_fc_shape(a) != DFL_OK)) return rc_fc_shape(a);
     if (a->d % 8 != 0 || a->hd % 8 != 0 || a->F % 8 != 0 || a->h_layer_stride % 8 != 0)
         return DFL_ERR_MISALIGNED;
     // The 16-byte rule of every kernel the step launches, likewise.
     const void* al[] = {ws, a->Xb, a->mix_gain, a->blk_gain, a->final_gain, a->W_lm, a->rope, a->ffn_gain,
-                        a->logits, a->vlog};
+                        a->logits, a->vlog, a->W_fc, a->fc_gain};
     for (const void* q : al)
         if (q && !aligned16(q)) return DFL_ERR_MISALIGNED;
     for (int l = 0; l < a->D; ++l) {
@@ -621,6 +751,7 @@ dfl_shape step_shape(const dfl_step_args* a, const dfl_ctx_cache* cache) {
     s.N = a->N; s.C = a->C; s.B = a->B; s.d = a->d; s.Hq = a->Hq; s.Hkv = a->Hkv; s.hd = a->hd; s.D = a->D;
     s.L = a->L; s.V = a->V; s.K = a->sample ? a->sample->K : 0; s.G = a->B - 1; s.row0 = 1; s.dtype = a->dtype;
     s.F = a->F; s.R = cache ? cache->R : 0;
+    s.fc = a->W_fc ? 1 : 0;
     return s;
 }
 
@@ -647,9 +778,11 @@ dfl_status draft_step_impl(const dfl_step_args* a, const dfl_ctx_cache* cache, v
     const int R = cache ? cache->R : C;
     const int64_t ctx_rows = (int64_t)N * R;   // context rows mixed and projected this step
     uint8_t* p = static_cast<uint8_t*>(ws);
-    size_t xc_bytes = (size_t)a->D * ctx_rows * d * e;
+    const bool fc = a->W_fc != nullptr;
+    size_t xc_bytes = fc ? al256((size_t)ctx_rows * d * e) + ws_fc_fuse(ctx_rows, d) : (size_t)a->D * ctx_rows * d * e;
     if (cache && a->V > 0 && s.K > 0) xc_bytes = std::max(xc_bytes, (size_t)N * (B - 1) * a->V * 4);
     uint8_t* Xc = carve(p, xc_bytes);
+    float* F_fc = fc ? reinterpret_cast<float*>(Xc + al256((size_t)ctx_rows * d * e)) : nullptr;
     void* Q = carve(p, (size_t)N * B * a->Hq * a->hd * e);
     void* Kc = cache ? nullptr : carve(p, (size_t)ctx_rows * a->Hkv * a->hd * e);
     void* Vc = cache ? nullptr : carve(p, (size_t)ctx_rows * a->Hkv * a->hd * e);
@@ -683,12 +816,19 @@ dfl_status draft_step_impl(const dfl_step_args* a, const dfl_ctx_cache* cache, v
                          const_cast<int32_t*>(plan.ctx_dst), const_cast<int32_t*>(plan.blk_pos), len_new,
                          dev_err(dctx), st)) != DFL_OK)
         return rc;
-    if ((rc = dfl_layer_mix_rmsnorm(a->H, a->h_layer_stride, a->L, ctx_rows, d, ddt, a->D, a->mix_logits,
-                                    a->mix_gain, a->eps, Xc, ctx_rows * d, stream)) != DFL_OK)
+    if (fc) {
+        if ((rc = fc_fuse_check(a->H, a->h_layer_stride, a->L, ctx_rows, d, dt, a->W_fc, a->fc_gain, Xc)) != DFL_OK)
+            return rc;
+        if ((rc = fc_fuse_impl(dctx, a->H, a->h_layer_stride, a->L, ctx_rows, d, dt, a->W_fc, a->fc_gain, a->eps, Xc,
+                               F_fc, st)) != DFL_OK)
+            return rc;
+    } else if ((rc = dfl_layer_mix_rmsnorm(a->H, a->h_layer_stride, a->L, ctx_rows, d, ddt, a->D, a->mix_logits,
+                                           a->mix_gain, a->eps, Xc, ctx_rows * d, stream)) != DFL_OK) {
         return rc;
+    }
     for (int l = 0; l < a->D; ++l) {
         const dfl_layer_weights& w = a->layers[l];
-        const void* xc_l = Xc + (size_t)l * ctx_rows * d * e;
+        const void* xc_l = Xc + (fc ? 0 : (size_t)l * ctx_rows * d * e);   // the fusion serves every layer
         if (cache) {
             void* Kl = static_cast<uint8_t*>(cache->K) + (size_t)l * cache->layer_stride * 2;
             void* Vl = static_cast<uint8_t*>(cache->V) + (size_t)l * cache->layer_stride * 2;
@@ -745,13 +885,17 @@ dfl_status step_tail(const dfl_step_args* a, const dfl_shape& s, uint8_t* Xc, si
         float* lse_z = reinterpret_cast<float*>(q);
         q += al256((size_t)N * G * 4);
         const float inv_T = 1.0f / a->sample->T;
-        if ((rc = lse_rows_f32(logits, N * G, a->V, inv_T, lse_z, st)) != DFL_OK) return rc;
+        if (a->tv_alpha || a->accept_rule == 1)
+            if ((rc = lse_rows_f32(logits, N * G, a->V, inv_T, lse_z, st)) != DFL_OK) return rc;
         if (a->tv_alpha && (rc = tv_run(logits, inv_T, a->vlog, dt == DFL_BF16, N, K, G, a->V, a->tv_alpha,
                                         a->tv_tokens, lse_z, lse_v, st)) != DFL_OK)
             return rc;
         if (a->accept_rule == 1)
             return spec_run(logits, inv_T, a->vlog, dt == DFL_BF16, samples, a->selected, N, K, G, a->V,
                             a->accept_seed, a->accept_len, a->bonus, lse_z, lse_v, true, q, st);
+        if (a->accept_rule == 2)
+            return sg_run(a->vlog, dt == DFL_BF16, samples, a->selected, N, K, G, a->V, a->accept_seed,
+                          a->accept_len, a->bonus, lse_v, true, q, st);
         return DFL_OK;
     }
     if (a->target) return dfl_greedy_accept(a->draft, a->target, N, B - 1, a->accept_len, a->bonus, stream);
@@ -796,8 +940,13 @@ dfl_status draft_step_host_impl(const dfl_step_args* a, void* H_dev, int chunks,
     const int64_t ctx_rows = (int64_t)N * C;
     // the plain step's carve, then layers 1..D-1's context K/V past its end
     uint8_t* p = static_cast<uint8_t*>(ws);
-    const size_t xc_bytes = (size_t)D * ctx_rows * d * 2;
+    const bool fc = a->W_fc != nullptr;
+    const size_t xc_bytes = fc ? al256((size_t)ctx_rows * d * 2) + ws_fc_fuse(ctx_rows, d) : (size_t)D * ctx_rows * d * 2;
     uint8_t* Xc = carve(p, xc_bytes);
+    float* F_fc = fc ? reinterpret_cast<float*>(Xc + al256((size_t)ctx_rows * d * 2)) : nullptr;
+    if (fc && (rc = fc_fuse_check(H_dev, a->h_layer_stride, L, ctx_rows, d, DFL_BF16, a->W_fc, a->fc_gain, Xc)) !=
+                  DFL_OK)
+        return rc;
     void* Q = carve(p, (size_t)N * B * a->Hq * a->hd * 2);
     uint8_t* Kc0 = carve(p, (size_t)ctx_rows * kv * 2);
     uint8_t* Vc0 = carve(p, (size_t)ctx_rows * kv * 2);
@@ -846,12 +995,17 @@ dfl_status draft_step_host_impl(const dfl_step_args* a, void* H_dev, int chunks,
                 return DFL_ERR_CUDA;
         if (cudaEventRecord(ev[c], dctx->copy_st) != cudaSuccess || cudaStreamWaitEvent(st, ev[c], 0) != cudaSuccess)
             return DFL_ERR_CUDA;
-        if ((rc = dfl_layer_mix_rmsnorm(Hd + off, a->h_layer_stride, L, rows, d, DFL_BF16, D, a->mix_logits,
-                                        a->mix_gain, a->eps, Xc + off, ctx_rows * d, stream)) != DFL_OK)
+        if (fc) {   // the group's rows of the one fused representation
+            if ((rc = fc_fuse_impl(dctx, Hd + off, a->h_layer_stride, L, rows, d, DFL_BF16, a->W_fc, a->fc_gain,
+                                   a->eps, Xc + off, F_fc + (size_t)r0 * d, st)) != DFL_OK)
+                return rc;
+        } else if ((rc = dfl_layer_mix_rmsnorm(Hd + off, a->h_layer_stride, L, rows, d, DFL_BF16, D, a->mix_logits,
+                                               a->mix_gain, a->eps, Xc + off, ctx_rows * d, stream)) != DFL_OK) {
             return rc;
+        }
         for (int l = 0; l < D; ++l) {   // context rows start at a sequence: position = row % C
             const dfl_layer_weights& w = a->layers[l];
-            const GemmArgs gc = ctx_kv_args(Xc + (size_t)l * ctx_rows * d * 2 + off, rows, C, d, w.Wkc, w.Wvc,
+            const GemmArgs gc = ctx_kv_args(Xc + (fc ? 0 : (size_t)l * ctx_rows * d * 2) + off, rows, C, d, w.Wkc, w.Wvc,
                                             a->Hkv, a->hd, a->rope, kc_of(l) + (size_t)r0 * kv * 2,
                                             vc_of(l) + (size_t)r0 * kv * 2, nullptr);
             if ((rc = gemm_tc(dctx, gc, st)) != DFL_OK) return rc;

@@ -34,6 +34,21 @@ bool make_map(CUtensorMap* m, const void* base, int rows, int K, int box_rows) {
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// bf16 [slabs][rows][w] with slab stride `sstride` elements, box = box_rows x 64
+// elements of one slab, 128-byte swizzle (the same shared-memory tile as the
+// 2-D map's).
+bool make_map_3d(CUtensorMap* m, const void* base, int rows, int w, int slabs, int64_t sstride, int box_rows) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)w, (cuuint64_t)rows, (cuuint64_t)slabs};
+    cuuint64_t strides[2] = {(cuuint64_t)w * 2, (cuuint64_t)sstride * 2};
+    cuuint32_t box[3] = {(cuuint32_t)GEMM_BK, (cuuint32_t)box_rows, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int BN, int EPI, int CM>
 dfl_status launch(DeviceCtx* ctx, const GemmProb& p0, const GemmProb& p1, int nprob, const char* tag,
                   cudaStream_t st, int slot) {
@@ -113,7 +128,15 @@ static dfl_status build_prob(const GemmArgs& g, int cm, GemmProb& P) {
     sh.nb = g.nb;
     sh.split_b = g.split_b;
     if (g.split_b && (g.nb != 2 || (g.N / 2) % (g.bn / 2) != 0)) return DFL_ERR_UNSUPPORTED_SHAPE;
-    if (!make_map(&P.a, g.A, g.M, g.K, GEMM_BM)) return DFL_ERR_CUDA;
+    if (g.a_slabs > 0) {
+        const int w = g.K / g.a_slabs;
+        if (g.K % g.a_slabs != 0 || w % GEMM_BK != 0) return DFL_ERR_UNSUPPORTED_SHAPE;
+        if ((g.a_slab_stride * 2) % 16 != 0 || g.a_slab_stride < (int64_t)g.M * w) return DFL_ERR_MISALIGNED;
+        if (!make_map_3d(&P.a, g.A, g.M, w, g.a_slabs, g.a_slab_stride, GEMM_BM)) return DFL_ERR_CUDA;
+        sh.a_kb_per_slab = w / GEMM_BK;
+    } else if (!make_map(&P.a, g.A, g.M, g.K, GEMM_BM)) {
+        return DFL_ERR_CUDA;
+    }
     for (int j = 0; j < 3; ++j) {
         const int jj = j < g.nb ? j : 0;
         if (!aligned16(g.B[jj])) return DFL_ERR_MISALIGNED;

@@ -43,6 +43,7 @@ struct GemmEpi {
     // residual
     float* resid;        // fp32 [M][ld_resid]
     int ld_resid;
+    int resid_store;     // EPI_RESID: store C instead of adding it (out = C)
     // argmax / sampling partials, [M][tiles_n]
     float* part_max;
     int* part_idx;
@@ -59,6 +60,7 @@ struct GemmShape {
     int b_begin[3];      // first column served by B tensor map 1, 2, 3
     int nb;              // number of B tensor maps
     int split_b;         // B tile = [BN/2 rows of map 0 ; BN/2 rows of map 1] at rows tn * BN/2
+    int a_kb_per_slab;   // > 0: A is a 3-D map [slabs][M][K / slabs]; k-block kb reads slab kb / a_kb_per_slab
 };
 
 // One GEMM of a launch: its tensor maps (A, up to three B segments), shape and
@@ -165,6 +167,7 @@ template <int BN>
 __device__ __forceinline__ void epi_resid(const GemmShape& sh, const GemmEpi& ep, uint32_t tbase,
                                           int row, int n0) {
     const bool ok = row < sh.M;
+    const bool rd = !ep.resid_store;
     float* out = ep.resid + (int64_t)(ok ? row : 0) * ep.ld_resid + n0;
     #pragma unroll 1
     for (int c = 0; c < BN / 32; c += 2) {
@@ -173,8 +176,8 @@ __device__ __forceinline__ void epi_resid(const GemmShape& sh, const GemmEpi& ep
         float4 r[16];
         #pragma unroll
         for (int q = 0; q < 8; ++q) {
-            r[q] = in0 ? p[q] : make_float4(0.f, 0.f, 0.f, 0.f);
-            r[8 + q] = in1 ? p[8 + q] : make_float4(0.f, 0.f, 0.f, 0.f);
+            r[q] = (in0 && rd) ? p[q] : make_float4(0.f, 0.f, 0.f, 0.f);
+            r[8 + q] = (in1 && rd) ? p[8 + q] : make_float4(0.f, 0.f, 0.f, 0.f);
         }
         float v[32], w[32];
         tmem_ld32(tbase + c * 32, v);
@@ -348,7 +351,11 @@ gemm_tc_kernel(const __grid_constant__ GemmProb p0, const __grid_constant__ Gemm
                 for (int kb = 0; kb < sh.num_kb; ++kb) {
                     if (*abort_flag || !mbar_wait(&empty[stage], phase ^ 1, err)) { aborted = true; break; }
                     mbar_arrive_expect_tx(&full[stage], Cfg::A_BYTES + Cfg::B_BYTES);
-                    tma_load_2d(sA + stage * Cfg::A_BYTES, &P->a, kb * GEMM_BK, m0, &full[stage]);
+                    if (sh.a_kb_per_slab)   // A = the slabs side by side along K
+                        tma_load_3d(sA + stage * Cfg::A_BYTES, &P->a, (kb % sh.a_kb_per_slab) * GEMM_BK, m0,
+                                    kb / sh.a_kb_per_slab, &full[stage]);
+                    else
+                        tma_load_2d(sA + stage * Cfg::A_BYTES, &P->a, kb * GEMM_BK, m0, &full[stage]);
                     if (sh.split_b) {   // [gate half (map 0) ; up half (map 1)] of the same features
                         const int fr = tn * (BN / 2);
                         if (CM == 1) {

@@ -15,9 +15,14 @@
 namespace dfl {
 
 // Per-device context: error-word address, SM count, cached attributes.
+// Everything here belongs to one CUDA context of the device (its id in
+// ctx_id); when another context becomes current on the device (after
+// cudaDeviceReset, or a context of the caller's own), the entry is set up
+// again for it before any use.
 struct DeviceCtx {
     int device = -1;
     int sm_count = 0;
+    std::atomic<uint64_t> ctx_id{0};   // unique id of the CUDA context this entry was set up in
     int* err_word = nullptr;       // device address of this device's error word
     // max-dynamic-smem attribute set (atomic: calls may come from several
     // host threads; setting it twice is harmless)
@@ -88,6 +93,11 @@ struct GemmArgs {
     GemmEpi ep;
     const char* tag;        // name in kernel traces
     int split_b;            // EPI_SWIGLU: B tile halves from maps 0 (gate) and 1 (up); N = 2F
+    // a_slabs > 0: A is a_slabs slabs of [M][K / a_slabs], slab i at element
+    // i * a_slab_stride, read as one [M][K] operand (slab i supplies columns
+    // i * K / a_slabs ...); K / a_slabs a multiple of 64
+    int a_slabs;
+    int64_t a_slab_stride;
 };
 
 dfl_status gemm_tc(DeviceCtx* ctx, const GemmArgs& g, cudaStream_t st);
@@ -104,5 +114,8 @@ EncodeTiledFn encode_fn();
 // fp32 CUDA-core GEMM: C = A[M][K] * B[N][K]^T; mode 0 store (ldc), 1 accumulate.
 dfl_status gemm_f32(const float* A, const float* B, float* C, int M, int N, int K, int ldc, int accumulate,
                     cudaStream_t st);
+// Same with row strides lda (A) and ldb (B) in elements.
+dfl_status gemm_f32_ld(const float* A, int64_t lda, const float* B, int64_t ldb, float* C, int M, int N, int K,
+                       int ldc, int accumulate, cudaStream_t st);
 
 }  // namespace dfl

@@ -273,22 +273,29 @@ constexpr size_t kNoAllocSlot = kNoAllocRows * 4;   // one fp32/int32 per row, p
 static __device__ __align__(256) uint8_t g_select_scratch[3 * kNoAllocSlot];
 
 std::mutex g_noalloc_mu;
-void* g_noalloc_ptr[64] = {};
+struct NoAllocAddr {
+    uint64_t ctx_id;   // the CUDA context the address belongs to
+    void* ptr;
+};
+NoAllocAddr g_noalloc[64] = {};
 
 // Device address of the array on the current device.  Host code cannot use
 // the symbol itself (it names a host-side stand-in), so the address is looked
-// up once per device with that device current, then cached.
-dfl_status noalloc_scratch(void** out) {
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess) return DFL_ERR_CUDA;
+// up with that device current, once per device and CUDA context, then
+// cached.  A new context on the device (after cudaDeviceReset, for one) loads
+// the library's device image again, possibly elsewhere, so the cached address
+// is only used while the context it was looked up in is current.
+dfl_status noalloc_scratch(const DeviceCtx* ctx, void** out) {
+    const int dev = ctx->device;
     if (dev < 0 || dev >= 64) return DFL_ERR_NO_DEVICE;
+    const uint64_t cid = ctx->ctx_id.load();
     std::lock_guard<std::mutex> lk(g_noalloc_mu);
-    if (!g_noalloc_ptr[dev]) {
+    if (!g_noalloc[dev].ptr || g_noalloc[dev].ctx_id != cid) {
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_select_scratch) != cudaSuccess || !p) return DFL_ERR_CUDA;
-        g_noalloc_ptr[dev] = p;
+        g_noalloc[dev] = NoAllocAddr{cid, p};
     }
-    *out = g_noalloc_ptr[dev];
+    *out = g_noalloc[dev].ptr;
     return DFL_OK;
 }
 
@@ -306,9 +313,10 @@ extern "C" dfl_status dfl_self_select_noalloc(const void* vlog, dfl_dtype dt, co
     if (!vlog || !drafts || !scores || !selected || !accept_len || !bonus) return DFL_ERR_INVALID_ARG;
     if (!aligned16(vlog)) return DFL_ERR_MISALIGNED;
     if ((size_t)N * K * (G + 1) > kNoAllocRows) return DFL_ERR_WORKSPACE;   // beyond the fixed array
-    if (!current_ctx()) return DFL_ERR_NO_DEVICE;
+    const DeviceCtx* ctx = current_ctx();
+    if (!ctx) return DFL_ERR_NO_DEVICE;
     void* scratch = nullptr;
-    const dfl_status rc = noalloc_scratch(&scratch);
+    const dfl_status rc = noalloc_scratch(ctx, &scratch);
     if (rc != DFL_OK) return rc;
     return self_select_run(vlog, dt == DFL_BF16, drafts, N, K, G, V, scores, selected, accept_len, bonus, scratch,
                            static_cast<cudaStream_t>(stream));

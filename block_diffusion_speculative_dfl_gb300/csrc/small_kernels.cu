@@ -2,6 +2,7 @@
 // acceptance, argmax combine, K-draft sampling, and the fp32 CUDA-core path
 // (GEMM, in-place rotary, attention, per-tile partials).
 #include "internal.h"
+#include "philox.cuh"
 #include "small_kernels.h"
 
 namespace dfl {
@@ -204,25 +205,6 @@ dfl_status argmax_combine(const float* pmax, const int* pidx, int64_t M, int til
     return last_launch();
 }
 
-// ---------------------------------------------------------------- Philox
-
-// Philox4x32-10 (Salmon, Moraes, Dror & Shaw, SC'11): ten rounds of two
-// 32x32->64 products with the round multipliers, key bumped by the Weyl
-// constants between rounds.  Returns output word 0.
-__device__ __forceinline__ uint32_t philox_word0(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3, uint32_t k0,
-                                                 uint32_t k1) {
-    #pragma unroll
-    for (int r = 0; r < 10; ++r) {
-        const uint32_t lo0 = 0xD2511F53u * c0, hi0 = __umulhi(0xD2511F53u, c0);
-        const uint32_t lo1 = 0xCD9E8D57u * c2, hi1 = __umulhi(0xCD9E8D57u, c2);
-        const uint32_t n0 = hi1 ^ c1 ^ k0, n2 = hi0 ^ c3 ^ k1;
-        c0 = n0; c1 = lo1; c2 = n2; c3 = lo0;
-        k0 += 0x9E3779B9u;
-        k1 += 0xBB67AE85u;
-    }
-    return c0;
-}
-
 // ------------------------------------------------------------- sampling
 
 // SpecDiff-2 notes, "Parallel drafting with diffusion LMs" / "Self-Selection
@@ -268,8 +250,7 @@ __global__ void sample_kernel(const float* logits, int64_t ld, const float* pmax
     const double S = P[tiles];
     const int n_seq = (int)(m / per), j = (int)(m % per);
     for (int k = lane; k < K; k += 32) {
-        const uint32_t x0 = philox_word0((uint32_t)n_seq, (uint32_t)j, (uint32_t)k, 0u, key0, key1);
-        const double u = ((double)(x0 >> 8) + 0.5) * (1.0 / 16777216.0);
+        const double u = philox_uniform24((uint32_t)n_seq, (uint32_t)j, (uint32_t)k, 0u, key0, key1);
         const double target = u * S;
         // first tile whose inclusive prefix exceeds the target
         int lo = 0, hi = tiles - 1;
@@ -346,7 +327,8 @@ dfl_status tile_partials(const float* logits, int64_t ld, int64_t M, int V, int 
 // ------------------------------------------------------------ fp32 GEMM
 
 // C[M][N] (=|+=) A[M][K] * B[N][K]^T on CUDA cores, 64x64 tiles.
-__global__ void gemm_f32_kernel(const float* A, const float* B, float* C, int M, int N, int K, int ldc, int acc) {
+__global__ void gemm_f32_kernel(const float* A, int64_t lda, const float* B, int64_t ldb, float* C, int M, int N,
+                                int K, int ldc, int acc) {
     __shared__ float As[16][64 + 1];
     __shared__ float Bs[16][64 + 1];
     const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
@@ -355,8 +337,8 @@ __global__ void gemm_f32_kernel(const float* A, const float* B, float* C, int M,
     for (int k0 = 0; k0 < K; k0 += 16) {
         for (int i = threadIdx.x; i < 64 * 16; i += 256) {
             const int row = i / 16, kk = i % 16;
-            As[kk][row] = (m0 + row < M && k0 + kk < K) ? A[(int64_t)(m0 + row) * K + k0 + kk] : 0.f;
-            Bs[kk][row] = (n0 + row < N && k0 + kk < K) ? B[(int64_t)(n0 + row) * K + k0 + kk] : 0.f;
+            As[kk][row] = (m0 + row < M && k0 + kk < K) ? A[(int64_t)(m0 + row) * lda + k0 + kk] : 0.f;
+            Bs[kk][row] = (n0 + row < N && k0 + kk < K) ? B[(int64_t)(n0 + row) * ldb + k0 + kk] : 0.f;
         }
         __syncthreads();
         #pragma unroll
@@ -385,12 +367,17 @@ __global__ void gemm_f32_kernel(const float* A, const float* B, float* C, int M,
     }
 }
 
-dfl_status gemm_f32(const float* A, const float* B, float* C, int M, int N, int K, int ldc, int accumulate,
-                    cudaStream_t st) {
+dfl_status gemm_f32_ld(const float* A, int64_t lda, const float* B, int64_t ldb, float* C, int M, int N, int K,
+                       int ldc, int accumulate, cudaStream_t st) {
     dim3 grid((N + 63) / 64, (M + 63) / 64);
     ProfScope ps("gemm_f32", st);
-    gemm_f32_kernel<<<grid, 256, 0, st>>>(A, B, C, M, N, K, ldc, accumulate);
+    gemm_f32_kernel<<<grid, 256, 0, st>>>(A, lda, B, ldb, C, M, N, K, ldc, accumulate);
     return last_launch();
+}
+
+dfl_status gemm_f32(const float* A, const float* B, float* C, int M, int N, int K, int ldc, int accumulate,
+                    cudaStream_t st) {
+    return gemm_f32_ld(A, K, B, K, C, M, N, K, ldc, accumulate, st);
 }
 
 // In-place rotate-half rotary on x[rows][heads][hd] (fp32); row r at position
@@ -491,6 +478,25 @@ __global__ void selftest_wait_kernel(int* status, uint64_t limit_ns) {
 dfl_status selftest_wait(int* status, uint64_t limit_ns, cudaStream_t st) {
     ProfScope ps("selftest_wait", st);
     selftest_wait_kernel<<<1, 32, 0, st>>>(status, limit_ns);
+    return last_launch();
+}
+
+// ----------------------------------------------------- Philox known answers
+
+// out[i] = Philox4x32-10(counter in[i][0..3], key in[i][4..5]): the device
+// generator's four output words, for checks against published vectors.
+__global__ void philox_block_kernel(const uint32_t* in, int n, uint32_t* out) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    const uint32_t* c = in + (int64_t)i * 6;
+    const uint4 x = philox4x32_10(c[0], c[1], c[2], c[3], c[4], c[5]);
+    uint32_t* o = out + (int64_t)i * 4;
+    o[0] = x.x; o[1] = x.y; o[2] = x.z; o[3] = x.w;
+}
+
+dfl_status philox_block(const uint32_t* in, int n, uint32_t* out, cudaStream_t st) {
+    ProfScope ps("philox_block", st);
+    philox_block_kernel<<<(n + 127) / 128, 128, 0, st>>>(in, n, out);
     return last_launch();
 }
 

@@ -67,6 +67,15 @@ dfl_status spec_run(const float* logits, float inv_T, const void* vlog, bool bf,
                     int32_t* next_token, const float* lse_z, const float* lse_v, bool lse_all, void* scratch,
                     cudaStream_t st);
 
+// sampled-greedy acceptance: scratch of sg_run, workspace of the entry point
+size_t sg_scratch_bytes(int N, int G, int V);
+size_t sg_ws_bytes(int N, int G, int V);
+dfl_status sg_run(const void* vlog, bool bf, const int32_t* drafts, const int32_t* sel, int N, int K, int G, int V,
+                  uint64_t seed, int32_t* accept_len, int32_t* next_token, const float* lse_v, bool lse_all,
+                  void* scratch, cudaStream_t st);
+// Philox4x32-10 of n (counter, key) sextuples (device [n][6] -> [n][4])
+dfl_status philox_block(const uint32_t* in, int n, uint32_t* out, cudaStream_t st);
+
 // self-selection
 size_t select_ws_bytes(int N, int K, int G);
 dfl_status self_select_run(const void* vlog, bool bf16, const int32_t* drafts, int N, int K, int G, int V,

@@ -38,6 +38,7 @@ class DraftShape:
     eps: float = 1e-6
     rope_theta: float = 1e6
     F: int = 0
+    fc: int = 0      # 1: DFlash fusion (one FC over the L target layers) instead of per-layer mixtures
 
     @property
     def torch_dtype(self):
@@ -52,7 +53,7 @@ class DraftModel:
     """Drafter parameters, workspace and outputs for one shape on one device."""
 
     def __init__(self, shape: DraftShape, mix_logits, mix_gain, blk_gain, final_gain, layers, W_lm=None,
-                 device="cuda", tv=False, accept_rule=0, accept_seed=0, ffn_gain=None):
+                 device="cuda", tv=False, accept_rule=0, accept_seed=0, ffn_gain=None, W_fc=None, fc_gain=None):
         s = self.shape = shape
         dev = torch.device(device)
         wd = shape.torch_dtype
@@ -60,8 +61,12 @@ class DraftModel:
         def dev_t(x, dtype):
             return torch.as_tensor(x).to(device=dev, dtype=dtype).contiguous()
 
-        self.mix_logits = dev_t(mix_logits, torch.float32)
-        self.mix_gain = dev_t(mix_gain, torch.float32)
+        self.mix_logits = dev_t(mix_logits, torch.float32) if mix_logits is not None else None
+        self.mix_gain = dev_t(mix_gain, torch.float32) if mix_gain is not None else None
+        if s.fc and (W_fc is None or fc_gain is None):
+            raise ValueError("a fused drafter (shape.fc) needs W_fc and fc_gain")
+        self.W_fc = dev_t(W_fc, wd) if s.fc else None
+        self.fc_gain = dev_t(fc_gain, torch.float32) if s.fc else None
         self.blk_gain = dev_t(blk_gain, torch.float32)
         self.final_gain = dev_t(final_gain, torch.float32)
         self.layers = [{k: dev_t(v, wd) for k, v in w.items()} for w in layers]
@@ -91,7 +96,7 @@ class DraftModel:
     def _workspace_bytes(self) -> int:
         s = self.shape
         return _lib.workspace_size(_lib.DFL_OP_DRAFT_STEP, N=s.N, C=s.C, B=s.B, d=s.d, Hq=s.Hq, Hkv=s.Hkv, hd=s.hd,
-                                   D=s.D, L=s.L, V=s.V, K=s.K, G=s.B - 1, row0=1, dtype=s.dt, F=s.F)
+                                   D=s.D, L=s.L, V=s.V, K=s.K, G=s.B - 1, row0=1, dtype=s.dt, F=s.F, fc=s.fc)
 
     def want_logits(self, on: bool = True):
         """Keep the fp32 logits [N*(B-1)][V] of each step (needed to check argmax bit-exactly)."""
@@ -116,6 +121,7 @@ class DraftModel:
         a.target = _lib.ptr(target)
         a.accept_len, a.bonus = _lib.ptr(self.accept_len), _lib.ptr(self.bonus)
         a.F, a.ffn_gain = s.F, _lib.ptr(self.ffn_gain)
+        a.W_fc, a.fc_gain = _lib.ptr(self.W_fc), _lib.ptr(self.fc_gain)
         if self._sp is not None:
             a.sample = C.pointer(self._sp)
             a.samples = _lib.ptr(self.samples)
@@ -134,7 +140,8 @@ class DraftModel:
         """``dfl_draft_step_host``: H from (pinned) host memory through ``H_dev``."""
         s = self.shape
         need = _lib.workspace_size(_lib.DFL_OP_DRAFT_STEP_HOST, N=s.N, C=s.C, B=s.B, d=s.d, Hq=s.Hq, Hkv=s.Hkv,
-                                   hd=s.hd, D=s.D, L=s.L, V=s.V, K=s.K, G=s.B - 1, row0=1, dtype=s.dt, F=s.F)
+                                   hd=s.hd, D=s.D, L=s.L, V=s.V, K=s.K, G=s.B - 1, row0=1, dtype=s.dt, F=s.F,
+                                   fc=s.fc)
         if need > self.ws_bytes:   # the context K/V of every layer is kept: a larger workspace
             self.ws = torch.empty(need, dtype=torch.uint8, device=self.Xb.device)
             self.ws_bytes = need
@@ -205,7 +212,7 @@ class CachedDraftModel(DraftModel):
         s = self.shape
         return _lib.workspace_size(_lib.DFL_OP_DRAFT_STEP_CACHED, N=s.N, C=s.C, B=s.B, d=s.d, Hq=s.Hq, Hkv=s.Hkv,
                                    hd=s.hd, D=s.D, L=s.L, V=s.V, K=s.K, G=s.B - 1, row0=1, dtype=s.dt, F=s.F,
-                                   R=self.R_max)
+                                   R=self.R_max, fc=s.fc)
 
     def _h_rows(self) -> int:
         return self.R

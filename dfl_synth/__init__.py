@@ -29,7 +29,7 @@ __all__ = [
     "gen_hidden", "gen_hidden_scales", "gen_mix_logits", "gen_gains",
     "gen_layer_weights", "gen_lm_head", "gen_block_init", "gen_verifier_logits",
     "plant_targets", "geometric_prefix", "WEIGHT_NAMES", "FFN_WEIGHT_NAMES", "gen_ffn_gains",
-    "gen_hidden_rows", "gen_cache_state",
+    "gen_hidden_rows", "gen_cache_state", "gen_fc_weights",
 ]
 
 
@@ -60,6 +60,8 @@ class Workload:
     F: int = 0                 # feed-forward width of full draft layers (0: no FFN)
     R: int = 0                 # cached-context workloads: new context rows per step
                                # (C is then the cache capacity per sequence)
+    fc: int = 0                # 1: context features from one FC over the L target layers
+                               # (DFlash fusion) instead of per-layer mixtures
 
     @property
     def gamma(self) -> int:
@@ -102,6 +104,12 @@ WORKLOADS = {
     "qwen3_8b_drafter_cached": Workload("qwen3_8b_drafter_cached", N=32, d=4096, Hq=32, Hkv=8, hd=128, D=7,
                                         L=9, B=16, C=4096, V=151936, dtype="bf16", seed=1007, geom_p=0.15,
                                         R=16),
+    # A next-row workload: the Qwen3-8B drafter in DFlash's form, where one
+    # fully connected layer fuses the 9 target layers into a representation
+    # shared by all 7 draft layers (in place of DFlare's per-layer mixtures).
+    "qwen3_8b_drafter_dflash": Workload("qwen3_8b_drafter_dflash", N=32, d=4096, Hq=32, Hkv=8, hd=128, D=7,
+                                        L=9, B=16, C=2048, V=151936, dtype="bf16", seed=1008, geom_p=0.15,
+                                        fc=1),
 }
 
 # Tensor ids keying the PCG64 streams.
@@ -109,6 +117,7 @@ _TID_H, _TID_HSCALE, _TID_MIX, _TID_W, _TID_LM = 1, 2, 3, 4, 5
 _TID_ANCHOR, _TID_MASK, _TID_VLOG, _TID_PLANT, _TID_GAIN = 6, 7, 8, 9, 10
 _TID_FFN_GAIN = 11
 _TID_HROWS, _TID_CACHE = 12, 13
+_TID_FC, _TID_FC_GAIN = 14, 15
 _HCHUNK = 256   # positions per stream of gen_hidden_rows
 WEIGHT_NAMES = ("Wq", "Wkc", "Wvc", "Wkb", "Wvb", "Wo")
 FFN_WEIGHT_NAMES = ("W1", "W3", "W2")
@@ -275,6 +284,24 @@ def gen_layer_weights(w: Workload, layer: int) -> dict:
                                1.0 / np.sqrt(in_f)), w.dtype)
 
     return dict(zip(names, _parallel(one, list(range(len(names))))))
+
+
+def gen_fc_weights(w: Workload, random_gain: bool = False):
+    """DFlash fusion: W_fc [d][L*d] ~ N(0, std 1/sqrt(L*d)) in the working
+    dtype (drawn in row chunks), and its RMSNorm gain [d] (ones, or
+    U(0.5, 1.5) for tests)."""
+    chunk = 512
+    out = np.empty((w.d, w.L * w.d), np.float32)
+
+    def one(c):
+        r0, r1 = c * chunk, min(w.d, (c + 1) * chunk)
+        out[r0:r1] = _finish(_normal((w.seed, _TID_FC, c), (r1 - r0, w.L * w.d), 1.0 / np.sqrt(w.L * w.d)),
+                             w.dtype)
+
+    _parallel(one, list(range((w.d + chunk - 1) // chunk)))
+    g = (_rng(w.seed, _TID_FC_GAIN).uniform(0.5, 1.5, w.d).astype(np.float32) if random_gain
+         else np.ones((w.d,), np.float32))
+    return out, g
 
 
 def gen_lm_head(w: Workload, as_bits: bool = False) -> np.ndarray:

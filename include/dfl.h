@@ -80,6 +80,8 @@ typedef struct dfl_shape {
     int32_t F;        /* FFN width (DFL_OP_BLOCK_FFN, DFL_OP_DRAFT_STEP) */
     int32_t R;        /* new context rows per sequence (DFL_OP_DRAFT_STEP_CACHED,
                          where C is the cache capacity) */
+    int32_t fc;       /* 1: the step's context features come from the DFlash
+                         fusion (dfl_fc_fuse) instead of per-layer mixtures */
 } dfl_shape;
 
 typedef enum dfl_op {
@@ -92,7 +94,9 @@ typedef enum dfl_op {
     DFL_OP_SPEC_ACCEPT = 7,
     DFL_OP_BLOCK_FFN = 8,
     DFL_OP_DRAFT_STEP_CACHED = 9,
-    DFL_OP_DRAFT_STEP_HOST = 10
+    DFL_OP_DRAFT_STEP_HOST = 10,
+    DFL_OP_FC_FUSE = 11,           /* rows = N*C, d */
+    DFL_OP_SAMPLED_GREEDY = 12     /* N, G, V */
 } dfl_op;
 
 /* Library version string (static storage). */
@@ -138,6 +142,34 @@ dfl_status dfl_layer_mix_rmsnorm(const void* H, int64_t layer_stride, int32_t L,
                                  int64_t rows, int32_t d, dfl_dtype dt, int32_t D,
                                  const float* mix_logits, const float* gain, float eps,
                                  void* Xc, int64_t xc_layer_stride, dfl_stream stream);
+
+/*
+ * dfl_fc_fuse -- DFlash's shared context representation: one fully connected
+ *   layer over the concatenated hidden states of L target layers.
+ *   DFlash article, "Writing a whole block in one forward pass": features
+ *   taken from several target layers are fused by a light projection and
+ *   injected into the K/V of every draft layer; the DFlare post ("Per-draft-
+ *   layer mixing of different information") names this fully connected
+ *   fusion as the baseline its per-layer mixtures replace.  Reading: no bias,
+ *   and an RMSNorm with its own gain follows (as after DFlare's mixture):
+ *     Xc = RMSNorm([H_1 | H_2 | ... | H_L] W_fc^T; gain)
+ *   One representation serves all draft layers (dfl_step_args.W_fc).
+ *   H           in, dt [L] slabs of [rows][d]; slab i starts at element
+ *               i * layer_stride (>= rows*d when L > 1)
+ *   W_fc        in, dt [d][L*d]: column block i multiplies slab i
+ *   gain        in, device fp32 [d]
+ *   Xc          out, dt [rows][d]
+ *   ws          dfl_workspace_size(DFL_OP_FC_FUSE) bytes (fp32 [rows][d]
+ *               pre-norm features; shape fields N*C = rows, d)
+ *   bf16: one tcgen05 GEMM with K = L*d whose A tiles are read slab by slab
+ *   (d a multiple of 64); fp32: CUDA-core GEMMs.  d <= 6144.
+ *   Errors: INVALID_ARG (null pointer, L outside 1..64, rows or d <= 0, slab
+ *   stride too small), MISALIGNED (pointers, d % 8, slab stride bytes % 16),
+ *   UNSUPPORTED_SHAPE (bf16 d % 64, d > 6144), WORKSPACE.
+ */
+dfl_status dfl_fc_fuse(const void* H, int64_t layer_stride, int32_t L, int64_t rows, int32_t d,
+                       dfl_dtype dt, const void* W_fc, const float* gain, float eps, void* Xc,
+                       void* ws, size_t ws_bytes, dfl_stream stream);
 
 /*
  * dfl_dual_kv_proj -- dual-source projections of one draft layer.
@@ -264,7 +296,9 @@ dfl_status dfl_self_select(const void* vlog, dfl_dtype dt, const int32_t* drafts
  *   with nothing launched.  The library allocates nothing for this call.
  *   The first call on each device looks up the array's device address
  *   (cudaGetSymbolAddress) and caches it; make that first call before any
- *   stream capture on that device.  All calls on a device share the array
+ *   stream capture on that device.  The address belongs to the device's
+ *   current CUDA context: when another context becomes current there (after
+ *   cudaDeviceReset, for example) the next call looks it up again.  All calls on a device share the array
  *   and it keeps the last call's contents (no call relies on them); calls
  *   whose kernels overlap on the GPU race on it and must be serialised.
  *   Errors: as dfl_self_select, plus DFL_ERR_WORKSPACE for the size limit.
@@ -306,7 +340,9 @@ dfl_status dfl_tv_acceptance(const float* logits, float T, const void* vlog, dfl
  *   the draw, key (seed lo, seed hi).
  *   logits  in, fp32 [N*G][V]; vlog in, dt [N][K][G+1][V]
  *   drafts  in, int32 [N][K][G]; sel in, int32 [N] draft to verify (nullable:
- *           draft 0); a token outside [0, V) is rejected
+ *           draft 0; an index outside 0..K-1 is read as draft 0 and records
+ *           DFL_ERR_INVALID_ARG in the device error word); a token outside
+ *           [0, V) is rejected
  *   accept_len out, int32 [N] (accepted drafts, 0..G); next_token out, int32 [N]
  *   ws      dfl_workspace_size(DFL_OP_SPEC_ACCEPT) bytes (N, G and V of the shape)
  *   Errors: INVALID_ARG, MISALIGNED (logits, vlog or ws), WORKSPACE.
@@ -315,6 +351,41 @@ dfl_status dfl_spec_accept(const float* logits, float T, const void* vlog, dfl_d
                            const int32_t* drafts, const int32_t* sel, int32_t N, int32_t K,
                            int32_t G, int32_t V, uint64_t seed, int32_t* accept_len,
                            int32_t* next_token, void* ws, size_t ws_bytes, dfl_stream stream);
+
+/*
+ * dfl_sampled_greedy_accept -- greedy acceptance against the verifier's own
+ *   samples (SpecDiff-2 notes, "Self-Selection Acceptance" and "Streak-
+ *   Distillation", read at temperature above zero).  For j = 1..G the
+ *   verifier draws y_j from P_j = softmax(v_j) by inverse CDF; x_j is accepted
+ *   while x_j == y_j.  The committed token is the verifier's sample at the
+ *   first mismatch, or y_{G+1} (row G) after G acceptances.  Draft
+ *   probabilities are not used; the expected number accepted is the streak
+ *   sum of P_j(x_j), the quantity self-selection maximises.  Uniforms: u =
+ *   ((x0 >> 8) + 1/2) 2^-24 of Philox4x32-10 at counter (n, j, 0, 3), key
+ *   (seed lo, seed hi).
+ *   vlog    in, dt [N][K][G+1][V]; drafts in, int32 [N][K][G]
+ *   sel     in, int32 [N] draft to verify (nullable: draft 0; an index
+ *           outside 0..K-1 is read as draft 0 and records DFL_ERR_INVALID_ARG
+ *           in the device error word)
+ *   accept_len out, int32 [N] (0..G); next_token out, int32 [N]
+ *   ws      dfl_workspace_size(DFL_OP_SAMPLED_GREEDY) bytes (N, G, V)
+ *   Errors: INVALID_ARG (K outside 1..64, G outside 1..1024), MISALIGNED
+ *   (vlog or ws), WORKSPACE, UNSUPPORTED_SHAPE (V above 536,862,720).
+ */
+dfl_status dfl_sampled_greedy_accept(const void* vlog, dfl_dtype dt, const int32_t* drafts,
+                                     const int32_t* sel, int32_t N, int32_t K, int32_t G,
+                                     int32_t V, uint64_t seed, int32_t* accept_len,
+                                     int32_t* next_token, void* ws, size_t ws_bytes,
+                                     dfl_stream stream);
+
+/*
+ * dfl_philox4x32_10 -- the library's device Philox4x32-10 (Salmon, Moraes,
+ *   Dror & Shaw, SC'11), the generator behind every uniform the sampling and
+ *   acceptance calls draw, for checks against the published known-answer
+ *   vectors.  in: device uint32 [n][6] = counter words 0..3, key words 0..1;
+ *   out: device uint32 [n][4] output words.  Errors: INVALID_ARG.
+ */
+dfl_status dfl_philox4x32_10(const uint32_t* in, int32_t n, uint32_t* out, dfl_stream stream);
 
 /*
  * dfl_block_ffn -- residual SwiGLU feed-forward block of a full draft layer.
@@ -377,12 +448,19 @@ typedef struct dfl_step_args {
     float* tv_alpha;               /* out, nullable: [N][K][B-1] TV acceptance proxy */
     float* tv_tokens;              /* out, nullable: [N][K] streak sum of tv_alpha */
     int32_t accept_rule;           /* 0: greedy on the selected draft; 1: lossless
-                                      stochastic acceptance (dfl_spec_accept), whose
-                                      accepted length and next token replace
-                                      accept_len / bonus */
-    uint64_t accept_seed;          /* Philox key of the stochastic rule */
+                                      stochastic acceptance (dfl_spec_accept); 2:
+                                      sampled-greedy acceptance
+                                      (dfl_sampled_greedy_accept); the accepted
+                                      length and next token of rules 1 and 2
+                                      replace accept_len / bonus */
+    uint64_t accept_seed;          /* Philox key of rules 1 and 2 */
     int32_t F;                     /* FFN width; 0: layers without a feed-forward block */
     const float* ffn_gain;         /* in [D][d] when F > 0 */
+    const void* W_fc;              /* in, nullable: [d][L*d] DFlash fusion (dfl_fc_fuse);
+                                      when set, one fused representation is every
+                                      layer's context features and mix_logits /
+                                      mix_gain are unused */
+    const float* fc_gain;          /* in [d] when W_fc != NULL */
 } dfl_step_args;
 
 /*

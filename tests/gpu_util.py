@@ -51,27 +51,40 @@ def rng_bf16(rng, shape, scale=1.0):
 
 # Inverse-CDF draws: the GPU sums fp32 expf weights in fp64, so its cumulative
 # weights sit within ~1e-7 (relative to the total) of the fp64 oracle's; a draw
-# whose target lies within SAMPLE_BAND of a CDF boundary may pick the neighbour.
+# whose target lies within SAMPLE_BAND of a CDF boundary may pick the token on
+# the far side of that boundary (the oracle's outcome set).
 SAMPLE_BAND = 3e-7
+
+
+def near_tie_cap(expected):
+    """Most near-tie cases a correct implementation shows, when ``expected``
+    is their expected count (Poisson, over four standard deviations)."""
+    return expected + 4.0 * np.sqrt(expected) + 3.0
 
 
 def check_samples(samples, z_rows, seed, K, T, cells):
     """cells: iterable of (n, j) window rows; z_rows[(n, j)] -> logits row.
 
-    Every draw away from a boundary must equal the oracle's; near a boundary
-    the neighbour is accepted.  Returns (exact, near)."""
+    Every draw must lie in the oracle's set of legitimate outcomes: the exact
+    inverse-CDF draw, plus the neighbour across a boundary closer than
+    SAMPLE_BAND.  Draws with more than one legitimate outcome must be about
+    as rare as the band predicts.  Returns (exact, near)."""
     import oracle as orc
     exact = near = 0
+    expected = 0.0
     for n, j in cells:
         z = z_rows(n, j)
+        q = orc.softmax_t(z, T)
+        # chance that a uniform falls within the band of its interval's edges
+        p_near = float(np.minimum(q, 2 * SAMPLE_BAND).sum())
         for k in range(K):
-            v, margin = orc.sample_inverse_cdf(z, T, orc.draw_uniform(seed, n, j, k))
+            legit = orc.sample_inverse_cdf_outcomes(z, T, orc.draw_uniform(seed, n, j, k), SAMPLE_BAND)
             s = int(samples[n, k, j])
-            if margin >= SAMPLE_BAND:
-                assert s == v, (n, j, k, s, v, margin)
+            assert s in legit, (n, j, k, s, legit)
+            if len(legit) == 1:
                 exact += 1
             else:
-                assert abs(s - v) <= 1, (n, j, k, s, v, margin)
                 near += 1
-    assert exact >= 0.8 * (exact + near), (exact, near)
+            expected += p_near
+    assert near <= near_tie_cap(expected), (near, expected)
     return exact, near

@@ -16,7 +16,7 @@ HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "df
 def _declared():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(dfl_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(dfl_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_header_declares_the_six_path_calls():
@@ -134,8 +134,9 @@ def test_header_is_plain_c_and_links(tmp_path):
 
 _OPS = ["DFL_OP_DUAL_KV_PROJ", "DFL_OP_BLOCK_ATTN", "DFL_OP_LM_HEAD", "DFL_OP_SELF_SELECT", "DFL_OP_DRAFT_STEP",
         "DFL_OP_TV_ACCEPTANCE", "DFL_OP_SPEC_ACCEPT", "DFL_OP_BLOCK_FFN", "DFL_OP_DRAFT_STEP_CACHED",
-        "DFL_OP_DRAFT_STEP_HOST"]
-_SHAPE = dict(N=3, C=96, B=16, d=256, Hq=4, Hkv=2, hd=128, D=2, L=3, V=1500, K=4, G=15, row0=1, dtype=1, F=384, R=8)
+        "DFL_OP_DRAFT_STEP_HOST", "DFL_OP_FC_FUSE", "DFL_OP_SAMPLED_GREEDY"]
+_SHAPE = dict(N=3, C=96, B=16, d=256, Hq=4, Hkv=2, hd=128, D=2, L=3, V=1500, K=4, G=15, row0=1, dtype=1, F=384, R=8,
+              fc=0)
 
 
 @pytest.mark.parametrize("op", _OPS)
@@ -180,6 +181,8 @@ def _entry_points():
     ws_tv = sz(dfl.DFL_OP_TV_ACCEPTANCE, N=2, K=4, G=8, V=1000, dtype=1)
     ws_sp = sz(dfl.DFL_OP_SPEC_ACCEPT, N=2, K=4, G=8, V=1000, dtype=1)
     ws_ffn = sz(dfl.DFL_OP_BLOCK_FFN, N=2, B=16, d=256, F=384, dtype=1)
+    ws_fc = sz(dfl.DFL_OP_FC_FUSE, N=1, C=64, d=256, dtype=1)
+    ws_sg = sz(dfl.DFL_OP_SAMPLED_GREEDY, N=2, G=8, V=1000, dtype=1)
     return [
         ("dfl_rope_table", [F, 80, 128, 1e6, None], [0], []),
         ("dfl_layer_mix_rmsnorm", [F, 64 * 256, 3, 64, 256, 1, 2, F, F, 1e-6, F, 64 * 256, None], [0, 7, 8, 10], [0, 8, 10]),

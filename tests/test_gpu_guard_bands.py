@@ -1,22 +1,21 @@
-"""Guard bands around every output and workspace buffer (GPU, opt-in).
+"""Guard bands around every output and workspace buffer (GPU).
 
 compute-sanitizer is closed on this machine, so out-of-bounds writes are looked
 for this way instead: each buffer a call writes (its outputs and its
 workspace of exactly dfl_workspace_size() bytes) sits between two 4 KiB bands
 of a known byte, and after the call the bands must be unchanged.  Shapes are
-ragged in every tile dimension.  Opt in with DFL_GUARD_BANDS=1.
+ragged in every tile dimension.
 """
-import os
-
 import numpy as np
 import pytest
 import torch
 
 import block_diffusion_speculative_dfl_gb300 as dfl
+from dfl_synth import (Workload, gen_block_init, gen_fc_weights, gen_gains, gen_hidden, gen_layer_weights,
+                       gen_lm_head, gen_mix_logits, gen_verifier_logits)
 from gpu_util import dev, rng_bf16
 
-pytestmark = [pytest.mark.gpu,
-              pytest.mark.skipif(os.environ.get("DFL_GUARD_BANDS") != "1", reason="opt-in: DFL_GUARD_BANDS=1")]
+pytestmark = pytest.mark.gpu
 
 GUARD = 4096
 PATTERN = 0xA5
@@ -156,4 +155,107 @@ def test_block_ffn_writes_only_its_outputs():
                       dev(rng_bf16(rng, (F, d), d ** -0.5), "bf16"), dev(rng_bf16(rng, (F, d), d ** -0.5), "bf16"),
                       dev(rng_bf16(rng, (d, F), F ** -0.5), "bf16"), F, ws.t, wsb)
     Xb.check("Xb")
+    ws.check("workspace")
+
+
+def test_no_alloc_self_select_writes_only_its_outputs():
+    N, K, G, V = 3, 4, 8, 1000
+    rng = np.random.default_rng(6)
+    vlog = dev(rng_bf16(rng, (N, K, G + 1, V), 4.0), "bf16")
+    drafts = dev(rng.integers(0, V, (N, K, G)).astype(np.int32))
+    sc, se = Guarded((N, K), torch.float32), Guarded((N,), torch.int32)
+    al, bo = Guarded((N,), torch.int32), Guarded((N,), torch.int32)
+    dfl.dfl_self_select_noalloc(vlog, dfl.DFL_BF16, drafts, N, K, G, V, sc.t, se.t, al.t, bo.t)
+    for g, name in ((sc, "scores"), (se, "selected"), (al, "accept_len"), (bo, "bonus")):
+        g.check("no-alloc self-select " + name)
+
+
+def test_sampled_greedy_and_philox_write_only_their_outputs():
+    N, K, G, V = 3, 4, 8, 1001
+    rng = np.random.default_rng(7)
+    vlog = dev(rng_bf16(rng, (N, K, G + 1, V), 4.0), "bf16")
+    drafts = dev(rng.integers(0, V, (N, K, G)).astype(np.int32))
+    al, nt = Guarded((N,), torch.int32), Guarded((N,), torch.int32)
+    ws, wsb = _ws(dfl.DFL_OP_SAMPLED_GREEDY, N=N, G=G, V=V)
+    dfl.dfl_sampled_greedy_accept(vlog, dfl.DFL_BF16, drafts, None, N, K, G, V, 5, al.t, nt.t, ws.t, wsb)
+    for g, name in ((al, "accept_len"), (nt, "next token"), (ws, "workspace")):
+        g.check("sampled greedy " + name)
+    out = Guarded((5, 4), torch.int32)
+    dfl.dfl_philox4x32_10(dev(rng.integers(0, 1 << 31, (5, 6)).astype(np.int32)), 5, out.t)
+    out.check("philox")
+
+
+def test_fc_fuse_writes_only_its_outputs():
+    rows, d, L = 300, 256, 3
+    rng = np.random.default_rng(8)
+    Xc = Guarded((rows, d), torch.bfloat16)
+    ws, wsb = _ws(dfl.DFL_OP_FC_FUSE, N=rows, C=1, d=d, dtype=dfl.DFL_BF16)
+    dfl.dfl_fc_fuse(dev(rng_bf16(rng, (L, rows, d)), "bf16"), rows * d, L, rows, d, dfl.DFL_BF16,
+                    dev(rng_bf16(rng, (d, L * d), (L * d) ** -0.5), "bf16"), dev(np.ones(d, np.float32)), 1e-6, Xc.t,
+                    ws.t, wsb)
+    Xc.check("Xc")
+    ws.check("workspace")
+
+
+def _small_model(w, **kw):
+    shape = dfl.DraftShape(N=w.N, d=w.d, Hq=w.Hq, Hkv=w.Hkv, hd=w.hd, D=w.D, L=w.L, B=w.B, C=w.C, V=w.V,
+                           dtype=w.dtype, K=w.K, T=w.T, seed=w.philox_seed, eps=w.eps, rope_theta=w.rope_theta,
+                           fc=w.fc)
+    g_mix, g_blk, g_fin = gen_gains(w)
+    W_fc, g_fc = gen_fc_weights(w) if w.fc else (None, None)
+    W_lm = torch.from_numpy(gen_lm_head(w, as_bits=True).view(np.int16)).view(torch.bfloat16)
+    return dfl.DraftModel(shape, gen_mix_logits(w), g_mix, g_blk, g_fin, [gen_layer_weights(w, l) for l in range(w.D)],
+                          W_lm, W_fc=W_fc, fc_gain=g_fc, **kw)
+
+
+def _guard_outputs(model, names):
+    """Replace the model's output buffers by guarded ones of the same shapes."""
+    gs = {}
+    for k in names:
+        t = getattr(model, k)
+        gs[k] = Guarded(tuple(t.shape), t.dtype)
+        setattr(model, k, gs[k].t)
+    return gs
+
+
+@pytest.mark.parametrize("fc,host_input", [(0, False), (1, False), (0, True)])
+def test_draft_step_writes_only_its_outputs(fc, host_input):
+    w = Workload("gbstep", N=3, d=256, Hq=4, Hkv=2, hd=64, D=2, L=3, B=16, C=90, V=1200, dtype="bf16", seed=91,
+                 fc=fc)
+    model = _small_model(w)
+    model.want_logits(True)
+    gs = _guard_outputs(model, ("Xb", "draft", "logits", "accept_len", "bonus"))
+    op = dfl._lib.DFL_OP_DRAFT_STEP_HOST if host_input else dfl.DFL_OP_DRAFT_STEP
+    ws, wsb = _ws(op, N=w.N, C=w.C, B=w.B, d=w.d, Hq=w.Hq, Hkv=w.Hkv, hd=w.hd, D=w.D, L=w.L, V=w.V, K=0, G=w.B - 1,
+                  row0=1, dtype=dfl.DFL_BF16, fc=fc)
+    model.ws, model.ws_bytes = ws.t, wsb
+    Hbits = torch.from_numpy(gen_hidden(w, as_bits=True).view(np.int16)).view(torch.bfloat16)
+    X0 = torch.from_numpy(gen_block_init(w)).cuda()
+    target = dev(np.random.default_rng(9).integers(0, w.V, (w.N, w.B)).astype(np.int32))
+    if host_input:
+        H_dev = Guarded(tuple(Hbits.shape), torch.bfloat16)
+        model._step_host(Hbits.pin_memory(), H_dev.t, X0, target, None, 2, torch.cuda.current_stream())
+        H_dev.check("H_dev")
+    else:
+        model.step(Hbits.cuda(), X0, target=target)
+    for k, g in gs.items():
+        g.check(k)
+    ws.check("workspace")
+
+
+@pytest.mark.parametrize("rule", [1, 2])
+def test_self_selection_step_writes_only_its_outputs(rule):
+    w = Workload("gbsel", N=3, d=256, Hq=4, Hkv=2, hd=64, D=2, L=3, B=9, C=80, V=1500, dtype="bf16", seed=93,
+                 K=4, T=1.5, philox_seed=0x5EEDD1F5)
+    model = _small_model(w, tv=True, accept_rule=rule, accept_seed=3)
+    gs = _guard_outputs(model, ("Xb", "draft", "accept_len", "bonus", "samples", "scores", "selected", "tv_alpha",
+                                "tv_tokens"))
+    ws, wsb = _ws(dfl.DFL_OP_DRAFT_STEP, N=w.N, C=w.C, B=w.B, d=w.d, Hq=w.Hq, Hkv=w.Hkv, hd=w.hd, D=w.D, L=w.L,
+                  V=w.V, K=w.K, G=w.B - 1, row0=1, dtype=dfl.DFL_BF16)
+    model.ws, model.ws_bytes = ws.t, wsb
+    vlog = torch.from_numpy(gen_verifier_logits(w, as_bits=True).view(np.int16)).cuda().view(torch.bfloat16)
+    H = torch.from_numpy(gen_hidden(w, as_bits=True).view(np.int16)).view(torch.bfloat16).cuda()
+    model.step(H, torch.from_numpy(gen_block_init(w)).cuda(), vlog=vlog)
+    for k, g in gs.items():
+        g.check(k)
     ws.check("workspace")

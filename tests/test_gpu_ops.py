@@ -8,7 +8,8 @@ import torch
 
 import block_diffusion_speculative_dfl_gb300 as dfl
 import oracle as orc
-from gpu_util import assert_bf16_close, assert_f32_close, check_samples, dev, host, rng_bf16
+from gpu_util import (BF16_MEAN_REL, assert_bf16_close, assert_f32_close, check_samples, dev, host,
+                      rel_rms_err, rng_bf16)
 
 pytestmark = pytest.mark.gpu
 
@@ -63,6 +64,45 @@ def test_mix_rmsnorm_f32():
     got = host(Xc)
     for l in range(D):
         assert_f32_close(got[l], orc.mix_rmsnorm(H, mix[l], gain[l], 1e-6), f"Xc[{l}]")
+
+
+# ------------------------------------------------------- DFlash fusion --
+
+@pytest.mark.parametrize("rows,d,L,pad", [
+    (300, 256, 3, 0),      # ragged last M tile
+    (1000, 512, 9, 64),    # nine slabs, slab stride beyond the rows
+    (129, 128, 1, 0),      # one slab: a plain GEMM
+    (2048, 4096, 9, 0),    # the Qwen3-8B shape (K = 36,864), one sequence's context
+    (77, 2880, 7, 0),      # the GPT-OSS shape (d = 45 * 64)
+])
+def test_fc_fuse_bf16(rows, d, L, pad):
+    rng = np.random.default_rng(rows + d + L)
+    stride = rows * d + pad
+    Hs = np.zeros((L, stride), np.float32)
+    H = rng_bf16(rng, (L, rows, d)) * rng.uniform(0.5, 2, (L, 1, 1)).astype(np.float32)
+    from dfl_synth import round_bf16
+    H = round_bf16(H)
+    Hs[:, :rows * d] = H.reshape(L, -1)
+    W = rng_bf16(rng, (d, L * d), (L * d) ** -0.5)
+    g = rng.uniform(0.5, 1.5, d).astype(np.float32)
+    Xc = torch.empty((rows, d), dtype=torch.bfloat16, device="cuda")
+    wsb = dfl.workspace_size(dfl.DFL_OP_FC_FUSE, N=rows, C=1, d=d, dtype=dfl.DFL_BF16)
+    dfl.dfl_fc_fuse(dev(Hs, "bf16"), stride, L, rows, d, dfl.DFL_BF16, dev(W, "bf16"), dev(g), 1e-6, Xc, _ws(wsb),
+                    wsb)
+    ref = orc.fc_fuse(H, W, g, 1e-6)
+    assert_bf16_close(host(Xc), ref, "Xc")
+
+
+def test_fc_fuse_f32():
+    rng = np.random.default_rng(5)
+    rows, d, L = 45, 96, 4
+    H = rng.standard_normal((L, rows, d)).astype(np.float32)
+    W = (rng.standard_normal((d, L * d)) * (L * d) ** -0.5).astype(np.float32)
+    g = rng.uniform(0.5, 1.5, d).astype(np.float32)
+    Xc = torch.empty((rows, d), dtype=torch.float32, device="cuda")
+    wsb = dfl.workspace_size(dfl.DFL_OP_FC_FUSE, N=rows, C=1, d=d, dtype=dfl.DFL_F32)
+    dfl.dfl_fc_fuse(dev(H), rows * d, L, rows, d, dfl.DFL_F32, dev(W), dev(g), 1e-6, Xc, _ws(wsb), wsb)
+    assert_f32_close(host(Xc), orc.fc_fuse(H, W, g, 1e-6), "Xc")
 
 
 # --------------------------------------------------------- dual projection --
@@ -187,6 +227,48 @@ def test_block_attn_bf16(N, C, B, Hq, Hkv, hd, d):
         ref[n * B:(n + 1) * B] = Xb[n * B:(n + 1) * B] + O.reshape(B, Hq * hd) @ Wo.astype(np.float64).T
     got = host(Xb_d)
     assert_bf16_close(got - Xb, ref - Xb, "O Wo^T")
+
+
+@pytest.mark.parametrize("N,C,B,Hq,Hkv,hd", [
+    (32, 2048, 16, 32, 8, 128),   # the Qwen3-8B drafter's attention
+    (16, 1024, 33, 32, 8, 128),   # the self-selection window (two head subsets per K/V head)
+    (32, 3072, 8, 64, 8, 64),     # the GPT-OSS-20B drafter's attention
+    (1, 700, 16, 32, 8, 128),     # key ranges split over items and combined
+    (3, 150, 12, 4, 2, 128),      # M = 64 products with padding rows
+])
+def test_block_attn_output_elementwise(N, C, B, Hq, Hkv, hd):
+    # With Wo = I (d = Hq*hd, exact in bf16) and a zero residual stream the
+    # call's output is the attention output O itself, compared element by
+    # element (a wrong key tile or head is not diluted by a random Wo).
+    d = Hq * hd
+    rng = np.random.default_rng(N * 31 + C)
+    Q = rng_bf16(rng, (N * B, Hq, hd))
+    Kc, Vc = rng_bf16(rng, (N * C, Hkv, hd)), rng_bf16(rng, (N * C, Hkv, hd))
+    Kb, Vb = rng_bf16(rng, (N * B, Hkv, hd)), rng_bf16(rng, (N * B, Hkv, hd))
+    Wo = torch.eye(d, dtype=torch.bfloat16, device="cuda")
+    Xb_d = torch.zeros((N * B, d), dtype=torch.float32, device="cuda")
+    wsb = dfl.workspace_size(dfl.DFL_OP_BLOCK_ATTN, N=N, C=C, B=B, Hq=Hq, Hkv=Hkv, hd=hd, dtype=dfl.DFL_BF16)
+    ws = _ws(wsb)
+    dfl.dfl_block_attn(dev(Q, "bf16"), dev(Kc, "bf16"), dev(Vc, "bf16"), dev(Kb, "bf16"), dev(Vb, "bf16"), N, C, B,
+                       Hq, Hkv, hd, dfl.DFL_BF16, Wo, d, Xb_d, ws, wsb)
+    got = host(Xb_d).reshape(N, B, Hq, hd)
+    for n in range(N):
+        K = np.concatenate([Kc[n * C:(n + 1) * C], Kb[n * B:(n + 1) * B]])
+        V = np.concatenate([Vc[n * C:(n + 1) * C], Vb[n * B:(n + 1) * B]])
+        vis = orc.block_visibility(C, B)
+        O = orc.attention(Q[n * B:(n + 1) * B], K, V, vis)
+        # Element-wise bound from the arithmetic: the probabilities enter the
+        # PV product rounded to bf16 (relative error <= 2^-9 each, so at most
+        # 2^-9 sum_i p_i |V_i| / l, which is attention over |V|) and O is
+        # stored in bf16 (2^-9 |O|), with 10% for the fp32 exponentials and
+        # accumulation.
+        A = orc.attention(Q[n * B:(n + 1) * B], K, np.abs(V), vis)
+        bound = 2.0 ** -9 * (A + 2 * np.abs(O)) * 1.1 + 1e-6
+        err = np.abs(got[n] - O)
+        assert np.all(err <= bound), (n, float((err / bound).max()), np.unravel_index(np.argmax(err / bound), err.shape))
+        for h in range(Hq):   # per head: the typical element as well
+            _, mean = rel_rms_err(got[n, :, h], O[:, h])
+            assert mean <= BF16_MEAN_REL, (n, h, mean)
 
 
 @pytest.mark.parametrize("N,C,B,Hq,Hkv,hd,d", [
