@@ -63,8 +63,14 @@ def parse_args(argv=None):
                    help="override sequences per GPU (a smaller case of the same kernels, e.g. for ncu)")
     p.add_argument("--context", type=int, default=0, help="override the context length (smaller case, e.g. for ncu)")
     p.add_argument("--tv", action="store_true", help="self-selection workloads: add the TV acceptance proxy")
-    p.add_argument("--accept-rule", choices=["greedy", "stochastic"], default="greedy",
-                   help="self-selection workloads: acceptance of the selected draft")
+    p.add_argument("--accept-rule", choices=["greedy", "stochastic", "sampled"], default="greedy",
+                   help="self-selection workloads: acceptance of the selected draft (argmax greedy, lossless "
+                        "stochastic, or greedy against the verifier's samples)")
+    p.add_argument("--kernel", choices=["mix", "attn", "fc_fuse"], default=None,
+                   help="time one operation alone at the workload's shape (one JSON line of kernel timings, "
+                        "not the benchmark line; for profiling)")
+    p.add_argument("--rows", type=int, default=0, help="--kernel mix / fc_fuse: context rows (default N * C)")
+    p.add_argument("--iters", type=int, default=10, help="--kernel: timed launches")
     p.add_argument("--e2e-steps", type=int, default=7)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -175,6 +181,8 @@ def kernel_work(w, ctx_lens=None):
     # the context and block projections of a layer run as one grouped launch
     both = "gemm_kv_qkv_append" if w.R > 0 else "gemm_kv_qkv"
     work[both] = tuple(a + b for a, b in zip(work[ctx], work["gemm_block_qkv"]))
+    if w.fc:   # DFlash fusion: one FC over the concatenated L slabs, fp32 pre-norm features out
+        work["gemm_fc_fuse"] = (2.0 * rows_c * d * L * d, 2.0 * (L * rows_c * d + d * L * d) + 4.0 * rows_c * d)
     if w.F > 0:
         M = rows_b
         work["gemm_ffn_gate_up"] = (2.0 * M * 2 * w.F * d, 2.0 * (M * d + 2 * w.F * d + M * w.F))
@@ -187,6 +195,42 @@ def kernel_work(w, ctx_lens=None):
         work["verifier_row_stats"] = (0.0, 2.0 * N * w.K * B * V)
         work["tv_alpha"] = (0.0, 4.0 * N * G * V + 2.0 * N * w.K * G * V)
     return work
+
+
+def tensor_peak_key(clk):
+    """Which measured bf16 peak a tensor-bound kernel of this run is held to.
+
+    The burst figure is cuBLAS at full clock; the sustained one the same GEMM
+    held at the power cap for seconds.  A timed region that saw the power cap,
+    or whose median SM clock sat below 97% of the maximum, ran at the
+    sustained level; otherwise at burst."""
+    reasons = clk.get("reasons") or []
+    sm, mx = clk.get("sm_mhz"), clk.get("sm_max_mhz")
+    if "sw_power_cap" in reasons:
+        return "bf16_tflops_sustained", "sw_power_cap active during the timed steps"
+    if sm and mx and sm < 0.97 * mx:
+        return "bf16_tflops_sustained", f"median SM clock {sm:.0f} of {mx:.0f} MHz"
+    if not sm:
+        return "bf16_tflops", "no clock samples: burst assumed"
+    return "bf16_tflops", f"no power cap, median SM clock {sm:.0f} of {mx:.0f} MHz"
+
+
+def kernel_table(prof, work, peaks, tkey):
+    """Per traced kernel: launches, time, share and (when its work is known)
+    bound, achieved rate and fraction of the chosen peak."""
+    traced = sum(t for _, t in prof.values()) or 1.0
+    kernels = {}
+    for name, (n_l, tot) in sorted(prof.items(), key=lambda kv: -kv[1][1]):
+        per = tot / n_l
+        ent = {"launches": n_l, "ms_per_launch": round(per, 5), "share": round(tot / traced, 4)}
+        if name in work:
+            fl, by = work[name]
+            tensor = fl / (peaks[tkey] * 1e12) >= by / (peaks["hbm_gbs"] * 1e9)
+            ent["bound"] = "tensor" if tensor else "hbm"
+            ent["achieved"] = round(fl / (per / 1e3) / 1e12, 2) if tensor else round(by / (per / 1e3) / 1e9, 1)
+            ent["frac"] = round(ent["achieved"] / (peaks[tkey] if tensor else peaks["hbm_gbs"]), 4)
+        kernels[name] = ent
+    return kernels
 
 
 class ClockSampler:
@@ -243,11 +287,12 @@ def workload(name, rank=0, batch=0, context=0):
 
 
 def host_params(w):
-    from dfl_synth import gen_ffn_gains, gen_gains, gen_layer_weights, gen_lm_head, gen_mix_logits
+    from dfl_synth import gen_fc_weights, gen_ffn_gains, gen_gains, gen_layer_weights, gen_lm_head, gen_mix_logits
     g_mix, g_blk, g_fin = gen_gains(w)
+    W_fc, g_fc = gen_fc_weights(w) if w.fc else (None, None)
     return {"mix": gen_mix_logits(w), "g_mix": g_mix, "g_blk": g_blk, "g_fin": g_fin, "g_ffn": gen_ffn_gains(w),
             "layers": [gen_layer_weights(w, l) for l in range(w.D)],
-            "W_lm_bits": gen_lm_head(w, as_bits=True) if w.V > 0 else None}
+            "W_lm_bits": gen_lm_head(w, as_bits=True) if w.V > 0 else None, "W_fc": W_fc, "g_fc": g_fc}
 
 
 def oracle_step(w, p, n, W_lm_f32, vlog_n=None):
@@ -259,7 +304,8 @@ def oracle_step(w, p, n, W_lm_f32, vlog_n=None):
     t0 = time.perf_counter()
     layers = [dict(W, g_ffn=p["g_ffn"][l]) if w.F > 0 else W for l, W in enumerate(p["layers"])]
     out = orc.draft_forward(Xb0, Hn, p["mix"], p["g_mix"], p["g_blk"], layers,
-                            {"Hq": w.Hq, "Hkv": w.Hkv, "hd": w.hd}, w.eps, w.rope_theta)
+                            {"Hq": w.Hq, "Hkv": w.Hkv, "hd": w.hd}, w.eps, w.rope_theta,
+                            fused=(p["W_fc"], p["g_fc"]) if w.fc else None)
     if w.V > 0:
         z = orc.lm_head_logits(out["Xb"][1:], p["g_fin"], w.eps, W_lm_f32)
         drafts = orc.argmax_lowest(z)
@@ -358,11 +404,12 @@ def run_ours(args, rank, world, local):
     p = host_params(w)
     shape = dfl.DraftShape(N=w.N, d=w.d, Hq=w.Hq, Hkv=w.Hkv, hd=w.hd, D=w.D, L=w.L, B=w.B, C=w.C, V=w.V,
                            dtype=w.dtype, K=w.K, T=w.T, seed=w.philox_seed, eps=w.eps, rope_theta=w.rope_theta,
-                           F=w.F)
+                           F=w.F, fc=w.fc)
     W_lm = (torch.from_numpy(p["W_lm_bits"].view(np.int16)).view(torch.bfloat16) if w.V > 0 else None)
     cached = w.R > 0
-    kw = dict(tv=args.tv and w.K > 0, accept_rule=1 if (args.accept_rule == "stochastic" and w.K > 0) else 0,
-              accept_seed=w.philox_seed ^ 0xACCE97, ffn_gain=p["g_ffn"])
+    rule = {"greedy": 0, "stochastic": 1, "sampled": 2}[args.accept_rule] if w.K > 0 else 0
+    kw = dict(tv=args.tv and w.K > 0, accept_rule=rule, accept_seed=w.philox_seed ^ 0xACCE97, ffn_gain=p["g_ffn"],
+              W_fc=p["W_fc"], fc_gain=p["g_fc"])
     X_host = torch.from_numpy(gen_block_init(w))
     X0 = X_host.cuda()
     n_host = n_new = None
@@ -434,28 +481,21 @@ def run_ours(args, rank, world, local):
 
     # roofline of the dominant kernel (largest share of traced time)
     peaks, peak_src = load_peaks()
+    tkey, why = tensor_peak_key(clk)
     work = kernel_work(w, ctx_lens)
-    traced = sum(t for _, t in prof.values())
-    kernels = {}
-    for name, (n_l, tot) in sorted(prof.items(), key=lambda kv: -kv[1][1]):
-        per = tot / n_l
-        ent = {"launches": n_l, "ms_per_launch": round(per, 5), "share": round(tot / traced, 4)}
-        if name in work:
-            fl, by = work[name]
-            tensor = fl / (peaks["bf16_tflops_sustained"] * 1e12) >= by / (peaks["hbm_gbs"] * 1e9)
-            ent["bound"] = "tensor" if tensor else "hbm"
-            ent["achieved"] = round(fl / (per / 1e3) / 1e12, 2) if tensor else round(by / (per / 1e3) / 1e9, 1)
-            ent["frac"] = round(ent["achieved"] / (peaks["bf16_tflops_sustained"] if tensor else peaks["hbm_gbs"]),
-                                4)
-        kernels[name] = ent
+    kernels = kernel_table(prof, work, peaks, tkey)
     dom = next(k for k in kernels if k in work)
     de = kernels[dom]
     roofline = {"kernel": dom, "bound": de["bound"], "achieved": de["achieved"],
-                "peak": peaks["bf16_tflops_sustained"] if de["bound"] == "tensor" else peaks["hbm_gbs"],
+                "peak": peaks[tkey] if de["bound"] == "tensor" else peaks["hbm_gbs"],
                 "unit": "TFLOP/s" if de["bound"] == "tensor" else "GB/s", "frac": de["frac"],
                 "traffic": ncu_traffic(dom, w.name),
-                "peak_source": f"{peak_src} ({'bf16 dense sustained' if de['bound'] == 'tensor' else 'HBM copy'})",
+                "peak_source": (f"{peak_src} ({'bf16 dense ' + ('burst' if tkey == 'bf16_tflops' else 'sustained')}"
+                                f": {why})" if de["bound"] == "tensor" else f"{peak_src} (HBM copy)"),
                 "algorithmic_per_launch": work[dom][0] if de["bound"] == "tensor" else work[dom][1]}
+    if de["bound"] == "tensor":   # both fractions, the chosen one in "frac"
+        roofline["frac_burst"] = round(de["achieved"] / peaks["bf16_tflops"], 4)
+        roofline["frac_sustained"] = round(de["achieved"] / peaks["bf16_tflops_sustained"], 4)
 
     # end to end through the public API: pinned host inputs in, results out
     e2e = None
@@ -503,14 +543,83 @@ def run_ours(args, rank, world, local):
                            "draft_layers": w.D, "target_layers": w.L, "block": w.B, "context": w.C, "vocab": w.V,
                            "ffn": w.F, "new_rows_per_step": w.R or None,
                            "K": w.K, "T": w.T, "parallelism": f"replicas x{world}",
+                           "context_features": "DFlash FC fusion" if w.fc else "per-layer mixtures",
                            "epilogue": ("self-selection" + (" + TV proxy" if args.tv else "") +
-                                        (" + stochastic acceptance" if args.accept_rule == "stochastic" else
-                                         " + greedy acceptance")) if w.K > 0 else "greedy acceptance",
+                                        {"greedy": " + greedy acceptance",
+                                         "stochastic": " + stochastic acceptance",
+                                         "sampled": " + sampled-greedy acceptance"}[args.accept_rule])
+                           if w.K > 0 else "greedy acceptance",
                            "l2": "inputs larger than L2; between timed steps a 256 MB buffer is written, then another read, so the dirty lines are written back before the next step"},
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
                 "clocks": clk, "kernels": kernels}
         print(json.dumps(line), flush=True)
     barrier(world)
+
+
+# ------------------------------------------------------- one operation --
+
+def run_kernel(args):
+    """One operation alone at a workload's shape (profiling aid): random bf16
+    inputs on the device, two untimed launches (so that a profiler's
+    ``-s 2 -c 1`` selects a warm one), then ``--iters`` launches each after an
+    L2 flush, timed by the library's own trace.  Prints one JSON line."""
+    import torch
+
+    import block_diffusion_speculative_dfl_gb300 as dfl
+    torch.cuda.set_device(0)
+    dfl.build()
+    dfl.load()
+    w = workload(args.workload, 0, args.batch, args.context)
+    peaks, _ = load_peaks()
+    g = torch.Generator(device="cuda").manual_seed(1)
+    rnd = lambda *sh: torch.randn(*sh, device="cuda", generator=g).to(torch.bfloat16)   # noqa: E731
+    rows = args.rows or w.N * w.C
+    if args.kernel == "mix":
+        H, Xc = rnd(w.L, rows, w.d), torch.empty(w.D, rows, w.d, device="cuda", dtype=torch.bfloat16)
+        mix, gain = torch.randn(w.D, w.L, device="cuda"), torch.ones(w.D, w.d, device="cuda")
+        call = lambda: dfl.dfl_layer_mix_rmsnorm(H, rows * w.d, w.L, rows, w.d, dfl.DFL_BF16, w.D, mix, gain,  # noqa
+                                                 w.eps, Xc, rows * w.d)
+        main, work = "mix_rmsnorm_bf16", (0.0, 2.0 * (w.L + w.D) * rows * w.d)
+    elif args.kernel == "fc_fuse":
+        H, Xc = rnd(w.L, rows, w.d), torch.empty(rows, w.d, device="cuda", dtype=torch.bfloat16)
+        W, gain = (rnd(w.d, w.L * w.d) * (w.L * w.d) ** -0.5).to(torch.bfloat16), torch.ones(w.d, device="cuda")
+        wsb = dfl.workspace_size(dfl.DFL_OP_FC_FUSE, N=rows, C=1, d=w.d, dtype=dfl.DFL_BF16)
+        ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+        call = lambda: dfl.dfl_fc_fuse(H, rows * w.d, w.L, rows, w.d, dfl.DFL_BF16, W, gain, w.eps, Xc, ws,  # noqa
+                                       wsb)
+        main = "gemm_fc_fuse"
+        work = (2.0 * rows * w.d * w.L * w.d, 2.0 * (w.L * rows * w.d + w.d * w.L * w.d) + 4.0 * rows * w.d)
+    else:
+        N, C, B, Hq, Hkv, hd, d = w.N, w.C, w.B, w.Hq, w.Hkv, w.hd, w.d
+        Q, Kc, Vc, Kb, Vb = rnd(N * B, Hq, hd), rnd(N * C, Hkv, hd), rnd(N * C, Hkv, hd), rnd(N * B, Hkv, hd), \
+            rnd(N * B, Hkv, hd)
+        Wo = (rnd(d, Hq * hd) * (Hq * hd) ** -0.5).to(torch.bfloat16)
+        Xb = torch.zeros(N * B, d, device="cuda")
+        wsb = dfl.workspace_size(dfl.DFL_OP_BLOCK_ATTN, N=N, C=C, B=B, Hq=Hq, Hkv=Hkv, hd=hd, dtype=dfl.DFL_BF16)
+        ws = torch.empty(max(wsb, 256), dtype=torch.uint8, device="cuda")
+        call = lambda: dfl.dfl_block_attn(Q, Kc, Vc, Kb, Vb, N, C, B, Hq, Hkv, hd, dfl.DFL_BF16, Wo, d, Xb, ws,  # noqa
+                                          wsb)
+        keys = N * (C + B)
+        main, work = "attn_tc", (4.0 * B * Hq * keys * hd, 2.0 * (2 * keys * Hkv * hd + 2 * N * B * Hq * hd))
+    flush = L2Flush()
+    for _ in range(2):
+        call()
+    torch.cuda.synchronize()
+    dfl.dfl_profile_enable(True)
+    for _ in range(args.iters):
+        flush()
+        call()
+    torch.cuda.synchronize()
+    dfl.dfl_profile_enable(False)
+    prof, _ = dfl.dfl_profile_report()
+    if dfl.dfl_get_device_error():
+        raise RuntimeError("device error during the timed launches")
+    if main not in prof:
+        main = next(iter(sorted(prof, key=lambda k: -prof[k][1])))
+    kernels = kernel_table(prof, {main: work}, peaks, "bf16_tflops")
+    print(json.dumps({"kernel_only": args.kernel, "workload": w.name, "rows": rows if args.kernel != "attn" else None,
+                      "us_per_launch": {k: round(v[1] / v[0] * 1e3, 2) for k, v in prof.items()},
+                      "main": main, "roofline": kernels[main]}), flush=True)
 
 
 # -------------------------------------------------------- reference arm --
@@ -551,6 +660,9 @@ def main(argv=None):
     rank, world, local = dist_env()
     if args.impl == "reference":
         run_reference(args, rank, world)
+        return
+    if args.kernel:
+        run_kernel(args)
         return
     run_ours(args, rank, world, local)
     if world > 1:
