@@ -106,15 +106,37 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
         :: "r"(smem_u32(dst)), "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar)) : "memory");
 }
 
-// Same, delivered to the same shared-memory offset of every CTA in
-// `cta_mask` (this cluster), each CTA's mbarrier at `bar`'s offset receiving
-// the bytes that land in that CTA.
-__device__ __forceinline__ void tma_load_2d_mc(void* dst, const CUtensorMap* map, int32_t x, int32_t y,
-                                               uint64_t* bar, uint16_t cta_mask) {
+// Same, for a CTA pair issuing tcgen05 cta_group::2 products: the copy lands
+// in this CTA's shared memory and its completion is counted on the mbarrier
+// at the shared::cluster address `bar_cluster`, which may be the peer CTA's.
+__device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* map, int32_t x, int32_t y,
+                                                 uint32_t bar_cluster) {
     asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%2, %3}], [%4], %5;"
-        :: "r"(smem_u32(dst)), "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar)), "h"(cta_mask) : "memory");
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];"
+        :: "r"(smem_u32(dst)), "l"(map), "r"(x), "r"(y), "r"(bar_cluster) : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d_pair(void* dst, const CUtensorMap* map, int32_t x, int32_t y,
+                                                 int32_t z, uint32_t bar_cluster) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];"
+        :: "r"(smem_u32(dst)), "l"(map), "r"(x), "r"(y), "r"(z), "r"(bar_cluster) : "memory");
+}
+
+// shared::cluster address of the variable at local shared address `a` in the
+// cluster's CTA `rank`.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t a, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
+    return r;
+}
+
+// One arrival on the mbarrier at a shared::cluster address (possibly another
+// CTA's), releasing this thread's prior memory operations to the cluster.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" :: "r"(bar_cluster) : "memory");
 }
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
@@ -147,6 +169,22 @@ __device__ __forceinline__ void tmem_relinquish() {
 
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(taddr), "r"(ncols) : "memory");
+}
+
+// The same for a CTA pair of tcgen05 cta_group::2 products: one warp of each
+// CTA of the pair executes it; the columns are allocated in both CTAs'
+// tensor memory at the same address.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t* dst, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;"
+                 :: "r"(smem_u32(dst)), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish_pair() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" :: "r"(taddr), "r"(ncols) : "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before() {
@@ -185,11 +223,34 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
                  :: "r"(smem_u32(bar)) : "memory");
 }
 
-// Arrive once on the mbarrier at `bar`'s offset in every CTA of `cta_mask`
-// when all previously issued tcgen05.mma of this thread have completed.
-__device__ __forceinline__ void mma_commit_mc(uint64_t* bar, uint16_t cta_mask) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
-                 :: "r"(smem_u32(bar)), "h"(cta_mask) : "memory");
+// D[tmem] (+)= A * B^T over a CTA pair (tcgen05 cta_group::2, issued by one
+// thread of the even CTA): A is M = 256 rows, the first 128 from this CTA's
+// shared memory at the descriptor's address and the other 128 from the peer's
+// at the same address; B's N rows likewise half from each CTA; each CTA's
+// tensor memory receives its own 128 rows of D.
+__device__ __forceinline__ void mma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                              uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        :: "r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate) : "memory");
+}
+
+// Arrive once on the mbarrier at `bar`'s offset in both CTAs of the pair
+// (cluster ranks 0 and 1; one completion signal delivered to each CTA, no
+// data moved) when all cta_group::2 products this thread issued before have
+// completed.
+__device__ __forceinline__ void mma_commit_pair_both(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
+                 :: "r"(smem_u32(bar)), "h"((uint16_t)3) : "memory");
+}
+
+// Arrive once on the mbarrier at the shared::cluster address `bar_cluster`
+// when all cta_group::2 products this thread issued before have completed.
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar_cluster) {
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                 :: "r"(bar_cluster) : "memory");
 }
 
 // 32 lanes x 32 consecutive 32-bit columns: thread i gets row (lane base + i).

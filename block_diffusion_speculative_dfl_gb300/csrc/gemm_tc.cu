@@ -54,7 +54,7 @@ dfl_status launch(DeviceCtx* ctx, const GemmProb& p0, const GemmProb& p1, int np
                   cudaStream_t st, int slot) {
     auto kern = gemm_tc_kernel<BN, EPI, CM>;
     if (!ctx->gemm_attr_set[slot]) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, GemmCfg<BN>::SMEM) !=
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, GemmCfg<BN, CM>::SMEM) !=
             cudaSuccess)
             return DFL_ERR_CUDA;
         if (CM > 1 && cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 0) != cudaSuccess)
@@ -68,7 +68,7 @@ dfl_status launch(DeviceCtx* ctx, const GemmProb& p0, const GemmProb& p1, int np
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(GEMM_THREADS);
-    cfg.dynamicSmemBytes = GemmCfg<BN>::SMEM;
+    cfg.dynamicSmemBytes = GemmCfg<BN, CM>::SMEM;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -167,8 +167,8 @@ static dfl_status launch_probs(DeviceCtx* ctx, const GemmProb& p0, const GemmPro
 dfl_status gemm_tc(DeviceCtx* ctx, const GemmArgs& g_in, cudaStream_t st) {
     GemmArgs g = g_in;
     if (g.bn == 0) g.bn = pick_bn(g, ctx->sm_count);
-    // Pair the M-tiles of each N-tile in 2-CTA clusters (B tile multicast) when
-    // there is more than one M-tile.
+    // Pair the M-tiles of each N-tile over two SMs (a 256-row tile of
+    // cta_group::2 products) when there is more than one M-tile.
     const int cm = (g.M + GEMM_BM - 1) / GEMM_BM >= 2 ? 2 : 1;
     GemmProb P;
     dfl_status rc = build_prob(g, cm, P);

@@ -2,11 +2,12 @@
 //
 // A and B are bf16, K-major (row-major with K contiguous), loaded by TMA with
 // 128-byte swizzling into a shared-memory ring; one elected thread issues
-// tcgen05.mma (128 x BN x 16) into a double-buffered TMEM accumulator; four
-// epilogue warps read TMEM with tcgen05.ld and apply one of three epilogues:
+// tcgen05.mma (128 x BN x 16 on one SM, or 256 x BN x 16 over an SM pair) into
+// a double-buffered TMEM accumulator; four epilogue warps read TMEM with
+// tcgen05.ld and apply one of four epilogues:
 //   EPI_STORE  bf16 store into up to three column segments, rotary embedding
 //              on segments that ask for it;
-//   EPI_RESID  fp32 residual accumulate (out += C);
+//   EPI_RESID  fp32 residual accumulate (out += C), or plain fp32 store;
 //   EPI_ARGMAX per-row max / argmax over the tile's columns (lowest column on
 //              ties), optional fp32 logits store and optional per-tile
 //              sum of exp((z - tile max) / T) in fp64 for sampling;
@@ -79,14 +80,16 @@ constexpr int GEMM_BM = 128;
 constexpr int GEMM_BK = 64;
 constexpr int GEMM_THREADS = 192;
 
-template <int BN>
+// CM = 2: each CTA of the pair holds half of the B tile (BN / 2 rows) per stage.
+template <int BN, int CM>
 struct GemmCfg {
-    static constexpr int STAGES = (BN == 256) ? 4 : 6;
     static constexpr int A_BYTES = GEMM_BM * GEMM_BK * 2;
-    static constexpr int B_BYTES = BN * GEMM_BK * 2;
+    static constexpr int B_BYTES = BN / CM * GEMM_BK * 2;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int STAGES = (200 * 1024 / STAGE_BYTES) < 8 ? (200 * 1024 / STAGE_BYTES) : 8;
     static constexpr int TMEM_COLS = 2 * BN;
     static constexpr int BAR_BYTES = 256;
-    static constexpr int SMEM = 1024 + STAGES * (A_BYTES + B_BYTES) + BAR_BYTES;
+    static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
 };
 
 // Tile t of a (tiles_mc x tiles_n) grid of cluster tiles, in walking order.
@@ -269,19 +272,22 @@ __device__ __forceinline__ void epi_swiglu(const GemmShape& sh, const GemmEpi& e
 
 // ------------------------------------------------------------------- kernel
 //
-// CM = 1: one CTA per output tile.  CM = 2: clusters of two CTAs own the two
-// M-tiles (2*tmc, 2*tmc + 1) of the same N-tile; the B tile they share is
-// loaded once, each CTA fetching half of it with TMA multicast into both
-// CTAs' shared memory, which halves each SM's B traffic from L2.  Every CTA
-// still issues its own cta_group::1 MMAs; a stage is refilled only after the
-// MMAs of both CTAs have released it (each CTA's commit arrives on both
-// CTAs' `empty` barrier).
+// CM = 1: one CTA per 128-row output tile, cta_group::1 products.
+// CM = 2: a cluster of two CTAs owns a 256-row tile (rows of M-tiles 2*tmc
+// and 2*tmc + 1) of one N-tile.  One thread of the even CTA issues tcgen05
+// cta_group::2 products, which read A's two 128-row halves and B's two
+// BN/2-row halves from the two CTAs' shared memory; each SM so loads half of
+// the B tile, and receives its own 128 rows of the accumulator in its tensor
+// memory.  Both CTAs' copies of a stage complete on the even CTA's `full`
+// barrier; the products' completion is committed to both CTAs' `empty` and
+// `tfull` barriers; the four epilogue warps of each CTA report a drained
+// accumulator on the even CTA's `tempty` barrier.
 
 template <int BN, int EPI, int CM>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
 gemm_tc_kernel(const __grid_constant__ GemmProb p0, const __grid_constant__ GemmProb p1, const int nprob,
                const DevErr err) {
-    using Cfg = GemmCfg<BN>;
+    using Cfg = GemmCfg<BN, CM>;
     constexpr int STAGES = Cfg::STAGES;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -299,8 +305,8 @@ gemm_tc_kernel(const __grid_constant__ GemmProb p0, const __grid_constant__ Gemm
     const int lane = threadIdx.x & 31;
 
     const uint32_t crank = (CM > 1) ? cluster_ctarank() : 0u;
+    const bool leader = crank == 0;   // the CTA that issues the products
     const int cid = blockIdx.x / CM, nclusters = gridDim.x / CM;
-    constexpr uint16_t kPair = (1u << CM) - 1u;
     // cluster tiles of each problem; tile t of the launch belongs to problem 0 if t < T0
     const int tmc0 = (p0.sh.tiles_m + CM - 1) / CM, tmc1 = (p1.sh.tiles_m + CM - 1) / CM;
     const int T0 = tmc0 * p0.sh.tiles_n;
@@ -310,10 +316,12 @@ gemm_tc_kernel(const __grid_constant__ GemmProb p0, const __grid_constant__ Gemm
         P = second ? &p1 : &p0;
         tile_coords(P->sh, second ? tmc1 : tmc0, second ? t - T0 : t, tmc, tn);
     };
+    // shared::cluster address of barrier `b` of this CTA in CTA `rank`
+    auto at = [](const uint64_t* b, uint32_t rank) { return mapa_shared(smem_u32(b), rank); };
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], CM); }
-        for (int a = 0; a < 2; ++a) { mbar_init(&tfull[a], 1); mbar_init(&tempty[a], 128); }
+        for (int s = 0; s < STAGES; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
+        for (int a = 0; a < 2; ++a) { mbar_init(&tfull[a], 1); mbar_init(&tempty[a], 4 * CM); }
         mbar_init(drain, 1);
         *abort_flag = 0;
         fence_barrier_init();
@@ -325,15 +333,18 @@ gemm_tc_kernel(const __grid_constant__ GemmProb p0, const __grid_constant__ Gemm
             for (int j = 0; j < P.sh.nb; ++j) prefetch_tensormap(&P.b[j]);
         }
     }
-    if (warp == 1) { tmem_alloc(tmem_holder, Cfg::TMEM_COLS); tmem_relinquish(); }
+    if (warp == 1) {
+        if (CM > 1) { tmem_alloc_pair(tmem_holder, Cfg::TMEM_COLS); tmem_relinquish_pair(); }
+        else { tmem_alloc(tmem_holder, Cfg::TMEM_COLS); tmem_relinquish(); }
+    }
     tc_fence_before();
-    if (CM > 1) cluster_sync(); else __syncthreads();   // peers' barriers are initialised before any multicast
+    if (CM > 1) cluster_sync(); else __syncthreads();   // the pair's barriers are initialised before any use
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
 
     if (warp == 0) {
         if (lane == 0) {
-            // ---------------- TMA producer
+            // ---------------- TMA producer (each CTA loads its own halves)
             int stage = 0;
             uint32_t phase = 0;
             uint32_t fills = 0;   // bit s: stage s has been filled at least once
@@ -350,27 +361,31 @@ gemm_tc_kernel(const __grid_constant__ GemmProb p0, const __grid_constant__ Gemm
                 else if (sh.nb > 1 && n0 >= sh.b_begin[1]) { mb = &P->b[1]; nb0 = n0 - sh.b_begin[1]; }
                 for (int kb = 0; kb < sh.num_kb; ++kb) {
                     if (*abort_flag || !mbar_wait(&empty[stage], phase ^ 1, err)) { aborted = true; break; }
-                    mbar_arrive_expect_tx(&full[stage], Cfg::A_BYTES + Cfg::B_BYTES);
-                    if (sh.a_kb_per_slab)   // A = the slabs side by side along K
-                        tma_load_3d(sA + stage * Cfg::A_BYTES, &P->a, (kb % sh.a_kb_per_slab) * GEMM_BK, m0,
-                                    kb / sh.a_kb_per_slab, &full[stage]);
-                    else
-                        tma_load_2d(sA + stage * Cfg::A_BYTES, &P->a, kb * GEMM_BK, m0, &full[stage]);
-                    if (sh.split_b) {   // [gate half (map 0) ; up half (map 1)] of the same features
-                        const int fr = tn * (BN / 2);
-                        if (CM == 1) {
-                            tma_load_2d(sB + stage * Cfg::B_BYTES, &P->b[0], kb * GEMM_BK, fr, &full[stage]);
-                            tma_load_2d(sB + stage * Cfg::B_BYTES + Cfg::B_BYTES / 2, &P->b[1], kb * GEMM_BK, fr,
-                                        &full[stage]);
+                    const int ax = (sh.a_kb_per_slab ? kb % sh.a_kb_per_slab : kb) * GEMM_BK;
+                    const int az = sh.a_kb_per_slab ? kb / sh.a_kb_per_slab : 0;   // A slab (3-D map)
+                    uint8_t* dA = sA + stage * Cfg::A_BYTES;
+                    uint8_t* dB = sB + stage * Cfg::B_BYTES;
+                    if (CM == 1) {
+                        mbar_arrive_expect_tx(&full[stage], Cfg::A_BYTES + Cfg::B_BYTES);
+                        if (sh.a_kb_per_slab) tma_load_3d(dA, &P->a, ax, m0, az, &full[stage]);
+                        else tma_load_2d(dA, &P->a, ax, m0, &full[stage]);
+                        if (sh.split_b) {   // [gate half (map 0) ; up half (map 1)] of the same features
+                            const int fr = tn * (BN / 2);
+                            tma_load_2d(dB, &P->b[0], kb * GEMM_BK, fr, &full[stage]);
+                            tma_load_2d(dB + Cfg::B_BYTES / 2, &P->b[1], kb * GEMM_BK, fr, &full[stage]);
                         } else {
-                            tma_load_2d_mc(sB + stage * Cfg::B_BYTES + crank * (Cfg::B_BYTES / 2),
-                                           crank ? &P->b[1] : &P->b[0], kb * GEMM_BK, fr, &full[stage], kPair);
+                            tma_load_2d(dB, mb, kb * GEMM_BK, nb0, &full[stage]);
                         }
-                    } else if (CM == 1) {
-                        tma_load_2d(sB + stage * Cfg::B_BYTES, mb, kb * GEMM_BK, nb0, &full[stage]);
-                    } else {   // this CTA's share of the B tile, to every CTA of the cluster
-                        tma_load_2d_mc(sB + stage * Cfg::B_BYTES + crank * (Cfg::B_BYTES / CM), mb, kb * GEMM_BK,
-                                       nb0 + (int)crank * (BN / CM), &full[stage], kPair);
+                    } else {
+                        // both CTAs' bytes complete on the leader's barrier
+                        const uint32_t fb = at(&full[stage], 0);
+                        if (leader) mbar_arrive_expect_tx(&full[stage], 2 * (Cfg::A_BYTES + Cfg::B_BYTES));
+                        if (sh.a_kb_per_slab) tma_load_3d_pair(dA, &P->a, ax, m0, az, fb);
+                        else tma_load_2d_pair(dA, &P->a, ax, m0, fb);
+                        if (sh.split_b)   // this CTA's half: the gate rows (CTA 0) or the up rows (CTA 1)
+                            tma_load_2d_pair(dB, crank ? &P->b[1] : &P->b[0], kb * GEMM_BK, tn * (BN / 2), fb);
+                        else
+                            tma_load_2d_pair(dB, mb, kb * GEMM_BK, nb0 + (int)crank * (BN / 2), fb);
                     }
                     fills |= 1u << stage;
                     if (++stage == STAGES) { stage = 0; phase ^= 1; }
@@ -380,18 +395,21 @@ gemm_tc_kernel(const __grid_constant__ GemmProb p0, const __grid_constant__ Gemm
                 *abort_flag = 1;
                 // Let every copy already issued land before the CTA exits.  The
                 // latest fill of stage s has parity phase(s) computed from the
-                // position of the ring at exit.
-                for (int s = 0; s < STAGES; ++s) {
-                    if (!(fills & (1u << s))) continue;
-                    const uint32_t par = (s < stage) ? phase : (phase ^ 1);
-                    mbar_wait(&full[s], par, err);
+                // position of the ring at exit.  (In a pair the copies complete
+                // on the leader's barriers, which count both CTAs' bytes.)
+                if (leader) {
+                    for (int s = 0; s < STAGES; ++s) {
+                        if (!(fills & (1u << s))) continue;
+                        const uint32_t par = (s < stage) ? phase : (phase ^ 1);
+                        mbar_wait(&full[s], par, err);
+                    }
                 }
             }
         }
     } else if (warp == 1) {
-        if (lane == 0) {
+        if (lane == 0 && leader) {
             // ---------------- MMA issuer
-            constexpr uint32_t idesc = idesc_bf16(GEMM_BM, BN);
+            constexpr uint32_t idesc = idesc_bf16(GEMM_BM * CM, BN);
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
@@ -409,22 +427,32 @@ gemm_tc_kernel(const __grid_constant__ GemmProb p0, const __grid_constant__ Gemm
                     const uint64_t ad = sw128_desc(smem_u32(sA + stage * Cfg::A_BYTES));
                     const uint64_t bd = sw128_desc(smem_u32(sB + stage * Cfg::B_BYTES));
                     #pragma unroll
-                    for (int k = 0; k < GEMM_BK / 16; ++k)
-                        mma_bf16(d_tmem, ad + 2 * k, bd + 2 * k, idesc, (kb | k) != 0);
+                    for (int k = 0; k < GEMM_BK / 16; ++k) {
+                        if (CM == 1) mma_bf16(d_tmem, ad + 2 * k, bd + 2 * k, idesc, (kb | k) != 0);
+                        else mma_bf16_pair(d_tmem, ad + 2 * k, bd + 2 * k, idesc, (kb | k) != 0);
+                    }
                     issued = true;
-                    if (CM == 1) mma_commit(&empty[stage]);
-                    else mma_commit_mc(&empty[stage], kPair);
+                    if (CM == 1) {
+                        mma_commit(&empty[stage]);
+                    } else {   // the stage is free in both CTAs
+                        mma_commit_pair_both(&empty[stage]);
+                    }
                     if (++stage == STAGES) { stage = 0; phase ^= 1; }
                 }
                 if (aborted) break;
-                mma_commit(&tfull[acc]);
+                if (CM == 1) {
+                    mma_commit(&tfull[acc]);
+                } else {
+                    mma_commit_pair_both(&tfull[acc]);
+                }
                 acc ^= 1;
                 if (acc == 0) acc_phase ^= 1;
             }
             if (aborted) {
                 *abort_flag = 1;
                 if (issued) {   // let issued MMAs finish before TMEM is released
-                    mma_commit(drain);
+                    if (CM == 1) mma_commit(drain);
+                    else mma_commit_pair(at(drain, 0));
                     mbar_wait(drain, 0, err);
                 }
             }
@@ -448,16 +476,23 @@ gemm_tc_kernel(const __grid_constant__ GemmProb p0, const __grid_constant__ Gemm
             else if (EPI == EPI_RESID) epi_resid<BN>(P->sh, P->ep, tbase, row, tn * BN);
             else if (EPI == EPI_SWIGLU) epi_swiglu<BN>(P->sh, P->ep, tbase, row, tn);
             else epi_argmax<BN>(P->sh, P->ep, tbase, row, tn * BN, tn);
+            // every lane's tensor-memory reads are complete before the warp reports
             tc_fence_before();
-            mbar_arrive(&tempty[acc]);
+            __syncwarp();
+            if (lane == 0) {
+                if (CM == 1) mbar_arrive(&tempty[acc]);
+                else mbar_arrive_cluster(at(&tempty[acc], 0));
+            }
             acc ^= 1;
             if (acc == 0) acc_phase ^= 1;
         }
     }
     __syncthreads();
+    if (CM > 1) cluster_sync();   // neither CTA's tensor memory is read or written any more
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+        if (CM > 1) tmem_dealloc_pair(tmem_base, Cfg::TMEM_COLS);
+        else tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
     }
     if (CM > 1) cluster_sync();   // no CTA leaves while a peer may still arrive on its barriers
 }
