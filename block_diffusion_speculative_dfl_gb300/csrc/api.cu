@@ -358,7 +358,7 @@ GemmArgs ctx_kv_args(const void* Xc, int64_t ctx_M, int ctx_per, int d, const vo
     gc.A = Xc; gc.M = (int)ctx_M; gc.K = d;
     gc.B[0] = Wkc; gc.B[1] = Wvc; gc.b_rows[0] = kv; gc.b_rows[1] = kv;
     gc.b_begin[0] = 0; gc.b_begin[1] = kv; gc.nb = 2; gc.N = 2 * kv;
-    gc.bn = (kv % 256 == 0) ? 256 : 128;
+    gc.bn = 0;   // chosen per shape (the grouped launch picks one width for both problems)
     gc.m_inner = 0;
     gc.epi = EPI_STORE;
     gc.ep.seg[0] = GemmSeg{Kc, 0, kv, rope != nullptr};

@@ -67,7 +67,7 @@ dfl_status launch(DeviceCtx* ctx, const GemmProb& p0, const GemmProb& p1, int np
     const int grid = (tiles < max_clusters ? tiles : max_clusters) * CM;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(GEMM_THREADS);
+    cfg.blockDim = dim3(GemmCfg<BN, CM>::THREADS);
     cfg.dynamicSmemBytes = GemmCfg<BN, CM>::SMEM;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
@@ -90,6 +90,25 @@ dfl_status launch_cm(DeviceCtx* ctx, const GemmProb& p0, const GemmProb& p1, int
     return launch<BN, EPI, 1>(ctx, p0, p1, nprob, tag, st, slot);
 }
 
+// Relative time of one tile of width bn with clusters of cm: its products
+// take ~bn units of tensor time and it reads (128 cm + bn) rows of operands
+// from L2 per k-block; at ~12 TB/s of L2-to-SM reads a 256-row pair tile of
+// width 256 is held to ~0.81 of the tensor rate, so the L2 term weighs 0.62.
+double tile_cost(int bn, int cm) {
+    const double l2 = 0.62 * (GEMM_BM * cm + bn);
+    return bn > l2 ? bn : l2;
+}
+
+// Tile widths a problem takes: 512 only as pair tiles with the rotary-store
+// or residual epilogue; every B segment must start on a tile boundary.
+bool width_ok(const GemmArgs& g, int bn, int cm) {
+    if (g.bn != 0) return g.bn == bn;
+    if (bn == 512 && (cm != 2 || (g.epi != EPI_STORE && g.epi != EPI_RESID) || g.split_b)) return false;
+    if (g.split_b) return (g.N / 2) % (bn / 2) == 0;
+    for (int j = 0; j < g.nb; ++j) if (g.b_begin[j] % bn != 0) return false;
+    return true;
+}
+
 }  // namespace
 
 // Tile width for bn == 0: the one that minimises (rounds of cluster tiles
@@ -98,25 +117,27 @@ dfl_status launch_cm(DeviceCtx* ctx, const GemmProb& p0, const GemmProb& p1, int
 // every B segment to start on a 256-column boundary.
 static int pick_bn(const GemmArgs& g, int sm_count) {
     if (g.split_b) return (g.N / 2) % 128 == 0 ? 256 : 128;
-    bool ok256 = true;
-    for (int j = 0; j < g.nb; ++j) ok256 = ok256 && (g.b_begin[j] % 256 == 0);
-    if (!ok256) return 128;
     const int tiles_m = (g.M + GEMM_BM - 1) / GEMM_BM;
     const int cm = tiles_m >= 2 ? 2 : 1;
     const int tiles_mc = (tiles_m + cm - 1) / cm;
     const int clusters = sm_count / cm;
+    // the busiest cluster's rounds of tiles times the cost of one tile
     auto cost = [&](int bn) {
         const int tiles = tiles_mc * ((g.N + bn - 1) / bn);
-        return (long)((tiles + clusters - 1) / clusters) * bn;
+        return (double)((tiles + clusters - 1) / clusters) * tile_cost(bn, cm);
     };
-    return cost(256) <= cost(128) ? 256 : 128;
+    int best = 128;
+    for (int bn : {256, 512})
+        if (width_ok(g, bn, cm) && cost(bn) <= cost(best)) best = bn;
+    return best;
 }
 
 // Validated problem of one GEMM for tile width bn and cluster size cm.
 static dfl_status build_prob(const GemmArgs& g, int cm, GemmProb& P) {
     if (g.M <= 0 || g.N <= 0 || g.K <= 0) return DFL_ERR_INVALID_ARG;
     if (g.K % 8 != 0 || !aligned16(g.A)) return DFL_ERR_MISALIGNED;
-    if (g.bn != 128 && g.bn != 256) return DFL_ERR_UNSUPPORTED_SHAPE;
+    if (g.bn != 128 && g.bn != 256 && g.bn != 512) return DFL_ERR_UNSUPPORTED_SHAPE;
+    if (g.bn == 512 && !width_ok(g, 512, cm)) return DFL_ERR_UNSUPPORTED_SHAPE;
     if (g.nb < 1 || g.nb > 3) return DFL_ERR_INVALID_ARG;
     GemmShape& sh = P.sh;
     sh = GemmShape{};
@@ -142,7 +163,8 @@ static dfl_status build_prob(const GemmArgs& g, int cm, GemmProb& P) {
         if (!aligned16(g.B[jj])) return DFL_ERR_MISALIGNED;
         // every tile of BN columns must come from one B map
         if (j < g.nb && !g.split_b && (g.b_begin[j] % g.bn != 0)) return DFL_ERR_UNSUPPORTED_SHAPE;
-        if (!make_map(&P.b[j], g.B[jj], g.b_rows[jj], g.K, g.split_b ? g.bn / 2 : g.bn / cm)) return DFL_ERR_CUDA;
+            const int box = g.split_b ? g.bn / 2 : (g.bn == 512 ? 128 : g.bn / cm);   // rows of one B copy
+        if (!make_map(&P.b[j], g.B[jj], g.b_rows[jj], g.K, box)) return DFL_ERR_CUDA;
         sh.b_begin[j] = g.b_begin[jj];
     }
     P.ep = g.ep;
@@ -151,6 +173,10 @@ static dfl_status build_prob(const GemmArgs& g, int cm, GemmProb& P) {
 
 static dfl_status launch_probs(DeviceCtx* ctx, const GemmProb& p0, const GemmProb& p1, int nprob, int bn, int epi,
                                int cm, const char* tag, cudaStream_t st) {
+    if (bn == 512) {   // pair tiles only (checked when the problem was built)
+        if (epi == EPI_STORE) return launch<512, EPI_STORE, 2>(ctx, p0, p1, nprob, tag, st, 16);
+        return launch<512, EPI_RESID, 2>(ctx, p0, p1, nprob, tag, st, 17);
+    }
     const int slot = (bn == 256 ? 0 : 4) + epi;
     if (bn == 256) {
         if (epi == EPI_STORE) return launch_cm<256, EPI_STORE>(ctx, p0, p1, nprob, tag, st, slot, cm);
@@ -181,18 +207,23 @@ dfl_status gemm_tc(DeviceCtx* ctx, const GemmArgs& g_in, cudaStream_t st) {
 // there is none.
 dfl_status gemm_tc2(DeviceCtx* ctx, const GemmArgs& g0_in, const GemmArgs& g1_in, const char* tag, cudaStream_t st) {
     GemmArgs g0 = g0_in, g1 = g1_in;
-    // One tile width for both: 256 when every B segment of both allows it (a
-    // grouped launch has enough tiles either way), else 128.
-    auto allows = [](const GemmArgs& g, int bn) {
-        if (g.bn != 0) return g.bn == bn;
-        if (g.split_b) return (g.N / 2) % (bn / 2) == 0;
-        for (int j = 0; j < g.nb; ++j) if (g.b_begin[j] % bn != 0) return false;
-        return true;
-    };
-    const int bn = allows(g0, 256) && allows(g1, 256) ? 256 : allows(g0, 128) && allows(g1, 128) ? 128 : 0;
     // Clusters of two only when both problems have at least two M-tiles.
     const int cm0 = (g0.M + GEMM_BM - 1) / GEMM_BM >= 2 ? 2 : 1, cm1 = (g1.M + GEMM_BM - 1) / GEMM_BM >= 2 ? 2 : 1;
     const int cm = cm0 < cm1 ? cm0 : cm1;
+    // One tile width for both: of the widths both take, the one with the
+    // smallest (rounds of the joint tile sequence) x (cost of a tile).
+    const int clusters = ctx->sm_count / cm;
+    auto tiles_of = [&](const GemmArgs& g, int bn) {
+        return ((g.M + GEMM_BM - 1) / GEMM_BM + cm - 1) / cm * ((g.N + bn - 1) / bn);
+    };
+    int bn = 0;
+    double best = 0.0;
+    for (int w : {128, 256, 512}) {
+        if (!width_ok(g0, w, cm) || !width_ok(g1, w, cm)) continue;
+        const int tiles = tiles_of(g0, w) + tiles_of(g1, w);
+        const double c = (double)((tiles + clusters - 1) / clusters) * tile_cost(w, cm);
+        if (bn == 0 || c <= best) { bn = w; best = c; }
+    }
     if (bn == 0 || g0.epi != g1.epi) {
         dfl_status rc = gemm_tc(ctx, g0, st);
         return rc != DFL_OK ? rc : gemm_tc(ctx, g1, st);

@@ -78,16 +78,27 @@ struct GemmProb {
 
 constexpr int GEMM_BM = 128;
 constexpr int GEMM_BK = 64;
-constexpr int GEMM_THREADS = 192;
 
-// CM = 2: each CTA of the pair holds half of the B tile (BN / 2 rows) per stage.
+// Tile width BN (128, 256, or 512 over a CTA pair only) and cluster shape CM.
+// CM = 2: each CTA of the pair holds half of the B tile (BN / 2 rows) per
+// stage.  BN = 512: each k-step issues two N = 256 pair products (columns
+// 0..255 and 256..511 of the tile), whose B halves interleave: CTA r holds
+// tile rows r*128.. and 256 + r*128.. (two 128-row copies); the accumulator
+// is the whole of tensor memory (one buffer), drained by eight epilogue
+// warps (two per lane quadrant, a column half each).
 template <int BN, int CM>
 struct GemmCfg {
+    static_assert(BN != 512 || CM == 2, "512-wide tiles are pair tiles");
+    static constexpr int EW = (BN == 512) ? 8 : 4;                 // epilogue warps
+    static constexpr int THREADS = 64 + 32 * EW;                   // producer warp, MMA warp, epilogue warps
+    static constexpr int NACC = (BN == 512) ? 1 : 2;               // accumulator buffers
+    static constexpr int MMA_N = (BN > 256) ? 256 : BN;            // N of one product
+    static constexpr int B_BOX = (BN == 512) ? 128 : BN / CM;      // rows of one B copy
     static constexpr int A_BYTES = GEMM_BM * GEMM_BK * 2;
     static constexpr int B_BYTES = BN / CM * GEMM_BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int STAGES = (200 * 1024 / STAGE_BYTES) < 8 ? (200 * 1024 / STAGE_BYTES) : 8;
-    static constexpr int TMEM_COLS = 2 * BN;
+    static constexpr int TMEM_COLS = NACC * BN;
     static constexpr int BAR_BYTES = 256;
     static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
 };
@@ -284,7 +295,7 @@ __device__ __forceinline__ void epi_swiglu(const GemmShape& sh, const GemmEpi& e
 // accumulator on the even CTA's `tempty` barrier.
 
 template <int BN, int EPI, int CM>
-__global__ void __launch_bounds__(GEMM_THREADS, 1)
+__global__ void __launch_bounds__(GemmCfg<BN, CM>::THREADS, 1)
 gemm_tc_kernel(const __grid_constant__ GemmProb p0, const __grid_constant__ GemmProb p1, const int nprob,
                const DevErr err) {
     using Cfg = GemmCfg<BN, CM>;
@@ -303,6 +314,7 @@ gemm_tc_kernel(const __grid_constant__ GemmProb p0, const __grid_constant__ Gemm
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    static_assert((EPI != EPI_SWIGLU && EPI != EPI_ARGMAX) || Cfg::EW == 4, "these epilogues take whole tiles");
 
     const uint32_t crank = (CM > 1) ? cluster_ctarank() : 0u;
     const bool leader = crank == 0;   // the CTA that issues the products
@@ -321,7 +333,7 @@ gemm_tc_kernel(const __grid_constant__ GemmProb p0, const __grid_constant__ Gemm
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
-        for (int a = 0; a < 2; ++a) { mbar_init(&tfull[a], 1); mbar_init(&tempty[a], 4 * CM); }
+        for (int a = 0; a < 2; ++a) { mbar_init(&tfull[a], 1); mbar_init(&tempty[a], Cfg::EW * CM); }
         mbar_init(drain, 1);
         *abort_flag = 0;
         fence_barrier_init();
@@ -382,10 +394,14 @@ gemm_tc_kernel(const __grid_constant__ GemmProb p0, const __grid_constant__ Gemm
                         if (leader) mbar_arrive_expect_tx(&full[stage], 2 * (Cfg::A_BYTES + Cfg::B_BYTES));
                         if (sh.a_kb_per_slab) tma_load_3d_pair(dA, &P->a, ax, m0, az, fb);
                         else tma_load_2d_pair(dA, &P->a, ax, m0, fb);
-                        if (sh.split_b)   // this CTA's half: the gate rows (CTA 0) or the up rows (CTA 1)
+                        if (sh.split_b) {   // this CTA's half: the gate rows (CTA 0) or the up rows (CTA 1)
                             tma_load_2d_pair(dB, crank ? &P->b[1] : &P->b[0], kb * GEMM_BK, tn * (BN / 2), fb);
-                        else
+                        } else if (BN == 512) {   // this CTA's halves of the two products' B tiles
+                            tma_load_2d_pair(dB, mb, kb * GEMM_BK, nb0 + (int)crank * 128, fb);
+                            tma_load_2d_pair(dB + Cfg::B_BYTES / 2, mb, kb * GEMM_BK, nb0 + 256 + (int)crank * 128, fb);
+                        } else {
                             tma_load_2d_pair(dB, mb, kb * GEMM_BK, nb0 + (int)crank * (BN / 2), fb);
+                        }
                     }
                     fills |= 1u << stage;
                     if (++stage == STAGES) { stage = 0; phase ^= 1; }
@@ -409,7 +425,7 @@ gemm_tc_kernel(const __grid_constant__ GemmProb p0, const __grid_constant__ Gemm
     } else if (warp == 1) {
         if (lane == 0 && leader) {
             // ---------------- MMA issuer
-            constexpr uint32_t idesc = idesc_bf16(GEMM_BM * CM, BN);
+            constexpr uint32_t idesc = idesc_bf16(GEMM_BM * CM, Cfg::MMA_N);
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
@@ -428,8 +444,14 @@ gemm_tc_kernel(const __grid_constant__ GemmProb p0, const __grid_constant__ Gemm
                     const uint64_t bd = sw128_desc(smem_u32(sB + stage * Cfg::B_BYTES));
                     #pragma unroll
                     for (int k = 0; k < GEMM_BK / 16; ++k) {
-                        if (CM == 1) mma_bf16(d_tmem, ad + 2 * k, bd + 2 * k, idesc, (kb | k) != 0);
-                        else mma_bf16_pair(d_tmem, ad + 2 * k, bd + 2 * k, idesc, (kb | k) != 0);
+                        if (CM == 1) {
+                            mma_bf16(d_tmem, ad + 2 * k, bd + 2 * k, idesc, (kb | k) != 0);
+                        } else {
+                            mma_bf16_pair(d_tmem, ad + 2 * k, bd + 2 * k, idesc, (kb | k) != 0);
+                            if (BN == 512)   // columns 256..511 from the second B halves (16 KB further)
+                                mma_bf16_pair(d_tmem + 256, ad + 2 * k, bd + ((Cfg::B_BYTES / 2) >> 4) + 2 * k, idesc,
+                                              (kb | k) != 0);
+                        }
                     }
                     issued = true;
                     if (CM == 1) {
@@ -445,8 +467,7 @@ gemm_tc_kernel(const __grid_constant__ GemmProb p0, const __grid_constant__ Gemm
                 } else {
                     mma_commit_pair_both(&tfull[acc]);
                 }
-                acc ^= 1;
-                if (acc == 0) acc_phase ^= 1;
+                if (++acc == Cfg::NACC) { acc = 0; acc_phase ^= 1; }
             }
             if (aborted) {
                 *abort_flag = 1;
@@ -458,8 +479,11 @@ gemm_tc_kernel(const __grid_constant__ GemmProb p0, const __grid_constant__ Gemm
             }
         }
     } else {
-        // ---------------- epilogue warps 2..5: TMEM lane quadrant = warp % 4
+        // ---------------- epilogue warps 2..: TMEM lane quadrant = warp % 4,
+        // column part (warp - 2) / 4 of COLS columns
+        constexpr int COLS = BN * 4 / Cfg::EW;
         const int q = warp & 3;
+        const int part = (warp - 2) >> 2;
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int t = cid; t < total; t += nclusters) {
@@ -471,10 +495,11 @@ gemm_tc_kernel(const __grid_constant__ GemmProb p0, const __grid_constant__ Gemm
             int tmc, tn;
             locate(t, P, tmc, tn);
             const int row = (tmc * CM + (int)crank) * GEMM_BM + q * 32 + lane;
-            const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
-            if (EPI == EPI_STORE) epi_store<BN>(P->sh, P->ep, tbase, row, tn * BN);
-            else if (EPI == EPI_RESID) epi_resid<BN>(P->sh, P->ep, tbase, row, tn * BN);
-            else if (EPI == EPI_SWIGLU) epi_swiglu<BN>(P->sh, P->ep, tbase, row, tn);
+            const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN + part * COLS;
+            const int n0 = tn * BN + part * COLS;
+            if (EPI == EPI_STORE) epi_store<COLS>(P->sh, P->ep, tbase, row, n0);
+            else if (EPI == EPI_RESID) epi_resid<COLS>(P->sh, P->ep, tbase, row, n0);
+            else if (EPI == EPI_SWIGLU) epi_swiglu<BN>(P->sh, P->ep, tbase, row, tn);   // one part: COLS == BN
             else epi_argmax<BN>(P->sh, P->ep, tbase, row, tn * BN, tn);
             // every lane's tensor-memory reads are complete before the warp reports
             tc_fence_before();
@@ -483,8 +508,7 @@ gemm_tc_kernel(const __grid_constant__ GemmProb p0, const __grid_constant__ Gemm
                 if (CM == 1) mbar_arrive(&tempty[acc]);
                 else mbar_arrive_cluster(at(&tempty[acc], 0));
             }
-            acc ^= 1;
-            if (acc == 0) acc_phase ^= 1;
+            if (++acc == Cfg::NACC) { acc = 0; acc_phase ^= 1; }
         }
     }
     __syncthreads();

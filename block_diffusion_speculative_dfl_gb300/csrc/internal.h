@@ -26,7 +26,7 @@ struct DeviceCtx {
     int* err_word = nullptr;       // device address of this device's error word
     // max-dynamic-smem attribute set (atomic: calls may come from several
     // host threads; setting it twice is harmless)
-    std::atomic<bool> gemm_attr_set[16] = {};   // gemm instantiations
+    std::atomic<bool> gemm_attr_set[18] = {};   // gemm instantiations
     std::atomic<bool> mix_attr_set{false};
     std::atomic<bool> attn_attr_set[4] = {};    // tcgen05 attention: head dim 64 / 128, M = 64 / 128 products
     // Host-input draft step: a copy stream and events, created on first use.
@@ -88,7 +88,7 @@ struct GemmArgs {
     int nb;
     int N;                  // total columns
     int m_inner;
-    int bn;                 // 128 or 256
+    int bn;                 // 128, 256 or 512 (pair tiles with the store or residual epilogue); 0: chosen
     int epi;                // EpiKind
     GemmEpi ep;
     const char* tag;        // name in kernel traces
