@@ -71,6 +71,7 @@ def parse_args(argv=None):
                         "not the benchmark line; for profiling)")
     p.add_argument("--rows", type=int, default=0, help="--kernel mix / fc_fuse: context rows (default N * C)")
     p.add_argument("--iters", type=int, default=10, help="--kernel: timed launches")
+    p.add_argument("--no-graph", action="store_true", help="time eager launches instead of a CUDA graph of the step")
     p.add_argument("--e2e-steps", type=int, default=7)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -455,28 +456,45 @@ def run_ours(args, rank, world, local):
         step()
         flush()
     torch.cuda.synchronize()
+    # The timed steps replay one CUDA graph of the step (a call allocates and
+    # synchronises nothing, so a captured step replays bit for bit), with no
+    # per-launch trace events in them; a traced pass of the same steps, eager,
+    # follows and gives each kernel's time (the roofline) and the launch count.
+    graph = None
+    if not args.no_graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step()
+        graph.replay()
+        torch.cuda.synchronize()
+    run = graph.replay if graph is not None else step
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     clocks = ClockSampler(torch.cuda.current_device())
     time.sleep(0.3)
-    dfl.dfl_profile_enable(True)
     barrier(world)
     torch.cuda.synchronize()
     torch.cuda.nvtx.range_push("bench_timed")   # profilers can select the timed steps' kernels by this range
     for a, b in evs:
         a.record()
-        step()
+        run()
         b.record()
         flush()
     torch.cuda.synchronize()
     torch.cuda.nvtx.range_pop()
     barrier(world)
+    ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    dfl.dfl_profile_enable(True)
+    for _ in range(args.steps):
+        step()
+        flush()
+    torch.cuda.synchronize()
     dfl.dfl_profile_enable(False)
     clk = clocks.stop()
     prof, launches = dfl.dfl_profile_report()
+    launches -= prof.get("copy_block_init", (0, 0.0))[0]   # a device-to-device copy, not a kernel
     err = dfl.dfl_get_device_error()
     if err:
         raise RuntimeError(f"device error {err} during the timed steps")
-    ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
     ms_max = reduce_scalar(ms, world, "max", device="cuda")
     units = w.N * w.B
     value = aggregate(units, ms_max / 1e3, world)
@@ -552,6 +570,9 @@ def run_ours(args, rank, world, local):
                                          "sampled": " + sampled-greedy acceptance"}[args.accept_rule])
                            if w.K > 0 else "greedy acceptance",
                            "l2": "inputs larger than L2; between timed steps a 256 MB buffer is written, then another read, so the dirty lines are written back before the next step"},
+                "timing": ("CUDA graph of the step, replayed; per-kernel times from a traced eager pass of the "
+                           "same steps" if graph is not None else "eager launches; per-kernel times from a traced "
+                           "eager pass of the same steps"),
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
                 "clocks": clk, "kernels": kernels}
         print(json.dumps(line), flush=True)
