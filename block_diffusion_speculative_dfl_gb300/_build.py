@@ -11,6 +11,11 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(os.path.dirname(PKG), "include")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT_DIR, "libdfl.so")
+# The bounds-checked variant (-DDFL_CHECK): kernels check the indices they
+# compute for global accesses against the extents their shapes give, record
+# DFL_ERR_BOUNDS and skip the access.  For tests; slower.
+CHECK_DIR = os.path.join(OUT_DIR, "check")
+LIB_CHECK = os.path.join(CHECK_DIR, "libdfl_check.so")
 SOURCES = ["api.cu", "mix_rmsnorm.cu", "gemm_tc.cu", "block_attn.cu", "block_attn_tc.cu", "small_kernels.cu", "self_select.cu",
            "accept_ext.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -29,16 +34,19 @@ def _newest_input() -> float:
     return max(os.path.getmtime(p) for p in paths)
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile every CUDA source and link libdfl.so; returns its path."""
-    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= _newest_input():
-        return LIB
-    os.makedirs(OUT_DIR, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, checked: bool = False) -> str:
+    """Compile every CUDA source and link libdfl.so (or, with `checked`, the
+    bounds-checked libdfl_check.so); returns its path."""
+    lib, out_dir = (LIB_CHECK, CHECK_DIR) if checked else (LIB, OUT_DIR)
+    flags = FLAGS + (["-DDFL_CHECK"] if checked else [])
+    if not force and os.path.exists(lib) and os.path.getmtime(lib) >= _newest_input():
+        return lib
+    os.makedirs(out_dir, exist_ok=True)
     nvcc = _nvcc()
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(OUT_DIR, src.replace(".cu", ".o"))
-        cmd = [nvcc, *FLAGS, "-c", os.path.join(CSRC, src), "-o", obj]
+        obj = os.path.join(out_dir, src.replace(".cu", ".o"))
+        cmd = [nvcc, *flags, "-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed on {src}:\n{r.stderr}")
@@ -48,13 +56,13 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
     with ThreadPoolExecutor(len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB + ".tmp"
+    tmp = lib + ".tmp"
     cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

@@ -9,10 +9,10 @@ from __future__ import annotations
 import ctypes as C
 import os
 
-from ._build import LIB
+from ._build import LIB, LIB_CHECK
 
 DFL_OK, DFL_ERR_INVALID_ARG, DFL_ERR_UNSUPPORTED_SHAPE, DFL_ERR_MISALIGNED = 0, 1, 2, 3
-DFL_ERR_WORKSPACE, DFL_ERR_CUDA, DFL_ERR_TIMEOUT, DFL_ERR_NO_DEVICE = 4, 5, 6, 7
+DFL_ERR_WORKSPACE, DFL_ERR_CUDA, DFL_ERR_TIMEOUT, DFL_ERR_NO_DEVICE, DFL_ERR_BOUNDS = 4, 5, 6, 7, 8
 DFL_F32, DFL_BF16 = 0, 1
 DFL_OP_DUAL_KV_PROJ, DFL_OP_BLOCK_ATTN, DFL_OP_LM_HEAD, DFL_OP_SELF_SELECT, DFL_OP_DRAFT_STEP = 1, 2, 3, 4, 5
 DFL_OP_TV_ACCEPTANCE, DFL_OP_SPEC_ACCEPT, DFL_OP_BLOCK_FFN, DFL_OP_DRAFT_STEP_CACHED = 6, 7, 8, 9
@@ -102,14 +102,18 @@ _lib = None
 
 
 def load(path: str | None = None) -> C.CDLL:
-    """Load libdfl.so (building it first if absent) and declare signatures."""
+    """Load libdfl.so (building it first if absent) and declare signatures.
+
+    With DFL_CHECKED_BUILD=1 in the environment the bounds-checked variant
+    (libdfl_check.so) is loaded instead."""
     global _lib
     if _lib is not None:
         return _lib
-    path = path or LIB
+    checked = os.environ.get("DFL_CHECKED_BUILD") == "1"
+    path = path or (LIB_CHECK if checked else LIB)
     if not os.path.exists(path):
         from ._build import build
-        build()
+        build(checked=checked)
     lib = C.CDLL(path)
     for name, (args, res) in _SIGS.items():
         fn = getattr(lib, name)

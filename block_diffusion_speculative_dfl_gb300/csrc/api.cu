@@ -189,6 +189,7 @@ extern "C" const char* dfl_status_string(dfl_status s) {
         case DFL_ERR_CUDA: return "CUDA call or launch failed";
         case DFL_ERR_TIMEOUT: return "device-side wait timed out";
         case DFL_ERR_NO_DEVICE: return "no sm_103a device is current";
+        case DFL_ERR_BOUNDS: return "a kernel index fell outside its buffer (bounds-checked build); access skipped";
     }
     return "unknown status";
 }
@@ -341,6 +342,7 @@ struct KvRowPlan {
     const int32_t* ctx_pos;
     const int32_t* ctx_dst;
     const int32_t* blk_pos;
+    int64_t dst_rows;   // rows of the cache layer the context rows are scattered to
 };
 
 // bf16 projections of one draft layer: context rows [Kc | Vc] = Xc [Wkc ; Wvc]^T
@@ -361,8 +363,9 @@ GemmArgs ctx_kv_args(const void* Xc, int64_t ctx_M, int ctx_per, int d, const vo
     gc.bn = 0;   // chosen per shape (the grouped launch picks one width for both problems)
     gc.m_inner = 0;
     gc.epi = EPI_STORE;
-    gc.ep.seg[0] = GemmSeg{Kc, 0, kv, rope != nullptr};
-    gc.ep.seg[1] = GemmSeg{Vc, kv, kv, 0};
+    const int64_t out_rows = plan ? plan->dst_rows : ctx_M;
+    gc.ep.seg[0] = GemmSeg{Kc, 0, kv, rope != nullptr, out_rows};
+    gc.ep.seg[1] = GemmSeg{Vc, kv, kv, 0, out_rows};
     gc.ep.nseg = 2;
     gc.ep.rope = rope; gc.ep.hd = hd; gc.ep.rows_per_seq = ctx_per; gc.ep.pos_off = 0;
     if (plan) { gc.ep.row_pos = plan->ctx_pos; gc.ep.row_dst = plan->ctx_dst; }
@@ -389,9 +392,9 @@ dfl_status dual_kv_proj_bf16(DeviceCtx* ctx, const void* Xc, int64_t ctx_M, int 
     gb.bn = 0;   // chosen per shape
     gb.m_inner = 1;
     gb.epi = EPI_STORE;
-    gb.ep.seg[0] = GemmSeg{Q, 0, qd, rope != nullptr};
-    gb.ep.seg[1] = GemmSeg{Kb, qd, kv, rope != nullptr};
-    gb.ep.seg[2] = GemmSeg{Vb, qd + kv, kv, 0};
+    gb.ep.seg[0] = GemmSeg{Q, 0, qd, rope != nullptr, (int64_t)N * B};
+    gb.ep.seg[1] = GemmSeg{Kb, qd, kv, rope != nullptr, (int64_t)N * B};
+    gb.ep.seg[2] = GemmSeg{Vb, qd + kv, kv, 0, (int64_t)N * B};
     gb.ep.nseg = 3;
     gb.ep.rope = rope; gb.ep.hd = hd; gb.ep.rows_per_seq = B; gb.ep.pos_off = ctx_per;
     if (plan) gb.ep.row_pos = plan->blk_pos;
@@ -576,7 +579,7 @@ extern "C" dfl_status dfl_block_ffn(float* Xb, int32_t N, int32_t B, int32_t d, 
         g.bn = 0;
         g.m_inner = 1;
         g.epi = EPI_SWIGLU;
-        g.ep.seg[0] = GemmSeg{h, 0, F, 0};
+        g.ep.seg[0] = GemmSeg{h, 0, F, 0, M};
         g.ep.nseg = 1;
         g.tag = "gemm_ffn_gate_up";
         if ((rc = gemm_tc(ctx, g, st)) != DFL_OK) return rc;
@@ -794,6 +797,7 @@ dfl_status draft_step_impl(const dfl_step_args* a, const dfl_ctx_cache* cache, v
         plan.ctx_pos = reinterpret_cast<int32_t*>(carve(p, (size_t)ctx_rows * 4));
         plan.ctx_dst = reinterpret_cast<int32_t*>(carve(p, (size_t)ctx_rows * 4));
         plan.blk_pos = reinterpret_cast<int32_t*>(carve(p, (size_t)N * B * 4));
+        plan.dst_rows = (int64_t)N * C;
         len_new = reinterpret_cast<int32_t*>(carve(p, (size_t)N * 4));
     }
     int32_t* samples = a->samples;

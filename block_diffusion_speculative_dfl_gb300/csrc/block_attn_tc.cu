@@ -570,6 +570,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
                 else tmem_ld32(tmem_base + lane_off + Cfg::O_COL + c0, o);
                 if (!real) continue;
                 const int c = hh * OPT + c0;   // O column of o[0]
+                if (!DFL_IN_BOUNDS(err.word, (x.direct ? qrow : (int64_t)x.s * NQ + qrow) * HD + c + 31,
+                                   (x.direct ? (int64_t)1 : (int64_t)a.S) * NQ * HD))
+                    continue;
                 if (x.direct) {
                     uint4* dst = reinterpret_cast<uint4*>(a.O + qrow * HD + c);
                     #pragma unroll
@@ -589,7 +592,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
             __syncwarp();
             tc_fence_before();
             mbar_arrive(&bb.o_empty);
-            if (real && !pad && !x.direct && hh == 0) a.lse[(int64_t)x.s * NQ + qrow] = m_run + log2f(l_tot);
+            if (real && !pad && !x.direct && hh == 0 &&
+                DFL_IN_BOUNDS(err.word, (int64_t)x.s * NQ + qrow, (int64_t)a.S * NQ))
+                a.lse[(int64_t)x.s * NQ + qrow] = m_run + log2f(l_tot);
             ++icount;
         }
         if (!ok) *abort_flag = 1;
@@ -607,13 +612,18 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
 // per query row; lane i owns HD/32 consecutive elements.
 template <int HD>
 __global__ void attn_tc_combine_kernel(const float* Opart, const float* lse, int64_t NQ, int rows_per_seq, int B,
-                                       int C, const int32_t* ctx_len, int kps, __nv_bfloat16* O) {
+                                       int C, const int32_t* ctx_len, int kps, int S_max, int* err,
+                                       __nv_bfloat16* O) {
     constexpr int PER = HD / 32;
     const int64_t q = blockIdx.x * (int64_t)(blockDim.x >> 5) + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (q >= NQ) return;
     const int n = (int)(q / rows_per_seq);
-    const int S = ((ctx_len ? ctx_len[n] : C) + B + kps - 1) / kps;
+    int S = ((ctx_len ? ctx_len[n] : C) + B + kps - 1) / kps;
+    if (S > S_max) {   // a context length beyond the capacity: never read past the partials
+        if (err && lane == 0) atomicCAS(err, 0, DFL_ERR_INVALID_ARG);
+        S = S_max;
+    }
     if (S <= 1) return;   // written by the attention kernel
     const float l0 = lane < S ? lse[lane * NQ + q] : -INFINITY;
     const float l1 = lane + 32 < S ? lse[(lane + 32) * NQ + q] : -INFINITY;
@@ -803,10 +813,10 @@ dfl_status attn_tc(const void* Q, const void* Kc, const void* Vc, const void* Kb
     const unsigned cgrid = (unsigned)((NQ + 7) / 8);
     if (hd == 128)
         attn_tc_combine_kernel<128><<<cgrid, 256, 0, st>>>(a.Opart, a.lse, (int64_t)NQ, B * Hq, B, C, ctx_len, a.kps,
-                                                           a.O);
+                                                           a.S, ctx->err_word, a.O);
     else
         attn_tc_combine_kernel<64><<<cgrid, 256, 0, st>>>(a.Opart, a.lse, (int64_t)NQ, B * Hq, B, C, ctx_len, a.kps,
-                                                          a.O);
+                                                          a.S, ctx->err_word, a.O);
     return last_launch();
 }
 

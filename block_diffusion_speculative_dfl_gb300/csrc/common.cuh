@@ -27,6 +27,21 @@ __device__ __forceinline__ void record_error(const DevErr& e, int code) {
     if (e.word) atomicCAS(e.word, 0, code);
 }
 
+// Bounds-checked build (compiled with -DDFL_CHECK): an index that a kernel
+// computed for a global access, outside the extent that the kernel's shape
+// gives for that buffer, records DFL_ERR_BOUNDS in the error word and the
+// access is skipped.  In the normal build the check compiles to `true`.
+#ifdef DFL_CHECK
+__device__ __forceinline__ bool in_bounds(int* word, int64_t i, int64_t n) {
+    if (i >= 0 && i < n) return true;
+    if (word) atomicCAS(word, 0, DFL_ERR_BOUNDS);
+    return false;
+}
+#define DFL_IN_BOUNDS(word, i, n) ::dfl::in_bounds((word), (int64_t)(i), (int64_t)(n))
+#else
+#define DFL_IN_BOUNDS(word, i, n) true
+#endif
+
 __device__ __forceinline__ uint64_t globaltimer_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

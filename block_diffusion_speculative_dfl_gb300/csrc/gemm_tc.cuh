@@ -24,10 +24,11 @@ namespace dfl {
 enum EpiKind { EPI_STORE = 0, EPI_RESID = 1, EPI_ARGMAX = 2, EPI_SWIGLU = 3 };
 
 struct GemmSeg {
-    void* out;        // bf16 [M][ld] (EPI_STORE)
+    void* out;        // bf16 [rows][ld] (EPI_STORE)
     int n_begin;      // first global column of the segment
     int ld;           // row stride, elements
     int rope;         // apply rotate-half rotary embedding
+    int64_t rows;     // rows of the output buffer (bounds-checked build)
 };
 
 struct GemmEpi {
@@ -126,14 +127,14 @@ __device__ __forceinline__ void store_bf16x32(void* dst, const float (&v)[32]) {
 
 template <int BN>
 __device__ __forceinline__ void epi_store(const GemmShape& sh, const GemmEpi& ep, uint32_t tbase,
-                                          int row, int n0) {
+                                          int row, int n0, int* ew) {
     int s = 0;
     #pragma unroll
     for (int j = 1; j < 3; ++j)
         if (j < ep.nseg && n0 >= ep.seg[j].n_begin) s = j;
     const GemmSeg sg = ep.seg[s];
     const int64_t orow = (row < sh.M) ? (ep.row_dst ? (int64_t)ep.row_dst[row] : (int64_t)row) : -1;
-    const bool ok = orow >= 0;
+    const bool ok = orow >= 0 && DFL_IN_BOUNDS(ew, orow, sg.rows) && DFL_IN_BOUNDS(ew, n0 - sg.n_begin + BN - 1, sg.ld);
     __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(sg.out) + (ok ? orow : 0) * sg.ld + (n0 - sg.n_begin);
     if (!sg.rope) {
         #pragma unroll 1
@@ -179,8 +180,8 @@ __device__ __forceinline__ void epi_store(const GemmShape& sh, const GemmEpi& ep
 
 template <int BN>
 __device__ __forceinline__ void epi_resid(const GemmShape& sh, const GemmEpi& ep, uint32_t tbase,
-                                          int row, int n0) {
-    const bool ok = row < sh.M;
+                                          int row, int n0, int* ew) {
+    const bool ok = row < sh.M && DFL_IN_BOUNDS(ew, (n0 + BN < sh.N ? n0 + BN : sh.N) - 1, ep.ld_resid);
     const bool rd = !ep.resid_store;
     float* out = ep.resid + (int64_t)(ok ? row : 0) * ep.ld_resid + n0;
     #pragma unroll 1
@@ -212,8 +213,9 @@ __device__ __forceinline__ void epi_resid(const GemmShape& sh, const GemmEpi& ep
 
 template <int BN>
 __device__ __forceinline__ void epi_argmax(const GemmShape& sh, const GemmEpi& ep, uint32_t tbase,
-                                           int row, int n0, int tn) {
-    const bool ok = row < sh.M;
+                                           int row, int n0, int tn, int* ew) {
+    const bool ok = row < sh.M && DFL_IN_BOUNDS(ew, tn, sh.tiles_n) &&
+                    (!ep.logits || DFL_IN_BOUNDS(ew, (n0 + BN < sh.N ? n0 + BN : sh.N) - 1, ep.ld_logits));
     float best = -INFINITY;
     int bidx = n0;
     float* lg = ep.logits ? ep.logits + (int64_t)(ok ? row : 0) * ep.ld_logits : nullptr;
@@ -264,8 +266,10 @@ __device__ __forceinline__ void epi_argmax(const GemmShape& sh, const GemmEpi& e
 }
 
 template <int BN>
-__device__ __forceinline__ void epi_swiglu(const GemmShape& sh, const GemmEpi& ep, uint32_t tbase, int row, int tn) {
-    const bool ok = row < sh.M;
+__device__ __forceinline__ void epi_swiglu(const GemmShape& sh, const GemmEpi& ep, uint32_t tbase, int row, int tn,
+                                           int* ew) {
+    const bool ok = row < sh.M && DFL_IN_BOUNDS(ew, row, ep.seg[0].rows) &&
+                    DFL_IN_BOUNDS(ew, (tn + 1) * (BN / 2) - 1, ep.seg[0].ld);
     const GemmSeg sg = ep.seg[0];
     __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(sg.out) + (int64_t)(ok ? row : 0) * sg.ld + tn * (BN / 2);
     #pragma unroll 1
@@ -497,10 +501,10 @@ gemm_tc_kernel(const __grid_constant__ GemmProb p0, const __grid_constant__ Gemm
             const int row = (tmc * CM + (int)crank) * GEMM_BM + q * 32 + lane;
             const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN + part * COLS;
             const int n0 = tn * BN + part * COLS;
-            if (EPI == EPI_STORE) epi_store<COLS>(P->sh, P->ep, tbase, row, n0);
-            else if (EPI == EPI_RESID) epi_resid<COLS>(P->sh, P->ep, tbase, row, n0);
-            else if (EPI == EPI_SWIGLU) epi_swiglu<BN>(P->sh, P->ep, tbase, row, tn);   // one part: COLS == BN
-            else epi_argmax<BN>(P->sh, P->ep, tbase, row, tn * BN, tn);
+            if (EPI == EPI_STORE) epi_store<COLS>(P->sh, P->ep, tbase, row, n0, err.word);
+            else if (EPI == EPI_RESID) epi_resid<COLS>(P->sh, P->ep, tbase, row, n0, err.word);
+            else if (EPI == EPI_SWIGLU) epi_swiglu<BN>(P->sh, P->ep, tbase, row, tn, err.word);   // one part
+            else epi_argmax<BN>(P->sh, P->ep, tbase, row, tn * BN, tn, err.word);
             // every lane's tensor-memory reads are complete before the warp reports
             tc_fence_before();
             __syncwarp();

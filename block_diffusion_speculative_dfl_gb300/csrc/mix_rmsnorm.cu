@@ -335,7 +335,10 @@ __global__ void __launch_bounds__(MIX_THREADS, 1) mix_rmsnorm_bf16_kernel(const 
         {
             const uint8_t* src = stage + g0 * 32;
             __nv_bfloat16* dst = a.Xc + row * a.d + g0 * 16;
-            for (int l = 0; l < a.D; ++l) {
+            // the span's last element of the last layer lies inside the D output slabs
+            const bool in = DFL_IN_BOUNDS(err.word, (a.D - 1) * a.xc_stride + row * a.d + (g0 + ng) * 16 - 1,
+                                          (a.D - 1) * a.xc_stride + a.rows * a.d);
+            for (int l = 0; l < a.D && in; ++l) {
                 for (int c = lane; c < 2 * ng; c += 32)
                     *reinterpret_cast<uint4*>(dst + c * 8) = *reinterpret_cast<const uint4*>(src + c * 16);
                 src += P.slab;

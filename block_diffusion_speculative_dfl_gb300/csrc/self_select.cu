@@ -197,6 +197,7 @@ __global__ void streak_select_kernel(const int32_t* drafts, int N, int K, int G,
         const int i = __shfl_xor_sync(0xFFFFFFFFu, bk, o);
         if (v > best || (v == best && i < bk)) { best = v; bk = i; }
     }
+    if (bk >= K) bk = 0;   // no score compared greater (all NaN): draft 0, never an index past the drafts
     const int64_t r0 = ((int64_t)n * K + bk) * G1;
     const int32_t* x = drafts + ((int64_t)n * K + bk) * G;
     int a = G;

@@ -59,7 +59,10 @@ typedef enum dfl_status {
     DFL_ERR_WORKSPACE = 4,         /* ws_bytes smaller than dfl_workspace_size() */
     DFL_ERR_CUDA = 5,              /* a CUDA runtime call or launch failed */
     DFL_ERR_TIMEOUT = 6,           /* a device-side bounded wait ran out */
-    DFL_ERR_NO_DEVICE = 7          /* no sm_103a device is current */
+    DFL_ERR_NO_DEVICE = 7,         /* no sm_103a device is current */
+    DFL_ERR_BOUNDS = 8             /* (bounds-checked build, -DDFL_CHECK) a kernel computed an
+                                      index outside the extent its shape gives; the access was
+                                      skipped and the code recorded in the device error word */
 } dfl_status;
 
 typedef enum dfl_dtype { DFL_F32 = 0, DFL_BF16 = 1 } dfl_dtype;
