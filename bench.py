@@ -293,7 +293,16 @@ def host_params(w):
     W_fc, g_fc = gen_fc_weights(w) if w.fc else (None, None)
     return {"mix": gen_mix_logits(w), "g_mix": g_mix, "g_blk": g_blk, "g_fin": g_fin, "g_ffn": gen_ffn_gains(w),
             "layers": [gen_layer_weights(w, l) for l in range(w.D)],
-            "W_lm_bits": gen_lm_head(w, as_bits=True) if w.V > 0 else None, "W_fc": W_fc, "g_fc": g_fc}
+            # W_lm in the working dtype: bf16 storage bits, or fp32 values for an fp32 workload
+            "W_lm": gen_lm_head(w, as_bits=w.dtype == "bf16") if w.V > 0 else None, "W_fc": W_fc, "g_fc": g_fc}
+
+
+def lm_head_f32(w, p):
+    """The LM head as fp32 values (the oracle's input)."""
+    from dfl_synth import bits_to_f32
+    if w.V == 0:
+        return None
+    return bits_to_f32(p["W_lm"]) if w.dtype == "bf16" else p["W_lm"]
 
 
 def oracle_step(w, p, n, W_lm_f32, vlog_n=None):
@@ -346,8 +355,8 @@ def oracle_step_cached(w, p, n, W_lm_f32, vlog_n=None):
 
 
 def cpu_baseline(w, p, seqs):
-    from dfl_synth import bits_to_f32, gen_verifier_logits
-    W_lm = bits_to_f32(p["W_lm_bits"]) if w.V > 0 else None
+    from dfl_synth import gen_verifier_logits
+    W_lm = lm_head_f32(w, p)
     step = oracle_step_cached if w.R > 0 else oracle_step
     total = 0.0
     for n in seqs:
@@ -406,7 +415,10 @@ def run_ours(args, rank, world, local):
     shape = dfl.DraftShape(N=w.N, d=w.d, Hq=w.Hq, Hkv=w.Hkv, hd=w.hd, D=w.D, L=w.L, B=w.B, C=w.C, V=w.V,
                            dtype=w.dtype, K=w.K, T=w.T, seed=w.philox_seed, eps=w.eps, rope_theta=w.rope_theta,
                            F=w.F, fc=w.fc)
-    W_lm = (torch.from_numpy(p["W_lm_bits"].view(np.int16)).view(torch.bfloat16) if w.V > 0 else None)
+    W_lm = None
+    if w.V > 0:
+        W_lm = (torch.from_numpy(p["W_lm"].view(np.int16)).view(torch.bfloat16) if w.dtype == "bf16"
+                else torch.from_numpy(p["W_lm"]))
     cached = w.R > 0
     rule = {"greedy": 0, "stochastic": 1, "sampled": 2}[args.accept_rule] if w.K > 0 else 0
     kw = dict(tv=args.tv and w.K > 0, accept_rule=rule, accept_seed=w.philox_seed ^ 0xACCE97, ffn_gain=p["g_ffn"],
@@ -428,11 +440,13 @@ def run_ours(args, rank, world, local):
         n_new = n_host.cuda()
     else:
         model = dfl.DraftModel(shape, p["mix"], p["g_mix"], p["g_blk"], p["g_fin"], p["layers"], W_lm, **kw)
-        H_host = torch.from_numpy(gen_hidden(w, as_bits=True).view(np.int16)).view(torch.bfloat16)
+        H_host = (torch.from_numpy(gen_hidden(w, as_bits=True).view(np.int16)).view(torch.bfloat16)
+                  if w.dtype == "bf16" else torch.from_numpy(gen_hidden(w)))
     H = H_host.cuda()
     vlog_host = vlog = None
     if w.K > 0:
-        vlog_host = torch.from_numpy(gen_verifier_logits(w, as_bits=True).view(np.int16)).view(torch.bfloat16)
+        vlog_host = (torch.from_numpy(gen_verifier_logits(w, as_bits=True).view(np.int16)).view(torch.bfloat16)
+                     if w.dtype == "bf16" else torch.from_numpy(gen_verifier_logits(w)))
         vlog = vlog_host.cuda()
 
     def run_step(target=None):
@@ -651,10 +665,10 @@ def run_reference(args, rank, world):
     """The fp64 CPU oracle on the same workload, one sequence per step."""
     if rank != 0:
         return
-    from dfl_synth import bits_to_f32, gen_verifier_logits
+    from dfl_synth import gen_verifier_logits
     w = workload(args.workload, 0, args.batch, args.context)
     p = host_params(w)
-    W_lm = bits_to_f32(p["W_lm_bits"]) if w.V > 0 else None
+    W_lm = lm_head_f32(w, p)
     times = []
     step = oracle_step_cached if w.R > 0 else oracle_step
     for i in range(args.warmup + args.steps):

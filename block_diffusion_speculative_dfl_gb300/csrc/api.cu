@@ -377,11 +377,15 @@ dfl_status dual_kv_proj_bf16(DeviceCtx* ctx, const void* Xc, int64_t ctx_M, int 
                              int B, int d, const float* blk_gain, float eps, const void* Wq, const void* Wkc,
                              const void* Wvc, const void* Wkb, const void* Wvb, int Hq, int Hkv, int hd,
                              const float* rope, void* Q, void* Kc, void* Vc, void* Kb, void* Vb, void* ws,
-                             const KvRowPlan* plan, cudaStream_t st) {
+                             const KvRowPlan* plan, cudaStream_t st, const float* Xb_init = nullptr) {
     const int kv = Hkv * hd, qd = Hq * hd;
     dfl_status rc;
     void* Xn = ws;
-    if ((rc = rmsnorm_rows(Xb, d, (int64_t)N * B, 1, 1, 0, blk_gain, eps, Xn, true, st)) != DFL_OK) return rc;
+    // With Xb_init the block's initial features are normalised from there and
+    // copied into the residual stream Xb by the same kernel (a step's first layer).
+    if ((rc = rmsnorm_rows(Xb_init ? Xb_init : Xb, d, (int64_t)N * B, 1, 1, 0, blk_gain, eps, Xn, true, st,
+                           Xb_init ? const_cast<float*>(Xb) : nullptr)) != DFL_OK)
+        return rc;
 
     // block rows: [Q | Kb | Vb] = Xn [Wq ; Wkb ; Wvb]^T
     GemmArgs gb{};
@@ -809,11 +813,15 @@ dfl_status draft_step_impl(const dfl_step_args* a, const dfl_ctx_cache* cache, v
     uint8_t* sub = p;
     const size_t sub_bytes = ws_bytes - (size_t)(sub - static_cast<uint8_t*>(ws));
 
-    {
-    ProfScope ps("copy_block_init", st);
-    if (cudaMemcpyAsync(a->Xb, a->Xb0, (size_t)N * B * d * sizeof(float), cudaMemcpyDeviceToDevice, st) !=
-        cudaSuccess)
-        return DFL_ERR_CUDA;
+    // bf16: the first layer's block RMSNorm reads Xb0 and copies it into the
+    // residual stream Xb; fp32: a device copy first.
+    const bool bf = dt == DFL_BF16;
+    if (bf && (rc = step_bf16_shape(a)) != DFL_OK) return rc;
+    if (!bf) {
+        ProfScope ps("copy_block_init", st);
+        if (cudaMemcpyAsync(a->Xb, a->Xb0, (size_t)N * B * d * sizeof(float), cudaMemcpyDeviceToDevice, st) !=
+            cudaSuccess)
+            return DFL_ERR_CUDA;
     }
     if (cache &&
         (rc = cache_plan(N, R, B, C, cache->ctx_len, cache->n_new, cache->advance, const_cast<int32_t*>(plan.ctx_pos),
@@ -838,16 +846,22 @@ dfl_status draft_step_impl(const dfl_step_args* a, const dfl_ctx_cache* cache, v
             void* Vl = static_cast<uint8_t*>(cache->V) + (size_t)l * cache->layer_stride * 2;
             if ((rc = dual_kv_proj_bf16(dctx, xc_l, ctx_rows, R, a->Xb, N, B, d, a->blk_gain + (size_t)l * d, a->eps,
                                         w.Wq, w.Wkc, w.Wvc, w.Wkb, w.Wvb, a->Hq, a->Hkv, a->hd, a->rope, Q, Kl, Vl,
-                                        Kb, Vb, sub, &plan, st)) != DFL_OK)
+                                        Kb, Vb, sub, &plan, st, l == 0 ? a->Xb0 : nullptr)) != DFL_OK)
                 return rc;
             if ((rc = block_attn_bf16(dctx, Q, Kl, Vl, Kb, Vb, N, C, B, a->Hq, a->Hkv, a->hd, w.Wo, d, a->Xb, sub,
                                       len_new, C, st)) != DFL_OK)
                 return rc;
         } else {
-            if ((rc = dfl_dual_kv_proj(xc_l, a->Xb, N, C, B, d, ddt, a->blk_gain + (size_t)l * d, a->eps, w.Wq,
-                                       w.Wkc, w.Wvc, w.Wkb, w.Wvb, a->Hq, a->Hkv, a->hd, a->rope, Q, Kc, Vc, Kb, Vb,
-                                       sub, sub_bytes, stream)) != DFL_OK)
+            if (bf) {
+                if ((rc = dual_kv_proj_bf16(dctx, xc_l, (int64_t)N * C, C, a->Xb, N, B, d, a->blk_gain + (size_t)l * d,
+                                            a->eps, w.Wq, w.Wkc, w.Wvc, w.Wkb, w.Wvb, a->Hq, a->Hkv, a->hd, a->rope, Q,
+                                            Kc, Vc, Kb, Vb, sub, nullptr, st, l == 0 ? a->Xb0 : nullptr)) != DFL_OK)
+                    return rc;
+            } else if ((rc = dfl_dual_kv_proj(xc_l, a->Xb, N, C, B, d, ddt, a->blk_gain + (size_t)l * d, a->eps, w.Wq,
+                                              w.Wkc, w.Wvc, w.Wkb, w.Wvb, a->Hq, a->Hkv, a->hd, a->rope, Q, Kc, Vc, Kb,
+                                              Vb, sub, sub_bytes, stream)) != DFL_OK) {
                 return rc;
+            }
             if ((rc = dfl_block_attn(Q, Kc, Vc, Kb, Vb, N, C, B, a->Hq, a->Hkv, a->hd, ddt, w.Wo, d, a->Xb, sub,
                                      sub_bytes, stream)) != DFL_OK)
                 return rc;

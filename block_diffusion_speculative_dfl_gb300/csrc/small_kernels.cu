@@ -40,7 +40,7 @@ constexpr int RN_MAXV = 12;   // float4 per thread -> d <= 6144
 template <typename OutT>
 __global__ void __launch_bounds__(RN_THREADS) rmsnorm_rows_kernel(const float* in, int d, int64_t M, int per,
                                                                   int stride, int off, const float* gain, float eps,
-                                                                  OutT* out) {
+                                                                  OutT* out, float* copy) {
     const int64_t m = blockIdx.x;
     const int tid = threadIdx.x;
     const int64_t src = (m / per) * stride + off + m % per;
@@ -53,6 +53,12 @@ __global__ void __launch_bounds__(RN_THREADS) rmsnorm_rows_kernel(const float* i
         const int e = tid + j * RN_THREADS;
         v[j] = e < nv ? x[e] : make_float4(0.f, 0.f, 0.f, 0.f);
         ss += v[j].x * v[j].x + v[j].y * v[j].y + v[j].z * v[j].z + v[j].w * v[j].w;
+    }
+    if (copy) {   // the input row, unchanged, to the same row of `copy`
+        float4* c4 = reinterpret_cast<float4*>(copy + src * d);
+        #pragma unroll
+        for (int j = 0; j < RN_MAXV; ++j)
+            if (tid + j * RN_THREADS < nv) c4[tid + j * RN_THREADS] = v[j];
     }
     __shared__ float red[RN_THREADS / 32];
     ss = warp_sum(ss);
@@ -84,16 +90,16 @@ __global__ void __launch_bounds__(RN_THREADS) rmsnorm_rows_kernel(const float* i
 }
 
 dfl_status rmsnorm_rows(const float* in, int d, int64_t M, int per, int stride, int off, const float* gain,
-                        float eps, void* out, bool bf16, cudaStream_t st) {
+                        float eps, void* out, bool bf16, cudaStream_t st, float* copy) {
     if (d > RN_THREADS * 4 * RN_MAXV || d % 4 != 0) return DFL_ERR_UNSUPPORTED_SHAPE;
     if (M > 0x7FFFFFFF) return DFL_ERR_UNSUPPORTED_SHAPE;
     ProfScope ps("rmsnorm_rows", st);
     if (bf16)
         rmsnorm_rows_kernel<__nv_bfloat16><<<(unsigned)M, RN_THREADS, 0, st>>>(in, d, M, per, stride, off, gain, eps,
-                                                                               static_cast<__nv_bfloat16*>(out));
+                                                                               static_cast<__nv_bfloat16*>(out), copy);
     else
         rmsnorm_rows_kernel<float><<<(unsigned)M, RN_THREADS, 0, st>>>(in, d, M, per, stride, off, gain, eps,
-                                                                       static_cast<float*>(out));
+                                                                       static_cast<float*>(out), copy);
     return last_launch();
 }
 

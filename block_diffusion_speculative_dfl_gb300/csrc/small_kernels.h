@@ -12,8 +12,9 @@ struct DevErr;
 
 dfl_status rope_table(float* table, int P, int hd, double theta, cudaStream_t st);
 // out[m] = RMSNorm(in[(m / per) * stride + off + m % per]) * gain; bf16 or fp32 out.
+// copy (nullable): each input row is also written, unchanged, to the same row of copy.
 dfl_status rmsnorm_rows(const float* in, int d, int64_t M, int per, int stride, int off, const float* gain,
-                        float eps, void* out, bool bf16, cudaStream_t st);
+                        float eps, void* out, bool bf16, cudaStream_t st, float* copy = nullptr);
 // Row plan of a cached draft step: per-row positions and cache rows of the
 // new context rows, block positions and the attended context lengths.
 dfl_status cache_plan(int N, int R, int B, int C, int32_t* ctx_len, const int32_t* n_new, int advance,
