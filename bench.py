@@ -31,6 +31,8 @@ import numpy as np  # noqa: E402
 METRIC = "drafted block-tokens/sec on 1 GB300 (+accept epilogue); % of HBM/tensor roofline"
 UNIT = "block-tokens/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# fp32 FMA on the CUDA cores (the fp32 path's GEMMs): 152 SMs x 128 lanes x 2 flop x 2.07 GHz, nominal
+FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 L2_FLUSH_BYTES = 256 << 20
 
 
@@ -191,6 +193,13 @@ def kernel_work(w, ctx_lens=None):
     if V > 0:
         M = N * (B - 1)
         work["gemm_lm_head"] = (2.0 * M * V * d, 2.0 * (M * d + V * d) + (4.0 * M * V if w.K > 0 else 0.0))
+    if w.dtype == "f32":   # CUDA-core path: the average fp32 GEMM launch of a step, and the attention
+        M = N * (B - 1)
+        gemm = D * (2.0 * rows_b * (qd + 2 * kv) * d + 2.0 * rows_c * 2 * kv * d + 2.0 * rows_b * d * qd)
+        gemm += 2.0 * D * rows_b * 3 * w.F * d + (2.0 * M * V * d if V > 0 else 0.0)
+        n_gemm = D * (6 + (3 if w.F > 0 else 0)) + (1 if V > 0 else 0)
+        work["gemm_f32"] = (gemm / n_gemm, 0.0)
+        work["attn_f32"] = (4.0 * B * Hq * keys * hd, 4.0 * (2 * keys * kv + 2 * rows_b * qd))
     if w.K > 0:
         G = B - 1
         work["verifier_row_stats"] = (0.0, 2.0 * N * w.K * B * V)
@@ -226,6 +235,12 @@ def kernel_table(prof, work, peaks, tkey):
         ent = {"launches": n_l, "ms_per_launch": round(per, 5), "share": round(tot / traced, 4)}
         if name in work:
             fl, by = work[name]
+            if name.endswith("_f32") and by == 0.0:   # fp32 FMA on the CUDA cores
+                ent["bound"] = "alu"
+                ent["achieved"] = round(fl / (per / 1e3) / 1e12, 3)
+                ent["frac"] = round(ent["achieved"] / FP32_ALU_TFLOPS, 4)
+                kernels[name] = ent
+                continue
             tensor = fl / (peaks[tkey] * 1e12) >= by / (peaks["hbm_gbs"] * 1e9)
             ent["bound"] = "tensor" if tensor else "hbm"
             ent["achieved"] = round(fl / (per / 1e3) / 1e12, 2) if tensor else round(by / (per / 1e3) / 1e9, 1)
@@ -520,13 +535,16 @@ def run_ours(args, rank, world, local):
     kernels = kernel_table(prof, work, peaks, tkey)
     dom = next(k for k in kernels if k in work)
     de = kernels[dom]
+    peak_of = {"tensor": peaks[tkey], "hbm": peaks["hbm_gbs"], "alu": FP32_ALU_TFLOPS}
     roofline = {"kernel": dom, "bound": de["bound"], "achieved": de["achieved"],
-                "peak": peaks[tkey] if de["bound"] == "tensor" else peaks["hbm_gbs"],
-                "unit": "TFLOP/s" if de["bound"] == "tensor" else "GB/s", "frac": de["frac"],
+                "peak": round(peak_of[de["bound"]], 1),
+                "unit": "GB/s" if de["bound"] == "hbm" else "TFLOP/s", "frac": de["frac"],
                 "traffic": ncu_traffic(dom, w.name),
                 "peak_source": (f"{peak_src} ({'bf16 dense ' + ('burst' if tkey == 'bf16_tflops' else 'sustained')}"
-                                f": {why})" if de["bound"] == "tensor" else f"{peak_src} (HBM copy)"),
-                "algorithmic_per_launch": work[dom][0] if de["bound"] == "tensor" else work[dom][1]}
+                                f": {why})" if de["bound"] == "tensor" else
+                                "nominal fp32 FMA rate: 152 SMs x 128 lanes x 2 flop x 2.07 GHz"
+                                if de["bound"] == "alu" else f"{peak_src} (HBM copy)"),
+                "algorithmic_per_launch": work[dom][1] if de["bound"] == "hbm" else work[dom][0]}
     if de["bound"] == "tensor":   # both fractions, the chosen one in "frac"
         roofline["frac_burst"] = round(de["achieved"] / peaks["bf16_tflops"], 4)
         roofline["frac_sustained"] = round(de["achieved"] / peaks["bf16_tflops_sustained"], 4)
