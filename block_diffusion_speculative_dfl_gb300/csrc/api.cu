@@ -103,9 +103,15 @@ uint64_t wait_limit_ns() { return g_wait_ns.load(); }
 
 size_t ws_dual_kv_proj(int N, int B, int d, int dt) { return al256((size_t)N * B * d * esz(dt)); }
 
-size_t ws_block_attn(int N, int C, int B, int Hq, int Hkv, int hd, int dt, bool ragged = false) {
+// fp32 partials of the output projection's K-split when the N*B block rows
+// fit one M-tile (up to 8 splits of [rows][d]); 0 when d is not given.
+size_t ws_oproj_split(int64_t rows, int d) { return (d > 0 && rows <= 128) ? al256((size_t)8 * rows * d * 4) : 0; }
+
+// The attention output and scratch, then (optional: used when the caller's
+// workspace holds it) room for the output projection's K-split partials.
+size_t ws_block_attn(int N, int C, int B, int Hq, int Hkv, int hd, int dt, bool ragged = false, int d = 0) {
     size_t b = al256((size_t)N * B * Hq * hd * esz(dt));
-    if (dt == DFL_BF16) b += al256(attn_ws_bytes(N, C, B, Hq, Hkv, hd, ragged));
+    if (dt == DFL_BF16) b += al256(attn_ws_bytes(N, C, B, Hq, Hkv, hd, ragged)) + ws_oproj_split((int64_t)N * B, d);
     return b;
 }
 
@@ -155,7 +161,7 @@ size_t step_ws_bytes(const dfl_shape& s, bool cached) {
     b += 2 * al256((size_t)s.N * s.B * s.Hkv * s.hd * e);                    // Kb, Vb
     if (cached) b += 2 * al256((size_t)rows * 4) + al256((size_t)s.N * s.B * 4) + al256((size_t)s.N * 4);
     size_t sub = ws_dual_kv_proj(s.N, s.B, s.d, s.dtype);
-    sub = std::max(sub, ws_block_attn(s.N, s.C, s.B, s.Hq, s.Hkv, s.hd, s.dtype, cached));
+    sub = std::max(sub, ws_block_attn(s.N, s.C, s.B, s.Hq, s.Hkv, s.hd, s.dtype, cached, s.d));
     if (s.F > 0) sub = std::max(sub, ws_block_ffn(s.N, s.B, s.d, s.F, s.dtype));
     if (s.V > 0) {
         sub = std::max(sub, ws_lm_head(s.N, s.B, 1, s.d, s.V, s.dtype, true));
@@ -202,7 +208,7 @@ extern "C" size_t dfl_workspace_size(dfl_op op, const dfl_shape* s) {
         if (v < 0) return 0;
     switch (op) {
         case DFL_OP_DUAL_KV_PROJ: return ws_dual_kv_proj(s->N, s->B, s->d, s->dtype);
-        case DFL_OP_BLOCK_ATTN: return ws_block_attn(s->N, s->C, s->B, s->Hq, s->Hkv, s->hd, s->dtype);
+        case DFL_OP_BLOCK_ATTN: return ws_block_attn(s->N, s->C, s->B, s->Hq, s->Hkv, s->hd, s->dtype, false, s->d);
         case DFL_OP_LM_HEAD:
             if (s->row0 < 0 || s->row0 >= s->B || s->V <= 0) return 0;
             return ws_lm_head(s->N, s->B, s->row0, s->d, s->V, s->dtype, s->dtype == DFL_F32);
@@ -416,8 +422,8 @@ dfl_status dual_kv_proj_bf16(DeviceCtx* ctx, const void* Xc, int64_t ctx_M, int 
 // and C_stride the context rows per sequence of Kc / Vc.
 dfl_status block_attn_bf16(DeviceCtx* ctx, const void* Q, const void* Kc, const void* Vc, const void* Kb,
                            const void* Vb, int N, int C, int B, int Hq, int Hkv, int hd, const void* Wo, int d,
-                           float* Xb, void* ws, const int32_t* ctx_len, int C_stride, cudaStream_t st,
-                           int policy_N = 0) {
+                           float* Xb, void* ws, size_t ws_bytes, const int32_t* ctx_len, int C_stride,
+                           cudaStream_t st, int policy_N = 0) {
     const int qd = Hq * hd;
     dfl_status rc;
     uint8_t* p = static_cast<uint8_t*>(ws);
@@ -432,6 +438,15 @@ dfl_status block_attn_bf16(DeviceCtx* ctx, const void* Q, const void* Kc, const 
     g.epi = EPI_RESID;
     g.ep.resid = Xb; g.ep.ld_resid = d;
     g.tag = "gemm_o_proj";
+    // With few block rows the projection streams Wo through a few CTAs: when
+    // the workspace has room, it is split along K (partials after the
+    // attention's scratch) and summed in a fixed order.
+    const size_t base = ws_block_attn(N, C, B, Hq, Hkv, hd, DFL_BF16, ctx_len != nullptr);
+    const size_t room = ws_oproj_split((int64_t)N * B, d);
+    if (room > 0 && ws_bytes >= base + room) {
+        g.split_part = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + base);
+        g.split_part_bytes = room;
+    }
     return gemm_tc(ctx, g, st);
 }
 
@@ -537,7 +552,7 @@ extern "C" dfl_status dfl_block_attn(const void* Q, const void* Kc, const void* 
     }
     if (hd != 64 && hd != 128) return DFL_ERR_UNSUPPORTED_SHAPE;
     if (d % 32 != 0) return DFL_ERR_UNSUPPORTED_SHAPE;
-    return block_attn_bf16(ctx, Q, Kc, Vc, Kb, Vb, N, C, B, Hq, Hkv, hd, Wo, d, Xb, ws, nullptr, C, st);
+    return block_attn_bf16(ctx, Q, Kc, Vc, Kb, Vb, N, C, B, Hq, Hkv, hd, Wo, d, Xb, ws, ws_bytes, nullptr, C, st);
 }
 
 // ------------------------------------------------------- feed-forward
@@ -849,7 +864,7 @@ dfl_status draft_step_impl(const dfl_step_args* a, const dfl_ctx_cache* cache, v
                                         Kb, Vb, sub, &plan, st, l == 0 ? a->Xb0 : nullptr)) != DFL_OK)
                 return rc;
             if ((rc = block_attn_bf16(dctx, Q, Kl, Vl, Kb, Vb, N, C, B, a->Hq, a->Hkv, a->hd, w.Wo, d, a->Xb, sub,
-                                      len_new, C, st)) != DFL_OK)
+                                      sub_bytes, len_new, C, st)) != DFL_OK)
                 return rc;
         } else {
             if (bf) {
@@ -1038,7 +1053,8 @@ dfl_status draft_step_host_impl(const dfl_step_args* a, void* H_dev, int chunks,
                                         nullptr, Kb, Vb, sub, nullptr, st)) != DFL_OK)
                 return rc;
             if ((rc = block_attn_bf16(dctx, Q, kc_of(l) + (size_t)r0 * kv * 2, vc_of(l) + (size_t)r0 * kv * 2, Kb, Vb,
-                                      Nc, C, B, a->Hq, a->Hkv, a->hd, w.Wo, d, Xb_c, sub, nullptr, C, st, N)) != DFL_OK)
+                                      Nc, C, B, a->Hq, a->Hkv, a->hd, w.Wo, d, Xb_c, sub, sub_bytes, nullptr, C, st,
+                                      N)) != DFL_OK)
                 return rc;
             if (a->F > 0 && (rc = dfl_block_ffn(Xb_c, Nc, B, d, DFL_BF16, a->ffn_gain + (size_t)l * d, a->eps, w.W1,
                                                 w.W3, w.W2, a->F, sub, sub_bytes, stream)) != DFL_OK)
@@ -1062,7 +1078,7 @@ dfl_status draft_step_host_impl(const dfl_step_args* a, void* H_dev, int chunks,
                                     Vb, sub, nullptr, st)) != DFL_OK)
             return rc;
         if ((rc = block_attn_bf16(dctx, Q, kc_of(l), vc_of(l), Kb, Vb, N, C, B, a->Hq, a->Hkv, a->hd, w.Wo, d, a->Xb,
-                                  sub, nullptr, C, st)) != DFL_OK)
+                                  sub, sub_bytes, nullptr, C, st)) != DFL_OK)
             return rc;
         if (a->F > 0 && (rc = dfl_block_ffn(a->Xb, N, B, d, DFL_BF16, a->ffn_gain + (size_t)l * d, a->eps, w.W1,
                                             w.W3, w.W2, a->F, sub, sub_bytes, stream)) != DFL_OK)

@@ -61,8 +61,8 @@ dfl_status launch(DeviceCtx* ctx, const GemmProb& p0, const GemmProb& p1, int np
             return DFL_ERR_CUDA;
         ctx->gemm_attr_set[slot] = true;
     }
-    int tiles = ((p0.sh.tiles_m + CM - 1) / CM) * p0.sh.tiles_n;
-    if (nprob > 1) tiles += ((p1.sh.tiles_m + CM - 1) / CM) * p1.sh.tiles_n;
+    int tiles = ((p0.sh.tiles_m + CM - 1) / CM) * p0.sh.tiles_n * p0.sh.ksplit;
+    if (nprob > 1) tiles += ((p1.sh.tiles_m + CM - 1) / CM) * p1.sh.tiles_n * p1.sh.ksplit;
     const int max_clusters = ctx->sm_count / CM;
     const int grid = (tiles < max_clusters ? tiles : max_clusters) * CM;
     cudaLaunchConfig_t cfg = {};
@@ -148,6 +148,9 @@ static dfl_status build_prob(const GemmArgs& g, int cm, GemmProb& P) {
     sh.m_inner = g.m_inner;
     sh.nb = g.nb;
     sh.split_b = g.split_b;
+    sh.ksplit = 1;
+    sh.kb_split = sh.num_kb;
+    sh.part_stride = 0;
     if (g.split_b && (g.nb != 2 || (g.N / 2) % (g.bn / 2) != 0)) return DFL_ERR_UNSUPPORTED_SHAPE;
     if (g.a_slabs > 0) {
         const int w = g.K / g.a_slabs;
@@ -190,16 +193,68 @@ static dfl_status launch_probs(DeviceCtx* ctx, const GemmProb& p0, const GemmPro
     return launch_cm<128, EPI_ARGMAX>(ctx, p0, p1, nprob, tag, st, slot, cm);
 }
 
+// out[m][n] += sum over s of part[s][m][n], s in order (one thread per four
+// columns; N a multiple of 4).
+__global__ void splitk_reduce_kernel(const float* part, int S, int64_t stride, int M, int N, float* out,
+                                     int64_t ld) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;   // float4 index over M x N
+    const int64_t per_row = N / 4;
+    if (i >= (int64_t)M * per_row) return;
+    const int64_t m = i / per_row, c = (i % per_row) * 4;
+    float4 acc = *reinterpret_cast<const float4*>(part + m * N + c);
+    for (int s = 1; s < S; ++s) {
+        const float4 v = *reinterpret_cast<const float4*>(part + s * stride + m * N + c);
+        acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+    }
+    float4* o = reinterpret_cast<float4*>(out + m * ld + c);
+    float4 r = *o;
+    r.x += acc.x; r.y += acc.y; r.z += acc.z; r.w += acc.w;
+    *o = r;
+}
+
+// K-splits of a residual GEMM with a single M-tile (a few rows streaming a
+// large weight): enough splits to spread the weight over the SMs, at least
+// eight k-blocks each; 1 when the GEMM does not qualify or the partials do
+// not fit the caller's buffer.
+static int pick_ksplit(const GemmArgs& g, int sm_count) {
+    if (g.epi != EPI_RESID || !g.split_part || g.ep.resid_store || g.N % 4 != 0) return 1;
+    if ((g.M + GEMM_BM - 1) / GEMM_BM != 1) return 1;
+    const int tiles = (g.N + g.bn - 1) / g.bn;
+    const int num_kb = (g.K + GEMM_BK - 1) / GEMM_BK;
+    int s = sm_count / tiles;
+    s = s < 8 ? s : 8;
+    s = s < num_kb / 8 ? s : num_kb / 8;
+    while (s > 1 && (size_t)s * g.M * g.N * sizeof(float) > g.split_part_bytes) --s;
+    return s > 1 ? s : 1;
+}
+
 dfl_status gemm_tc(DeviceCtx* ctx, const GemmArgs& g_in, cudaStream_t st) {
     GemmArgs g = g_in;
     if (g.bn == 0) g.bn = pick_bn(g, ctx->sm_count);
     // Pair the M-tiles of each N-tile over two SMs (a 256-row tile of
     // cta_group::2 products) when there is more than one M-tile.
     const int cm = (g.M + GEMM_BM - 1) / GEMM_BM >= 2 ? 2 : 1;
+    const int ksplit = cm == 1 ? pick_ksplit(g, ctx->sm_count) : 1;
+    GemmArgs gk = g;
+    if (ksplit > 1) {   // each split stores its fp32 partial; a fixed-order sum then adds them to the output
+        gk.ep.resid = g.split_part;
+        gk.ep.ld_resid = g.N;
+        gk.ep.resid_store = 1;
+    }
     GemmProb P;
-    dfl_status rc = build_prob(g, cm, P);
+    dfl_status rc = build_prob(gk, cm, P);
     if (rc != DFL_OK) return rc;
-    return launch_probs(ctx, P, P, 1, g.bn, g.epi, cm, g.tag, st);
+    if (ksplit > 1) {
+        P.sh.ksplit = ksplit;
+        P.sh.kb_split = (P.sh.num_kb + ksplit - 1) / ksplit;
+        P.sh.part_stride = (int64_t)g.M * g.N;
+    }
+    if ((rc = launch_probs(ctx, P, P, 1, g.bn, g.epi, cm, g.tag, st)) != DFL_OK || ksplit == 1) return rc;
+    ProfScope ps("splitk_reduce", st);
+    const int64_t n4 = (int64_t)g.M * (g.N / 4);
+    splitk_reduce_kernel<<<(unsigned)((n4 + 255) / 256), 256, 0, st>>>(g.split_part, ksplit, (int64_t)g.M * g.N, g.M,
+                                                                       g.N, g.ep.resid, g.ep.ld_resid);
+    return last_launch();
 }
 
 // Two independent GEMMs in one launch (same epilogue kind; problem 0's tiles

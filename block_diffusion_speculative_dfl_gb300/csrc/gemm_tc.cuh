@@ -63,6 +63,13 @@ struct GemmShape {
     int nb;              // number of B tensor maps
     int split_b;         // B tile = [BN/2 rows of map 0 ; BN/2 rows of map 1] at rows tn * BN/2
     int a_kb_per_slab;   // > 0: A is a 3-D map [slabs][M][K / slabs]; k-block kb reads slab kb / a_kb_per_slab
+    // split K (EPI_RESID only): output tile (tmc, tn) is computed by ksplit
+    // consecutive tiles of the sequence, split s over k-blocks
+    // [s * kb_split, min(num_kb, (s + 1) * kb_split)), each storing its fp32
+    // partial at resid + s * part_stride (a fixed-order reduction follows)
+    int ksplit;
+    int kb_split;
+    int64_t part_stride;
 };
 
 // One GEMM of a launch: its tensor maps (A, up to three B segments), shape and
@@ -104,10 +111,19 @@ struct GemmCfg {
     static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
 };
 
-// Tile t of a (tiles_mc x tiles_n) grid of cluster tiles, in walking order.
-__device__ __forceinline__ void tile_coords(const GemmShape& sh, int tiles_mc, int t, int& tmc, int& tn) {
+// Tile t of a (tiles_mc x tiles_n) grid of cluster tiles (x ksplit K-splits,
+// the splits of one output tile consecutive), in walking order.
+__device__ __forceinline__ void tile_coords(const GemmShape& sh, int tiles_mc, int t, int& tmc, int& tn, int& ks) {
+    ks = t % sh.ksplit;
+    t /= sh.ksplit;
     if (sh.m_inner) { tmc = t % tiles_mc; tn = t / tiles_mc; }
     else            { tn = t % sh.tiles_n; tmc = t / sh.tiles_n; }
+}
+
+// k-blocks [kb0, kb1) of split ks
+__device__ __forceinline__ void split_range(const GemmShape& sh, int ks, int& kb0, int& kb1) {
+    kb0 = ks * sh.kb_split;
+    kb1 = kb0 + sh.kb_split < sh.num_kb ? kb0 + sh.kb_split : sh.num_kb;
 }
 
 __device__ __forceinline__ void store_bf16x32(void* dst, const float (&v)[32]) {
@@ -180,10 +196,10 @@ __device__ __forceinline__ void epi_store(const GemmShape& sh, const GemmEpi& ep
 
 template <int BN>
 __device__ __forceinline__ void epi_resid(const GemmShape& sh, const GemmEpi& ep, uint32_t tbase,
-                                          int row, int n0, int* ew) {
+                                          int row, int n0, int* ew, int ks) {
     const bool ok = row < sh.M && DFL_IN_BOUNDS(ew, (n0 + BN < sh.N ? n0 + BN : sh.N) - 1, ep.ld_resid);
     const bool rd = !ep.resid_store;
-    float* out = ep.resid + (int64_t)(ok ? row : 0) * ep.ld_resid + n0;
+    float* out = ep.resid + ks * sh.part_stride + (int64_t)(ok ? row : 0) * ep.ld_resid + n0;
     #pragma unroll 1
     for (int c = 0; c < BN / 32; c += 2) {
         const bool in0 = ok && n0 + c * 32 < sh.N, in1 = ok && n0 + c * 32 + 32 < sh.N;
@@ -325,12 +341,12 @@ gemm_tc_kernel(const __grid_constant__ GemmProb p0, const __grid_constant__ Gemm
     const int cid = blockIdx.x / CM, nclusters = gridDim.x / CM;
     // cluster tiles of each problem; tile t of the launch belongs to problem 0 if t < T0
     const int tmc0 = (p0.sh.tiles_m + CM - 1) / CM, tmc1 = (p1.sh.tiles_m + CM - 1) / CM;
-    const int T0 = tmc0 * p0.sh.tiles_n;
-    const int total = T0 + (nprob > 1 ? tmc1 * p1.sh.tiles_n : 0);
-    auto locate = [&](int t, const GemmProb*& P, int& tmc, int& tn) {
+    const int T0 = tmc0 * p0.sh.tiles_n * p0.sh.ksplit;
+    const int total = T0 + (nprob > 1 ? tmc1 * p1.sh.tiles_n * p1.sh.ksplit : 0);
+    auto locate = [&](int t, const GemmProb*& P, int& tmc, int& tn, int& ks) {
         const bool second = t >= T0;
         P = second ? &p1 : &p0;
-        tile_coords(P->sh, second ? tmc1 : tmc0, second ? t - T0 : t, tmc, tn);
+        tile_coords(P->sh, second ? tmc1 : tmc0, second ? t - T0 : t, tmc, tn, ks);
     };
     // shared::cluster address of barrier `b` of this CTA in CTA `rank`
     auto at = [](const uint64_t* b, uint32_t rank) { return mapa_shared(smem_u32(b), rank); };
@@ -367,15 +383,16 @@ gemm_tc_kernel(const __grid_constant__ GemmProb p0, const __grid_constant__ Gemm
             bool aborted = false;
             for (int t = cid; t < total && !aborted; t += nclusters) {
                 const GemmProb* P;
-                int tmc, tn;
-                locate(t, P, tmc, tn);
+                int tmc, tn, ks, kb0, kb1;
+                locate(t, P, tmc, tn, ks);
                 const GemmShape& sh = P->sh;
+                split_range(sh, ks, kb0, kb1);
                 const int m0 = (tmc * CM + (int)crank) * GEMM_BM, n0 = tn * BN;
                 const CUtensorMap* mb = &P->b[0];
                 int nb0 = n0;
                 if (sh.nb > 2 && n0 >= sh.b_begin[2]) { mb = &P->b[2]; nb0 = n0 - sh.b_begin[2]; }
                 else if (sh.nb > 1 && n0 >= sh.b_begin[1]) { mb = &P->b[1]; nb0 = n0 - sh.b_begin[1]; }
-                for (int kb = 0; kb < sh.num_kb; ++kb) {
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (*abort_flag || !mbar_wait(&empty[stage], phase ^ 1, err)) { aborted = true; break; }
                     const int ax = (sh.a_kb_per_slab ? kb % sh.a_kb_per_slab : kb) * GEMM_BK;
                     const int az = sh.a_kb_per_slab ? kb / sh.a_kb_per_slab : 0;   // A slab (3-D map)
@@ -437,24 +454,27 @@ gemm_tc_kernel(const __grid_constant__ GemmProb p0, const __grid_constant__ Gemm
             bool aborted = false;
             bool issued = false;
             for (int t = cid; t < total && !aborted; t += nclusters) {
-                const int num_kb = (t >= T0 ? p1 : p0).sh.num_kb;
+                const GemmShape& shp = (t >= T0 ? p1 : p0).sh;
+                int kb0, kb1;
+                split_range(shp, (t >= T0 ? t - T0 : t) % shp.ksplit, kb0, kb1);
                 if (*abort_flag || !mbar_wait(&tempty[acc], acc_phase ^ 1, err)) { aborted = true; break; }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
-                for (int kb = 0; kb < num_kb; ++kb) {
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (*abort_flag || !mbar_wait(&full[stage], phase, err)) { aborted = true; break; }
                     tc_fence_after();
                     const uint64_t ad = sw128_desc(smem_u32(sA + stage * Cfg::A_BYTES));
                     const uint64_t bd = sw128_desc(smem_u32(sB + stage * Cfg::B_BYTES));
                     #pragma unroll
                     for (int k = 0; k < GEMM_BK / 16; ++k) {
+                        const uint32_t accum = (kb != kb0 || k != 0);
                         if (CM == 1) {
-                            mma_bf16(d_tmem, ad + 2 * k, bd + 2 * k, idesc, (kb | k) != 0);
+                            mma_bf16(d_tmem, ad + 2 * k, bd + 2 * k, idesc, accum);
                         } else {
-                            mma_bf16_pair(d_tmem, ad + 2 * k, bd + 2 * k, idesc, (kb | k) != 0);
+                            mma_bf16_pair(d_tmem, ad + 2 * k, bd + 2 * k, idesc, accum);
                             if (BN == 512)   // columns 256..511 from the second B halves (16 KB further)
                                 mma_bf16_pair(d_tmem + 256, ad + 2 * k, bd + ((Cfg::B_BYTES / 2) >> 4) + 2 * k, idesc,
-                                              (kb | k) != 0);
+                                              accum);
                         }
                     }
                     issued = true;
@@ -496,13 +516,13 @@ gemm_tc_kernel(const __grid_constant__ GemmProb p0, const __grid_constant__ Gemm
             if (!__all_sync(0xFFFFFFFFu, ready)) { *abort_flag = 1; break; }
             tc_fence_after();
             const GemmProb* P;
-            int tmc, tn;
-            locate(t, P, tmc, tn);
+            int tmc, tn, ks;
+            locate(t, P, tmc, tn, ks);
             const int row = (tmc * CM + (int)crank) * GEMM_BM + q * 32 + lane;
             const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN + part * COLS;
             const int n0 = tn * BN + part * COLS;
             if (EPI == EPI_STORE) epi_store<COLS>(P->sh, P->ep, tbase, row, n0, err.word);
-            else if (EPI == EPI_RESID) epi_resid<COLS>(P->sh, P->ep, tbase, row, n0, err.word);
+            else if (EPI == EPI_RESID) epi_resid<COLS>(P->sh, P->ep, tbase, row, n0, err.word, ks);
             else if (EPI == EPI_SWIGLU) epi_swiglu<BN>(P->sh, P->ep, tbase, row, tn, err.word);   // one part
             else epi_argmax<BN>(P->sh, P->ep, tbase, row, tn * BN, tn, err.word);
             // every lane's tensor-memory reads are complete before the warp reports

@@ -98,6 +98,10 @@ struct GemmArgs {
     // i * K / a_slabs ...); K / a_slabs a multiple of 64
     int a_slabs;
     int64_t a_slab_stride;
+    // EPI_RESID with a single M-tile: a buffer for fp32 partials of a K-split
+    // (nullable: no split)
+    float* split_part;
+    size_t split_part_bytes;
 };
 
 dfl_status gemm_tc(DeviceCtx* ctx, const GemmArgs& g, cudaStream_t st);

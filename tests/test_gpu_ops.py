@@ -229,6 +229,42 @@ def test_block_attn_bf16(N, C, B, Hq, Hkv, hd, d):
     assert_bf16_close(got - Xb, ref - Xb, "O Wo^T")
 
 
+@pytest.mark.parametrize("N,C,B,Hq,Hkv,hd,d", [
+    (1, 1024, 16, 32, 8, 128, 4096),   # the single-layer (batch 1) shape: Wo split over 4 K-ranges
+    (3, 200, 16, 16, 2, 128, 2048),    # 48 block rows, 4 splits
+    (2, 90, 16, 8, 2, 64, 1056),       # d not a multiple of the tile: ragged last N-tile
+])
+def test_output_projection_k_split(N, C, B, Hq, Hkv, hd, d):
+    # With at most 128 block rows and room in the workspace (a size asked for
+    # with d), the output projection is split along K into fp32 partials that
+    # a fixed-order sum adds to the residual: the same result as the unsplit
+    # projection within bf16 arithmetic, bit-reproducible from run to run.
+    rng = np.random.default_rng(N * 11 + d)
+    Q = rng_bf16(rng, (N * B, Hq, hd))
+    Kc, Vc = rng_bf16(rng, (N * C, Hkv, hd)), rng_bf16(rng, (N * C, Hkv, hd))
+    Kb, Vb = rng_bf16(rng, (N * B, Hkv, hd)), rng_bf16(rng, (N * B, Hkv, hd))
+    Wo = rng_bf16(rng, (d, Hq * hd), (Hq * hd) ** -0.5)
+    Xb = rng.standard_normal((N * B, d)).astype(np.float32)
+    args = [dev(Q, "bf16"), dev(Kc, "bf16"), dev(Vc, "bf16"), dev(Kb, "bf16"), dev(Vb, "bf16")]
+    base = dfl.workspace_size(dfl.DFL_OP_BLOCK_ATTN, N=N, C=C, B=B, Hq=Hq, Hkv=Hkv, hd=hd, dtype=dfl.DFL_BF16)
+    full = dfl.workspace_size(dfl.DFL_OP_BLOCK_ATTN, N=N, C=C, B=B, Hq=Hq, Hkv=Hkv, hd=hd, d=d, dtype=dfl.DFL_BF16)
+    assert full > base
+    out = {}
+    for name, nbytes in (("unsplit", base), ("split", full), ("split again", full)):
+        Xd = dev(Xb)
+        dfl.dfl_block_attn(*args, N, C, B, Hq, Hkv, hd, dfl.DFL_BF16, dev(Wo, "bf16"), d, Xd, _ws(nbytes), nbytes)
+        out[name] = host(Xd)
+    ref = np.empty((N * B, d))
+    for n in range(N):
+        K = np.concatenate([Kc[n * C:(n + 1) * C], Kb[n * B:(n + 1) * B]])
+        V = np.concatenate([Vc[n * C:(n + 1) * C], Vb[n * B:(n + 1) * B]])
+        O = orc.attention(Q[n * B:(n + 1) * B], K, V, orc.block_visibility(C, B))
+        ref[n * B:(n + 1) * B] = Xb[n * B:(n + 1) * B] + O.reshape(B, Hq * hd) @ Wo.astype(np.float64).T
+    for name in ("unsplit", "split"):
+        assert_bf16_close(out[name] - Xb, ref - Xb, name)
+    assert np.array_equal(out["split"].view(np.uint32), out["split again"].view(np.uint32))
+
+
 @pytest.mark.parametrize("N,C,B,Hq,Hkv,hd", [
     (32, 2048, 16, 32, 8, 128),   # the Qwen3-8B drafter's attention
     (16, 1024, 33, 32, 8, 128),   # the self-selection window (two head subsets per K/V head)
