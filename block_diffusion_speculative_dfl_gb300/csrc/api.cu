@@ -103,9 +103,9 @@ uint64_t wait_limit_ns() { return g_wait_ns.load(); }
 
 size_t ws_dual_kv_proj(int N, int B, int d, int dt) { return al256((size_t)N * B * d * esz(dt)); }
 
-// fp32 partials of the output projection's K-split when the N*B block rows
-// fit one M-tile (up to 8 splits of [rows][d]); 0 when d is not given.
-size_t ws_oproj_split(int64_t rows, int d) { return (d > 0 && rows <= 128) ? al256((size_t)8 * rows * d * 4) : 0; }
+// fp32 partials of the output projection's K-split (up to 8 splits of
+// [rows][d]); 0 when d is not given.
+size_t ws_oproj_split(int64_t rows, int d) { return d > 0 ? al256((size_t)8 * rows * d * 4) : 0; }
 
 // The attention output and scratch, then (optional: used when the caller's
 // workspace holds it) room for the output projection's K-split partials.
@@ -438,7 +438,7 @@ dfl_status block_attn_bf16(DeviceCtx* ctx, const void* Q, const void* Kc, const 
     g.epi = EPI_RESID;
     g.ep.resid = Xb; g.ep.ld_resid = d;
     g.tag = "gemm_o_proj";
-    // With few block rows the projection streams Wo through a few CTAs: when
+    // The projection's few output tiles stream Wo through a few CTAs: when
     // the workspace has room, it is split along K (partials after the
     // attention's scratch) and summed in a fixed order.
     const size_t base = ws_block_attn(N, C, B, Hq, Hkv, hd, DFL_BF16, ctx_len != nullptr);
