@@ -81,6 +81,7 @@ __device__ __forceinline__ void lse_merge(float& m, float& s, float m2, float s2
 // 16-byte loads when V is a multiple of 8.
 template <bool BF16>
 __global__ void __launch_bounds__(XT) row_lse_kernel(RowMap m, int V, float scale, float* lse) {
+    grid_dep_begin();
     const int64_t r = blockIdx.x;
     const void* row = row_ptr<BF16>(m, r, V);
     float mx = -INFINITY, s = 0.f;
@@ -125,6 +126,7 @@ template <bool BF16>
 __global__ void __launch_bounds__(XT) tv_alpha_kernel(const float* logits, const float* lse_z, float inv_T,
                                                       const void* vlog, const float* lse_v, int K, int G, int V,
                                                       float* alpha) {
+    grid_dep_begin();
     const int64_t nj = blockIdx.x;   // n * G + j
     const int64_t n = nj / G, j = nj % G;
     const float* z = logits + nj * V;
@@ -186,6 +188,7 @@ __global__ void __launch_bounds__(XT) tv_alpha_kernel(const float* logits, const
 
 // tokens_per_draft[n][k] = sum_m prod_{j<=m} alpha[n][k][j] (fp64).
 __global__ void tv_streak_kernel(const float* alpha, int64_t NK, int G, float* tpd) {
+    grid_dep_begin();
     const int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
     if (i >= NK) return;
     double prod = 1.0, tot = 0.0;
@@ -243,6 +246,7 @@ __device__ __forceinline__ float draw_weight(const SpecArgs& a, int64_t n, int j
 
 template <bool BF16>
 __global__ void spec_test_kernel(const SpecArgs a, int N) {
+    grid_dep_begin();
     const int64_t n = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
     if (n >= N) return;
     const int64_t kd = sel_of(a.vm, n);
@@ -263,6 +267,7 @@ __global__ void spec_test_kernel(const SpecArgs a, int N) {
 
 template <bool BF16>
 __global__ void residual_group_kernel(const SpecArgs a) {
+    grid_dep_begin();
     const int64_t n = blockIdx.y;
     const int g = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
@@ -279,6 +284,7 @@ __global__ void residual_group_kernel(const SpecArgs a) {
 
 template <bool BF16>
 __global__ void residual_pick_kernel(const SpecArgs a, int32_t* accept_len, int32_t* next_token) {
+    grid_dep_begin();
     const int64_t n = blockIdx.x;
     const int lane = threadIdx.x;
     const int j = a.stop[n];
@@ -356,6 +362,7 @@ __device__ __forceinline__ float sg_lse(const SgArgs& a, int64_t r) {
 
 template <bool BF16>
 __global__ void vdraw_group_kernel(const SgArgs a) {
+    grid_dep_begin();
     const int64_t r = blockIdx.x;
     const int g = blockIdx.y * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
@@ -382,6 +389,7 @@ __global__ void vdraw_group_kernel(const SgArgs a) {
 
 template <bool BF16>
 __global__ void vdraw_pick_kernel(const SgArgs a) {
+    grid_dep_begin();
     const int64_t r = blockIdx.x;
     const int lane = threadIdx.x;
     const int64_t n = r / (a.G + 1);
@@ -426,6 +434,7 @@ __global__ void vdraw_pick_kernel(const SgArgs a) {
 
 __global__ void sg_accept_kernel(const SgArgs a, const int32_t* drafts, int N, int32_t* accept_len,
                                  int32_t* next_token) {
+    grid_dep_begin();
     const int64_t n = blockIdx.x * (int64_t)(blockDim.x >> 5) + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (n >= N) return;
@@ -464,7 +473,7 @@ size_t spec_ws_bytes(int N, int G, int V) {
 // which already has the verifier rows' LSEs from self-selection).
 dfl_status lse_rows_f32(const float* logits, int rows, int V, float inv_T, float* lse, cudaStream_t st) {
     ProfScope ps("row_lse", st);
-    row_lse_kernel<false><<<(unsigned)rows, XT, 0, st>>>(RowMap{logits, 1, 1, nullptr}, V, inv_T, lse);
+    launch_pdl(row_lse_kernel<false>, (unsigned)rows, XT, 0, st, RowMap{logits, 1, 1, nullptr}, V, inv_T, lse);
     return last_launch();
 }
 
@@ -472,13 +481,15 @@ dfl_status tv_run(const float* logits, float inv_T, const void* vlog, bool bf, i
                   float* alpha, float* tpd, const float* lse_z, const float* lse_v_all, cudaStream_t st) {
     {
         ProfScope ps("tv_alpha", st);
-        if (bf) tv_alpha_kernel<true><<<(unsigned)(N * G), XT, 0, st>>>(logits, lse_z, inv_T, vlog, lse_v_all, K, G, V, alpha);
-        else tv_alpha_kernel<false><<<(unsigned)(N * G), XT, 0, st>>>(logits, lse_z, inv_T, vlog, lse_v_all, K, G, V, alpha);
+        if (bf) launch_pdl(tv_alpha_kernel<true>, (unsigned)(N * G), XT, 0, st, logits, lse_z, inv_T, vlog, lse_v_all,
+                           K, G, V, alpha);
+        else launch_pdl(tv_alpha_kernel<false>, (unsigned)(N * G), XT, 0, st, logits, lse_z, inv_T, vlog, lse_v_all,
+                        K, G, V, alpha);
     }
     dfl_status rc = last_launch();
     if (rc != DFL_OK || !tpd) return rc;
     ProfScope ps("tv_streak", st);
-    tv_streak_kernel<<<(unsigned)((N * K + 127) / 128), 128, 0, st>>>(alpha, (int64_t)N * K, G, tpd);
+    launch_pdl(tv_streak_kernel, (unsigned)((N * K + 127) / 128), 128, 0, st, alpha, (int64_t)N * K, G, tpd);
     return last_launch();
 }
 
@@ -498,13 +509,13 @@ dfl_status spec_run(const float* logits, float inv_T, const void* vlog, bool bf,
     sa.gsum = reinterpret_cast<double*>(p + al256((size_t)N * 4));
     const dim3 ggrid((sa.ngroups + 7) / 8, N);
     if (bf) {
-        spec_test_kernel<true><<<(N + 127) / 128, 128, 0, st>>>(sa, N);
-        residual_group_kernel<true><<<ggrid, 256, 0, st>>>(sa);
-        residual_pick_kernel<true><<<N, 32, 0, st>>>(sa, accept_len, next_token);
+        launch_pdl(spec_test_kernel<true>, (N + 127) / 128, 128, 0, st, sa, N);
+        launch_pdl(residual_group_kernel<true>, ggrid, 256, 0, st, sa);
+        launch_pdl(residual_pick_kernel<true>, N, 32, 0, st, sa, accept_len, next_token);
     } else {
-        spec_test_kernel<false><<<(N + 127) / 128, 128, 0, st>>>(sa, N);
-        residual_group_kernel<false><<<ggrid, 256, 0, st>>>(sa);
-        residual_pick_kernel<false><<<N, 32, 0, st>>>(sa, accept_len, next_token);
+        launch_pdl(spec_test_kernel<false>, (N + 127) / 128, 128, 0, st, sa, N);
+        launch_pdl(residual_group_kernel<false>, ggrid, 256, 0, st, sa);
+        launch_pdl(residual_pick_kernel<false>, N, 32, 0, st, sa, accept_len, next_token);
     }
     return last_launch();
 }
@@ -529,13 +540,13 @@ dfl_status sg_run(const void* vlog, bool bf, const int32_t* drafts, const int32_
     sa.gsum = reinterpret_cast<double*>(p + al256((size_t)rows * 4));
     const dim3 ggrid((unsigned)rows, (sa.ngroups + 7) / 8);
     if (bf) {
-        vdraw_group_kernel<true><<<ggrid, 256, 0, st>>>(sa);
-        vdraw_pick_kernel<true><<<(unsigned)rows, 32, 0, st>>>(sa);
+        launch_pdl(vdraw_group_kernel<true>, ggrid, 256, 0, st, sa);
+        launch_pdl(vdraw_pick_kernel<true>, (unsigned)rows, 32, 0, st, sa);
     } else {
-        vdraw_group_kernel<false><<<ggrid, 256, 0, st>>>(sa);
-        vdraw_pick_kernel<false><<<(unsigned)rows, 32, 0, st>>>(sa);
+        launch_pdl(vdraw_group_kernel<false>, ggrid, 256, 0, st, sa);
+        launch_pdl(vdraw_pick_kernel<false>, (unsigned)rows, 32, 0, st, sa);
     }
-    sg_accept_kernel<<<(N + 3) / 4, 128, 0, st>>>(sa, drafts, N, accept_len, next_token);
+    launch_pdl(sg_accept_kernel, (N + 3) / 4, 128, 0, st, sa, drafts, N, accept_len, next_token);
     return last_launch();
 }
 
@@ -562,11 +573,11 @@ extern "C" dfl_status dfl_tv_acceptance(const float* logits, float T, const void
     const bool bf = dt == DFL_BF16;
     {
         ProfScope ps("row_lse", st);
-        row_lse_kernel<false><<<(unsigned)(N * G), XT, 0, st>>>(RowMap{logits, 1, G, nullptr}, V, inv_T, lse_z);
+        launch_pdl(row_lse_kernel<false>, (unsigned)(N * G), XT, 0, st, RowMap{logits, 1, G, nullptr}, V, inv_T, lse_z);
         // every verifier row of every draft, [N*K][G+1]
         const RowMap all{vlog, 1, G + 1, nullptr};
-        if (bf) row_lse_kernel<true><<<(unsigned)(N * K * (G + 1)), XT, 0, st>>>(all, V, 1.f, lse_v);
-        else row_lse_kernel<false><<<(unsigned)(N * K * (G + 1)), XT, 0, st>>>(all, V, 1.f, lse_v);
+        if (bf) launch_pdl(row_lse_kernel<true>, (unsigned)(N * K * (G + 1)), XT, 0, st, all, V, 1.f, lse_v);
+        else launch_pdl(row_lse_kernel<false>, (unsigned)(N * K * (G + 1)), XT, 0, st, all, V, 1.f, lse_v);
     }
     dfl_status rc = last_launch();
     if (rc != DFL_OK) return rc;
@@ -593,9 +604,9 @@ extern "C" dfl_status dfl_spec_accept(const float* logits, float T, const void* 
     const RowMap vm{vlog, K, G + 1, sel, err_word()};
     {
         ProfScope ps("row_lse", st);
-        row_lse_kernel<false><<<(unsigned)(N * G), XT, 0, st>>>(RowMap{logits, 1, G, nullptr}, V, inv_T, lse_z);
-        if (bf) row_lse_kernel<true><<<(unsigned)(N * (G + 1)), XT, 0, st>>>(vm, V, 1.f, lse_v);
-        else row_lse_kernel<false><<<(unsigned)(N * (G + 1)), XT, 0, st>>>(vm, V, 1.f, lse_v);
+        launch_pdl(row_lse_kernel<false>, (unsigned)(N * G), XT, 0, st, RowMap{logits, 1, G, nullptr}, V, inv_T, lse_z);
+        if (bf) launch_pdl(row_lse_kernel<true>, (unsigned)(N * (G + 1)), XT, 0, st, vm, V, 1.f, lse_v);
+        else launch_pdl(row_lse_kernel<false>, (unsigned)(N * (G + 1)), XT, 0, st, vm, V, 1.f, lse_v);
     }
     dfl_status rc = last_launch();
     if (rc != DFL_OK) return rc;
@@ -621,8 +632,8 @@ extern "C" dfl_status dfl_sampled_greedy_accept(const void* vlog, dfl_dtype dt, 
     {
         ProfScope ps("row_lse", st);
         const RowMap vm{vlog, K, G + 1, sel, err_word()};
-        if (bf) row_lse_kernel<true><<<(unsigned)(N * (G + 1)), XT, 0, st>>>(vm, V, 1.f, lse_v);
-        else row_lse_kernel<false><<<(unsigned)(N * (G + 1)), XT, 0, st>>>(vm, V, 1.f, lse_v);
+        if (bf) launch_pdl(row_lse_kernel<true>, (unsigned)(N * (G + 1)), XT, 0, st, vm, V, 1.f, lse_v);
+        else launch_pdl(row_lse_kernel<false>, (unsigned)(N * (G + 1)), XT, 0, st, vm, V, 1.f, lse_v);
     }
     dfl_status rc = last_launch();
     if (rc != DFL_OK) return rc;

@@ -3,6 +3,7 @@
 #include <algorithm>
 #include <atomic>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <initializer_list>
 #include <mutex>
@@ -97,6 +98,14 @@ DeviceCtx* current_ctx() {
 }
 
 DevErr dev_err(DeviceCtx* ctx) { return DevErr{ctx->err_word, g_wait_ns.load()}; }
+
+bool pdl_on() {
+    static const bool on = [] {
+        const char* e = std::getenv("DFL_PDL");
+        return !(e && e[0] == '0');
+    }();
+    return on;
+}
 uint64_t wait_limit_ns() { return g_wait_ns.load(); }
 
 // ------------------------------------------------------------ workspaces

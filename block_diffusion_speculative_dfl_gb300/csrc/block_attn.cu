@@ -63,6 +63,7 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], 
 // ST: K/V stages in the ring (ST - 1 tiles in flight while one is used).
 template <int HD, int ST>
 __global__ void __launch_bounds__(ATT_MAX_WARPS * 32) attn_bf16_kernel(const AttnArgs a) {
+    grid_dep_begin();
     constexpr int CH = HD / 8;        // 16-byte chunks per row
     constexpr int ROWB = HD * 2;
     extern __shared__ uint8_t smem_raw[];
@@ -248,6 +249,7 @@ __global__ void __launch_bounds__(ATT_MAX_WARPS * 32) attn_bf16_kernel(const Att
 // once per row (S <= 64).
 template <int HD>
 __global__ void attn_combine_kernel(const float* Opart, const float* lse, int S, int64_t NQ, __nv_bfloat16* O) {
+    grid_dep_begin();
     constexpr int PER = HD / 32;
     const int64_t q = blockIdx.x * (int64_t)(blockDim.x >> 5) + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
@@ -355,7 +357,7 @@ dfl_status attn_bf16(const void* Q, const void* Kc, const void* Vc, const void* 
     ProfScope ps("attn_bf16", st);
     auto run = [&](auto kern) -> bool {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return false;
-        kern<<<grid, NW * 32, smem, st>>>(a);
+        launch_pdl(kern, grid, NW * 32, smem, st, a);
         return true;
     };
     bool ok;
@@ -369,9 +371,9 @@ dfl_status attn_bf16(const void* Q, const void* Kc, const void* Vc, const void* 
     ProfScope ps("attn_combine", st);
     const unsigned cgrid = (unsigned)((NQ + 7) / 8);
     if (hd == 128)
-        attn_combine_kernel<128><<<cgrid, 256, 0, st>>>(a.Opart, a.lse, a.S, (int64_t)NQ, a.O);
+        launch_pdl(attn_combine_kernel<128>, cgrid, 256, 0, st, a.Opart, a.lse, a.S, (int64_t)NQ, a.O);
     else
-        attn_combine_kernel<64><<<cgrid, 256, 0, st>>>(a.Opart, a.lse, a.S, (int64_t)NQ, a.O);
+        launch_pdl(attn_combine_kernel<64>, cgrid, 256, 0, st, a.Opart, a.lse, a.S, (int64_t)NQ, a.O);
     return last_launch();
 }
 

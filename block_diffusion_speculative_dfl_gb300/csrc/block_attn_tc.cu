@@ -224,6 +224,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder + pp * Cfg::PIPE_COLS;
+    grid_dep_begin();   // global memory only from here on
 
     if (role == 0 || role == 7) {
         if (role == 0 && lane == 0) {
@@ -614,6 +615,7 @@ template <int HD>
 __global__ void attn_tc_combine_kernel(const float* Opart, const float* lse, int64_t NQ, int rows_per_seq, int B,
                                        int C, const int32_t* ctx_len, int kps, int S_max, int* err,
                                        __nv_bfloat16* O) {
+    grid_dep_begin();
     constexpr int PER = HD / 32;
     const int64_t q = blockIdx.x * (int64_t)(blockDim.x >> 5) + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
@@ -796,7 +798,7 @@ dfl_status attn_tc(const void* Q, const void* Kc, const void* Vc, const void* Kb
                     return DFL_ERR_CUDA;
                 ctx->attn_attr_set[slot] = true;
             }
-            kern<<<grid, threads, smem, st>>>(mq, mkc, mvc, mkb, mvb, a, err);
+            launch_pdl(kern, grid, threads, smem, st, mq, mkc, mvc, mkb, mvb, a, err);
             return last_launch();
         };
         // M = 64 products when each item has at most 64 query rows
@@ -812,11 +814,11 @@ dfl_status attn_tc(const void* Q, const void* Kc, const void* Vc, const void* Kb
     ProfScope ps("attn_combine", st);
     const unsigned cgrid = (unsigned)((NQ + 7) / 8);
     if (hd == 128)
-        attn_tc_combine_kernel<128><<<cgrid, 256, 0, st>>>(a.Opart, a.lse, (int64_t)NQ, B * Hq, B, C, ctx_len, a.kps,
-                                                           a.S, ctx->err_word, a.O);
+        launch_pdl(attn_tc_combine_kernel<128>, cgrid, 256, 0, st, a.Opart, a.lse, (int64_t)NQ, B * Hq, B, C, ctx_len,
+                   a.kps, a.S, ctx->err_word, a.O);
     else
-        attn_tc_combine_kernel<64><<<cgrid, 256, 0, st>>>(a.Opart, a.lse, (int64_t)NQ, B * Hq, B, C, ctx_len, a.kps,
-                                                          a.S, ctx->err_word, a.O);
+        launch_pdl(attn_tc_combine_kernel<64>, cgrid, 256, 0, st, a.Opart, a.lse, (int64_t)NQ, B * Hq, B, C, ctx_len,
+                   a.kps, a.S, ctx->err_word, a.O);
     return last_launch();
 }
 

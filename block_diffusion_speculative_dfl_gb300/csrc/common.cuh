@@ -48,6 +48,25 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
     return t;
 }
 
+// ---------------------------------------------- programmatic dependent launch --
+//
+// Every kernel of the library is launched with programmatic stream
+// serialisation (launch_pdl on the host), so its CTAs may start while the
+// previous grid in the stream is still running.  Each kernel therefore calls
+// grid_dep_begin() in every CTA, on every path, before its first access to
+// global memory (other than the kernel parameters): the call returns once the
+// previous grid has completed and its writes are visible.  Work before it is
+// limited to this CTA's own shared memory, barriers and TMEM allocation, so
+// it overlaps the previous grid's tail.  The call then allows the next grid
+// in the stream to launch; since a CTA makes it only after allocating its
+// TMEM, a later grid's CTAs can never hold TMEM that an earlier grid still
+// needs, and since every CTA waits before it exits, a grid completes only
+// after its predecessor has.
+__device__ __forceinline__ void grid_dep_begin() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------- mbarriers --
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

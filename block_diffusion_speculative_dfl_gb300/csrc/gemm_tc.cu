@@ -70,13 +70,15 @@ dfl_status launch(DeviceCtx* ctx, const GemmProb& p0, const GemmProb& p1, int np
     cfg.blockDim = dim3(GemmCfg<BN, CM>::THREADS);
     cfg.dynamicSmemBytes = GemmCfg<BN, CM>::SMEM;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = CM;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // waits in grid_dep_begin
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = pdl_on() ? 2 : 1;
     const DevErr err = dev_err(ctx);
     ProfScope ps(tag ? tag : "gemm_tc", st);
     if (cudaLaunchKernelEx(&cfg, kern, p0, p1, nprob, err) != cudaSuccess) return DFL_ERR_CUDA;
@@ -197,6 +199,7 @@ static dfl_status launch_probs(DeviceCtx* ctx, const GemmProb& p0, const GemmPro
 // columns; N a multiple of 4).
 __global__ void splitk_reduce_kernel(const float* part, int S, int64_t stride, int M, int N, float* out,
                                      int64_t ld) {
+    grid_dep_begin();
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;   // float4 index over M x N
     const int64_t per_row = N / 4;
     if (i >= (int64_t)M * per_row) return;
@@ -257,8 +260,8 @@ dfl_status gemm_tc(DeviceCtx* ctx, const GemmArgs& g_in, cudaStream_t st) {
     if ((rc = launch_probs(ctx, P, P, 1, g.bn, g.epi, cm, g.tag, st)) != DFL_OK || ksplit == 1) return rc;
     ProfScope ps("splitk_reduce", st);
     const int64_t n4 = (int64_t)g.M * (g.N / 4);
-    splitk_reduce_kernel<<<(unsigned)((n4 + 255) / 256), 256, 0, st>>>(g.split_part, ksplit, (int64_t)g.M * g.N, g.M,
-                                                                       g.N, g.ep.resid, g.ep.ld_resid);
+    launch_pdl(splitk_reduce_kernel, (unsigned)((n4 + 255) / 256), 256, 0, st, g.split_part, ksplit,
+               (int64_t)g.M * g.N, g.M, g.N, g.ep.resid, g.ep.ld_resid);
     return last_launch();
 }
 

@@ -373,6 +373,7 @@ gemm_tc_kernel(const __grid_constant__ GemmProb p0, const __grid_constant__ Gemm
     if (CM > 1) cluster_sync(); else __syncthreads();   // the pair's barriers are initialised before any use
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
+    grid_dep_begin();   // global memory only from here on
 
     if (warp == 0) {
         if (lane == 0) {

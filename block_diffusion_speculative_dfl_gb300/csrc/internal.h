@@ -46,6 +46,28 @@ uint64_t wait_limit_ns();
 
 inline dfl_status cuda_status(cudaError_t e) { return e == cudaSuccess ? DFL_OK : DFL_ERR_CUDA; }
 inline dfl_status last_launch() { return cuda_status(cudaGetLastError()); }
+
+// Every kernel launch of the library goes through launch_pdl: programmatic
+// stream serialisation lets the grid start while the previous grid in the
+// stream finishes (each kernel waits for it in grid_dep_begin before touching
+// global memory).  DFL_PDL=0 in the environment launches plainly instead.
+bool pdl_on();
+
+template <typename... P, typename... A>
+inline dfl_status launch_pdl(void (*kern)(P...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                             A&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = pdl_on() ? 1 : 0;
+    return cuda_status(cudaLaunchKernelEx(&cfg, kern, static_cast<A&&>(args)...));
+}
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 // Row counts index TMA coordinates and GEMM extents, which are 32-bit.
 inline bool rows_fit(int64_t rows) { return rows < ((int64_t)1 << 31); }

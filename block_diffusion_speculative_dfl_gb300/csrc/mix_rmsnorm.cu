@@ -164,6 +164,7 @@ __global__ void __launch_bounds__(MIX_THREADS, 1) mix_rmsnorm_bf16_kernel(const 
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    grid_dep_begin();   // global memory only from here on
     const uint32_t tgain = *tmem_holder + ((uint32_t)(32 * (tw & 3)) << 16) + (uint32_t)((tw >> 2) * MIX_GCOLS);
 
     // Row k of this CTA.
@@ -372,6 +373,7 @@ __global__ void __launch_bounds__(MIX_THREADS, 1) mix_rmsnorm_bf16_kernel(const 
 __global__ void mix_rmsnorm_f32_kernel(const float* H, int64_t layer_stride, int L, int64_t rows, int d, int D,
                                        const float* mix_logits, const float* gain, float eps, float* Xc,
                                        int64_t xc_stride) {
+    grid_dep_begin();
     extern __shared__ float fsm[];
     float* w = fsm;              // [D][L]
     float* red = w + D * L;      // [D][32]
@@ -454,7 +456,7 @@ extern "C" dfl_status dfl_layer_mix_rmsnorm(const void* H, int64_t layer_stride,
                   static_cast<__nv_bfloat16*>(Xc), xc_layer_stride};
         const int64_t grid = rows < ctx->sm_count ? rows : ctx->sm_count;
         ProfScope ps("mix_rmsnorm_bf16", st);
-        kern<<<(unsigned)grid, MIX_THREADS, smem, st>>>(a, nstage, dev_err(ctx));
+        launch_pdl(kern, (unsigned)grid, MIX_THREADS, smem, st, a, nstage, dev_err(ctx));
         return last_launch();
     }
     const size_t smem = (size_t)(D * L + D * 32 + (size_t)D * d) * sizeof(float);
@@ -465,8 +467,7 @@ extern "C" dfl_status dfl_layer_mix_rmsnorm(const void* H, int64_t layer_stride,
         return DFL_ERR_CUDA;
     if (rows > 0x7FFFFFFF) return DFL_ERR_UNSUPPORTED_SHAPE;
     ProfScope ps("mix_rmsnorm_f32", st);
-    mix_rmsnorm_f32_kernel<<<(unsigned)rows, 256, smem, st>>>(static_cast<const float*>(H), layer_stride, L, rows,
-                                                             d, D, mix_logits, gain, eps, static_cast<float*>(Xc),
-                                                             xc_layer_stride);
+    launch_pdl(mix_rmsnorm_f32_kernel, (unsigned)rows, 256, smem, st, static_cast<const float*>(H), layer_stride, L,
+               rows, d, D, mix_logits, gain, eps, static_cast<float*>(Xc), xc_layer_stride);
     return last_launch();
 }

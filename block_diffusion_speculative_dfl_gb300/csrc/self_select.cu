@@ -73,6 +73,7 @@ template <bool BF16>
 __global__ void __launch_bounds__(RS_THREADS) verifier_row_stats_kernel(const void* vlog, int K, int G, int V,
                                                                         const int32_t* drafts, float* lse, int* amax,
                                                                         float* zx) {
+    grid_dep_begin();
     const int64_t rr = blockIdx.x;
     const int G1 = G + 1;
     const size_t esz = BF16 ? 2 : 4;
@@ -175,6 +176,7 @@ __global__ void __launch_bounds__(RS_THREADS) verifier_row_stats_kernel(const vo
 __global__ void streak_select_kernel(const int32_t* drafts, int N, int K, int G, const float* lse, const int* amax,
                                      const float* zx, float* scores, int32_t* selected, int32_t* accept_len,
                                      int32_t* bonus) {
+    grid_dep_begin();
     const int n = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (n >= N) return;
@@ -232,16 +234,17 @@ dfl_status self_select_run(const void* vlog, bool bf16, const int32_t* drafts, i
     {
     ProfScope ps("verifier_row_stats", st);
     if (bf16)
-        verifier_row_stats_kernel<true><<<(unsigned)rows, RS_THREADS, 0, st>>>(vlog, K, G, V, drafts, lse, amax, zx);
+        launch_pdl(verifier_row_stats_kernel<true>, (unsigned)rows, RS_THREADS, 0, st, vlog, K, G, V, drafts, lse,
+                   amax, zx);
     else
-        verifier_row_stats_kernel<false><<<(unsigned)rows, RS_THREADS, 0, st>>>(vlog, K, G, V, drafts, lse, amax,
-                                                                                 zx);
+        launch_pdl(verifier_row_stats_kernel<false>, (unsigned)rows, RS_THREADS, 0, st, vlog, K, G, V, drafts, lse,
+                   amax, zx);
     rc = last_launch();
     }
     if (rc != DFL_OK) return rc;
     ProfScope ps("streak_select", st);
-    streak_select_kernel<<<(N + 3) / 4, 128, 0, st>>>(drafts, N, K, G, lse, amax, zx, scores, selected, accept_len,
-                                                        bonus);
+    launch_pdl(streak_select_kernel, (N + 3) / 4, 128, 0, st, drafts, N, K, G, lse, amax, zx, scores, selected,
+               accept_len, bonus);
     return last_launch();
 }
 

@@ -10,6 +10,7 @@ namespace dfl {
 // ------------------------------------------------------------ rotary table
 
 __global__ void rope_table_kernel(float* table, int P, int hd, double theta) {
+    grid_dep_begin();
     const int half = hd / 2;
     const int64_t n = (int64_t)P * half;
     for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < n; t += (int64_t)gridDim.x * blockDim.x) {
@@ -25,8 +26,7 @@ dfl_status rope_table(float* table, int P, int hd, double theta, cudaStream_t st
     const int64_t n = (int64_t)P * (hd / 2);
     const int grid = (int)((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096);
     ProfScope ps("rope_table", st);
-    rope_table_kernel<<<grid, 256, 0, st>>>(table, P, hd, theta);
-    return last_launch();
+    return launch_pdl(rope_table_kernel, grid, 256, 0, st, table, P, hd, theta);
 }
 
 // ------------------------------------------------------------ row RMSNorm
@@ -41,6 +41,7 @@ template <typename OutT>
 __global__ void __launch_bounds__(RN_THREADS) rmsnorm_rows_kernel(const float* in, int d, int64_t M, int per,
                                                                   int stride, int off, const float* gain, float eps,
                                                                   OutT* out, float* copy) {
+    grid_dep_begin();
     const int64_t m = blockIdx.x;
     const int tid = threadIdx.x;
     const int64_t src = (m / per) * stride + off + m % per;
@@ -95,12 +96,10 @@ dfl_status rmsnorm_rows(const float* in, int d, int64_t M, int per, int stride, 
     if (M > 0x7FFFFFFF) return DFL_ERR_UNSUPPORTED_SHAPE;
     ProfScope ps("rmsnorm_rows", st);
     if (bf16)
-        rmsnorm_rows_kernel<__nv_bfloat16><<<(unsigned)M, RN_THREADS, 0, st>>>(in, d, M, per, stride, off, gain, eps,
-                                                                               static_cast<__nv_bfloat16*>(out), copy);
-    else
-        rmsnorm_rows_kernel<float><<<(unsigned)M, RN_THREADS, 0, st>>>(in, d, M, per, stride, off, gain, eps,
-                                                                       static_cast<float*>(out), copy);
-    return last_launch();
+        return launch_pdl(rmsnorm_rows_kernel<__nv_bfloat16>, (unsigned)M, RN_THREADS, 0, st, in, d, M, per, stride,
+                          off, gain, eps, static_cast<__nv_bfloat16*>(out), copy);
+    return launch_pdl(rmsnorm_rows_kernel<float>, (unsigned)M, RN_THREADS, 0, st, in, d, M, per, stride, off, gain,
+                      eps, static_cast<float*>(out), copy);
 }
 
 // --------------------------------------------------------- greedy accept
@@ -110,6 +109,7 @@ dfl_status rmsnorm_rows(const float* in, int d, int64_t M, int per, int stride, 
 // token.  One warp per sequence.
 __global__ void greedy_accept_kernel(const int32_t* draft, const int32_t* target, int N, int n,
                                      int32_t* accept_len, int32_t* bonus) {
+    grid_dep_begin();
     const int s = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (s >= N) return;
@@ -130,8 +130,7 @@ __global__ void greedy_accept_kernel(const int32_t* draft, const int32_t* target
 dfl_status greedy_accept(const int32_t* draft, const int32_t* target, int N, int n, int32_t* accept_len,
                          int32_t* bonus, cudaStream_t st) {
     ProfScope ps("greedy_accept", st);
-    greedy_accept_kernel<<<(N + 7) / 8, 256, 0, st>>>(draft, target, N, n, accept_len, bonus);
-    return last_launch();
+    return launch_pdl(greedy_accept_kernel, (N + 7) / 8, 256, 0, st, draft, target, N, n, accept_len, bonus);
 }
 
 // ------------------------------------------------------ context-cache plan
@@ -146,6 +145,7 @@ dfl_status greedy_accept(const int32_t* draft, const int32_t* target, int N, int
 __global__ void cache_plan_kernel(int N, int R, int B, int C, int32_t* ctx_len, const int32_t* n_new, int advance,
                                   int32_t* pos_ctx, int32_t* dst_ctx, int32_t* pos_blk, int32_t* len_new,
                                   DevErr err) {
+    grid_dep_begin();
     const int n = blockIdx.x;
     __shared__ int s_c0, s_m;
     if (threadIdx.x == 0) {
@@ -174,9 +174,8 @@ dfl_status cache_plan(int N, int R, int B, int C, int32_t* ctx_len, const int32_
                       int32_t* pos_ctx, int32_t* dst_ctx, int32_t* pos_blk, int32_t* len_new, DevErr err,
                       cudaStream_t st) {
     ProfScope ps("cache_plan", st);
-    cache_plan_kernel<<<N, 128, 0, st>>>(N, R, B, C, ctx_len, n_new, advance, pos_ctx, dst_ctx, pos_blk, len_new,
-                                         err);
-    return last_launch();
+    return launch_pdl(cache_plan_kernel, N, 128, 0, st, N, R, B, C, ctx_len, n_new, advance, pos_ctx, dst_ctx,
+                      pos_blk, len_new, err);
 }
 
 // --------------------------------------------------------- argmax combine
@@ -185,6 +184,7 @@ dfl_status cache_plan(int N, int R, int B, int C, int32_t* ctx_len, const int32_
 // (tiles are disjoint and ordered, and each partial already holds its tile's
 // lowest maximal column).  One warp per row.
 __global__ void argmax_combine_kernel(const float* pmax, const int* pidx, int64_t M, int tiles, int32_t* out) {
+    grid_dep_begin();
     const int64_t m = blockIdx.x * (int64_t)(blockDim.x >> 5) + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (m >= M) return;
@@ -207,8 +207,7 @@ __global__ void argmax_combine_kernel(const float* pmax, const int* pidx, int64_
 dfl_status argmax_combine(const float* pmax, const int* pidx, int64_t M, int tiles, int32_t* out,
                           cudaStream_t st) {
     ProfScope ps("argmax_combine", st);
-    argmax_combine_kernel<<<(unsigned)((M + 7) / 8), 256, 0, st>>>(pmax, pidx, M, tiles, out);
-    return last_launch();
+    return launch_pdl(argmax_combine_kernel, (unsigned)((M + 7) / 8), 256, 0, st, pmax, pidx, M, tiles, out);
 }
 
 // ------------------------------------------------------------- sampling
@@ -224,6 +223,7 @@ dfl_status argmax_combine(const float* pmax, const int* pidx, int64_t M, int til
 __global__ void sample_kernel(const float* logits, int64_t ld, const float* pmax, const double* psum, int64_t M,
                               int per, int tiles, int bn, int V, int K, float inv_T, uint32_t key0, uint32_t key1,
                               int32_t* samples) {
+    grid_dep_begin();
     extern __shared__ double pref[];   // [warps][tiles + 1]
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t m = blockIdx.x * (int64_t)(blockDim.x >> 5) + w;
@@ -288,10 +288,9 @@ dfl_status sample_rows(const float* logits, int64_t ld, const float* pmax, const
         cudaFuncSetAttribute(sample_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return DFL_ERR_CUDA;
     ProfScope ps("sample_inverse_cdf", st);
-    sample_kernel<<<(unsigned)((M + warps - 1) / warps), warps * 32, smem, st>>>(
-        logits, ld, pmax, psum, M, per, tiles, bn, V, K, 1.0f / T, (uint32_t)(seed & 0xFFFFFFFFu),
-        (uint32_t)(seed >> 32), samples);
-    return last_launch();
+    return launch_pdl(sample_kernel, (unsigned)((M + warps - 1) / warps), warps * 32, smem, st, logits, ld, pmax,
+                      psum, M, per, tiles, bn, V, K, 1.0f / T, (uint32_t)(seed & 0xFFFFFFFFu), (uint32_t)(seed >> 32),
+                      samples);
 }
 
 // Per-tile partials from materialised fp32 logits (the fp32 path): max,
@@ -300,6 +299,7 @@ dfl_status sample_rows(const float* logits, int64_t ld, const float* pmax, const
 // forms them.  Thread per (row, tile).
 __global__ void tile_partials_kernel(const float* logits, int64_t ld, int64_t M, int V, int bn, int tiles,
                                      float inv_T, float* pmax, int* pidx, double* psum) {
+    grid_dep_begin();
     const int64_t id = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
     if (id >= M * tiles) return;
     const int64_t m = id / tiles;
@@ -325,9 +325,8 @@ dfl_status tile_partials(const float* logits, int64_t ld, int64_t M, int V, int 
                          float* pmax, int* pidx, double* psum, cudaStream_t st) {
     const int64_t n = M * tiles;
     ProfScope ps("tile_partials", st);
-    tile_partials_kernel<<<(unsigned)((n + 127) / 128), 128, 0, st>>>(logits, ld, M, V, bn, tiles, inv_T, pmax,
-                                                                       pidx, psum);
-    return last_launch();
+    return launch_pdl(tile_partials_kernel, (unsigned)((n + 127) / 128), 128, 0, st, logits, ld, M, V, bn, tiles,
+                      inv_T, pmax, pidx, psum);
 }
 
 // ------------------------------------------------------------ fp32 GEMM
@@ -335,6 +334,7 @@ dfl_status tile_partials(const float* logits, int64_t ld, int64_t M, int V, int 
 // C[M][N] (=|+=) A[M][K] * B[N][K]^T on CUDA cores, 64x64 tiles.
 __global__ void gemm_f32_kernel(const float* A, int64_t lda, const float* B, int64_t ldb, float* C, int M, int N,
                                 int K, int ldc, int acc) {
+    grid_dep_begin();
     __shared__ float As[16][64 + 1];
     __shared__ float Bs[16][64 + 1];
     const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
@@ -377,8 +377,7 @@ dfl_status gemm_f32_ld(const float* A, int64_t lda, const float* B, int64_t ldb,
                        int ldc, int accumulate, cudaStream_t st) {
     dim3 grid((N + 63) / 64, (M + 63) / 64);
     ProfScope ps("gemm_f32", st);
-    gemm_f32_kernel<<<grid, 256, 0, st>>>(A, lda, B, ldb, C, M, N, K, ldc, accumulate);
-    return last_launch();
+    return launch_pdl(gemm_f32_kernel, grid, 256, 0, st, A, lda, B, ldb, C, M, N, K, ldc, accumulate);
 }
 
 dfl_status gemm_f32(const float* A, const float* B, float* C, int M, int N, int K, int ldc, int accumulate,
@@ -390,6 +389,7 @@ dfl_status gemm_f32(const float* A, const float* B, float* C, int M, int N, int 
 // pos_off + r % per.
 __global__ void rope_inplace_f32_kernel(float* x, int64_t rows, int heads, int hd, int per, int pos_off,
                                         const float* rope) {
+    grid_dep_begin();
     const int half = hd / 2;
     const int64_t n = rows * heads * half;
     for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < n; t += (int64_t)gridDim.x * blockDim.x) {
@@ -410,12 +410,12 @@ dfl_status rope_inplace_f32(float* x, int64_t rows, int heads, int hd, int per, 
     const int64_t n = rows * heads * (hd / 2);
     const int grid = (int)((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096);
     ProfScope ps("rope_f32", st);
-    rope_inplace_f32_kernel<<<grid, 256, 0, st>>>(x, rows, heads, hd, per, pos_off, rope);
-    return last_launch();
+    return launch_pdl(rope_inplace_f32_kernel, grid, 256, 0, st, x, rows, heads, hd, per, pos_off, rope);
 }
 
 // h[i] = silu(gate[i]) * up[i] (fp32 path of the feed-forward block).
 __global__ void swiglu_f32_kernel(const float* gate, const float* up, float* h, int64_t n) {
+    grid_dep_begin();
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
         const float g = gate[i];
         h[i] = g / (1.f + expf(-g)) * up[i];
@@ -425,14 +425,14 @@ __global__ void swiglu_f32_kernel(const float* gate, const float* up, float* h, 
 dfl_status swiglu_f32(const float* gate, const float* up, float* h, int64_t n, cudaStream_t st) {
     ProfScope ps("swiglu_f32", st);
     const int64_t blocks = (n + 255) / 256;
-    swiglu_f32_kernel<<<(unsigned)(blocks < 4096 ? blocks : 4096), 256, 0, st>>>(gate, up, h, n);
-    return last_launch();
+    return launch_pdl(swiglu_f32_kernel, (unsigned)(blocks < 4096 ? blocks : 4096), 256, 0, st, gate, up, h, n);
 }
 
 // fp32 block attention: one CTA per (sequence, query head), one warp per
 // query row at a time, online softmax over [context ; block] keys, no mask.
 __global__ void attn_f32_kernel(const float* Q, const float* Kc, const float* Vc, const float* Kb, const float* Vb,
                                 int N, int C, int B, int Hq, int Hkv, int hd, float* O) {
+    grid_dep_begin();
     const int n = blockIdx.x / Hq, h = blockIdx.x % Hq;
     const int g = h / (Hq / Hkv);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -464,13 +464,13 @@ __global__ void attn_f32_kernel(const float* Q, const float* Kc, const float* Vc
 dfl_status attn_f32(const float* Q, const float* Kc, const float* Vc, const float* Kb, const float* Vb, int N, int C,
                     int B, int Hq, int Hkv, int hd, float* O, cudaStream_t st) {
     ProfScope ps("attn_f32", st);
-    attn_f32_kernel<<<N * Hq, 128, 0, st>>>(Q, Kc, Vc, Kb, Vb, N, C, B, Hq, Hkv, hd, O);
-    return last_launch();
+    return launch_pdl(attn_f32_kernel, N * Hq, 128, 0, st, Q, Kc, Vc, Kb, Vb, N, C, B, Hq, Hkv, hd, O);
 }
 
 // ------------------------------------------------------- wait self-test
 
 __global__ void selftest_wait_kernel(int* status, uint64_t limit_ns) {
+    grid_dep_begin();
     __shared__ uint64_t bar;
     if (threadIdx.x == 0) {
         *status = 0;
@@ -483,8 +483,7 @@ __global__ void selftest_wait_kernel(int* status, uint64_t limit_ns) {
 
 dfl_status selftest_wait(int* status, uint64_t limit_ns, cudaStream_t st) {
     ProfScope ps("selftest_wait", st);
-    selftest_wait_kernel<<<1, 32, 0, st>>>(status, limit_ns);
-    return last_launch();
+    return launch_pdl(selftest_wait_kernel, 1, 32, 0, st, status, limit_ns);
 }
 
 // ----------------------------------------------------- Philox known answers
@@ -492,6 +491,7 @@ dfl_status selftest_wait(int* status, uint64_t limit_ns, cudaStream_t st) {
 // out[i] = Philox4x32-10(counter in[i][0..3], key in[i][4..5]): the device
 // generator's four output words, for checks against published vectors.
 __global__ void philox_block_kernel(const uint32_t* in, int n, uint32_t* out) {
+    grid_dep_begin();
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= n) return;
     const uint32_t* c = in + (int64_t)i * 6;
@@ -502,8 +502,7 @@ __global__ void philox_block_kernel(const uint32_t* in, int n, uint32_t* out) {
 
 dfl_status philox_block(const uint32_t* in, int n, uint32_t* out, cudaStream_t st) {
     ProfScope ps("philox_block", st);
-    philox_block_kernel<<<(n + 127) / 128, 128, 0, st>>>(in, n, out);
-    return last_launch();
+    return launch_pdl(philox_block_kernel, (n + 127) / 128, 128, 0, st, in, n, out);
 }
 
 }  // namespace dfl
