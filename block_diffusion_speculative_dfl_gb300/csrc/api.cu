@@ -127,9 +127,12 @@ size_t ws_block_attn(int N, int C, int B, int Hq, int Hkv, int hd, int dt, bool 
 // fp32 pre-norm features of the DFlash fusion, [rows][d]
 size_t ws_fc_fuse(int64_t rows, int d) { return al256((size_t)rows * d * 4); }
 
-size_t ws_block_ffn(int N, int B, int d, int F, int dt) {
+// Normalised rows and hidden activations, then (bf16, with_split: used when
+// the caller's workspace holds it) room for the down projection's K-split
+// partials.
+size_t ws_block_ffn(int N, int B, int d, int F, int dt, bool with_split = false) {
     const size_t M = (size_t)N * B;
-    if (dt == DFL_BF16) return al256(M * d * 2) + al256(M * F * 2);
+    if (dt == DFL_BF16) return al256(M * d * 2) + al256(M * F * 2) + (with_split ? ws_oproj_split((int64_t)M, d) : 0);
     return al256(M * d * 4) + 3 * al256(M * F * 4);
 }
 
@@ -171,7 +174,7 @@ size_t step_ws_bytes(const dfl_shape& s, bool cached) {
     if (cached) b += 2 * al256((size_t)rows * 4) + al256((size_t)s.N * s.B * 4) + al256((size_t)s.N * 4);
     size_t sub = ws_dual_kv_proj(s.N, s.B, s.d, s.dtype);
     sub = std::max(sub, ws_block_attn(s.N, s.C, s.B, s.Hq, s.Hkv, s.hd, s.dtype, cached, s.d));
-    if (s.F > 0) sub = std::max(sub, ws_block_ffn(s.N, s.B, s.d, s.F, s.dtype));
+    if (s.F > 0) sub = std::max(sub, ws_block_ffn(s.N, s.B, s.d, s.F, s.dtype, true));
     if (s.V > 0) {
         sub = std::max(sub, ws_lm_head(s.N, s.B, 1, s.d, s.V, s.dtype, true));
         if (s.K > 0) {
@@ -224,7 +227,7 @@ extern "C" size_t dfl_workspace_size(dfl_op op, const dfl_shape* s) {
         case DFL_OP_SELF_SELECT: return al256(select_ws_bytes(s->N, s->K, s->G));
         case DFL_OP_TV_ACCEPTANCE: return tv_ws_bytes(s->N, s->K, s->G);
         case DFL_OP_SPEC_ACCEPT: return spec_ws_bytes(s->N, s->G, s->V);
-        case DFL_OP_BLOCK_FFN: return s->F > 0 ? ws_block_ffn(s->N, s->B, s->d, s->F, s->dtype) : 0;
+        case DFL_OP_BLOCK_FFN: return s->F > 0 ? ws_block_ffn(s->N, s->B, s->d, s->F, s->dtype, true) : 0;
         case DFL_OP_DRAFT_STEP: return step_ws_bytes(*s, false);
         case DFL_OP_DRAFT_STEP_CACHED: return step_ws_bytes(*s, true);
         case DFL_OP_DRAFT_STEP_HOST: return step_host_ws_bytes(*s);
@@ -620,6 +623,14 @@ extern "C" dfl_status dfl_block_ffn(float* Xb, int32_t N, int32_t B, int32_t d, 
     g.epi = EPI_RESID;
     g.ep.resid = Xb; g.ep.ld_resid = d;
     g.tag = "gemm_ffn_down";
+    // A long K (F) over few output tiles: split along K when the workspace
+    // has room for the partials (after the activations), summed in a fixed order.
+    const size_t base = ws_block_ffn(N, B, d, F, dt);
+    const size_t room = ws_oproj_split(M, d);
+    if (ws_bytes >= base + room) {
+        g.split_part = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + base);
+        g.split_part_bytes = room;
+    }
     return gemm_tc(ctx, g, st);
 }
 

@@ -270,9 +270,11 @@ dfl_status gemm_tc(DeviceCtx* ctx, const GemmArgs& g_in, cudaStream_t st) {
 // there is none.
 dfl_status gemm_tc2(DeviceCtx* ctx, const GemmArgs& g0_in, const GemmArgs& g1_in, const char* tag, cudaStream_t st) {
     GemmArgs g0 = g0_in, g1 = g1_in;
-    // Clusters of two only when both problems have at least two M-tiles.
-    const int cm0 = (g0.M + GEMM_BM - 1) / GEMM_BM >= 2 ? 2 : 1, cm1 = (g1.M + GEMM_BM - 1) / GEMM_BM >= 2 ? 2 : 1;
-    const int cm = cm0 < cm1 ? cm0 : cm1;
+    // Pair tiles even when a problem has a single M-tile (the block projection
+    // of a small batch): the odd CTA of its tiles holds no rows (zero-filled
+    // A, nothing stored), but each SM then streams half of the B tile
+    // (measured at batch 1: 39.2 -> 37.2 us; batch 2: 65.3 -> 57.8 us).
+    const int cm = 2;
     // One tile width for both: of the widths both take, the one with the
     // smallest (rounds of the joint tile sequence) x (cost of a tile).
     const int clusters = ctx->sm_count / cm;

@@ -215,7 +215,9 @@ dfl_status dfl_dual_kv_proj(const void* Xc, const float* Xb, int32_t N, int32_t 
  *   Wo   in, dt [d][Hq*hd]
  *   Xb   in/out, fp32 [N*B][d]
  *   ws   scratch of dfl_workspace_size(DFL_OP_BLOCK_ATTN) bytes (split-KV
- *        partial results)
+ *        partial results, then fp32 partials of the output projection split
+ *        along K; a buffer without room for the latter is accepted down to
+ *        the size without them, and the projection then runs unsplit)
  *   Errors: INVALID_ARG, UNSUPPORTED_SHAPE, MISALIGNED, WORKSPACE.
  */
 dfl_status dfl_block_attn(const void* Q, const void* Kc, const void* Vc, const void* Kb,
@@ -397,8 +399,10 @@ dfl_status dfl_philox4x32_10(const uint32_t* in, int32_t n, uint32_t* out, dfl_s
  *     Xn = RMSNorm(Xb; ffn_gain),  Xb <- Xb + (silu(Xn W1^T) * (Xn W3^T)) W2^T
  *   Xb   in/out, fp32 [N*B][d]
  *   W1, W3 in, dt [F][d]; W2 in, dt [d][F]; ffn_gain in, fp32 [d]
- *   ws   dfl_workspace_size(DFL_OP_BLOCK_FFN) bytes (normalised rows and the
- *        [N*B][F] hidden activations)
+ *   ws   dfl_workspace_size(DFL_OP_BLOCK_FFN) bytes (normalised rows, the
+ *        [N*B][F] hidden activations, then, bf16, fp32 partials of the down
+ *        projection split along K; a buffer without room for the partials
+ *        is accepted and the projection then runs unsplit)
  *   bf16: one tensor-core GEMM for gate and up with the SwiGLU in its
  *   epilogue (needs F % 64 == 0), then the down projection with a residual
  *   epilogue.  fp32: CUDA-core GEMMs.
