@@ -108,7 +108,8 @@ struct GemmCfg {
     static constexpr int STAGES = (200 * 1024 / STAGE_BYTES) < 8 ? (200 * 1024 / STAGE_BYTES) : 8;
     static constexpr int TMEM_COLS = NACC * BN;
     static constexpr int BAR_BYTES = 256;
-    static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
+    static constexpr int STG_BYTES = 32 * 80;                      // bf16 store staging per epilogue warp
+    static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + BAR_BYTES + EW * STG_BYTES;
 };
 
 // Tile t of a (tiles_mc x tiles_n) grid of cluster tiles (x ksplit K-splits,
@@ -126,24 +127,38 @@ __device__ __forceinline__ void split_range(const GemmShape& sh, int ks, int& kb
     kb1 = kb0 + sh.kb_split < sh.num_kb ? kb0 + sh.kb_split : sh.num_kb;
 }
 
-__device__ __forceinline__ void store_bf16x32(void* dst, const float (&v)[32]) {
-    uint4* p = reinterpret_cast<uint4*>(dst);
+// Stores 32 bf16 values of each lane's row (lane r: v to dst, when ok) through
+// the warp's 2,560-byte staging buffer: rows are written to shared memory one
+// per lane (80-byte pitch: each quarter-warp's 16-byte writes hit distinct
+// banks), then each store instruction covers 8 rows x 64 contiguous bytes
+// (lane l: row l / 4 + 8 i, 16-byte chunk l % 4) instead of 32 rows x 16
+// bytes, a quarter of the L2 write requests.
+__device__ __forceinline__ void store_rows_bf16x32(uint8_t* stg, const float (&v)[32], __nv_bfloat16* dst,
+                                                   bool ok) {
+    const int lane = threadIdx.x & 31;
+    uint4* srow = reinterpret_cast<uint4*>(stg + lane * 80);
     #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        uint4 u;
-        u.x = pack_bf16(v[8 * q + 0], v[8 * q + 1]);
-        u.y = pack_bf16(v[8 * q + 2], v[8 * q + 3]);
-        u.z = pack_bf16(v[8 * q + 4], v[8 * q + 5]);
-        u.w = pack_bf16(v[8 * q + 6], v[8 * q + 7]);
-        p[q] = u;
+    for (int q = 0; q < 4; ++q)
+        srow[q] = make_uint4(pack_bf16(v[8 * q + 0], v[8 * q + 1]), pack_bf16(v[8 * q + 2], v[8 * q + 3]),
+                             pack_bf16(v[8 * q + 4], v[8 * q + 5]), pack_bf16(v[8 * q + 6], v[8 * q + 7]));
+    __syncwarp();
+    const int c = lane & 3;
+    #pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int r = (lane >> 2) + 8 * i;
+        const unsigned long long p = __shfl_sync(0xFFFFFFFFu, reinterpret_cast<unsigned long long>(dst), r);
+        const bool rok = __shfl_sync(0xFFFFFFFFu, ok, r);
+        const uint4 val = *reinterpret_cast<const uint4*>(stg + r * 80 + c * 16);
+        if (rok) reinterpret_cast<uint4*>(p)[c] = val;
     }
+    __syncwarp();   // the buffer is written again by the next call
 }
 
 // ---------------------------------------------------------------- epilogues
 
 template <int BN>
 __device__ __forceinline__ void epi_store(const GemmShape& sh, const GemmEpi& ep, uint32_t tbase,
-                                          int row, int n0, int* ew) {
+                                          int row, int n0, int* ew, uint8_t* stg) {
     int s = 0;
     #pragma unroll
     for (int j = 1; j < 3; ++j)
@@ -157,7 +172,7 @@ __device__ __forceinline__ void epi_store(const GemmShape& sh, const GemmEpi& ep
         for (int c = 0; c < BN / 32; ++c) {
             float v[32];
             tmem_ld32(tbase + c * 32, v);
-            if (ok) store_bf16x32(out + c * 32, v);
+            store_rows_bf16x32(stg, v, out + c * 32, ok);
         }
         return;
     }
@@ -178,18 +193,16 @@ __device__ __forceinline__ void epi_store(const GemmShape& sh, const GemmEpi& ep
             float x[32], y[32];
             tmem_ld32(tbase + h0 + c, x);
             tmem_ld32(tbase + h0 + c + half, y);
-            if (ok) {
-                #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const float a0 = x[2 * j], b0 = y[2 * j], a1 = x[2 * j + 1], b1 = y[2 * j + 1];
-                    x[2 * j] = a0 * t[j].x - b0 * t[j].y;
-                    y[2 * j] = b0 * t[j].x + a0 * t[j].y;
-                    x[2 * j + 1] = a1 * t[j].z - b1 * t[j].w;
-                    y[2 * j + 1] = b1 * t[j].z + a1 * t[j].w;
-                }
-                store_bf16x32(out + h0 + c, x);
-                store_bf16x32(out + h0 + c + half, y);
+            #pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const float a0 = x[2 * j], b0 = y[2 * j], a1 = x[2 * j + 1], b1 = y[2 * j + 1];
+                x[2 * j] = a0 * t[j].x - b0 * t[j].y;
+                y[2 * j] = b0 * t[j].x + a0 * t[j].y;
+                x[2 * j + 1] = a1 * t[j].z - b1 * t[j].w;
+                y[2 * j + 1] = b1 * t[j].z + a1 * t[j].w;
             }
+            store_rows_bf16x32(stg, x, out + h0 + c, ok);
+            store_rows_bf16x32(stg, y, out + h0 + c + half, ok);
         }
     }
 }
@@ -283,7 +296,7 @@ __device__ __forceinline__ void epi_argmax(const GemmShape& sh, const GemmEpi& e
 
 template <int BN>
 __device__ __forceinline__ void epi_swiglu(const GemmShape& sh, const GemmEpi& ep, uint32_t tbase, int row, int tn,
-                                           int* ew) {
+                                           int* ew, uint8_t* stg) {
     const bool ok = row < sh.M && DFL_IN_BOUNDS(ew, row, ep.seg[0].rows) &&
                     DFL_IN_BOUNDS(ew, (tn + 1) * (BN / 2) - 1, ep.seg[0].ld);
     const GemmSeg sg = ep.seg[0];
@@ -293,11 +306,9 @@ __device__ __forceinline__ void epi_swiglu(const GemmShape& sh, const GemmEpi& e
         float g[32], u[32];
         tmem_ld32(tbase + c * 32, g);
         tmem_ld32(tbase + BN / 2 + c * 32, u);
-        if (ok) {
-            #pragma unroll
-            for (int j = 0; j < 32; ++j) g[j] = g[j] / (1.f + expf(-g[j])) * u[j];
-            store_bf16x32(out + c * 32, g);
-        }
+        #pragma unroll
+        for (int j = 0; j < 32; ++j) g[j] = g[j] / (1.f + expf(-g[j])) * u[j];
+        store_rows_bf16x32(stg, g, out + c * 32, ok);
     }
 }
 
@@ -331,6 +342,7 @@ gemm_tc_kernel(const __grid_constant__ GemmProb p0, const __grid_constant__ Gemm
     uint64_t* drain = tempty + 2;
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+    uint8_t* stg_base = reinterpret_cast<uint8_t*>(full) + Cfg::BAR_BYTES;   // EW store staging buffers
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -522,9 +534,10 @@ gemm_tc_kernel(const __grid_constant__ GemmProb p0, const __grid_constant__ Gemm
             const int row = (tmc * CM + (int)crank) * GEMM_BM + q * 32 + lane;
             const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN + part * COLS;
             const int n0 = tn * BN + part * COLS;
-            if (EPI == EPI_STORE) epi_store<COLS>(P->sh, P->ep, tbase, row, n0, err.word);
+            uint8_t* stg = stg_base + (warp - 2) * Cfg::STG_BYTES;
+            if (EPI == EPI_STORE) epi_store<COLS>(P->sh, P->ep, tbase, row, n0, err.word, stg);
             else if (EPI == EPI_RESID) epi_resid<COLS>(P->sh, P->ep, tbase, row, n0, err.word, ks);
-            else if (EPI == EPI_SWIGLU) epi_swiglu<BN>(P->sh, P->ep, tbase, row, tn, err.word);   // one part
+            else if (EPI == EPI_SWIGLU) epi_swiglu<BN>(P->sh, P->ep, tbase, row, tn, err.word, stg);   // one part
             else epi_argmax<BN>(P->sh, P->ep, tbase, row, tn * BN, tn, err.word);
             // every lane's tensor-memory reads are complete before the warp reports
             tc_fence_before();
