@@ -156,38 +156,59 @@ __device__ __forceinline__ void store_rows_bf16x32(uint8_t* stg, const float (&v
 
 // ---------------------------------------------------------------- epilogues
 
+// Where one lane's row of a store-epilogue tile goes: output row, whether it
+// is stored, and for a rotary segment the (cos, sin) pairs of its position.
+struct StoreRow {
+    __nv_bfloat16* out;   // the row's first element of the tile's columns
+    const float4* cs;     // rotary segments: (cos, sin) pairs of the row's position
+    int hd;               // rotary head dimension (0: no rotary)
+    bool ok;
+};
+
 template <int BN>
-__device__ __forceinline__ void epi_store(const GemmShape& sh, const GemmEpi& ep, uint32_t tbase,
-                                          int row, int n0, int* ew, uint8_t* stg) {
+__device__ __forceinline__ StoreRow store_row(const GemmShape& sh, const GemmEpi& ep, int row, int n0, int* ew) {
     int s = 0;
     #pragma unroll
     for (int j = 1; j < 3; ++j)
         if (j < ep.nseg && n0 >= ep.seg[j].n_begin) s = j;
     const GemmSeg sg = ep.seg[s];
     const int64_t orow = (row < sh.M) ? (ep.row_dst ? (int64_t)ep.row_dst[row] : (int64_t)row) : -1;
-    const bool ok = orow >= 0 && DFL_IN_BOUNDS(ew, orow, sg.rows) && DFL_IN_BOUNDS(ew, n0 - sg.n_begin + BN - 1, sg.ld);
-    __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(sg.out) + (ok ? orow : 0) * sg.ld + (n0 - sg.n_begin);
-    if (!sg.rope) {
+    StoreRow r;
+    r.ok = orow >= 0 && DFL_IN_BOUNDS(ew, orow, sg.rows) && DFL_IN_BOUNDS(ew, n0 - sg.n_begin + BN - 1, sg.ld);
+    r.out = reinterpret_cast<__nv_bfloat16*>(sg.out) + (r.ok ? orow : 0) * sg.ld + (n0 - sg.n_begin);
+    r.hd = sg.rope ? ep.hd : 0;
+    const int pos = !(r.ok && sg.rope) ? 0 : (ep.row_pos ? ep.row_pos[row] : ep.pos_off + row % ep.rows_per_seq);
+    r.cs = sg.rope ? reinterpret_cast<const float4*>(ep.rope + (int64_t)pos * ep.hd) : nullptr;
+    return r;
+}
+
+// (cos, sin) of rotation pairs [c, c + 32) of the row: 256 contiguous bytes.
+__device__ __forceinline__ void load_rope32(const StoreRow& r, int c, float4 (&t)[16]) {
+    #pragma unroll
+    for (int j = 0; j < 16; ++j) t[j] = r.ok ? __ldg(r.cs + c / 2 + j) : make_float4(1.f, 0.f, 1.f, 0.f);
+}
+
+// bf16 store of the tile's BN columns of the row, with rotary where the
+// segment has it.  t: (cos, sin) of pairs [0, 32), already loaded (the
+// kernel loads them before the tile's products finish).
+template <int BN>
+__device__ __forceinline__ void epi_store(const StoreRow& r, uint32_t tbase, uint8_t* stg, float4 (&t)[16]) {
+    if (r.hd == 0) {
         #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
             float v[32];
             tmem_ld32(tbase + c * 32, v);
-            store_rows_bf16x32(stg, v, out + c * 32, ok);
+            store_rows_bf16x32(stg, v, r.out + c * 32, r.ok);
         }
         return;
     }
-    const int hd = ep.hd;
+    const int hd = r.hd;
     const int half = hd >> 1;
-    const int pos = !ok ? 0 : (ep.row_pos ? ep.row_pos[row] : ep.pos_off + row % ep.rows_per_seq);
-    const float4* cs = reinterpret_cast<const float4*>(ep.rope + (int64_t)pos * hd);   // (cos, sin) pairs
-    // One chunk of 32 rotation pairs at a time: its cos/sin (256 contiguous
-    // bytes of the thread's position) are loaded once, 16 bytes per load, and
-    // serve every head of the tile.
+    // One chunk of 32 rotation pairs at a time: its cos/sin serve every head
+    // of the tile.
     #pragma unroll 1
     for (int c = 0; c < half; c += 32) {
-        float4 t[16];
-        #pragma unroll
-        for (int j = 0; j < 16; ++j) t[j] = ok ? __ldg(cs + c / 2 + j) : make_float4(1.f, 0.f, 1.f, 0.f);
+        if (c > 0) load_rope32(r, c, t);
         #pragma unroll 1
         for (int h0 = 0; h0 < BN; h0 += hd) {
             float x[32], y[32];
@@ -201,8 +222,8 @@ __device__ __forceinline__ void epi_store(const GemmShape& sh, const GemmEpi& ep
                 x[2 * j + 1] = a1 * t[j].z - b1 * t[j].w;
                 y[2 * j + 1] = b1 * t[j].z + a1 * t[j].w;
             }
-            store_rows_bf16x32(stg, x, out + h0 + c, ok);
-            store_rows_bf16x32(stg, y, out + h0 + c + half, ok);
+            store_rows_bf16x32(stg, x, r.out + h0 + c, r.ok);
+            store_rows_bf16x32(stg, y, r.out + h0 + c + half, r.ok);
         }
     }
 }
@@ -525,17 +546,26 @@ gemm_tc_kernel(const __grid_constant__ GemmProb p0, const __grid_constant__ Gemm
         uint32_t acc_phase = 0;
         for (int t = cid; t < total; t += nclusters) {
             if (__any_sync(0xFFFFFFFFu, *abort_flag != 0)) break;
-            const bool ready = mbar_wait(&tfull[acc], acc_phase, err);
-            if (!__all_sync(0xFFFFFFFFu, ready)) { *abort_flag = 1; break; }
-            tc_fence_after();
             const GemmProb* P;
             int tmc, tn, ks;
             locate(t, P, tmc, tn, ks);
             const int row = (tmc * CM + (int)crank) * GEMM_BM + q * 32 + lane;
+            // Store epilogue: place the row and start loading the first rotary
+            // chunk while the tile's products are still running (an L2 round
+            // trip under the other SMs' operand traffic).
+            StoreRow srow{};
+            float4 rope0[16];
+            if constexpr (EPI == EPI_STORE) {
+                srow = store_row<COLS>(P->sh, P->ep, row, tn * BN + part * COLS, err.word);
+                if (srow.hd) load_rope32(srow, 0, rope0);
+            }
+            const bool ready = mbar_wait(&tfull[acc], acc_phase, err);
+            if (!__all_sync(0xFFFFFFFFu, ready)) { *abort_flag = 1; break; }
+            tc_fence_after();
             const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN + part * COLS;
             const int n0 = tn * BN + part * COLS;
             uint8_t* stg = stg_base + (warp - 2) * Cfg::STG_BYTES;
-            if (EPI == EPI_STORE) epi_store<COLS>(P->sh, P->ep, tbase, row, n0, err.word, stg);
+            if (EPI == EPI_STORE) epi_store<COLS>(srow, tbase, stg, rope0);
             else if (EPI == EPI_RESID) epi_resid<COLS>(P->sh, P->ep, tbase, row, n0, err.word, ks);
             else if (EPI == EPI_SWIGLU) epi_swiglu<BN>(P->sh, P->ep, tbase, row, tn, err.word, stg);   // one part
             else epi_argmax<BN>(P->sh, P->ep, tbase, row, tn * BN, tn, err.word);
