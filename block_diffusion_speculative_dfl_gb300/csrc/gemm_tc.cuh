@@ -228,6 +228,63 @@ __device__ __forceinline__ void epi_store(const StoreRow& r, uint32_t tbase, uin
     }
 }
 
+// First rotation pair of the chunk that the part-p warp of a 512-wide tile
+// works on (see epi_store512).
+__device__ __forceinline__ int store512_first_pair(int hd, int part) {
+    const int nc = hd / 64;   // chunks of 32 pairs per head
+    return nc >= 2 ? part * (nc / 2) * 32 : 0;
+}
+
+// bf16 store of a 512-wide tile's row with eight epilogue warps, two per
+// lane quadrant.  With rotary heads of 64 or more pairs, the part-p warp
+// takes pairs [32 p nc/2, 32 (p + 1) nc/2) of every head in the tile (nc =
+// chunks per head), so each warp needs only its own chunks of the row's
+// cos/sin, the first of them loaded (in t) before the tile's products end;
+// with 32-pair heads, or without rotary, it takes its half of the columns.
+// tb: the row's lane quadrant at column 0 of the tile.
+__device__ __forceinline__ void epi_store512(const StoreRow& r, uint32_t tb, int part, uint8_t* stg,
+                                             float4 (&t)[16]) {
+    if (r.hd == 0) {
+        #pragma unroll 1
+        for (int c = 0; c < 8; ++c) {
+            float v[32];
+            tmem_ld32(tb + part * 256 + c * 32, v);
+            store_rows_bf16x32(stg, v, r.out + part * 256 + c * 32, r.ok);
+        }
+        return;
+    }
+    const int hd = r.hd;
+    const int half = hd >> 1;
+    const int nc = half / 32;
+    auto rotate_store = [&](int h0, int c) {
+        float x[32], y[32];
+        tmem_ld32(tb + h0 + c, x);
+        tmem_ld32(tb + h0 + c + half, y);
+        #pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const float a0 = x[2 * j], b0 = y[2 * j], a1 = x[2 * j + 1], b1 = y[2 * j + 1];
+            x[2 * j] = a0 * t[j].x - b0 * t[j].y;
+            y[2 * j] = b0 * t[j].x + a0 * t[j].y;
+            x[2 * j + 1] = a1 * t[j].z - b1 * t[j].w;
+            y[2 * j + 1] = b1 * t[j].z + a1 * t[j].w;
+        }
+        store_rows_bf16x32(stg, x, r.out + h0 + c, r.ok);
+        store_rows_bf16x32(stg, y, r.out + h0 + c + half, r.ok);
+    };
+    if (nc >= 2) {
+        #pragma unroll 1
+        for (int ci = 0; ci < nc / 2; ++ci) {
+            const int c = store512_first_pair(hd, part) + ci * 32;
+            if (ci > 0) load_rope32(r, c, t);
+            #pragma unroll 1
+            for (int h0 = 0; h0 < 512; h0 += hd) rotate_store(h0, c);
+        }
+    } else {
+        #pragma unroll 1
+        for (int h0 = part * 256; h0 < part * 256 + 256; h0 += hd) rotate_store(h0, 0);
+    }
+}
+
 template <int BN>
 __device__ __forceinline__ void epi_resid(const GemmShape& sh, const GemmEpi& ep, uint32_t tbase,
                                           int row, int n0, int* ew, int ks) {
@@ -555,7 +612,10 @@ gemm_tc_kernel(const __grid_constant__ GemmProb p0, const __grid_constant__ Gemm
             // trip under the other SMs' operand traffic).
             StoreRow srow{};
             float4 rope0[16];
-            if constexpr (EPI == EPI_STORE) {
+            if constexpr (EPI == EPI_STORE && BN == 512) {
+                srow = store_row<512>(P->sh, P->ep, row, tn * BN, err.word);
+                if (srow.hd) load_rope32(srow, store512_first_pair(srow.hd, part), rope0);
+            } else if constexpr (EPI == EPI_STORE) {
                 srow = store_row<COLS>(P->sh, P->ep, row, tn * BN + part * COLS, err.word);
                 if (srow.hd) load_rope32(srow, 0, rope0);
             }
@@ -565,7 +625,9 @@ gemm_tc_kernel(const __grid_constant__ GemmProb p0, const __grid_constant__ Gemm
             const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN + part * COLS;
             const int n0 = tn * BN + part * COLS;
             uint8_t* stg = stg_base + (warp - 2) * Cfg::STG_BYTES;
-            if (EPI == EPI_STORE) epi_store<COLS>(srow, tbase, stg, rope0);
+            if constexpr (EPI == EPI_STORE && BN == 512)
+                epi_store512(srow, tmem_base + ((uint32_t)(q * 32) << 16), part, stg, rope0);
+            else if (EPI == EPI_STORE) epi_store<COLS>(srow, tbase, stg, rope0);
             else if (EPI == EPI_RESID) epi_resid<COLS>(P->sh, P->ep, tbase, row, n0, err.word, ks);
             else if (EPI == EPI_SWIGLU) epi_swiglu<BN>(P->sh, P->ep, tbase, row, tn, err.word, stg);   // one part
             else epi_argmax<BN>(P->sh, P->ep, tbase, row, tn * BN, tn, err.word);
