@@ -141,6 +141,11 @@ def _proj_ref(c, N, C, B, Hq, Hkv, hd, rope, theta=1e6):
     (2, 200, 16, 520, 8, 2, 128, False),   # K tail (520 = 8 * 65), no rotary
     (3, 150, 8, 256, 16, 2, 64, True),     # hd 64: ctx BN=128, GQA group 8
     (1, 64, 33, 256, 4, 2, 128, True),     # 33-row block (anchor + 32 masks)
+    # 256x512 pair tiles (the width the full-size drafters take): rotary split by
+    # pairs (hd 128) and by heads (hd 64), V without rotary, ragged context rows
+    # (16,000 = 62.5 pair tiles), a 128-row block whose pairs' odd CTA has no rows
+    (8, 2000, 16, 1024, 8, 4, 128, True),
+    (8, 2000, 16, 1024, 16, 8, 64, True),
 ])
 def test_dual_kv_proj_bf16(N, C, B, d, Hq, Hkv, hd, rope):
     c = _proj_case(N, C, B, d, Hq, Hkv, hd, "bf16", seed=N * 1000 + C + d)
