@@ -302,7 +302,11 @@ __global__ void __launch_bounds__(MIX_THREADS, 1) mix_rmsnorm_bf16_kernel(const 
         ss += __shfl_xor_sync(0xFFFFFFFFu, ss, 1);
         ss += __shfl_xor_sync(0xFFFFFFFFu, ss, 2);
         if ((lane & 3) == 0) red[(team * MIX_TEAM_WARPS + tw) * 8 + l_out] = ss;
-        if (!team_sync_and(bar_id, bar_n, ok)) break;   // a bounded wait ran out (error recorded)
+        // The first chunk's gains for pass 2 are fetched across the team's
+        // barrier (a tensor-memory round trip costs ~1 us under the mix's load).
+        uint32_t gpre[16];
+        tmem_ld16_issue(tgain, gpre);
+        if (!team_sync_and(bar_id, bar_n, ok)) { tmem_ld16_wait(gpre); break; }   // a bounded wait ran out
         float tot = 0.f;
         #pragma unroll
         for (int w = 0; w < MIX_TEAM_WARPS; ++w) tot += red[(team * MIX_TEAM_WARPS + w) * 8 + l_out];
@@ -312,10 +316,7 @@ __global__ void __launch_bounds__(MIX_THREADS, 1) mix_rmsnorm_bf16_kernel(const 
         // ---- pass 2: normalised bf16 output over the consumed input of the span.
         // The collective mma.sync consumes every lane's ldmatrix result, so a
         // group's input has been read in full before any lane overwrites it.
-        #pragma unroll 1
-        for (int c = 0; 4 * c < ng; ++c) {
-            float gv[16];
-            tmem_ld16(tgain + 16 * c, gv);
+        auto pass2_chunk = [&](int c, const float (&gv)[16]) {
             const uint32_t ldc = ld0 + 128u * c;
             uint8_t* outc = stage + st_rel + 128 * c;
             #pragma unroll
@@ -330,6 +331,19 @@ __global__ void __launch_bounds__(MIX_THREADS, 1) mix_rmsnorm_bf16_kernel(const 
                     }
                 }
             }
+        };
+        {
+            tmem_ld16_wait(gpre);
+            float gv[16];
+            #pragma unroll
+            for (int i = 0; i < 16; ++i) gv[i] = __uint_as_float(gpre[i]);
+            pass2_chunk(0, gv);
+        }
+        #pragma unroll 1
+        for (int c = 1; 4 * c < ng; ++c) {
+            float gv[16];
+            tmem_ld16(tgain + 16 * c, gv);
+            pass2_chunk(c, gv);
         }
         // Copy the span's D output rows out: 16 bytes per lane, ng * 32 contiguous bytes per row.
         __syncwarp();
