@@ -169,16 +169,22 @@ __global__ void __launch_bounds__(MIX_THREADS, 1) mix_rmsnorm_bf16_kernel(const 
 
     // Row k of this CTA.
     auto row_of = [&](int k) -> int64_t { return blockIdx.x + (int64_t)k * gridDim.x; };
-    auto issue = [&](int k) {   // one thread: stage row k's L slices
+    // One warp stages row k's L slices, a slice per lane (L <= 16): issued
+    // from one thread, each bulk copy held that thread ~80 ns, and the whole
+    // team waited for the issuing warp at its next barrier.
+    auto issue = [&](int k) {
         const int s = k % nstage;
         const int64_t row = row_of(k);
         uint8_t* dst = in0 + s * P.stage_bytes;
-        ++fills[s];
-        mbar_arrive_expect_tx(&full[s], tx_bytes);
-        for (int i = 0; i < a.L; ++i)
-            bulk_g2s(dst + i * P.slab, a.H + i * a.layer_stride + row * a.d, row_bytes, &full[s]);
+        if (lane == 0) {
+            ++fills[s];
+            mbar_arrive_expect_tx(&full[s], tx_bytes);
+        }
+        __syncwarp();
+        if (lane < a.L)
+            bulk_g2s(dst + lane * P.slab, a.H + lane * a.layer_stride + row * a.d, row_bytes, &full[s]);
     };
-    if (tid == 0)
+    if (warp == 0)
         for (int q = 0; q < nstage; ++q)
             if (row_of(q) < a.rows) issue(q);
 
@@ -262,7 +268,6 @@ __global__ void __launch_bounds__(MIX_THREADS, 1) mix_rmsnorm_bf16_kernel(const 
 
     // With a single stage (very wide rows) only team 0 works.
     const int tstep = nstage >= 2 ? MIX_TEAMS : 1;
-    const bool leader = tw == 0 && lane == 0;
     const bool full_span = ng == GPW;   // warp-uniform; false only for the last warps of ragged widths
     bool ok = true;
     int s = team % nstage;
@@ -365,7 +370,7 @@ __global__ void __launch_bounds__(MIX_THREADS, 1) mix_rmsnorm_bf16_kernel(const 
         // every warp is done with the stage.
         fence_proxy_async_smem();
         team_sync(bar_id, bar_n);
-        if (leader && row_of(k + nstage) < a.rows) issue(k + nstage);
+        if (tw == 0 && row_of(k + nstage) < a.rows) issue(k + nstage);
         s += tstep;
         if (s >= nstage) { s -= nstage; par ^= 1u; }
     }
