@@ -681,7 +681,12 @@ extern "C" dfl_status dfl_lm_head_argmax(const float* Xb, int32_t N, int32_t B, 
     GemmArgs g{};
     g.A = Xn; g.M = (int)M; g.K = d;
     g.B[0] = W_lm; g.b_rows[0] = V; g.b_begin[0] = 0; g.nb = 1; g.N = V;
-    g.bn = 256;
+    // Partials are 256 columns wide: 256-wide tiles, or (pair tiles, no logits
+    // or sampling sums to store) 512-wide tiles writing two partials each, whose
+    // single accumulator exposes its drain once per tile: worth it over a K of
+    // 4,096 (Qwen shape 0.389 -> 0.357 ms), not over 2,880 (GPT-OSS shape 0.207
+    // -> 0.222 ms), where 256-wide tiles hide their drain behind two accumulators.
+    g.bn = (M > GEMM_BM && d >= 4096 && !logits_out && !sp) ? 512 : 256;
     g.m_inner = 1;
     g.epi = EPI_ARGMAX;
     g.ep.part_max = pmax; g.ep.part_idx = pidx; g.ep.part_sum = sp ? psum : nullptr;

@@ -102,10 +102,15 @@ double tile_cost(int bn, int cm) {
 }
 
 // Tile widths a problem takes: 512 only as pair tiles with the rotary-store
-// or residual epilogue; every B segment must start on a tile boundary.
+// or residual epilogue, or with the argmax epilogue when it stores neither
+// logits nor sampling sums (the drain a 512-wide tile exposes stays short);
+// every B segment must start on a tile boundary; a width the caller fixed is
+// the only one.
 bool width_ok(const GemmArgs& g, int bn, int cm) {
+    const bool light_argmax = g.epi == EPI_ARGMAX && !g.ep.logits && !g.ep.part_sum;
+    if (bn == 512 && (cm != 2 || (g.epi != EPI_STORE && g.epi != EPI_RESID && !light_argmax) || g.split_b))
+        return false;
     if (g.bn != 0) return g.bn == bn;
-    if (bn == 512 && (cm != 2 || (g.epi != EPI_STORE && g.epi != EPI_RESID) || g.split_b)) return false;
     if (g.split_b) return (g.N / 2) % (bn / 2) == 0;
     for (int j = 0; j < g.nb; ++j) if (g.b_begin[j] % bn != 0) return false;
     return true;
@@ -180,6 +185,7 @@ static dfl_status launch_probs(DeviceCtx* ctx, const GemmProb& p0, const GemmPro
                                int cm, const char* tag, cudaStream_t st) {
     if (bn == 512) {   // pair tiles only (checked when the problem was built)
         if (epi == EPI_STORE) return launch<512, EPI_STORE, 2>(ctx, p0, p1, nprob, tag, st, 16);
+        if (epi == EPI_ARGMAX) return launch<512, EPI_ARGMAX, 2>(ctx, p0, p1, nprob, tag, st, 18);
         return launch<512, EPI_RESID, 2>(ctx, p0, p1, nprob, tag, st, 17);
     }
     const int slot = (bn == 256 ? 0 : 4) + epi;

@@ -318,10 +318,13 @@ __device__ __forceinline__ void epi_resid(const GemmShape& sh, const GemmEpi& ep
     }
 }
 
+// Partials of BN columns from n0: partial tile pt of npt per row (a 512-wide
+// tile writes two, one per epilogue warp of a lane quadrant, so the partials
+// are 256 columns wide either way).
 template <int BN>
 __device__ __forceinline__ void epi_argmax(const GemmShape& sh, const GemmEpi& ep, uint32_t tbase,
-                                           int row, int n0, int tn, int* ew) {
-    const bool ok = row < sh.M && DFL_IN_BOUNDS(ew, tn, sh.tiles_n) &&
+                                           int row, int n0, int pt, int npt, int* ew) {
+    const bool ok = row < sh.M && n0 < sh.N && DFL_IN_BOUNDS(ew, pt, npt) &&
                     (!ep.logits || DFL_IN_BOUNDS(ew, (n0 + BN < sh.N ? n0 + BN : sh.N) - 1, ep.ld_logits));
     float best = -INFINITY;
     int bidx = n0;
@@ -365,7 +368,7 @@ __device__ __forceinline__ void epi_argmax(const GemmShape& sh, const GemmEpi& e
         }
     }
     if (ok) {
-        const int64_t o = (int64_t)row * sh.tiles_n + tn;
+        const int64_t o = (int64_t)row * npt + pt;
         ep.part_max[o] = best;
         ep.part_idx[o] = bidx;
         if (ep.part_sum) ep.part_sum[o] = s;
@@ -424,7 +427,8 @@ gemm_tc_kernel(const __grid_constant__ GemmProb p0, const __grid_constant__ Gemm
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    static_assert((EPI != EPI_SWIGLU && EPI != EPI_ARGMAX) || Cfg::EW == 4, "these epilogues take whole tiles");
+    static_assert(EPI != EPI_SWIGLU || Cfg::EW == 4, "this epilogue takes whole tiles");
+    static_assert(EPI != EPI_ARGMAX || Cfg::EW == 4 || BN == 512, "argmax partials are 256 columns wide");
 
     const uint32_t crank = (CM > 1) ? cluster_ctarank() : 0u;
     const bool leader = crank == 0;   // the CTA that issues the products
@@ -630,7 +634,9 @@ gemm_tc_kernel(const __grid_constant__ GemmProb p0, const __grid_constant__ Gemm
             else if (EPI == EPI_STORE) epi_store<COLS>(srow, tbase, stg, rope0);
             else if (EPI == EPI_RESID) epi_resid<COLS>(P->sh, P->ep, tbase, row, n0, err.word, ks);
             else if (EPI == EPI_SWIGLU) epi_swiglu<BN>(P->sh, P->ep, tbase, row, tn, err.word, stg);   // one part
-            else epi_argmax<BN>(P->sh, P->ep, tbase, row, tn * BN, tn, err.word);
+            else if (BN == 512)
+                epi_argmax<COLS>(P->sh, P->ep, tbase, row, n0, 2 * tn + part, (P->sh.N + 255) / 256, err.word);
+            else epi_argmax<BN>(P->sh, P->ep, tbase, row, tn * BN, tn, P->sh.tiles_n, err.word);
             // every lane's tensor-memory reads are complete before the warp reports
             tc_fence_before();
             __syncwarp();

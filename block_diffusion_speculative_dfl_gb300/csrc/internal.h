@@ -26,7 +26,7 @@ struct DeviceCtx {
     int* err_word = nullptr;       // device address of this device's error word
     // max-dynamic-smem attribute set (atomic: calls may come from several
     // host threads; setting it twice is harmless)
-    std::atomic<bool> gemm_attr_set[18] = {};   // gemm instantiations
+    std::atomic<bool> gemm_attr_set[19] = {};   // gemm instantiations
     std::atomic<bool> mix_attr_set{false};
     std::atomic<bool> attn_attr_set[4] = {};    // tcgen05 attention: head dim 64 / 128, M = 64 / 128 products
     // Host-input draft step: a copy stream and events, created on first use.
@@ -68,6 +68,7 @@ inline dfl_status launch_pdl(void (*kern)(P...), dim3 grid, dim3 block, size_t s
     cfg.numAttrs = pdl_on() ? 1 : 0;
     return cuda_status(cudaLaunchKernelEx(&cfg, kern, static_cast<A&&>(args)...));
 }
+
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 // Row counts index TMA coordinates and GEMM extents, which are 32-bit.
 inline bool rows_fit(int64_t rows) { return rows < ((int64_t)1 << 31); }
@@ -110,7 +111,7 @@ struct GemmArgs {
     int nb;
     int N;                  // total columns
     int m_inner;
-    int bn;                 // 128, 256 or 512 (pair tiles with the store or residual epilogue); 0: chosen
+    int bn;                 // 128, 256 or 512 (pair tiles; store, residual or light argmax epilogue); 0: chosen
     int epi;                // EpiKind
     GemmEpi ep;
     const char* tag;        // name in kernel traces

@@ -385,6 +385,30 @@ def test_lm_head_argmax_bf16(N, B, row0, d, V):
     assert np.array_equal(host(am).reshape(-1), orc.argmax_lowest(z))
 
 
+@pytest.mark.parametrize("N,B,row0,d,V", [(12, 16, 1, 4096, 5003), (12, 16, 1, 4096, 4700),
+                                            (40, 16, 1, 4096, 3000)])
+def test_lm_head_argmax_wide_tiles(N, B, row0, d, V):
+    """Greedy heads of more than 128 rows and K >= 4096 take 512-wide pair tiles, whose two
+    epilogue warps per lane quadrant each write a 256-column partial; the
+    argmax must equal the one of the 256-wide path (logits stored) and the
+    oracle's lowest-index argmax of those logits.  V = 4700 leaves the last
+    512-wide tile's second half without columns; V = 5003 a partial last one."""
+    X, g, W = _lm_case(N, B, d, V, seed=V + N)
+    nr = B - row0
+    wsb = dfl.workspace_size(dfl.DFL_OP_LM_HEAD, N=N, B=B, row0=row0, d=d, V=V, dtype=dfl.DFL_BF16)
+    ws = _ws(wsb)
+    am_wide = torch.full((N, nr), -1, dtype=torch.int32, device="cuda")
+    dfl.dfl_lm_head_argmax(dev(X), N, B, row0, d, dfl.DFL_BF16, dev(g), 1e-6, dev(W, "bf16"), V, am_wide, None,
+                           None, None, ws, wsb)
+    am = torch.empty((N, nr), dtype=torch.int32, device="cuda")
+    lg = torch.empty((N * nr, V), dtype=torch.float32, device="cuda")
+    dfl.dfl_lm_head_argmax(dev(X), N, B, row0, d, dfl.DFL_BF16, dev(g), 1e-6, dev(W, "bf16"), V, am, lg, None,
+                           None, ws, wsb)
+    z = host(lg)
+    assert np.array_equal(host(am_wide), host(am))
+    assert np.array_equal(host(am_wide).reshape(-1), orc.argmax_lowest(z))
+
+
 def test_lm_head_argmax_ties_take_lowest_index():
     N, B, d, V = 1, 4, 256, 1000
     rng = np.random.default_rng(21)
