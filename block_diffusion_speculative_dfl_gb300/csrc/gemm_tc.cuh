@@ -2,11 +2,15 @@
 //
 // A and B are bf16, K-major (row-major with K contiguous), loaded by TMA with
 // 128-byte swizzling into a shared-memory ring; one elected thread issues
-// tcgen05.mma (128 x BN x 16 on one SM, or 256 x BN x 16 over an SM pair) into
-// a double-buffered TMEM accumulator; four epilogue warps read TMEM with
-// tcgen05.ld and apply one of four epilogues:
+// tcgen05.mma (128 x BN x 16 on one SM, or 256 x BN x 16 over an SM pair; a
+// 512-wide pair tile as two 256-wide products per step) into a TMEM
+// accumulator, double-buffered up to 256 columns (a 512-wide tile's single
+// accumulator fills tensor memory); four epilogue warps (eight for 512-wide
+// tiles, two per lane quadrant) read TMEM with tcgen05.ld and apply one of
+// four epilogues:
 //   EPI_STORE  bf16 store into up to three column segments, rotary embedding
-//              on segments that ask for it;
+//              on segments that ask for it (stores staged per warp in shared
+//              memory, so that each instruction writes whole row segments);
 //   EPI_RESID  fp32 residual accumulate (out += C), or plain fp32 store;
 //   EPI_ARGMAX per-row max / argmax over the tile's columns (lowest column on
 //              ties), optional fp32 logits store and optional per-tile
