@@ -25,7 +25,12 @@
  *              Host pointers appear only where stated (parameter structs).
  *   Launch     Calls are asynchronous on the given stream (a cudaStream_t
  *              passed as void*, NULL = legacy default stream).  They do not
- *              synchronise and may be captured into a CUDA graph.
+ *              synchronise and may be captured into a CUDA graph.  Kernels
+ *              are launched with programmatic dependent launch: a kernel may
+ *              start while the previous kernel in the stream finishes and
+ *              waits for it before touching global memory (results are the
+ *              same either way); DFL_PDL=0 in the environment, read once per
+ *              process, launches plainly.
  *   Layout     Row-major, contiguous.  Weights are [out][in] (in contiguous).
  *              bf16 tensors hold raw bf16 bits (2 bytes per element).
  *              The block residual stream Xb is always fp32.
