@@ -131,20 +131,17 @@ __device__ __forceinline__ void split_range(const GemmShape& sh, int ks, int& kb
     kb1 = kb0 + sh.kb_split < sh.num_kb ? kb0 + sh.kb_split : sh.num_kb;
 }
 
-// Stores 32 bf16 values of each lane's row (lane r: v to dst, when ok) through
-// the warp's 2,560-byte staging buffer: rows are written to shared memory one
-// per lane (80-byte pitch: each quarter-warp's 16-byte writes hit distinct
-// banks), then each store instruction covers 8 rows x 64 contiguous bytes
-// (lane l: row l / 4 + 8 i, 16-byte chunk l % 4) instead of 32 rows x 16
-// bytes, a quarter of the L2 write requests.
-__device__ __forceinline__ void store_rows_bf16x32(uint8_t* stg, const float (&v)[32], __nv_bfloat16* dst,
-                                                   bool ok) {
+// Stores 64 bytes of each lane's row (lane r: q to dst, when ok) through the
+// warp's 2,560-byte staging buffer: rows are written to shared memory one per
+// lane (80-byte pitch: each quarter-warp's 16-byte writes hit distinct banks),
+// then each store instruction covers 8 rows x 64 contiguous bytes (lane l:
+// row l / 4 + 8 i, 16-byte chunk l % 4) instead of 32 rows x 16 bytes, a
+// quarter of the L2 write requests.  Every lane of the warp calls it.
+__device__ __forceinline__ void store_rows_64B(uint8_t* stg, const uint4 (&q)[4], void* dst, bool ok) {
     const int lane = threadIdx.x & 31;
     uint4* srow = reinterpret_cast<uint4*>(stg + lane * 80);
     #pragma unroll
-    for (int q = 0; q < 4; ++q)
-        srow[q] = make_uint4(pack_bf16(v[8 * q + 0], v[8 * q + 1]), pack_bf16(v[8 * q + 2], v[8 * q + 3]),
-                             pack_bf16(v[8 * q + 4], v[8 * q + 5]), pack_bf16(v[8 * q + 6], v[8 * q + 7]));
+    for (int k = 0; k < 4; ++k) srow[k] = q[k];
     __syncwarp();
     const int c = lane & 3;
     #pragma unroll
@@ -156,6 +153,27 @@ __device__ __forceinline__ void store_rows_bf16x32(uint8_t* stg, const float (&v
         if (rok) reinterpret_cast<uint4*>(p)[c] = val;
     }
     __syncwarp();   // the buffer is written again by the next call
+}
+
+// 32 bf16 values of the lane's row.
+__device__ __forceinline__ void store_rows_bf16x32(uint8_t* stg, const float (&v)[32], __nv_bfloat16* dst,
+                                                   bool ok) {
+    uint4 q[4];
+    #pragma unroll
+    for (int k = 0; k < 4; ++k)
+        q[k] = make_uint4(pack_bf16(v[8 * k + 0], v[8 * k + 1]), pack_bf16(v[8 * k + 2], v[8 * k + 3]),
+                          pack_bf16(v[8 * k + 4], v[8 * k + 5]), pack_bf16(v[8 * k + 6], v[8 * k + 7]));
+    store_rows_64B(stg, q, dst, ok);
+}
+
+// 16 fp32 values of the lane's row, from v[0..16).
+__device__ __forceinline__ void store_rows_f32x16(uint8_t* stg, const float* v, float* dst, bool ok) {
+    uint4 q[4];
+    #pragma unroll
+    for (int k = 0; k < 4; ++k)
+        q[k] = make_uint4(__float_as_uint(v[4 * k]), __float_as_uint(v[4 * k + 1]), __float_as_uint(v[4 * k + 2]),
+                          __float_as_uint(v[4 * k + 3]));
+    store_rows_64B(stg, q, dst, ok);
 }
 
 // ---------------------------------------------------------------- epilogues
@@ -291,7 +309,7 @@ __device__ __forceinline__ void epi_store512(const StoreRow& r, uint32_t tb, int
 
 template <int BN>
 __device__ __forceinline__ void epi_resid(const GemmShape& sh, const GemmEpi& ep, uint32_t tbase,
-                                          int row, int n0, int* ew, int ks) {
+                                          int row, int n0, int* ew, int ks, uint8_t* stg) {
     const bool ok = row < sh.M && DFL_IN_BOUNDS(ew, (n0 + BN < sh.N ? n0 + BN : sh.N) - 1, ep.ld_resid);
     const bool rd = !ep.resid_store;
     float* out = ep.resid + ks * sh.part_stride + (int64_t)(ok ? row : 0) * ep.ld_resid + n0;
@@ -314,6 +332,19 @@ __device__ __forceinline__ void epi_resid(const GemmShape& sh, const GemmEpi& ep
             r[8 + q].x += w[4 * q + 0]; r[8 + q].y += w[4 * q + 1];
             r[8 + q].z += w[4 * q + 2]; r[8 + q].w += w[4 * q + 3];
         }
+        if (!rd) {   // a plain store (split partials, fp32 outputs): staged, 16 columns per call
+            const bool u0 = n0 + c * 32 < sh.N, u1 = n0 + c * 32 + 32 < sh.N;   // warp-uniform
+            const float* rf = reinterpret_cast<const float*>(r);
+            if (u0) {
+                store_rows_f32x16(stg, rf, out + c * 32, ok);
+                store_rows_f32x16(stg, rf + 16, out + c * 32 + 16, ok);
+            }
+            if (u1) {
+                store_rows_f32x16(stg, rf + 32, out + c * 32 + 32, ok);
+                store_rows_f32x16(stg, rf + 48, out + c * 32 + 48, ok);
+            }
+            continue;
+        }
         #pragma unroll
         for (int q = 0; q < 8; ++q) {
             if (in0) p[q] = r[q];
@@ -327,7 +358,7 @@ __device__ __forceinline__ void epi_resid(const GemmShape& sh, const GemmEpi& ep
 // are 256 columns wide either way).
 template <int BN>
 __device__ __forceinline__ void epi_argmax(const GemmShape& sh, const GemmEpi& ep, uint32_t tbase,
-                                           int row, int n0, int pt, int npt, int* ew) {
+                                           int row, int n0, int pt, int npt, int* ew, uint8_t* stg) {
     const bool ok = row < sh.M && n0 < sh.N && DFL_IN_BOUNDS(ew, pt, npt) &&
                     (!ep.logits || DFL_IN_BOUNDS(ew, (n0 + BN < sh.N ? n0 + BN : sh.N) - 1, ep.ld_logits));
     float best = -INFINITY;
@@ -341,12 +372,11 @@ __device__ __forceinline__ void epi_argmax(const GemmShape& sh, const GemmEpi& e
         #pragma unroll
         for (int j = 0; j < 32; ++j)
             if (cb + j < sh.N && v[j] > best) { best = v[j]; bidx = cb + j; }
-        if (ok && lg) {
-            if (cb + 32 <= sh.N && (ep.ld_logits & 3) == 0) {
-                float4* p = reinterpret_cast<float4*>(lg + cb);
-                #pragma unroll
-                for (int q = 0; q < 8; ++q) p[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-            } else {
+        if (lg) {
+            if (cb + 32 <= sh.N && (ep.ld_logits & 3) == 0) {   // warp-uniform: staged, 16 columns per call
+                store_rows_f32x16(stg, v, lg + cb, ok);
+                store_rows_f32x16(stg, v + 16, lg + cb + 16, ok);
+            } else if (ok) {
                 #pragma unroll
                 for (int j = 0; j < 32; ++j) if (cb + j < sh.N) lg[cb + j] = v[j];
             }
@@ -636,11 +666,12 @@ gemm_tc_kernel(const __grid_constant__ GemmProb p0, const __grid_constant__ Gemm
             if constexpr (EPI == EPI_STORE && BN == 512)
                 epi_store512(srow, tmem_base + ((uint32_t)(q * 32) << 16), part, stg, rope0);
             else if (EPI == EPI_STORE) epi_store<COLS>(srow, tbase, stg, rope0);
-            else if (EPI == EPI_RESID) epi_resid<COLS>(P->sh, P->ep, tbase, row, n0, err.word, ks);
+            else if (EPI == EPI_RESID) epi_resid<COLS>(P->sh, P->ep, tbase, row, n0, err.word, ks, stg);
             else if (EPI == EPI_SWIGLU) epi_swiglu<BN>(P->sh, P->ep, tbase, row, tn, err.word, stg);   // one part
             else if (BN == 512)
-                epi_argmax<COLS>(P->sh, P->ep, tbase, row, n0, 2 * tn + part, (P->sh.N + 255) / 256, err.word);
-            else epi_argmax<BN>(P->sh, P->ep, tbase, row, tn * BN, tn, P->sh.tiles_n, err.word);
+                epi_argmax<COLS>(P->sh, P->ep, tbase, row, n0, 2 * tn + part, (P->sh.N + 255) / 256, err.word,
+                                 stg);
+            else epi_argmax<BN>(P->sh, P->ep, tbase, row, tn * BN, tn, P->sh.tiles_n, err.word, stg);
             // every lane's tensor-memory reads are complete before the warp reports
             tc_fence_before();
             __syncwarp();
