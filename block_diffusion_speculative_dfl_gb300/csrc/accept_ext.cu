@@ -395,24 +395,40 @@ __global__ void vdraw_pick_kernel(const SgArgs a) {
     const int64_t n = r / (a.G + 1);
     const int j = (int)(r % (a.G + 1));
     const double* gs = a.gsum + r * a.ngroups;
-    __shared__ int gsel;
-    __shared__ double rel_s;
-    if (lane == 0) {
-        double total = 0.0;
-        for (int g = 0; g < a.ngroups; ++g) total += gs[g];
-        const double target = philox_uniform24((uint32_t)n, (uint32_t)j, 0u, 3u, a.key0, a.key1) * total;
-        double run = 0.0;
-        int g = 0;
-        for (; g < a.ngroups - 1; ++g) {
-            if (run + gs[g] > target) break;
-            run += gs[g];
+    // The row's total (lane-strided partial sums, a fixed tree to lane 0, then
+    // broadcast so that every lane holds the same value) and the group holding
+    // u * total: an exclusive scan of the group sums 32 groups at a time,
+    // the last group taking a target that rounding puts past the others.
+    double part = 0.0;
+    for (int gg = lane; gg < a.ngroups; gg += 32) part += gs[gg];
+    #pragma unroll
+    for (int o = 16; o > 0; o >>= 1) part += __shfl_down_sync(0xFFFFFFFFu, part, o);
+    const double total = __shfl_sync(0xFFFFFFFFu, part, 0);
+    const double target = philox_uniform24((uint32_t)n, (uint32_t)j, 0u, 3u, a.key0, a.key1) * total;
+    int g = a.ngroups - 1;
+    double before = 0.0;   // sum of the groups before the chunk
+    bool found = false;
+    for (int base = 0; base < a.ngroups - 1 && !found; base += 32) {
+        const int gg = base + lane;
+        double x = gg < a.ngroups - 1 ? gs[gg] : 0.0;
+        #pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const double y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+            if (lane >= o) x += y;
         }
-        gsel = g;
-        rel_s = target - run;
+        const unsigned hit = __ballot_sync(0xFFFFFFFFu, gg < a.ngroups - 1 && before + x > target);
+        const double excl = __shfl_up_sync(0xFFFFFFFFu, x, 1);   // lane l: groups base .. base + l - 1
+        if (hit) {
+            const int l = __ffs(hit) - 1;
+            const double e = __shfl_sync(0xFFFFFFFFu, excl, l);
+            g = base + l;
+            before += l ? e : 0.0;
+            found = true;
+        } else {
+            before += __shfl_sync(0xFFFFFFFFu, x, 31);
+        }
     }
-    __syncwarp();
-    const int g = gsel;
-    const double rel = rel_s;
+    const double rel = target - before;
     const void* vr = row_ptr<BF16>(a.vm, r, a.V);
     const float lse = sg_lse(a, r);
     const int b0 = g * RG, b1 = min(a.V, b0 + RG);

@@ -234,11 +234,17 @@ __global__ void sample_kernel(const float* logits, int64_t ld, const float* pmax
     float Mx = -INFINITY;
     for (int t = lane; t < tiles; t += 32) Mx = fmaxf(Mx, pm[t]);
     Mx = warp_max(Mx);
-    // prefix sums: lane owns a contiguous chunk of tiles
+    // prefix sums: lane owns a contiguous chunk of tiles; each tile weight (an
+    // fp64 exp, slow on this part) is computed once, kept in P[t] and turned
+    // into the prefix in place
     const int chunk = (tiles + 31) / 32;
     const int t0 = lane * chunk, t1 = min(tiles, t0 + chunk);
     double loc = 0.0;
-    for (int t = t0; t < t1; ++t) loc += ps[t] * exp((double)(pm[t] - Mx) * (double)inv_T);
+    for (int t = t0; t < t1; ++t) {
+        const double wt = ps[t] * exp((double)(pm[t] - Mx) * (double)inv_T);
+        P[t] = wt;
+        loc += wt;
+    }
     double excl = loc;
     #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -248,8 +254,9 @@ __global__ void sample_kernel(const float* logits, int64_t ld, const float* pmax
     excl -= loc;
     double run = excl;
     for (int t = t0; t < t1; ++t) {
+        const double wt = P[t];
         P[t] = run;
-        run += ps[t] * exp((double)(pm[t] - Mx) * (double)inv_T);
+        run += wt;
     }
     if (lane == 31) P[tiles] = run;
     __syncwarp();
