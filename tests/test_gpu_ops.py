@@ -270,6 +270,44 @@ def test_output_projection_k_split(N, C, B, Hq, Hkv, hd, d):
     assert np.array_equal(out["split"].view(np.uint32), out["split again"].view(np.uint32))
 
 
+@pytest.mark.parametrize("N,C,B,Hq,Hkv,hd,d", [
+    (1, 64, 16, 32, 8, 128, 4096),    # 16 rows, one M-tile: single-CTA tiles
+    (3, 64, 16, 16, 2, 128, 2048),    # 48 rows, 32 k-blocks
+    (4, 64, 16, 16, 2, 128, 1056),    # ragged last N-tile (1056 = 4 x 256 + 32)
+    (2, 64, 16, 64, 8, 64, 2880),     # the GPT-OSS width: 2880 = 11 x 256 + 64
+    (10, 64, 17, 32, 8, 128, 4096),   # 170 rows: pair tiles whose odd CTA holds 42 rows
+    (16, 64, 33, 32, 8, 128, 4096),   # 528 rows (the self-selection batch): a third pair tile of 16 rows
+])
+def test_output_projection_few_tiles(N, C, B, Hq, Hkv, hd, d):
+    # Output projections of few tiles with ragged edges (single-CTA and pair
+    # tiles, a pair tile whose odd CTA holds few or no rows, a last N-tile of
+    # 32 or 64 columns), run with a workspace that holds no split partials:
+    # the projection's result within bf16 arithmetic, bit-identical from run
+    # to run.
+    rng = np.random.default_rng(N * 13 + d)
+    Q = rng_bf16(rng, (N * B, Hq, hd))
+    Kc, Vc = rng_bf16(rng, (N * C, Hkv, hd)), rng_bf16(rng, (N * C, Hkv, hd))
+    Kb, Vb = rng_bf16(rng, (N * B, Hkv, hd)), rng_bf16(rng, (N * B, Hkv, hd))
+    Wo = rng_bf16(rng, (d, Hq * hd), (Hq * hd) ** -0.5)
+    Xb = rng.standard_normal((N * B, d)).astype(np.float32)
+    args = [dev(Q, "bf16"), dev(Kc, "bf16"), dev(Vc, "bf16"), dev(Kb, "bf16"), dev(Vb, "bf16")]
+    wsb = dfl.workspace_size(dfl.DFL_OP_BLOCK_ATTN, N=N, C=C, B=B, Hq=Hq, Hkv=Hkv, hd=hd, dtype=dfl.DFL_BF16)
+    outs = []
+    for _ in range(2):
+        Xd = dev(Xb)
+        dfl.dfl_block_attn(*args, N, C, B, Hq, Hkv, hd, dfl.DFL_BF16, dev(Wo, "bf16"), d, Xd, _ws(wsb), wsb)
+        outs.append(host(Xd))
+    ref = np.empty((N * B, d))
+    for n in range(N):
+        K = np.concatenate([Kc[n * C:(n + 1) * C], Kb[n * B:(n + 1) * B]])
+        V = np.concatenate([Vc[n * C:(n + 1) * C], Vb[n * B:(n + 1) * B]])
+        O = orc.attention(Q[n * B:(n + 1) * B], K, V, orc.block_visibility(C, B))
+        ref[n * B:(n + 1) * B] = Xb[n * B:(n + 1) * B] + O.reshape(B, Hq * hd) @ Wo.astype(np.float64).T
+    assert_bf16_close(outs[0] - Xb, ref - Xb, "O Wo^T")
+    assert np.array_equal(outs[0].view(np.uint32), outs[1].view(np.uint32))
+    assert dfl.dfl_get_device_error() == 0
+
+
 @pytest.mark.parametrize("N,C,B,Hq,Hkv,hd", [
     (32, 2048, 16, 32, 8, 128),   # the Qwen3-8B drafter's attention
     (16, 1024, 33, 32, 8, 128),   # the self-selection window (two head subsets per K/V head)
@@ -529,7 +567,8 @@ def test_bounded_wait_times_out_and_context_survives():
 
 # --------------------------------------------------------- feed-forward --
 
-@pytest.mark.parametrize("N,B,d,F", [(3, 16, 256, 384), (20, 16, 512, 1024), (2, 33, 256, 192)])
+@pytest.mark.parametrize("N,B,d,F", [(3, 16, 256, 384), (20, 16, 512, 1024), (2, 33, 256, 192),
+                                     (4, 16, 1024, 4096)])   # a down projection of 4 tiles over 64 k-blocks
 def test_block_ffn_bf16(N, B, d, F):
     rng = np.random.default_rng(N * F)
     Xb = rng.standard_normal((N * B, d)).astype(np.float32)
