@@ -155,6 +155,53 @@ __device__ __forceinline__ void store_rows_64B(uint8_t* stg, const uint4 (&q)[4]
     __syncwarp();   // the buffer is written again by the next call
 }
 
+// The four rows whose 16-byte chunks a lane stores in store_rows_64B (rows
+// l / 4 + 8 i of the warp's 32): their addresses at the tile's first column,
+// 0 for a row that is not stored, gathered once per tile instead of by every
+// call.
+struct StagedRows {
+    unsigned long long p[4];
+};
+
+__device__ __forceinline__ StagedRows staged_rows(const void* row_base, bool ok) {
+    const int lane = threadIdx.x & 31;
+    const unsigned long long mine = ok ? reinterpret_cast<unsigned long long>(row_base) : 0ull;
+    StagedRows sr;
+    #pragma unroll
+    for (int i = 0; i < 4; ++i) sr.p[i] = __shfl_sync(0xFFFFFFFFu, mine, (lane >> 2) + 8 * i);
+    return sr;
+}
+
+// store_rows_64B with the rows gathered beforehand: each lane's 64 bytes go
+// `off` bytes past its row's address.
+__device__ __forceinline__ void store_rows_64B_at(uint8_t* stg, const uint4 (&q)[4], const StagedRows& sr,
+                                                  uint32_t off) {
+    const int lane = threadIdx.x & 31;
+    uint4* srow = reinterpret_cast<uint4*>(stg + lane * 80);
+    #pragma unroll
+    for (int k = 0; k < 4; ++k) srow[k] = q[k];
+    __syncwarp();
+    const int c = lane & 3;
+    #pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int r = (lane >> 2) + 8 * i;
+        const uint4 val = *reinterpret_cast<const uint4*>(stg + r * 80 + c * 16);
+        if (sr.p[i]) reinterpret_cast<uint4*>(sr.p[i] + off)[c] = val;
+    }
+    __syncwarp();   // the buffer is written again by the next call
+}
+
+// 32 bf16 values of the lane's row, `col` columns past the row's tile start.
+__device__ __forceinline__ void store_rows_bf16x32_at(uint8_t* stg, const float (&v)[32], const StagedRows& sr,
+                                                      int col) {
+    uint4 q[4];
+    #pragma unroll
+    for (int k = 0; k < 4; ++k)
+        q[k] = make_uint4(pack_bf16(v[8 * k + 0], v[8 * k + 1]), pack_bf16(v[8 * k + 2], v[8 * k + 3]),
+                          pack_bf16(v[8 * k + 4], v[8 * k + 5]), pack_bf16(v[8 * k + 6], v[8 * k + 7]));
+    store_rows_64B_at(stg, q, sr, (uint32_t)col * 2u);
+}
+
 // 32 bf16 values of the lane's row.
 __device__ __forceinline__ void store_rows_bf16x32(uint8_t* stg, const float (&v)[32], __nv_bfloat16* dst,
                                                    bool ok) {
@@ -215,12 +262,13 @@ __device__ __forceinline__ void load_rope32(const StoreRow& r, int c, float4 (&t
 // kernel loads them before the tile's products finish).
 template <int BN>
 __device__ __forceinline__ void epi_store(const StoreRow& r, uint32_t tbase, uint8_t* stg, float4 (&t)[16]) {
+    const StagedRows sr = staged_rows(r.out, r.ok);
     if (r.hd == 0) {
         #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
             float v[32];
             tmem_ld32(tbase + c * 32, v);
-            store_rows_bf16x32(stg, v, r.out + c * 32, r.ok);
+            store_rows_bf16x32_at(stg, v, sr, c * 32);
         }
         return;
     }
@@ -244,8 +292,8 @@ __device__ __forceinline__ void epi_store(const StoreRow& r, uint32_t tbase, uin
                 x[2 * j + 1] = a1 * t[j].z - b1 * t[j].w;
                 y[2 * j + 1] = b1 * t[j].z + a1 * t[j].w;
             }
-            store_rows_bf16x32(stg, x, r.out + h0 + c, r.ok);
-            store_rows_bf16x32(stg, y, r.out + h0 + c + half, r.ok);
+            store_rows_bf16x32_at(stg, x, sr, h0 + c);
+            store_rows_bf16x32_at(stg, y, sr, h0 + c + half);
         }
     }
 }
@@ -266,12 +314,13 @@ __device__ __forceinline__ int store512_first_pair(int hd, int part) {
 // tb: the row's lane quadrant at column 0 of the tile.
 __device__ __forceinline__ void epi_store512(const StoreRow& r, uint32_t tb, int part, uint8_t* stg,
                                              float4 (&t)[16]) {
+    const StagedRows sr = staged_rows(r.out, r.ok);
     if (r.hd == 0) {
         #pragma unroll 1
         for (int c = 0; c < 8; ++c) {
             float v[32];
             tmem_ld32(tb + part * 256 + c * 32, v);
-            store_rows_bf16x32(stg, v, r.out + part * 256 + c * 32, r.ok);
+            store_rows_bf16x32_at(stg, v, sr, part * 256 + c * 32);
         }
         return;
     }
@@ -290,8 +339,8 @@ __device__ __forceinline__ void epi_store512(const StoreRow& r, uint32_t tb, int
             x[2 * j + 1] = a1 * t[j].z - b1 * t[j].w;
             y[2 * j + 1] = b1 * t[j].z + a1 * t[j].w;
         }
-        store_rows_bf16x32(stg, x, r.out + h0 + c, r.ok);
-        store_rows_bf16x32(stg, y, r.out + h0 + c + half, r.ok);
+        store_rows_bf16x32_at(stg, x, sr, h0 + c);
+        store_rows_bf16x32_at(stg, y, sr, h0 + c + half);
     };
     if (nc >= 2) {
         #pragma unroll 1
