@@ -136,14 +136,15 @@ def source_hash(files):
     return h.hexdigest()[:16]
 
 
-# kernel trace name -> source files its code lives in (for the traffic record)
-KERNEL_SOURCES = {
-    "gemm_ctx_kv": ["gemm_tc.cuh", "gemm_tc.cu"], "gemm_block_qkv": ["gemm_tc.cuh", "gemm_tc.cu"],
-    "gemm_kv_qkv": ["gemm_tc.cuh", "gemm_tc.cu"], "gemm_kv_qkv_append": ["gemm_tc.cuh", "gemm_tc.cu"],
-    "gemm_o_proj": ["gemm_tc.cuh", "gemm_tc.cu"], "gemm_lm_head": ["gemm_tc.cuh", "gemm_tc.cu"],
+# kernel trace name -> source files its code lives in (for the traffic record):
+# the kernel's own files, then the device helpers every kernel uses
+_GEMM_SRC = ["gemm_tc.cuh", "gemm_tc.cu"]
+KERNEL_SOURCES = {k: v + ["common.cuh"] for k, v in {
+    "gemm_ctx_kv": _GEMM_SRC, "gemm_block_qkv": _GEMM_SRC, "gemm_kv_qkv": _GEMM_SRC, "gemm_kv_qkv_append": _GEMM_SRC,
+    "gemm_o_proj": _GEMM_SRC, "gemm_lm_head": _GEMM_SRC,
     "mix_rmsnorm_bf16": ["mix_rmsnorm.cu"], "attn_bf16": ["block_attn.cu"], "attn_tc": ["block_attn_tc.cu"],
     "verifier_row_stats": ["self_select.cu"],
-}
+}.items()}
 
 
 def ncu_traffic(kernel, workload):
